@@ -1,0 +1,413 @@
+"""Encoders, block layouts and dequantizers (oracle; test infrastructure only).
+
+The write path of [turbo4 post-mortem] section 1 is: extract the norm ->
+normalise -> random rotation -> nearest centroid ("抽范数 -> 归一化 -> 随机旋转 ->
+最近质心"), then pack.  Block layouts:
+
+* turbo4 (section 5, section 7): 128 elements in 68 bytes = fp32 norm + qs[64],
+  two 4-bit indices per byte, element j in bits 4*(j%2) of qs[j/2]
+  (4.25 bits/value, 3.76x vs fp16).
+* turbo3 (section 1 "3.5-bit", section 4 "2+1 scheme"): 32-element blocks of
+  14 bytes = fp16 norm + qs[8] + signs[4]; low two index bits of element j in
+  bits 2*(j%4) of qs[j/4], high bit in bit j%8 of signs[j/8].
+* prod3 keys ("3-bit keys = 2-bit MSE + 1-bit QJL", [Triton deep dive] trick 2;
+  residual norm rnorm of [turbo4 post-mortem] section 2 bugs 3, 5, 6): 56 bytes =
+  fp32 norm + fp32 residual norm + qs[32] (2-bit indices) + signs[16].
+* vgroup2 values ([Triton deep dive] trick 3 "v * scale + zero" and the write
+  path's "2-bit group quantization + bit packing"): 48 bytes = q[32] (2-bit
+  codes) + 4 x (fp16 scale, fp16 zero) for groups of 32 elements.
+
+Readings taken where the pages are silent (all listed in the design doc):
+
+* Header first, little-endian, in every block.
+* The canonical fp32 norm: squares rounded separately (no fused multiply-add),
+  partial sums p_l = (x_4l^2 + x_4l+1^2) + (x_4l+2^2 + x_4l+3^2) for l = 0..31,
+  then p_l <- p_l + p_{l xor h} for h = 16, 8, 4, 2, 1, then an IEEE sqrt.
+* u = x / n (IEEE fp32 division); a zero norm gives u = 0, so every index is the
+  code of coordinate 0 (K/2 - 1); NaN input propagates into the norm and every
+  comparison with NaN is false (index 0).
+* Nearest centroid = number of boundaries strictly below the coordinate (ties to
+  the lower index).
+* turbo3 stores the norm of the whole 128-vector (fp16, round-to-nearest, IEEE
+  overflow to inf) in each of its four 32-element blocks.
+* prod3: residual r = u - Pi^T c[idx] in the unrotated normalised space
+  (section 2 bug 6), gamma = ||r||, sign bit i = 1 when (S r)_i >= 0.
+* vgroup2 per group: mn, mx by IEEE min/max (NaN ignored), mn <- mn + 0 (folds
+  -0 to +0), scale = fp16(fp32((mx - mn) / 3)), zero = fp16(mn),
+  code = clamp(rint((v - zero) / scale), 0, 3) with half-even rint, IEEE
+  max/min clamping (NaN -> 0), and code 0 when scale is not > 0.  Values are
+  not rotated.
+"""
+
+import math
+from functools import lru_cache
+
+import numpy as np
+
+from .codebook import make_codebook, stored_codebook
+from .rotation import dense_rotation, qjl_matrix, wht_rotate_fp32, wht_rotation_matrix, wht_signs
+
+ROW_BYTES = {"turbo4": 68, "turbo3": 56, "prod3": 56, "vgroup2": 48}
+CODE_BITS = {"turbo4": 4, "turbo3": 3, "prod3": 2}
+DEFAULT_CODEBOOK = {"turbo4": "quantile", "turbo3": "lloyd", "prod3": "lloyd"}
+QJL_SCALE_NUM = math.sqrt(math.pi / 2.0)  # the estimator's constant is sqrt(pi/2) / d
+
+
+def canonical_norm_fp32(x):
+    """The canonical fp32 norm of each row of x ([N, 128]); see the module docstring."""
+    x32 = np.asarray(x, dtype=np.float32)
+    if x32.shape[-1] != 128:
+        raise ValueError("the canonical norm tree is defined for d = 128")
+    sq = x32 * x32
+    p = (sq[:, 0::4] + sq[:, 1::4]) + (sq[:, 2::4] + sq[:, 3::4])  # [N, 32], one per lane
+    lanes = np.arange(32)
+    for h in (16, 8, 4, 2, 1):
+        p = p + p[:, lanes ^ h]
+    return np.sqrt(p[:, 0]).astype(np.float32)
+
+
+def normalize_fp32(x, n32):
+    """u = x / n in fp32 (IEEE division); rows with n == 0 give u = 0."""
+    x32 = np.asarray(x, dtype=np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        u = x32 / n32[:, None]
+    u[n32 == 0] = 0.0
+    return u.astype(np.float32)
+
+
+def nearest_index(y, b32):
+    """idx = #{k : y > b32[k]} (strict), compared in the precision of y."""
+    y = np.asarray(y)
+    b = b32.astype(y.dtype) if y.dtype == np.float64 else b32
+    return (y[..., None] > b).sum(axis=-1).astype(np.uint8)
+
+
+class Rotation:
+    """A seeded rotation: "wht" (randomized Hadamard) or "dense" (QR of a Gaussian)."""
+
+    def __init__(self, kind, seed, d=128):
+        self.kind = kind
+        self.seed = seed
+        self.d = d
+        if kind == "wht":
+            self.signs = wht_signs(seed, d)
+            self.R = wht_rotation_matrix(self.signs)  # exact fp64 (1/sqrt d) H D
+        elif kind == "dense":
+            self.pi32 = dense_rotation(seed, d).astype(np.float32)
+            self.R = self.pi32.astype(np.float64)  # the stored fp32 Pi, used in fp64 arithmetic
+        else:
+            raise ValueError(f"unknown rotation {kind!r}")
+
+    def encode_coords(self, u32):
+        """Rotated coordinates used for the index decision.
+
+        WHT: canonical fp32 butterfly (bit-exact contract).  Dense: y = Pi u in fp64
+        with the stored fp32 Pi (results may differ from a GPU only within 1e-5 of a
+        boundary).
+        """
+        if self.kind == "wht":
+            return wht_rotate_fp32(u32, self.signs)
+        return np.asarray(u32, dtype=np.float64) @ self.R.T
+
+    def forward(self, u):
+        """y = R u (fp64, row vectors)."""
+        return np.asarray(u, dtype=np.float64) @ self.R.T
+
+    def inverse(self, y):
+        """u = R^T y (fp64, row vectors)."""
+        return np.asarray(y, dtype=np.float64) @ self.R
+
+
+@lru_cache(maxsize=None)
+def _codebook(bits, d, kind):
+    return stored_codebook(make_codebook(bits, d, kind))
+
+
+@lru_cache(maxsize=None)
+def _rotation(kind, seed, d):
+    return Rotation(kind, seed, d)
+
+
+@lru_cache(maxsize=None)
+def _qjl32(seed, d):
+    return qjl_matrix(seed, d).astype(np.float32)
+
+
+def encode_turbo(x, rotation, b32):
+    """turbo4/turbo3 encode: returns (fp32 norms [N], indices [N, d], rotated coords)."""
+    n = canonical_norm_fp32(x)
+    u = normalize_fp32(x, n)
+    y = rotation.encode_coords(u)
+    return n, nearest_index(y, b32), y
+
+
+def pack_turbo4(n32, idx):
+    """[turbo4 post-mortem] sections 5, 7: fp32 norm, then qs[64] nibbles."""
+    N = len(n32)
+    out = np.zeros((N, 68), dtype=np.uint8)
+    out[:, 0:4] = np.asarray(n32, dtype="<f4").reshape(N, 1).view(np.uint8)
+    idx = np.asarray(idx, dtype=np.uint8)
+    out[:, 4:68] = idx[:, 0::2] | (idx[:, 1::2] << 4)
+    return out
+
+
+def unpack_turbo4(blocks):
+    """Inverse of pack_turbo4, using the section-5 extraction (qs[j/2] >> ((j%2)*4)) & 0xF."""
+    blocks = np.asarray(blocks, dtype=np.uint8)
+    n = blocks[:, 0:4].copy().view("<f4").reshape(-1)
+    j = np.arange(128)
+    idx = (blocks[:, 4 + j // 2] >> ((j % 2) * 4)) & 0xF
+    return n.astype(np.float32), idx.astype(np.uint8)
+
+
+def pack_turbo3(n32, idx):
+    """[turbo4 post-mortem] section 4 "2+1" layout, four 14-byte blocks per 128-vector."""
+    N = len(n32)
+    out = np.zeros((N, 56), dtype=np.uint8)
+    n16 = np.asarray(n32, dtype=np.float32).astype("<f2").reshape(N, 1).view(np.uint8)
+    idx = np.asarray(idx, dtype=np.uint8)
+    for c in range(4):
+        base = 14 * c
+        out[:, base:base + 2] = n16
+        sub = idx[:, 32 * c:32 * c + 32]
+        for j in range(32):
+            out[:, base + 2 + j // 4] |= (sub[:, j] & 3) << (2 * (j % 4))
+            out[:, base + 10 + j // 8] |= (sub[:, j] >> 2) << (j % 8)
+    return out
+
+
+def unpack_turbo3(blocks):
+    """Per-block fp16 norms [N, 4] and indices [N, 128] via the section-4 extraction.
+
+    idx = (qs[j/4] >> ((j%4)*2)) & 0x3; if (signs[j/8] & (1 << (j%8))) idx |= 4.
+    """
+    blocks = np.asarray(blocks, dtype=np.uint8)
+    N = blocks.shape[0]
+    norms = np.zeros((N, 4), dtype=np.float32)
+    idx = np.zeros((N, 128), dtype=np.uint8)
+    j = np.arange(32)
+    for c in range(4):
+        base = 14 * c
+        norms[:, c] = blocks[:, base:base + 2].copy().view("<f2").reshape(-1).astype(np.float32)
+        qs = blocks[:, base + 2:base + 10]
+        sg = blocks[:, base + 10:base + 14]
+        v = (qs[:, j // 4] >> ((j % 4) * 2)) & 0x3
+        hb = (sg[:, j // 8] >> (j % 8)) & 1
+        idx[:, 32 * c:32 * c + 32] = v | (hb << 2)
+    return norms, idx
+
+
+def encode_prod(x, rotation, c32, b32, S32):
+    """2-bit MSE + 1-bit QJL keys ([Triton deep dive] trick 2; [turbo4 post-mortem] section 2).
+
+    Returns (n fp32, gamma fp32, idx, sign bits, y, z): y the rotated coordinates
+    used for idx, z = S r the projection whose signs are stored.
+    """
+    n = canonical_norm_fp32(x)
+    u = normalize_fp32(x, n)
+    y = rotation.encode_coords(u)
+    idx = nearest_index(y, b32)
+    y_hat = c32.astype(np.float64)[idx]
+    x_tilde = rotation.inverse(y_hat)  # Pi^T y_hat, back in the unrotated normalised space
+    r = u.astype(np.float64) - x_tilde
+    gamma = np.sqrt(np.sum(r * r, axis=1))
+    sign_bits, z = qjl_sign_bits(S32, r)
+    return n, gamma.astype(np.float32), idx, sign_bits, y, z
+
+
+def qjl_sign_bits(S, r):
+    """QJL sketch of residuals r ([..., d]): z = S r and bits (z >= 0), leading axes batched.
+
+    ``S`` is [d, d] or batched [..., d, d] (one matrix per residual).
+    """
+    S = np.asarray(S, dtype=np.float64)
+    z = np.einsum("...ij,...j->...i", S, np.asarray(r, dtype=np.float64))
+    return (z >= 0.0).astype(np.uint8), z
+
+
+def qjl_residual_estimate(S, sign_bits, gamma):
+    """QJL reconstruction of the residual: (sqrt(pi/2)/d) * gamma * S^T sigma, sigma = +-1.
+
+    [turbo4 post-mortem] section 2 bug 2 (a matrix-vector product with S^T, scaled by
+    sqrt(pi/2)/sqrt(d) * ||x|| for S with N(0, 1/d) entries, i.e. sqrt(pi/2)/d for
+    the N(0,1) S used here -- [Triton deep dive] trick 2).  Leading axes batched.
+    """
+    S = np.asarray(S, dtype=np.float64)
+    d = S.shape[-1]
+    sigma = np.where(np.asarray(sign_bits) == 1, 1.0, -1.0)
+    st_sigma = np.einsum("...ij,...i->...j", S, sigma)
+    return (QJL_SCALE_NUM / d) * np.asarray(gamma, dtype=np.float64)[..., None] * st_sigma
+
+
+def _pack_2bit(codes):
+    N, d = codes.shape
+    out = np.zeros((N, d // 4), dtype=np.uint8)
+    for j in range(d):
+        out[:, j // 4] |= (codes[:, j] & 3) << (2 * (j % 4))
+    return out
+
+
+def _unpack_2bit(q, d):
+    j = np.arange(d)
+    return ((q[:, j // 4] >> (2 * (j % 4))) & 3).astype(np.uint8)
+
+
+def pack_prod(n32, gamma32, idx, sign_bits):
+    """fp32 norm, fp32 residual norm, qs[32] (2-bit, element j at bits 2*(j%4) of byte j/4),
+    signs[16] (bit i%8 of byte i/8, 1 means +1)."""
+    N = len(n32)
+    out = np.zeros((N, 56), dtype=np.uint8)
+    out[:, 0:4] = np.asarray(n32, dtype="<f4").reshape(N, 1).view(np.uint8)
+    out[:, 4:8] = np.asarray(gamma32, dtype="<f4").reshape(N, 1).view(np.uint8)
+    out[:, 8:40] = _pack_2bit(np.asarray(idx, dtype=np.uint8))
+    sb = np.asarray(sign_bits, dtype=np.uint8)
+    for i in range(128):
+        out[:, 40 + i // 8] |= sb[:, i] << (i % 8)
+    return out
+
+
+def unpack_prod(blocks):
+    blocks = np.asarray(blocks, dtype=np.uint8)
+    n = blocks[:, 0:4].copy().view("<f4").reshape(-1)
+    gamma = blocks[:, 4:8].copy().view("<f4").reshape(-1)
+    idx = _unpack_2bit(blocks[:, 8:40], 128)
+    i = np.arange(128)
+    sign_bits = (blocks[:, 40 + i // 8] >> (i % 8)) & 1
+    return n, gamma, idx, sign_bits.astype(np.uint8)
+
+
+def encode_vgroup(x, group=32):
+    """2-bit asymmetric group quantization of values (no rotation); see module docstring.
+
+    Returns (codes [N, d] uint8, scale fp16 [N, G], zero fp16 [N, G]).
+    """
+    x32 = np.asarray(x, dtype=np.float32)
+    N, d = x32.shape
+    G = d // group
+    xg = x32.reshape(N, G, group)
+    mn = np.fmin.reduce(xg, axis=2).astype(np.float32)
+    mx = np.fmax.reduce(xg, axis=2).astype(np.float32)
+    mn = (mn + np.float32(0.0)).astype(np.float32)
+    rng = (mx - mn).astype(np.float32)
+    s32 = (rng / np.float32(3.0)).astype(np.float32)
+    with np.errstate(over="ignore"):
+        scale16 = s32.astype(np.float16)
+        zero16 = mn.astype(np.float16)
+    s = scale16.astype(np.float32)[:, :, None]
+    z = zero16.astype(np.float32)[:, :, None]
+    with np.errstate(divide="ignore", invalid="ignore", over="ignore"):
+        t = ((xg - z).astype(np.float32) / s).astype(np.float32)
+    r = np.rint(t)
+    code = np.fmin(np.fmax(r, np.float32(0.0)), np.float32(3.0))
+    code = np.where(s > 0, code, np.float32(0.0))
+    return code.reshape(N, d).astype(np.uint8), scale16, zero16
+
+
+def pack_vgroup(codes, scale16, zero16):
+    N = codes.shape[0]
+    out = np.zeros((N, 48), dtype=np.uint8)
+    out[:, 0:32] = _pack_2bit(codes)
+    for g in range(4):
+        out[:, 32 + 4 * g:34 + 4 * g] = np.asarray(scale16[:, g], dtype="<f2").reshape(N, 1).view(np.uint8)
+        out[:, 34 + 4 * g:36 + 4 * g] = np.asarray(zero16[:, g], dtype="<f2").reshape(N, 1).view(np.uint8)
+    return out
+
+
+def unpack_vgroup(blocks):
+    blocks = np.asarray(blocks, dtype=np.uint8)
+    N = blocks.shape[0]
+    codes = _unpack_2bit(blocks[:, 0:32], 128)
+    scale = np.zeros((N, 4), dtype=np.float32)
+    zero = np.zeros((N, 4), dtype=np.float32)
+    for g in range(4):
+        scale[:, g] = blocks[:, 32 + 4 * g:34 + 4 * g].copy().view("<f2").reshape(-1).astype(np.float32)
+        zero[:, g] = blocks[:, 34 + 4 * g:36 + 4 * g].copy().view("<f2").reshape(-1).astype(np.float32)
+    return codes, scale, zero
+
+
+class Codec:
+    """One compressed format with its codebook, rotation and (for prod3) QJL matrix.
+
+    ``fmt`` in {"turbo4", "turbo3", "prod3", "vgroup2"}; ``rotation`` in
+    {"wht", "dense"}.  ``qjl_seed`` must differ from ``rot_seed`` for prod3
+    ([turbo4 post-mortem] section 10).
+    """
+
+    def __init__(self, fmt, d=128, rotation="wht", rot_seed=0, qjl_seed=None, codebook=None):
+        if d != 128:
+            raise ValueError("only d = 128 is defined")
+        self.fmt = fmt
+        self.d = d
+        self.row_bytes = ROW_BYTES[fmt]
+        self.rot = None
+        if fmt in CODE_BITS:
+            self.rot = _rotation(rotation, rot_seed, d)
+            self.codebook_kind = codebook or DEFAULT_CODEBOOK[fmt]
+            self.c32, self.b32 = _codebook(CODE_BITS[fmt], d, self.codebook_kind)
+        if fmt == "prod3":
+            if qjl_seed is None or qjl_seed == rot_seed:
+                raise ValueError("prod3 needs a QJL seed independent of the rotation seed")
+            self.S32 = _qjl32(qjl_seed, d)
+            self.qjl_seed = qjl_seed
+
+    # -- write path -----------------------------------------------------------------
+    def encode(self, x):
+        """Packed rows [N, row_bytes] plus the intermediate values used by parity checks."""
+        x = np.asarray(x, dtype=np.float32)
+        if self.fmt == "turbo4":
+            n, idx, y = encode_turbo(x, self.rot, self.b32)
+            return pack_turbo4(n, idx), {"n": n, "idx": idx, "y": y}
+        if self.fmt == "turbo3":
+            n, idx, y = encode_turbo(x, self.rot, self.b32)
+            return pack_turbo3(n, idx), {"n": n, "idx": idx, "y": y}
+        if self.fmt == "prod3":
+            n, gamma, idx, sb, y, z = encode_prod(x, self.rot, self.c32, self.b32, self.S32)
+            return pack_prod(n, gamma, idx, sb), {"n": n, "gamma": gamma, "idx": idx, "sign_bits": sb, "y": y, "z": z}
+        if self.fmt == "vgroup2":
+            codes, s16, z16 = encode_vgroup(x)
+            return pack_vgroup(codes, s16, z16), {"codes": codes, "scale": s16, "zero": z16}
+        raise ValueError(self.fmt)
+
+    # -- read side ------------------------------------------------------------------
+    def fields(self, blocks):
+        """Decoded fields in fp64: per-row scalars and per-element rotated-basis values."""
+        blocks = np.asarray(blocks, dtype=np.uint8).reshape(-1, self.row_bytes)
+        c = self.c32.astype(np.float64) if self.fmt in CODE_BITS else None
+        if self.fmt == "turbo4":
+            n, idx = unpack_turbo4(blocks)
+            return {"n": n.astype(np.float64), "y_hat": c[idx]}
+        if self.fmt == "turbo3":
+            norms, idx = unpack_turbo3(blocks)
+            n_elem = np.repeat(norms.astype(np.float64), 32, axis=1)
+            return {"n_elem": n_elem, "y_hat": c[idx]}
+        if self.fmt == "prod3":
+            n, gamma, idx, sb = unpack_prod(blocks)
+            return {"n": n.astype(np.float64), "gamma": gamma.astype(np.float64), "y_hat": c[idx],
+                    "sigma": np.where(sb == 1, 1.0, -1.0)}
+        codes, scale, zero = unpack_vgroup(blocks)
+        s = np.repeat(scale.astype(np.float64), 32, axis=1)
+        z = np.repeat(zero.astype(np.float64), 32, axis=1)
+        return {"v_hat": codes.astype(np.float64) * s + z}
+
+    def dequantize(self, blocks, unrotate=True):
+        """fp64 reconstruction x_hat of each row ([turbo4 post-mortem] section 4 dequant).
+
+        turbo4: n * Pi^T c[idx]; turbo3: per-32-block norm * Pi^T c[idx]; prod3:
+        n * (Pi^T c[idx] + (sqrt(pi/2)/d) * gamma * S^T sigma) (section 2 bug 2:
+        the QJL correction is a matrix-vector product with S^T, not raw +-1);
+        vgroup2: code * scale + zero.  With unrotate=False the turbo formats
+        return the rotated-basis values n * c[idx] (prod3 ignores it).
+        """
+        f = self.fields(blocks)
+        if self.fmt == "turbo4":
+            y = f["y_hat"] * f["n"][:, None]
+            return self.rot.inverse(y) if unrotate else y
+        if self.fmt == "turbo3":
+            y = f["y_hat"] * f["n_elem"]
+            return self.rot.inverse(y) if unrotate else y
+        if self.fmt == "prod3":
+            mse = self.rot.inverse(f["y_hat"])
+            sign_bits = (f["sigma"] > 0).astype(np.uint8)
+            qjl = qjl_residual_estimate(self.S32, sign_bits, f["gamma"])
+            return f["n"][:, None] * (mse + qjl)
+        return f["v_hat"]

@@ -1,0 +1,97 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and check a pin catches each one.
+
+Each case monkeypatches one oracle function with a broken variant and asserts that
+the corresponding pin fails; nothing here touches a GPU."""
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import oracle.attention as att
+import oracle.codebook as cb
+import oracle.formats as fm
+import oracle.rotation as rot
+from conftest import golden_lines
+
+D = 128
+
+
+def printed_table():
+    return np.array([float(v) for v in golden_lines("turbo4_centroids_d128.txt")])
+
+
+def test_codebook_wrong_cell_index_is_caught(monkeypatch):
+    good = cb.quantile_codebook(4, D)
+    assert np.max(np.abs(good - printed_table())) <= 5e-5 + 1e-9
+
+    def shifted(bits, d):  # off-by-one in the quantile cells
+        K = 1 << bits
+        sigma = 1 / math.sqrt(d)
+        t = [cb.std_normal_quantile(min(k + 0.5, K) / K) for k in range(K + 1)]
+        return np.array([sigma * cb._cond_mean_std(t[k], t[k + 1]) if t[k] < t[k + 1] else 0.0
+                         for k in range(K)])
+
+    bad = shifted(4, D)
+    assert np.max(np.abs(bad - printed_table())) > 1e-3
+
+
+def test_fwht_dropped_stage_is_caught():
+    from scipy import linalg
+    H = linalg.hadamard(D).astype(np.float64)
+
+    def fwht_missing_last_stage(v):
+        v = np.array(v, copy=True)
+        h = 1
+        while h < D // 2:
+            w = v.reshape(v.shape[:-1] + (D // (2 * h), 2, h))
+            a, b = w[..., 0, :].copy(), w[..., 1, :].copy()
+            w[..., 0, :], w[..., 1, :] = a + b, a - b
+            v = w.reshape(v.shape)
+            h *= 2
+        return v
+
+    assert np.array_equal(rot.fwht(np.eye(D)), H.T)
+    assert not np.array_equal(fwht_missing_last_stage(np.eye(D)), H.T)
+
+
+def test_transposed_query_rotation_is_caught(monkeypatch):
+    """Rotating q with Pi^T instead of Pi breaks compressed-domain == brute force."""
+    kc = fm.Codec("turbo4", rotation="dense", rot_seed=3)
+    x = np.random.default_rng(1).standard_normal((24, D)).astype(np.float32)
+    kb = kc.encode(x)[0].reshape(1, 1, 24, -1)
+    q = np.random.default_rng(2).standard_normal((1, 1, D))
+    kh = kc.dequantize(kb.reshape(-1, 68)).reshape(1, 1, 24, D)
+    ref, _ = oracle.attention_reference(q, kh, kh)
+    monkeypatch.setattr(kc.rot, "forward", lambda u: np.asarray(u, dtype=np.float64) @ kc.rot.R)
+    out, _ = att.attention_compressed_domain(q, kc, kb, kc, kb)
+    assert np.max(np.abs(out - ref)) > 1e-3
+
+
+def test_qjl_raw_signs_without_matrix_is_caught():
+    """Section 2 bug 2 (signs used as raw +-1 instead of S^T sigma) breaks the brute-force
+    prod score identity."""
+    kc = fm.Codec("prod3", rotation="dense", rot_seed=3, qjl_seed=1003)
+    x = np.random.default_rng(4).standard_normal((16, D)).astype(np.float32)
+    blk, aux = kc.encode(x)
+    good = kc.dequantize(blk)
+    f = kc.fields(blk)
+    raw = f["n"][:, None] * (kc.rot.inverse(f["y_hat"]) + (math.sqrt(math.pi / 2) / D) * f["gamma"][:, None] * f["sigma"])
+    q = np.random.default_rng(5).standard_normal(D)
+    assert np.max(np.abs(good @ q - raw @ q)) > 1e-2
+
+
+def test_norm_without_square_is_caught():
+    x = np.random.default_rng(6).standard_normal((10, D)).astype(np.float32)
+    n = fm.canonical_norm_fp32(x)
+    ref = np.linalg.norm(x.astype(np.float64), axis=1)
+    assert np.max(np.abs(n - ref) / ref) < 4e-7
+    bad = np.sqrt(np.abs(x).sum(1))
+    assert np.max(np.abs(bad - ref) / ref) > 1e-2
+
+
+def test_wrong_gqa_mapping_is_caught():
+    wrong = [h % 8 for h in range(32)]
+    right = [oracle.gqa_kv_head(h, 32, 8) for h in range(32)]
+    assert wrong != right and right[:4] == [0, 0, 0, 0]
