@@ -1,0 +1,270 @@
+"""Thin Python binding of the GB300 compressed-KV library (``include/tq.h``).
+
+Every function here only marshals arguments for the C ABI of ``lib/libtq.so``:
+device buffers are passed as torch tensors (or raw integer addresses), streams
+default to torch's current CUDA stream.  All computation runs in the library's
+CUDA kernels; if the library has not been built, importing this package raises
+ImportError instead of falling back to anything else.
+
+Build the library with ``python -m compressed_attention_gb300._build`` (or
+``__graft_entry__.build()``).
+"""
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "lib", "libtq.so")
+
+D = 128
+
+# tq_status
+TQ_OK, TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_ALIGNMENT, TQ_ERR_CUDA, TQ_ERR_ALLOC, TQ_ERR_WORKSPACE = range(7)
+# tq_format
+TQ_FMT_TURBO4, TQ_FMT_TURBO3, TQ_FMT_PROD3, TQ_FMT_VGROUP2 = range(4)
+# tq_codebook_kind
+TQ_CB_DEFAULT, TQ_CB_QUANTILE, TQ_CB_LLOYD = range(3)
+# tq_rotation_kind
+TQ_ROT_WHT, TQ_ROT_DENSE = range(2)
+# tq_dtype
+TQ_DTYPE_F32, TQ_DTYPE_BF16, TQ_DTYPE_F16 = range(3)
+
+FORMATS = {"turbo4": TQ_FMT_TURBO4, "turbo3": TQ_FMT_TURBO3, "prod3": TQ_FMT_PROD3, "vgroup2": TQ_FMT_VGROUP2}
+ROTATIONS = {"wht": TQ_ROT_WHT, "dense": TQ_ROT_DENSE}
+CODEBOOKS = {None: TQ_CB_DEFAULT, "default": TQ_CB_DEFAULT, "quantile": TQ_CB_QUANTILE, "lloyd": TQ_CB_LLOYD}
+
+
+class TQError(RuntimeError):
+    def __init__(self, status, func, detail):
+        self.status = status
+        super().__init__(f"{func} failed with status {status}: {detail}")
+
+
+class tq_params(ctypes.Structure):
+    _fields_ = [("d", ctypes.c_int32), ("format", ctypes.c_int32), ("codebook", ctypes.c_int32),
+                ("rotation", ctypes.c_int32), ("rot_seed", ctypes.c_uint64), ("qjl_seed", ctypes.c_uint64)]
+
+
+_vp, _i32, _i64, _u64, _f32, _sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64,
+                                    ctypes.c_float, ctypes.c_size_t)
+
+_SIGNATURES = {
+    "tq_make_codebook": (_i32, [_i32, _i32, _i32, _vp, _vp]),
+    "tq_make_rotation": (_i32, [_i32, _i32, _u64, _vp]),
+    "tq_make_qjl_matrix": (_i32, [_i32, _u64, _vp]),
+    "tq_row_bytes": (_i64, [_i32]),
+    "tq_cache_bytes": (_sz, [_i32, _i64]),
+    "tq_status_string": (ctypes.c_char_p, [_i32]),
+    "tq_last_error": (ctypes.c_char_p, []),
+    "tq_ctx_create": (_i32, [ctypes.POINTER(tq_params), ctypes.POINTER(_vp)]),
+    "tq_ctx_destroy": (_i32, [_vp]),
+    "tq_ctx_device_status": (_i32, [_vp, ctypes.POINTER(ctypes.c_int32), _i32]),
+    "tq_quantize_set_rows": (_i32, [_vp, _vp, _i32, _i64, _i64, _vp, _vp, _i64, _vp]),
+    "tq_dequantize": (_i32, [_vp, _vp, _i64, _i32, _vp, _vp]),
+    "tq_decode_workspace_size": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, ctypes.POINTER(_sz)]),
+    "tq_decode_num_splits": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, ctypes.POINTER(_i32)]),
+    "tq_decode_attention": (_i32, [_vp, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _f32,
+                                   _vp, _vp, _vp, _sz, _vp]),
+    "tq_decode_prepare_q": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _sz, _vp]),
+    "tq_decode_partial": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _sz, _vp]),
+    "tq_decode_combine": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _sz, _vp]),
+}
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is not built; run `python -m compressed_attention_gb300._build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in _SIGNATURES.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    return lib
+
+
+lib = _load()
+
+
+def _check(status, func):
+    if status != TQ_OK:
+        raise TQError(status, func, lib.tq_last_error().decode())
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    if hasattr(x, "ctypes"):  # numpy array (host)
+        return x.ctypes.data
+    raise TypeError(f"cannot take the address of {type(x).__name__}")
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dtype_code(t):
+    import torch
+    return {torch.float32: TQ_DTYPE_F32, torch.bfloat16: TQ_DTYPE_BF16, torch.float16: TQ_DTYPE_F16}[t.dtype]
+
+
+# --------------------------------------------------------------------------- host only
+
+def tq_make_codebook(bits, d=D, kind="quantile"):
+    """(centroids float32[2^bits], boundaries float32[2^bits - 1]) built on the host."""
+    import numpy as np
+    K = 1 << bits
+    c = np.zeros(K, np.float32)
+    b = np.zeros(max(K - 1, 1), np.float32)
+    _check(lib.tq_make_codebook(bits, d, CODEBOOKS[kind], c.ctypes.data, b.ctypes.data), "tq_make_codebook")
+    return c, b[:K - 1]
+
+
+def tq_make_rotation(kind, seed, d=D):
+    """Dense: float32 [d, d] Pi (y = Pi u).  WHT: float32 [d] signs."""
+    import numpy as np
+    out = np.zeros((d, d) if kind == "dense" else (d,), np.float32)
+    _check(lib.tq_make_rotation(ROTATIONS[kind], d, seed, out.ctypes.data), "tq_make_rotation")
+    return out
+
+
+def tq_make_qjl_matrix(seed, d=D):
+    import numpy as np
+    out = np.zeros((d, d), np.float32)
+    _check(lib.tq_make_qjl_matrix(d, seed, out.ctypes.data), "tq_make_qjl_matrix")
+    return out
+
+
+def tq_row_bytes(fmt):
+    return int(lib.tq_row_bytes(FORMATS.get(fmt, fmt)))
+
+
+def tq_cache_bytes(fmt, n_rows):
+    return int(lib.tq_cache_bytes(FORMATS.get(fmt, fmt), n_rows))
+
+
+# --------------------------------------------------------------------------- contexts
+
+class Ctx:
+    """Owns one tq_ctx (codebook, rotation, QJL matrix on the current device)."""
+
+    def __init__(self, fmt, rotation="wht", rot_seed=0, qjl_seed=0, codebook=None, d=D):
+        self.fmt = fmt
+        self.rotation = rotation
+        self.rot_seed = rot_seed
+        self.qjl_seed = qjl_seed
+        p = tq_params(d, FORMATS[fmt], CODEBOOKS[codebook], ROTATIONS[rotation], rot_seed, qjl_seed)
+        h = _vp()
+        _check(lib.tq_ctx_create(ctypes.byref(p), ctypes.byref(h)), "tq_ctx_create")
+        self.handle = h.value
+        self.row_bytes = tq_row_bytes(fmt)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            lib.tq_ctx_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def tq_ctx_create(fmt, rotation="wht", rot_seed=0, qjl_seed=0, codebook=None, d=D):
+    return Ctx(fmt, rotation, rot_seed, qjl_seed, codebook, d)
+
+
+def tq_ctx_destroy(ctx):
+    ctx.close()
+
+
+def tq_ctx_device_status(ctx, clear=True):
+    v = ctypes.c_int32(0)
+    _check(lib.tq_ctx_device_status(ctx.handle, ctypes.byref(v), int(clear)), "tq_ctx_device_status")
+    return v.value
+
+
+# --------------------------------------------------------------------------- write / read
+
+def tq_quantize_set_rows(ctx, src, dst_cache, row_ids=None, n_rows=None, stream=None):
+    """Quantize rows of ``src`` ([n, 128] fp32/bf16 CUDA tensor) into ``dst_cache`` (uint8 CUDA
+    tensor of packed rows) at slots ``row_ids`` (int64 CUDA tensor) or 0..n-1."""
+    n = src.shape[0] if n_rows is None else n_rows
+    stride = src.stride(0) if src.dim() == 2 else D
+    dst_rows = dst_cache.numel() // ctx.row_bytes
+    _check(lib.tq_quantize_set_rows(ctx.handle, _ptr(src), _dtype_code(src), n, stride, _ptr(row_ids),
+                                    _ptr(dst_cache), dst_rows, _stream(stream)), "tq_quantize_set_rows")
+
+
+def tq_dequantize(ctx, cache, n_rows, dst, unrotate=True, stream=None):
+    _check(lib.tq_dequantize(ctx.handle, _ptr(cache), n_rows, int(unrotate), _ptr(dst), _stream(stream)),
+           "tq_dequantize")
+
+
+def tq_decode_workspace_size(k_ctx, v_ctx, B, Hq, Hkv, L):
+    n = _sz(0)
+    _check(lib.tq_decode_workspace_size(k_ctx.handle, v_ctx.handle, B, Hq, Hkv, L, ctypes.byref(n)),
+           "tq_decode_workspace_size")
+    return n.value
+
+
+def tq_decode_num_splits(k_ctx, v_ctx, B, Hq, Hkv, L):
+    n = _i32(0)
+    _check(lib.tq_decode_num_splits(k_ctx.handle, v_ctx.handle, B, Hq, Hkv, L, ctypes.byref(n)),
+           "tq_decode_num_splits")
+    return n.value
+
+
+def _q_args(q):
+    return _ptr(q), _dtype_code(q)
+
+
+def tq_decode_attention(k_ctx, v_ctx, q, k_cache, v_cache, out, workspace, B, Hq, Hkv, L,
+                        seq_lens=None, scale=0.0, scores=None, stream=None):
+    qp, qd = _q_args(q)
+    _check(lib.tq_decode_attention(k_ctx.handle, v_ctx.handle, qp, qd, _ptr(k_cache), _ptr(v_cache),
+                                   _ptr(seq_lens), B, Hq, Hkv, L, scale, _ptr(out), _ptr(scores),
+                                   _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                   _stream(stream)), "tq_decode_attention")
+
+
+def tq_decode_prepare_q(k_ctx, v_ctx, q, workspace, B, Hq, Hkv, L, scale=0.0, stream=None):
+    qp, qd = _q_args(q)
+    _check(lib.tq_decode_prepare_q(k_ctx.handle, v_ctx.handle, qp, qd, B, Hq, Hkv, L, scale, _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(stream)),
+           "tq_decode_prepare_q")
+
+
+def tq_decode_partial(k_ctx, v_ctx, k_cache, v_cache, workspace, B, Hq, Hkv, L, seq_lens=None, scores=None,
+                      stream=None):
+    _check(lib.tq_decode_partial(k_ctx.handle, v_ctx.handle, _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
+                                 B, Hq, Hkv, L, _ptr(scores), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream(stream)),
+           "tq_decode_partial")
+
+
+def tq_decode_combine(k_ctx, v_ctx, out, workspace, B, Hq, Hkv, L, stream=None):
+    _check(lib.tq_decode_combine(k_ctx.handle, v_ctx.handle, B, Hq, Hkv, L, _ptr(out), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream(stream)),
+           "tq_decode_combine")
+
+
+def alloc_workspace(nbytes, device="cuda"):
+    """A 256-byte aligned uint8 CUDA tensor of at least ``nbytes`` bytes."""
+    import torch
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def alloc_cache(fmt, n_rows, device="cuda"):
+    """A uint8 CUDA tensor sized by tq_cache_bytes (readable to the next 16-byte boundary)."""
+    import torch
+    return torch.zeros(tq_cache_bytes(fmt, n_rows), dtype=torch.uint8, device=device)

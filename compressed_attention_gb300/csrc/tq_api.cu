@@ -1,0 +1,379 @@
+// The extern "C" entry points of tq.h: argument validation on the host, context
+// construction, and dispatch to the kernel launchers.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "tq_internal.h"
+
+namespace tq {
+const char *last_error();
+}
+
+using namespace tq;
+
+namespace {
+
+tq_status fail(tq_status s, const char *msg) {
+  set_error("%s", msg);
+  return s;
+}
+
+tq_status cuda_fail(cudaError_t e, const char *where) {
+  set_error("%s: %s", where, cudaGetErrorString(e));
+  return TQ_ERR_CUDA;
+}
+
+bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+int code_bits(int fmt) {
+  switch (fmt) {
+    case TQ_FMT_TURBO4: return 4;
+    case TQ_FMT_TURBO3: return 3;
+    case TQ_FMT_PROD3: return 2;
+    default: return 0;
+  }
+}
+
+tq_status build_rotation(int kind, uint64_t seed, std::vector<float> &r, uint32_t *neg) {
+  r.assign((size_t)D * D, 0.f);
+  if (kind == TQ_ROT_DENSE) {
+    std::vector<double> pi((size_t)D * D);
+    if (!dense_rotation_f64(seed, D, pi.data())) return fail(TQ_ERR_INVALID_ARG, "rank-deficient Gaussian");
+    for (size_t i = 0; i < pi.size(); ++i) r[i] = (float)pi[i];
+    return TQ_OK;
+  }
+  uint64_t out[D];
+  splitmix64_fill(seed, out, D);
+  for (int i = 0; i < 4; ++i) neg[i] = 0;
+  double s[D];
+  for (int j = 0; j < D; ++j) {
+    const bool minus = (out[j] >> 63) != 0;
+    s[j] = minus ? -1.0 : 1.0;
+    if (minus) neg[j / 32] |= 1u << (j % 32);
+  }
+  // R = (1/sqrt(d)) H D with H the Sylvester Hadamard matrix, H[i][j] = (-1)^popcount(i & j).
+  const double inv = 1.0 / std::sqrt((double)D);
+  for (int i = 0; i < D; ++i)
+    for (int j = 0; j < D; ++j) {
+      const double h = (__builtin_popcount(i & j) & 1) ? -1.0 : 1.0;
+      r[(size_t)i * D + j] = (float)(h * s[j] * inv);
+    }
+  return TQ_OK;
+}
+
+template <typename T>
+tq_status to_device(T **dst, const T *src, size_t n) {
+  cudaError_t e = cudaMalloc((void **)dst, n * sizeof(T));
+  if (e != cudaSuccess) return fail(TQ_ERR_ALLOC, "cudaMalloc failed");
+  e = cudaMemcpy(*dst, src, n * sizeof(T), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy");
+  return TQ_OK;
+}
+
+bool decode_pair_supported(const tq_ctx *k, const tq_ctx *v) {
+  return k->fmt == TQ_FMT_TURBO4 && v->fmt == TQ_FMT_TURBO4;
+}
+
+tq_status check_decode_common(const tq_ctx *k, const tq_ctx *v, int B, int Hq, int Hkv, int L,
+                              DecodeShape *shape) {
+  if (!k || !v) return fail(TQ_ERR_INVALID_ARG, "null context");
+  if (B < 1 || Hq < 1 || Hkv < 1 || L < 1) return fail(TQ_ERR_INVALID_ARG, "B, Hq, Hkv and L must be >= 1");
+  if (Hq % Hkv != 0) return fail(TQ_ERR_INVALID_ARG, "Hq must be a multiple of Hkv");
+  if (!decode_pair_supported(k, v))
+    return fail(TQ_ERR_UNSUPPORTED, "no decode kernel for this (key, value) format pair");
+  decode_shape(k, v, B, Hq, Hkv, L, shape);
+  if ((int64_t)B * Hkv * shape->n_hg > 65535) return fail(TQ_ERR_UNSUPPORTED, "B * Hkv too large for one launch");
+  return TQ_OK;
+}
+
+tq_status check_workspace(const DecodeShape &s, void *ws, size_t bytes, Workspace *w) {
+  if (!ws) return fail(TQ_ERR_INVALID_ARG, "null workspace");
+  if (!aligned(ws, 256)) return fail(TQ_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  *w = carve_workspace(s, ws);
+  if (bytes < w->bytes) return fail(TQ_ERR_WORKSPACE, "workspace smaller than tq_decode_workspace_size()");
+  return TQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *tq_status_string(tq_status s) {
+  switch (s) {
+    case TQ_OK: return "ok";
+    case TQ_ERR_INVALID_ARG: return "invalid argument";
+    case TQ_ERR_UNSUPPORTED: return "unsupported";
+    case TQ_ERR_ALIGNMENT: return "misaligned pointer or stride";
+    case TQ_ERR_CUDA: return "CUDA error";
+    case TQ_ERR_ALLOC: return "allocation failed";
+    case TQ_ERR_WORKSPACE: return "workspace too small";
+  }
+  return "unknown status";
+}
+
+const char *tq_last_error(void) { return tq::last_error(); }
+
+int64_t tq_row_bytes(int format) {
+  switch (format) {
+    case TQ_FMT_TURBO4: return 68;
+    case TQ_FMT_TURBO3: return 56;
+    case TQ_FMT_PROD3: return 56;
+    case TQ_FMT_VGROUP2: return 48;
+  }
+  return -1;
+}
+
+size_t tq_cache_bytes(int format, int64_t n_rows) {
+  const int64_t rb = tq_row_bytes(format);
+  if (rb < 0 || n_rows < 0) return 0;
+  return ((size_t)n_rows * (size_t)rb + 15) & ~(size_t)15;
+}
+
+tq_status tq_make_codebook(int bits, int d, int kind, float *centroids, float *boundaries) {
+  if (d != D) return fail(TQ_ERR_UNSUPPORTED, "only d = 128 is supported");
+  if (bits < 1 || bits > 4) return fail(TQ_ERR_UNSUPPORTED, "bits must be 1..4");
+  if (kind != TQ_CB_QUANTILE && kind != TQ_CB_LLOYD) return fail(TQ_ERR_INVALID_ARG, "bad codebook kind");
+  if (!centroids) return fail(TQ_ERR_INVALID_ARG, "null centroids");
+  double c[16];
+  if (!make_codebook_f64(bits, d, kind, c)) return fail(TQ_ERR_INVALID_ARG, "codebook construction failed");
+  store_codebook(c, 1 << bits, centroids, boundaries);
+  return TQ_OK;
+}
+
+tq_status tq_make_rotation(int kind, int d, uint64_t seed, float *out) {
+  if (d != D) return fail(TQ_ERR_UNSUPPORTED, "only d = 128 is supported");
+  if (!out) return fail(TQ_ERR_INVALID_ARG, "null output");
+  if (kind != TQ_ROT_WHT && kind != TQ_ROT_DENSE) return fail(TQ_ERR_INVALID_ARG, "bad rotation kind");
+  std::vector<float> r;
+  uint32_t neg[4];
+  tq_status s = build_rotation(kind, seed, r, neg);
+  if (s != TQ_OK) return s;
+  if (kind == TQ_ROT_DENSE) {
+    std::memcpy(out, r.data(), r.size() * sizeof(float));
+  } else {
+    for (int j = 0; j < D; ++j) out[j] = ((neg[j / 32] >> (j % 32)) & 1u) ? -1.f : 1.f;
+  }
+  return TQ_OK;
+}
+
+tq_status tq_make_qjl_matrix(int d, uint64_t seed, float *out) {
+  if (d != D) return fail(TQ_ERR_UNSUPPORTED, "only d = 128 is supported");
+  if (!out) return fail(TQ_ERR_INVALID_ARG, "null output");
+  std::vector<double> g((size_t)D * D);
+  gaussian_fill(seed, g.data(), g.size());
+  for (size_t i = 0; i < g.size(); ++i) out[i] = (float)g[i];
+  return TQ_OK;
+}
+
+tq_status tq_ctx_create(const tq_params *params, tq_ctx **out) {
+  if (!params || !out) return fail(TQ_ERR_INVALID_ARG, "null argument");
+  *out = nullptr;
+  const tq_params &p = *params;
+  if (p.d != D) return fail(TQ_ERR_UNSUPPORTED, "only d = 128 is supported");
+  if (p.format < TQ_FMT_TURBO4 || p.format > TQ_FMT_VGROUP2) return fail(TQ_ERR_INVALID_ARG, "bad format");
+  const bool rotated = p.format != TQ_FMT_VGROUP2;
+  if (rotated && p.rotation != TQ_ROT_WHT && p.rotation != TQ_ROT_DENSE)
+    return fail(TQ_ERR_INVALID_ARG, "bad rotation kind");
+  if (rotated && p.codebook != TQ_CB_DEFAULT && p.codebook != TQ_CB_QUANTILE && p.codebook != TQ_CB_LLOYD)
+    return fail(TQ_ERR_INVALID_ARG, "bad codebook kind");
+  if (p.format == TQ_FMT_PROD3 && p.qjl_seed == p.rot_seed)
+    return fail(TQ_ERR_INVALID_ARG, "the QJL seed must differ from the rotation seed");
+
+  tq_ctx *c = new (std::nothrow) tq_ctx();
+  if (!c) return fail(TQ_ERR_ALLOC, "host allocation failed");
+  c->p = p;
+  c->fmt = p.format;
+  cudaError_t e = cudaGetDevice(&c->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
+  if (e != cudaSuccess) {
+    delete c;
+    return cuda_fail(e, "cudaGetDevice");
+  }
+  tq_status s = TQ_OK;
+  if (rotated) {
+    const int bits = code_bits(p.format);
+    int kind = p.codebook;
+    if (kind == TQ_CB_DEFAULT) kind = (p.format == TQ_FMT_TURBO4) ? TQ_CB_QUANTILE : TQ_CB_LLOYD;
+    double c64[16];
+    make_codebook_f64(bits, D, kind, c64);
+    c->cb.bits = bits;
+    c->cb.K = 1 << bits;
+    store_codebook(c64, c->cb.K, c->cb.c, c->cb.b);
+    c->f16 = make_f16_table(c->cb.c, c->cb.K);
+    std::vector<float> r;
+    s = build_rotation(p.rotation, p.rot_seed, r, c->wht_neg);
+    if (s == TQ_OK) s = to_device(&c->d_pi, r.data(), r.size());
+    if (s == TQ_OK) {
+      std::vector<float> rt((size_t)D * D);
+      for (int i = 0; i < D; ++i)
+        for (int j = 0; j < D; ++j) rt[(size_t)j * D + i] = r[(size_t)i * D + j];
+      s = to_device(&c->d_pit, rt.data(), rt.size());
+    }
+    if (s == TQ_OK && p.format == TQ_FMT_PROD3) {
+      std::vector<float> S((size_t)D * D);
+      tq_make_qjl_matrix(D, p.qjl_seed, S.data());
+      s = to_device(&c->d_S, S.data(), S.size());
+    }
+  }
+  if (s == TQ_OK) {
+    e = cudaMalloc((void **)&c->d_status, sizeof(int32_t));
+    if (e != cudaSuccess) s = fail(TQ_ERR_ALLOC, "cudaMalloc failed");
+    else if ((e = cudaMemset(c->d_status, 0, sizeof(int32_t))) != cudaSuccess) s = cuda_fail(e, "cudaMemset");
+  }
+  if (s != TQ_OK) {
+    tq_ctx_destroy(c);
+    return s;
+  }
+  *out = c;
+  return TQ_OK;
+}
+
+tq_status tq_ctx_destroy(tq_ctx *ctx) {
+  if (!ctx) return TQ_OK;
+  cudaFree(ctx->d_pi);
+  cudaFree(ctx->d_pit);
+  cudaFree(ctx->d_S);
+  cudaFree(ctx->d_status);
+  delete ctx;
+  return TQ_OK;
+}
+
+tq_status tq_ctx_device_status(const tq_ctx *ctx, int32_t *status, int clear) {
+  if (!ctx || !status) return fail(TQ_ERR_INVALID_ARG, "null argument");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  e = cudaMemcpy(status, ctx->d_status, sizeof(int32_t), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy");
+  if (clear && (e = cudaMemset(ctx->d_status, 0, sizeof(int32_t))) != cudaSuccess) return cuda_fail(e, "cudaMemset");
+  return TQ_OK;
+}
+
+tq_status tq_quantize_set_rows(const tq_ctx *ctx, const void *src, int src_dtype, int64_t n_rows,
+                               int64_t src_row_stride, const int64_t *row_ids, void *dst_cache,
+                               int64_t dst_rows, tq_stream_t stream) {
+  if (!ctx) return fail(TQ_ERR_INVALID_ARG, "null context");
+  if (n_rows < 0) return fail(TQ_ERR_INVALID_ARG, "n_rows < 0");
+  if (n_rows == 0) return TQ_OK;
+  if (!src || !dst_cache) return fail(TQ_ERR_INVALID_ARG, "null source or cache");
+  if (src_dtype != TQ_DTYPE_F32 && src_dtype != TQ_DTYPE_BF16)
+    return fail(TQ_ERR_UNSUPPORTED, "source dtype must be F32 or BF16");
+  if (src_row_stride < D) return fail(TQ_ERR_INVALID_ARG, "source row stride < 128");
+  if (dst_rows < 1) return fail(TQ_ERR_INVALID_ARG, "dst_rows < 1");
+  if (!row_ids && dst_rows < n_rows) return fail(TQ_ERR_INVALID_ARG, "identity slots need dst_rows >= n_rows");
+  const size_t esz = src_dtype == TQ_DTYPE_F32 ? 4 : 2;
+  const size_t need = src_dtype == TQ_DTYPE_F32 ? 16 : 8;
+  if (!aligned(src, need) || ((size_t)src_row_stride * esz) % need != 0)
+    return fail(TQ_ERR_ALIGNMENT, "source rows must be 16-byte (F32) or 8-byte (BF16) aligned");
+  if (!aligned(dst_cache, 16)) return fail(TQ_ERR_ALIGNMENT, "cache must be 16-byte aligned");
+  if (row_ids && !aligned(row_ids, 8)) return fail(TQ_ERR_ALIGNMENT, "row_ids must be 8-byte aligned");
+  WriteLaunch w{src, src_dtype, n_rows, src_row_stride, row_ids, (uint8_t *)dst_cache, dst_rows};
+  cudaError_t e = launch_write(ctx, w, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "write kernel launch");
+  return TQ_OK;
+}
+
+tq_status tq_dequantize(const tq_ctx *ctx, const void *cache, int64_t n_rows, int unrotate,
+                        float *dst, tq_stream_t stream) {
+  if (!ctx) return fail(TQ_ERR_INVALID_ARG, "null context");
+  if (n_rows < 0) return fail(TQ_ERR_INVALID_ARG, "n_rows < 0");
+  if (n_rows == 0) return TQ_OK;
+  if (!cache || !dst) return fail(TQ_ERR_INVALID_ARG, "null cache or output");
+  if (!aligned(cache, 16)) return fail(TQ_ERR_ALIGNMENT, "cache must be 16-byte aligned");
+  if (!aligned(dst, 4)) return fail(TQ_ERR_ALIGNMENT, "output must be 4-byte aligned");
+  cudaError_t e = launch_dequantize(ctx, (const uint8_t *)cache, n_rows, unrotate, dst, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "dequantize launch");
+  return TQ_OK;
+}
+
+tq_status tq_decode_num_splits(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, int Hq, int Hkv,
+                               int L, int *n_split) {
+  if (!n_split) return fail(TQ_ERR_INVALID_ARG, "null output");
+  DecodeShape s;
+  tq_status st = check_decode_common(k_ctx, v_ctx, B, Hq, Hkv, L, &s);
+  if (st != TQ_OK) return st;
+  *n_split = s.n_split;
+  return TQ_OK;
+}
+
+tq_status tq_decode_workspace_size(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, int Hq,
+                                   int Hkv, int L, size_t *bytes) {
+  if (!bytes) return fail(TQ_ERR_INVALID_ARG, "null output");
+  DecodeShape s;
+  tq_status st = check_decode_common(k_ctx, v_ctx, B, Hq, Hkv, L, &s);
+  if (st != TQ_OK) return st;
+  *bytes = carve_workspace(s, nullptr).bytes;
+  return TQ_OK;
+}
+
+tq_status tq_decode_prepare_q(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *q,
+                              int q_dtype, int B, int Hq, int Hkv, int L, float scale,
+                              void *workspace, size_t workspace_bytes, tq_stream_t stream) {
+  DecodeShape s;
+  tq_status st = check_decode_common(k_ctx, v_ctx, B, Hq, Hkv, L, &s);
+  if (st != TQ_OK) return st;
+  if (!q) return fail(TQ_ERR_INVALID_ARG, "null q");
+  if (q_dtype != TQ_DTYPE_F32 && q_dtype != TQ_DTYPE_BF16 && q_dtype != TQ_DTYPE_F16)
+    return fail(TQ_ERR_INVALID_ARG, "bad q dtype");
+  if (!aligned(q, 16)) return fail(TQ_ERR_ALIGNMENT, "q must be 16-byte aligned");
+  if (!std::isfinite(scale)) return fail(TQ_ERR_INVALID_ARG, "scale must be finite");
+  if (scale == 0.f) scale = 1.0f / std::sqrt((float)D);
+  Workspace w;
+  if ((st = check_workspace(s, workspace, workspace_bytes, &w)) != TQ_OK) return st;
+  cudaError_t e = launch_prepare_q(k_ctx, q, q_dtype, s, scale, w, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "prepare_q launch");
+  return TQ_OK;
+}
+
+tq_status tq_decode_partial(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *k_cache,
+                            const void *v_cache, const int32_t *seq_lens, int B, int Hq, int Hkv,
+                            int L, float *scores_dbg, void *workspace, size_t workspace_bytes,
+                            tq_stream_t stream) {
+  DecodeShape s;
+  tq_status st = check_decode_common(k_ctx, v_ctx, B, Hq, Hkv, L, &s);
+  if (st != TQ_OK) return st;
+  if (!k_cache || !v_cache) return fail(TQ_ERR_INVALID_ARG, "null cache");
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return fail(TQ_ERR_ALIGNMENT, "caches must be 16-byte aligned");
+  if (seq_lens && !aligned(seq_lens, 4)) return fail(TQ_ERR_ALIGNMENT, "seq_lens must be 4-byte aligned");
+  if (scores_dbg && !aligned(scores_dbg, 4)) return fail(TQ_ERR_ALIGNMENT, "scores must be 4-byte aligned");
+  Workspace w;
+  if ((st = check_workspace(s, workspace, workspace_bytes, &w)) != TQ_OK) return st;
+  cudaError_t e = launch_partial(k_ctx, v_ctx, (const uint8_t *)k_cache, (const uint8_t *)v_cache,
+                                 seq_lens, s, scores_dbg, w, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "partial launch");
+  return TQ_OK;
+}
+
+tq_status tq_decode_combine(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, int Hq, int Hkv,
+                            int L, float *out, void *workspace, size_t workspace_bytes,
+                            tq_stream_t stream) {
+  DecodeShape s;
+  tq_status st = check_decode_common(k_ctx, v_ctx, B, Hq, Hkv, L, &s);
+  if (st != TQ_OK) return st;
+  if (!out) return fail(TQ_ERR_INVALID_ARG, "null output");
+  if (!aligned(out, 4)) return fail(TQ_ERR_ALIGNMENT, "output must be 4-byte aligned");
+  Workspace w;
+  if ((st = check_workspace(s, workspace, workspace_bytes, &w)) != TQ_OK) return st;
+  cudaError_t e = launch_combine(k_ctx, v_ctx, s, out, w, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  return TQ_OK;
+}
+
+tq_status tq_decode_attention(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *q,
+                              int q_dtype, const void *k_cache, const void *v_cache,
+                              const int32_t *seq_lens, int B, int Hq, int Hkv, int L, float scale,
+                              float *out, float *scores_dbg, void *workspace,
+                              size_t workspace_bytes, tq_stream_t stream) {
+  tq_status st = tq_decode_prepare_q(k_ctx, v_ctx, q, q_dtype, B, Hq, Hkv, L, scale, workspace,
+                                     workspace_bytes, stream);
+  if (st != TQ_OK) return st;
+  st = tq_decode_partial(k_ctx, v_ctx, k_cache, v_cache, seq_lens, B, Hq, Hkv, L, scores_dbg,
+                         workspace, workspace_bytes, stream);
+  if (st != TQ_OK) return st;
+  return tq_decode_combine(k_ctx, v_ctx, B, Hq, Hkv, L, out, workspace, workspace_bytes, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,105 @@
+// Internal declarations shared by the host library and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tq.h"
+
+namespace tq {
+
+constexpr int D = 128;
+
+// Device status codes (see tq_ctx_device_status in tq.h).
+enum DevErr : int32_t { DEVERR_ROW_OOB = 1, DEVERR_SEQLEN = 2, DEVERR_TIMEOUT = 3 };
+
+// Stored codebook: K fp32 centroids and K-1 fp32 decision boundaries.
+struct Codebook {
+  int bits = 0;
+  int K = 0;
+  float c[16] = {};
+  float b[15] = {};
+};
+
+// fp16 operand table of a symmetric codebook for the tensor-core decode.
+// Magnitude m (0 = largest) of the scaled centroid alpha*|c_m| as fp16; byte
+// planes split for prmt lookups: lo[] holds the low bytes of entries 0..7, hi[]
+// the high bytes.  alpha is chosen so the fp16 rounding error of all entries
+// is smallest (it is divided out again after the products).
+struct F16Table {
+  uint32_t lo[2] = {0, 0};
+  uint32_t hi[2] = {0, 0};
+  float alpha = 1.0f;
+  float max_rel_err = 0.0f;
+};
+
+}  // namespace tq
+
+struct tq_ctx {
+  tq_params p{};
+  int device = 0;
+  int num_sms = 0;
+  int fmt = 0;
+  tq::Codebook cb{};
+  tq::F16Table f16{};
+  uint32_t wht_neg[4] = {0, 0, 0, 0};  // bit j set: WHT sign j is -1
+  float *d_pi = nullptr;                // rotation R (dense Pi or the WHT matrix), fp32 row-major
+  float *d_pit = nullptr;               // R^T, fp32 row-major
+  float *d_S = nullptr;                 // QJL matrix S, fp32 [128][128] row-major
+  int32_t *d_status = nullptr;          // device status word
+};
+
+namespace tq {
+
+// ---- host helpers (tq_host.cpp) ----
+bool make_codebook_f64(int bits, int d, int kind, double *c);
+void store_codebook(const double *c64, int K, float *c32, float *b32);
+void splitmix64_fill(uint64_t seed, uint64_t *out, size_t n);
+void gaussian_fill(uint64_t seed, double *out, size_t n);
+bool dense_rotation_f64(uint64_t seed, int d, double *pi);
+F16Table make_f16_table(const float *c32, int K);
+void set_error(const char *fmt, ...);
+
+// ---- kernel launchers ----
+struct WriteLaunch {
+  const void *src;
+  int src_dtype;
+  int64_t n_rows;
+  int64_t stride;
+  const int64_t *row_ids;
+  uint8_t *dst;
+  int64_t dst_rows;
+};
+cudaError_t launch_write(const tq_ctx *ctx, const WriteLaunch &w, cudaStream_t st);
+
+cudaError_t launch_dequantize(const tq_ctx *ctx, const uint8_t *cache, int64_t n_rows,
+                              int unrotate, float *dst, cudaStream_t st);
+
+struct DecodeShape {
+  int B, Hq, Hkv, L;
+  int gq;       // q-heads per KV head
+  int n_hg;     // head groups (of at most 8 q-heads) per KV head
+  int n_split;  // key splits
+  int chunk;    // keys per split (multiple of the tile)
+};
+struct Workspace {
+  uint32_t *qhl;     // [B*Hq][2 operands][128 fp16]: hi then lo, per operand (q_rot, sketch)
+  float *qsc;        // [B*Hq][2] power-of-two scales of the two operands
+  float *partials;   // [B*Hq][n_split][PARTIAL_FLOATS]
+  size_t bytes;
+};
+constexpr int PARTIAL_FLOATS = 2 + 4 + D;  // max, sum, 4 group zero-terms, acc[128]
+
+bool decode_shape(const tq_ctx *k, const tq_ctx *v, int B, int Hq, int Hkv, int L,
+                  DecodeShape *s);
+Workspace carve_workspace(const DecodeShape &s, void *base);
+
+cudaError_t launch_prepare_q(const tq_ctx *k, const void *q, int q_dtype, const DecodeShape &s,
+                             float scale, const Workspace &ws, cudaStream_t st);
+cudaError_t launch_partial(const tq_ctx *k, const tq_ctx *v, const uint8_t *kc,
+                           const uint8_t *vc, const int32_t *seq_lens, const DecodeShape &s,
+                           float *scores_dbg, const Workspace &ws, cudaStream_t st);
+cudaError_t launch_combine(const tq_ctx *k, const tq_ctx *v, const DecodeShape &s, float *out,
+                           const Workspace &ws, cudaStream_t st);
+
+}  // namespace tq

@@ -1,0 +1,386 @@
+// Write path / SET_ROWS kernels: norm -> normalise -> rotate -> nearest centroid
+// -> pack, one warp per row ("turboquant_plus: how the turbo4 KV format came
+// back", section 1 encode chain; section 2 dedicated SET_ROWS per format;
+// sections 4-5 block layouts).  The V group quantizer follows "TurboQuant fused
+// Triton kernels deep dive", "write path and codebook" (2-bit group
+// quantization, value = code * scale + zero).
+//
+// Lane l of a warp holds elements 4l..4l+3 of its row.  The norm is the
+// canonical fp32 tree: squares and adds rounded one by one (no contraction),
+// four-element partial sums per lane, then a butterfly over lanes 16,8,4,2,1.
+// The WHT rotation is the same butterfly over elements (stages 1, 2 inside a
+// lane, 4..64 across lanes), so its result is bit-identical to a plain
+// sequential fp32 implementation of the same stage order.
+#include "tq_device.cuh"
+#include "tq_internal.h"
+
+namespace tq {
+
+namespace {
+
+constexpr int WARPS = 8;
+constexpr int ROWBUF = 72;  // per-warp staging for one packed row (max 68 bytes)
+
+struct WriteParams {
+  const void *src;
+  int64_t n_rows;
+  int64_t stride;
+  const int64_t *row_ids;
+  uint8_t *dst;
+  int64_t dst_rows;
+  int32_t *status;
+  float c[16];
+  float b[15];
+  uint32_t wht_neg[4];
+  const float *pi;  // dense: fp32 [128][128]
+  const float *S;   // prod3: fp32 [128][128]
+};
+
+template <int SRC>
+__device__ __forceinline__ void load4(const void *src, int64_t row, int64_t stride, int lane,
+                                      float (&x)[4]) {
+  if (SRC == TQ_DTYPE_F32) {
+    const float4 v = *reinterpret_cast<const float4 *>(static_cast<const float *>(src) +
+                                                       row * stride + 4 * lane);
+    x[0] = v.x, x[1] = v.y, x[2] = v.z, x[3] = v.w;
+  } else {
+    const uint2 v = *reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(src) +
+                                                     row * stride + 4 * lane);
+    x[0] = bf16_bits_to_f32(v.x & 0xFFFFu);
+    x[1] = bf16_bits_to_f32(v.x >> 16);
+    x[2] = bf16_bits_to_f32(v.y & 0xFFFFu);
+    x[3] = bf16_bits_to_f32(v.y >> 16);
+  }
+}
+
+// Canonical fp32 norm and u = x / n (u = 0 when n == 0).
+__device__ __forceinline__ float norm_normalize(float (&x)[4]) {
+  float p = __fadd_rn(__fadd_rn(__fmul_rn(x[0], x[0]), __fmul_rn(x[1], x[1])),
+                      __fadd_rn(__fmul_rn(x[2], x[2]), __fmul_rn(x[3], x[3])));
+#pragma unroll
+  for (int h = 16; h >= 1; h >>= 1) p = __fadd_rn(p, __shfl_xor_sync(FULL_MASK, p, h));
+  const float n = __fsqrt_rn(p);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) x[e] = (n == 0.0f) ? 0.0f : __fdiv_rn(x[e], n);
+  return n;
+}
+
+// Randomized Hadamard in the canonical fp32 order; lane holds elements 4l..4l+3.
+__device__ __forceinline__ void wht_rotate(float (&v)[4], const uint32_t (&neg)[4], int lane) {
+  const uint32_t nb = (neg[lane >> 3] >> ((lane & 7) * 4)) & 0xFu;
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    if (nb & (1u << e)) v[e] = -v[e];
+  float a0 = __fadd_rn(v[0], v[1]), a1 = __fsub_rn(v[0], v[1]);
+  float a2 = __fadd_rn(v[2], v[3]), a3 = __fsub_rn(v[2], v[3]);
+  v[0] = __fadd_rn(a0, a2), v[2] = __fsub_rn(a0, a2);
+  v[1] = __fadd_rn(a1, a3), v[3] = __fsub_rn(a1, a3);
+#pragma unroll
+  for (int m = 1; m <= 16; m <<= 1) {
+    const bool high = (lane & m) != 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float o = __shfl_xor_sync(FULL_MASK, v[e], m);
+      v[e] = high ? __fsub_rn(o, v[e]) : __fadd_rn(v[e], o);
+    }
+  }
+  const float inv_sqrt_d = __int_as_float(0x3DB504F3);  // fp32 nearest 1/sqrt(128)
+#pragma unroll
+  for (int e = 0; e < 4; ++e) v[e] = __fmul_rn(v[e], inv_sqrt_d);
+}
+
+// Number of boundaries strictly below y (binary search over NB sorted boundaries).
+template <int NB>
+__device__ __forceinline__ uint32_t bucket(float y, const float *sb) {
+  uint32_t pos = 0;
+#pragma unroll
+  for (int step = (NB + 1) / 2; step >= 1; step >>= 1)
+    if (y > sb[pos + step - 1]) pos += step;
+  return pos;
+}
+
+// Pack one turbo4 / turbo3 row from per-lane indices (elements 4l..4l+3) and store
+// it at dst + slot * row_bytes through the warp's staging buffer.
+template <int FMT>
+__device__ __forceinline__ void pack_store_turbo(const uint32_t (&idx)[4], float n, uint8_t *buf,
+                                                 uint8_t *dst_row, int lane) {
+  if (FMT == TQ_FMT_TURBO4) {
+    if (lane == 0) *reinterpret_cast<float *>(buf) = n;
+    buf[4 + 2 * lane] = (uint8_t)(idx[0] | (idx[1] << 4));
+    buf[5 + 2 * lane] = (uint8_t)(idx[2] | (idx[3] << 4));
+    __syncwarp();
+    if (lane < 17)
+      reinterpret_cast<uint32_t *>(dst_row)[lane] = reinterpret_cast<const uint32_t *>(buf)[lane];
+  } else {  // turbo3: four 14-byte blocks {fp16 norm, qs[8], signs[4]}
+    const int c = lane >> 3, q = lane & 7;
+    uint8_t *blk = buf + 14 * c;
+    if (q == 0) {
+      const __half hn = __float2half_rn(n);
+      const uint16_t bits = *reinterpret_cast<const uint16_t *>(&hn);
+      blk[0] = (uint8_t)(bits & 0xFF);
+      blk[1] = (uint8_t)(bits >> 8);
+    }
+    blk[2 + q] = (uint8_t)((idx[0] & 3) | ((idx[1] & 3) << 2) | ((idx[2] & 3) << 4) |
+                           ((idx[3] & 3) << 6));
+    const uint32_t nib = (idx[0] >> 2) | ((idx[1] >> 2) << 1) | ((idx[2] >> 2) << 2) |
+                         ((idx[3] >> 2) << 3);
+    const uint32_t other = __shfl_xor_sync(FULL_MASK, nib, 1);
+    if ((q & 1) == 0) blk[10 + (q >> 1)] = (uint8_t)(nib | (other << 4));
+    __syncwarp();
+    if (lane < 14)
+      reinterpret_cast<uint32_t *>(dst_row)[lane] = reinterpret_cast<const uint32_t *>(buf)[lane];
+  }
+  __syncwarp();
+}
+
+__device__ __forceinline__ bool slot_of(const WriteParams &p, int64_t row, int lane,
+                                        int64_t *slot) {
+  const int64_t s = p.row_ids ? p.row_ids[row] : row;
+  if (s < 0 || s >= p.dst_rows) {
+    if (lane == 0) atomicExch(p.status, (int32_t)DEVERR_ROW_OOB);
+    return false;
+  }
+  *slot = s;
+  return true;
+}
+
+// ------------------------------------------------------------------ WHT turbo4/turbo3
+template <int FMT, int SRC>
+__global__ void __launch_bounds__(WARPS * 32) k_write_wht(const WriteParams p) {
+  constexpr int NB = (FMT == TQ_FMT_TURBO4) ? 15 : 7;
+  constexpr int RB = (FMT == TQ_FMT_TURBO4) ? 68 : 56;
+  __shared__ float sb[16];
+  __shared__ __align__(16) uint8_t rowbuf[WARPS][ROWBUF];
+  if (threadIdx.x < NB) sb[threadIdx.x] = p.b[threadIdx.x];
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int64_t row = (int64_t)blockIdx.x * WARPS + warp; row < p.n_rows;
+       row += (int64_t)gridDim.x * WARPS) {
+    int64_t slot;
+    if (!slot_of(p, row, lane, &slot)) continue;
+    float v[4];
+    load4<SRC>(p.src, row, p.stride, lane, v);
+    const float n = norm_normalize(v);
+    wht_rotate(v, p.wht_neg, lane);
+    uint32_t idx[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) idx[e] = bucket<NB>(v[e], sb);
+    pack_store_turbo<FMT>(idx, n, rowbuf[warp], p.dst + slot * RB, lane);
+  }
+}
+
+// ------------------------------------------------- dense rotation (CUDA-core matvec)
+// Pi (and S) staged in shared memory with a padded row stride of 129 floats so
+// that lane l working on row l + 32m and lane l reading column l + 32m are both
+// bank-conflict free.
+constexpr int PSTR = 129;
+
+template <int FMT, int SRC>
+__global__ void __launch_bounds__(WARPS * 32) k_write_dense(const WriteParams p) {
+  extern __shared__ __align__(16) float dsm[];
+  float *P = dsm;                                                    // [128][129]
+  float *S = P + D * PSTR;                                           // prod3 only
+  float *vec = S + (FMT == TQ_FMT_PROD3 ? D * PSTR : 0);             // [WARPS][3][128]
+  uint8_t *ib = reinterpret_cast<uint8_t *>(vec + WARPS * 3 * D);    // [WARPS][128] indices
+  uint8_t *rowbuf = ib + WARPS * D;                                  // [WARPS][ROWBUF]
+  float *sb = reinterpret_cast<float *>(rowbuf + WARPS * ROWBUF);    // [16]
+  for (int i = threadIdx.x; i < D * D; i += blockDim.x) {
+    P[(i >> 7) * PSTR + (i & 127)] = p.pi[i];
+    if (FMT == TQ_FMT_PROD3) S[(i >> 7) * PSTR + (i & 127)] = p.S[i];
+  }
+  if (threadIdx.x < 15) sb[threadIdx.x] = p.b[threadIdx.x];
+  __syncthreads();
+  constexpr int NB = (FMT == TQ_FMT_TURBO4) ? 15 : (FMT == TQ_FMT_TURBO3 ? 7 : 3);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float *u = vec + warp * 3 * D;
+  float *yh = u + D;
+  float *rr = yh + D;
+  uint8_t *myib = ib + warp * D;
+  uint8_t *buf = rowbuf + warp * ROWBUF;
+  for (int64_t row = (int64_t)blockIdx.x * WARPS + warp; row < p.n_rows;
+       row += (int64_t)gridDim.x * WARPS) {
+    int64_t slot;
+    if (!slot_of(p, row, lane, &slot)) continue;
+    float x[4];
+    load4<SRC>(p.src, row, p.stride, lane, x);
+    const float n = norm_normalize(x);
+    *reinterpret_cast<float4 *>(u + 4 * lane) = make_float4(x[0], x[1], x[2], x[3]);
+    __syncwarp();
+    float y[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int k = 0; k < D; k += 4) {
+      const float4 uk = *reinterpret_cast<const float4 *>(u + k);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const float *Pr = P + (lane + 32 * m) * PSTR + k;
+        y[m] = fmaf(Pr[0], uk.x, y[m]);
+        y[m] = fmaf(Pr[1], uk.y, y[m]);
+        y[m] = fmaf(Pr[2], uk.z, y[m]);
+        y[m] = fmaf(Pr[3], uk.w, y[m]);
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < 4; ++m) myib[lane + 32 * m] = (uint8_t)bucket<NB>(y[m], sb);
+    __syncwarp();
+    uint32_t idx[4];
+    const uint32_t w4 = *reinterpret_cast<const uint32_t *>(myib + 4 * lane);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) idx[e] = (w4 >> (8 * e)) & 0xFF;
+    if (FMT != TQ_FMT_PROD3) {
+      pack_store_turbo<FMT>(idx, n, buf, p.dst + slot * (FMT == TQ_FMT_TURBO4 ? 68 : 56), lane);
+      continue;
+    }
+    // prod3: residual in the unrotated normalised space, its norm, and QJL signs.
+#pragma unroll
+    for (int m = 0; m < 4; ++m) yh[lane + 32 * m] = p.c[myib[lane + 32 * m]];
+    __syncwarp();
+    float r[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int k = 0; k < D; ++k) {
+      const float yk = yh[k];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) r[m] = fmaf(P[k * PSTR + lane + 32 * m], yk, r[m]);
+    }
+    float g2 = 0.f;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      r[m] = u[lane + 32 * m] - r[m];
+      rr[lane + 32 * m] = r[m];
+      g2 = fmaf(r[m], r[m], g2);
+    }
+#pragma unroll
+    for (int h = 16; h >= 1; h >>= 1) g2 += __shfl_xor_sync(FULL_MASK, g2, h);
+    __syncwarp();
+    float z[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int k = 0; k < D; ++k) {
+      const float rk = rr[k];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) z[m] = fmaf(S[(lane + 32 * m) * PSTR + k], rk, z[m]);
+    }
+    uint32_t sbits[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) sbits[m] = __ballot_sync(FULL_MASK, z[m] >= 0.0f);
+    if (lane == 0) {
+      reinterpret_cast<float *>(buf)[0] = n;
+      reinterpret_cast<float *>(buf)[1] = sqrtf(g2);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) reinterpret_cast<uint32_t *>(buf)[10 + m] = sbits[m];
+    }
+    buf[8 + lane] = (uint8_t)((idx[0] & 3) | ((idx[1] & 3) << 2) | ((idx[2] & 3) << 4) |
+                              ((idx[3] & 3) << 6));
+    __syncwarp();
+    if (lane < 14)
+      reinterpret_cast<uint32_t *>(p.dst + slot * 56)[lane] =
+          reinterpret_cast<const uint32_t *>(buf)[lane];
+    __syncwarp();
+  }
+}
+
+// ------------------------------------------------------------------ V group quant
+template <int SRC>
+__global__ void __launch_bounds__(WARPS * 32) k_write_vgroup(const WriteParams p) {
+  __shared__ __align__(16) uint8_t rowbuf[WARPS][ROWBUF];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t *buf = rowbuf[warp];
+  for (int64_t row = (int64_t)blockIdx.x * WARPS + warp; row < p.n_rows;
+       row += (int64_t)gridDim.x * WARPS) {
+    int64_t slot;
+    if (!slot_of(p, row, lane, &slot)) continue;
+    float x[4];
+    load4<SRC>(p.src, row, p.stride, lane, x);
+    float mn = fminf(fminf(x[0], x[1]), fminf(x[2], x[3]));
+    float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+#pragma unroll
+    for (int h = 1; h <= 4; h <<= 1) {  // lanes 8g..8g+7 hold group g
+      mn = fminf(mn, __shfl_xor_sync(FULL_MASK, mn, h));
+      mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, h));
+    }
+    mn = __fadd_rn(mn, 0.0f);
+    mx = __fadd_rn(mx, 0.0f);
+    const float s32 = __fdiv_rn(__fsub_rn(mx, mn), 3.0f);
+    const __half sh = __float2half_rn(s32);
+    const __half zh = __float2half_rn(mn);
+    const float s = __half2float(sh), z = __half2float(zh);
+    uint32_t byte = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float c = 0.0f;
+      if (s > 0.0f) c = fminf(fmaxf(rintf(__fdiv_rn(__fsub_rn(x[e], z), s)), 0.0f), 3.0f);
+      byte |= ((uint32_t)c) << (2 * e);
+    }
+    buf[lane] = (uint8_t)byte;
+    if ((lane & 7) == 0) {
+      const int g = lane >> 3;
+      *reinterpret_cast<__half *>(buf + 32 + 4 * g) = sh;
+      *reinterpret_cast<__half *>(buf + 34 + 4 * g) = zh;
+    }
+    __syncwarp();
+    if (lane < 12)
+      reinterpret_cast<uint32_t *>(p.dst + slot * 48)[lane] =
+          reinterpret_cast<const uint32_t *>(buf)[lane];
+    __syncwarp();
+  }
+}
+
+template <typename K>
+cudaError_t launch_rows(K kernel, const WriteParams &p, int64_t n_rows, int num_sms, size_t smem,
+                        int blocks_per_sm, cudaStream_t st) {
+  int64_t want = (n_rows + WARPS - 1) / WARPS;
+  int64_t cap = (int64_t)num_sms * blocks_per_sm;
+  const int grid = (int)(want < cap ? want : cap);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  kernel<<<grid, WARPS * 32, smem, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_write(const tq_ctx *ctx, const WriteLaunch &w, cudaStream_t st) {
+  WriteParams p{};
+  p.src = w.src;
+  p.n_rows = w.n_rows;
+  p.stride = w.stride;
+  p.row_ids = w.row_ids;
+  p.dst = w.dst;
+  p.dst_rows = w.dst_rows;
+  p.status = ctx->d_status;
+  for (int k = 0; k < ctx->cb.K; ++k) p.c[k] = ctx->cb.c[k];
+  for (int k = 0; k + 1 < ctx->cb.K; ++k) p.b[k] = ctx->cb.b[k];
+  for (int i = 0; i < 4; ++i) p.wht_neg[i] = ctx->wht_neg[i];
+  p.pi = ctx->d_pi;
+  p.S = ctx->d_S;
+  const bool bf16 = (w.src_dtype == TQ_DTYPE_BF16);
+  const int fmt = ctx->fmt;
+  const int sms = ctx->num_sms;
+  if (fmt == TQ_FMT_VGROUP2)
+    return bf16 ? launch_rows(k_write_vgroup<TQ_DTYPE_BF16>, p, w.n_rows, sms, 0, 8, st)
+                : launch_rows(k_write_vgroup<TQ_DTYPE_F32>, p, w.n_rows, sms, 0, 8, st);
+  if (ctx->p.rotation == TQ_ROT_WHT && fmt != TQ_FMT_PROD3) {
+    if (fmt == TQ_FMT_TURBO4)
+      return bf16 ? launch_rows(k_write_wht<TQ_FMT_TURBO4, TQ_DTYPE_BF16>, p, w.n_rows, sms, 0, 8, st)
+                  : launch_rows(k_write_wht<TQ_FMT_TURBO4, TQ_DTYPE_F32>, p, w.n_rows, sms, 0, 8, st);
+    return bf16 ? launch_rows(k_write_wht<TQ_FMT_TURBO3, TQ_DTYPE_BF16>, p, w.n_rows, sms, 0, 8, st)
+                : launch_rows(k_write_wht<TQ_FMT_TURBO3, TQ_DTYPE_F32>, p, w.n_rows, sms, 0, 8, st);
+  }
+  // Dense rotation (prod3 always takes this path; its WHT variant multiplies by the
+  // materialised WHT matrix, which the context stores in d_pi as well).
+  const size_t mats = (fmt == TQ_FMT_PROD3 ? 2 : 1) * (size_t)D * PSTR * sizeof(float);
+  const size_t smem = mats + WARPS * 3 * D * sizeof(float) + WARPS * D + WARPS * ROWBUF +
+                      16 * sizeof(float);
+  const int per_sm = fmt == TQ_FMT_PROD3 ? 1 : 2;
+  switch (fmt) {
+    case TQ_FMT_TURBO4:
+      return bf16 ? launch_rows(k_write_dense<TQ_FMT_TURBO4, TQ_DTYPE_BF16>, p, w.n_rows, sms, smem, per_sm, st)
+                  : launch_rows(k_write_dense<TQ_FMT_TURBO4, TQ_DTYPE_F32>, p, w.n_rows, sms, smem, per_sm, st);
+    case TQ_FMT_TURBO3:
+      return bf16 ? launch_rows(k_write_dense<TQ_FMT_TURBO3, TQ_DTYPE_BF16>, p, w.n_rows, sms, smem, per_sm, st)
+                  : launch_rows(k_write_dense<TQ_FMT_TURBO3, TQ_DTYPE_F32>, p, w.n_rows, sms, smem, per_sm, st);
+    default:
+      return bf16 ? launch_rows(k_write_dense<TQ_FMT_PROD3, TQ_DTYPE_BF16>, p, w.n_rows, sms, smem, per_sm, st)
+                  : launch_rows(k_write_dense<TQ_FMT_PROD3, TQ_DTYPE_F32>, p, w.n_rows, sms, smem, per_sm, st);
+  }
+}
+
+}  // namespace tq

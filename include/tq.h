@@ -1,0 +1,229 @@
+/*
+ * tq.h -- C ABI of the GB300 compressed-KV library (TurboQuant-style KV-cache
+ * compression: write path = quantize / SET_ROWS, read path = fused decode
+ * attention over the packed cache).
+ *
+ * Sources for the operations (page title, section):
+ *   [turbo4 post-mortem]  "turboquant_plus: how the turbo4 KV format came back",
+ *                         sections 1 (encode chain: norm -> normalise -> random
+ *                         rotation -> nearest centroid), 2 (SET_ROWS bugs),
+ *                         4 (dequant by direct extraction), 5 (16-centroid
+ *                         turbo4, nibble packing), 7 (68-byte block), 9, 10.
+ *   [Triton deep dive]    "TurboQuant fused Triton kernels deep dive", tricks
+ *                         1-3 (rotate q once, QJL query sketch once, single-pass
+ *                         online softmax with in-register value dequant) and
+ *                         "write path and codebook" (Lloyd-Max codebook, 2-bit
+ *                         group value quantization).
+ *
+ * Conventions common to every call
+ *   - Head dimension d = 128 only; any other d returns TQ_ERR_UNSUPPORTED.
+ *   - All functions return a tq_status; no exception crosses the ABI.
+ *     tq_last_error() gives a one-line description of the last failure on the
+ *     calling thread.
+ *   - Device calls are asynchronous on the given stream (a cudaStream_t; NULL
+ *     is the legacy default stream).  Arguments are validated on the host
+ *     before any launch.  Launch failures map to TQ_ERR_CUDA.  Conditions only
+ *     the device can see (a row id out of range, a sequence length outside
+ *     [1, L], a bounded wait that ran out) are recorded in the context's
+ *     device status word, read with tq_ctx_device_status().
+ *   - The caller owns every device buffer (sources, caches, q, outputs,
+ *     workspace).  The library owns only tq_ctx, which is immutable after
+ *     creation and may be shared across streams.
+ *   - Cache layout: rows of one packed record each, row r at byte r * row_bytes.
+ *     For decode the cache is [B][Hkv][L] rows.  Cache base pointers must be
+ *     16-byte aligned and the cache must be readable up to the next 16-byte
+ *     boundary past its last row (tq_cache_bytes() returns that size).
+ */
+#ifndef TQ_H_
+#define TQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TQ_HEAD_DIM 128
+
+typedef struct CUstream_st *tq_stream_t; /* identical to cudaStream_t */
+typedef struct tq_ctx tq_ctx;
+
+typedef enum tq_status {
+  TQ_OK = 0,
+  TQ_ERR_INVALID_ARG = 1,  /* null pointer, bad size, bad enum, L == 0, ... */
+  TQ_ERR_UNSUPPORTED = 2,  /* d != 128, format pair without a decode kernel, ... */
+  TQ_ERR_ALIGNMENT = 3,    /* a pointer or stride breaks the stated alignment */
+  TQ_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+  TQ_ERR_ALLOC = 5,        /* device or host allocation failed */
+  TQ_ERR_WORKSPACE = 6     /* workspace smaller than tq_decode_workspace_size() */
+} tq_status;
+
+/* Packed formats ([turbo4 post-mortem] sections 1, 4, 5, 7; [Triton deep dive] tricks 2-3).
+ *   TURBO4  68 B/row: fp32 norm, qs[64]; 4-bit index j in bits 4*(j%2) of qs[j/2].
+ *   TURBO3  56 B/row: four 14-B blocks {fp16 norm, qs[8], signs[4]}; index j of a
+ *           block: low 2 bits at bits 2*(j%4) of qs[j/4], high bit at bit j%8 of
+ *           signs[j/8]; each block carries the fp16 norm of the whole row.
+ *   PROD3   56 B/row (keys): fp32 norm, fp32 residual norm, qs[32] 2-bit MSE
+ *           indices (bits 2*(j%4) of byte j/4), signs[16] QJL bits (bit i%8 of
+ *           byte i/8, 1 = +1).
+ *   VGROUP2 48 B/row (values): q[32] 2-bit codes (bits 2*(j%4) of byte j/4),
+ *           then 4 x {fp16 scale, fp16 zero} for groups of 32; value = code*scale+zero.
+ * Every header is little-endian and comes first. */
+typedef enum tq_format {
+  TQ_FMT_TURBO4 = 0,
+  TQ_FMT_TURBO3 = 1,
+  TQ_FMT_PROD3 = 2,
+  TQ_FMT_VGROUP2 = 3
+} tq_format;
+
+/* Codebook construction for the rotated-coordinate law N(0, 1/d).
+ *   QUANTILE: conditional means of 2^bits equal-probability cells (reproduces the
+ *             printed 16-entry d=128 table, [turbo4 post-mortem] section 5).
+ *   LLOYD:    converged Lloyd-Max from the QUANTILE start ([turbo4 post-mortem]
+ *             sections 5, 9; [Triton deep dive] "write path and codebook").
+ *   DEFAULT:  QUANTILE for TURBO4, LLOYD for TURBO3 and PROD3. */
+typedef enum tq_codebook_kind {
+  TQ_CB_DEFAULT = 0,
+  TQ_CB_QUANTILE = 1,
+  TQ_CB_LLOYD = 2
+} tq_codebook_kind;
+
+/* Rotation y = R u applied before quantization.
+ *   WHT:   R = (1/sqrt(d)) H D, D a seeded +-1 diagonal, H Sylvester Hadamard
+ *          ([turbo4 post-mortem] sections 1, 10).
+ *   DENSE: R = Pi, the Q factor (diag(R) > 0) of a seeded Gaussian d x d matrix
+ *          ([Triton deep dive] trick 1), stored in fp32.
+ * Randomness: splitmix64 outputs of the seed; WHT sign j = -1 when the top bit of
+ * output j is set; Gaussians by Box-Muller on output pairs (row-major). */
+typedef enum tq_rotation_kind {
+  TQ_ROT_WHT = 0,
+  TQ_ROT_DENSE = 1
+} tq_rotation_kind;
+
+typedef enum tq_dtype {
+  TQ_DTYPE_F32 = 0,
+  TQ_DTYPE_BF16 = 1,
+  TQ_DTYPE_F16 = 2
+} tq_dtype;
+
+typedef struct tq_params {
+  int32_t d;          /* must be 128 */
+  int32_t format;     /* tq_format */
+  int32_t codebook;   /* tq_codebook_kind (ignored for VGROUP2) */
+  int32_t rotation;   /* tq_rotation_kind (ignored for VGROUP2, which is not rotated) */
+  uint64_t rot_seed;  /* seed of the rotation */
+  uint64_t qjl_seed;  /* seed of the QJL matrix S (PROD3 only; must differ from rot_seed,
+                         [turbo4 post-mortem] section 10) */
+} tq_params;
+
+/* ---------------------------------------------------------------- host only */
+
+/* Codebook of 2^bits centroids and 2^bits - 1 decision boundaries for N(0, 1/d),
+ * built in fp64 and rounded to fp32; boundaries are the fp32 rounding of the
+ * midpoints of adjacent stored centroids.  bits in 1..4, d == 128, kind QUANTILE
+ * or LLOYD.  centroids: host array of 2^bits floats; boundaries: host array of
+ * 2^bits - 1 floats (may be NULL).  Caller-owned.  No device work. */
+tq_status tq_make_codebook(int bits, int d, int kind, float *centroids, float *boundaries);
+
+/* The seeded rotation as host data.  DENSE: out is d*d floats, row-major Pi
+ * (y = Pi u).  WHT: out is d floats, the diagonal D (+1/-1).  No device work. */
+tq_status tq_make_rotation(int kind, int d, uint64_t seed, float *out);
+
+/* The QJL matrix S (d*d floats, row-major, i.i.d. N(0,1) from `seed`).  No device work. */
+tq_status tq_make_qjl_matrix(int d, uint64_t seed, float *out);
+
+/* Bytes of one packed row of `format` (68, 56, 56, 48); -1 for a bad format. */
+int64_t tq_row_bytes(int format);
+
+/* Bytes a cache of n_rows rows must provide: n_rows * row_bytes rounded up to 16. */
+size_t tq_cache_bytes(int format, int64_t n_rows);
+
+const char *tq_status_string(tq_status s);
+const char *tq_last_error(void);
+
+/* ------------------------------------------------------------- context / device */
+
+/* Builds codebook, rotation and (PROD3) QJL matrix on the current CUDA device.
+ * *out receives a context owned by the library; free it with tq_ctx_destroy(). */
+tq_status tq_ctx_create(const tq_params *params, tq_ctx **out);
+tq_status tq_ctx_destroy(tq_ctx *ctx);
+
+/* Reads (synchronising the device) and optionally clears the context's device
+ * status word: 0 = no device-side error; 1 = row id out of range (write skipped);
+ * 2 = sequence length outside [1, L] (clamped); 3 = a bounded wait ran out. */
+tq_status tq_ctx_device_status(const tq_ctx *ctx, int32_t *status, int clear);
+
+/* Write path / SET_ROWS ([turbo4 post-mortem] sections 1, 2): quantize n_rows
+ * source rows of 128 elements and store packed row i at cache slot row_ids[i].
+ *   src            device, n_rows rows of src_dtype (F32 or BF16), row i at
+ *                  src + i * src_row_stride elements.  BF16 rows must be 8-byte
+ *                  aligned, F32 rows 16-byte aligned.
+ *   row_ids        device int64[n_rows] cache slots, or NULL for slot i.
+ *   dst_cache      device, dst_rows packed rows of ctx's format (16-byte aligned).
+ * Rows whose slot is outside [0, dst_rows) are skipped and flagged (status 1).
+ * n_rows == 0 is a no-op.  Rows of the same slot written twice race. */
+tq_status tq_quantize_set_rows(const tq_ctx *ctx, const void *src, int src_dtype,
+                               int64_t n_rows, int64_t src_row_stride,
+                               const int64_t *row_ids, void *dst_cache, int64_t dst_rows,
+                               tq_stream_t stream);
+
+/* Dequantize ([turbo4 post-mortem] section 4; [Triton deep dive] "hybrid" path):
+ * dst[i] = reconstruction of packed row i, fp32 [n_rows][128] (device).  With
+ * unrotate != 0 the rotated formats are mapped back by R^T; with 0 they return
+ * the rotated-basis values norm * c[idx] (PROD3 and VGROUP2 always reconstruct
+ * the original space). */
+tq_status tq_dequantize(const tq_ctx *ctx, const void *cache, int64_t n_rows, int unrotate,
+                        float *dst, tq_stream_t stream);
+
+/* Decode attention ([Triton deep dive] tricks 1-3): for batch b and q-head h,
+ * with KV head kv = floor(h * Hkv / Hq),
+ *   out[b,h] = sum_t softmax_t(scale * <q[b,h], K_hat[b,kv,t]>) V_hat[b,kv,t],
+ * t < seq_lens[b], computed from the packed caches without materialising K/V:
+ * q is rotated (and, for PROD3 keys, sketched with S) once, every key is scored
+ * from its indices, online softmax runs split-K across SMs, values are
+ * dequantized in registers, and the output is un-rotated once per head.
+ *   k_ctx / v_ctx  contexts of the key and value caches.  Supported pairs:
+ *                  (TURBO4, TURBO4) and (PROD3, VGROUP2).
+ *   q              device [B][Hq][128] of q_dtype (F32, BF16 or F16), 16-byte aligned.
+ *   k_cache/v_cache device [B][Hkv][L] packed rows.
+ *   seq_lens       device int32[B] lengths in [1, L], or NULL for all L.
+ *   scale          softmax scale; 0 selects 1/sqrt(128).
+ *   out            device fp32 [B][Hq][128].
+ *   scores_dbg     NULL, or device fp32 [B][Hq][L]: the scaled scores (tests).
+ *   workspace      device scratch of at least tq_decode_workspace_size() bytes,
+ *                  256-byte aligned; its contents need no initialisation.
+ * Hq must be a multiple of Hkv.  L >= 1, B >= 1. */
+tq_status tq_decode_workspace_size(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, int Hq,
+                                   int Hkv, int L, size_t *bytes);
+tq_status tq_decode_attention(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *q,
+                              int q_dtype, const void *k_cache, const void *v_cache,
+                              const int32_t *seq_lens, int B, int Hq, int Hkv, int L,
+                              float scale, float *out, float *scores_dbg, void *workspace,
+                              size_t workspace_bytes, tq_stream_t stream);
+
+/* The three stages of tq_decode_attention, for callers that time or overlap them;
+ * same arguments and workspace, run in this order on one stream:
+ *   prepare_q: q_rot = R q (and S q), pre-scaled and split for the tensor cores;
+ *   partial:   split-K scan of the packed caches -> per-split (max, sum, acc);
+ *   combine:   log-sum-exp merge of the splits, 1/sum, un-rotation, write out. */
+tq_status tq_decode_prepare_q(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *q,
+                              int q_dtype, int B, int Hq, int Hkv, int L, float scale,
+                              void *workspace, size_t workspace_bytes, tq_stream_t stream);
+tq_status tq_decode_partial(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *k_cache,
+                            const void *v_cache, const int32_t *seq_lens, int B, int Hq,
+                            int Hkv, int L, float *scores_dbg, void *workspace,
+                            size_t workspace_bytes, tq_stream_t stream);
+tq_status tq_decode_combine(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, int Hq, int Hkv,
+                            int L, float *out, void *workspace, size_t workspace_bytes,
+                            tq_stream_t stream);
+
+/* Number of key splits the decode uses for this shape on the current device. */
+tq_status tq_decode_num_splits(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, int Hq,
+                               int Hkv, int L, int *n_split);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TQ_H_ */

@@ -32,8 +32,8 @@ Readings taken where the pages are silent (all listed in the design doc):
   overflow to inf) in each of its four 32-element blocks.
 * prod3: residual r = u - Pi^T c[idx] in the unrotated normalised space
   (section 2 bug 6), gamma = ||r||, sign bit i = 1 when (S r)_i >= 0.
-* vgroup2 per group: mn, mx by IEEE min/max (NaN ignored), mn <- mn + 0 (folds
-  -0 to +0), scale = fp16(fp32((mx - mn) / 3)), zero = fp16(mn),
+* vgroup2 per group: mn, mx by IEEE min/max (NaN ignored), mn <- mn + 0 and
+  mx <- mx + 0 (fold -0 to +0, so min/max tie order cannot change a bit), scale = fp16(fp32((mx - mn) / 3)), zero = fp16(mn),
   code = clamp(rint((v - zero) / scale), 0, 3) with half-even rint, IEEE
   max/min clamping (NaN -> 0), and code 0 when scale is not > 0.  Values are
   not rotated.
@@ -288,6 +288,7 @@ def encode_vgroup(x, group=32):
     mn = np.fmin.reduce(xg, axis=2).astype(np.float32)
     mx = np.fmax.reduce(xg, axis=2).astype(np.float32)
     mn = (mn + np.float32(0.0)).astype(np.float32)
+    mx = (mx + np.float32(0.0)).astype(np.float32)
     rng = (mx - mn).astype(np.float32)
     s32 = (rng / np.float32(3.0)).astype(np.float32)
     with np.errstate(over="ignore"):

@@ -1,0 +1,92 @@
+"""CPU-only checks of the C-ABI library: it loads, exports every declared symbol, and its
+host-side constructions (codebooks, rotations, QJL matrix, sizes, argument validation)
+agree with the oracle.  No kernel is launched here."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def tq():
+    from compressed_attention_gb300 import _build
+    _build.build()
+    import compressed_attention_gb300 as m
+    return m
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "tq.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("tq_make_codebook", "tq_quantize_set_rows", "tq_decode_attention", "tq_dequantize"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(tq):
+    lib = ctypes.CDLL(tq.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert missing == []
+
+
+@pytest.mark.parametrize("bits,kind", [(1, "quantile"), (2, "lloyd"), (3, "lloyd"), (4, "quantile"), (4, "lloyd")])
+def test_host_codebook_matches_oracle(tq, bits, kind):
+    c, b = tq.tq_make_codebook(bits, 128, kind)
+    c32, b32 = oracle.stored_codebook(oracle.make_codebook(bits, 128, kind))
+    assert np.max(np.abs(c - c32)) <= 1e-7
+    assert np.max(np.abs(b - b32)) <= 1e-7 if bits > 1 else True
+
+
+@pytest.mark.parametrize("seed", [0, 2, 3, 12345])
+def test_host_dense_rotation_matches_oracle(tq, seed):
+    pi = tq.tq_make_rotation("dense", seed).astype(np.float64)
+    ref = oracle.dense_rotation(seed, 128)
+    assert np.max(np.abs(pi - ref)) <= 1e-6
+    assert np.max(np.abs(pi.T @ pi - np.eye(128))) <= 1e-6
+
+
+@pytest.mark.parametrize("seed", [0, 5, 2**64 - 1])
+def test_host_wht_signs_match_oracle(tq, seed):
+    assert np.array_equal(tq.tq_make_rotation("wht", seed), oracle.wht_signs(seed, 128).astype(np.float32))
+
+
+def test_host_qjl_matrix_matches_oracle(tq):
+    S = tq.tq_make_qjl_matrix(1003)
+    assert np.max(np.abs(S - oracle.qjl_matrix(1003, 128))) <= 1e-6
+
+
+def test_sizes(tq):
+    assert [tq.tq_row_bytes(f) for f in ("turbo4", "turbo3", "prod3", "vgroup2")] == [68, 56, 56, 48]
+    assert tq.tq_cache_bytes("turbo4", 3) == 208  # 204 rounded up to 16
+    assert tq.tq_cache_bytes("vgroup2", 1) == 48
+    assert tq.lib.tq_row_bytes(9) == -1
+
+
+def test_host_validation_errors(tq):
+    lib = tq.lib
+    c = np.zeros(16, np.float32)
+    assert lib.tq_make_codebook(4, 64, 1, c.ctypes.data, None) == tq.TQ_ERR_UNSUPPORTED
+    assert lib.tq_make_codebook(5, 128, 1, c.ctypes.data, None) == tq.TQ_ERR_UNSUPPORTED
+    assert lib.tq_make_codebook(4, 128, 7, c.ctypes.data, None) == tq.TQ_ERR_INVALID_ARG
+    assert lib.tq_make_codebook(4, 128, 1, None, None) == tq.TQ_ERR_INVALID_ARG
+    assert lib.tq_quantize_set_rows(None, None, 0, 1, 128, None, None, 1, None) == tq.TQ_ERR_INVALID_ARG
+    assert lib.tq_decode_attention(None, None, None, 0, None, None, None, 1, 1, 1, 1, 0.0, None, None,
+                                   None, 0, None) == tq.TQ_ERR_INVALID_ARG
+    p = tq.tq_params(64, 0, 0, 0, 0, 0)
+    h = ctypes.c_void_p()
+    assert lib.tq_ctx_create(ctypes.byref(p), ctypes.byref(h)) == tq.TQ_ERR_UNSUPPORTED
+    p = tq.tq_params(128, tq.TQ_FMT_PROD3, 0, tq.TQ_ROT_DENSE, 7, 7)
+    assert lib.tq_ctx_create(ctypes.byref(p), ctypes.byref(h)) == tq.TQ_ERR_INVALID_ARG
+    assert b"QJL seed" in lib.tq_last_error()
+    assert lib.tq_status_string(tq.TQ_ERR_WORKSPACE) == b"workspace too small"

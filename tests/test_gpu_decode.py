@@ -1,0 +1,224 @@
+"""GPU parity of the fused decode attention against the oracle.
+
+Small shapes (several tiles, several splits, ragged tails and ragged batches) use
+caches encoded by the oracle, so both sides attend over identical packed bytes and
+scores can be compared one by one (max abs 2e-3) as well as outputs (max abs 2e-3,
+per-head relative 1e-3).  The full-size workloads run in the launch configuration
+the benchmark times, with caches written by the GPU write path, and compare sampled
+heads against the oracle run on that head's own inputs."""
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_util import ATOL, check_outputs, lib, torch_rows
+from oracle.formats import Codec
+
+pytestmark = pytest.mark.gpu
+
+
+def oracle_cache(codec, B, Hkv, L, seed, scale=1.0, dist="normal"):
+    x = (np.random.default_rng(seed).standard_normal((B * Hkv * L, 128)) * scale).astype(np.float32)
+    if dist == "lognormal":
+        s = np.exp(np.random.default_rng(seed + 1).normal(0, 0.5, 128)).astype(np.float32)
+        s[7] *= 8
+        x = x * s
+    blk, _ = codec.encode(x)
+    return blk.reshape(B, Hkv, L, -1)
+
+
+def upload_cache(tq, fmt, blocks):
+    import torch
+    flat = blocks.reshape(-1)
+    t = tq.alloc_cache(fmt, blocks.shape[0] * blocks.shape[1] * blocks.shape[2])
+    t[: flat.size].copy_(torch.from_numpy(flat.copy()))
+    return t
+
+
+def run_decode(tq, kctx, vctx, q_t, kc, vc, B, Hq, Hkv, L, lens=None, scores=True, staged=False):
+    import torch
+    ws = tq.alloc_workspace(tq.tq_decode_workspace_size(kctx, vctx, B, Hq, Hkv, L))
+    out = torch.empty((B, Hq, 128), dtype=torch.float32, device="cuda")
+    sc = torch.full((B, Hq, L), float("nan"), dtype=torch.float32, device="cuda") if scores else None
+    sl = None if lens is None else torch.tensor(np.asarray(lens, np.int32), device="cuda")
+    if staged:
+        tq.tq_decode_prepare_q(kctx, vctx, q_t, ws, B, Hq, Hkv, L)
+        tq.tq_decode_partial(kctx, vctx, kc, vc, ws, B, Hq, Hkv, L, seq_lens=sl, scores=sc)
+        tq.tq_decode_combine(kctx, vctx, out, ws, B, Hq, Hkv, L)
+    else:
+        tq.tq_decode_attention(kctx, vctx, q_t, kc, vc, out, ws, B, Hq, Hkv, L, seq_lens=sl, scores=sc)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), (sc.cpu().numpy() if scores else None)
+
+
+def reference(q32, kcodec, kb, vcodec, vb, lens):
+    B, Hkv, L, _ = kb.shape
+    kh = kcodec.dequantize(kb.reshape(-1, kb.shape[-1])).reshape(B, Hkv, L, 128)
+    vh = vcodec.dequantize(vb.reshape(-1, vb.shape[-1])).reshape(B, Hkv, L, 128)
+    return oracle.attention_reference(q32, kh, vh, lens)
+
+
+CASES = [
+    # B, Hq, Hkv, L, lens
+    (2, 8, 2, 300, [137, 300]),       # GQA 4, ragged batch, ragged tail, 2 splits
+    (1, 1, 1, 512, None),             # single head
+    (3, 6, 1, 1000, [1, 999, 1000]),  # GQA 6, a length-1 sequence
+    (1, 12, 1, 700, None),            # 12 q-heads per KV head: two head groups
+    (2, 8, 8, 129, [64, 129]),        # no grouping
+]
+
+
+@pytest.mark.parametrize("rot", ["wht", "dense"])
+@pytest.mark.parametrize("case", CASES)
+def test_decode_turbo4_parity(rot, case):
+    tq = lib()
+    B, Hq, Hkv, L, lens = case
+    kcodec = Codec("turbo4", rotation=rot, rot_seed=3)
+    vcodec = Codec("turbo4", rotation=rot, rot_seed=4)
+    kb = oracle_cache(kcodec, B, Hkv, L, 1, scale=2.0, dist="lognormal")
+    vb = oracle_cache(vcodec, B, Hkv, L, 2)
+    q_t, q32 = torch_rows(np.random.default_rng(3).standard_normal((B, Hq, 128)).astype(np.float32), "bf16")
+    kctx, vctx = tq.Ctx("turbo4", rot, 3), tq.Ctx("turbo4", rot, 4)
+    out, sc = run_decode(tq, kctx, vctx, q_t, upload_cache(tq, "turbo4", kb), upload_cache(tq, "turbo4", vb),
+                         B, Hq, Hkv, L, lens)
+    ref, s_ref = reference(q32, kcodec, kb, vcodec, vb, lens)
+    check_outputs(out, ref)
+    m = ~np.isnan(s_ref)
+    assert np.array_equal(m, ~np.isnan(sc)), "scores written for the wrong keys"
+    assert np.max(np.abs(sc[m] - s_ref[m])) <= ATOL
+    assert tq.tq_ctx_device_status(kctx) == 0
+
+
+@pytest.mark.parametrize("q_dtype", ["f32", "bf16", "f16"])
+def test_decode_q_dtypes_and_staged_calls(q_dtype):
+    tq = lib()
+    B, Hq, Hkv, L = 2, 4, 1, 257
+    codec = Codec("turbo4", rotation="wht", rot_seed=0)
+    kb, vb = oracle_cache(codec, B, Hkv, L, 5), oracle_cache(codec, B, Hkv, L, 6)
+    q_t, q32 = torch_rows(np.random.default_rng(4).standard_normal((B, Hq, 128)).astype(np.float32), q_dtype)
+    ctx = tq.Ctx("turbo4", "wht", 0)
+    kc, vc = upload_cache(tq, "turbo4", kb), upload_cache(tq, "turbo4", vb)
+    out1, _ = run_decode(tq, ctx, ctx, q_t, kc, vc, B, Hq, Hkv, L, scores=False)
+    out2, _ = run_decode(tq, ctx, ctx, q_t, kc, vc, B, Hq, Hkv, L, scores=False, staged=True)
+    ref, _ = reference(q32, codec, kb, codec, vb, None)
+    check_outputs(out1, ref)
+    assert np.array_equal(out1, out2)
+
+
+def test_decode_scale_argument_and_peaked_attention():
+    """A large explicit scale makes the softmax peaked; results still match."""
+    tq = lib()
+    B, Hq, Hkv, L = 1, 4, 1, 400
+    codec = Codec("turbo4", rotation="dense", rot_seed=1)
+    kb, vb = oracle_cache(codec, B, Hkv, L, 7, scale=3.0), oracle_cache(codec, B, Hkv, L, 8)
+    q_t, q32 = torch_rows(np.random.default_rng(5).standard_normal((B, Hq, 128)).astype(np.float32), "f32")
+    ctx = tq.Ctx("turbo4", "dense", 1)
+    import torch
+    ws = tq.alloc_workspace(tq.tq_decode_workspace_size(ctx, ctx, B, Hq, Hkv, L))
+    out = torch.empty((B, Hq, 128), dtype=torch.float32, device="cuda")
+    scale = 0.5
+    tq.tq_decode_attention(ctx, ctx, q_t, upload_cache(tq, "turbo4", kb), upload_cache(tq, "turbo4", vb), out, ws,
+                           B, Hq, Hkv, L, scale=scale)
+    kh = codec.dequantize(kb.reshape(-1, 68)).reshape(B, Hkv, L, 128)
+    vh = codec.dequantize(vb.reshape(-1, 68)).reshape(B, Hkv, L, 128)
+    ref, s = oracle.attention_reference(q32, kh, vh, scale=scale)
+    assert np.nanmax(s) - np.nanmin(s) > 20  # genuinely peaked
+    check_outputs(out.cpu().numpy(), ref)
+
+
+def test_decode_zero_query_and_zero_values():
+    """q = 0 gives uniform weights (mean of V_hat); all-zero value vectors give 0."""
+    tq = lib()
+    B, Hq, Hkv, L = 1, 2, 1, 200
+    codec = Codec("turbo4", rotation="wht", rot_seed=2)
+    kb = oracle_cache(codec, B, Hkv, L, 9)
+    vb = oracle_cache(codec, B, Hkv, L, 10)
+    vb_zero, _ = codec.encode(np.zeros((L, 128), np.float32))
+    vb[0, 0, 100:] = vb_zero[100:]
+    q = np.zeros((B, Hq, 128), np.float32)
+    q[0, 1] = np.random.default_rng(1).standard_normal(128)
+    q_t, q32 = torch_rows(q, "f32")
+    ctx = tq.Ctx("turbo4", "wht", 2)
+    out, _ = run_decode(tq, ctx, ctx, q_t, upload_cache(tq, "turbo4", kb), upload_cache(tq, "turbo4", vb),
+                        B, Hq, Hkv, L, scores=False)
+    ref, _ = reference(q32, codec, kb, codec, vb, None)
+    check_outputs(out, ref)
+    vh = codec.dequantize(vb.reshape(-1, 68))
+    assert np.allclose(out[0, 0], vh.mean(0), atol=1e-5)
+
+
+def test_decode_bad_seq_len_is_clamped_and_flagged():
+    tq = lib()
+    B, Hq, Hkv, L = 2, 2, 1, 100
+    codec = Codec("turbo4", rotation="wht", rot_seed=0)
+    kb, vb = oracle_cache(codec, B, Hkv, L, 11), oracle_cache(codec, B, Hkv, L, 12)
+    q_t, q32 = torch_rows(np.random.default_rng(6).standard_normal((B, Hq, 128)).astype(np.float32), "f32")
+    ctx = tq.Ctx("turbo4", "wht", 0)
+    out, _ = run_decode(tq, ctx, ctx, q_t, upload_cache(tq, "turbo4", kb), upload_cache(tq, "turbo4", vb),
+                        B, Hq, Hkv, L, lens=[500, 0], scores=False)
+    assert tq.tq_ctx_device_status(ctx) == 2
+    ref, _ = reference(q32, codec, kb, codec, vb, [100, 1])
+    check_outputs(out, ref)
+
+
+def test_decode_rejects_bad_arguments():
+    import torch
+    tq = lib()
+    ctx = tq.Ctx("turbo4", "wht", 0)
+    ws_small = tq.alloc_workspace(256)
+    q = torch.zeros((1, 4, 128), dtype=torch.float32, device="cuda")
+    cache = tq.alloc_cache("turbo4", 64)
+    out = torch.zeros((1, 4, 128), dtype=torch.float32, device="cuda")
+    with pytest.raises(tq.TQError) as e:
+        tq.tq_decode_attention(ctx, ctx, q, cache, cache, out, ws_small, 1, 4, 1, 64)
+    assert e.value.status == tq.TQ_ERR_WORKSPACE
+    with pytest.raises(tq.TQError) as e:
+        tq.tq_decode_workspace_size(ctx, ctx, 1, 5, 2, 64)  # Hq not a multiple of Hkv
+    assert e.value.status == tq.TQ_ERR_INVALID_ARG
+    t3 = tq.Ctx("turbo3", "wht", 0)
+    with pytest.raises(tq.TQError) as e:
+        tq.tq_decode_workspace_size(t3, t3, 1, 4, 1, 64)
+    assert e.value.status == tq.TQ_ERR_UNSUPPORTED
+
+
+def _full_size(name, rot, rot_seed, sample_heads):
+    """Write the whole cache with the GPU write path, decode in the benchmark's launch
+    configuration, and compare sampled (b, h) outputs with the oracle on that head's inputs."""
+    import torch
+    tq = lib()
+    cfg = synth.WORKLOADS[name]
+    B, Hq, Hkv, L = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["L"]
+    kctx, vctx = tq.Ctx("turbo4", rot, rot_seed), tq.Ctx("turbo4", rot, rot_seed + 100)
+    kc, vc = tq.alloc_cache("turbo4", B * Hkv * L), tq.alloc_cache("turbo4", B * Hkv * L)
+    for tensor, ctx, cache in (("K", kctx, kc), ("V", vctx, vc)):
+        for b in range(B):
+            for h in range(Hkv):
+                x32, bits = synth.kv_unit(cfg, tensor, b, h)
+                src = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+                rows = torch.arange((b * Hkv + h) * L, (b * Hkv + h + 1) * L, dtype=torch.int64, device="cuda")
+                tq.tq_quantize_set_rows(ctx, src, cache, row_ids=rows)
+    q32, qbits = synth.queries(cfg)
+    q_t = torch.from_numpy(qbits.view(np.int16)).view(torch.bfloat16).cuda()
+    out, _ = run_decode(tq, kctx, vctx, q_t, kc, vc, B, Hq, Hkv, L, scores=False)
+    assert tq.tq_ctx_device_status(kctx) == 0
+    kcod = Codec("turbo4", rotation=rot, rot_seed=rot_seed)
+    vcod = Codec("turbo4", rotation=rot, rot_seed=rot_seed + 100)
+    for (b, h) in sample_heads:
+        kv = oracle.gqa_kv_head(h, Hq, Hkv)
+        xk, _ = synth.kv_unit(cfg, "K", b, kv)
+        xv, _ = synth.kv_unit(cfg, "V", b, kv)
+        kh = kcod.dequantize(kcod.encode(xk)[0])[None, None]
+        vh = vcod.dequantize(vcod.encode(xv)[0])[None, None]
+        ref, _ = oracle.attention_reference(q32[b:b + 1, h:h + 1], kh, vh)
+        check_outputs(out[b:b + 1, h:h + 1], ref)
+
+
+def test_full_size_gqa_lognormal_dense():
+    _full_size("gqa_lognormal", "dense", 2, [(0, 0), (3, 13), (7, 31)])
+
+
+def test_full_size_long_context_wht():
+    _full_size("long_context", "wht", 5, [(0, 0), (0, 17), (0, 31)])

@@ -1,0 +1,183 @@
+"""GPU parity of the write path (quantize / SET_ROWS) against the oracle encoder.
+
+WHT rotation and value group quantization: packed rows bit-exact.  Dense rotation:
+norm bytes bit-exact; indices may differ only within 1e-5 of a decision boundary;
+prod3 residual norms within 1e-5 relative and QJL signs only where the oracle
+projection is within 1e-4 of zero (rows whose indices all match)."""
+
+import numpy as np
+import pytest
+
+import synth
+from gpu_util import band_ok, lib, to_host_bytes, torch_rows
+from oracle.formats import Codec, unpack_prod, unpack_turbo3, unpack_turbo4
+
+pytestmark = pytest.mark.gpu
+
+
+def special_rows():
+    x = np.random.default_rng(77).standard_normal((8, 128)).astype(np.float32)
+    x[0] = 0.0                      # zero vector: norm 0, every index K/2 - 1
+    x[1, 3] = np.nan                # NaN propagates into the norm
+    x[2] *= 1e-20                   # tiny
+    x[3] *= 1e18                    # huge (squares overflow to inf)
+    x[4, :] = 1.0                   # constant
+    x[5, 17] = np.inf
+    x[6] = -x[6]
+    return x
+
+
+def make_rows(n, seed, scale=1.0):
+    x = (np.random.default_rng(seed).standard_normal((n, 128)) * scale).astype(np.float32)
+    return np.concatenate([special_rows(), x])
+
+
+def write_gpu(tq, ctx, x_t, n_rows, row_ids=None, capacity=None):
+    import torch
+    capacity = n_rows if capacity is None else capacity
+    cache = tq.alloc_cache(ctx.fmt, capacity + 2)
+    cache.fill_(0xA5)  # canary pattern everywhere, including past the last slot
+    rid = None if row_ids is None else torch.from_numpy(row_ids).cuda()
+    tq.tq_quantize_set_rows(ctx, x_t, cache, row_ids=rid, n_rows=n_rows)
+    torch.cuda.synchronize()
+    return cache
+
+
+@pytest.mark.parametrize("fmt", ["turbo4", "turbo3"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("seed", [0, 5])
+def test_write_wht_bit_exact(fmt, dtype, seed):
+    tq = lib()
+    x_t, x32 = torch_rows(make_rows(1000, seed, scale=3.0), dtype)
+    ref, _ = Codec(fmt, rotation="wht", rot_seed=seed).encode(x32)
+    ctx = tq.Ctx(fmt, "wht", seed)
+    cache = write_gpu(tq, ctx, x_t, len(x32))
+    got = to_host_bytes(cache, len(x32), ctx.row_bytes)
+    bad = np.nonzero(np.any(got != ref, axis=1))[0]
+    assert bad.size == 0, f"{bad.size} rows differ, first {bad[:5]}"
+    assert tq.tq_ctx_device_status(ctx) == 0
+
+
+@pytest.mark.parametrize("fmt", ["turbo4", "turbo3"])
+def test_write_dense_band(fmt):
+    tq = lib()
+    x_t, x32 = torch_rows(make_rows(3000, 9, scale=2.0)[8:], "bf16")  # finite rows
+    codec = Codec(fmt, rotation="dense", rot_seed=2)
+    ref, aux = codec.encode(x32)
+    ctx = tq.Ctx(fmt, "dense", 2)
+    got = to_host_bytes(write_gpu(tq, ctx, x_t, len(x32)), len(x32), ctx.row_bytes)
+    if fmt == "turbo4":
+        n, idx = unpack_turbo4(got)
+        assert np.array_equal(got[:, :4], ref[:, :4])
+    else:
+        norms, idx = unpack_turbo3(got)
+        assert np.array_equal(norms, unpack_turbo3(ref)[0])
+    ok, ndiff = band_ok(idx, aux["idx"], aux["y"], codec.b32)
+    assert ok, f"{ndiff} indices differ outside the boundary band"
+
+
+def test_write_prod3_band():
+    tq = lib()
+    x_t, x32 = torch_rows(make_rows(3000, 11, scale=2.0)[8:], "bf16")
+    codec = Codec("prod3", rotation="dense", rot_seed=3, qjl_seed=1003)
+    ref, aux = codec.encode(x32)
+    ctx = tq.Ctx("prod3", "dense", 3, 1003)
+    got = to_host_bytes(write_gpu(tq, ctx, x_t, len(x32)), len(x32), 56)
+    n, gamma, idx, sb = unpack_prod(got)
+    assert np.array_equal(got[:, :4], ref[:, :4])
+    ok, _ = band_ok(idx, aux["idx"], aux["y"], codec.b32)
+    assert ok
+    same = np.all(idx == aux["idx"], axis=1)
+    assert same.mean() > 0.99
+    rel = np.abs(gamma[same] - aux["gamma"][same]) / aux["gamma"][same]
+    assert rel.max() < 1e-5
+    flip = (sb != aux["sign_bits"]) & same[:, None]
+    assert np.all(np.abs(aux["z"][flip]) < 1e-4)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_write_vgroup_bit_exact(dtype):
+    tq = lib()
+    x = make_rows(1000, 13, scale=5.0)
+    x[8, :32] = -0.0
+    x[9, 32:64] = 7.0
+    x_t, x32 = torch_rows(x, dtype)
+    ref, _ = Codec("vgroup2").encode(x32)
+    ctx = tq.Ctx("vgroup2")
+    got = to_host_bytes(write_gpu(tq, ctx, x_t, len(x32)), len(x32), 48)
+    bad = np.nonzero(np.any(got != ref, axis=1))[0]
+    assert bad.size == 0, f"{bad.size} rows differ, first {bad[:5]}"
+
+
+def test_scatter_row_ids_canaries_and_oob_flag():
+    """SET_ROWS writes row i to slot row_ids[i]; slots never written keep their canary
+    bytes; an out-of-range slot is skipped and flagged (status 1)."""
+    import torch
+    tq = lib()
+    n, cap = 200, 300
+    x_t, x32 = torch_rows(make_rows(n - 8, 17), "bf16")
+    slots = synth.row_permutation(cap, 3)[:n].copy()
+    slots[5] = cap + 10  # out of range
+    ctx = tq.Ctx("turbo4", "wht", 0)
+    cache = write_gpu(tq, ctx, x_t, n, row_ids=slots, capacity=cap)
+    assert tq.tq_ctx_device_status(ctx) == 1
+    assert tq.tq_ctx_device_status(ctx) == 0  # cleared by the read
+    ref, _ = Codec("turbo4", rotation="wht", rot_seed=0).encode(x32)
+    host = cache.cpu().numpy()
+    rows = host[: cap * 68].reshape(cap, 68)
+    for i in range(n):
+        if i == 5:
+            continue
+        assert np.array_equal(rows[slots[i]], ref[i])
+    untouched = sorted(set(range(cap)) - set(int(s) for s in slots if s < cap))
+    assert np.all(rows[untouched] == 0xA5)
+    assert np.all(host[cap * 68:] == 0xA5)  # nothing written past the last slot
+
+
+def test_strided_source_rows():
+    """Rows taken from a wider tensor (stride > 128) quantize like contiguous rows."""
+    import torch
+    tq = lib()
+    x = make_rows(300, 19)[8:]
+    wide = np.zeros((len(x), 256), np.float32)
+    wide[:, 64:192] = x
+    t = torch.from_numpy(wide).cuda()[:, 64:192]
+    ctx = tq.Ctx("turbo4", "wht", 1)
+    cache = write_gpu(tq, ctx, t, len(x))
+    ref, _ = Codec("turbo4", rotation="wht", rot_seed=1).encode(x)
+    assert np.array_equal(to_host_bytes(cache, len(x), 68), ref)
+
+
+def test_zero_rows_is_noop_and_bad_alignment_rejected():
+    import torch
+    tq = lib()
+    ctx = tq.Ctx("turbo4", "wht", 0)
+    cache = tq.alloc_cache("turbo4", 4)
+    x = torch.zeros((4, 128), dtype=torch.float32, device="cuda")
+    tq.tq_quantize_set_rows(ctx, x, cache, n_rows=0)
+    raw = torch.zeros(4 * 128 + 1, dtype=torch.float32, device="cuda")
+    st = tq.lib.tq_quantize_set_rows(ctx.handle, raw.data_ptr() + 4, tq.TQ_DTYPE_F32, 4, 128, None,
+                                     cache.data_ptr(), 4, None)
+    assert st == tq.TQ_ERR_ALIGNMENT
+
+
+@pytest.mark.parametrize("fmt,rot", [("turbo4", "wht"), ("turbo3", "wht"), ("turbo4", "dense"), ("turbo3", "dense")])
+def test_write_chunk_full_size(fmt, rot):
+    """The 16,384-token x 8-KV-head bf16 chunk (K and V), every row checked."""
+    tq = lib()
+    cfg = synth.WORKLOADS["write_chunk"]
+    ctx = tq.Ctx(fmt, rot, 4)
+    codec = Codec(fmt, rotation=rot, rot_seed=4)
+    for tensor in ("K", "V"):
+        x32, bits = synth.write_rows(cfg, tensor)
+        import torch
+        x_t = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+        got = to_host_bytes(write_gpu(tq, ctx, x_t, len(x32)), len(x32), ctx.row_bytes)
+        ref, aux = codec.encode(x32)
+        if rot == "wht":
+            assert np.array_equal(got, ref)
+        else:
+            idx = unpack_turbo4(got)[1] if fmt == "turbo4" else unpack_turbo3(got)[1]
+            ok, ndiff = band_ok(idx, aux["idx"], aux["y"], codec.b32)
+            assert ok, f"{ndiff} indices outside the band"
+    assert tq.tq_ctx_device_status(ctx) == 0
