@@ -6,8 +6,8 @@ default to torch's current CUDA stream.  All computation runs in the library's
 CUDA kernels; if the library has not been built, importing this package raises
 ImportError instead of falling back to anything else.
 
-Build the library with ``python -m compressed_attention_gb300._build`` (or
-``__graft_entry__.build()``).
+Build the library with ``python compressed_attention_gb300/_build.py`` (or
+``__graft_entry__.build()``); the build script does not import this package.
 """
 
 import ctypes
@@ -73,7 +73,7 @@ _SIGNATURES = {
 
 def _load():
     if not os.path.exists(LIB_PATH):
-        raise ImportError(f"{LIB_PATH} is not built; run `python -m compressed_attention_gb300._build`")
+        raise ImportError(f"{LIB_PATH} is not built; run `python compressed_attention_gb300/_build.py`")
     lib = ctypes.CDLL(LIB_PATH)
     for name, (res, args) in _SIGNATURES.items():
         f = getattr(lib, name)

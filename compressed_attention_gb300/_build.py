@@ -4,6 +4,9 @@ Every translation unit is compiled in parallel with
 ``-gencode arch=compute_103a,code=sm_103a -lineinfo -O3``, then linked with the
 static CUDA runtime into one position-independent shared library.  The build is
 skipped when the library is newer than every source and header.
+
+This file is loaded by path (``load()`` below, or ``python _build.py``) so that it
+never imports the package, whose import needs the built library.
 """
 
 import os
@@ -75,6 +78,15 @@ def build(force=False, verbose=False, extra_flags=()):
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
     return LIB
+
+
+def load():
+    """This module, imported by file path without importing the package."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("tq_build", os.path.abspath(__file__))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
 
 
 if __name__ == "__main__":

@@ -10,8 +10,8 @@ BAND = 1e-5   # dense rotation: indices may differ only this close to a boundary
 
 
 def lib():
-    from compressed_attention_gb300 import _build
-    _build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import compressed_attention_gb300 as tq
     return tq
 

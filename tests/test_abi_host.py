@@ -16,8 +16,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def tq():
-    from compressed_attention_gb300 import _build
-    _build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import compressed_attention_gb300 as m
     return m
 
