@@ -6,25 +6,30 @@
 // Three launches:
 //   k_prepare_q  q_rot = R q (one warp per query), pre-scaled by
 //                log2(e) * scale / alpha and by a power of two, split into fp16
-//                hi + lo parts (the tensor-core A operand).
-//   k_partial_*  one CTA per (batch, KV head, head group, key split): a producer
-//                warp streams 64-key tiles of the K and V caches into shared
-//                memory with 1-D bulk async copies on an mbarrier ring; four
-//                consumer warps each take 16 keys of a tile, decode the nibbles
-//                to fp16 centroids with byte permutes, and run the score and PV
-//                products as m16n8k16 MMAs with fp32 accumulators.
+//                hi + lo parts (the tensor-core operand).
+//   k_partial_t4 one CTA per (batch, KV head, group of 4 or 8 q-heads, key split):
+//                a producer warp streams 128-key tiles of the K and V caches into
+//                shared memory with 1-D bulk async copies on an mbarrier ring;
+//                eight consumer warps each take 16 keys of a tile, turn nibble
+//                pairs into fp16x2 centroid pairs (a conflict-free shared-memory
+//                table, or byte permutes for a tunable share of the words), and run
+//                the score and PV products as m16n8k16 MMAs with fp32 accumulators.
 //   k_combine    log-sum-exp merge of the splits, 1/sum, un-rotation R^T o.
 //
-// Operand layout of the MMAs (one warp, 16 keys, up to 8 q-heads of one KV head):
-//   score  S[16 x 8 keys] = Q[16 x 128] * K_hat^T : row h = q_hi of head h, row
-//          h+8 = q_lo of head h, so S[h] + S[h+8] is the score at fp32 accuracy.
-//   PV     O[16 x 128] += P[16 x 16 keys] * V_hat : row h = p_hi, row h+8 = p_lo.
-//   The score accumulator fragment of two key tiles is exactly the A fragment
-//   of the PV product, so probabilities never leave registers.
-// Centroids enter as fp16 values alpha * |c| with the sign applied from the
-// index; alpha (chosen on the host) minimises the fp16 rounding error of the
-// table and is divided out through q and in the combine.
+// MMA operand layout (one warp, 16 keys, 4 q-heads per column group):
+//   score  S^T[16 keys x 8] = K_hat[16 keys x 128] Q^T : column 2h holds q_hi of
+//          head h and column 2h+1 its q_lo, so the two add to the fp32-accurate score.
+//   PV     O^T[128 x 8] += V_hat^T[128 x 16 keys] P^T : columns again hi/lo pairs.
+//   Heads fill the N = 8 columns exactly for four q-heads per KV head, so no MMA
+//   row is padding.  Probabilities move from the score accumulator layout to the
+//   PV operand layout with four shuffles per 16 keys.
+// Centroids enter as fp16 values alpha * c; alpha (chosen on the host) minimises
+// the fp16 rounding error of the table and is divided out through q and in the
+// combine.
 #include <math.h>
+#include <string.h>
+
+#include <cstring>
 
 #include "tq_device.cuh"
 #include "tq_internal.h"
@@ -33,12 +38,12 @@ namespace tq {
 
 namespace {
 
-constexpr int TILE = 64;              // keys per pipeline stage
-constexpr int CWARPS = 4;             // consumer warps (16 keys each per tile)
+constexpr int TILE = 128;             // keys per pipeline stage
+constexpr int CWARPS = 8;             // consumer warps (16 keys each per tile)
 constexpr int NTHREADS = (CWARPS + 1) * 32;
 constexpr int NSTAGE = 4;             // pipeline depth
 constexpr int T4_ROW = 68;
-constexpr int STAGE_BUF = 4416;       // >= 64 * 68 + 2 * 16, multiple of 32
+constexpr int STAGE_BUF = 8736;       // >= 128 * 68 + 2 * 15, multiple of 32
 constexpr float P_SHIFT = 14.0f;      // p' = 2^14 * exp2(.) keeps fp16 normal
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 constexpr float LOG2E = 1.4426950408889634f;
@@ -149,25 +154,59 @@ struct PartialParams {
   const float *qsc;
   float *part;
   float *scores;
-  uint32_t klo[2], khi[2], vlo[2], vhi[2];
+  uint32_t c16[8];                      // the 16 fp16 centroids of the shared table, pairs per word
+  uint32_t klo[2], khi[2], vlo[2], vhi[2];  // byte-permute tables (K and V codebooks)
   int32_t *status;
 };
 
+// Shared memory of one CTA.  The stage buffers are reused as the merge area once
+// every copy has landed and been consumed.
 struct SmemPartial {
+  uint32_t lut[256][32];                // byte -> (c[lo nibble], c[hi nibble]) as fp16x2, one copy per bank
   uint8_t kbuf[NSTAGE][STAGE_BUF];
   uint8_t vbuf[NSTAGE][STAGE_BUF];
   uint64_t full[NSTAGE];
   uint64_t empty[NSTAGE];
   float mw[CWARPS][8];
   float lw[CWARPS][8];
-  float osm[8][D];
   int abort_flag;
   int first_unconsumed;
   int issued;
 };
+static_assert(sizeof(float) * CWARPS * 8 * D <= sizeof(uint8_t) * NSTAGE * STAGE_BUF,
+              "merge area must fit in the K stage buffers");
 
-template <bool SCORES>
-__global__ void __launch_bounds__(NTHREADS, 2) k_partial_t4(const PartialParams p) {
+// Table lookup of one byte of w: two fp16 centroids from this lane's copy of the table.
+__device__ __forceinline__ uint32_t lut_byte(uint32_t tbl_lane, uint32_t w, int i) {
+  const uint32_t b = (i == 0) ? (w & 0xFFu) : (i == 3 ? (w >> 24) : ((w >> (8 * i)) & 0xFFu));
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(b * 128u + tbl_lane));
+  return v;
+}
+
+// Four bytes of w -> four fp16x2 words, either from the table or by byte permutes.
+template <bool PRMT>
+__device__ __forceinline__ void decode4(uint32_t tbl_lane, uint32_t w, const uint32_t (&lo)[2],
+                                        const uint32_t (&hi)[2], uint32_t (&r)[4]) {
+  if (PRMT) {
+    decode8<0x5140u, 0x7362u>(w, lo, hi, r);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r[i] = lut_byte(tbl_lane, w, i);
+  }
+}
+
+__device__ __forceinline__ uint32_t ld_u32(const uint8_t *p) {
+  return *reinterpret_cast<const uint32_t *>(p);
+}
+
+// One CTA = (batch b, KV head, group of up to 4*NG q-heads, key split).  Thread
+// (g, t) = (lane / 4, lane % 4) of a consumer warp owns, per 16-key block: keys g
+// and g+8 of the score product (head t of every column group) and dims 16g..16g+15
+// of the PV product.  KPRMT / VPRMT words (of 4 / 2 per key) are decoded by byte
+// permutes instead of the table, to balance the ALU and shared-memory pipes.
+template <int NG, bool SCORES, int KPRMT, int VPRMT>
+__global__ void __launch_bounds__(NTHREADS) __maxnreg__(NG == 1 ? 112 : 168) k_partial_t4(const PartialParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   SmemPartial &sm = *reinterpret_cast<SmemPartial *>(smem_raw);
   const int split = blockIdx.x;
@@ -187,7 +226,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) k_partial_t4(const PartialParams 
   const int key0 = split * p.chunk;
   const int nkeys = max(0, min(key0 + p.chunk, Lb) - key0);
   const int ntiles = (nkeys + TILE - 1) / TILE;
-  const int G = min(8, p.gq - hg * 8);
+  const int G = min(4 * NG, p.gq - hg * 4 * NG);  // valid q-heads in this group
+  const int head0 = kvh * p.gq + hg * 4 * NG;
   const size_t unit_row0 = (size_t)bk * p.L;
 
   if (threadIdx.x == 0) {
@@ -200,14 +240,25 @@ __global__ void __launch_bounds__(NTHREADS, 2) k_partial_t4(const PartialParams 
     sm.issued = 0;
     fence_mbar_init();
   }
+  for (int i = threadIdx.x; i < 256 * 32; i += NTHREADS) {
+    const int byte = i >> 5;
+    const uint32_t lo = (p.c16[(byte & 15) >> 1] >> (16 * (byte & 1))) & 0xFFFFu;
+    const uint32_t hi = (p.c16[(byte >> 4) >> 1] >> (16 * ((byte >> 4) & 1))) & 0xFFFFu;
+    sm.lut[byte][i & 31] = lo | (hi << 16);
+  }
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
 
-  float O[16][4];
-  float M = -INFINITY, lsum = 0.f;
+  float O[NG][8][4];
+  float M[NG], lsum[NG];
 #pragma unroll
-  for (int n = 0; n < 16; ++n) O[n][0] = O[n][1] = O[n][2] = O[n][3] = 0.f;
+  for (int c = 0; c < NG; ++c) {
+    M[c] = -INFINITY;
+    lsum[c] = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) O[c][mt][0] = O[c][mt][1] = O[c][mt][2] = O[c][mt][3] = 0.f;
+  }
 
   if (warp == CWARPS) {
     // ---------------- producer: one elected lane streams K and V tiles
@@ -234,35 +285,35 @@ __global__ void __launch_bounds__(NTHREADS, 2) k_partial_t4(const PartialParams 
     }
   } else {
     // ---------------- consumers
-    const int hq = kvh * p.gq + hg * 8 + g;
-    const bool head_ok = g < G;
-    uint32_t qa[8][4];
-    float qs = 0.f;
-    if (head_ok) {
-      const uint4 *qp = reinterpret_cast<const uint4 *>(p.qhl + (size_t)(b * p.Hq + hq) * 256);
-      uint32_t hw[16], lw[16];
+    // q as the B operand: column g = (head slot g/2, part g%2 = hi/lo), rows = dims.
+    uint32_t qb[NG][8][2];
+    float qs[NG];
+    {
+      const int hs = g >> 1, part = g & 1;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint4 a = qp[4 * t + i];        // hi words 16t .. 16t+15
-        const uint4 c = qp[16 + 4 * t + i];   // lo words 64 + 16t ..
-        hw[4 * i] = a.x, hw[4 * i + 1] = a.y, hw[4 * i + 2] = a.z, hw[4 * i + 3] = a.w;
-        lw[4 * i] = c.x, lw[4 * i + 1] = c.y, lw[4 * i + 2] = c.z, lw[4 * i + 3] = c.w;
+      for (int c = 0; c < NG; ++c) {
+        const int slot = c * 4 + hs;
+        if (slot < G) {
+          const uint32_t *qw = p.qhl + (size_t)(b * p.Hq + head0 + slot) * 256 + part * 64 + 16 * t;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            qb[c][kk][0] = qw[2 * kk];
+            qb[c][kk][1] = qw[2 * kk + 1];
+          }
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) qb[c][kk][0] = qb[c][kk][1] = 0u;
+        }
+        const int my = c * 4 + t;  // the head whose scores this thread holds
+        qs[c] = (my < G) ? p.qsc[2 * (b * p.Hq + head0 + my)] : 0.f;
       }
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        qa[kk][0] = hw[2 * kk];
-        qa[kk][1] = lw[2 * kk];
-        qa[kk][2] = hw[2 * kk + 1];
-        qa[kk][3] = lw[2 * kk + 1];
-      }
-      qs = p.qsc[2 * (b * p.Hq + hq)];
-    } else {
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) qa[kk][0] = qa[kk][1] = qa[kk][2] = qa[kk][3] = 0u;
     }
+    const uint32_t tbl_lane = smem_addr(&sm.lut[0][lane]);
     const uint32_t klo[2] = {p.klo[0], p.klo[1]}, khi[2] = {p.khi[0], p.khi[1]};
     const uint32_t vlo[2] = {p.vlo[0], p.vlo[1]}, vhi[2] = {p.vhi[0], p.vhi[1]};
     const int kb = warp * 16;
+    const int src_a = 4 * (2 * t) + (g >> 1), src_b = src_a + 4;
+    const bool lo_part = (g & 1) != 0;
 
     for (int i = 0; i < ntiles; ++i) {
       const int s = i % NSTAGE;
@@ -278,138 +329,172 @@ __global__ void __launch_bounds__(NTHREADS, 2) k_partial_t4(const PartialParams 
       const uint8_t *Ks = sm.kbuf[s] + (start & 15);
       const uint8_t *Vs = sm.vbuf[s] + (start & 15);
       if (kb < nk) {
-        // ---- scores: two n-tiles of 8 keys (kb + g and kb + 8 + g for this lane)
-        float sc0[4] = {0.f, 0.f, 0.f, 0.f}, sc1[4] = {0.f, 0.f, 0.f, 0.f};
-        const uint8_t *kp0 = Ks + (kb + g) * T4_ROW + 4 + 16 * t;
-        const uint8_t *kp1 = kp0 + 8 * T4_ROW;
+        // ---- scores S^T[16 keys x 8 cols] = K_hat[keys x dims] Q^T, two accumulator chains
+        float sa[NG][4], sb[NG][4];
+#pragma unroll
+        for (int c = 0; c < NG; ++c)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sa[c][e] = sb[c][e] = 0.f;
+        const uint8_t *kr0 = Ks + (kb + g) * T4_ROW + 4 + 16 * t;
+        const uint8_t *kr1 = kr0 + 8 * T4_ROW;
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
-          uint32_t r[4];
-          decode8<0x5140u, 0x7362u>(*reinterpret_cast<const uint32_t *>(kp0 + 4 * w), klo, khi, r);
-          mma_f16(sc0, qa[2 * w], r[0], r[1]);
-          mma_f16(sc0, qa[2 * w + 1], r[2], r[3]);
-          decode8<0x5140u, 0x7362u>(*reinterpret_cast<const uint32_t *>(kp1 + 4 * w), klo, khi, r);
-          mma_f16(sc1, qa[2 * w], r[0], r[1]);
-          mma_f16(sc1, qa[2 * w + 1], r[2], r[3]);
-        }
-        // ---- online softmax over this lane's 4 keys of head g
-        const int kl[4] = {kb + 2 * t, kb + 2 * t + 1, kb + 8 + 2 * t, kb + 9 + 2 * t};
-        float sv[4] = {sc0[0] + sc0[2], sc0[1] + sc0[3], sc1[0] + sc1[2], sc1[1] + sc1[3]};
-        float uv[4];
+          uint32_t d0[4], d1[4];
+          if (w < KPRMT) {
+            decode4<true>(tbl_lane, ld_u32(kr0 + 4 * w), klo, khi, d0);
+            decode4<true>(tbl_lane, ld_u32(kr1 + 4 * w), klo, khi, d1);
+          } else {
+            decode4<false>(tbl_lane, ld_u32(kr0 + 4 * w), klo, khi, d0);
+            decode4<false>(tbl_lane, ld_u32(kr1 + 4 * w), klo, khi, d1);
+          }
+          const uint32_t a0[4] = {d0[0], d1[0], d0[1], d1[1]};
+          const uint32_t a1[4] = {d0[2], d1[2], d0[3], d1[3]};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float nkn = *reinterpret_cast<const float *>(Ks + kl[e] * T4_ROW);
-          const float nvn = *reinterpret_cast<const float *>(Vs + kl[e] * T4_ROW);
-          const bool valid = kl[e] < nk;
-          sv[e] = valid ? sv[e] * (nkn * qs) : -INFINITY;
-          uv[e] = valid ? sv[e] + fmaxf(log2_approx(nvn), -64.f) : -INFINITY;
-          if (SCORES && valid && head_ok)
-            p.scores[((size_t)(b * p.Hq + hq)) * p.L + kf + kl[e]] = sv[e] * LN2;
-        }
-        float bm = fmaxf(fmaxf(uv[0], uv[1]), fmaxf(uv[2], uv[3]));
-        bm = fmaxf(bm, __shfl_xor_sync(FULL_MASK, bm, 1));
-        bm = fmaxf(bm, __shfl_xor_sync(FULL_MASK, bm, 2));
-        if (bm > M) {
-          const float alpha = exp2_approx(M - bm);
-          M = bm;
-          lsum *= alpha;
-#pragma unroll
-          for (int n = 0; n < 16; ++n) {
-            O[n][0] *= alpha, O[n][1] *= alpha, O[n][2] *= alpha, O[n][3] *= alpha;
+          for (int c = 0; c < NG; ++c) {
+            mma_f16(sa[c], a0, qb[c][2 * w][0], qb[c][2 * w][1]);
+            mma_f16(sb[c], a1, qb[c][2 * w + 1][0], qb[c][2 * w + 1][1]);
           }
         }
-        const float Mu = (M == -INFINITY) ? 0.f : M;
-        float pp[4];
+        // ---- online softmax: keys kb+g, kb+g+8 of head t in each column group
+        const float nk0 = *reinterpret_cast<const float *>(Ks + (kb + g) * T4_ROW);
+        const float nk1 = *reinterpret_cast<const float *>(Ks + (kb + g + 8) * T4_ROW);
+        const float nv0 = *reinterpret_cast<const float *>(Vs + (kb + g) * T4_ROW);
+        const float nv1 = *reinterpret_cast<const float *>(Vs + (kb + g + 8) * T4_ROW);
+        const bool ok0 = kb + g < nk, ok1 = kb + g + 8 < nk;
+        const float nu0 = ok0 ? fmaxf(log2_approx(nv0), -64.f) : 0.f;
+        const float nu1 = ok1 ? fmaxf(log2_approx(nv1), -64.f) : 0.f;
+        uint32_t pb[NG][2];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          lsum += exp2_approx(sv[e] - Mu);
-          pp[e] = exp2_approx(uv[e] - Mu + P_SHIFT);
+        for (int c = 0; c < NG; ++c) {
+          const float s0 = ok0 ? (sa[c][0] + sa[c][1] + sb[c][0] + sb[c][1]) * (nk0 * qs[c]) : -INFINITY;
+          const float s1 = ok1 ? (sa[c][2] + sa[c][3] + sb[c][2] + sb[c][3]) * (nk1 * qs[c]) : -INFINITY;
+          if (SCORES && c * 4 + t < G) {
+            float *srow = p.scores + (size_t)(b * p.Hq + head0 + c * 4 + t) * p.L + kf + kb;
+            if (ok0) srow[g] = s0 * LN2;
+            if (ok1) srow[g + 8] = s1 * LN2;
+          }
+          const float u0 = s0 + nu0, u1 = s1 + nu1;
+          float bm = fmaxf(u0, u1);
+          bm = fmaxf(bm, __shfl_xor_sync(FULL_MASK, bm, 4));
+          bm = fmaxf(bm, __shfl_xor_sync(FULL_MASK, bm, 8));
+          bm = fmaxf(bm, __shfl_xor_sync(FULL_MASK, bm, 16));
+          if (bm > M[c]) {
+            const float alpha = exp2_approx(M[c] - bm);
+            M[c] = bm;
+            lsum[c] *= alpha;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+              O[c][mt][0] *= alpha, O[c][mt][1] *= alpha, O[c][mt][2] *= alpha, O[c][mt][3] *= alpha;
+            }
+          }
+          const float Mu = (M[c] == -INFINITY) ? 0.f : M[c];
+          lsum[c] += exp2_approx(s0 - Mu) + exp2_approx(s1 - Mu);
+          const float pp0 = exp2_approx(u0 - Mu + P_SHIFT);
+          const float pp1 = exp2_approx(u1 - Mu + P_SHIFT);
+          // P^T as the B operand: column g takes head g/2, hi (g even) or lo (g odd) part
+          const float v0 = __shfl_sync(FULL_MASK, pp0, src_a), v1 = __shfl_sync(FULL_MASK, pp0, src_b);
+          const float v2 = __shfl_sync(FULL_MASK, pp1, src_a), v3 = __shfl_sync(FULL_MASK, pp1, src_b);
+          uint32_t h01, l01, h23, l23;
+          split_half2(v0, v1, h01, l01);
+          split_half2(v2, v3, h23, l23);
+          pb[c][0] = lo_part ? l01 : h01;
+          pb[c][1] = lo_part ? l23 : h23;
         }
-        uint32_t pa[4];
-        split_half2(pp[0], pp[1], pa[0], pa[1]);
-        split_half2(pp[2], pp[3], pa[2], pa[3]);
-        // ---- PV: V_hat columns 16 g + n of keys 2t, 2t+1 (b0b1) and 2t+8, 2t+9 (b2b3)
-        const uint8_t *v0 = Vs + (kb + 2 * t) * T4_ROW + 4 + 8 * g;
-        const uint8_t *v2 = v0 + 8 * T4_ROW;
+        // ---- O^T[dims x cols] += V_hat^T[dims x keys] P^T: keys 2t, 2t+1 (ab) and 2t+8, 2t+9 (cd)
+        const uint8_t *va = Vs + (kb + 2 * t) * T4_ROW + 4 + 8 * g;
+        const uint8_t *vc = va + 8 * T4_ROW;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const uint32_t xa = *reinterpret_cast<const uint32_t *>(v0 + 4 * half);
-          const uint32_t xb = *reinterpret_cast<const uint32_t *>(v0 + T4_ROW + 4 * half);
-          const uint32_t xc = *reinterpret_cast<const uint32_t *>(v2 + 4 * half);
-          const uint32_t xd = *reinterpret_cast<const uint32_t *>(v2 + T4_ROW + 4 * half);
+        for (int w = 0; w < 2; ++w) {
+          const uint32_t xa = ld_u32(va + 4 * w), xb = ld_u32(va + T4_ROW + 4 * w);
+          const uint32_t xc = ld_u32(vc + 4 * w), xd = ld_u32(vc + T4_ROW + 4 * w);
+          // byte i of z_lo = (low nibble of key a, low nibble of key b) of byte 8g + 4w + i
+          const uint32_t zlo_ab = (xa & 0x0F0F0F0Fu) | ((xb << 4) & 0xF0F0F0F0u);
+          const uint32_t zhi_ab = ((xa >> 4) & 0x0F0F0F0Fu) | (xb & 0xF0F0F0F0u);
+          const uint32_t zlo_cd = (xc & 0x0F0F0F0Fu) | ((xd << 4) & 0xF0F0F0F0u);
+          const uint32_t zhi_cd = ((xc >> 4) & 0x0F0F0F0Fu) | (xd & 0xF0F0F0F0u);
+          uint32_t r0[4], r1[4], r2[4], r3[4];
+          if (w < VPRMT) {
+            decode4<true>(tbl_lane, zlo_ab, vlo, vhi, r0);
+            decode4<true>(tbl_lane, zhi_ab, vlo, vhi, r1);
+            decode4<true>(tbl_lane, zlo_cd, vlo, vhi, r2);
+            decode4<true>(tbl_lane, zhi_cd, vlo, vhi, r3);
+          } else {
+            decode4<false>(tbl_lane, zlo_ab, vlo, vhi, r0);
+            decode4<false>(tbl_lane, zhi_ab, vlo, vhi, r1);
+            decode4<false>(tbl_lane, zlo_cd, vlo, vhi, r2);
+            decode4<false>(tbl_lane, zhi_cd, vlo, vhi, r3);
+          }
 #pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            const uint32_t sel = q ? 0x7362u : 0x5140u;
-            uint32_t r01[4], r23[4];
-            decode8<0x6240u, 0x7351u>(prmt(xa, xb, sel), vlo, vhi, r01);
-            decode8<0x6240u, 0x7351u>(prmt(xc, xd, sel), vlo, vhi, r23);
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t a[4] = {r0[j], r1[j], r2[j], r3[j]};
 #pragma unroll
-            for (int dd = 0; dd < 4; ++dd) mma_f16(O[half * 8 + q * 4 + dd], pa, r01[dd], r23[dd]);
+            for (int c = 0; c < NG; ++c) mma_f16(O[c][4 * w + j], a, pb[c][0], pb[c][1]);
           }
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.empty[s]);
     }
-    lsum += __shfl_xor_sync(FULL_MASK, lsum, 1);
-    lsum += __shfl_xor_sync(FULL_MASK, lsum, 2);
+#pragma unroll
+    for (int c = 0; c < NG; ++c) {
+      lsum[c] += __shfl_xor_sync(FULL_MASK, lsum[c], 4);
+      lsum[c] += __shfl_xor_sync(FULL_MASK, lsum[c], 8);
+      lsum[c] += __shfl_xor_sync(FULL_MASK, lsum[c], 16);
+    }
   }
 
-  // ---------------- merge the consumer warps' states, write this split's partial
+  // ---------------- drain (only after a bounded wait gave up), then merge the warps
   __syncthreads();
-  if (warp < CWARPS && t == 0) {
-    sm.mw[warp][g] = M;
-    sm.lw[warp][g] = lsum;
-  }
-  __syncthreads();
-  float fac = 0.f;
-  if (warp < CWARPS) {
-    float ms = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < CWARPS; ++w) ms = fmaxf(ms, sm.mw[w][g]);
-    fac = (M == -INFINITY) ? 0.f : exp2_approx(M - ms);
-  }
-  for (int w = 0; w < CWARPS; ++w) {
-    if (warp == w && g < G) {
-      float *orow = sm.osm[g];
-#pragma unroll
-      for (int n = 0; n < 16; ++n) {
-        const float a = (O[n][0] + O[n][2]) * fac, c = (O[n][1] + O[n][3]) * fac;
-        if (w == 0) {
-          orow[32 * t + n] = a;
-          orow[32 * t + 16 + n] = c;
-        } else {
-          orow[32 * t + n] += a;
-          orow[32 * t + 16 + n] += c;
-        }
-      }
-    }
-    __syncthreads();
-  }
-  for (int idx = threadIdx.x; idx < G * (D + 6); idx += NTHREADS) {
-    const int gg = idx / (D + 6), j = idx % (D + 6);
-    const int hq = kvh * p.gq + hg * 8 + gg;
-    float *dst = p.part + ((size_t)(b * p.Hq + hq) * p.n_split + split) * PARTIAL_FLOATS;
-    float ms = -INFINITY;
-    for (int w = 0; w < CWARPS; ++w) ms = fmaxf(ms, sm.mw[w][gg]);
-    if (j == 0) {
-      dst[0] = ms;
-    } else if (j == 1) {
-      float ls = 0.f;
-      if (ms != -INFINITY)
-        for (int w = 0; w < CWARPS; ++w)
-          if (sm.mw[w][gg] != -INFINITY) ls += sm.lw[w][gg] * exp2_approx(sm.mw[w][gg] - ms);
-      dst[1] = ls;
-    } else if (j < 6) {
-      dst[j] = 0.f;
-    } else {
-      dst[j] = (ms == -INFINITY) ? 0.f : sm.osm[gg][j - 6];
-    }
-  }
-  // drain: if a wait gave up, let every issued copy land before the CTA exits
   if (threadIdx.x == 0 && sm.abort_flag) {
     for (int i = sm.first_unconsumed; i < sm.issued; ++i)
       (void)mbar_wait_bounded(&sm.full[i % NSTAGE], (i / NSTAGE) & 1, WAIT_LIMIT_NS);
+  }
+  if (warp < CWARPS && g == 0) {
+#pragma unroll
+    for (int c = 0; c < NG; ++c) {
+      sm.mw[warp][c * 4 + t] = M[c];
+      sm.lw[warp][c * 4 + t] = lsum[c];
+    }
+  }
+  __syncthreads();
+  float *osm = reinterpret_cast<float *>(&sm.kbuf[0][0]);  // [CWARPS][8 heads][128]
+  if (warp < CWARPS) {
+#pragma unroll
+    for (int c = 0; c < NG; ++c) {
+      const int hh = c * 4 + t;
+      float ms = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < CWARPS; ++w) ms = fmaxf(ms, sm.mw[w][hh]);
+      const float fac = (M[c] == -INFINITY) ? 0.f : exp2_approx(M[c] - ms);
+      float *orow = osm + (warp * 8 + hh) * D + 16 * g;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        orow[2 * mt] = (O[c][mt][0] + O[c][mt][1]) * fac;
+        orow[2 * mt + 1] = (O[c][mt][2] + O[c][mt][3]) * fac;
+      }
+    }
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * D; idx += NTHREADS) {
+    const int hh = idx / D, j = idx % D;
+    float ms = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < CWARPS; ++w) ms = fmaxf(ms, sm.mw[w][hh]);
+    float acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < CWARPS; ++w) acc += osm[(w * 8 + hh) * D + j];
+    float *dst = p.part + ((size_t)(b * p.Hq + head0 + hh) * p.n_split + split) * PARTIAL_FLOATS;
+    dst[6 + j] = (ms == -INFINITY) ? 0.f : acc;
+    if (j < 6) {
+      float v = 0.f;
+      if (j == 0) {
+        v = ms;
+      } else if (j == 1 && ms != -INFINITY) {
+        for (int w = 0; w < CWARPS; ++w)
+          if (sm.mw[w][hh] != -INFINITY) v += sm.lw[w][hh] * exp2_approx(sm.mw[w][hh] - ms);
+      }
+      dst[j] = v;
+    }
   }
 }
 
@@ -454,7 +539,8 @@ bool decode_shape(const tq_ctx *k, const tq_ctx *v, int B, int Hq, int Hkv, int 
   (void)v;
   s->B = B, s->Hq = Hq, s->Hkv = Hkv, s->L = L;
   s->gq = Hq / Hkv;
-  s->n_hg = (s->gq + 7) / 8;
+  s->heads_per_cta = s->gq <= 4 ? 4 : 8;
+  s->n_hg = (s->gq + s->heads_per_cta - 1) / s->heads_per_cta;
   const int units = B * Hkv * s->n_hg;
   const int slots = k->num_sms * 2;
   int want = (4 * slots + units - 1) / units;
@@ -499,6 +585,20 @@ cudaError_t launch_prepare_q(const tq_ctx *k, const void *q, int q_dtype, const 
   return cudaGetLastError();
 }
 
+template <int NG, bool SC, int KP, int VP>
+cudaError_t launch_t4(const PartialParams &p, dim3 grid, cudaStream_t st) {
+  const size_t smem = sizeof(SmemPartial);
+  cudaError_t e = cudaFuncSetAttribute(k_partial_t4<NG, SC, KP, VP>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  k_partial_t4<NG, SC, KP, VP><<<grid, NTHREADS, smem, st>>>(p);
+  return cudaGetLastError();
+}
+
+// Decode-word split between the table (shared-memory pipe) and byte permutes (ALU pipe).
+constexpr int K_PRMT_WORDS = 0;   // of 4 key words per key and thread
+constexpr int V_PRMT_WORDS = 1;   // of 2 value words per key pair and thread
+
 cudaError_t launch_partial(const tq_ctx *k, const tq_ctx *v, const uint8_t *kc,
                            const uint8_t *vc, const int32_t *seq_lens, const DecodeShape &s,
                            float *scores_dbg, const Workspace &ws, cudaStream_t st) {
@@ -511,20 +611,17 @@ cudaError_t launch_partial(const tq_ctx *k, const tq_ctx *v, const uint8_t *kc,
     p.klo[i] = k->f16.lo[i], p.khi[i] = k->f16.hi[i];
     p.vlo[i] = v->f16.lo[i], p.vhi[i] = v->f16.hi[i];
   }
+  for (int i = 0; i < 8; ++i) p.c16[i] = k->f16.c16[i];
   p.status = k->d_status;
-  const size_t smem = sizeof(SmemPartial);
   dim3 grid(s.n_split, s.B * s.Hkv * s.n_hg);
-  cudaError_t e;
-  if (scores_dbg) {
-    e = cudaFuncSetAttribute(k_partial_t4<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    k_partial_t4<true><<<grid, NTHREADS, smem, st>>>(p);
-  } else {
-    e = cudaFuncSetAttribute(k_partial_t4<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    k_partial_t4<false><<<grid, NTHREADS, smem, st>>>(p);
+  const bool same_table = std::memcmp(k->f16.c16, v->f16.c16, sizeof(k->f16.c16)) == 0;
+  const bool two = s.heads_per_cta == 8;
+  if (!same_table) {  // the value codebook is not the table's: values by byte permutes only
+    if (two) return scores_dbg ? launch_t4<2, true, K_PRMT_WORDS, 2>(p, grid, st) : launch_t4<2, false, K_PRMT_WORDS, 2>(p, grid, st);
+    return scores_dbg ? launch_t4<1, true, K_PRMT_WORDS, 2>(p, grid, st) : launch_t4<1, false, K_PRMT_WORDS, 2>(p, grid, st);
   }
-  return cudaGetLastError();
+  if (two) return scores_dbg ? launch_t4<2, true, K_PRMT_WORDS, V_PRMT_WORDS>(p, grid, st) : launch_t4<2, false, K_PRMT_WORDS, V_PRMT_WORDS>(p, grid, st);
+  return scores_dbg ? launch_t4<1, true, K_PRMT_WORDS, V_PRMT_WORDS>(p, grid, st) : launch_t4<1, false, K_PRMT_WORDS, V_PRMT_WORDS>(p, grid, st);
 }
 
 cudaError_t launch_combine(const tq_ctx *k, const tq_ctx *v, const DecodeShape &s, float *out,

@@ -200,6 +200,12 @@ F16Table make_f16_table(const float *c32, int K) {
   }
   std::memcpy(t.lo, lo, 8);
   std::memcpy(t.hi, hi, 8);
+  // signed entries in index order: idx < K/2 is -mag[idx], idx >= K/2 is +mag[K-1-idx]
+  for (int idx = 0; idx < K; ++idx) {
+    const int m = idx < nm ? idx : K - 1 - idx;
+    const uint16_t bits = (uint16_t)(lo[m] | (hi[m] << 8) | (idx < nm ? 0x8000 : 0));
+    t.c16[idx / 2] |= (uint32_t)bits << (16 * (idx % 2));
+  }
   t.alpha = (float)best_a;
   t.max_rel_err = (float)best_err;
   return t;

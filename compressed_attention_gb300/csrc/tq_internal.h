@@ -29,6 +29,7 @@ struct Codebook {
 struct F16Table {
   uint32_t lo[2] = {0, 0};
   uint32_t hi[2] = {0, 0};
+  uint32_t c16[8] = {};  // the K signed fp16 entries (alpha * c_k), two per word, index order
   float alpha = 1.0f;
   float max_rel_err = 0.0f;
 };
@@ -78,7 +79,8 @@ cudaError_t launch_dequantize(const tq_ctx *ctx, const uint8_t *cache, int64_t n
 struct DecodeShape {
   int B, Hq, Hkv, L;
   int gq;       // q-heads per KV head
-  int n_hg;     // head groups (of at most 8 q-heads) per KV head
+  int heads_per_cta;  // q-heads one CTA serves (4 or 8)
+  int n_hg;     // head groups per KV head
   int n_split;  // key splits
   int chunk;    // keys per split (multiple of the tile)
 };
