@@ -8,9 +8,9 @@
 //                log2(e) * scale / alpha and by a power of two, split into fp16
 //                hi + lo parts (the tensor-core operand).
 //   k_partial_t4 one CTA per (batch, KV head, group of 4 or 8 q-heads, key split):
-//                a producer warp streams 128-key tiles of the K and V caches into
+//                a producer warp streams 112-key tiles of the K and V caches into
 //                shared memory with 1-D bulk async copies on an mbarrier ring;
-//                eight consumer warps each take 16 keys of a tile, turn nibble
+//                seven consumer warps each take 16 keys of a tile, turn nibble
 //                pairs into fp16x2 centroid pairs (a conflict-free shared-memory
 //                table, or byte permutes for a tunable share of the words), and run
 //                the score and PV products as m16n8k16 MMAs with fp32 accumulators.
@@ -38,12 +38,12 @@ namespace tq {
 
 namespace {
 
-constexpr int TILE = 128;             // keys per pipeline stage
-constexpr int CWARPS = 8;             // consumer warps (16 keys each per tile)
-constexpr int NTHREADS = (CWARPS + 1) * 32;
-constexpr int NSTAGE = 4;             // pipeline depth
+constexpr int CWARPS = 7;             // consumer warps (16 keys each per tile)
+constexpr int TILE = 16 * CWARPS;     // keys per pipeline stage (112)
+constexpr int NTHREADS = (CWARPS + 1) * 32;  // + one producer warp: 8 warps, 2 CTAs per SM
+constexpr int NSTAGE = 3;             // pipeline depth
 constexpr int T4_ROW = 68;
-constexpr int STAGE_BUF = 8736;       // >= 128 * 68 + 2 * 15, multiple of 32
+constexpr int STAGE_BUF = 7648;       // >= 112 * 68 + 2 * 15, multiple of 32
 constexpr float P_SHIFT = 14.0f;      // p' = 2^14 * exp2(.) keeps fp16 normal
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 constexpr float LOG2E = 1.4426950408889634f;
@@ -154,15 +154,18 @@ struct PartialParams {
   const float *qsc;
   float *part;
   float *scores;
-  uint32_t c16[8];                      // the 16 fp16 centroids of the shared table, pairs per word
+  uint32_t kc16[8], vc16[8];                // signed fp16 centroids (K, V), two per word
   uint32_t klo[2], khi[2], vlo[2], vhi[2];  // byte-permute tables (K and V codebooks)
   int32_t *status;
 };
 
-// Shared memory of one CTA.  The stage buffers are reused as the merge area once
-// every copy has landed and been consumed.
+// Shared memory of one CTA.  lut[b][s]: slots s < 32 hold the key table and
+// s >= 32 the value table; entry = (c[b & 15], c[b >> 4]) as fp16x2.  Lane l reads
+// slot l (keys) or 32 + l (values), so a warp's 32 lookups always hit 32 distinct
+// banks, and the byte offset (b << 8) | (4 * slot) is one byte permute away from
+// the packed word.  The stage buffers double as the merge area at the end.
 struct SmemPartial {
-  uint32_t lut[256][32];                // byte -> (c[lo nibble], c[hi nibble]) as fp16x2, one copy per bank
+  uint32_t lut[256][64];
   uint8_t kbuf[NSTAGE][STAGE_BUF];
   uint8_t vbuf[NSTAGE][STAGE_BUF];
   uint64_t full[NSTAGE];
@@ -173,26 +176,28 @@ struct SmemPartial {
   int first_unconsumed;
   int issued;
 };
-static_assert(sizeof(float) * CWARPS * 8 * D <= sizeof(uint8_t) * NSTAGE * STAGE_BUF,
-              "merge area must fit in the K stage buffers");
+static_assert(sizeof(float) * CWARPS * 8 * D <= 2 * NSTAGE * STAGE_BUF,
+              "merge area must fit in the stage buffers");
 
-// Table lookup of one byte of w: two fp16 centroids from this lane's copy of the table.
-__device__ __forceinline__ uint32_t lut_byte(uint32_t tbl_lane, uint32_t w, int i) {
-  const uint32_t b = (i == 0) ? (w & 0xFFu) : (i == 3 ? (w >> 24) : ((w >> (8 * i)) & 0xFFu));
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(b * 128u + tbl_lane));
-  return v;
+// Table lookup of byte I of w: off = (byte << 8) | laneword.byte0.
+template <int I>
+__device__ __forceinline__ uint32_t lut_byte(const uint8_t *lut_base, uint32_t laneword, uint32_t w) {
+  const uint32_t off = prmt(laneword, w, 0x1100u | ((4u + I) << 4));
+  return *reinterpret_cast<const uint32_t *>(lut_base + off);
 }
 
-// Four bytes of w -> four fp16x2 words, either from the table or by byte permutes.
+// Four bytes of w -> four fp16x2 words, from the table or by byte permutes.
 template <bool PRMT>
-__device__ __forceinline__ void decode4(uint32_t tbl_lane, uint32_t w, const uint32_t (&lo)[2],
-                                        const uint32_t (&hi)[2], uint32_t (&r)[4]) {
+__device__ __forceinline__ void decode4(const uint8_t *lut_base, uint32_t laneword, uint32_t w,
+                                        const uint32_t (&lo)[2], const uint32_t (&hi)[2],
+                                        uint32_t (&r)[4]) {
   if (PRMT) {
     decode8<0x5140u, 0x7362u>(w, lo, hi, r);
   } else {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) r[i] = lut_byte(tbl_lane, w, i);
+    r[0] = lut_byte<0>(lut_base, laneword, w);
+    r[1] = lut_byte<1>(lut_base, laneword, w);
+    r[2] = lut_byte<2>(lut_base, laneword, w);
+    r[3] = lut_byte<3>(lut_base, laneword, w);
   }
 }
 
@@ -200,13 +205,24 @@ __device__ __forceinline__ uint32_t ld_u32(const uint8_t *p) {
   return *reinterpret_cast<const uint32_t *>(p);
 }
 
-// One CTA = (batch b, KV head, group of up to 4*NG q-heads, key split).  Thread
-// (g, t) = (lane / 4, lane % 4) of a consumer warp owns, per 16-key block: keys g
-// and g+8 of the score product (head t of every column group) and dims 16g..16g+15
-// of the PV product.  KPRMT / VPRMT words (of 4 / 2 per key) are decoded by byte
-// permutes instead of the table, to balance the ALU and shared-memory pipes.
-template <int NG, bool SCORES, int KPRMT, int VPRMT>
-__global__ void __launch_bounds__(NTHREADS) __maxnreg__(NG == 1 ? 112 : 168) k_partial_t4(const PartialParams p) {
+// Physical key (within a 16-key block) of score row r.  Rows g and g+8 belong to
+// lane group g.  With this order the packed-word loads of a warp hit every bank at
+// most twice, and the PV operand of lane (g, t) -- keys a_t, a_t+2, a_t+4, a_t+6
+// with a_t = {0, 1, 8, 9}[t] -- comes from score rows t, 4+t, 8+t, 12+t, i.e. from
+// the same register of lanes 4t+h and 4(4+t)+h.
+__device__ __forceinline__ int key_of_row(int r) {
+  // rows 0..7: 0 1 8 9 2 3 10 11; rows 8..15: 4 5 12 13 6 7 14 15
+  return ((r & 1) | ((r & 2) << 2) | ((r & 4) >> 1) | ((r & 8) >> 1));
+}
+
+// One CTA = (batch b, KV head, group of up to 4*NG q-heads, key split).  Lane
+// (g, t) = (lane / 4, lane % 4) of a consumer warp owns, per 16-key block, score
+// rows g and g+8 (head t of every column group) and dims 16g..16g+15 of the PV
+// product.  KP of the 4 key words and VP of the 2 value words per lane are decoded
+// by byte permutes instead of the table, to balance the ALU and shared-memory pipes.
+template <int NG, bool SCORES, int KP, int VP>
+__global__ void __launch_bounds__(NTHREADS) __maxnreg__(NG == 1 ? 128 : 168)
+    k_partial_t4(const PartialParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   SmemPartial &sm = *reinterpret_cast<SmemPartial *>(smem_raw);
   const int split = blockIdx.x;
@@ -240,11 +256,12 @@ __global__ void __launch_bounds__(NTHREADS) __maxnreg__(NG == 1 ? 112 : 168) k_p
     sm.issued = 0;
     fence_mbar_init();
   }
-  for (int i = threadIdx.x; i < 256 * 32; i += NTHREADS) {
-    const int byte = i >> 5;
-    const uint32_t lo = (p.c16[(byte & 15) >> 1] >> (16 * (byte & 1))) & 0xFFFFu;
-    const uint32_t hi = (p.c16[(byte >> 4) >> 1] >> (16 * ((byte >> 4) & 1))) & 0xFFFFu;
-    sm.lut[byte][i & 31] = lo | (hi << 16);
+  for (int i = threadIdx.x; i < 256 * 64; i += NTHREADS) {
+    const int byte = i >> 6;
+    const uint32_t *c16 = (i & 32) ? p.vc16 : p.kc16;
+    const uint32_t lo = (c16[(byte & 15) >> 1] >> (16 * (byte & 1))) & 0xFFFFu;
+    const uint32_t hi = (c16[(byte >> 4) >> 1] >> (16 * ((byte >> 4) & 1))) & 0xFFFFu;
+    sm.lut[byte][i & 63] = lo | (hi << 16);
   }
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -304,16 +321,20 @@ __global__ void __launch_bounds__(NTHREADS) __maxnreg__(NG == 1 ? 112 : 168) k_p
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) qb[c][kk][0] = qb[c][kk][1] = 0u;
         }
-        const int my = c * 4 + t;  // the head whose scores this thread holds
+        const int my = c * 4 + t;  // the head whose scores this lane holds
         qs[c] = (my < G) ? p.qsc[2 * (b * p.Hq + head0 + my)] : 0.f;
       }
     }
-    const uint32_t tbl_lane = smem_addr(&sm.lut[0][lane]);
+    const uint8_t *lut_base = reinterpret_cast<const uint8_t *>(&sm.lut[0][0]);
+    const uint32_t kword = 4u * lane, vword = 128u + 4u * lane;
     const uint32_t klo[2] = {p.klo[0], p.klo[1]}, khi[2] = {p.khi[0], p.khi[1]};
     const uint32_t vlo[2] = {p.vlo[0], p.vlo[1]}, vhi[2] = {p.vhi[0], p.vhi[1]};
     const int kb = warp * 16;
-    const int src_a = 4 * (2 * t) + (g >> 1), src_b = src_a + 4;
-    const bool lo_part = (g & 1) != 0;
+    const int rk0 = key_of_row(g), rk1 = key_of_row(g + 8);
+    const int at = (t & 1) | ((t & 2) << 2);  // a_t = 0, 1, 8, 9
+    const int hs = g >> 1;
+    const int src0 = 4 * t + hs, src1 = 4 * (4 + t) + hs;
+    const float lo_sel = (g & 1) ? 1.f : 0.f;
 
     for (int i = 0; i < ntiles; ++i) {
       const int s = i % NSTAGE;
@@ -326,26 +347,28 @@ __global__ void __launch_bounds__(NTHREADS) __maxnreg__(NG == 1 ? 112 : 168) k_p
       const int kf = key0 + i * TILE;
       const int nk = min(TILE, nkeys - i * TILE);
       const size_t start = (unit_row0 + kf) * T4_ROW;
-      const uint8_t *Ks = sm.kbuf[s] + (start & 15);
-      const uint8_t *Vs = sm.vbuf[s] + (start & 15);
-      if (kb < nk) {
-        // ---- scores S^T[16 keys x 8 cols] = K_hat[keys x dims] Q^T, two accumulator chains
+      const uint8_t *Ks = sm.kbuf[s] + (start & 15) + kb * T4_ROW;
+      const uint8_t *Vs = sm.vbuf[s] + (start & 15) + kb * T4_ROW;
+      const int nkb = nk - kb;  // valid keys of this warp's block (may be <= 0 or > 16)
+      if (nkb > 0) {
+        // ---- scores S^T[16 rows x 8 cols] = K_hat Q^T, two accumulator chains
         float sa[NG][4], sb[NG][4];
 #pragma unroll
         for (int c = 0; c < NG; ++c)
 #pragma unroll
           for (int e = 0; e < 4; ++e) sa[c][e] = sb[c][e] = 0.f;
-        const uint8_t *kr0 = Ks + (kb + g) * T4_ROW + 4 + 16 * t;
-        const uint8_t *kr1 = kr0 + 8 * T4_ROW;
+        const uint8_t *kr0 = Ks + rk0 * T4_ROW + 4 + 16 * t;
+        const uint8_t *kr1 = Ks + rk1 * T4_ROW + 4 + 16 * t;
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
           uint32_t d0[4], d1[4];
-          if (w < KPRMT) {
-            decode4<true>(tbl_lane, ld_u32(kr0 + 4 * w), klo, khi, d0);
-            decode4<true>(tbl_lane, ld_u32(kr1 + 4 * w), klo, khi, d1);
+          const uint32_t x0 = ld_u32(kr0 + 4 * w), x1 = ld_u32(kr1 + 4 * w);
+          if (w < KP) {
+            decode4<true>(lut_base, kword, x0, klo, khi, d0);
+            decode4<true>(lut_base, kword, x1, klo, khi, d1);
           } else {
-            decode4<false>(tbl_lane, ld_u32(kr0 + 4 * w), klo, khi, d0);
-            decode4<false>(tbl_lane, ld_u32(kr1 + 4 * w), klo, khi, d1);
+            decode4<false>(lut_base, kword, x0, klo, khi, d0);
+            decode4<false>(lut_base, kword, x1, klo, khi, d1);
           }
           const uint32_t a0[4] = {d0[0], d1[0], d0[1], d1[1]};
           const uint32_t a1[4] = {d0[2], d1[2], d0[3], d1[3]};
@@ -355,23 +378,23 @@ __global__ void __launch_bounds__(NTHREADS) __maxnreg__(NG == 1 ? 112 : 168) k_p
             mma_f16(sb[c], a1, qb[c][2 * w + 1][0], qb[c][2 * w + 1][1]);
           }
         }
-        // ---- online softmax: keys kb+g, kb+g+8 of head t in each column group
-        const float nk0 = *reinterpret_cast<const float *>(Ks + (kb + g) * T4_ROW);
-        const float nk1 = *reinterpret_cast<const float *>(Ks + (kb + g + 8) * T4_ROW);
-        const float nv0 = *reinterpret_cast<const float *>(Vs + (kb + g) * T4_ROW);
-        const float nv1 = *reinterpret_cast<const float *>(Vs + (kb + g + 8) * T4_ROW);
-        const bool ok0 = kb + g < nk, ok1 = kb + g + 8 < nk;
+        // ---- online softmax over the two keys of this lane, head t of each group
+        const float nk0 = *reinterpret_cast<const float *>(Ks + rk0 * T4_ROW);
+        const float nk1 = *reinterpret_cast<const float *>(Ks + rk1 * T4_ROW);
+        const float nv0 = *reinterpret_cast<const float *>(Vs + rk0 * T4_ROW);
+        const float nv1 = *reinterpret_cast<const float *>(Vs + rk1 * T4_ROW);
+        const bool ok0 = rk0 < nkb, ok1 = rk1 < nkb;
         const float nu0 = ok0 ? fmaxf(log2_approx(nv0), -64.f) : 0.f;
         const float nu1 = ok1 ? fmaxf(log2_approx(nv1), -64.f) : 0.f;
         uint32_t pb[NG][2];
 #pragma unroll
         for (int c = 0; c < NG; ++c) {
-          const float s0 = ok0 ? (sa[c][0] + sa[c][1] + sb[c][0] + sb[c][1]) * (nk0 * qs[c]) : -INFINITY;
-          const float s1 = ok1 ? (sa[c][2] + sa[c][3] + sb[c][2] + sb[c][3]) * (nk1 * qs[c]) : -INFINITY;
+          const float s0 = ok0 ? ((sa[c][0] + sa[c][1]) + (sb[c][0] + sb[c][1])) * (nk0 * qs[c]) : -INFINITY;
+          const float s1 = ok1 ? ((sa[c][2] + sa[c][3]) + (sb[c][2] + sb[c][3])) * (nk1 * qs[c]) : -INFINITY;
           if (SCORES && c * 4 + t < G) {
             float *srow = p.scores + (size_t)(b * p.Hq + head0 + c * 4 + t) * p.L + kf + kb;
-            if (ok0) srow[g] = s0 * LN2;
-            if (ok1) srow[g + 8] = s1 * LN2;
+            if (ok0) srow[rk0] = s0 * LN2;
+            if (ok1) srow[rk1] = s1 * LN2;
           }
           const float u0 = s0 + nu0, u1 = s1 + nu1;
           float bm = fmaxf(u0, u1);
@@ -391,38 +414,39 @@ __global__ void __launch_bounds__(NTHREADS) __maxnreg__(NG == 1 ? 112 : 168) k_p
           lsum[c] += exp2_approx(s0 - Mu) + exp2_approx(s1 - Mu);
           const float pp0 = exp2_approx(u0 - Mu + P_SHIFT);
           const float pp1 = exp2_approx(u1 - Mu + P_SHIFT);
-          // P^T as the B operand: column g takes head g/2, hi (g even) or lo (g odd) part
-          const float v0 = __shfl_sync(FULL_MASK, pp0, src_a), v1 = __shfl_sync(FULL_MASK, pp0, src_b);
-          const float v2 = __shfl_sync(FULL_MASK, pp1, src_a), v3 = __shfl_sync(FULL_MASK, pp1, src_b);
-          uint32_t h01, l01, h23, l23;
-          split_half2(v0, v1, h01, l01);
-          split_half2(v2, v3, h23, l23);
-          pb[c][0] = lo_part ? l01 : h01;
-          pb[c][1] = lo_part ? l23 : h23;
+          // P^T as the B operand: column g takes head g/2, hi (g even) or lo (g odd) part,
+          // for the keys a_t, a_t+2 (k 2t, 2t+1) and a_t+4, a_t+6 (k 2t+8, 2t+9).
+          const float va = __shfl_sync(FULL_MASK, pp0, src0), vb = __shfl_sync(FULL_MASK, pp0, src1);
+          const float vc = __shfl_sync(FULL_MASK, pp1, src0), vd = __shfl_sync(FULL_MASK, pp1, src1);
+          const __half2 hab = __floats2half2_rn(va, vb), hcd = __floats2half2_rn(vc, vd);
+          const float2 fab = __half22float2(hab), fcd = __half22float2(hcd);
+          const __half2 rab = __floats2half2_rn(fmaf(-lo_sel, fab.x, va), fmaf(-lo_sel, fab.y, vb));
+          const __half2 rcd = __floats2half2_rn(fmaf(-lo_sel, fcd.x, vc), fmaf(-lo_sel, fcd.y, vd));
+          pb[c][0] = *reinterpret_cast<const uint32_t *>(&rab);
+          pb[c][1] = *reinterpret_cast<const uint32_t *>(&rcd);
         }
-        // ---- O^T[dims x cols] += V_hat^T[dims x keys] P^T: keys 2t, 2t+1 (ab) and 2t+8, 2t+9 (cd)
-        const uint8_t *va = Vs + (kb + 2 * t) * T4_ROW + 4 + 8 * g;
-        const uint8_t *vc = va + 8 * T4_ROW;
+        // ---- O^T[dims x cols] += V_hat^T[dims x keys] P^T
+        const uint8_t *va_p = Vs + at * T4_ROW + 4 + 8 * g;  // key a_t; a_t+2, +4, +6 follow
 #pragma unroll
         for (int w = 0; w < 2; ++w) {
-          const uint32_t xa = ld_u32(va + 4 * w), xb = ld_u32(va + T4_ROW + 4 * w);
-          const uint32_t xc = ld_u32(vc + 4 * w), xd = ld_u32(vc + T4_ROW + 4 * w);
-          // byte i of z_lo = (low nibble of key a, low nibble of key b) of byte 8g + 4w + i
+          const uint32_t xa = ld_u32(va_p + 4 * w), xb = ld_u32(va_p + 2 * T4_ROW + 4 * w);
+          const uint32_t xc = ld_u32(va_p + 4 * T4_ROW + 4 * w), xd = ld_u32(va_p + 6 * T4_ROW + 4 * w);
+          // byte i of zlo = (low nibble of key a, low nibble of key b) of byte 8g + 4w + i
           const uint32_t zlo_ab = (xa & 0x0F0F0F0Fu) | ((xb << 4) & 0xF0F0F0F0u);
           const uint32_t zhi_ab = ((xa >> 4) & 0x0F0F0F0Fu) | (xb & 0xF0F0F0F0u);
           const uint32_t zlo_cd = (xc & 0x0F0F0F0Fu) | ((xd << 4) & 0xF0F0F0F0u);
           const uint32_t zhi_cd = ((xc >> 4) & 0x0F0F0F0Fu) | (xd & 0xF0F0F0F0u);
           uint32_t r0[4], r1[4], r2[4], r3[4];
-          if (w < VPRMT) {
-            decode4<true>(tbl_lane, zlo_ab, vlo, vhi, r0);
-            decode4<true>(tbl_lane, zhi_ab, vlo, vhi, r1);
-            decode4<true>(tbl_lane, zlo_cd, vlo, vhi, r2);
-            decode4<true>(tbl_lane, zhi_cd, vlo, vhi, r3);
+          if (w < VP) {
+            decode4<true>(lut_base, vword, zlo_ab, vlo, vhi, r0);
+            decode4<true>(lut_base, vword, zhi_ab, vlo, vhi, r1);
+            decode4<true>(lut_base, vword, zlo_cd, vlo, vhi, r2);
+            decode4<true>(lut_base, vword, zhi_cd, vlo, vhi, r3);
           } else {
-            decode4<false>(tbl_lane, zlo_ab, vlo, vhi, r0);
-            decode4<false>(tbl_lane, zhi_ab, vlo, vhi, r1);
-            decode4<false>(tbl_lane, zlo_cd, vlo, vhi, r2);
-            decode4<false>(tbl_lane, zhi_cd, vlo, vhi, r3);
+            decode4<false>(lut_base, vword, zlo_ab, vlo, vhi, r0);
+            decode4<false>(lut_base, vword, zhi_ab, vlo, vhi, r1);
+            decode4<false>(lut_base, vword, zlo_cd, vlo, vhi, r2);
+            decode4<false>(lut_base, vword, zhi_cd, vlo, vhi, r3);
           }
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -457,7 +481,7 @@ __global__ void __launch_bounds__(NTHREADS) __maxnreg__(NG == 1 ? 112 : 168) k_p
     }
   }
   __syncthreads();
-  float *osm = reinterpret_cast<float *>(&sm.kbuf[0][0]);  // [CWARPS][8 heads][128]
+  float *osm = reinterpret_cast<float *>(&sm.kbuf[0][0]);  // [CWARPS][8 heads][128], spans kbuf+vbuf
   if (warp < CWARPS) {
 #pragma unroll
     for (int c = 0; c < NG; ++c) {
@@ -588,16 +612,20 @@ cudaError_t launch_prepare_q(const tq_ctx *k, const void *q, int q_dtype, const 
 template <int NG, bool SC, int KP, int VP>
 cudaError_t launch_t4(const PartialParams &p, dim3 grid, cudaStream_t st) {
   const size_t smem = sizeof(SmemPartial);
-  cudaError_t e = cudaFuncSetAttribute(k_partial_t4<NG, SC, KP, VP>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto kern = k_partial_t4<NG, SC, KP, VP>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  k_partial_t4<NG, SC, KP, VP><<<grid, NTHREADS, smem, st>>>(p);
+  kern<<<grid, NTHREADS, smem, st>>>(p);
   return cudaGetLastError();
 }
 
-// Decode-word split between the table (shared-memory pipe) and byte permutes (ALU pipe).
-constexpr int K_PRMT_WORDS = 0;   // of 4 key words per key and thread
-constexpr int V_PRMT_WORDS = 1;   // of 2 value words per key pair and thread
+// Decode-word split between the table (shared-memory pipe) and byte permutes (ALU pipe):
+// of the 4 key words and 2 value words a lane decodes per 16-key block.
+constexpr int K_PRMT_WORDS = 1;
+constexpr int V_PRMT_WORDS = 0;
 
 cudaError_t launch_partial(const tq_ctx *k, const tq_ctx *v, const uint8_t *kc,
                            const uint8_t *vc, const int32_t *seq_lens, const DecodeShape &s,
@@ -611,17 +639,14 @@ cudaError_t launch_partial(const tq_ctx *k, const tq_ctx *v, const uint8_t *kc,
     p.klo[i] = k->f16.lo[i], p.khi[i] = k->f16.hi[i];
     p.vlo[i] = v->f16.lo[i], p.vhi[i] = v->f16.hi[i];
   }
-  for (int i = 0; i < 8; ++i) p.c16[i] = k->f16.c16[i];
+  for (int i = 0; i < 8; ++i) p.kc16[i] = k->f16.c16[i], p.vc16[i] = v->f16.c16[i];
   p.status = k->d_status;
   dim3 grid(s.n_split, s.B * s.Hkv * s.n_hg);
-  const bool same_table = std::memcmp(k->f16.c16, v->f16.c16, sizeof(k->f16.c16)) == 0;
-  const bool two = s.heads_per_cta == 8;
-  if (!same_table) {  // the value codebook is not the table's: values by byte permutes only
-    if (two) return scores_dbg ? launch_t4<2, true, K_PRMT_WORDS, 2>(p, grid, st) : launch_t4<2, false, K_PRMT_WORDS, 2>(p, grid, st);
-    return scores_dbg ? launch_t4<1, true, K_PRMT_WORDS, 2>(p, grid, st) : launch_t4<1, false, K_PRMT_WORDS, 2>(p, grid, st);
-  }
-  if (two) return scores_dbg ? launch_t4<2, true, K_PRMT_WORDS, V_PRMT_WORDS>(p, grid, st) : launch_t4<2, false, K_PRMT_WORDS, V_PRMT_WORDS>(p, grid, st);
-  return scores_dbg ? launch_t4<1, true, K_PRMT_WORDS, V_PRMT_WORDS>(p, grid, st) : launch_t4<1, false, K_PRMT_WORDS, V_PRMT_WORDS>(p, grid, st);
+  if (s.heads_per_cta == 8)
+    return scores_dbg ? launch_t4<2, true, K_PRMT_WORDS, V_PRMT_WORDS>(p, grid, st)
+                      : launch_t4<2, false, K_PRMT_WORDS, V_PRMT_WORDS>(p, grid, st);
+  return scores_dbg ? launch_t4<1, true, K_PRMT_WORDS, V_PRMT_WORDS>(p, grid, st)
+                    : launch_t4<1, false, K_PRMT_WORDS, V_PRMT_WORDS>(p, grid, st);
 }
 
 cudaError_t launch_combine(const tq_ctx *k, const tq_ctx *v, const DecodeShape &s, float *out,
