@@ -214,9 +214,12 @@ tq_status tq_ctx_create(const tq_params *params, tq_ctx **out) {
       s = to_device(&c->d_pit, rt.data(), rt.size());
     }
     if (s == TQ_OK && p.format == TQ_FMT_PROD3) {
-      std::vector<float> S((size_t)D * D);
+      std::vector<float> S((size_t)D * D), St((size_t)D * D);
       tq_make_qjl_matrix(D, p.qjl_seed, S.data());
+      for (int i = 0; i < D; ++i)
+        for (int j = 0; j < D; ++j) St[(size_t)j * D + i] = S[(size_t)i * D + j];
       s = to_device(&c->d_S, S.data(), S.size());
+      if (s == TQ_OK) s = to_device(&c->d_St, St.data(), St.size());
     }
   }
   if (s == TQ_OK) {
@@ -237,6 +240,7 @@ tq_status tq_ctx_destroy(tq_ctx *ctx) {
   cudaFree(ctx->d_pi);
   cudaFree(ctx->d_pit);
   cudaFree(ctx->d_S);
+  cudaFree(ctx->d_St);
   cudaFree(ctx->d_status);
   delete ctx;
   return TQ_OK;

@@ -83,37 +83,59 @@ struct QprepParams {
   float *qsc;
 };
 
-constexpr int QWARPS = 8;
+constexpr int QWARPS = 8;  // queries per CTA, one warp each
 
+// Stage a 128 x 128 fp32 matrix in shared memory with 16-byte loads, all in flight.
+__device__ __forceinline__ void stage_matrix(float *dst, const float *src) {
+  const float4 *s4 = reinterpret_cast<const float4 *>(src);
+  float4 *d4 = reinterpret_cast<float4 *>(dst);
+  constexpr int N4 = D * D / 4;
+  constexpr int PER = N4 / (QWARPS * 32);
+  float4 v[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) v[i] = s4[threadIdx.x + i * QWARPS * 32];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) d4[threadIdx.x + i * QWARPS * 32] = v[i];
+}
+
+// q_rot = R q for 8 queries per CTA: R^T staged once in shared memory, lane l of
+// warp w computes q_rot[l + 32 m] of query w.
 __global__ void __launch_bounds__(QWARPS * 32) k_prepare_q(const QprepParams p) {
-  __shared__ __align__(16) float qv[QWARPS][D];
-  __shared__ __align__(16) __half hs[QWARPS][2][D];
+  extern __shared__ __align__(16) float qsm[];
+  float *rt = qsm;                       // [128][128]
+  float *qv = qsm + D * D;               // [QWARPS][128]
+  __half *hs = reinterpret_cast<__half *>(qv + QWARPS * D);  // [QWARPS][2][128]
+  stage_matrix(rt, p.rt);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qi = blockIdx.x * QWARPS + warp;
-  if (qi >= p.n_q) return;
-  float x[4];
-  if (p.q_dtype == TQ_DTYPE_F32) {
-    const float4 v = reinterpret_cast<const float4 *>(p.q)[(size_t)qi * 32 + lane];
-    x[0] = v.x, x[1] = v.y, x[2] = v.z, x[3] = v.w;
-  } else {
-    const uint2 v = reinterpret_cast<const uint2 *>(p.q)[(size_t)qi * 32 + lane];
-    const uint32_t w[4] = {v.x & 0xFFFFu, v.x >> 16, v.y & 0xFFFFu, v.y >> 16};
+  const bool live = qi < p.n_q;
+  float x[4] = {0.f, 0.f, 0.f, 0.f};
+  if (live) {
+    if (p.q_dtype == TQ_DTYPE_F32) {
+      const float4 v = reinterpret_cast<const float4 *>(p.q)[(size_t)qi * 32 + lane];
+      x[0] = v.x, x[1] = v.y, x[2] = v.z, x[3] = v.w;
+    } else {
+      const uint2 v = reinterpret_cast<const uint2 *>(p.q)[(size_t)qi * 32 + lane];
+      const uint32_t w[4] = {v.x & 0xFFFFu, v.x >> 16, v.y & 0xFFFFu, v.y >> 16};
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      if (p.q_dtype == TQ_DTYPE_BF16) {
-        x[e] = bf16_bits_to_f32(w[e]);
-      } else {
-        const unsigned short us = (unsigned short)w[e];
-        x[e] = __half2float(*reinterpret_cast<const __half *>(&us));
+      for (int e = 0; e < 4; ++e) {
+        if (p.q_dtype == TQ_DTYPE_BF16) {
+          x[e] = bf16_bits_to_f32(w[e]);
+        } else {
+          const unsigned short us = (unsigned short)w[e];
+          x[e] = __half2float(*reinterpret_cast<const __half *>(&us));
+        }
       }
     }
   }
-  *reinterpret_cast<float4 *>(&qv[warp][4 * lane]) = make_float4(x[0], x[1], x[2], x[3]);
-  __syncwarp();
+  *reinterpret_cast<float4 *>(&qv[warp * D + 4 * lane]) = make_float4(x[0], x[1], x[2], x[3]);
+  __syncthreads();
+  if (!live) return;
   float y[4] = {0.f, 0.f, 0.f, 0.f};  // q_rot[j], j = lane + 32 m
+#pragma unroll 8
   for (int k = 0; k < D; ++k) {
-    const float qk = qv[warp][k];
-    const float *row = p.rt + k * D + lane;
+    const float qk = qv[warp * D + k];
+    const float *row = rt + k * D + lane;
 #pragma unroll
     for (int m = 0; m < 4; ++m) y[m] = fmaf(row[32 * m], qk, y[m]);
   }
@@ -127,16 +149,17 @@ __global__ void __launch_bounds__(QWARPS * 32) k_prepare_q(const QprepParams p) 
   for (int h = 16; h >= 1; h >>= 1) amax = fmaxf(amax, __shfl_xor_sync(FULL_MASK, amax, h));
   int e = 0;
   if (amax > 0.f && isfinite(amax)) e = ilogbf(amax) - 13;  // amax * 2^-e in [2^13, 2^14)
+  __half *hw = hs + warp * 2 * D;
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
     const float v = ldexpf(y[m], -e);
     const __half h = __float2half_rn(v);
-    hs[warp][0][lane + 32 * m] = h;
-    hs[warp][1][lane + 32 * m] = __float2half_rn(v - __half2float(h));
+    hw[lane + 32 * m] = h;
+    hw[D + lane + 32 * m] = __float2half_rn(v - __half2float(h));
   }
   __syncwarp();
   uint32_t *dst = p.qhl + (size_t)qi * 256;
-  const uint32_t *src = reinterpret_cast<const uint32_t *>(&hs[warp][0][0]);
+  const uint32_t *src = reinterpret_cast<const uint32_t *>(hw);
 #pragma unroll
   for (int i = 0; i < 4; ++i) dst[lane + 32 * i] = src[lane + 32 * i];
   if (lane == 0) {
@@ -524,36 +547,78 @@ __global__ void __launch_bounds__(NTHREADS) __maxnreg__(NG == 1 ? 128 : 168)
 
 struct CombineParams {
   const float *part;
+  int n_heads;      // B * Hq
   int n_split;
   const float *r;   // R (row-major) of the value rotation, or null
   float inv_vscale; // 1 / (2^14 * alpha_V)
   float *out;
 };
 
-__global__ void __launch_bounds__(D) k_combine(const CombineParams p) {
-  __shared__ float o[D];
-  const int bh = blockIdx.x, j = threadIdx.x;
-  const float *part = p.part + (size_t)bh * p.n_split * PARTIAL_FLOATS;
-  float ms = -INFINITY;
-  for (int s = 0; s < p.n_split; ++s)
-    if (part[s * PARTIAL_FLOATS + 1] > 0.f) ms = fmaxf(ms, part[s * PARTIAL_FLOATS]);
-  float lsum = 0.f, acc = 0.f;
-  for (int s = 0; s < p.n_split; ++s) {
-    const float *ps = part + s * PARTIAL_FLOATS;
-    if (ps[1] > 0.f) {
-      const float w = exp2f(ps[0] - ms);
-      lsum += w * ps[1];
-      acc += w * ps[6 + j];
+// Merge the splits of 8 heads per CTA (one warp each): m* = max m_s,
+// l* = sum l_s 2^(m_s - m*), o = sum acc_s 2^(m_s - m*) / l*, then out = R^T o with R
+// staged once per CTA.
+__global__ void __launch_bounds__(QWARPS * 32) k_combine(const CombineParams p) {
+  extern __shared__ __align__(16) float csm[];
+  float *r = csm;              // [128][128]
+  float *o = csm + D * D;      // [QWARPS][128]
+  if (p.r) stage_matrix(r, p.r);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.x * QWARPS + warp;
+  const bool live = bh < p.n_heads;
+  if (live) {
+    const float *part = p.part + (size_t)bh * p.n_split * PARTIAL_FLOATS;
+    float ms = -INFINITY;
+    for (int s = lane; s < p.n_split; s += 32) {
+      const float *ps = part + (size_t)s * PARTIAL_FLOATS;
+      if (ps[1] > 0.f) ms = fmaxf(ms, ps[0]);
     }
+#pragma unroll
+    for (int h = 16; h >= 1; h >>= 1) ms = fmaxf(ms, __shfl_xor_sync(FULL_MASK, ms, h));
+    float lsum = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int s0 = 0; s0 < p.n_split; s0 += 32) {
+      const int s = s0 + lane;
+      float w = 0.f;
+      if (s < p.n_split) {
+        const float *ps = part + (size_t)s * PARTIAL_FLOATS;
+        if (ps[1] > 0.f) {
+          w = exp2f(ps[0] - ms);
+          lsum += w * ps[1];
+        }
+      }
+      const int n = min(32, p.n_split - s0);
+      for (int i = 0; i < n; ++i) {
+        const float wi = __shfl_sync(FULL_MASK, w, i);
+        if (wi != 0.f) {
+          const float *ps = part + (size_t)(s0 + i) * PARTIAL_FLOATS + 6;
+#pragma unroll
+          for (int m = 0; m < 4; ++m) acc[m] = fmaf(wi, ps[lane + 32 * m], acc[m]);
+        }
+      }
+    }
+#pragma unroll
+    for (int h = 16; h >= 1; h >>= 1) lsum += __shfl_xor_sync(FULL_MASK, lsum, h);
+    const float f = p.inv_vscale / lsum;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) o[warp * D + lane + 32 * m] = acc[m] * f;
   }
-  o[j] = acc * p.inv_vscale / lsum;
   __syncthreads();
-  float r = o[j];
+  if (!live) return;
+  float res[4];
   if (p.r) {
-    r = 0.f;
-    for (int k = 0; k < D; ++k) r = fmaf(p.r[k * D + j], o[k], r);  // (R^T o)_j
+    res[0] = res[1] = res[2] = res[3] = 0.f;
+#pragma unroll 8
+    for (int k = 0; k < D; ++k) {
+      const float ok = o[warp * D + k];
+      const float *row = r + k * D + lane;  // (R^T o)_j = sum_k R[k][j] o_k
+#pragma unroll
+      for (int m = 0; m < 4; ++m) res[m] = fmaf(row[32 * m], ok, res[m]);
+    }
+  } else {
+#pragma unroll
+    for (int m = 0; m < 4; ++m) res[m] = o[warp * D + lane + 32 * m];
   }
-  p.out[(size_t)bh * D + j] = r;
+#pragma unroll
+  for (int m = 0; m < 4; ++m) p.out[(size_t)bh * D + lane + 32 * m] = res[m];
 }
 
 }  // namespace
@@ -605,7 +670,10 @@ cudaError_t launch_prepare_q(const tq_ctx *k, const void *q, int q_dtype, const 
   p.qhl = ws.qhl;
   p.qsc = ws.qsc;
   const int grid = (p.n_q + QWARPS - 1) / QWARPS;
-  k_prepare_q<<<grid, QWARPS * 32, 0, st>>>(p);
+  const size_t smem = (size_t)D * D * 4 + QWARPS * D * 4 + QWARPS * 2 * D * 2;
+  cudaError_t e = cudaFuncSetAttribute(k_prepare_q, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  k_prepare_q<<<grid, QWARPS * 32, smem, st>>>(p);
   return cudaGetLastError();
 }
 
@@ -654,11 +722,15 @@ cudaError_t launch_combine(const tq_ctx *k, const tq_ctx *v, const DecodeShape &
   (void)k;
   CombineParams p{};
   p.part = ws.partials;
+  p.n_heads = s.B * s.Hq;
   p.n_split = s.n_split;
   p.r = v->d_pi;
   p.inv_vscale = 1.0f / (exp2f(P_SHIFT) * v->f16.alpha);
   p.out = out;
-  k_combine<<<s.B * s.Hq, D, 0, st>>>(p);
+  const size_t smem = (size_t)D * D * 4 + QWARPS * D * 4;
+  cudaError_t e = cudaFuncSetAttribute(k_combine, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  k_combine<<<(p.n_heads + QWARPS - 1) / QWARPS, QWARPS * 32, smem, st>>>(p);
   return cudaGetLastError();
 }
 

@@ -47,6 +47,7 @@ struct tq_ctx {
   float *d_pi = nullptr;                // rotation R (dense Pi or the WHT matrix), fp32 row-major
   float *d_pit = nullptr;               // R^T, fp32 row-major
   float *d_S = nullptr;                 // QJL matrix S, fp32 [128][128] row-major
+  float *d_St = nullptr;                // S^T, fp32 row-major
   int32_t *d_status = nullptr;          // device status word
 };
 

