@@ -586,12 +586,22 @@ __global__ void __launch_bounds__(QWARPS * 32) k_combine(const CombineParams p) 
         }
       }
       const int n = min(32, p.n_split - s0);
-      for (int i = 0; i < n; ++i) {
-        const float wi = __shfl_sync(FULL_MASK, w, i);
-        if (wi != 0.f) {
-          const float *ps = part + (size_t)(s0 + i) * PARTIAL_FLOATS + 6;
+      for (int i0 = 0; i0 < n; i0 += 8) {  // eight splits' loads in flight at a time
+        float v[8][4];
 #pragma unroll
-          for (int m = 0; m < 4; ++m) acc[m] = fmaf(wi, ps[lane + 32 * m], acc[m]);
+        for (int i = 0; i < 8; ++i) {
+          const int si = min(s0 + i0 + i, p.n_split - 1);
+          const float *ps = part + (size_t)si * PARTIAL_FLOATS + 6;
+#pragma unroll
+          for (int m = 0; m < 4; ++m) v[i][m] = ps[lane + 32 * m];
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float wi = __shfl_sync(FULL_MASK, w, (i0 + i) & 31);
+          if (i0 + i < n) {
+#pragma unroll
+            for (int m = 0; m < 4; ++m) acc[m] = fmaf(wi, v[i][m], acc[m]);
+          }
         }
       }
     }

@@ -20,7 +20,6 @@ namespace {
 
 constexpr int WARPS = 8;
 constexpr int ROWBUF = 72;  // per-warp staging for one packed row (max 68 bytes)
-constexpr int64_t SMALL_BATCH_ROWS = 2048;
 
 struct WriteParams {
   const void *src;
@@ -173,23 +172,36 @@ __global__ void __launch_bounds__(WARPS * 32) k_write_wht(const WriteParams p) {
 }
 
 // ------------------------------------------------- dense rotation (CUDA-core matvec)
-// Pi (and S) staged in shared memory with a padded row stride of 129 floats so
-// that lane l working on row l + 32m and lane l reading column l + 32m are both
-// bank-conflict free.
-constexpr int PSTR = 129;
+// The matrices are staged once per CTA in shared memory, unpadded and in the
+// orientation that makes lane l's accesses for outputs l + 32 m consecutive:
+// R^T for y = R u, R for x_tilde = R^T y_hat, S^T for z = S r.  Staging issues all
+// 16-byte loads before the first store, so it costs one memory latency.
+__device__ __forceinline__ void stage128(float *dst, const float *src) {
+  const float4 *s4 = reinterpret_cast<const float4 *>(src);
+  float4 *d4 = reinterpret_cast<float4 *>(dst);
+  constexpr int PER = D * D / 4 / (WARPS * 32);
+  float4 v[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) v[i] = s4[threadIdx.x + i * WARPS * 32];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) d4[threadIdx.x + i * WARPS * 32] = v[i];
+}
 
 template <int FMT, int SRC>
 __global__ void __launch_bounds__(WARPS * 32) k_write_dense(const WriteParams p) {
   extern __shared__ __align__(16) float dsm[];
-  float *P = dsm;                                                    // [128][129]
-  float *S = P + D * PSTR;                                           // prod3 only
-  float *vec = S + (FMT == TQ_FMT_PROD3 ? D * PSTR : 0);             // [WARPS][3][128]
+  constexpr int NMAT = (FMT == TQ_FMT_PROD3) ? 3 : 1;
+  float *RT = dsm;                                                   // [128][128] R^T
+  float *Rm = dsm + D * D;                                           // prod3: R
+  float *ST = dsm + 2 * D * D;                                       // prod3: S^T
+  float *vec = dsm + NMAT * D * D;                                   // [WARPS][3][128]
   uint8_t *ib = reinterpret_cast<uint8_t *>(vec + WARPS * 3 * D);    // [WARPS][128] indices
   uint8_t *rowbuf = ib + WARPS * D;                                  // [WARPS][ROWBUF]
   float *sb = reinterpret_cast<float *>(rowbuf + WARPS * ROWBUF);    // [16]
-  for (int i = threadIdx.x; i < D * D; i += blockDim.x) {
-    P[(i >> 7) * PSTR + (i & 127)] = p.pi[i];
-    if (FMT == TQ_FMT_PROD3) S[(i >> 7) * PSTR + (i & 127)] = p.S[i];
+  stage128(RT, p.pit);
+  if (FMT == TQ_FMT_PROD3) {
+    stage128(Rm, p.pi);
+    stage128(ST, p.St);
   }
   if (threadIdx.x < 15) sb[threadIdx.x] = p.b[threadIdx.x];
   __syncthreads();
@@ -210,16 +222,12 @@ __global__ void __launch_bounds__(WARPS * 32) k_write_dense(const WriteParams p)
     *reinterpret_cast<float4 *>(u + 4 * lane) = make_float4(x[0], x[1], x[2], x[3]);
     __syncwarp();
     float y[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int k = 0; k < D; k += 4) {
-      const float4 uk = *reinterpret_cast<const float4 *>(u + k);
+#pragma unroll 8
+    for (int k = 0; k < D; ++k) {
+      const float uk = u[k];
+      const float *rt = RT + k * D + lane;  // (R u)_j = sum_k R^T[k][j] u_k
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const float *Pr = P + (lane + 32 * m) * PSTR + k;
-        y[m] = fmaf(Pr[0], uk.x, y[m]);
-        y[m] = fmaf(Pr[1], uk.y, y[m]);
-        y[m] = fmaf(Pr[2], uk.z, y[m]);
-        y[m] = fmaf(Pr[3], uk.w, y[m]);
-      }
+      for (int m = 0; m < 4; ++m) y[m] = fmaf(rt[32 * m], uk, y[m]);
     }
 #pragma unroll
     for (int m = 0; m < 4; ++m) myib[lane + 32 * m] = (uint8_t)bucket<NB>(y[m], sb);
@@ -237,101 +245,10 @@ __global__ void __launch_bounds__(WARPS * 32) k_write_dense(const WriteParams p)
     for (int m = 0; m < 4; ++m) yh[lane + 32 * m] = p.c[myib[lane + 32 * m]];
     __syncwarp();
     float r[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
     for (int k = 0; k < D; ++k) {
       const float yk = yh[k];
-#pragma unroll
-      for (int m = 0; m < 4; ++m) r[m] = fmaf(P[k * PSTR + lane + 32 * m], yk, r[m]);
-    }
-    float g2 = 0.f;
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      r[m] = u[lane + 32 * m] - r[m];
-      rr[lane + 32 * m] = r[m];
-      g2 = fmaf(r[m], r[m], g2);
-    }
-#pragma unroll
-    for (int h = 16; h >= 1; h >>= 1) g2 += __shfl_xor_sync(FULL_MASK, g2, h);
-    __syncwarp();
-    float z[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int k = 0; k < D; ++k) {
-      const float rk = rr[k];
-#pragma unroll
-      for (int m = 0; m < 4; ++m) z[m] = fmaf(S[(lane + 32 * m) * PSTR + k], rk, z[m]);
-    }
-    uint32_t sbits[4];
-#pragma unroll
-    for (int m = 0; m < 4; ++m) sbits[m] = __ballot_sync(FULL_MASK, z[m] >= 0.0f);
-    if (lane == 0) {
-      reinterpret_cast<float *>(buf)[0] = n;
-      reinterpret_cast<float *>(buf)[1] = sqrtf(g2);
-#pragma unroll
-      for (int m = 0; m < 4; ++m) reinterpret_cast<uint32_t *>(buf)[10 + m] = sbits[m];
-    }
-    buf[8 + lane] = (uint8_t)((idx[0] & 3) | ((idx[1] & 3) << 2) | ((idx[2] & 3) << 4) |
-                              ((idx[3] & 3) << 6));
-    __syncwarp();
-    if (lane < 14)
-      reinterpret_cast<uint32_t *>(p.dst + slot * 56)[lane] =
-          reinterpret_cast<const uint32_t *>(buf)[lane];
-    __syncwarp();
-  }
-}
-
-// ------------------------------------- dense rotation, few rows (matrices read from L2)
-// For the handful of rows a decode step writes, staging the 64 KB matrices per CTA
-// costs more than the rows: each warp streams R^T (and R, S^T for prod3) straight
-// from L2 with coalesced 128-byte rows.  Same arithmetic as k_write_dense.
-template <int FMT, int SRC>
-__global__ void __launch_bounds__(WARPS * 32) k_write_dense_l2(const WriteParams p) {
-  __shared__ __align__(16) float vec[WARPS][3][D];
-  __shared__ __align__(16) uint8_t ib[WARPS][D];
-  __shared__ __align__(16) uint8_t rowbuf[WARPS][ROWBUF];
-  __shared__ float sb[16];
-  if (threadIdx.x < 15) sb[threadIdx.x] = p.b[threadIdx.x];
-  __syncthreads();
-  constexpr int NB = (FMT == TQ_FMT_TURBO4) ? 15 : (FMT == TQ_FMT_TURBO3 ? 7 : 3);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float *u = vec[warp][0];
-  float *yh = vec[warp][1];
-  float *rr = vec[warp][2];
-  uint8_t *myib = ib[warp];
-  uint8_t *buf = rowbuf[warp];
-  for (int64_t row = (int64_t)blockIdx.x * WARPS + warp; row < p.n_rows;
-       row += (int64_t)gridDim.x * WARPS) {
-    int64_t slot;
-    if (!slot_of(p, row, lane, &slot)) continue;
-    float x[4];
-    load4<SRC>(p.src, row, p.stride, lane, x);
-    const float n = norm_normalize(x);
-    *reinterpret_cast<float4 *>(u + 4 * lane) = make_float4(x[0], x[1], x[2], x[3]);
-    __syncwarp();
-    float y[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-    for (int k = 0; k < D; ++k) {
-      const float uk = u[k];
-      const float *rt = p.pit + k * D + lane;  // (R u)_j = sum_k R^T[k][j] u_k
-#pragma unroll
-      for (int m = 0; m < 4; ++m) y[m] = fmaf(rt[32 * m], uk, y[m]);
-    }
-#pragma unroll
-    for (int m = 0; m < 4; ++m) myib[lane + 32 * m] = (uint8_t)bucket<NB>(y[m], sb);
-    __syncwarp();
-    uint32_t idx[4];
-    const uint32_t w4 = *reinterpret_cast<const uint32_t *>(myib + 4 * lane);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) idx[e] = (w4 >> (8 * e)) & 0xFF;
-    if (FMT != TQ_FMT_PROD3) {
-      pack_store_turbo<FMT>(idx, n, buf, p.dst + slot * (FMT == TQ_FMT_TURBO4 ? 68 : 56), lane);
-      continue;
-    }
-#pragma unroll
-    for (int m = 0; m < 4; ++m) yh[lane + 32 * m] = p.c[myib[lane + 32 * m]];
-    __syncwarp();
-    float r[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-    for (int k = 0; k < D; ++k) {
-      const float yk = yh[k];
-      const float *rk = p.pi + k * D + lane;  // (R^T y)_j = sum_k R[k][j] y_k
+      const float *rk = Rm + k * D + lane;  // (R^T y)_j = sum_k R[k][j] y_k
 #pragma unroll
       for (int m = 0; m < 4; ++m) r[m] = fmaf(rk[32 * m], yk, r[m]);
     }
@@ -346,10 +263,10 @@ __global__ void __launch_bounds__(WARPS * 32) k_write_dense_l2(const WriteParams
     for (int h = 16; h >= 1; h >>= 1) g2 += __shfl_xor_sync(FULL_MASK, g2, h);
     __syncwarp();
     float z[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
+#pragma unroll 8
     for (int k = 0; k < D; ++k) {
       const float rk = rr[k];
-      const float *st = p.St + k * D + lane;  // (S r)_i = sum_k S^T[k][i] r_k
+      const float *st = ST + k * D + lane;  // (S r)_i = sum_k S^T[k][i] r_k
 #pragma unroll
       for (int m = 0; m < 4; ++m) z[m] = fmaf(st[32 * m], rk, z[m]);
     }
@@ -465,22 +382,8 @@ cudaError_t launch_write(const tq_ctx *ctx, const WriteLaunch &w, cudaStream_t s
                 : launch_rows(k_write_wht<TQ_FMT_TURBO3, TQ_DTYPE_F32>, p, w.n_rows, sms, 0, 8, st);
   }
   // Dense rotation (prod3 always takes this path; its WHT variant multiplies by the
-  // materialised WHT matrix, which the context stores in d_pi as well).  Small batches
-  // (a decode step's new tokens) read the matrices from L2; large ones stage them.
-  if (w.n_rows <= SMALL_BATCH_ROWS) {
-    switch (fmt) {
-      case TQ_FMT_TURBO4:
-        return bf16 ? launch_rows(k_write_dense_l2<TQ_FMT_TURBO4, TQ_DTYPE_BF16>, p, w.n_rows, sms, 0, 8, st)
-                    : launch_rows(k_write_dense_l2<TQ_FMT_TURBO4, TQ_DTYPE_F32>, p, w.n_rows, sms, 0, 8, st);
-      case TQ_FMT_TURBO3:
-        return bf16 ? launch_rows(k_write_dense_l2<TQ_FMT_TURBO3, TQ_DTYPE_BF16>, p, w.n_rows, sms, 0, 8, st)
-                    : launch_rows(k_write_dense_l2<TQ_FMT_TURBO3, TQ_DTYPE_F32>, p, w.n_rows, sms, 0, 8, st);
-      default:
-        return bf16 ? launch_rows(k_write_dense_l2<TQ_FMT_PROD3, TQ_DTYPE_BF16>, p, w.n_rows, sms, 0, 8, st)
-                    : launch_rows(k_write_dense_l2<TQ_FMT_PROD3, TQ_DTYPE_F32>, p, w.n_rows, sms, 0, 8, st);
-    }
-  }
-  const size_t mats = (fmt == TQ_FMT_PROD3 ? 2 : 1) * (size_t)D * PSTR * sizeof(float);
+  // materialised WHT matrix, which the context stores as well).
+  const size_t mats = (fmt == TQ_FMT_PROD3 ? 3 : 1) * (size_t)D * D * sizeof(float);
   const size_t smem = mats + WARPS * 3 * D * sizeof(float) + WARPS * D + WARPS * ROWBUF +
                       16 * sizeof(float);
   const int per_sm = fmt == TQ_FMT_PROD3 ? 1 : 2;
