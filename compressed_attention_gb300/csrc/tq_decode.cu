@@ -279,12 +279,17 @@ __global__ void __launch_bounds__(NTHREADS) __maxnreg__(NG == 1 ? 128 : 168)
     sm.issued = 0;
     fence_mbar_init();
   }
-  for (int i = threadIdx.x; i < 256 * 64; i += NTHREADS) {
-    const int byte = i >> 6;
-    const uint32_t *c16 = (i & 32) ? p.vc16 : p.kc16;
+  // Fill the table: each (byte, half) entry is computed once and stored to its 32
+  // slots with 16-byte stores (512 pieces of 8 slots over the CTA's threads).
+  for (int piece = threadIdx.x; piece < 256 * 8; piece += NTHREADS) {
+    const int byte = piece >> 3, chunk = piece & 7;  // chunks 0-3: key slots, 4-7: value slots
+    const uint32_t *c16 = (chunk & 4) ? p.vc16 : p.kc16;
     const uint32_t lo = (c16[(byte & 15) >> 1] >> (16 * (byte & 1))) & 0xFFFFu;
     const uint32_t hi = (c16[(byte >> 4) >> 1] >> (16 * ((byte >> 4) & 1))) & 0xFFFFu;
-    sm.lut[byte][i & 63] = lo | (hi << 16);
+    const uint32_t e = lo | (hi << 16);
+    uint4 *dst = reinterpret_cast<uint4 *>(&sm.lut[byte][chunk * 8]);
+    dst[0] = make_uint4(e, e, e, e);
+    dst[1] = make_uint4(e, e, e, e);
   }
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
