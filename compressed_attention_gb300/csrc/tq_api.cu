@@ -85,8 +85,7 @@ tq_status check_decode_common(const tq_ctx *k, const tq_ctx *v, int B, int Hq, i
   if (Hq % Hkv != 0) return fail(TQ_ERR_INVALID_ARG, "Hq must be a multiple of Hkv");
   if (!decode_pair_supported(k, v))
     return fail(TQ_ERR_UNSUPPORTED, "no decode kernel for this (key, value) format pair");
-  decode_shape(k, v, B, Hq, Hkv, L, shape);
-  if ((int64_t)B * Hkv * shape->n_hg > 65535) return fail(TQ_ERR_UNSUPPORTED, "B * Hkv too large for one launch");
+  if (!decode_shape(k, v, B, Hq, Hkv, L, shape)) return fail(TQ_ERR_UNSUPPORTED, "shape too large");
   return TQ_OK;
 }
 
@@ -299,7 +298,7 @@ tq_status tq_decode_num_splits(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, 
   DecodeShape s;
   tq_status st = check_decode_common(k_ctx, v_ctx, B, Hq, Hkv, L, &s);
   if (st != TQ_OK) return st;
-  *n_split = s.n_split;
+  *n_split = s.n_part;
   return TQ_OK;
 }
 

@@ -38,12 +38,12 @@ namespace tq {
 
 namespace {
 
-constexpr int CWARPS = 7;             // consumer warps (16 keys each per tile)
-constexpr int TILE = 16 * CWARPS;     // keys per pipeline stage (112)
-constexpr int NTHREADS = (CWARPS + 1) * 32;  // + one producer warp: 8 warps, 2 CTAs per SM
-constexpr int NSTAGE = 3;             // pipeline depth
+constexpr int CWARPS = 15;            // consumer warps (16 keys each per tile)
+constexpr int TILE = 16 * CWARPS;     // keys per pipeline stage (240)
+constexpr int NTHREADS = (CWARPS + 1) * 32;  // + one producer warp; one CTA per SM
+constexpr int NSTAGE = 4;             // pipeline depth (about 128 KB in flight per SM)
 constexpr int T4_ROW = 68;
-constexpr int STAGE_BUF = 7648;       // >= 112 * 68 + 2 * 15, multiple of 32
+constexpr int STAGE_BUF = 16352;      // >= 240 * 68 + 2 * 15, multiple of 32
 constexpr float P_SHIFT = 14.0f;      // p' = 2^14 * exp2(.) keeps fp16 normal
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 constexpr float LOG2E = 1.4426950408889634f;
@@ -172,7 +172,8 @@ struct PartialParams {
   const uint8_t *kc;
   const uint8_t *vc;
   const int32_t *seq_lens;
-  int B, Hq, Hkv, L, gq, n_hg, n_split, chunk;
+  int B, Hq, Hkv, L, gq, n_hg;
+  int tiles_per_unit, tiles_per_cta, total_tiles, n_part;
   const uint32_t *qhl;
   const float *qsc;
   float *part;
@@ -186,21 +187,18 @@ struct PartialParams {
 // s >= 32 the value table; entry = (c[b & 15], c[b >> 4]) as fp16x2.  Lane l reads
 // slot l (keys) or 32 + l (values), so a warp's 32 lookups always hit 32 distinct
 // banks, and the byte offset (b << 8) | (4 * slot) is one byte permute away from
-// the packed word.  The stage buffers double as the merge area at the end.
+// the packed word.
 struct SmemPartial {
   uint32_t lut[256][64];
   uint8_t kbuf[NSTAGE][STAGE_BUF];
   uint8_t vbuf[NSTAGE][STAGE_BUF];
+  float osm[CWARPS][4][D];              // per-warp accumulators of 4 heads, for the merge
   uint64_t full[NSTAGE];
   uint64_t empty[NSTAGE];
   float mw[CWARPS][8];
   float lw[CWARPS][8];
   int abort_flag;
-  int first_unconsumed;
-  int issued;
 };
-static_assert(sizeof(float) * CWARPS * 8 * D <= 2 * NSTAGE * STAGE_BUF,
-              "merge area must fit in the stage buffers");
 
 // Table lookup of byte I of w: off = (byte << 8) | laneword.byte0.
 template <int I>
@@ -238,36 +236,47 @@ __device__ __forceinline__ int key_of_row(int r) {
   return ((r & 1) | ((r & 2) << 2) | ((r & 4) >> 1) | ((r & 8) >> 1));
 }
 
-// One CTA = (batch b, KV head, group of up to 4*NG q-heads, key split).  Lane
-// (g, t) = (lane / 4, lane % 4) of a consumer warp owns, per 16-key block, score
-// rows g and g+8 (head t of every column group) and dims 16g..16g+15 of the PV
-// product.  KP of the 4 key words and VP of the 2 value words per lane are decoded
-// by byte permutes instead of the table, to balance the ALU and shared-memory pipes.
+// Barrier over the consumer warps only (the producer warp never joins it).
+__device__ __forceinline__ void consumers_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(CWARPS * 32) : "memory");
+}
+
+// Work item = the tiles of one unit (batch, KV head, head group) inside this CTA's
+// contiguous range of the global tile sequence; units are laid end to end, so a CTA
+// touches at most a few units and each (unit, CTA) pair gives one partial.
+struct Item {
+  int unit, t0, t1, slot;  // tiles [t0, t1) of the unit; partial slot of this CTA
+};
+__device__ __forceinline__ bool next_item(const PartialParams &p, int cta, int &t, Item &it) {
+  const int end = min((cta + 1) * p.tiles_per_cta, p.total_tiles);
+  if (t >= end) return false;
+  it.unit = t / p.tiles_per_unit;
+  it.t0 = t - it.unit * p.tiles_per_unit;
+  it.t1 = min(end - it.unit * p.tiles_per_unit, p.tiles_per_unit);
+  it.slot = cta - (it.unit * p.tiles_per_unit) / p.tiles_per_cta;
+  t += it.t1 - it.t0;
+  return true;
+}
+
+__device__ __forceinline__ int unit_len(const PartialParams &p, int unit) {
+  const int b = unit / (p.Hkv * p.n_hg);
+  if (!p.seq_lens) return p.L;
+  const int v = p.seq_lens[b];
+  return v < 1 ? 1 : (v > p.L ? p.L : v);
+}
+
+// Persistent split-K decode: one CTA per SM streams its tile range through a ring of
+// NSTAGE stages.  Lane (g, t) = (lane / 4, lane % 4) of a consumer warp owns, per
+// 16-key block, score rows g and g+8 (head t of every column group) and dims
+// 16g..16g+15 of the PV product.  KP of the 4 key words and VP of the 2 value words
+// per lane are decoded by byte permutes instead of the table, to balance the ALU and
+// shared-memory pipes.
 template <int NG, bool SCORES, int KP, int VP>
-__global__ void __launch_bounds__(NTHREADS) __maxnreg__(NG == 1 ? 128 : 168)
+__global__ void __launch_bounds__(NTHREADS, 1) __maxnreg__(NG == 1 ? 128 : 128)
     k_partial_t4(const PartialParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   SmemPartial &sm = *reinterpret_cast<SmemPartial *>(smem_raw);
-  const int split = blockIdx.x;
-  const int unit = blockIdx.y;
-  const int hg = unit % p.n_hg;
-  const int bk = unit / p.n_hg;  // b * Hkv + kv-head
-  const int b = bk / p.Hkv, kvh = bk % p.Hkv;
-  int Lb = p.L;
-  if (p.seq_lens) {
-    int v = p.seq_lens[b];
-    if (v < 1 || v > p.L) {
-      if (threadIdx.x == 0) atomicExch(p.status, (int32_t)DEVERR_SEQLEN);
-      v = v < 1 ? 1 : p.L;
-    }
-    Lb = v;
-  }
-  const int key0 = split * p.chunk;
-  const int nkeys = max(0, min(key0 + p.chunk, Lb) - key0);
-  const int ntiles = (nkeys + TILE - 1) / TILE;
-  const int G = min(4 * NG, p.gq - hg * 4 * NG);  // valid q-heads in this group
-  const int head0 = kvh * p.gq + hg * 4 * NG;
-  const size_t unit_row0 = (size_t)bk * p.L;
+  const int cta = blockIdx.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
@@ -275,12 +284,14 @@ __global__ void __launch_bounds__(NTHREADS) __maxnreg__(NG == 1 ? 128 : 168)
       mbar_init(&sm.empty[s], CWARPS);
     }
     sm.abort_flag = 0;
-    sm.first_unconsumed = ntiles;
-    sm.issued = 0;
     fence_mbar_init();
   }
+  if (threadIdx.x == 0 && p.seq_lens) {
+    for (int b = 0; b < p.B; ++b)
+      if (p.seq_lens[b] < 1 || p.seq_lens[b] > p.L) atomicExch(p.status, (int32_t)DEVERR_SEQLEN);
+  }
   // Fill the table: each (byte, half) entry is computed once and stored to its 32
-  // slots with 16-byte stores (512 pieces of 8 slots over the CTA's threads).
+  // slots with 16-byte stores.
   for (int piece = threadIdx.x; piece < 256 * 8; piece += NTHREADS) {
     const int byte = piece >> 3, chunk = piece & 7;  // chunks 0-3: key slots, 4-7: value slots
     const uint32_t *c16 = (chunk & 4) ? p.vc16 : p.kc16;
@@ -295,85 +306,114 @@ __global__ void __launch_bounds__(NTHREADS) __maxnreg__(NG == 1 ? 128 : 168)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
 
-  float O[NG][8][4];
-  float M[NG], lsum[NG];
-#pragma unroll
-  for (int c = 0; c < NG; ++c) {
-    M[c] = -INFINITY;
-    lsum[c] = 0.f;
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) O[c][mt][0] = O[c][mt][1] = O[c][mt][2] = O[c][mt][3] = 0.f;
+  if (warp == CWARPS) {
+    // ---------------- producer: one elected lane streams every tile of every item
+    if (lane == 0) {
+      int ctr = 0, tt = cta * p.tiles_per_cta;
+      Item it;
+      bool ok = true;
+      while (ok && next_item(p, cta, tt, it)) {
+        const int Lb = unit_len(p, it.unit);
+        const size_t unit_row0 = (size_t)(it.unit / p.n_hg) * p.L;
+        for (int j = it.t0; j < it.t1; ++j) {
+          const int kf = j * TILE;
+          if (kf >= Lb) break;  // consumers skip the same tiles
+          const int nk = min(TILE, Lb - kf);
+          const int s = ctr % NSTAGE;
+          if (ctr >= NSTAGE &&
+              !mbar_wait_bounded(&sm.empty[s], ((ctr / NSTAGE) - 1) & 1, WAIT_LIMIT_NS)) {
+            atomicExch(&sm.abort_flag, 1);
+            atomicExch(p.status, (int32_t)DEVERR_TIMEOUT);
+            ok = false;
+            break;
+          }
+          const size_t start = (unit_row0 + kf) * T4_ROW;
+          const size_t a0 = start & ~(size_t)15;
+          const size_t a1 = (start + (size_t)nk * T4_ROW + 15) & ~(size_t)15;
+          const uint32_t bytes = (uint32_t)(a1 - a0);
+          mbar_arrive_expect_tx(&sm.full[s], 2 * bytes);
+          bulk_g2s(sm.kbuf[s], p.kc + a0, bytes, &sm.full[s]);
+          bulk_g2s(sm.vbuf[s], p.vc + a0, bytes, &sm.full[s]);
+          ++ctr;
+        }
+      }
+      // Let every issued copy land before the CTA can exit (only matters after a
+      // bounded wait gave up; otherwise the consumers have consumed them all).
+      if (!ok || sm.abort_flag) {
+        for (int c = (ctr > NSTAGE ? ctr - NSTAGE : 0); c < ctr; ++c)
+          (void)mbar_wait_bounded(&sm.full[c % NSTAGE], (c / NSTAGE) & 1, WAIT_LIMIT_NS);
+      }
+    }
+    return;
   }
 
-  if (warp == CWARPS) {
-    // ---------------- producer: one elected lane streams K and V tiles
-    if (lane == 0) {
-      int i = 0;
-      for (; i < ntiles; ++i) {
-        const int s = i % NSTAGE;
-        if (i >= NSTAGE && !mbar_wait_bounded(&sm.empty[s], ((i / NSTAGE) - 1) & 1, WAIT_LIMIT_NS)) {
-          atomicExch(&sm.abort_flag, 1);
-          atomicExch(p.status, (int32_t)DEVERR_TIMEOUT);
-          break;
-        }
-        const int kf = key0 + i * TILE;
-        const int nk = min(TILE, nkeys - i * TILE);
-        const size_t start = (unit_row0 + kf) * T4_ROW;
-        const size_t a0 = start & ~(size_t)15;
-        const size_t a1 = (start + (size_t)nk * T4_ROW + 15) & ~(size_t)15;
-        const uint32_t bytes = (uint32_t)(a1 - a0);
-        mbar_arrive_expect_tx(&sm.full[s], 2 * bytes);
-        bulk_g2s(sm.kbuf[s], p.kc + a0, bytes, &sm.full[s]);
-        bulk_g2s(sm.vbuf[s], p.vc + a0, bytes, &sm.full[s]);
-      }
-      sm.issued = i;
-    }
-  } else {
-    // ---------------- consumers
+  // ---------------- consumers
+  const uint8_t *lut_base = reinterpret_cast<const uint8_t *>(&sm.lut[0][0]);
+  const uint32_t kword = 4u * lane, vword = 128u + 4u * lane;
+  const uint32_t klo[2] = {p.klo[0], p.klo[1]}, khi[2] = {p.khi[0], p.khi[1]};
+  const uint32_t vlo[2] = {p.vlo[0], p.vlo[1]}, vhi[2] = {p.vhi[0], p.vhi[1]};
+  const int kb = warp * 16;
+  const int rk0 = key_of_row(g), rk1 = key_of_row(g + 8);
+  const int at = (t & 1) | ((t & 2) << 2);  // a_t = 0, 1, 8, 9
+  const int hs = g >> 1;
+  const int src0 = 4 * t + hs, src1 = 4 * (4 + t) + hs;
+  const float lo_sel = (g & 1) ? 1.f : 0.f;
+
+  int ctr = 0, tt = cta * p.tiles_per_cta;
+  Item it;
+  bool aborted = false;
+  while (!aborted && next_item(p, cta, tt, it)) {
+    const int Lb = unit_len(p, it.unit);
+    const int hg = it.unit % p.n_hg;
+    const int bk = it.unit / p.n_hg;
+    const int b = bk / p.Hkv, kvh = bk % p.Hkv;
+    const int G = min(4 * NG, p.gq - hg * 4 * NG);
+    const int head0 = kvh * p.gq + hg * 4 * NG;
+    const size_t unit_row0 = (size_t)bk * p.L;
+
     // q as the B operand: column g = (head slot g/2, part g%2 = hi/lo), rows = dims.
     uint32_t qb[NG][8][2];
     float qs[NG];
-    {
-      const int hs = g >> 1, part = g & 1;
 #pragma unroll
-      for (int c = 0; c < NG; ++c) {
-        const int slot = c * 4 + hs;
-        if (slot < G) {
-          const uint32_t *qw = p.qhl + (size_t)(b * p.Hq + head0 + slot) * 256 + part * 64 + 16 * t;
+    for (int c = 0; c < NG; ++c) {
+      const int slot = c * 4 + hs;
+      if (slot < G) {
+        const uint32_t *qw = p.qhl + (size_t)(b * p.Hq + head0 + slot) * 256 + (g & 1) * 64 + 16 * t;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            qb[c][kk][0] = qw[2 * kk];
-            qb[c][kk][1] = qw[2 * kk + 1];
-          }
-        } else {
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) qb[c][kk][0] = qb[c][kk][1] = 0u;
+        for (int kk = 0; kk < 8; ++kk) {
+          qb[c][kk][0] = qw[2 * kk];
+          qb[c][kk][1] = qw[2 * kk + 1];
         }
-        const int my = c * 4 + t;  // the head whose scores this lane holds
-        qs[c] = (my < G) ? p.qsc[2 * (b * p.Hq + head0 + my)] : 0.f;
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) qb[c][kk][0] = qb[c][kk][1] = 0u;
       }
+      const int my = c * 4 + t;  // the head whose scores this lane holds
+      qs[c] = (my < G) ? p.qsc[2 * (b * p.Hq + head0 + my)] : 0.f;
     }
-    const uint8_t *lut_base = reinterpret_cast<const uint8_t *>(&sm.lut[0][0]);
-    const uint32_t kword = 4u * lane, vword = 128u + 4u * lane;
-    const uint32_t klo[2] = {p.klo[0], p.klo[1]}, khi[2] = {p.khi[0], p.khi[1]};
-    const uint32_t vlo[2] = {p.vlo[0], p.vlo[1]}, vhi[2] = {p.vhi[0], p.vhi[1]};
-    const int kb = warp * 16;
-    const int rk0 = key_of_row(g), rk1 = key_of_row(g + 8);
-    const int at = (t & 1) | ((t & 2) << 2);  // a_t = 0, 1, 8, 9
-    const int hs = g >> 1;
-    const int src0 = 4 * t + hs, src1 = 4 * (4 + t) + hs;
-    const float lo_sel = (g & 1) ? 1.f : 0.f;
+    float O[NG][8][4];
+    float M[NG], lsum[NG];
+#pragma unroll
+    for (int c = 0; c < NG; ++c) {
+      M[c] = -INFINITY;
+      lsum[c] = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) O[c][mt][0] = O[c][mt][1] = O[c][mt][2] = O[c][mt][3] = 0.f;
+    }
 
-    for (int i = 0; i < ntiles; ++i) {
-      const int s = i % NSTAGE;
-      if (!mbar_wait_bounded(&sm.full[s], (i / NSTAGE) & 1, WAIT_LIMIT_NS)) {
-        atomicExch(&sm.abort_flag, 1);
-        atomicMin(&sm.first_unconsumed, i);
-        if (lane == 0) atomicExch(p.status, (int32_t)DEVERR_TIMEOUT);
+    for (int j = it.t0; j < it.t1; ++j) {
+      const int kf = j * TILE;
+      if (kf >= Lb) break;
+      const int s = ctr % NSTAGE;
+      if (!mbar_wait_bounded(&sm.full[s], (ctr / NSTAGE) & 1, WAIT_LIMIT_NS)) {
+        if (lane == 0) {
+          atomicExch(p.status, (int32_t)DEVERR_TIMEOUT);
+          atomicExch(&sm.abort_flag, 1);
+        }
+        aborted = true;
         break;
       }
-      const int kf = key0 + i * TILE;
-      const int nk = min(TILE, nkeys - i * TILE);
+      const int nk = min(TILE, Lb - kf);
       const size_t start = (unit_row0 + kf) * T4_ROW;
       const uint8_t *Ks = sm.kbuf[s] + (start & 15) + kb * T4_ROW;
       const uint8_t *Vs = sm.vbuf[s] + (start & 15) + kb * T4_ROW;
@@ -477,75 +517,71 @@ __global__ void __launch_bounds__(NTHREADS) __maxnreg__(NG == 1 ? 128 : 168)
             decode4<false>(lut_base, vword, zhi_cd, vlo, vhi, r3);
           }
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t a[4] = {r0[j], r1[j], r2[j], r3[j]};
+          for (int jj = 0; jj < 4; ++jj) {
+            const uint32_t a[4] = {r0[jj], r1[jj], r2[jj], r3[jj]};
 #pragma unroll
-            for (int c = 0; c < NG; ++c) mma_f16(O[c][4 * w + j], a, pb[c][0], pb[c][1]);
+            for (int c = 0; c < NG; ++c) mma_f16(O[c][4 * w + jj], a, pb[c][0], pb[c][1]);
           }
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.empty[s]);
+      ++ctr;
     }
+    // A warp that gave up waiting has set the flag before any warp can get here past
+    // the same tile, so either every consumer warp enters the merge barriers or none.
+    if (aborted || *reinterpret_cast<volatile int *>(&sm.abort_flag)) break;
 #pragma unroll
     for (int c = 0; c < NG; ++c) {
       lsum[c] += __shfl_xor_sync(FULL_MASK, lsum[c], 4);
       lsum[c] += __shfl_xor_sync(FULL_MASK, lsum[c], 8);
       lsum[c] += __shfl_xor_sync(FULL_MASK, lsum[c], 16);
     }
-  }
 
-  // ---------------- drain (only after a bounded wait gave up), then merge the warps
-  __syncthreads();
-  if (threadIdx.x == 0 && sm.abort_flag) {
-    for (int i = sm.first_unconsumed; i < sm.issued; ++i)
-      (void)mbar_wait_bounded(&sm.full[i % NSTAGE], (i / NSTAGE) & 1, WAIT_LIMIT_NS);
-  }
-  if (warp < CWARPS && g == 0) {
+    // ---- merge the consumer warps' states of this item and write its partial
+    if (g == 0) {
 #pragma unroll
-    for (int c = 0; c < NG; ++c) {
-      sm.mw[warp][c * 4 + t] = M[c];
-      sm.lw[warp][c * 4 + t] = lsum[c];
+      for (int c = 0; c < NG; ++c) {
+        sm.mw[warp][c * 4 + t] = M[c];
+        sm.lw[warp][c * 4 + t] = lsum[c];
+      }
     }
-  }
-  __syncthreads();
-  float *osm = reinterpret_cast<float *>(&sm.kbuf[0][0]);  // [CWARPS][8 heads][128], spans kbuf+vbuf
-  if (warp < CWARPS) {
+    consumers_sync();
 #pragma unroll
     for (int c = 0; c < NG; ++c) {
       const int hh = c * 4 + t;
       float ms = -INFINITY;
-#pragma unroll
       for (int w = 0; w < CWARPS; ++w) ms = fmaxf(ms, sm.mw[w][hh]);
       const float fac = (M[c] == -INFINITY) ? 0.f : exp2_approx(M[c] - ms);
-      float *orow = osm + (warp * 8 + hh) * D + 16 * g;
+      float *orow = &sm.osm[warp][t][16 * g];
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         orow[2 * mt] = (O[c][mt][0] + O[c][mt][1]) * fac;
         orow[2 * mt + 1] = (O[c][mt][2] + O[c][mt][3]) * fac;
       }
-    }
-  }
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < G * D; idx += NTHREADS) {
-    const int hh = idx / D, j = idx % D;
-    float ms = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < CWARPS; ++w) ms = fmaxf(ms, sm.mw[w][hh]);
-    float acc = 0.f;
-#pragma unroll
-    for (int w = 0; w < CWARPS; ++w) acc += osm[(w * 8 + hh) * D + j];
-    float *dst = p.part + ((size_t)(b * p.Hq + head0 + hh) * p.n_split + split) * PARTIAL_FLOATS;
-    dst[6 + j] = (ms == -INFINITY) ? 0.f : acc;
-    if (j < 6) {
-      float v = 0.f;
-      if (j == 0) {
-        v = ms;
-      } else if (j == 1 && ms != -INFINITY) {
-        for (int w = 0; w < CWARPS; ++w)
-          if (sm.mw[w][hh] != -INFINITY) v += sm.lw[w][hh] * exp2_approx(sm.mw[w][hh] - ms);
+      consumers_sync();
+      const int Gc = min(4, G - c * 4);
+      for (int idx = threadIdx.x; idx < Gc * D; idx += CWARPS * 32) {
+        const int h4 = idx / D, jd = idx % D;
+        const int hh2 = c * 4 + h4;
+        float ms2 = -INFINITY;
+        for (int w = 0; w < CWARPS; ++w) ms2 = fmaxf(ms2, sm.mw[w][hh2]);
+        float acc = 0.f;
+        for (int w = 0; w < CWARPS; ++w) acc += sm.osm[w][h4][jd];
+        float *dst = p.part + ((size_t)(b * p.Hq + head0 + hh2) * p.n_part + it.slot) * PARTIAL_FLOATS;
+        dst[6 + jd] = (ms2 == -INFINITY) ? 0.f : acc;
+        if (jd < 6) {
+          float v = 0.f;
+          if (jd == 0) {
+            v = ms2;
+          } else if (jd == 1 && ms2 != -INFINITY) {
+            for (int w = 0; w < CWARPS; ++w)
+              if (sm.mw[w][hh2] != -INFINITY) v += sm.lw[w][hh2] * exp2_approx(sm.mw[w][hh2] - ms2);
+          }
+          dst[jd] = v;
+        }
       }
-      dst[j] = v;
+      consumers_sync();
     }
   }
 }
@@ -553,7 +589,8 @@ __global__ void __launch_bounds__(NTHREADS) __maxnreg__(NG == 1 ? 128 : 168)
 struct CombineParams {
   const float *part;
   int n_heads;      // B * Hq
-  int n_split;
+  int n_split;      // partial slots per head
+  int Hq, gq, heads_per_cta, n_hg, tiles_per_unit, tiles_per_cta;
   const float *r;   // R (row-major) of the value rotation, or null
   float inv_vscale; // 1 / (2^14 * alpha_V)
   float *out;
@@ -572,30 +609,35 @@ __global__ void __launch_bounds__(QWARPS * 32) k_combine(const CombineParams p) 
   const bool live = bh < p.n_heads;
   if (live) {
     const float *part = p.part + (size_t)bh * p.n_split * PARTIAL_FLOATS;
+    // slots written for this head: CTAs whose tile range meets its unit
+    const int b = bh / p.Hq, h = bh % p.Hq;
+    const int unit = (b * (p.Hq / p.gq) + h / p.gq) * p.n_hg + (h % p.gq) / p.heads_per_cta;
+    const int first = unit * p.tiles_per_unit;
+    const int n_split = ((first + p.tiles_per_unit - 1) / p.tiles_per_cta) - first / p.tiles_per_cta + 1;
     float ms = -INFINITY;
-    for (int s = lane; s < p.n_split; s += 32) {
+    for (int s = lane; s < n_split; s += 32) {
       const float *ps = part + (size_t)s * PARTIAL_FLOATS;
       if (ps[1] > 0.f) ms = fmaxf(ms, ps[0]);
     }
 #pragma unroll
     for (int h = 16; h >= 1; h >>= 1) ms = fmaxf(ms, __shfl_xor_sync(FULL_MASK, ms, h));
     float lsum = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int s0 = 0; s0 < p.n_split; s0 += 32) {
+    for (int s0 = 0; s0 < n_split; s0 += 32) {
       const int s = s0 + lane;
       float w = 0.f;
-      if (s < p.n_split) {
+      if (s < n_split) {
         const float *ps = part + (size_t)s * PARTIAL_FLOATS;
         if (ps[1] > 0.f) {
           w = exp2f(ps[0] - ms);
           lsum += w * ps[1];
         }
       }
-      const int n = min(32, p.n_split - s0);
+      const int n = min(32, n_split - s0);
       for (int i0 = 0; i0 < n; i0 += 8) {  // eight splits' loads in flight at a time
         float v[8][4];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const int si = min(s0 + i0 + i, p.n_split - 1);
+          const int si = min(s0 + i0 + i, n_split - 1);
           const float *ps = part + (size_t)si * PARTIAL_FLOATS + 6;
 #pragma unroll
           for (int m = 0; m < 4; ++m) v[i][m] = ps[lane + 32 * m];
@@ -645,17 +687,17 @@ bool decode_shape(const tq_ctx *k, const tq_ctx *v, int B, int Hq, int Hkv, int 
   s->gq = Hq / Hkv;
   s->heads_per_cta = s->gq <= 4 ? 4 : 8;
   s->n_hg = (s->gq + s->heads_per_cta - 1) / s->heads_per_cta;
-  const int units = B * Hkv * s->n_hg;
-  const int slots = k->num_sms * 2;
-  int want = (4 * slots + units - 1) / units;
-  if (want < 1) want = 1;
-  int max_split = (L + 255) / 256;
-  if (max_split < 1) max_split = 1;
-  int n = want < max_split ? want : max_split;
-  int chunk = (L + n - 1) / n;
-  chunk = (chunk + TILE - 1) / TILE * TILE;
-  s->chunk = chunk;
-  s->n_split = (L + chunk - 1) / chunk;
+  const int64_t units = (int64_t)B * Hkv * s->n_hg;
+  s->tiles_per_unit = (L + TILE - 1) / TILE;
+  const int64_t total = units * s->tiles_per_unit;
+  if (total > INT32_MAX) return false;
+  s->total_tiles = (int)total;
+  // One persistent CTA per SM; contiguous equal tile ranges (the last may be shorter).
+  const int64_t tpc = (total + k->num_sms - 1) / k->num_sms;
+  s->tiles_per_cta = (int)(tpc < 1 ? 1 : tpc);
+  s->grid = (int)((total + s->tiles_per_cta - 1) / s->tiles_per_cta);
+  // Partial slots per head: CTAs whose range meets one unit.
+  s->n_part = (s->tiles_per_unit + s->tiles_per_cta - 1) / s->tiles_per_cta + 1;
   return true;
 }
 
@@ -664,7 +706,7 @@ Workspace carve_workspace(const DecodeShape &s, void *base) {
   const size_t nq = (size_t)s.B * s.Hq;
   const size_t b_qhl = up(nq * 256 * sizeof(uint32_t));
   const size_t b_qsc = up(nq * 2 * sizeof(float));
-  const size_t b_part = up(nq * s.n_split * PARTIAL_FLOATS * sizeof(float));
+  const size_t b_part = up(nq * s.n_part * PARTIAL_FLOATS * sizeof(float));
   Workspace w{};
   uint8_t *p = static_cast<uint8_t *>(base);
   w.qhl = reinterpret_cast<uint32_t *>(p);
@@ -716,7 +758,8 @@ cudaError_t launch_partial(const tq_ctx *k, const tq_ctx *v, const uint8_t *kc,
   PartialParams p{};
   p.kc = kc, p.vc = vc, p.seq_lens = seq_lens;
   p.B = s.B, p.Hq = s.Hq, p.Hkv = s.Hkv, p.L = s.L, p.gq = s.gq, p.n_hg = s.n_hg;
-  p.n_split = s.n_split, p.chunk = s.chunk;
+  p.tiles_per_unit = s.tiles_per_unit, p.tiles_per_cta = s.tiles_per_cta;
+  p.total_tiles = s.total_tiles, p.n_part = s.n_part;
   p.qhl = ws.qhl, p.qsc = ws.qsc, p.part = ws.partials, p.scores = scores_dbg;
   for (int i = 0; i < 2; ++i) {
     p.klo[i] = k->f16.lo[i], p.khi[i] = k->f16.hi[i];
@@ -724,7 +767,7 @@ cudaError_t launch_partial(const tq_ctx *k, const tq_ctx *v, const uint8_t *kc,
   }
   for (int i = 0; i < 8; ++i) p.kc16[i] = k->f16.c16[i], p.vc16[i] = v->f16.c16[i];
   p.status = k->d_status;
-  dim3 grid(s.n_split, s.B * s.Hkv * s.n_hg);
+  dim3 grid(s.grid);
   if (s.heads_per_cta == 8)
     return scores_dbg ? launch_t4<2, true, K_PRMT_WORDS, V_PRMT_WORDS>(p, grid, st)
                       : launch_t4<2, false, K_PRMT_WORDS, V_PRMT_WORDS>(p, grid, st);
@@ -738,7 +781,9 @@ cudaError_t launch_combine(const tq_ctx *k, const tq_ctx *v, const DecodeShape &
   CombineParams p{};
   p.part = ws.partials;
   p.n_heads = s.B * s.Hq;
-  p.n_split = s.n_split;
+  p.n_split = s.n_part;
+  p.Hq = s.Hq, p.gq = s.gq, p.heads_per_cta = s.heads_per_cta, p.n_hg = s.n_hg;
+  p.tiles_per_unit = s.tiles_per_unit, p.tiles_per_cta = s.tiles_per_cta;
   p.r = v->d_pi;
   p.inv_vscale = 1.0f / (exp2f(P_SHIFT) * v->f16.alpha);
   p.out = out;

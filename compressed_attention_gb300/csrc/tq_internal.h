@@ -82,8 +82,11 @@ struct DecodeShape {
   int gq;       // q-heads per KV head
   int heads_per_cta;  // q-heads one CTA serves (4 or 8)
   int n_hg;     // head groups per KV head
-  int n_split;  // key splits
-  int chunk;    // keys per split (multiple of the tile)
+  int tiles_per_unit;  // key tiles of one (batch, KV head, head group) unit
+  int total_tiles;     // over all units, laid end to end
+  int tiles_per_cta;   // contiguous range per persistent CTA
+  int grid;            // persistent CTAs (at most one per SM)
+  int n_part;          // partial slots per head
 };
 struct Workspace {
   uint32_t *qhl;     // [B*Hq][2 operands][128 fp16]: hi then lo, per operand (q_rot, sketch)
