@@ -412,7 +412,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) __maxnreg__(NG == 1 ? 128 : 128)
       }
       const int nk = min(TILE, Lb - kf);
       const size_t start = (unit_row0 + kf) * T4_ROW;
-      const uint32_t soff = (uint32_t)s * STAGE_BUF + (uint32_t)(start & 15) + kb * T4_ROW + order_token();
+      const uint32_t soff = (uint32_t)s * STAGE_BUF + (uint32_t)(start & 15) + kb * T4_ROW;
       const uint32_t Ks = kbuf0 + soff, Vs = vbuf0 + soff;
       const int nkb = nk - kb;  // valid keys of this warp's block (may be <= 0 or > 16)
       if (nkb > 0) {

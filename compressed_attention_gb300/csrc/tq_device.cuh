@@ -68,27 +68,18 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
 
-// Shared-memory loads by 32-bit shared-window address.  They are plain (reorderable)
-// loads; callers order them after the mbarrier wait that publishes the data by adding
-// an opaque zero produced after the wait (order_token) to the address.
+// Shared-memory loads by 32-bit shared-window address.  Volatile keeps them after
+// the mbarrier wait that publishes the data they read.
 __device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
   uint32_t v;
-  asm("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
   return v;
 }
 
 __device__ __forceinline__ float lds_f32(uint32_t addr) {
   float v;
-  asm("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
   return v;
-}
-
-// A zero the compiler cannot see through, emitted in program order after the
-// preceding volatile asm (the mbarrier wait).
-__device__ __forceinline__ uint32_t order_token() {
-  uint32_t z;
-  asm volatile("mov.u32 %0, 0;" : "=r"(z)::"memory");
-  return z;
 }
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
