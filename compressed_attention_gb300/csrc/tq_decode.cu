@@ -200,16 +200,16 @@ struct SmemPartial {
   int abort_flag;
 };
 
-// Table lookup of byte I of w: the shared address is lut + ((byte << 8) | laneword.byte0),
-// the table base being a constant of the shared window.
+// Table lookup of byte I of w: off = (byte << 8) | laneword.byte0.
 template <int I>
-__device__ __forceinline__ uint32_t lut_byte(uint32_t lut, uint32_t laneword, uint32_t w) {
-  return lds_u32(lut + prmt(laneword, w, 0x1100u | ((4u + I) << 4)));
+__device__ __forceinline__ uint32_t lut_byte(const uint8_t *lut_base, uint32_t laneword, uint32_t w) {
+  const uint32_t off = prmt(laneword, w, 0x1100u | ((4u + I) << 4));
+  return *reinterpret_cast<const uint32_t *>(lut_base + off);
 }
 
 // Four bytes of w -> four fp16x2 words, from the table or by byte permutes.
 template <bool PRMT>
-__device__ __forceinline__ void decode4(uint32_t lut_base, uint32_t laneword, uint32_t w,
+__device__ __forceinline__ void decode4(const uint8_t *lut_base, uint32_t laneword, uint32_t w,
                                         const uint32_t (&lo)[2], const uint32_t (&hi)[2],
                                         uint32_t (&r)[4]) {
   if (PRMT) {
@@ -220,6 +220,10 @@ __device__ __forceinline__ void decode4(uint32_t lut_base, uint32_t laneword, ui
     r[2] = lut_byte<2>(lut_base, laneword, w);
     r[3] = lut_byte<3>(lut_base, laneword, w);
   }
+}
+
+__device__ __forceinline__ uint32_t ld_u32(const uint8_t *p) {
+  return *reinterpret_cast<const uint32_t *>(p);
 }
 
 // Physical key (within a 16-key block) of score row r.  Rows g and g+8 belong to
@@ -344,8 +348,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) __maxnreg__(NG == 1 ? 128 : 128)
   }
 
   // ---------------- consumers
-  const uint32_t lut_base = smem_addr(&sm.lut[0][0]);
-  const uint32_t kbuf0 = smem_addr(&sm.kbuf[0][0]), vbuf0 = smem_addr(&sm.vbuf[0][0]);
+  const uint8_t *lut_base = reinterpret_cast<const uint8_t *>(&sm.lut[0][0]);
   const uint32_t kword = 4u * lane, vword = 128u + 4u * lane;
   const uint32_t klo[2] = {p.klo[0], p.klo[1]}, khi[2] = {p.khi[0], p.khi[1]};
   const uint32_t vlo[2] = {p.vlo[0], p.vlo[1]}, vhi[2] = {p.vhi[0], p.vhi[1]};
@@ -412,8 +415,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) __maxnreg__(NG == 1 ? 128 : 128)
       }
       const int nk = min(TILE, Lb - kf);
       const size_t start = (unit_row0 + kf) * T4_ROW;
-      const uint32_t soff = (uint32_t)s * STAGE_BUF + (uint32_t)(start & 15) + kb * T4_ROW;
-      const uint32_t Ks = kbuf0 + soff, Vs = vbuf0 + soff;
+      const uint8_t *Ks = sm.kbuf[s] + (start & 15) + kb * T4_ROW;
+      const uint8_t *Vs = sm.vbuf[s] + (start & 15) + kb * T4_ROW;
       const int nkb = nk - kb;  // valid keys of this warp's block (may be <= 0 or > 16)
       if (nkb > 0) {
         // ---- scores S^T[16 rows x 8 cols] = K_hat Q^T, two accumulator chains
@@ -422,12 +425,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) __maxnreg__(NG == 1 ? 128 : 128)
         for (int c = 0; c < NG; ++c)
 #pragma unroll
           for (int e = 0; e < 4; ++e) sa[c][e] = sb[c][e] = 0.f;
-        const uint32_t kr0 = Ks + rk0 * T4_ROW + 4 + 16 * t;
-        const uint32_t kr1 = Ks + rk1 * T4_ROW + 4 + 16 * t;
+        const uint8_t *kr0 = Ks + rk0 * T4_ROW + 4 + 16 * t;
+        const uint8_t *kr1 = Ks + rk1 * T4_ROW + 4 + 16 * t;
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
           uint32_t d0[4], d1[4];
-          const uint32_t x0 = lds_u32(kr0 + 4 * w), x1 = lds_u32(kr1 + 4 * w);
+          const uint32_t x0 = ld_u32(kr0 + 4 * w), x1 = ld_u32(kr1 + 4 * w);
           if (w < KP) {
             decode4<true>(lut_base, kword, x0, klo, khi, d0);
             decode4<true>(lut_base, kword, x1, klo, khi, d1);
@@ -444,8 +447,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) __maxnreg__(NG == 1 ? 128 : 128)
           }
         }
         // ---- online softmax over the two keys of this lane, head t of each group
-        const float nk0 = lds_f32(Ks + rk0 * T4_ROW), nk1 = lds_f32(Ks + rk1 * T4_ROW);
-        const float nv0 = lds_f32(Vs + rk0 * T4_ROW), nv1 = lds_f32(Vs + rk1 * T4_ROW);
+        const float nk0 = *reinterpret_cast<const float *>(Ks + rk0 * T4_ROW);
+        const float nk1 = *reinterpret_cast<const float *>(Ks + rk1 * T4_ROW);
+        const float nv0 = *reinterpret_cast<const float *>(Vs + rk0 * T4_ROW);
+        const float nv1 = *reinterpret_cast<const float *>(Vs + rk1 * T4_ROW);
         const bool ok0 = rk0 < nkb, ok1 = rk1 < nkb;
         const float nu0 = ok0 ? fmaxf(log2_approx(nv0), -64.f) : 0.f;
         const float nu1 = ok1 ? fmaxf(log2_approx(nv1), -64.f) : 0.f;
@@ -489,11 +494,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) __maxnreg__(NG == 1 ? 128 : 128)
           pb[c][1] = *reinterpret_cast<const uint32_t *>(&rcd);
         }
         // ---- O^T[dims x cols] += V_hat^T[dims x keys] P^T
-        const uint32_t va_p = Vs + at * T4_ROW + 4 + 8 * g;  // key a_t; a_t+2, +4, +6 follow
+        const uint8_t *va_p = Vs + at * T4_ROW + 4 + 8 * g;  // key a_t; a_t+2, +4, +6 follow
 #pragma unroll
         for (int w = 0; w < 2; ++w) {
-          const uint32_t xa = lds_u32(va_p + 4 * w), xb = lds_u32(va_p + 2 * T4_ROW + 4 * w);
-          const uint32_t xc = lds_u32(va_p + 4 * T4_ROW + 4 * w), xd = lds_u32(va_p + 6 * T4_ROW + 4 * w);
+          const uint32_t xa = ld_u32(va_p + 4 * w), xb = ld_u32(va_p + 2 * T4_ROW + 4 * w);
+          const uint32_t xc = ld_u32(va_p + 4 * T4_ROW + 4 * w), xd = ld_u32(va_p + 6 * T4_ROW + 4 * w);
           // byte i of zlo = (low nibble of key a, low nibble of key b) of byte 8g + 4w + i
           const uint32_t zlo_ab = (xa & 0x0F0F0F0Fu) | ((xb << 4) & 0xF0F0F0F0u);
           const uint32_t zhi_ab = ((xa >> 4) & 0x0F0F0F0Fu) | (xb & 0xF0F0F0F0u);
