@@ -188,6 +188,8 @@ tq_status tq_ctx_create(const tq_params *params, tq_ctx **out) {
   c->fmt = p.format;
   cudaError_t e = cudaGetDevice(&c->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&c->reserved_smem, cudaDevAttrReservedSharedMemoryPerBlock, c->device);
   if (e != cudaSuccess) {
     delete c;
     return cuda_fail(e, "cudaGetDevice");

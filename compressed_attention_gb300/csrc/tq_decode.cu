@@ -183,15 +183,15 @@ struct PartialParams {
   int32_t *status;
 };
 
-// Shared memory of one CTA.  lut[b][s]: slots s < 32 hold the key table and
-// s >= 32 the value table; entry = (c[b & 15], c[b >> 4]) as fp16x2.  Lane l reads
-// slot l (keys) or 32 + l (values), so a warp's 32 lookups always hit 32 distinct
-// banks, and the byte offset (b << 8) | (4 * slot) is one byte permute away from
-// the packed word.
-struct SmemPartial {
-  uint32_t lut[256][64];
-  uint8_t kbuf[NSTAGE][STAGE_BUF];
-  uint8_t vbuf[NSTAGE][STAGE_BUF];
+// Shared memory of one CTA, as offsets from the start of dynamic shared memory.
+// The 64 KB table lut[b][s] (slots s < 32: key table, s >= 32: value table; entry =
+// (c[b & 15], c[b >> 4]) as fp16x2) sits at shared-window address 0x10000 when the
+// device reserves the usual 1 KB at the window start, so a lookup's address
+// (b << 8) | (4 * slot) is one byte permute of the packed word and the table base
+// rides in the load's immediate.  Lane l reads slot l (keys) or 32 + l (values): a
+// warp's 32 lookups hit 32 distinct banks.  Eight stage buffers (K and V of NSTAGE
+// stages) and the merge scratch are packed around the table.
+struct SmemHead {
   float osm[CWARPS][4][D];              // per-warp accumulators of 4 heads, for the merge
   uint64_t full[NSTAGE];
   uint64_t empty[NSTAGE];
@@ -199,26 +199,45 @@ struct SmemPartial {
   float lw[CWARPS][8];
   int abort_flag;
 };
+constexpr uint32_t LUT_WINDOW = 0x10000;           // shared-window address of the table
+constexpr uint32_t RESERVED_SMEM = 1024;           // window bytes before dynamic smem
+constexpr uint32_t STAGE_A_OFF = (sizeof(SmemHead) + 15) & ~15u;
+constexpr uint32_t LUT_OFF = LUT_WINDOW - RESERVED_SMEM;
+constexpr uint32_t STAGE_B_OFF = LUT_OFF + 256 * 64 * 4;
+constexpr uint32_t SMEM_BYTES = STAGE_B_OFF + 6 * STAGE_BUF;
+static_assert(STAGE_A_OFF + 2 * STAGE_BUF <= LUT_OFF, "two stage buffers below the table");
+static_assert(NSTAGE == 4, "stage buffer placement assumes four stages");
 
-// Table lookup of byte I of w: off = (byte << 8) | laneword.byte0.
-template <int I>
-__device__ __forceinline__ uint32_t lut_byte(const uint8_t *lut_base, uint32_t laneword, uint32_t w) {
+// Stage buffer i (0..3: K of stage i, 4..7: V of stage i - 4).
+__device__ __forceinline__ uint8_t *stage_buf(uint8_t *smem, int i) {
+  return smem + (i < 2 ? STAGE_A_OFF + i * STAGE_BUF : STAGE_B_OFF + (i - 2) * STAGE_BUF);
+}
+
+// Table lookup of byte I of w.  FIXED: the table is at window address LUT_WINDOW and
+// the load carries it as an immediate; otherwise the table's address is added.
+template <bool FIXED, int I>
+__device__ __forceinline__ uint32_t lut_byte(uint32_t lut_addr, uint32_t laneword, uint32_t w) {
   const uint32_t off = prmt(laneword, w, 0x1100u | ((4u + I) << 4));
-  return *reinterpret_cast<const uint32_t *>(lut_base + off);
+  uint32_t v;
+  if (FIXED)
+    asm("ld.shared.u32 %0, [%1+65536];" : "=r"(v) : "r"(off));
+  else
+    asm("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(off + lut_addr));
+  return v;
 }
 
 // Four bytes of w -> four fp16x2 words, from the table or by byte permutes.
-template <bool PRMT>
-__device__ __forceinline__ void decode4(const uint8_t *lut_base, uint32_t laneword, uint32_t w,
+template <bool PRMT, bool FIXED>
+__device__ __forceinline__ void decode4(uint32_t lut_addr, uint32_t laneword, uint32_t w,
                                         const uint32_t (&lo)[2], const uint32_t (&hi)[2],
                                         uint32_t (&r)[4]) {
   if (PRMT) {
     decode8<0x5140u, 0x7362u>(w, lo, hi, r);
   } else {
-    r[0] = lut_byte<0>(lut_base, laneword, w);
-    r[1] = lut_byte<1>(lut_base, laneword, w);
-    r[2] = lut_byte<2>(lut_base, laneword, w);
-    r[3] = lut_byte<3>(lut_base, laneword, w);
+    r[0] = lut_byte<FIXED, 0>(lut_addr, laneword, w);
+    r[1] = lut_byte<FIXED, 1>(lut_addr, laneword, w);
+    r[2] = lut_byte<FIXED, 2>(lut_addr, laneword, w);
+    r[3] = lut_byte<FIXED, 3>(lut_addr, laneword, w);
   }
 }
 
@@ -271,12 +290,17 @@ __device__ __forceinline__ int unit_len(const PartialParams &p, int unit) {
 // 16g..16g+15 of the PV product.  KP of the 4 key words and VP of the 2 value words
 // per lane are decoded by byte permutes instead of the table, to balance the ALU and
 // shared-memory pipes.
-template <int NG, bool SCORES, int KP, int VP>
-__global__ void __launch_bounds__(NTHREADS, 1) __maxnreg__(NG == 1 ? 128 : 128)
+template <int NG, bool SCORES, int KP, int VP, bool FIXED>
+__global__ void __maxnreg__(128)
     k_partial_t4(const PartialParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  SmemPartial &sm = *reinterpret_cast<SmemPartial *>(smem_raw);
+  SmemHead &sm = *reinterpret_cast<SmemHead *>(smem_raw);
+  uint32_t *lut = reinterpret_cast<uint32_t *>(smem_raw + LUT_OFF);
   const int cta = blockIdx.x;
+  if (FIXED && smem_addr(smem_raw) != RESERVED_SMEM) {  // layout assumption broken: refuse
+    if (threadIdx.x == 0) atomicExch(p.status, (int32_t)DEVERR_LAYOUT);
+    return;
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
@@ -298,7 +322,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) __maxnreg__(NG == 1 ? 128 : 128)
     const uint32_t lo = (c16[(byte & 15) >> 1] >> (16 * (byte & 1))) & 0xFFFFu;
     const uint32_t hi = (c16[(byte >> 4) >> 1] >> (16 * ((byte >> 4) & 1))) & 0xFFFFu;
     const uint32_t e = lo | (hi << 16);
-    uint4 *dst = reinterpret_cast<uint4 *>(&sm.lut[byte][chunk * 8]);
+    uint4 *dst = reinterpret_cast<uint4 *>(lut + byte * 64 + chunk * 8);
     dst[0] = make_uint4(e, e, e, e);
     dst[1] = make_uint4(e, e, e, e);
   }
@@ -332,8 +356,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) __maxnreg__(NG == 1 ? 128 : 128)
           const size_t a1 = (start + (size_t)nk * T4_ROW + 15) & ~(size_t)15;
           const uint32_t bytes = (uint32_t)(a1 - a0);
           mbar_arrive_expect_tx(&sm.full[s], 2 * bytes);
-          bulk_g2s(sm.kbuf[s], p.kc + a0, bytes, &sm.full[s]);
-          bulk_g2s(sm.vbuf[s], p.vc + a0, bytes, &sm.full[s]);
+          bulk_g2s(stage_buf(smem_raw, s), p.kc + a0, bytes, &sm.full[s]);
+          bulk_g2s(stage_buf(smem_raw, 4 + s), p.vc + a0, bytes, &sm.full[s]);
           ++ctr;
         }
       }
@@ -348,7 +372,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) __maxnreg__(NG == 1 ? 128 : 128)
   }
 
   // ---------------- consumers
-  const uint8_t *lut_base = reinterpret_cast<const uint8_t *>(&sm.lut[0][0]);
+  const uint32_t lut_base = smem_addr(lut);
   const uint32_t kword = 4u * lane, vword = 128u + 4u * lane;
   const uint32_t klo[2] = {p.klo[0], p.klo[1]}, khi[2] = {p.khi[0], p.khi[1]};
   const uint32_t vlo[2] = {p.vlo[0], p.vlo[1]}, vhi[2] = {p.vhi[0], p.vhi[1]};
@@ -415,8 +439,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) __maxnreg__(NG == 1 ? 128 : 128)
       }
       const int nk = min(TILE, Lb - kf);
       const size_t start = (unit_row0 + kf) * T4_ROW;
-      const uint8_t *Ks = sm.kbuf[s] + (start & 15) + kb * T4_ROW;
-      const uint8_t *Vs = sm.vbuf[s] + (start & 15) + kb * T4_ROW;
+      const uint8_t *Ks = stage_buf(smem_raw, s) + (start & 15) + kb * T4_ROW;
+      const uint8_t *Vs = stage_buf(smem_raw, 4 + s) + (start & 15) + kb * T4_ROW;
       const int nkb = nk - kb;  // valid keys of this warp's block (may be <= 0 or > 16)
       if (nkb > 0) {
         // ---- scores S^T[16 rows x 8 cols] = K_hat Q^T, two accumulator chains
@@ -432,11 +456,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) __maxnreg__(NG == 1 ? 128 : 128)
           uint32_t d0[4], d1[4];
           const uint32_t x0 = ld_u32(kr0 + 4 * w), x1 = ld_u32(kr1 + 4 * w);
           if (w < KP) {
-            decode4<true>(lut_base, kword, x0, klo, khi, d0);
-            decode4<true>(lut_base, kword, x1, klo, khi, d1);
+            decode4<true, FIXED>(lut_base, kword, x0, klo, khi, d0);
+            decode4<true, FIXED>(lut_base, kword, x1, klo, khi, d1);
           } else {
-            decode4<false>(lut_base, kword, x0, klo, khi, d0);
-            decode4<false>(lut_base, kword, x1, klo, khi, d1);
+            decode4<false, FIXED>(lut_base, kword, x0, klo, khi, d0);
+            decode4<false, FIXED>(lut_base, kword, x1, klo, khi, d1);
           }
           const uint32_t a0[4] = {d0[0], d1[0], d0[1], d1[1]};
           const uint32_t a1[4] = {d0[2], d1[2], d0[3], d1[3]};
@@ -506,15 +530,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) __maxnreg__(NG == 1 ? 128 : 128)
           const uint32_t zhi_cd = ((xc >> 4) & 0x0F0F0F0Fu) | (xd & 0xF0F0F0F0u);
           uint32_t r0[4], r1[4], r2[4], r3[4];
           if (w < VP) {
-            decode4<true>(lut_base, vword, zlo_ab, vlo, vhi, r0);
-            decode4<true>(lut_base, vword, zhi_ab, vlo, vhi, r1);
-            decode4<true>(lut_base, vword, zlo_cd, vlo, vhi, r2);
-            decode4<true>(lut_base, vword, zhi_cd, vlo, vhi, r3);
+            decode4<true, FIXED>(lut_base, vword, zlo_ab, vlo, vhi, r0);
+            decode4<true, FIXED>(lut_base, vword, zhi_ab, vlo, vhi, r1);
+            decode4<true, FIXED>(lut_base, vword, zlo_cd, vlo, vhi, r2);
+            decode4<true, FIXED>(lut_base, vword, zhi_cd, vlo, vhi, r3);
           } else {
-            decode4<false>(lut_base, vword, zlo_ab, vlo, vhi, r0);
-            decode4<false>(lut_base, vword, zhi_ab, vlo, vhi, r1);
-            decode4<false>(lut_base, vword, zlo_cd, vlo, vhi, r2);
-            decode4<false>(lut_base, vword, zhi_cd, vlo, vhi, r3);
+            decode4<false, FIXED>(lut_base, vword, zlo_ab, vlo, vhi, r0);
+            decode4<false, FIXED>(lut_base, vword, zhi_ab, vlo, vhi, r1);
+            decode4<false, FIXED>(lut_base, vword, zlo_cd, vlo, vhi, r2);
+            decode4<false, FIXED>(lut_base, vword, zhi_cd, vlo, vhi, r3);
           }
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) {
@@ -734,10 +758,10 @@ cudaError_t launch_prepare_q(const tq_ctx *k, const void *q, int q_dtype, const 
   return cudaGetLastError();
 }
 
-template <int NG, bool SC, int KP, int VP>
+template <int NG, bool SC, int KP, int VP, bool FIXED>
 cudaError_t launch_t4(const PartialParams &p, dim3 grid, cudaStream_t st) {
-  const size_t smem = sizeof(SmemPartial);
-  auto kern = k_partial_t4<NG, SC, KP, VP>;
+  const size_t smem = SMEM_BYTES;
+  auto kern = k_partial_t4<NG, SC, KP, VP, FIXED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -768,11 +792,19 @@ cudaError_t launch_partial(const tq_ctx *k, const tq_ctx *v, const uint8_t *kc,
   for (int i = 0; i < 8; ++i) p.kc16[i] = k->f16.c16[i], p.vc16[i] = v->f16.c16[i];
   p.status = k->d_status;
   dim3 grid(s.grid);
-  if (s.heads_per_cta == 8)
-    return scores_dbg ? launch_t4<2, true, K_PRMT_WORDS, V_PRMT_WORDS>(p, grid, st)
-                      : launch_t4<2, false, K_PRMT_WORDS, V_PRMT_WORDS>(p, grid, st);
-  return scores_dbg ? launch_t4<1, true, K_PRMT_WORDS, V_PRMT_WORDS>(p, grid, st)
-                    : launch_t4<1, false, K_PRMT_WORDS, V_PRMT_WORDS>(p, grid, st);
+  const bool fixed = k->reserved_smem == (int)RESERVED_SMEM;
+  if (s.heads_per_cta == 8) {
+    if (fixed)
+      return scores_dbg ? launch_t4<2, true, K_PRMT_WORDS, V_PRMT_WORDS, true>(p, grid, st)
+                        : launch_t4<2, false, K_PRMT_WORDS, V_PRMT_WORDS, true>(p, grid, st);
+    return scores_dbg ? launch_t4<2, true, K_PRMT_WORDS, V_PRMT_WORDS, false>(p, grid, st)
+                      : launch_t4<2, false, K_PRMT_WORDS, V_PRMT_WORDS, false>(p, grid, st);
+  }
+  if (fixed)
+    return scores_dbg ? launch_t4<1, true, K_PRMT_WORDS, V_PRMT_WORDS, true>(p, grid, st)
+                      : launch_t4<1, false, K_PRMT_WORDS, V_PRMT_WORDS, true>(p, grid, st);
+  return scores_dbg ? launch_t4<1, true, K_PRMT_WORDS, V_PRMT_WORDS, false>(p, grid, st)
+                    : launch_t4<1, false, K_PRMT_WORDS, V_PRMT_WORDS, false>(p, grid, st);
 }
 
 cudaError_t launch_combine(const tq_ctx *k, const tq_ctx *v, const DecodeShape &s, float *out,

@@ -11,7 +11,7 @@ namespace tq {
 constexpr int D = 128;
 
 // Device status codes (see tq_ctx_device_status in tq.h).
-enum DevErr : int32_t { DEVERR_ROW_OOB = 1, DEVERR_SEQLEN = 2, DEVERR_TIMEOUT = 3 };
+enum DevErr : int32_t { DEVERR_ROW_OOB = 1, DEVERR_SEQLEN = 2, DEVERR_TIMEOUT = 3, DEVERR_LAYOUT = 4 };
 
 // Stored codebook: K fp32 centroids and K-1 fp32 decision boundaries.
 struct Codebook {
@@ -40,6 +40,7 @@ struct tq_ctx {
   tq_params p{};
   int device = 0;
   int num_sms = 0;
+  int reserved_smem = 0;  // shared-window bytes reserved before dynamic shared memory
   int fmt = 0;
   tq::Codebook cb{};
   tq::F16Table f16{};

@@ -151,7 +151,9 @@ tq_status tq_ctx_destroy(tq_ctx *ctx);
 
 /* Reads (synchronising the device) and optionally clears the context's device
  * status word: 0 = no device-side error; 1 = row id out of range (write skipped);
- * 2 = sequence length outside [1, L] (clamped); 3 = a bounded wait ran out. */
+ * 2 = sequence length outside [1, L] (clamped); 3 = a bounded wait ran out;
+ * 4 = the decode kernel found shared memory laid out unlike the device reported
+ * (no output was computed). */
 tq_status tq_ctx_device_status(const tq_ctx *ctx, int32_t *status, int clear);
 
 /* Write path / SET_ROWS ([turbo4 post-mortem] sections 1, 2): quantize n_rows
