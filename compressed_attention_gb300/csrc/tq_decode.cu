@@ -44,7 +44,9 @@ constexpr int NTHREADS = (CWARPS + 1) * 32;  // + one producer warp; one CTA per
 constexpr int NSTAGE = 4;             // pipeline depth (about 128 KB in flight per SM)
 constexpr int T4_ROW = 68;
 constexpr int STAGE_BUF = 16352;      // >= 240 * 68 + 2 * 15, multiple of 32
-constexpr float P_SHIFT = 14.0f;      // p' = 2^14 * exp2(.) keeps fp16 normal
+constexpr float P_SHIFT = 7.0f;       // p' = 2^7 * exp2(.) keeps fp16 normal
+constexpr float RESCALE_SLACK = 8.0f; // rescale only when the max grows by more than 2^8,
+                                      // so p' <= 2^(7+8) stays inside fp16
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
@@ -493,7 +495,7 @@ __global__ void __maxnreg__(128)
           bm = fmaxf(bm, __shfl_xor_sync(FULL_MASK, bm, 4));
           bm = fmaxf(bm, __shfl_xor_sync(FULL_MASK, bm, 8));
           bm = fmaxf(bm, __shfl_xor_sync(FULL_MASK, bm, 16));
-          if (bm > M[c]) {
+          if (bm > M[c] + RESCALE_SLACK) {  // also taken while M is -inf
             const float alpha = exp2_approx(M[c] - bm);
             M[c] = bm;
             lsum[c] *= alpha;
@@ -773,7 +775,7 @@ cudaError_t launch_t4(const PartialParams &p, dim3 grid, cudaStream_t st) {
 
 // Decode-word split between the table (shared-memory pipe) and byte permutes (ALU pipe):
 // of the 4 key words and 2 value words a lane decodes per 16-key block.
-constexpr int K_PRMT_WORDS = 1;
+constexpr int K_PRMT_WORDS = 0;
 constexpr int V_PRMT_WORDS = 0;
 
 cudaError_t launch_partial(const tq_ctx *k, const tq_ctx *v, const uint8_t *kc,
