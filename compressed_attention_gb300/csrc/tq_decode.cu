@@ -7,13 +7,15 @@
 //   k_prepare_q  q_rot = R q (one warp per query), pre-scaled by
 //                log2(e) * scale / alpha and by a power of two, split into fp16
 //                hi + lo parts (the tensor-core operand).
-//   k_partial_t4 one CTA per (batch, KV head, group of 4 or 8 q-heads, key split):
-//                a producer warp streams 112-key tiles of the K and V caches into
-//                shared memory with 1-D bulk async copies on an mbarrier ring;
-//                seven consumer warps each take 16 keys of a tile, turn nibble
-//                pairs into fp16x2 centroid pairs (a conflict-free shared-memory
-//                table, or byte permutes for a tunable share of the words), and run
-//                the score and PV products as m16n8k16 MMAs with fp32 accumulators.
+//   k_partial_t4 persistent: one CTA per SM takes a contiguous range of 240-key tiles
+//                of the (batch, KV head, group of 4 or 8 q-heads) units laid end to
+//                end, writing one partial (max, sum, acc) per unit it touches.  A
+//                producer warp streams the K and V tiles into shared memory with 1-D
+//                bulk async copies on a four-stage mbarrier ring; fifteen consumer
+//                warps each take 16 keys of a tile, turn nibble pairs into fp16x2
+//                centroid pairs (a conflict-free shared-memory table, or byte
+//                permutes for a tunable share of the words), and run the score and
+//                PV products as m16n8k16 MMAs with fp32 accumulators.
 //   k_combine    log-sum-exp merge of the splits, 1/sum, un-rotation R^T o.
 //
 // MMA operand layout (one warp, 16 keys, 4 q-heads per column group):
@@ -618,7 +620,7 @@ struct CombineParams {
   int n_split;      // partial slots per head
   int Hq, gq, heads_per_cta, n_hg, tiles_per_unit, tiles_per_cta;
   const float *r;   // R (row-major) of the value rotation, or null
-  float inv_vscale; // 1 / (2^14 * alpha_V)
+  float inv_vscale; // 1 / (2^P_SHIFT * alpha_V)
   float *out;
 };
 
