@@ -68,6 +68,8 @@ _SIGNATURES = {
     "tq_decode_prepare_q": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _sz, _vp]),
     "tq_decode_partial": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _sz, _vp]),
     "tq_decode_combine": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _sz, _vp]),
+    "tq_decode_attention_static": (_i32, [_vp, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _f32,
+                                          _vp, _vp]),
 }
 
 
@@ -235,6 +237,19 @@ def tq_decode_attention(k_ctx, v_ctx, q, k_cache, v_cache, out, workspace, B, Hq
                                    _ptr(seq_lens), B, Hq, Hkv, L, scale, _ptr(out), _ptr(scores),
                                    _ptr(workspace), workspace.numel() * workspace.element_size(),
                                    _stream(stream)), "tq_decode_attention")
+
+
+TQ_STATIC_WORKSPACE_BYTES = 4 << 20  # capacity of the static scratch of tq_decode_attention_static
+
+
+def tq_decode_attention_static(k_ctx, v_ctx, q, k_cache, v_cache, out, B, Hq, Hkv, L, seq_lens=None,
+                               scale=0.0, stream=None):
+    """tq_decode_attention with its scratch in the library's static device area (no workspace
+    argument, no allocation); calls that overlap on one device race on that area."""
+    qp, qd = _q_args(q)
+    _check(lib.tq_decode_attention_static(k_ctx.handle, v_ctx.handle, qp, qd, _ptr(k_cache), _ptr(v_cache),
+                                          _ptr(seq_lens), B, Hq, Hkv, L, scale, _ptr(out), _stream(stream)),
+           "tq_decode_attention_static")
 
 
 def tq_decode_prepare_q(k_ctx, v_ctx, q, workspace, B, Hq, Hkv, L, scale=0.0, stream=None):

@@ -224,6 +224,36 @@ tq_status tq_decode_combine(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, int
 tq_status tq_decode_num_splits(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, int Hq,
                                int Hkv, int L, int *n_split);
 
+/* tq_decode_attention without a workspace argument and without any allocation.
+ * The method's pages have no counterpart: this is a deployment variant of the
+ * same fused decode, with identical arithmetic and outputs.
+ *
+ * For callers that can neither allocate device memory nor hand over a
+ * workspace: plugin code inside a host framework that owns and accounts for
+ * all device memory, and step loops where cudaMalloc / cudaFree could wait for
+ * the whole device.  The scratch (rotated queries, split-K partials) lives in
+ * a static device array of TQ_STATIC_WORKSPACE_BYTES that the library's module
+ * carries on each device; the call performs no allocation of any kind.
+ *
+ * Arguments: as tq_decode_attention (no scores_dbg, workspace or size).
+ * Errors: TQ_ERR_WORKSPACE when the shape needs more scratch than
+ *   TQ_STATIC_WORKSPACE_BYTES (tq_decode_workspace_size() tells; such shapes
+ *   use tq_decode_attention); the other errors of tq_decode_attention.
+ * Set-up: the first call on each device (that of k_ctx) looks up the static
+ *   area's address once with that device current, which may load the module
+ *   there; make that first call before any other work that must not be
+ *   interrupted by module loading.
+ * Nothing in the area needs to start at zero: every word the decode reads is
+ *   written earlier in the same call.
+ * Concurrency: all calls on one device share the single area.  Two calls whose
+ *   executions overlap on the device (different streams, or otherwise not
+ *   ordered) race on it and give wrong results; order them on one stream. */
+#define TQ_STATIC_WORKSPACE_BYTES (4u << 20)
+tq_status tq_decode_attention_static(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *q,
+                                     int q_dtype, const void *k_cache, const void *v_cache,
+                                     const int32_t *seq_lens, int B, int Hq, int Hkv, int L,
+                                     float scale, float *out, tq_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
