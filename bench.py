@@ -130,6 +130,23 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+# ----------------------------------------------------------------------------- ranks
+
+def max_over_ranks(x, dist, device):
+    """Largest value of the scalar x over all ranks (x itself without a process group)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank, world, ms):
+    """Whole-job rate (units/s) when every rank processes units_per_rank in at most ms."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 # ----------------------------------------------------------------------------- CPU side
 
 def cpu_oracle_sample(cfg, min_seconds=10.0, max_units=64):
@@ -322,11 +339,7 @@ def run_tq(args, rank, world, dist):
         if dist:
             dist.barrier()
     clk = clocks.summary()
-    total_ms = sum(step_ms)
-    if dist:
-        t = torch.tensor([total_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), dist, device)
 
     # end to end through the public API with host buffers: q and the new K/V rows copied in,
     # the output read back, every step.
@@ -357,33 +370,35 @@ def run_tq(args, rank, world, dist):
 
     kv_bytes, alg_bytes = algorithmic_bytes(cfg)
     ms_per_step = total_ms / args.steps
-    value = world * alg_bytes / (ms_per_step * 1e-3) / 1e9
+    value = job_rate(alg_bytes, world, ms_per_step) / 1e9
     keys = B * Hkv * L
-    part_avg = statistics.mean(part_ms)
+    part_avg = max_over_ranks(statistics.mean(part_ms), dist, device)
     peak, peak_kind = measured_peak()
     achieved = kv_bytes / (part_avg * 1e-3) / 1e9
-    e2e_gbs = world * alg_bytes / (statistics.mean(e2e_ms) * 1e-3) / 1e9
+    e2e_step_ms = max_over_ranks(statistics.mean(e2e_ms), dist, device)
+    e2e_gbs = job_rate(alg_bytes, world, e2e_step_ms) / 1e9
     if rank != 0:
         return
-    cpu = cpu_oracle_sample(cfg) if world == 1 or rank == 0 else None
+    cpu = cpu_oracle_sample(cfg) if world == 1 else None  # host-core baseline: N=1 only
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": config_dict(cfg),
-        "keys_per_s": world * keys / (ms_per_step * 1e-3),
-        "q_head_scores_per_s": world * B * Hq * L / (ms_per_step * 1e-3),
+        "keys_per_s": job_rate(keys, world, ms_per_step),
+        "q_head_scores_per_s": job_rate(B * Hq * L, world, ms_per_step),
         "hbm_frac_of_measured_step": value / peak,
         "operands": "4-bit packed K/V decoded in registers to fp16 centroids; fp16 hi+lo q and p; fp32 accumulate",
         "roofline": {"bound": "hbm", "kernel": "k_partial_t4 (split-K decode)", "achieved": achieved,
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": profiled_traffic(), "algorithmic_bytes_per_launch": kv_bytes,
                      "avg_launch_ms": part_avg},
-        "cpu_baseline": {"value": cpu["gbs"], "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
-                         "keys_per_s": cpu["keys_per_s"],
-                         "sample": f"{cpu['units']} whole (batch, KV head) units of {cfg['L']} keys x "
-                                   f"{Hq // Hkv} q-heads, fp64 dequantize-then-softmax, {cpu['seconds']:.1f} s"},
+        "cpu_baseline": None if cpu is None else {
+            "value": cpu["gbs"], "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+            "keys_per_s": cpu["keys_per_s"],
+            "sample": f"{cpu['units']} whole (batch, KV head) units of {cfg['L']} keys x "
+                      f"{Hq // Hkv} q-heads, fp64 dequantize-then-softmax, {cpu['seconds']:.1f} s"},
         "e2e": {"value": e2e_gbs, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": statistics.mean(e2e_ms)},
+                "ms_per_step": e2e_step_ms},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
