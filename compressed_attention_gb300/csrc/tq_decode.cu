@@ -33,6 +33,7 @@
 
 #include <cstring>
 
+#include "tq_decode_common.cuh"
 #include "tq_device.cuh"
 #include "tq_internal.h"
 
@@ -42,16 +43,11 @@ namespace {
 
 constexpr int CWARPS = 15;            // consumer warps (16 keys each per tile)
 constexpr int TILE = 16 * CWARPS;     // keys per pipeline stage (240)
+static_assert(TILE == T4_TILE, "tile size shared with the host");
 constexpr int NTHREADS = (CWARPS + 1) * 32;  // + one producer warp; one CTA per SM
 constexpr int NSTAGE = 4;             // pipeline depth (about 128 KB in flight per SM)
 constexpr int T4_ROW = 68;
 constexpr int STAGE_BUF = 16352;      // >= 240 * 68 + 2 * 15, multiple of 32
-constexpr float P_SHIFT = 7.0f;       // p' = 2^7 * exp2(.) keeps fp16 normal
-constexpr float RESCALE_SLACK = 8.0f; // rescale only when the max grows by more than 2^8,
-                                      // so p' <= 2^(7+8) stays inside fp16
-constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
-constexpr float LOG2E = 1.4426950408889634f;
-constexpr float LN2 = 0.6931471805599453f;
 
 // 8 packed 4-bit indices -> 8 fp16 centroid values as four fp16x2 words.
 // Magnitude index m = idx for idx < 8 (negative centroids), 15 - idx otherwise;
@@ -82,7 +78,9 @@ struct QprepParams {
   int q_dtype;
   int n_q;            // B * Hq
   const float *rt;    // R^T, fp32 [128][128] (row k = column k of R)
+  const float *st;    // S^T for the QJL sketch (prod3 keys), or null
   float mul;          // log2(e) * scale / alpha_K
+  float mul_sk;       // log2(e) * scale * sqrt(pi/2) / d (sketch)
   uint32_t *qhl;
   float *qsc;
 };
@@ -102,14 +100,49 @@ __device__ __forceinline__ void stage_matrix(float *dst, const float *src) {
   for (int i = 0; i < PER; ++i) d4[threadIdx.x + i * QWARPS * 32] = v[i];
 }
 
-// q_rot = R q for 8 queries per CTA: R^T staged once in shared memory, lane l of
-// warp w computes q_rot[l + 32 m] of query w.
+// y = M x for the staged M^T (lane l computes y[l + 32 m]), times mul, scaled by a power
+// of two 2^-e so that the largest element lies in [2^13, 2^14), split into fp16 hi and
+// lo written to hw[0..127] and hw[128..255].  Returns e.
+__device__ __forceinline__ int transform_split(const float *mt, const float *x, float mul,
+                                               __half *hw, int lane) {
+  float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+  for (int k = 0; k < D; ++k) {
+    const float xk = x[k];
+    const float *row = mt + k * D + lane;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) y[m] = fmaf(row[32 * m], xk, y[m]);
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    y[m] *= mul;
+    amax = fmaxf(amax, fabsf(y[m]));
+  }
+#pragma unroll
+  for (int h = 16; h >= 1; h >>= 1) amax = fmaxf(amax, __shfl_xor_sync(FULL_MASK, amax, h));
+  int e = 0;
+  if (amax > 0.f && isfinite(amax)) e = ilogbf(amax) - 13;
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const float v = ldexpf(y[m], -e);
+    const __half h = __float2half_rn(v);
+    hw[lane + 32 * m] = h;
+    hw[D + lane + 32 * m] = __float2half_rn(v - __half2float(h));
+  }
+  return e;
+}
+
+// For 8 queries per CTA: q_rot = R q and, with SKETCH, the QJL sketch S q, each
+// pre-scaled and split into the fp16 hi + lo tensor-core operands:
+// qhl[q][0..127] = q_rot (hi, lo), qhl[q][128..255] = sketch (hi, lo).
+template <bool SKETCH>
 __global__ void __launch_bounds__(QWARPS * 32) k_prepare_q(const QprepParams p) {
   extern __shared__ __align__(16) float qsm[];
-  float *rt = qsm;                       // [128][128]
+  float *mt = qsm;                       // [128][128]
   float *qv = qsm + D * D;               // [QWARPS][128]
   __half *hs = reinterpret_cast<__half *>(qv + QWARPS * D);  // [QWARPS][2][128]
-  stage_matrix(rt, p.rt);
+  stage_matrix(mt, p.rt);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qi = blockIdx.x * QWARPS + warp;
   const bool live = qi < p.n_q;
@@ -134,41 +167,31 @@ __global__ void __launch_bounds__(QWARPS * 32) k_prepare_q(const QprepParams p) 
   }
   *reinterpret_cast<float4 *>(&qv[warp * D + 4 * lane]) = make_float4(x[0], x[1], x[2], x[3]);
   __syncthreads();
-  if (!live) return;
-  float y[4] = {0.f, 0.f, 0.f, 0.f};  // q_rot[j], j = lane + 32 m
-#pragma unroll 8
-  for (int k = 0; k < D; ++k) {
-    const float qk = qv[warp * D + k];
-    const float *row = rt + k * D + lane;
-#pragma unroll
-    for (int m = 0; m < 4; ++m) y[m] = fmaf(row[32 * m], qk, y[m]);
-  }
-  float amax = 0.f;
-#pragma unroll
-  for (int m = 0; m < 4; ++m) {
-    y[m] *= p.mul;
-    amax = fmaxf(amax, fabsf(y[m]));
-  }
-#pragma unroll
-  for (int h = 16; h >= 1; h >>= 1) amax = fmaxf(amax, __shfl_xor_sync(FULL_MASK, amax, h));
-  int e = 0;
-  if (amax > 0.f && isfinite(amax)) e = ilogbf(amax) - 13;  // amax * 2^-e in [2^13, 2^14)
   __half *hw = hs + warp * 2 * D;
-#pragma unroll
-  for (int m = 0; m < 4; ++m) {
-    const float v = ldexpf(y[m], -e);
-    const __half h = __float2half_rn(v);
-    hw[lane + 32 * m] = h;
-    hw[D + lane + 32 * m] = __float2half_rn(v - __half2float(h));
-  }
-  __syncwarp();
   uint32_t *dst = p.qhl + (size_t)qi * 256;
   const uint32_t *src = reinterpret_cast<const uint32_t *>(hw);
+  if (live) {
+    const int e = transform_split(mt, qv + warp * D, p.mul, hw, lane);
+    __syncwarp();
 #pragma unroll
-  for (int i = 0; i < 4; ++i) dst[lane + 32 * i] = src[lane + 32 * i];
-  if (lane == 0) {
-    p.qsc[2 * qi] = ldexpf(1.0f, e);
-    p.qsc[2 * qi + 1] = 0.f;
+    for (int i = 0; i < 4; ++i) dst[lane + 32 * i] = src[lane + 32 * i];
+    if (lane == 0) {
+      p.qsc[2 * qi] = ldexpf(1.0f, e);
+      if (!SKETCH) p.qsc[2 * qi + 1] = 0.f;
+    }
+  }
+  if (SKETCH) {
+    __syncthreads();  // every warp is done with R^T
+    stage_matrix(mt, p.st);
+    __syncthreads();
+    if (live) {
+      __syncwarp();
+      const int e = transform_split(mt, qv + warp * D, p.mul_sk, hw, lane);
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 4; ++i) dst[128 + lane + 32 * i] = src[lane + 32 * i];
+      if (lane == 0) p.qsc[2 * qi + 1] = ldexpf(1.0f, e);
+    }
   }
 }
 
@@ -203,8 +226,6 @@ struct SmemHead {
   float lw[CWARPS][8];
   int abort_flag;
 };
-constexpr uint32_t LUT_WINDOW = 0x10000;           // shared-window address of the table
-constexpr uint32_t RESERVED_SMEM = 1024;           // window bytes before dynamic smem
 constexpr uint32_t STAGE_A_OFF = (sizeof(SmemHead) + 15) & ~15u;
 constexpr uint32_t LUT_OFF = LUT_WINDOW - RESERVED_SMEM;
 constexpr uint32_t STAGE_B_OFF = LUT_OFF + 256 * 64 * 4;
@@ -260,33 +281,7 @@ __device__ __forceinline__ int key_of_row(int r) {
 }
 
 // Barrier over the consumer warps only (the producer warp never joins it).
-__device__ __forceinline__ void consumers_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(CWARPS * 32) : "memory");
-}
-
-// Work item = the tiles of one unit (batch, KV head, head group) inside this CTA's
-// contiguous range of the global tile sequence; units are laid end to end, so a CTA
-// touches at most a few units and each (unit, CTA) pair gives one partial.
-struct Item {
-  int unit, t0, t1, slot;  // tiles [t0, t1) of the unit; partial slot of this CTA
-};
-__device__ __forceinline__ bool next_item(const PartialParams &p, int cta, int &t, Item &it) {
-  const int end = min((cta + 1) * p.tiles_per_cta, p.total_tiles);
-  if (t >= end) return false;
-  it.unit = t / p.tiles_per_unit;
-  it.t0 = t - it.unit * p.tiles_per_unit;
-  it.t1 = min(end - it.unit * p.tiles_per_unit, p.tiles_per_unit);
-  it.slot = cta - (it.unit * p.tiles_per_unit) / p.tiles_per_cta;
-  t += it.t1 - it.t0;
-  return true;
-}
-
-__device__ __forceinline__ int unit_len(const PartialParams &p, int unit) {
-  const int b = unit / (p.Hkv * p.n_hg);
-  if (!p.seq_lens) return p.L;
-  const int v = p.seq_lens[b];
-  return v < 1 ? 1 : (v > p.L ? p.L : v);
-}
+__device__ __forceinline__ void consumers_sync() { named_sync1<CWARPS * 32>(); }
 
 // Persistent split-K decode: one CTA per SM streams its tile range through a ring of
 // NSTAGE stages.  Lane (g, t) = (lane / 4, lane % 4) of a consumer warp owns, per
@@ -713,10 +708,12 @@ bool decode_shape(const tq_ctx *k, const tq_ctx *v, int B, int Hq, int Hkv, int 
   (void)v;
   s->B = B, s->Hq = Hq, s->Hkv = Hkv, s->L = L;
   s->gq = Hq / Hkv;
-  s->heads_per_cta = s->gq <= 4 ? 4 : 8;
+  s->pv = k->fmt == TQ_FMT_PROD3;
+  s->tile = s->pv ? PV_TILE : T4_TILE;
+  s->heads_per_cta = (s->pv || s->gq > 4) ? 8 : 4;
   s->n_hg = (s->gq + s->heads_per_cta - 1) / s->heads_per_cta;
   const int64_t units = (int64_t)B * Hkv * s->n_hg;
-  s->tiles_per_unit = (L + TILE - 1) / TILE;
+  s->tiles_per_unit = (L + s->tile - 1) / s->tile;
   const int64_t total = units * s->tiles_per_unit;
   if (total > INT32_MAX) return false;
   s->total_tiles = (int)total;
@@ -751,14 +748,17 @@ cudaError_t launch_prepare_q(const tq_ctx *k, const void *q, int q_dtype, const 
   p.q_dtype = q_dtype;
   p.n_q = s.B * s.Hq;
   p.rt = k->d_pit;
+  p.st = s.pv ? k->d_St : nullptr;
   p.mul = LOG2E * scale / k->f16.alpha;
+  p.mul_sk = (float)(LOG2E * (double)scale * 1.2533141373155003 / D);  // sqrt(pi/2) / d
   p.qhl = ws.qhl;
   p.qsc = ws.qsc;
   const int grid = (p.n_q + QWARPS - 1) / QWARPS;
   const size_t smem = (size_t)D * D * 4 + QWARPS * D * 4 + QWARPS * 2 * D * 2;
-  cudaError_t e = cudaFuncSetAttribute(k_prepare_q, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto kern = s.pv ? k_prepare_q<true> : k_prepare_q<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  k_prepare_q<<<grid, QWARPS * 32, smem, st>>>(p);
+  kern<<<grid, QWARPS * 32, smem, st>>>(p);
   return cudaGetLastError();
 }
 
@@ -783,6 +783,7 @@ constexpr int V_PRMT_WORDS = 0;
 cudaError_t launch_partial(const tq_ctx *k, const tq_ctx *v, const uint8_t *kc,
                            const uint8_t *vc, const int32_t *seq_lens, const DecodeShape &s,
                            float *scores_dbg, const Workspace &ws, cudaStream_t st) {
+  if (s.pv) return launch_partial_pv(k, v, kc, vc, seq_lens, s, scores_dbg, ws, st);
   PartialParams p{};
   p.kc = kc, p.vc = vc, p.seq_lens = seq_lens;
   p.B = s.B, p.Hq = s.Hq, p.Hkv = s.Hkv, p.L = s.L, p.gq = s.gq, p.n_hg = s.n_hg;
@@ -820,8 +821,9 @@ cudaError_t launch_combine(const tq_ctx *k, const tq_ctx *v, const DecodeShape &
   p.n_split = s.n_part;
   p.Hq = s.Hq, p.gq = s.gq, p.heads_per_cta = s.heads_per_cta, p.n_hg = s.n_hg;
   p.tiles_per_unit = s.tiles_per_unit, p.tiles_per_cta = s.tiles_per_cta;
-  p.r = v->d_pi;
-  p.inv_vscale = 1.0f / (exp2f(P_SHIFT) * v->f16.alpha);
+  const bool vgroup = v->fmt == TQ_FMT_VGROUP2;  // values are not rotated
+  p.r = vgroup ? nullptr : v->d_pi;
+  p.inv_vscale = 1.0f / (exp2f(P_SHIFT) * (vgroup ? 1.0f : v->f16.alpha));
   p.out = out;
   const size_t smem = (size_t)D * D * 4 + QWARPS * D * 4;
   cudaError_t e = cudaFuncSetAttribute(k_combine, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

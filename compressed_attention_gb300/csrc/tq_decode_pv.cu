@@ -1,0 +1,471 @@
+// Fused decode over prod3 keys and vgroup2 values ("TurboQuant fused Triton kernels
+// deep dive", tricks 1-3 and "write path and codebook"): every key is scored from its
+// 2-bit MSE indices and its 1-bit QJL signs,
+//   score = n * ( <q_rot, c[idx]> + gamma * sqrt(pi/2)/d * <S q, sigma> ) * scale,
+// with q_rot = Pi q and the sketch S q computed once per query; values are the 2-bit
+// group codes, value = code * scale_G + zero_G, never expanded in memory, and not
+// rotated, so the combine applies no un-rotation.
+//
+// Persistent split-K like the turbo4 kernel: one CTA per SM takes a contiguous range
+// of 176-key tiles of the (batch, KV head, 8-head group) units; a producer warp
+// streams the K (56 B rows) and V (48 B rows) tiles with 1-D bulk copies on a
+// four-stage mbarrier ring; eleven consumer warps take 16 keys each.
+//
+// MMA orientation (m16n8k16, fp16 operands, fp32 accumulate), per 8-key block:
+//   scores  C[16 x 8 keys] = Q[16 x 128] K_hat^T : rows 0-7 hold head g's fp16 hi
+//           part, rows 8-15 its lo part, so lane (g, t) ends with head g's exact
+//           scores for keys 2t, 2t+1 -- already the layout the PV product takes.
+//           The QJL term is a second product with the +-1 signs as the B operand.
+//   PV      O^T[128 dims x 8 heads] += codes^T[dims x 16 keys] P_G^T : the codes
+//           enter as fp16 subnormal integers (bits = code, value code * 2^-24), the
+//           per-key group scale sits in P_G = p * scale_G, split hi + lo into two
+//           products with the same codes; each 16-dim m-tile lies inside one group.
+// Zero points add sum_t p_t zero_{t,G} per head and group, accumulated in fp32.
+#include <math.h>
+
+#include "tq_decode_common.cuh"
+#include "tq_device.cuh"
+#include "tq_internal.h"
+
+namespace tq {
+
+namespace {
+
+constexpr int CW = 11;                 // consumer warps, 16 keys each per tile; with the
+                                       // producer 12 warps = 3 per scheduler at 168 registers
+constexpr int NTH = (CW + 1) * 32;     // + one producer warp; one CTA per SM
+static_assert(16 * CW == PV_TILE, "a tile is 16 keys per consumer warp");
+constexpr int NST = 4;                 // pipeline stages
+constexpr int K_ROW = 56, V_ROW = 48;
+constexpr int K_BUF = PV_TILE * K_ROW + 16;  // start rounded down to 16 B
+constexpr int V_BUF = PV_TILE * V_ROW; // V rows start 16-byte aligned
+
+// Key of column c of 8-key block nb.  Chosen so that the packed-word, sign, norm and
+// header loads of a warp are free of shared-memory bank conflicts for 56- and 48-byte
+// rows (checked exhaustively on the host against the access pattern below).
+__constant__ int KEY_ORDER[2][8] = {{7, 15, 3, 11, 13, 5, 1, 9}, {12, 4, 0, 8, 14, 6, 2, 10}};
+
+struct PvParams {
+  const uint8_t *kc;
+  const uint8_t *vc;
+  const int32_t *seq_lens;
+  int B, Hq, Hkv, L, gq, n_hg;
+  int tiles_per_unit, tiles_per_cta, total_tiles, n_part;
+  const uint32_t *qhl;
+  const float *qsc;
+  float *part;
+  float *scores;
+  uint32_t kc16[2];   // the four signed fp16 entries alpha * c_k of the 2-bit table
+  int32_t *status;
+};
+
+struct PvHead {
+  float osm[CW][8][D];  // per-warp O of 8 heads (zero terms folded in), for the merge
+  float mw[CW][8];
+  float lw[CW][8];
+  float zw[CW][8][4];
+  uint64_t full[NST];
+  uint64_t empty[NST];
+  int abort_flag;
+};
+// Layout: head, value buffer 0 | MSE table at window LUT_WINDOW | value buffers 1-3,
+// key buffers 0-3, sign table.
+constexpr uint32_t VBUF0_OFF = (sizeof(PvHead) + 255) & ~255u;
+constexpr uint32_t MSE_OFF = LUT_WINDOW - RESERVED_SMEM;        // 256 x 32 slots x 8 B
+constexpr uint32_t HIGH_OFF = MSE_OFF + 256 * 32 * 8;
+constexpr uint32_t SIGN_OFF = HIGH_OFF + 3 * V_BUF + NST * K_BUF;  // 16 x 32 slots x 8 B
+constexpr uint32_t SMEM_PV = SIGN_OFF + 16 * 32 * 8;
+static_assert(VBUF0_OFF + V_BUF <= MSE_OFF, "first value buffer below the table");
+static_assert(SMEM_PV <= 227 * 1024, "shared memory budget");
+
+__device__ __forceinline__ uint8_t *kbuf(uint8_t *smem, int s) {
+  return smem + HIGH_OFF + 3 * V_BUF + s * K_BUF;
+}
+__device__ __forceinline__ uint8_t *vbuf(uint8_t *smem, int s) {
+  return smem + (s == 0 ? VBUF0_OFF : HIGH_OFF + (s - 1) * V_BUF);
+}
+
+__device__ __forceinline__ uint2 lds64(const uint8_t *p) { return *reinterpret_cast<const uint2 *>(p); }
+__device__ __forceinline__ uint32_t lds32(const uint8_t *p) { return *reinterpret_cast<const uint32_t *>(p); }
+
+// Table entry (two fp16x2 words) at shared-window offset `off` from a table base:
+// FIXED puts the base in the load's immediate (the table is at a known window address).
+template <bool FIXED, uint32_t WINDOW>
+__device__ __forceinline__ void lut2(uint32_t base, uint32_t off, uint32_t &w0, uint32_t &w1) {
+  if (FIXED)
+    asm("ld.shared.v2.u32 {%0, %1}, [%2+%3];" : "=r"(w0), "=r"(w1) : "r"(off), "n"(WINDOW));
+  else
+    asm("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(w0), "=r"(w1) : "r"(off + base));
+}
+
+// Offset (byte I of w) * 256 + lane * 8 as one byte permute of the lane word lane * 8.
+template <int I>
+__device__ __forceinline__ uint32_t lut_off(uint32_t laneword, uint32_t w) {
+  return prmt(laneword, w, 0x1100u | ((4u + I) << 4));
+}
+
+template <bool SCORES, bool FIXED>
+__global__ void __maxnreg__(168) k_partial_pv(const PvParams p) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  PvHead &sm = *reinterpret_cast<PvHead *>(smem_raw);
+  uint32_t *mse_lut = reinterpret_cast<uint32_t *>(smem_raw + MSE_OFF);
+  uint32_t *sign_lut = reinterpret_cast<uint32_t *>(smem_raw + SIGN_OFF);
+  const int cta = blockIdx.x;
+  if (FIXED && smem_addr(smem_raw) != RESERVED_SMEM) {
+    if (threadIdx.x == 0) atomicExch(p.status, (int32_t)DEVERR_LAYOUT);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], CW);
+    }
+    sm.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (threadIdx.x == 0 && p.seq_lens) {
+    for (int b = 0; b < p.B; ++b)
+      if (p.seq_lens[b] < 1 || p.seq_lens[b] > p.L) atomicExch(p.status, (int32_t)DEVERR_SEQLEN);
+  }
+  // MSE table: byte of four 2-bit indices -> (c[i0], c[i1]), (c[i2], c[i3]) as fp16x2,
+  // one 8-byte slot per lane.  Sign table: nibble of four QJL bits -> four fp16 +-1.
+  for (int piece = threadIdx.x; piece < 256 * 16; piece += NTH) {
+    const int byte = piece >> 4, chunk = piece & 15;
+    auto c = [&](int i) { return (p.kc16[i >> 1] >> (16 * (i & 1))) & 0xFFFFu; };
+    const uint32_t w0 = c(byte & 3) | (c((byte >> 2) & 3) << 16);
+    const uint32_t w1 = c((byte >> 4) & 3) | (c(byte >> 6) << 16);
+    reinterpret_cast<uint4 *>(mse_lut + byte * 64)[chunk] = make_uint4(w0, w1, w0, w1);
+  }
+  for (int piece = threadIdx.x; piece < 16 * 16; piece += NTH) {
+    const int nib = piece >> 4, chunk = piece & 15;
+    auto sg = [&](int i) { return ((nib >> i) & 1) ? 0x3C00u : 0xBC00u; };
+    const uint32_t w0 = sg(0) | (sg(1) << 16), w1 = sg(2) | (sg(3) << 16);
+    reinterpret_cast<uint4 *>(sign_lut + nib * 64)[chunk] = make_uint4(w0, w1, w0, w1);
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+
+  if (warp == CW) {
+    // ---------------- producer
+    if (lane == 0) {
+      int ctr = 0, tt = cta * p.tiles_per_cta;
+      Item it;
+      bool ok = true;
+      while (ok && next_item(p, cta, tt, it)) {
+        const int Lb = unit_len(p, it.unit);
+        const size_t unit_row0 = (size_t)(it.unit / p.n_hg) * p.L;
+        for (int j = it.t0; j < it.t1; ++j) {
+          const int kf = j * PV_TILE;
+          if (kf >= Lb) break;
+          const int nk = min(PV_TILE, Lb - kf);
+          const int s = ctr % NST;
+          if (ctr >= NST && !mbar_wait_bounded(&sm.empty[s], ((ctr / NST) - 1) & 1, WAIT_LIMIT_NS)) {
+            atomicExch(&sm.abort_flag, 1);
+            atomicExch(p.status, (int32_t)DEVERR_TIMEOUT);
+            ok = false;
+            break;
+          }
+          const size_t ks = (unit_row0 + kf) * K_ROW;
+          const size_t k0 = ks & ~(size_t)15;
+          const size_t k1 = (ks + (size_t)nk * K_ROW + 15) & ~(size_t)15;
+          const uint32_t kbytes = (uint32_t)(k1 - k0);
+          const uint32_t vbytes = (uint32_t)nk * V_ROW;  // row starts are 16-byte aligned
+          mbar_arrive_expect_tx(&sm.full[s], kbytes + vbytes);
+          bulk_g2s(kbuf(smem_raw, s), p.kc + k0, kbytes, &sm.full[s]);
+          bulk_g2s(vbuf(smem_raw, s), p.vc + (unit_row0 + kf) * V_ROW, vbytes, &sm.full[s]);
+          ++ctr;
+        }
+      }
+      if (!ok || sm.abort_flag) {
+        for (int c = (ctr > NST ? ctr - NST : 0); c < ctr; ++c)
+          (void)mbar_wait_bounded(&sm.full[c % NST], (c / NST) & 1, WAIT_LIMIT_NS);
+      }
+    }
+    return;
+  }
+
+  // ---------------- consumers
+  const uint32_t mse_base = smem_addr(mse_lut), sign_base = smem_addr(sign_lut);
+  constexpr uint32_t SIGN_WINDOW = RESERVED_SMEM + SIGN_OFF;
+  const uint32_t laneword = 8u * lane;
+  const int kb = warp * 16;
+  const int kr0 = KEY_ORDER[0][g], kr1 = KEY_ORDER[1][g];  // B-operand keys (column g)
+  int ks[4];                                               // this lane's softmax / PV keys
+  ks[0] = KEY_ORDER[0][2 * t], ks[1] = KEY_ORDER[0][2 * t + 1];
+  ks[2] = KEY_ORDER[1][2 * t], ks[3] = KEY_ORDER[1][2 * t + 1];
+  const uint32_t code_sel = (uint32_t)(g & 3) | ((4u + (g & 3)) << 8);
+  const int code_word = 4 * (g >> 2);  // byte offset of word (g >> 2) inside a group
+
+  int ctr = 0, tt = cta * p.tiles_per_cta;
+  Item it;
+  bool aborted = false;
+  while (!aborted && next_item(p, cta, tt, it)) {
+    const int Lb = unit_len(p, it.unit);
+    const int hg = it.unit % p.n_hg;
+    const int bk = it.unit / p.n_hg;
+    const int b = bk / p.Hkv, kvh = bk % p.Hkv;
+    const int G = min(8, p.gq - hg * 8);
+    const int head0 = kvh * p.gq + hg * 8;
+    const size_t unit_row0 = (size_t)bk * p.L;
+
+    // q and the sketch S q as A operands: rows g / g+8 = fp16 hi / lo of head g; k-step
+    // s covers dims 32t + 4s .. 32t + 4s + 3 in lane t.
+    uint32_t qa[8][4], qq[8][4];
+    float qsm = 0.f, qsq = 0.f;
+    if (g < G) {
+      const uint4 *qw = reinterpret_cast<const uint4 *>(p.qhl + (size_t)(b * p.Hq + head0 + g) * 256);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const uint4 mh = qw[4 * t + v], ml = qw[16 + 4 * t + v];
+        const uint4 sh = qw[32 + 4 * t + v], sl = qw[48 + 4 * t + v];
+        const uint32_t mhw[4] = {mh.x, mh.y, mh.z, mh.w}, mlw[4] = {ml.x, ml.y, ml.z, ml.w};
+        const uint32_t shw[4] = {sh.x, sh.y, sh.z, sh.w}, slw[4] = {sl.x, sl.y, sl.z, sl.w};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int s = 2 * v + h;
+          qa[s][0] = mhw[2 * h], qa[s][1] = mlw[2 * h], qa[s][2] = mhw[2 * h + 1], qa[s][3] = mlw[2 * h + 1];
+          qq[s][0] = shw[2 * h], qq[s][1] = slw[2 * h], qq[s][2] = shw[2 * h + 1], qq[s][3] = slw[2 * h + 1];
+        }
+      }
+      qsm = p.qsc[2 * (b * p.Hq + head0 + g)];
+      qsq = p.qsc[2 * (b * p.Hq + head0 + g) + 1];
+    } else {
+#pragma unroll
+      for (int s = 0; s < 8; ++s)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) qa[s][e] = qq[s][e] = 0u;
+    }
+    float O[8][4];
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) O[mt][0] = O[mt][1] = O[mt][2] = O[mt][3] = 0.f;
+    float M = -INFINITY, lsum = 0.f, zt[4] = {0.f, 0.f, 0.f, 0.f};
+
+    for (int j = it.t0; j < it.t1; ++j) {
+      const int kf = j * PV_TILE;
+      if (kf >= Lb) break;
+      const int s = ctr % NST;
+      if (!mbar_wait_bounded(&sm.full[s], (ctr / NST) & 1, WAIT_LIMIT_NS)) {
+        if (lane == 0) {
+          atomicExch(p.status, (int32_t)DEVERR_TIMEOUT);
+          atomicExch(&sm.abort_flag, 1);
+        }
+        aborted = true;
+        break;
+      }
+      if (*reinterpret_cast<volatile int *>(&sm.abort_flag)) {
+        aborted = true;
+        break;
+      }
+      const int nk = min(PV_TILE, Lb - kf);
+      const size_t kstart = (unit_row0 + kf) * K_ROW;
+      const uint8_t *Ks = kbuf(smem_raw, s) + (kstart & 15) + kb * K_ROW;
+      const uint8_t *Vs = vbuf(smem_raw, s) + kb * V_ROW;
+      const int nkb = nk - kb;
+      if (nkb > 0) {
+        // ---- scores of two 8-key blocks: MSE and QJL products
+        float cm[2][4], cq[2][4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) cm[0][e] = cm[1][e] = cq[0][e] = cq[1][e] = 0.f;
+        const uint2 m0 = lds64(Ks + kr0 * K_ROW + 8 + 8 * t), m1 = lds64(Ks + kr1 * K_ROW + 8 + 8 * t);
+        const uint32_t sw0 = lds32(Ks + kr0 * K_ROW + 40 + 4 * t), sw1 = lds32(Ks + kr1 * K_ROW + 40 + 4 * t);
+        const uint32_t ev0 = sw0 & 0x0F0F0F0Fu, od0 = (sw0 >> 4) & 0x0F0F0F0Fu;
+        const uint32_t ev1 = sw1 & 0x0F0F0F0Fu, od1 = (sw1 >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+        for (int st = 0; st < 8; ++st) {
+          const uint32_t mw0 = st < 4 ? m0.x : m0.y, mw1 = st < 4 ? m1.x : m1.y;
+          const uint32_t nw0 = (st & 1) ? od0 : ev0, nw1 = (st & 1) ? od1 : ev1;
+          uint32_t b00, b01, b10, b11, s00, s01, s10, s11;
+          uint32_t om0, om1, on0, on1;
+          switch (st & 3) {
+            case 0: om0 = lut_off<0>(laneword, mw0), om1 = lut_off<0>(laneword, mw1); break;
+            case 1: om0 = lut_off<1>(laneword, mw0), om1 = lut_off<1>(laneword, mw1); break;
+            case 2: om0 = lut_off<2>(laneword, mw0), om1 = lut_off<2>(laneword, mw1); break;
+            default: om0 = lut_off<3>(laneword, mw0), om1 = lut_off<3>(laneword, mw1); break;
+          }
+          switch (st >> 1) {
+            case 0: on0 = lut_off<0>(laneword, nw0), on1 = lut_off<0>(laneword, nw1); break;
+            case 1: on0 = lut_off<1>(laneword, nw0), on1 = lut_off<1>(laneword, nw1); break;
+            case 2: on0 = lut_off<2>(laneword, nw0), on1 = lut_off<2>(laneword, nw1); break;
+            default: on0 = lut_off<3>(laneword, nw0), on1 = lut_off<3>(laneword, nw1); break;
+          }
+          lut2<FIXED, LUT_WINDOW>(mse_base, om0, b00, b01);
+          lut2<FIXED, LUT_WINDOW>(mse_base, om1, b10, b11);
+          lut2<FIXED, SIGN_WINDOW>(sign_base, on0, s00, s01);
+          lut2<FIXED, SIGN_WINDOW>(sign_base, on1, s10, s11);
+          mma_f16(cm[0], qa[st], b00, b01);
+          mma_f16(cm[1], qa[st], b10, b11);
+          mma_f16(cq[0], qq[st], s00, s01);
+          mma_f16(cq[1], qq[st], s10, s11);
+        }
+        // ---- online softmax for head g over keys ks[0..3]
+        float sc[4], u[4], tn[4];
+        uint4 hv[4];  // value headers: word G = (fp16 scale_G, fp16 zero_G)
+        bool ok[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int kr = ks[i];
+          ok[i] = kr < nkb;
+          const float2 ng = *reinterpret_cast<const float2 *>(Ks + kr * K_ROW);
+          hv[i] = *reinterpret_cast<const uint4 *>(Vs + kr * V_ROW + 32);
+          if (!ok[i]) hv[i] = make_uint4(0u, 0u, 0u, 0u);
+          const float smax = fmaxf(fmaxf(__half2float(__ushort_as_half((unsigned short)(hv[i].x & 0xFFFFu))),
+                                         __half2float(__ushort_as_half((unsigned short)(hv[i].y & 0xFFFFu)))),
+                                   fmaxf(__half2float(__ushort_as_half((unsigned short)(hv[i].z & 0xFFFFu))),
+                                         __half2float(__ushort_as_half((unsigned short)(hv[i].w & 0xFFFFu)))));
+          // nu = exponent with smax * 2^-nu in [1/2, 1) (scales are >= 0); 2^-nu exact
+          int nu = (int)((__float_as_uint(smax) >> 23) & 0xFF) - 126;
+          nu = max(nu, -64);
+          tn[i] = __uint_as_float((uint32_t)(127 - nu) << 23);
+          const int nb = i >> 1, e = i & 1;
+          const float mse = cm[nb][e] + cm[nb][2 + e];
+          const float qjl = cq[nb][e] + cq[nb][2 + e];
+          sc[i] = ok[i] ? ng.x * fmaf(ng.y * qsq, qjl, qsm * mse) : -INFINITY;
+          u[i] = sc[i] + (float)nu;
+          if (SCORES && ok[i] && g < G)
+            p.scores[(size_t)(b * p.Hq + head0 + g) * p.L + kf + kb + kr] = sc[i] * LN2;
+        }
+        float bm = fmaxf(fmaxf(u[0], u[1]), fmaxf(u[2], u[3]));
+        bm = fmaxf(bm, __shfl_xor_sync(FULL_MASK, bm, 1));
+        bm = fmaxf(bm, __shfl_xor_sync(FULL_MASK, bm, 2));
+        const bool need = bm > M + RESCALE_SLACK;  // also taken while M is -inf
+        if (__any_sync(FULL_MASK, need)) {
+          const float alpha = need ? exp2_approx(M - bm) : 1.f;
+          if (need) M = bm;
+          lsum *= alpha;
+#pragma unroll
+          for (int G4 = 0; G4 < 4; ++G4) zt[G4] *= alpha;
+          const float aa = __shfl_sync(FULL_MASK, alpha, 8 * t), ab = __shfl_sync(FULL_MASK, alpha, 8 * t + 4);
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) O[mt][0] *= aa, O[mt][1] *= ab, O[mt][2] *= aa, O[mt][3] *= ab;
+        }
+        const float Mu = (M == -INFINITY) ? 0.f : M;
+        float pp[4], pw[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          lsum += exp2_approx(sc[i] - Mu);
+          pp[i] = exp2_approx(u[i] - Mu + P_SHIFT);  // 2^(s - M + P) * 2^nu
+          pw[i] = pp[i] * tn[i];                      // 2^(s - M + P)
+        }
+        // ---- PV per group: codes as the A operand, p * scale_G (hi + lo) as B; the
+        // zero points accumulate in fp32.
+#pragma unroll
+        for (int G4 = 0; G4 < 4; ++G4) {
+          float sg[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t w = G4 == 0 ? hv[i].x : G4 == 1 ? hv[i].y : G4 == 2 ? hv[i].z : hv[i].w;
+            const float2 sz = __half22float2(*reinterpret_cast<const __half2 *>(&w));
+            sg[i] = sz.x;
+            zt[G4] = fmaf(pw[i], sz.y, zt[G4]);
+          }
+          uint32_t b0h, b0l, b1h, b1l;
+          split_half2(pp[0] * (sg[0] * tn[0]), pp[1] * (sg[1] * tn[1]), b0h, b0l);
+          split_half2(pp[2] * (sg[2] * tn[2]), pp[3] * (sg[3] * tn[3]), b1h, b1l);
+          const int wo = 8 * G4 + code_word;
+          const uint32_t wa = lds32(Vs + ks[0] * V_ROW + wo), wb = lds32(Vs + ks[1] * V_ROW + wo);
+          const uint32_t wc = lds32(Vs + ks[2] * V_ROW + wo), wd = lds32(Vs + ks[3] * V_ROW + wo);
+          const uint32_t zab = prmt(wa, wb, code_sel), zcd = prmt(wc, wd, code_sel);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t a[4] = {(zab >> (4 * h)) & 0x00030003u, (zab >> (4 * h + 2)) & 0x00030003u,
+                                   (zcd >> (4 * h)) & 0x00030003u, (zcd >> (4 * h + 2)) & 0x00030003u};
+            mma_f16(O[2 * G4 + h], a, b0h, b1h);
+            mma_f16(O[2 * G4 + h], a, b0l, b1l);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.empty[s]);
+      ++ctr;
+    }
+    if (aborted || *reinterpret_cast<volatile int *>(&sm.abort_flag)) break;
+    lsum += __shfl_xor_sync(FULL_MASK, lsum, 1);
+    lsum += __shfl_xor_sync(FULL_MASK, lsum, 2);
+#pragma unroll
+    for (int G4 = 0; G4 < 4; ++G4) {
+      zt[G4] += __shfl_xor_sync(FULL_MASK, zt[G4], 1);
+      zt[G4] += __shfl_xor_sync(FULL_MASK, zt[G4], 2);
+    }
+
+    // ---- merge the consumer warps' states of this item and write its partial
+    if (t == 0) {
+      sm.mw[warp][g] = M;
+      sm.lw[warp][g] = lsum;
+#pragma unroll
+      for (int G4 = 0; G4 < 4; ++G4) sm.zw[warp][g][G4] = zt[G4];
+    }
+    named_sync1<CW * 32>();
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int hh = 2 * t + e;  // head of accumulator columns c0/c2 (e = 0), c1/c3 (e = 1)
+      float ms = -INFINITY;
+      for (int w = 0; w < CW; ++w) ms = fmaxf(ms, sm.mw[w][hh]);
+      const float mine = sm.mw[warp][hh];
+      const float fac = (mine == -INFINITY) ? 0.f : exp2_approx(mine - ms);
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        const int G4 = mt >> 1;
+        const float z = sm.zw[warp][hh][G4];
+        const int d0 = 32 * G4 + 4 * g + 2 * (mt & 1);
+        sm.osm[warp][hh][d0] = fmaf(O[mt][e], 16777216.f, z) * fac;
+        sm.osm[warp][hh][d0 + 1] = fmaf(O[mt][2 + e], 16777216.f, z) * fac;
+      }
+    }
+    named_sync1<CW * 32>();
+    for (int idx = threadIdx.x; idx < G * D; idx += CW * 32) {
+      const int hh = idx / D, jd = idx % D;
+      float ms = -INFINITY;
+      for (int w = 0; w < CW; ++w) ms = fmaxf(ms, sm.mw[w][hh]);
+      float acc = 0.f;
+      for (int w = 0; w < CW; ++w) acc += sm.osm[w][hh][jd];
+      float *dst = p.part + ((size_t)(b * p.Hq + head0 + hh) * p.n_part + it.slot) * PARTIAL_FLOATS;
+      dst[6 + jd] = (ms == -INFINITY) ? 0.f : acc;
+      if (jd < 6) {
+        float v = 0.f;
+        if (jd == 0) {
+          v = ms;
+        } else if (jd == 1 && ms != -INFINITY) {
+          for (int w = 0; w < CW; ++w)
+            if (sm.mw[w][hh] != -INFINITY) v += sm.lw[w][hh] * exp2_approx(sm.mw[w][hh] - ms);
+        }
+        dst[jd] = v;
+      }
+    }
+    named_sync1<CW * 32>();
+  }
+}
+
+template <bool SC, bool FIXED>
+cudaError_t launch_pv(const PvParams &p, dim3 grid, cudaStream_t st) {
+  auto kern = k_partial_pv<SC, FIXED>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_PV);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, NTH, SMEM_PV, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_partial_pv(const tq_ctx *k, const tq_ctx *v, const uint8_t *kc,
+                              const uint8_t *vc, const int32_t *seq_lens, const DecodeShape &s,
+                              float *scores_dbg, const Workspace &ws, cudaStream_t st) {
+  (void)v;
+  PvParams p{};
+  p.kc = kc, p.vc = vc, p.seq_lens = seq_lens;
+  p.B = s.B, p.Hq = s.Hq, p.Hkv = s.Hkv, p.L = s.L, p.gq = s.gq, p.n_hg = s.n_hg;
+  p.tiles_per_unit = s.tiles_per_unit, p.tiles_per_cta = s.tiles_per_cta;
+  p.total_tiles = s.total_tiles, p.n_part = s.n_part;
+  p.qhl = ws.qhl, p.qsc = ws.qsc, p.part = ws.partials, p.scores = scores_dbg;
+  p.kc16[0] = k->f16.c16[0], p.kc16[1] = k->f16.c16[1];
+  p.status = k->d_status;
+  dim3 grid(s.grid);
+  const bool fixed = k->reserved_smem == (int)RESERVED_SMEM;
+  if (fixed) return scores_dbg ? launch_pv<true, true>(p, grid, st) : launch_pv<false, true>(p, grid, st);
+  return scores_dbg ? launch_pv<true, false>(p, grid, st) : launch_pv<false, false>(p, grid, st);
+}
+
+}  // namespace tq

@@ -78,8 +78,13 @@ cudaError_t launch_write(const tq_ctx *ctx, const WriteLaunch &w, cudaStream_t s
 cudaError_t launch_dequantize(const tq_ctx *ctx, const uint8_t *cache, int64_t n_rows,
                               int unrotate, float *dst, cudaStream_t st);
 
+constexpr int T4_TILE = 240;  // keys per tile of the turbo4 decode
+constexpr int PV_TILE = 176;  // keys per tile of the prod3-key / vgroup2-value decode
+
 struct DecodeShape {
   int B, Hq, Hkv, L;
+  int tile;     // keys per tile (T4_TILE or PV_TILE)
+  bool pv;      // prod3 keys with vgroup2 values
   int gq;       // q-heads per KV head
   int heads_per_cta;  // q-heads one CTA serves (4 or 8)
   int n_hg;     // head groups per KV head
@@ -106,6 +111,9 @@ cudaError_t launch_prepare_q(const tq_ctx *k, const void *q, int q_dtype, const 
 cudaError_t launch_partial(const tq_ctx *k, const tq_ctx *v, const uint8_t *kc,
                            const uint8_t *vc, const int32_t *seq_lens, const DecodeShape &s,
                            float *scores_dbg, const Workspace &ws, cudaStream_t st);
+cudaError_t launch_partial_pv(const tq_ctx *k, const tq_ctx *v, const uint8_t *kc,
+                              const uint8_t *vc, const int32_t *seq_lens, const DecodeShape &s,
+                              float *scores_dbg, const Workspace &ws, cudaStream_t st);
 cudaError_t launch_combine(const tq_ctx *k, const tq_ctx *v, const DecodeShape &s, float *out,
                            const Workspace &ws, cudaStream_t st);
 
