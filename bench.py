@@ -1,17 +1,26 @@
-"""Benchmark of the compressed-KV decode step on GB300.
+"""Benchmark of the compressed-KV hot path on GB300.
 
-One step = one decode step of the whole hot path on the GQA workload
+Default (the headline line): one decode step of the whole path on the GQA workload
 (B=8, Hq=32, Hkv=8, d=128, context 32,768, turbo4 4-bit K and V, dense seeded
 rotation, bf16 q, K/V N(0,1) x per-channel lognormal(0, 0.5) with 1% x8 outlier
 channels):
   write path : SET_ROWS of the step's new K and V rows (B*Hkv each) into the cache,
   read path  : q rotation + split, split-K fused decode over the packed cache,
                combine + un-rotation.
-The metric is effective HBM bandwidth of the decode (algorithmic bytes / time),
-with keys/s alongside; the dominant kernel (split-K decode) is also timed alone
-for the roofline.  Inputs are synthetic and seeded (see synth.py).
+The metric is effective HBM bandwidth of the decode (algorithmic bytes / time), with
+keys/s alongside; the dominant kernel (split-K decode) is also timed alone for the
+roofline.
+
+--workload picks another workload of the same path:
+  long_context  B=1, Hq=32, Hkv=8, L=131,072, turbo4 K and V, randomized WHT
+  prod_vgroup   B=4, Hq=24, Hkv=4, L=30,000, prod3 keys (2-bit + QJL), vgroup2 values
+  single_head   B=1, Hq=Hkv=1, L=512, fp32 q, turbo4 K and V, randomized WHT
+  write_chunk   SET_ROWS of 16,384 tokens x 8 KV heads of bf16 K and V
+                (--write-format turbo4|turbo3, --write-rotation dense|wht)
+Inputs are synthetic and seeded (see synth.py).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tq|reference]
+                       [--workload NAME]
 Under torchrun every rank runs the same per-GPU workload (weak scaling) and rank 0
 prints one JSON line.
 """
@@ -19,7 +28,6 @@ prints one JSON line.
 import argparse
 import hashlib
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -34,20 +42,26 @@ sys.path.insert(0, ROOT)
 
 import synth  # noqa: E402
 
-METRIC = "fused compressed-KV decode attention: effective HBM GB/s (% of peak), keys/s"
-WORKLOAD = "gqa_lognormal"
-ROT_SEED_K, ROT_SEED_V = 2, 102
-ROW_BYTES = 68
+DECODE_METRIC = "fused compressed-KV decode attention: effective HBM GB/s (% of peak), keys/s"
+WRITE_METRIC = "quantize / SET_ROWS write path: effective HBM GB/s (% of peak), rows/s"
 L2_FLUSH_BYTES = 256 << 20
-PROFILE = os.path.join(ROOT, "profiles", "decode_partial_gqa_lognormal.md")
 FALLBACK_HBM_GBS = 6800.0
+ROW_BYTES = {"turbo4": 68, "turbo3": 56, "prod3": 56, "vgroup2": 48}
+CSRC = os.path.join(ROOT, "compressed_attention_gb300", "csrc")
 
-
-def algorithmic_bytes(cfg):
-    """Packed K + V of every key of every KV head, plus q (bf16) in and out (fp32)."""
-    B, Hq, Hkv, L = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["L"]
-    kv = B * Hkv * L * 2 * ROW_BYTES
-    return kv, kv + B * Hq * 128 * 2 + B * Hq * 128 * 4
+# Decode workloads: formats, rotation and seeds of the K and V contexts, and the kernel
+# that dominates the step.
+DECODE = {
+    "gqa_lognormal": dict(k_fmt="turbo4", v_fmt="turbo4", rotation="dense", k_seed=2, v_seed=102, qjl_seed=0,
+                          kernel="k_partial_t4", source="tq_decode.cu"),
+    "long_context": dict(k_fmt="turbo4", v_fmt="turbo4", rotation="wht", k_seed=5, v_seed=105, qjl_seed=0,
+                         kernel="k_partial_t4", source="tq_decode.cu"),
+    "prod_vgroup": dict(k_fmt="prod3", v_fmt="vgroup2", rotation="dense", k_seed=3, v_seed=0, qjl_seed=1003,
+                        kernel="k_partial_pv", source="tq_decode_pv.cu"),
+    "single_head": dict(k_fmt="turbo4", v_fmt="turbo4", rotation="wht", k_seed=0, v_seed=100, qjl_seed=0,
+                        kernel="k_partial_t4", source="tq_decode.cu"),
+}
+WRITE_KERNEL = {"dense": ("k_write_dense", "tq_write.cu"), "wht": ("k_write_wht", "tq_write.cu")}
 
 
 def measured_peak():
@@ -58,18 +72,19 @@ def measured_peak():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def profiled_traffic():
-    """Per-launch DRAM bytes of the decode kernel from the committed ncu summary, or None
-    when the kernel source changed since the capture."""
-    if not os.path.exists(PROFILE):
+def profiled_traffic(profile_name, source):
+    """Per-launch DRAM bytes of a kernel from its committed ncu summary
+    (profiles/<profile_name>.md), or None when the kernel source changed since the
+    capture or there is no summary."""
+    path = os.path.join(ROOT, "profiles", profile_name + ".md")
+    if not os.path.exists(path):
         return None
     fields = {}
-    for ln in open(PROFILE):
+    for ln in open(path):
         if ":" in ln and ln.strip().startswith("- "):
             k, v = ln.strip()[2:].split(":", 1)
             fields[k.strip()] = v.strip()
-    src = os.path.join(ROOT, "compressed_attention_gb300", "csrc", "tq_decode.cu")
-    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    digest = hashlib.sha256(open(os.path.join(CSRC, source), "rb").read()).hexdigest()[:16]
     if fields.get("source_sha256_16") != digest:
         return None
     try:
@@ -149,124 +164,182 @@ def job_rate(units_per_rank, world, ms):
 
 # ----------------------------------------------------------------------------- CPU side
 
-def cpu_oracle_sample(cfg, min_seconds=10.0, max_units=64):
-    """Time the oracle (fp64 dequantize-then-softmax attention) on whole (b, KV head) units
-    of the workload until about ``min_seconds`` of CPU work; returns GB/s and keys/s."""
-    import oracle
+def decode_codecs(spec):
     from oracle.formats import Codec
-    kc = Codec("turbo4", rotation="dense", rot_seed=ROT_SEED_K)
-    vc = Codec("turbo4", rotation="dense", rot_seed=ROT_SEED_V)
-    q32, _ = synth.queries(cfg)
-    L, g = cfg["L"], cfg["Hq"] // cfg["Hkv"]
-    elapsed, units = 0.0, 0
+
+    def make(fmt, seed):
+        if fmt == "vgroup2":
+            return Codec("vgroup2")
+        return Codec(fmt, rotation=spec["rotation"], rot_seed=seed, qjl_seed=spec["qjl_seed"])
+    return make(spec["k_fmt"], spec["k_seed"]), make(spec["v_fmt"], spec["v_seed"])
+
+
+def unit_rows(name, cfg, tensor, b, h):
+    """K or V rows of one (batch, KV head) unit: (fp32 values, bf16 bits or None)."""
+    if name == "single_head":
+        K, V, _ = synth.single_head_inputs()
+        return (K if tensor == "K" else V), None
+    return synth.kv_unit(cfg, tensor, b, h)
+
+
+def decode_queries(name, cfg):
+    """q [B, Hq, 128]: (fp32 values, bf16 bits or None)."""
+    if name == "single_head":
+        return synth.single_head_inputs()[2].reshape(1, 1, 128), None
+    return synth.queries(cfg)
+
+
+def decode_unit_bytes(spec):
+    return ROW_BYTES[spec["k_fmt"]] + ROW_BYTES[spec["v_fmt"]]
+
+
+class OracleDecode:
+    """The oracle (fp64 dequantize-then-softmax attention) over whole (batch, KV head)
+    units of a decode workload; inputs are encoded once, outside any timing."""
+
+    def __init__(self, name, n_units=2):
+        import oracle
+        self.attend = oracle.attention_reference
+        self.cfg, self.spec = synth.WORKLOADS[name], DECODE[name]
+        self.kc, self.vc = decode_codecs(self.spec)
+        self.q32, _ = decode_queries(name, self.cfg)
+        self.g = self.cfg["Hq"] // self.cfg["Hkv"]
+        self.blocks = []
+        for u in range(min(n_units, self.cfg["B"] * self.cfg["Hkv"])):
+            b, h = divmod(u, self.cfg["Hkv"])
+            self.blocks.append((b, h, self.kc.encode(unit_rows(name, self.cfg, "K", b, h)[0])[0],
+                                self.vc.encode(unit_rows(name, self.cfg, "V", b, h)[0])[0]))
+
+    def unit(self, i):
+        b, h, kb, vb = self.blocks[i % len(self.blocks)]
+        self.attend(self.q32[b:b + 1, h * self.g:(h + 1) * self.g], self.kc.dequantize(kb)[None, None],
+                    self.vc.dequantize(vb)[None, None])
+        return self.cfg["L"]
+
+
+class OracleWrite:
+    """The oracle encoder over a block of rows of the write workload."""
+
+    def __init__(self, fmt, rotation, n_tokens=256):
+        from oracle.formats import Codec
+        cfg = synth.WORKLOADS["write_chunk"]
+        self.codec = Codec(fmt, rotation=rotation, rot_seed=cfg["seed"])
+        self.x32, _ = synth.write_rows(cfg, "K", n_tokens=n_tokens)
+
+    def unit(self, i):
+        self.codec.encode(self.x32)
+        return len(self.x32)
+
+
+def cpu_sample(oracle_leg, unit_bytes, what, min_seconds=10.0, max_units=64):
+    """Time the oracle on whole units until about min_seconds of CPU work."""
+    elapsed, units, items = 0.0, 0, 0
     while units < max_units and (elapsed < min_seconds or units == 0):
-        b, h = divmod(units, cfg["Hkv"])
-        b %= cfg["B"]
-        kb = kc.encode(synth.kv_unit(cfg, "K", b, h)[0])[0]  # inputs: packed blocks (untimed)
-        vb = vc.encode(synth.kv_unit(cfg, "V", b, h)[0])[0]
         t0 = time.perf_counter()
-        kh = kc.dequantize(kb)[None, None]
-        vh = vc.dequantize(vb)[None, None]
-        oracle.attention_reference(q32[b:b + 1, h * g:(h + 1) * g], kh, vh)
+        items += oracle_leg.unit(units)
         elapsed += time.perf_counter() - t0
         units += 1
-    keys = units * L
-    return {"gbs": keys * 2 * ROW_BYTES / elapsed / 1e9, "keys_per_s": keys / elapsed, "units": units,
-            "seconds": elapsed}
+    return {"value": items * unit_bytes / elapsed / 1e9, "unit": "GB/s", "cores": os.cpu_count(),
+            "kind": "oracle", "rate": items / elapsed,
+            "sample": f"{units} {what}, {elapsed:.1f} s"}
 
 
 def run_reference(args, rank, world):
+    """The reference arm: the oracle as it stands on the host cores, one bounded sample of
+    the workload per step, on rank 0 only."""
     if rank != 0:
         return
-    cfg = synth.WORKLOADS[WORKLOAD]
-    import oracle
-    from oracle.formats import Codec
-    kc = Codec("turbo4", rotation="dense", rot_seed=ROT_SEED_K)
-    vc = Codec("turbo4", rotation="dense", rot_seed=ROT_SEED_V)
-    q32, _ = synth.queries(cfg)
-    g = cfg["Hq"] // cfg["Hkv"]
-    blocks = {}
-    for u in range(2):
-        b, h = divmod(u, cfg["Hkv"])
-        blocks[u] = (kc.encode(synth.kv_unit(cfg, "K", b, h)[0])[0], vc.encode(synth.kv_unit(cfg, "V", b, h)[0])[0])
-
-    def step(u):
-        b, h = divmod(u, cfg["Hkv"])
-        kb, vb = blocks[u % 2]
-        oracle.attention_reference(q32[b:b + 1, h * g:(h + 1) * g], kc.dequantize(kb)[None, None],
-                                   vc.dequantize(vb)[None, None])
-
+    if args.workload == "write_chunk":
+        leg = OracleWrite(args.write_format, args.write_rotation)
+        unit_bytes = 256 + ROW_BYTES[args.write_format]
+        metric, what = WRITE_METRIC, f"blocks of {len(leg.x32)} bf16 rows encoded by the oracle"
+        config = write_config(args)
+    else:
+        leg = OracleDecode(args.workload)
+        unit_bytes = decode_unit_bytes(leg.spec)
+        metric = DECODE_METRIC
+        what = (f"(batch, KV head) units of {leg.cfg['L']} keys x {leg.g} q-heads, "
+                "fp64 dequantize-then-softmax")
+        config = decode_config(args.workload)
     for i in range(args.warmup):
-        step(i)
+        leg.unit(i)
     t0 = time.perf_counter()
-    for i in range(args.steps):
-        step(i)
+    items = sum(leg.unit(i) for i in range(args.steps))
     dt = time.perf_counter() - t0
-    keys = args.steps * cfg["L"]
-    gbs = keys * 2 * ROW_BYTES / dt / 1e9
-    sample = f"one (batch, KV head) unit per step: {cfg['L']} keys x {g} q-heads"
-    line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world,
+    gbs = items * unit_bytes / dt / 1e9
+    line = {"impl": "reference", "metric": metric, "value": gbs, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": config_dict(cfg),
-            "keys_per_s": keys / dt,
+            "data": "synthetic", "config": config, "items_per_s": items / dt,
             "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
-                             "sample": sample},
+                             "sample": f"one of {what} per step"},
             "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
-def config_dict(cfg):
-    return {"workload": f"{WORKLOAD}: B={cfg['B']} Hq={cfg['Hq']} Hkv={cfg['Hkv']} d=128 L={cfg['L']}",
+def decode_config(name):
+    cfg, spec = synth.WORKLOADS[name], DECODE[name]
+    return {"workload": f"{name}: B={cfg['B']} Hq={cfg['Hq']} Hkv={cfg['Hkv']} d=128 L={cfg['L']}",
             "B": cfg["B"], "Hq": cfg["Hq"], "Hkv": cfg["Hkv"], "L": cfg["L"], "d": 128,
-            "k_format": "turbo4", "v_format": "turbo4", "rotation": "dense",
-            "l2": "flushed before every step: 256 MB write then a read of it (no dirty lines left); "
-                  "packed K/V 285 MB > 129 MB L2",
+            "k_format": spec["k_fmt"], "v_format": spec["v_fmt"], "rotation": spec["rotation"],
+            "q_dtype": cfg["q_dtype"],
+            "l2": "flushed before every step: 256 MB write then a read of it (no dirty lines left)",
             "launch": "each step replayed from CUDA graphs, steps queued back to back"}
+
+
+def write_config(args):
+    cfg = synth.WORKLOADS["write_chunk"]
+    return {"workload": f"write_chunk: {cfg['N']} tokens x {cfg['Hkv']} KV heads x 128, bf16 K and V",
+            "rows_per_tensor": cfg["N"] * cfg["Hkv"], "format": args.write_format,
+            "rotation": args.write_rotation,
+            "l2": "flushed before every step: 256 MB write then a read of it (no dirty lines left)",
+            "launch": "each step replayed from a CUDA graph, steps queued back to back"}
 
 
 # ----------------------------------------------------------------------------- GPU side
 
-def build_workload(tq, torch, cfg, device):
+def make_ctx(tq, fmt, spec, seed):
+    if fmt == "vgroup2":
+        return tq.Ctx("vgroup2")
+    return tq.Ctx(fmt, spec["rotation"], seed, spec["qjl_seed"])
+
+
+def to_device_rows(torch, x32, bits, device):
+    if bits is None:
+        return torch.from_numpy(np.ascontiguousarray(x32, dtype=np.float32)).to(device)
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def build_decode(name, tq, torch, device):
+    cfg, spec = synth.WORKLOADS[name], DECODE[name]
     B, Hq, Hkv, L = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["L"]
-    kctx = tq.Ctx("turbo4", "dense", ROT_SEED_K)
-    vctx = tq.Ctx("turbo4", "dense", ROT_SEED_V)
-    kc = tq.alloc_cache("turbo4", B * Hkv * L, device)
-    vc = tq.alloc_cache("turbo4", B * Hkv * L, device)
+    kctx = make_ctx(tq, spec["k_fmt"], spec, spec["k_seed"])
+    vctx = make_ctx(tq, spec["v_fmt"], spec, spec["v_seed"])
+    kc = tq.alloc_cache(spec["k_fmt"], B * Hkv * L, device)
+    vc = tq.alloc_cache(spec["v_fmt"], B * Hkv * L, device)
     for tensor, ctx, cache in (("K", kctx, kc), ("V", vctx, vc)):
         for b in range(B):
             for h in range(Hkv):
-                _, bits = synth.kv_unit(cfg, tensor, b, h)
-                src = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(device)
+                x32, bits = unit_rows(name, cfg, tensor, b, h)
+                src = to_device_rows(torch, x32, bits, device)
                 rows = torch.arange((b * Hkv + h) * L, (b * Hkv + h + 1) * L, dtype=torch.int64, device=device)
                 tq.tq_quantize_set_rows(ctx, src, cache, row_ids=rows)
-    _, qbits = synth.queries(cfg)
-    q = torch.from_numpy(qbits.view(np.int16)).view(torch.bfloat16).to(device)
+    q32, qbits = decode_queries(name, cfg)
+    q = to_device_rows(torch, q32, qbits, device).reshape(B, Hq, 128)
     # the step's new token: one K and one V row per (b, KV head), written to slot L-1
     rng = np.random.default_rng([cfg["seed"], 99])
-    new_k = torch.from_numpy(synth.bf16_bits(rng.standard_normal((B * Hkv, 128), dtype=np.float32))
-                             .view(np.int16)).view(torch.bfloat16).to(device)
-    new_v = torch.from_numpy(synth.bf16_bits(rng.standard_normal((B * Hkv, 128), dtype=np.float32))
-                             .view(np.int16)).view(torch.bfloat16).to(device)
+    new = []
+    for _ in range(2):
+        x = rng.standard_normal((B * Hkv, 128), dtype=np.float32)
+        new.append(to_device_rows(torch, x, synth.bf16_bits(x) if cfg["kv_dtype"] == "bf16" else None, device))
     slots = torch.tensor([(u + 1) * L - 1 for u in range(B * Hkv)], dtype=torch.int64, device=device)
     ws = tq.alloc_workspace(tq.tq_decode_workspace_size(kctx, vctx, B, Hq, Hkv, L), device)
     out = torch.empty((B, Hq, 128), dtype=torch.float32, device=device)
     torch.cuda.synchronize()
-    return dict(kctx=kctx, vctx=vctx, kc=kc, vc=vc, q=q, new_k=new_k, new_v=new_v, slots=slots, ws=ws, out=out)
+    return dict(kctx=kctx, vctx=vctx, kc=kc, vc=vc, q=q, new_k=new[0], new_v=new[1], slots=slots, ws=ws, out=out)
 
 
-def run_tq(args, rank, world, dist):
-    import torch
-
-    import compressed_attention_gb300 as tq
-
-    local = int(os.environ.get("LOCAL_RANK", 0))
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-    cfg = synth.WORKLOADS[WORKLOAD]
-    B, Hq, Hkv, L = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["L"]
-    w = build_workload(tq, torch, cfg, device)
-    stream = torch.cuda.current_stream()
+def flusher(torch, device):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     flush_f32 = flush.view(torch.float32)
 
@@ -276,8 +349,66 @@ def run_tq(args, rank, world, dist):
         # so the timed step neither hits cached inputs nor pays for the flush's write-backs.
         flush.zero_()
         flush_f32.sum()
+    return flush_l2
 
-    launches_per_step = 5
+
+def graphs_of(torch, fns, warmup, flush_l2):
+    """Warm the callables up eagerly, capture each in its own CUDA graph, warm the graphs."""
+    for _ in range(warmup):
+        flush_l2()
+        for fn in fns:
+            fn()
+    torch.cuda.synchronize()
+    graphs = []
+    for fn in fns:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        graphs.append(g)
+    for _ in range(warmup):
+        flush_l2()
+        for g in graphs:
+            g.replay()
+    torch.cuda.synchronize()
+    return graphs
+
+
+def timed_graph_steps(torch, stream, graphs, steps, flush_l2):
+    """Replay the graphs once per step with events between them; steps and flushes are
+    queued without a host synchronisation, so the host runs ahead of the device and no
+    enqueue gap enters a timed region.  Returns per-step event times (ms) between
+    consecutive graphs: [steps][len(graphs)]."""
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(graphs) + 1)] for _ in range(steps)]
+    for e in ev:
+        flush_l2()
+        e[0].record(stream)
+        for i, g in enumerate(graphs):
+            g.replay()
+            e[i + 1].record(stream)
+    torch.cuda.synchronize()
+    return [[e[i].elapsed_time(e[i + 1]) for i in range(len(graphs))] for e in ev]
+
+
+def common_line(metric, args, world, ms_per_step, value, config, dtype):
+    return {"metric": metric, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": dtype, "data": "synthetic", "config": config}
+
+
+def run_decode(args, rank, world, dist):
+    import torch
+
+    import compressed_attention_gb300 as tq
+
+    name = args.workload
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    cfg, spec = synth.WORKLOADS[name], DECODE[name]
+    B, Hq, Hkv, L = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["L"]
+    w = build_decode(name, tq, torch, device)
+    stream = torch.cuda.current_stream()
+    flush_l2 = flusher(torch, device)
 
     def write_and_prepare():
         tq.tq_quantize_set_rows(w["kctx"], w["new_k"], w["kc"], row_ids=w["slots"])
@@ -290,73 +421,37 @@ def run_tq(args, rank, world, dist):
     def combine():
         tq.tq_decode_combine(w["kctx"], w["vctx"], w["out"], w["ws"], B, Hq, Hkv, L)
 
-    for _ in range(args.warmup):
-        flush_l2()
-        write_and_prepare()
-        partial()
-        combine()
-    torch.cuda.synchronize()
-
+    launches_per_step = 5
     # The step is replayed from three CUDA graphs (write + q preparation, split-K decode,
-    # combine) so host launch latency stays out of the device-timed region; events between
-    # the graphs time the decode kernel alone on the same stream.
-    graphs = []
-    for fn in (write_and_prepare, partial, combine):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            fn()
-        graphs.append(g)
-    for _ in range(args.warmup):
-        flush_l2()
-        for g in graphs:
-            g.replay()
-    torch.cuda.synchronize()
+    # combine); the events between them time the decode kernel alone on its stream.
+    graphs = graphs_of(torch, (write_and_prepare, partial, combine), args.warmup, flush_l2)
     if dist:
         dist.barrier()
-
-    def timed_steps():
-        # Every step and its L2 flush are queued without a host synchronisation in between,
-        # so the host runs ahead of the device and no enqueue gap enters a timed region.
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-        for e in ev:
-            flush_l2()
-            e[0].record(stream)
-            graphs[0].replay()
-            e[1].record(stream)
-            graphs[1].replay()
-            e[2].record(stream)
-            graphs[2].replay()
-            e[3].record(stream)
-        torch.cuda.synchronize()
-        return ([e[0].elapsed_time(e[3]) for e in ev], [e[1].elapsed_time(e[2]) for e in ev])
-
     with ClockSampler(local) as clocks:
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
-        step_ms, part_ms = timed_steps()
-        torch.cuda.synchronize()
+        times = timed_graph_steps(torch, stream, graphs, args.steps, flush_l2)
         if dist:
             dist.barrier()
     clk = clocks.summary()
-    total_ms = max_over_ranks(sum(step_ms), dist, device)
+    total_ms = max_over_ranks(sum(sum(t) for t in times), dist, device)
+    part_avg = max_over_ranks(statistics.mean(t[1] for t in times), dist, device)
 
     # end to end through the public API with host buffers: q and the new K/V rows copied in,
     # the output read back, every step.
-    hq = torch.empty(w["q"].shape, dtype=torch.bfloat16, pin_memory=True).copy_(w["q"].cpu())
-    hk = torch.empty(w["new_k"].shape, dtype=torch.bfloat16, pin_memory=True).copy_(w["new_k"].cpu())
-    hv = torch.empty(w["new_v"].shape, dtype=torch.bfloat16, pin_memory=True).copy_(w["new_v"].cpu())
+    pinned = {k: torch.empty(w[k].shape, dtype=w[k].dtype, pin_memory=True).copy_(w[k].cpu())
+              for k in ("q", "new_k", "new_v")}
     hout = torch.empty(w["out"].shape, dtype=torch.float32, pin_memory=True)
-    h2d = (hq.numel() + hk.numel() + hv.numel()) * 2
+    h2d = sum(t.numel() * t.element_size() for t in pinned.values())
     d2h = hout.numel() * 4
     e2e_ms = []
     for i in range(args.warmup + args.steps):
         flush_l2()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        w["q"].copy_(hq, non_blocking=True)
-        w["new_k"].copy_(hk, non_blocking=True)
-        w["new_v"].copy_(hv, non_blocking=True)
+        for k, t in pinned.items():
+            w[k].copy_(t, non_blocking=True)
         tq.tq_quantize_set_rows(w["kctx"], w["new_k"], w["kc"], row_ids=w["slots"])
         tq.tq_quantize_set_rows(w["vctx"], w["new_v"], w["vc"], row_ids=w["slots"])
         tq.tq_decode_attention(w["kctx"], w["vctx"], w["q"], w["kc"], w["vc"], w["out"], w["ws"], B, Hq, Hkv, L)
@@ -368,40 +463,128 @@ def run_tq(args, rank, world, dist):
     if status:
         raise RuntimeError(f"device status {status} after the benchmark")
 
-    kv_bytes, alg_bytes = algorithmic_bytes(cfg)
+    kv_bytes = B * Hkv * L * decode_unit_bytes(spec)
+    alg_bytes = kv_bytes + w["q"].numel() * w["q"].element_size() + B * Hq * 128 * 4
     ms_per_step = total_ms / args.steps
     value = job_rate(alg_bytes, world, ms_per_step) / 1e9
-    keys = B * Hkv * L
-    part_avg = max_over_ranks(statistics.mean(part_ms), dist, device)
     peak, peak_kind = measured_peak()
     achieved = kv_bytes / (part_avg * 1e-3) / 1e9
     e2e_step_ms = max_over_ranks(statistics.mean(e2e_ms), dist, device)
-    e2e_gbs = job_rate(alg_bytes, world, e2e_step_ms) / 1e9
     if rank != 0:
         return
-    cpu = cpu_oracle_sample(cfg) if world == 1 else None  # host-core baseline: N=1 only
-    line = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": config_dict(cfg),
-        "keys_per_s": job_rate(keys, world, ms_per_step),
+    cpu = None
+    if world == 1:  # the host-core baseline: N=1 only
+        leg = OracleDecode(name)
+        cpu = cpu_sample(leg, decode_unit_bytes(spec),
+                         f"whole (batch, KV head) units of {L} keys x {Hq // Hkv} q-heads, "
+                         "fp64 dequantize-then-softmax")
+    line = common_line(DECODE_METRIC, args, world, ms_per_step, value, decode_config(name), "f32")
+    line.update({
+        "keys_per_s": job_rate(B * Hkv * L, world, ms_per_step),
         "q_head_scores_per_s": job_rate(B * Hq * L, world, ms_per_step),
         "hbm_frac_of_measured_step": value / peak,
-        "operands": "4-bit packed K/V decoded in registers to fp16 centroids; fp16 hi+lo q and p; fp32 accumulate",
-        "roofline": {"bound": "hbm", "kernel": "k_partial_t4 (split-K decode)", "achieved": achieved,
+        "algorithmic_bytes_per_step": alg_bytes,
+        "operands": "packed K/V decoded in registers to fp16 operands; fp16 hi+lo q and p; fp32 accumulate",
+        "roofline": {"bound": "hbm", "kernel": spec["kernel"] + " (split-K decode)", "achieved": achieved,
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": profiled_traffic(), "algorithmic_bytes_per_launch": kv_bytes,
-                     "avg_launch_ms": part_avg},
-        "cpu_baseline": None if cpu is None else {
-            "value": cpu["gbs"], "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
-            "keys_per_s": cpu["keys_per_s"],
-            "sample": f"{cpu['units']} whole (batch, KV head) units of {cfg['L']} keys x "
-                      f"{Hq // Hkv} q-heads, fp64 dequantize-then-softmax, {cpu['seconds']:.1f} s"},
-        "e2e": {"value": e2e_gbs, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_step_ms},
+                     "traffic": profiled_traffic("decode_partial_" + name, spec["source"]),
+                     "algorithmic_bytes_per_launch": kv_bytes, "avg_launch_ms": part_avg},
+        "cpu_baseline": cpu,
+        "e2e": {"value": job_rate(alg_bytes, world, e2e_step_ms) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step_ms},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
-    }
+    })
+    print(json.dumps(line), flush=True)
+
+
+def run_write(args, rank, world, dist):
+    import torch
+
+    import compressed_attention_gb300 as tq
+
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    cfg = synth.WORKLOADS["write_chunk"]
+    fmt, rot = args.write_format, args.write_rotation
+    kctx, vctx = tq.Ctx(fmt, rot, cfg["seed"]), tq.Ctx(fmt, rot, cfg["seed"] + 100)
+    x = {}
+    for tensor in ("K", "V"):
+        x32, bits = synth.write_rows(cfg, tensor)
+        x[tensor] = to_device_rows(torch, x32, bits, device)
+    n = x["K"].shape[0]
+    caches = {"K": tq.alloc_cache(fmt, n, device), "V": tq.alloc_cache(fmt, n, device)}
+    stream = torch.cuda.current_stream()
+    flush_l2 = flusher(torch, device)
+    fns = (lambda: tq.tq_quantize_set_rows(kctx, x["K"], caches["K"]),
+           lambda: tq.tq_quantize_set_rows(vctx, x["V"], caches["V"]))
+    graphs = graphs_of(torch, fns, args.warmup, flush_l2)
+    if dist:
+        dist.barrier()
+    with ClockSampler(local) as clocks:
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        times = timed_graph_steps(torch, stream, graphs, args.steps, flush_l2)
+        if dist:
+            dist.barrier()
+    clk = clocks.summary()
+    total_ms = max_over_ranks(sum(sum(t) for t in times), dist, device)
+    launch_avg = max_over_ranks(statistics.mean(v for t in times for v in t), dist, device)
+
+    # end to end through the public API: the bf16 rows copied in from pinned host memory,
+    # quantized, and the packed caches read back, every step.
+    hx = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True).copy_(v.cpu()) for k, v in x.items()}
+    hc = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in caches.items()}
+    h2d = sum(t.numel() * t.element_size() for t in hx.values())
+    d2h = sum(t.numel() * t.element_size() for t in hc.values())
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush_l2()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for k in ("K", "V"):
+            x[k].copy_(hx[k], non_blocking=True)
+        tq.tq_quantize_set_rows(kctx, x["K"], caches["K"])
+        tq.tq_quantize_set_rows(vctx, x["V"], caches["V"])
+        for k in ("K", "V"):
+            hc[k].copy_(caches[k], non_blocking=True)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append((time.perf_counter() - t0) * 1e3)
+    if tq.tq_ctx_device_status(kctx) or tq.tq_ctx_device_status(vctx):
+        raise RuntimeError("device status set after the benchmark")
+
+    row_bytes = ROW_BYTES[fmt]
+    launch_bytes = n * (256 + row_bytes)
+    alg_bytes = 2 * launch_bytes
+    ms_per_step = total_ms / args.steps
+    value = job_rate(alg_bytes, world, ms_per_step) / 1e9
+    peak, peak_kind = measured_peak()
+    e2e_step_ms = max_over_ranks(statistics.mean(e2e_ms), dist, device)
+    if rank != 0:
+        return
+    cpu = None
+    if world == 1:
+        leg = OracleWrite(fmt, rot)
+        cpu = cpu_sample(leg, 256 + row_bytes, f"blocks of {len(leg.x32)} bf16 rows encoded by the oracle")
+    kernel, source = WRITE_KERNEL[rot]
+    line = common_line(WRITE_METRIC, args, world, ms_per_step, value, write_config(args), "f32")
+    line.update({
+        "rows_per_s": job_rate(2 * n, world, ms_per_step),
+        "algorithmic_bytes_per_step": alg_bytes,
+        "roofline": {"bound": "hbm", "kernel": kernel, "achieved": launch_bytes / (launch_avg * 1e-3) / 1e9,
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": launch_bytes / (launch_avg * 1e-3) / 1e9 / peak,
+                     "traffic": profiled_traffic(f"write_{fmt}_{rot}_write_chunk", source),
+                     "algorithmic_bytes_per_launch": launch_bytes, "avg_launch_ms": launch_avg},
+        "cpu_baseline": cpu,
+        "e2e": {"value": job_rate(alg_bytes, world, e2e_step_ms) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step_ms},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+    })
     print(json.dumps(line), flush=True)
 
 
@@ -411,22 +594,28 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["tq", "reference"], default="tq")
+    ap.add_argument("--workload", choices=sorted(DECODE) + ["write_chunk"], default="gqa_lognormal")
+    ap.add_argument("--write-format", choices=["turbo4", "turbo3"], default="turbo4")
+    ap.add_argument("--write-rotation", choices=["dense", "wht"], default="dense")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
-    dist = None
     if args.impl == "reference":
         run_reference(args, rank, world)
         return
+    dist = None
     if world > 1:
         import torch
         import torch.distributed as dist
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         dist.init_process_group("nccl")
     try:
-        run_tq(args, rank, world, dist)
+        if args.workload == "write_chunk":
+            run_write(args, rank, world, dist)
+        else:
+            run_decode(args, rank, world, dist)
     finally:
         if dist is not None:
             dist.destroy_process_group()
