@@ -98,12 +98,6 @@ __device__ __forceinline__ void lut2(uint32_t base, uint32_t off, uint32_t &w0, 
     asm("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(w0), "=r"(w1) : "r"(off + base));
 }
 
-// Offset (byte I of w) * 256 + lane * 8 as one byte permute of the lane word lane * 8.
-template <int I>
-__device__ __forceinline__ uint32_t lut_off(uint32_t laneword, uint32_t w) {
-  return prmt(laneword, w, 0x1100u | ((4u + I) << 4));
-}
-
 template <bool SCORES, bool FIXED>
 __global__ void __maxnreg__(168) k_partial_pv(const PvParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -131,14 +125,15 @@ __global__ void __maxnreg__(168) k_partial_pv(const PvParams p) {
   // one 8-byte slot per lane.  Sign table: nibble of four QJL bits -> four fp16 +-1.
   for (int piece = threadIdx.x; piece < 256 * 16; piece += NTH) {
     const int byte = piece >> 4, chunk = piece & 15;
-    auto c = [&](int i) { return (p.kc16[i >> 1] >> (16 * (i & 1))) & 0xFFFFu; };
+    const uint32_t k0 = p.kc16[0], k1 = p.kc16[1];  // (no reference capture: keeps p out of local memory)
+    auto c = [k0, k1](int i) { return ((i >> 1 ? k1 : k0) >> (16 * (i & 1))) & 0xFFFFu; };
     const uint32_t w0 = c(byte & 3) | (c((byte >> 2) & 3) << 16);
     const uint32_t w1 = c((byte >> 4) & 3) | (c(byte >> 6) << 16);
     reinterpret_cast<uint4 *>(mse_lut + byte * 64)[chunk] = make_uint4(w0, w1, w0, w1);
   }
   for (int piece = threadIdx.x; piece < 16 * 16; piece += NTH) {
     const int nib = piece >> 4, chunk = piece & 15;
-    auto sg = [&](int i) { return ((nib >> i) & 1) ? 0x3C00u : 0xBC00u; };
+    auto sg = [nib](int i) { return ((nib >> i) & 1) ? 0x3C00u : 0xBC00u; };
     const uint32_t w0 = sg(0) | (sg(1) << 16), w1 = sg(2) | (sg(3) << 16);
     reinterpret_cast<uint4 *>(sign_lut + nib * 64)[chunk] = make_uint4(w0, w1, w0, w1);
   }
@@ -276,19 +271,10 @@ __global__ void __maxnreg__(168) k_partial_pv(const PvParams p) {
           const uint32_t mw0 = st < 4 ? m0.x : m0.y, mw1 = st < 4 ? m1.x : m1.y;
           const uint32_t nw0 = (st & 1) ? od0 : ev0, nw1 = (st & 1) ? od1 : ev1;
           uint32_t b00, b01, b10, b11, s00, s01, s10, s11;
-          uint32_t om0, om1, on0, on1;
-          switch (st & 3) {
-            case 0: om0 = lut_off<0>(laneword, mw0), om1 = lut_off<0>(laneword, mw1); break;
-            case 1: om0 = lut_off<1>(laneword, mw0), om1 = lut_off<1>(laneword, mw1); break;
-            case 2: om0 = lut_off<2>(laneword, mw0), om1 = lut_off<2>(laneword, mw1); break;
-            default: om0 = lut_off<3>(laneword, mw0), om1 = lut_off<3>(laneword, mw1); break;
-          }
-          switch (st >> 1) {
-            case 0: on0 = lut_off<0>(laneword, nw0), on1 = lut_off<0>(laneword, nw1); break;
-            case 1: on0 = lut_off<1>(laneword, nw0), on1 = lut_off<1>(laneword, nw1); break;
-            case 2: on0 = lut_off<2>(laneword, nw0), on1 = lut_off<2>(laneword, nw1); break;
-            default: on0 = lut_off<3>(laneword, nw0), on1 = lut_off<3>(laneword, nw1); break;
-          }
+          // table offsets: byte st & 3 of the MSE word, nibble-byte st >> 1 of the sign word
+          const uint32_t selm = 0x1100u | ((4u + (st & 3)) << 4), seln = 0x1100u | ((4u + (st >> 1)) << 4);
+          const uint32_t om0 = prmt(laneword, mw0, selm), om1 = prmt(laneword, mw1, selm);
+          const uint32_t on0 = prmt(laneword, nw0, seln), on1 = prmt(laneword, nw1, seln);
           lut2<FIXED, LUT_WINDOW>(mse_base, om0, b00, b01);
           lut2<FIXED, LUT_WINDOW>(mse_base, om1, b10, b11);
           lut2<FIXED, SIGN_WINDOW>(sign_base, on0, s00, s01);
@@ -309,13 +295,10 @@ __global__ void __maxnreg__(168) k_partial_pv(const PvParams p) {
           const float2 ng = *reinterpret_cast<const float2 *>(Ks + kr * K_ROW);
           hv[i] = *reinterpret_cast<const uint4 *>(Vs + kr * V_ROW + 32);
           if (!ok[i]) hv[i] = make_uint4(0u, 0u, 0u, 0u);
-          const float smax = fmaxf(fmaxf(__half2float(__ushort_as_half((unsigned short)(hv[i].x & 0xFFFFu))),
-                                         __half2float(__ushort_as_half((unsigned short)(hv[i].y & 0xFFFFu)))),
-                                   fmaxf(__half2float(__ushort_as_half((unsigned short)(hv[i].z & 0xFFFFu))),
-                                         __half2float(__ushort_as_half((unsigned short)(hv[i].w & 0xFFFFu)))));
-          // nu = exponent with smax * 2^-nu in [1/2, 1) (scales are >= 0); 2^-nu exact
-          int nu = (int)((__float_as_uint(smax) >> 23) & 0xFF) - 126;
-          nu = max(nu, -64);
+          // nu = fp16 exponent of the largest scale minus 14, so scale * 2^-nu < 1 for every
+          // group (scales are >= 0, so their fp16 bit patterns order like their values)
+          const uint32_t mb = __vmaxu2(__vmaxu2(hv[i].x, hv[i].y), __vmaxu2(hv[i].z, hv[i].w));
+          const int nu = (int)((mb >> 10) & 0x1Fu) - 14;
           tn[i] = __uint_as_float((uint32_t)(127 - nu) << 23);
           const int nb = i >> 1, e = i & 1;
           const float mse = cm[nb][e] + cm[nb][2 + e];
@@ -356,12 +339,12 @@ __global__ void __maxnreg__(168) k_partial_pv(const PvParams p) {
           for (int i = 0; i < 4; ++i) {
             const uint32_t w = G4 == 0 ? hv[i].x : G4 == 1 ? hv[i].y : G4 == 2 ? hv[i].z : hv[i].w;
             const float2 sz = __half22float2(*reinterpret_cast<const __half2 *>(&w));
-            sg[i] = sz.x;
+              sg[i] = pw[i] * sz.x;  // 2^(s - M + P) * scale_G <= p' (scale * 2^-nu < 1)
             zt[G4] = fmaf(pw[i], sz.y, zt[G4]);
           }
           uint32_t b0h, b0l, b1h, b1l;
-          split_half2(pp[0] * (sg[0] * tn[0]), pp[1] * (sg[1] * tn[1]), b0h, b0l);
-          split_half2(pp[2] * (sg[2] * tn[2]), pp[3] * (sg[3] * tn[3]), b1h, b1l);
+          split_half2(sg[0], sg[1], b0h, b0l);
+          split_half2(sg[2], sg[3], b1h, b1l);
           const int wo = 8 * G4 + code_word;
           const uint32_t wa = lds32(Vs + ks[0] * V_ROW + wo), wb = lds32(Vs + ks[1] * V_ROW + wo);
           const uint32_t wc = lds32(Vs + ks[2] * V_ROW + wo), wd = lds32(Vs + ks[3] * V_ROW + wo);
