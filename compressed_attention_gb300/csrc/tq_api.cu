@@ -1,5 +1,6 @@
 // The extern "C" entry points of tq.h: argument validation on the host, context
 // construction, and dispatch to the kernel launchers.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -215,6 +216,17 @@ tq_status tq_ctx_create(const tq_params *params, tq_ctx **out) {
         for (int j = 0; j < D; ++j) rt[(size_t)j * D + i] = r[(size_t)i * D + j];
       s = to_device(&c->d_pit, rt.data(), rt.size());
     }
+    if (s == TQ_OK && p.rotation == TQ_ROT_DENSE) {
+      // bf16 hi + lo parts of R for the tensor-core write: hi = RN(r), lo = RN(r - hi)
+      std::vector<uint16_t> rb(2 * (size_t)D * D);
+      for (size_t i = 0; i < (size_t)D * D; ++i) {
+        const __nv_bfloat16 hi = __float2bfloat16_rn(r[i]);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(r[i] - __bfloat162float(hi));
+        rb[i] = __bfloat16_as_ushort(hi);
+        rb[(size_t)D * D + i] = __bfloat16_as_ushort(lo);
+      }
+      s = to_device(&c->d_pib, rb.data(), rb.size());
+    }
     if (s == TQ_OK && p.format == TQ_FMT_PROD3) {
       std::vector<float> S((size_t)D * D), St((size_t)D * D);
       tq_make_qjl_matrix(D, p.qjl_seed, S.data());
@@ -243,6 +255,7 @@ tq_status tq_ctx_destroy(tq_ctx *ctx) {
   cudaFree(ctx->d_pit);
   cudaFree(ctx->d_S);
   cudaFree(ctx->d_St);
+  cudaFree(ctx->d_pib);
   cudaFree(ctx->d_status);
   delete ctx;
   return TQ_OK;

@@ -49,6 +49,7 @@ struct tq_ctx {
   float *d_pit = nullptr;               // R^T, fp32 row-major
   float *d_S = nullptr;                 // QJL matrix S, fp32 [128][128] row-major
   float *d_St = nullptr;                // S^T, fp32 row-major
+  uint16_t *d_pib = nullptr;            // dense R as bf16 hi then lo, [2][128][128] (tensor-core write)
   int32_t *d_status = nullptr;          // device status word
 };
 
@@ -74,6 +75,8 @@ struct WriteLaunch {
   int64_t dst_rows;
 };
 cudaError_t launch_write(const tq_ctx *ctx, const WriteLaunch &w, cudaStream_t st);
+bool write_tc_eligible(const tq_ctx *ctx, const WriteLaunch &w);
+cudaError_t launch_write_tc(const tq_ctx *ctx, const WriteLaunch &w, cudaStream_t st);
 
 cudaError_t launch_dequantize(const tq_ctx *ctx, const uint8_t *cache, int64_t n_rows,
                               int unrotate, float *dst, cudaStream_t st);

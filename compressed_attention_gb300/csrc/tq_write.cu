@@ -381,8 +381,10 @@ cudaError_t launch_write(const tq_ctx *ctx, const WriteLaunch &w, cudaStream_t s
     return bf16 ? launch_rows(k_write_wht<TQ_FMT_TURBO3, TQ_DTYPE_BF16>, p, w.n_rows, sms, 0, 8, st)
                 : launch_rows(k_write_wht<TQ_FMT_TURBO3, TQ_DTYPE_F32>, p, w.n_rows, sms, 0, 8, st);
   }
-  // Dense rotation (prod3 always takes this path; its WHT variant multiplies by the
-  // materialised WHT matrix, which the context stores as well).
+  // Dense rotation on the tensor cores for 16-byte aligned bf16 rows (turbo4 / turbo3).
+  if (write_tc_eligible(ctx, w)) return launch_write_tc(ctx, w, st);
+  // Dense rotation on the CUDA cores (prod3 always takes this path; its WHT variant
+  // multiplies by the materialised WHT matrix, which the context stores as well).
   const size_t mats = (fmt == TQ_FMT_PROD3 ? 3 : 1) * (size_t)D * D * sizeof(float);
   const size_t smem = mats + WARPS * 3 * D * sizeof(float) + WARPS * D + WARPS * ROWBUF +
                       16 * sizeof(float);

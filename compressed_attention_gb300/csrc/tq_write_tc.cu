@@ -1,0 +1,348 @@
+// Write path under the dense rotation on the 5th-generation tensor cores: the batched
+// rotation Y = X Pi^T ([rows, 128] x [128, 128], "turboquant_plus: how the turbo4 KV
+// format came back", section 1 encode chain; "TurboQuant fused Triton kernels deep
+// dive", trick 1 for the dense orthogonal Pi) runs as tcgen05 MMAs with the
+// accumulator in tensor memory, and one thread per row finishes the chain: the
+// canonical fp32 norm, y = acc / n, nearest centroid, packing, scatter.
+//
+// Per 128-row tile: a TMA load brings the bf16 rows into shared memory in the 128-byte
+// swizzled K-major layout (two 64-column halves); the MMA multiplies them by Pi split
+// into bf16 hi + lo parts (two accumulating products, K = 128 each), so the rotated
+// coordinates carry about 16 significant bits of Pi against the exact bf16 inputs --
+// enough to keep index decisions identical to the fp64 oracle except within 1e-5 of a
+// decision boundary.  Two CTAs share an SM; each holds Pi (64 KB), one row tile
+// (32 KB) and a 128-column fp32 accumulator in tensor memory.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "tq_device.cuh"
+#include "tq_internal.h"
+
+namespace tq {
+
+namespace {
+
+constexpr int TC_THREADS = 128;        // four warps: thread r owns row r of the tile
+constexpr int TC_ROWS = 128;           // rows per tile (the MMA's M)
+constexpr uint32_t HALF_BYTES = TC_ROWS * 128;  // one 64-column half of a bf16 tile
+constexpr uint32_t TILE_BYTES = 2 * HALF_BYTES; // 32 KB
+constexpr uint32_t TMEM_COLS = 128;
+constexpr uint64_t TC_WAIT_NS = 2000000000ull;
+
+// Shared memory: Pi hi (32 KB), Pi lo (32 KB), the row tile (32 KB), all 1024-byte
+// aligned for the 128-byte swizzle; then barriers, boundaries and the TMEM address.
+constexpr uint32_t OFF_PIH = 0;
+constexpr uint32_t OFF_PIL = TILE_BYTES;
+constexpr uint32_t OFF_X = 2 * TILE_BYTES;
+constexpr uint32_t OFF_MISC = 3 * TILE_BYTES;
+constexpr uint32_t SMEM_TC = OFF_MISC + 256 + 1024;  // + slack to align the base to 1024
+
+struct TcMisc {
+  uint64_t x_full;
+  uint64_t mma_done;
+  uint32_t tmem_addr;
+  int abort_flag;
+  float b[16];
+};
+
+struct TcParams {
+  const uint16_t *pib;       // Pi hi then lo, bf16 bits [2][128][128] row-major (row j = output j)
+  const int64_t *row_ids;
+  uint8_t *dst;
+  int64_t n_rows;
+  int64_t dst_rows;
+  int32_t *status;
+  float b[15];
+};
+
+// Offset of element (row, k) of a 128 x 128 bf16 tile in the 128-byte swizzled K-major
+// layout: two halves of 64 columns, rows of 128 bytes, 16-byte chunk c of row r stored
+// at chunk position c ^ (r % 8).
+__host__ __device__ constexpr uint32_t sw128_offset(uint32_t row, uint32_t k) {
+  return (k >> 6) * HALF_BYTES + row * 128 + ((((k & 63) >> 3) ^ (row & 7)) << 4) + (k & 7) * 2;
+}
+
+// tcgen05 shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (the leading offset is unused for this layout).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)1 << 16;                    // leading byte offset (unused), 16 B
+  d |= (uint64_t)((1024u >> 4) & 0x3FFFu) << 32;  // stride byte offset: 1024 B
+  d |= (uint64_t)1 << 46;                    // descriptor version
+  d |= (uint64_t)2 << 61;                    // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor: kind::f16 with bf16 A and B, fp32 D, both K-major, M = 128,
+// N = 128.
+constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols));
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols));
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(IDESC), "r"(accumulate));
+}
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint64_t *bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+template <int NB>
+__device__ __forceinline__ uint32_t bucket_s(float y, const float *sb) {
+  uint32_t pos = 0;
+#pragma unroll
+  for (int step = (NB + 1) / 2; step >= 1; step >>= 1)
+    if (y > sb[pos + step - 1]) pos += step;
+  return pos;
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(TC_THREADS, 2) k_write_dense_tc(const __grid_constant__ CUtensorMap xmap,
+                                                                     const TcParams p) {
+  constexpr int NB = (FMT == TQ_FMT_TURBO4) ? 15 : 7;
+  extern __shared__ uint8_t smem_dyn[];
+  // 1024-byte aligned base for the swizzled tiles
+  uint8_t *smem = smem_dyn + ((1024u - (smem_addr(smem_dyn) & 1023u)) & 1023u);
+  TcMisc &ms = *reinterpret_cast<TcMisc *>(smem + OFF_MISC);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int64_t n_tiles = (p.n_rows + TC_ROWS - 1) / TC_ROWS;
+
+  if (warp == 0) tmem_alloc(smem_addr(&ms.tmem_addr), TMEM_COLS);
+  if (tid == 0) {
+    mbar_init(&ms.x_full, 1);
+    mbar_init(&ms.mma_done, 1);
+    ms.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (tid == 0) {  // constant indices: a runtime index into the parameters would copy them to local memory
+#pragma unroll
+    for (int k = 0; k < NB; ++k) ms.b[k] = p.b[k];
+  }
+  // Pi hi / lo into the swizzled layout, 16-byte chunks
+  for (int i = tid; i < 2 * TC_ROWS * 16; i += TC_THREADS) {
+    const int m = i / (TC_ROWS * 16), rem = i % (TC_ROWS * 16);
+    const int row = rem >> 4, chunk = rem & 15;
+    const uint4 v = reinterpret_cast<const uint4 *>(p.pib + (size_t)m * TC_ROWS * 128 + (size_t)row * 128)[chunk];
+    *reinterpret_cast<uint4 *>(smem + (m ? OFF_PIL : OFF_PIH) + sw128_offset(row, chunk * 8)) = v;
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> tensor-core reads
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ms.tmem_addr;
+  const uint32_t sx = smem_addr(smem + OFF_X);
+  const uint32_t spih = smem_addr(smem + OFF_PIH), spil = smem_addr(smem + OFF_PIL);
+
+  if (tid == 0 && blockIdx.x < n_tiles) {
+    mbar_arrive_expect_tx(&ms.x_full, TILE_BYTES);
+    tma_load_2d(sx, &xmap, &ms.x_full, 0, (int)(blockIdx.x * TC_ROWS));
+    tma_load_2d(sx + HALF_BYTES, &xmap, &ms.x_full, 64, (int)(blockIdx.x * TC_ROWS));
+  }
+  uint32_t phase = 0;
+  for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, phase ^= 1u) {
+    // ---- wait for the rows, then one thread issues the 16 MMAs
+    if (!mbar_wait_bounded(&ms.x_full, phase, TC_WAIT_NS)) ms.abort_flag = 1;
+    if (tid == 0 && !ms.abort_flag) {
+      tc_fence_after();
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        const uint32_t sb = part ? spil : spih;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t koff = (ks >> 2) * HALF_BYTES + (ks & 3) * 32;
+          umma_bf16(tmem, sw128_desc(sx + koff), sw128_desc(sb + koff), (part | ks) ? 1u : 0u);
+        }
+      }
+      umma_commit(&ms.mma_done);
+    }
+    // ---- canonical fp32 norm of this thread's row, from the staged bf16 tile
+    const int64_t row = tile * TC_ROWS + tid;
+    float pl[32];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const uint4 v = *reinterpret_cast<const uint4 *>(smem + OFF_X + sw128_offset(tid, c * 8));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {  // elements 8c + 4h .. 8c + 4h + 3 -> group l = 2c + h
+        const float x0 = __uint_as_float(w[2 * h] << 16), x1 = __uint_as_float(w[2 * h] & 0xFFFF0000u);
+        const float x2 = __uint_as_float(w[2 * h + 1] << 16), x3 = __uint_as_float(w[2 * h + 1] & 0xFFFF0000u);
+        pl[2 * c + h] = __fadd_rn(__fadd_rn(__fmul_rn(x0, x0), __fmul_rn(x1, x1)),
+                                  __fadd_rn(__fmul_rn(x2, x2), __fmul_rn(x3, x3)));
+      }
+    }
+#pragma unroll
+    for (int h = 16; h >= 1; h >>= 1)
+#pragma unroll
+      for (int l = 0; l < h; ++l) pl[l] = __fadd_rn(pl[l], pl[l + h]);
+    const float n = __fsqrt_rn(pl[0]);
+    const float inv = 1.0f / n;
+    // ---- accumulator ready; the row tile is no longer needed: prefetch the next one
+    if (!mbar_wait_bounded(&ms.mma_done, phase, TC_WAIT_NS)) ms.abort_flag = 1;
+    tc_fence_after();
+    __syncthreads();
+    if (ms.abort_flag) {
+      if (tid == 0) {
+        atomicExch(p.status, (int32_t)DEVERR_TIMEOUT);
+        (void)mbar_wait_bounded(&ms.x_full, phase, TC_WAIT_NS);  // let a late copy land
+      }
+      break;
+    }
+    const int64_t next = tile + gridDim.x;
+    if (tid == 0 && next < n_tiles) {
+      mbar_arrive_expect_tx(&ms.x_full, TILE_BYTES);
+      tma_load_2d(sx, &xmap, &ms.x_full, 0, (int)(next * TC_ROWS));
+      tma_load_2d(sx + HALF_BYTES, &xmap, &ms.x_full, 64, (int)(next * TC_ROWS));
+    }
+    // ---- y = acc / n, nearest centroid, pack (whole row in this thread), store
+    const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+    const bool live = row < p.n_rows;
+    int64_t slot = row;
+    if (live && p.row_ids) slot = p.row_ids[row];
+    const bool ok = live && slot >= 0 && slot < p.dst_rows;
+    if (live && !ok) atomicExch(p.status, (int32_t)DEVERR_ROW_OOB);
+    uint32_t q[16];  // turbo4: 128 nibbles; turbo3: 2-bit low parts [0..7], high bits [8..11]
+#pragma unroll
+    for (int i = 0; i < 16; ++i) q[i] = 0u;
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch) {
+      float acc[32];
+      tmem_ld32(lane_addr + ch * 32, acc);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float y = (n == 0.0f) ? 0.0f : acc[i] * inv;
+        const uint32_t idx = bucket_s<NB>(y, ms.b);
+        const int j = ch * 32 + i;
+        if (FMT == TQ_FMT_TURBO4) {
+          q[j >> 3] |= idx << (4 * (j & 7));
+        } else {
+          q[j >> 4] |= (idx & 3u) << (2 * (j & 15));
+          q[8 + (j >> 5)] |= (idx >> 2) << (j & 31);
+        }
+      }
+    }
+    if (ok) {
+      if (FMT == TQ_FMT_TURBO4) {
+        uint32_t *d = reinterpret_cast<uint32_t *>(p.dst + slot * 68);
+        d[0] = __float_as_uint(n);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) d[1 + i] = q[i];
+      } else {
+        // four 14-byte blocks {fp16 norm, qs[8], signs[4]}, stored as 16-bit halves
+        uint16_t *d = reinterpret_cast<uint16_t *>(p.dst + slot * 56);
+        const uint16_t hn = __half_as_ushort(__float2half_rn(n));
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          d[7 * c] = hn;
+          d[7 * c + 1] = (uint16_t)(q[2 * c] & 0xFFFFu);
+          d[7 * c + 2] = (uint16_t)(q[2 * c] >> 16);
+          d[7 * c + 3] = (uint16_t)(q[2 * c + 1] & 0xFFFFu);
+          d[7 * c + 4] = (uint16_t)(q[2 * c + 1] >> 16);
+          d[7 * c + 5] = (uint16_t)(q[8 + c] & 0xFFFFu);
+          d[7 * c + 6] = (uint16_t)(q[8 + c] >> 16);
+        }
+      }
+    }
+    tc_fence_before();
+    __syncthreads();  // accumulator free for the next tile's MMAs
+  }
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link to libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+}  // namespace
+
+bool write_tc_eligible(const tq_ctx *ctx, const WriteLaunch &w) {
+  if (ctx->p.rotation != TQ_ROT_DENSE || !ctx->d_pib) return false;
+  if (ctx->fmt != TQ_FMT_TURBO4 && ctx->fmt != TQ_FMT_TURBO3) return false;
+  if (w.src_dtype != TQ_DTYPE_BF16) return false;
+  if ((uintptr_t)w.src % 16 != 0 || (w.stride * 2) % 16 != 0) return false;
+  // Small batches (a decode step's few new rows) stay on the CUDA-core kernel, which
+  // spreads them over many CTAs; the tensor-core kernel takes whole 128-row tiles.
+  if (w.n_rows < 16 * TC_ROWS || w.n_rows > ((int64_t)1 << 31) - TC_ROWS) return false;
+  return encode_fn() != nullptr;
+}
+
+cudaError_t launch_write_tc(const tq_ctx *ctx, const WriteLaunch &w, cudaStream_t st) {
+  CUtensorMap map;
+  const cuuint64_t dims[2] = {128, (cuuint64_t)w.n_rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)w.stride * 2};
+  const cuuint32_t box[2] = {64, TC_ROWS};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode_fn()(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(w.src), dims, strides,
+                                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  TcParams p{};
+  p.pib = ctx->d_pib;
+  p.row_ids = w.row_ids;
+  p.dst = w.dst;
+  p.n_rows = w.n_rows;
+  p.dst_rows = w.dst_rows;
+  p.status = ctx->d_status;
+  for (int k = 0; k + 1 < ctx->cb.K; ++k) p.b[k] = ctx->cb.b[k];
+  const int64_t n_tiles = (w.n_rows + TC_ROWS - 1) / TC_ROWS;
+  const int grid = (int)(n_tiles < 2 * ctx->num_sms ? n_tiles : 2 * ctx->num_sms);
+  auto kern = ctx->fmt == TQ_FMT_TURBO4 ? k_write_dense_tc<TQ_FMT_TURBO4> : k_write_dense_tc<TQ_FMT_TURBO3>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_TC);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, TC_THREADS, SMEM_TC, st>>>(map, p);
+  return cudaGetLastError();
+}
+
+}  // namespace tq

@@ -181,3 +181,41 @@ def test_write_chunk_full_size(fmt, rot):
             ok, ndiff = band_ok(idx, aux["idx"], aux["y"], codec.b32)
             assert ok, f"{ndiff} indices outside the band"
     assert tq.tq_ctx_device_status(ctx) == 0
+
+
+@pytest.mark.parametrize("fmt", ["turbo4", "turbo3"])
+def test_write_dense_tensor_core_scatter_and_stride(fmt):
+    """Batches of 2048+ bf16 rows take the tensor-core write: rows read through a tensor
+    map from a wider tensor (stride 192 elements), scattered to permuted slots; an
+    out-of-range slot is skipped and flagged."""
+    import torch
+    tq = lib()
+    n, cap = 2300, 2600
+    x = make_rows(n, 23, scale=2.0)[8:]
+    wide = np.zeros((len(x), 192), np.float32)
+    wide[:, 32:160] = x
+    bits = synth.bf16_bits(wide)
+    t = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()[:, 32:160]
+    x32 = synth.bf16_to_f32(bits)[:, 32:160]
+    slots = synth.row_permutation(cap, 5)[:len(x)].copy()
+    slots[17] = cap + 3
+    ctx = tq.Ctx(fmt, "dense", 6)
+    cache = write_gpu(tq, ctx, t, len(x), row_ids=slots, capacity=cap)
+    assert tq.tq_ctx_device_status(ctx) == 1
+    codec = Codec(fmt, rotation="dense", rot_seed=6)
+    ref, aux = codec.encode(x32)
+    rb = ctx.row_bytes
+    host = cache.cpu().numpy()
+    rows = host[: cap * rb].reshape(cap, rb)
+    live = np.array([i for i in range(len(x)) if i != 17])
+    got = rows[slots[live]]
+    if fmt == "turbo4":
+        assert np.array_equal(got[:, :4], ref[live, :4])
+        idx = unpack_turbo4(got)[1]
+    else:
+        assert np.array_equal(unpack_turbo3(got)[0], unpack_turbo3(ref[live])[0])
+        idx = unpack_turbo3(got)[1]
+    ok, ndiff = band_ok(idx, aux["idx"][live], aux["y"][live], codec.b32)
+    assert ok, f"{ndiff} indices differ outside the boundary band"
+    untouched = sorted(set(range(cap)) - set(int(s) for s in slots if s < cap))
+    assert np.all(rows[untouched] == 0xA5)
