@@ -284,7 +284,7 @@ def decode_config(name):
             "k_format": spec["k_fmt"], "v_format": spec["v_fmt"], "rotation": spec["rotation"],
             "q_dtype": cfg["q_dtype"],
             "l2": "flushed before every step: 256 MB write then a read of it (no dirty lines left)",
-            "launch": "each step replayed from CUDA graphs, steps queued back to back"}
+            "launch": "CUDA graphs"}
 
 
 def write_config(args):
@@ -293,7 +293,7 @@ def write_config(args):
             "rows_per_tensor": cfg["N"] * cfg["Hkv"], "format": args.write_format,
             "rotation": args.write_rotation,
             "l2": "flushed before every step: 256 MB write then a read of it (no dirty lines left)",
-            "launch": "each step replayed from a CUDA graph, steps queued back to back"}
+            "launch": "CUDA graphs"}
 
 
 # ----------------------------------------------------------------------------- GPU side
@@ -352,41 +352,35 @@ def flusher(torch, device):
     return flush_l2
 
 
-def graphs_of(torch, fns, warmup, flush_l2):
-    """Warm the callables up eagerly, capture each in its own CUDA graph, warm the graphs."""
+def timed_graph_steps(torch, stream, fns, steps, warmup, flush_l2):
+    """Time `steps` steps, each one replay of a CUDA graph running the callables `fns` in
+    order, with the L2 flushed before every step; returns the per-step times (ms).
+
+    The whole step is one graph, so the kernels of the library keep their programmatic
+    launch overlap (each may start its prologue while the previous one finishes).  All
+    steps and flushes are queued without a host synchronisation, so the host runs ahead
+    of the device and no enqueue gap enters a timed region."""
     for _ in range(warmup):
         flush_l2()
         for fn in fns:
             fn()
     torch.cuda.synchronize()
-    graphs = []
-    for fn in fns:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for fn in fns:
             fn()
-        graphs.append(g)
     for _ in range(warmup):
         flush_l2()
-        for g in graphs:
-            g.replay()
+        g.replay()
     torch.cuda.synchronize()
-    return graphs
-
-
-def timed_graph_steps(torch, stream, graphs, steps, flush_l2):
-    """Replay the graphs once per step with events between them; steps and flushes are
-    queued without a host synchronisation, so the host runs ahead of the device and no
-    enqueue gap enters a timed region.  Returns per-step event times (ms) between
-    consecutive graphs: [steps][len(graphs)]."""
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(graphs) + 1)] for _ in range(steps)]
-    for e in ev:
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for e0, e1 in ev:
         flush_l2()
-        e[0].record(stream)
-        for i, g in enumerate(graphs):
-            g.replay()
-            e[i + 1].record(stream)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
     torch.cuda.synchronize()
-    return [[e[i].elapsed_time(e[i + 1]) for i in range(len(graphs))] for e in ev]
+    return [e0.elapsed_time(e1) for e0, e1 in ev]
 
 
 def common_line(metric, args, world, ms_per_step, value, config, dtype):
@@ -422,21 +416,21 @@ def run_decode(args, rank, world, dist):
         tq.tq_decode_combine(w["kctx"], w["vctx"], w["out"], w["ws"], B, Hq, Hkv, L)
 
     launches_per_step = 5
-    # The step is replayed from three CUDA graphs (write + q preparation, split-K decode,
-    # combine); the events between them time the decode kernel alone on its stream.
-    graphs = graphs_of(torch, (write_and_prepare, partial, combine), args.warmup, flush_l2)
     if dist:
         dist.barrier()
     with ClockSampler(local) as clocks:
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
-        times = timed_graph_steps(torch, stream, graphs, args.steps, flush_l2)
+        # the step, then the decode kernel alone (the roofline), same workload and flushes
+        step_ms = timed_graph_steps(torch, stream, (write_and_prepare, partial, combine), args.steps,
+                                    args.warmup, flush_l2)
+        part_ms = timed_graph_steps(torch, stream, (partial,), args.steps, args.warmup, flush_l2)
         if dist:
             dist.barrier()
     clk = clocks.summary()
-    total_ms = max_over_ranks(sum(sum(t) for t in times), dist, device)
-    part_avg = max_over_ranks(statistics.mean(t[1] for t in times), dist, device)
+    total_ms = max_over_ranks(sum(step_ms), dist, device)
+    part_avg = max_over_ranks(statistics.mean(part_ms), dist, device)
 
     # end to end through the public API with host buffers: q and the new K/V rows copied in,
     # the output read back, every step.
@@ -479,6 +473,8 @@ def run_decode(args, rank, world, dist):
                          f"whole (batch, KV head) units of {L} keys x {Hq // Hkv} q-heads, "
                          "fp64 dequantize-then-softmax")
     line = common_line(DECODE_METRIC, args, world, ms_per_step, value, decode_config(name), "f32")
+    line["config"]["launch"] = ("each step one CUDA graph, steps queued back to back; the dominant kernel "
+                                "timed alone the same way for the roofline")
     line.update({
         "keys_per_s": job_rate(B * Hkv * L, world, ms_per_step),
         "q_head_scores_per_s": job_rate(B * Hq * L, world, ms_per_step),
@@ -519,19 +515,19 @@ def run_write(args, rank, world, dist):
     flush_l2 = flusher(torch, device)
     fns = (lambda: tq.tq_quantize_set_rows(kctx, x["K"], caches["K"]),
            lambda: tq.tq_quantize_set_rows(vctx, x["V"], caches["V"]))
-    graphs = graphs_of(torch, fns, args.warmup, flush_l2)
     if dist:
         dist.barrier()
     with ClockSampler(local) as clocks:
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
-        times = timed_graph_steps(torch, stream, graphs, args.steps, flush_l2)
+        step_ms = timed_graph_steps(torch, stream, fns, args.steps, args.warmup, flush_l2)
+        launch_ms = timed_graph_steps(torch, stream, fns[:1], args.steps, args.warmup, flush_l2)
         if dist:
             dist.barrier()
     clk = clocks.summary()
-    total_ms = max_over_ranks(sum(sum(t) for t in times), dist, device)
-    launch_avg = max_over_ranks(statistics.mean(v for t in times for v in t), dist, device)
+    total_ms = max_over_ranks(sum(step_ms), dist, device)
+    launch_avg = max_over_ranks(statistics.mean(launch_ms), dist, device)
 
     # end to end through the public API: the bf16 rows copied in from pinned host memory,
     # quantized, and the packed caches read back, every step.
@@ -571,6 +567,8 @@ def run_write(args, rank, world, dist):
         cpu = cpu_sample(leg, 256 + row_bytes, f"blocks of {len(leg.x32)} bf16 rows encoded by the oracle")
     kernel, source = WRITE_KERNEL[rot]
     line = common_line(WRITE_METRIC, args, world, ms_per_step, value, write_config(args), "f32")
+    line["config"]["launch"] = ("each step one CUDA graph, steps queued back to back; the dominant kernel "
+                                "timed alone the same way for the roofline")
     line.update({
         "rows_per_s": job_rate(2 * n, world, ms_per_step),
         "algorithmic_bytes_per_step": alg_bytes,

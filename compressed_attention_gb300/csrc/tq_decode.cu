@@ -142,7 +142,9 @@ __global__ void __launch_bounds__(QWARPS * 32) k_prepare_q(const QprepParams p) 
   float *mt = qsm;                       // [128][128]
   float *qv = qsm + D * D;               // [QWARPS][128]
   __half *hs = reinterpret_cast<__half *>(qv + QWARPS * D);  // [QWARPS][2][128]
+  pdl_trigger();
   stage_matrix(mt, p.rt);
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qi = blockIdx.x * QWARPS + warp;
   const bool live = qi < p.n_q;
@@ -296,6 +298,7 @@ __global__ void __maxnreg__(128)
   SmemHead &sm = *reinterpret_cast<SmemHead *>(smem_raw);
   uint32_t *lut = reinterpret_cast<uint32_t *>(smem_raw + LUT_OFF);
   const int cta = blockIdx.x;
+  pdl_trigger();
   if (FIXED && smem_addr(smem_raw) != RESERVED_SMEM) {  // layout assumption broken: refuse
     if (threadIdx.x == 0) atomicExch(p.status, (int32_t)DEVERR_LAYOUT);
     return;
@@ -309,10 +312,6 @@ __global__ void __maxnreg__(128)
     sm.abort_flag = 0;
     fence_mbar_init();
   }
-  if (threadIdx.x == 0 && p.seq_lens) {
-    for (int b = 0; b < p.B; ++b)
-      if (p.seq_lens[b] < 1 || p.seq_lens[b] > p.L) atomicExch(p.status, (int32_t)DEVERR_SEQLEN);
-  }
   // Fill the table: each (byte, half) entry is computed once and stored to its 32
   // slots with 16-byte stores.
   for (int piece = threadIdx.x; piece < 256 * 8; piece += NTHREADS) {
@@ -324,6 +323,11 @@ __global__ void __maxnreg__(128)
     uint4 *dst = reinterpret_cast<uint4 *>(lut + byte * 64 + chunk * 8);
     dst[0] = make_uint4(e, e, e, e);
     dst[1] = make_uint4(e, e, e, e);
+  }
+  pdl_wait();  // the caches, q and the workspace may be written by the previous kernel
+  if (threadIdx.x == 0 && p.seq_lens) {
+    for (int b = 0; b < p.B; ++b)
+      if (p.seq_lens[b] < 1 || p.seq_lens[b] > p.L) atomicExch(p.status, (int32_t)DEVERR_SEQLEN);
   }
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -626,7 +630,9 @@ __global__ void __launch_bounds__(QWARPS * 32) k_combine(const CombineParams p) 
   extern __shared__ __align__(16) float csm[];
   float *r = csm;              // [128][128]
   float *o = csm + D * D;      // [QWARPS][128]
+  pdl_trigger();
   if (p.r) stage_matrix(r, p.r);
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.x * QWARPS + warp;
   const bool live = bh < p.n_heads;
@@ -758,8 +764,7 @@ cudaError_t launch_prepare_q(const tq_ctx *k, const void *q, int q_dtype, const 
   auto kern = s.pv ? k_prepare_q<true> : k_prepare_q<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, QWARPS * 32, smem, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(QWARPS * 32), smem, st, p);
 }
 
 template <int NG, bool SC, int KP, int VP, bool FIXED>
@@ -771,8 +776,7 @@ cudaError_t launch_t4(const PartialParams &p, dim3 grid, cudaStream_t st) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                              (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  kern<<<grid, NTHREADS, smem, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(NTHREADS), smem, st, p);
 }
 
 // Decode-word split between the table (shared-memory pipe) and byte permutes (ALU pipe):
@@ -828,8 +832,7 @@ cudaError_t launch_combine(const tq_ctx *k, const tq_ctx *v, const DecodeShape &
   const size_t smem = (size_t)D * D * 4 + QWARPS * D * 4;
   cudaError_t e = cudaFuncSetAttribute(k_combine, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  k_combine<<<(p.n_heads + QWARPS - 1) / QWARPS, QWARPS * 32, smem, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(k_combine, dim3((p.n_heads + QWARPS - 1) / QWARPS), dim3(QWARPS * 32), smem, st, p);
 }
 
 }  // namespace tq

@@ -105,6 +105,7 @@ __global__ void __maxnreg__(168) k_partial_pv(const PvParams p) {
   uint32_t *mse_lut = reinterpret_cast<uint32_t *>(smem_raw + MSE_OFF);
   uint32_t *sign_lut = reinterpret_cast<uint32_t *>(smem_raw + SIGN_OFF);
   const int cta = blockIdx.x;
+  pdl_trigger();
   if (FIXED && smem_addr(smem_raw) != RESERVED_SMEM) {
     if (threadIdx.x == 0) atomicExch(p.status, (int32_t)DEVERR_LAYOUT);
     return;
@@ -116,10 +117,6 @@ __global__ void __maxnreg__(168) k_partial_pv(const PvParams p) {
     }
     sm.abort_flag = 0;
     fence_mbar_init();
-  }
-  if (threadIdx.x == 0 && p.seq_lens) {
-    for (int b = 0; b < p.B; ++b)
-      if (p.seq_lens[b] < 1 || p.seq_lens[b] > p.L) atomicExch(p.status, (int32_t)DEVERR_SEQLEN);
   }
   // MSE table: byte of four 2-bit indices -> (c[i0], c[i1]), (c[i2], c[i3]) as fp16x2,
   // one 8-byte slot per lane.  Sign table: nibble of four QJL bits -> four fp16 +-1.
@@ -136,6 +133,11 @@ __global__ void __maxnreg__(168) k_partial_pv(const PvParams p) {
     auto sg = [nib](int i) { return ((nib >> i) & 1) ? 0x3C00u : 0xBC00u; };
     const uint32_t w0 = sg(0) | (sg(1) << 16), w1 = sg(2) | (sg(3) << 16);
     reinterpret_cast<uint4 *>(sign_lut + nib * 64)[chunk] = make_uint4(w0, w1, w0, w1);
+  }
+  pdl_wait();  // the caches, q and the workspace may be written by the previous kernel
+  if (threadIdx.x == 0 && p.seq_lens) {
+    for (int b = 0; b < p.B; ++b)
+      if (p.seq_lens[b] < 1 || p.seq_lens[b] > p.L) atomicExch(p.status, (int32_t)DEVERR_SEQLEN);
   }
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -427,8 +429,7 @@ cudaError_t launch_pv(const PvParams &p, dim3 grid, cudaStream_t st) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                              (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  kern<<<grid, NTH, SMEM_PV, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(NTH), SMEM_PV, st, p);
 }
 
 }  // namespace

@@ -62,6 +62,16 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// ---- programmatic dependent launch ----
+// Every kernel of the library is launched so that it may start while the previous
+// kernel on the stream is still finishing: it runs its prologue (work that reads only
+// the immutable context), then waits here until the previous grid has completed and its
+// memory is visible.  Without such a launch the wait returns at once.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Allows the next kernel on the stream to be scheduled (it still waits in pdl_wait for
+// this grid to complete before touching its results).
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---- mbarrier + bulk async copy (shared::cta barriers, CTA-local copies) ----
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {

@@ -55,6 +55,26 @@ struct tq_ctx {
 
 namespace tq {
 
+// Launch with programmatic stream serialization: the kernel may begin its prologue
+// while the previous kernel on the stream finishes (it waits with pdl_wait before
+// touching anything that kernel may write).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 // ---- host helpers (tq_host.cpp) ----
 bool make_codebook_f64(int bits, int d, int kind, double *c);
 void store_codebook(const double *c64, int K, float *c32, float *b32);

@@ -19,6 +19,7 @@ namespace tq {
 namespace {
 
 constexpr int WARPS = 8;
+constexpr int64_t SMALL_ROWS = 256;  // at most this many dense rows: one CTA per row
 constexpr int ROWBUF = 72;  // per-warp staging for one packed row (max 68 bytes)
 
 struct WriteParams {
@@ -153,8 +154,10 @@ __global__ void __launch_bounds__(WARPS * 32) k_write_wht(const WriteParams p) {
   constexpr int RB = (FMT == TQ_FMT_TURBO4) ? 68 : 56;
   __shared__ float sb[16];
   __shared__ __align__(16) uint8_t rowbuf[WARPS][ROWBUF];
+  pdl_trigger();
   if (threadIdx.x < NB) sb[threadIdx.x] = p.b[threadIdx.x];
   __syncthreads();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int64_t row = (int64_t)blockIdx.x * WARPS + warp; row < p.n_rows;
        row += (int64_t)gridDim.x * WARPS) {
@@ -198,6 +201,7 @@ __global__ void __launch_bounds__(WARPS * 32) k_write_dense(const WriteParams p)
   uint8_t *ib = reinterpret_cast<uint8_t *>(vec + WARPS * 3 * D);    // [WARPS][128] indices
   uint8_t *rowbuf = ib + WARPS * D;                                  // [WARPS][ROWBUF]
   float *sb = reinterpret_cast<float *>(rowbuf + WARPS * ROWBUF);    // [16]
+  pdl_trigger();
   stage128(RT, p.pit);
   if (FMT == TQ_FMT_PROD3) {
     stage128(Rm, p.pi);
@@ -205,6 +209,7 @@ __global__ void __launch_bounds__(WARPS * 32) k_write_dense(const WriteParams p)
   }
   if (threadIdx.x < 15) sb[threadIdx.x] = p.b[threadIdx.x];
   __syncthreads();
+  pdl_wait();
   constexpr int NB = (FMT == TQ_FMT_TURBO4) ? 15 : (FMT == TQ_FMT_TURBO3 ? 7 : 3);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float *u = vec + warp * 3 * D;
@@ -289,9 +294,77 @@ __global__ void __launch_bounds__(WARPS * 32) k_write_dense(const WriteParams p)
   }
 }
 
+// ---------------------------------------- dense rotation, small batches (one CTA per row)
+// For the few rows of a decode step: thread j computes output coordinate j from row j
+// of R read straight from L2 (no 64 KB staging), so the launch costs about one memory
+// latency.  Norm, normalisation and packing follow the same canonical order as above.
+template <int FMT, int SRC>
+__global__ void __launch_bounds__(D) k_write_dense_row(const WriteParams p) {
+  constexpr int NB = (FMT == TQ_FMT_TURBO4) ? 15 : 7;
+  __shared__ float u[D];
+  __shared__ float grp[32];
+  __shared__ float sb[16];
+  __shared__ float nsh;
+  __shared__ __align__(16) uint8_t ib[D];
+  __shared__ __align__(16) uint8_t buf[ROWBUF];
+  const int64_t row = blockIdx.x;
+  const int j = threadIdx.x, lane = j & 31;
+  if (j == 0) {
+#pragma unroll
+    for (int k = 0; k < NB; ++k) sb[k] = p.b[k];  // constant indices keep p in parameter space
+  }
+  pdl_trigger();
+  pdl_wait();
+  const int64_t slot = p.row_ids ? p.row_ids[row] : row;
+  if (slot < 0 || slot >= p.dst_rows) {
+    if (j == 0) atomicExch(p.status, (int32_t)DEVERR_ROW_OOB);
+    return;
+  }
+  float x;
+  if (SRC == TQ_DTYPE_F32)
+    x = static_cast<const float *>(p.src)[row * p.stride + j];
+  else
+    x = bf16_bits_to_f32(static_cast<const uint16_t *>(p.src)[row * p.stride + j]);
+  // canonical norm: groups of four (pairs summed first), then the butterfly over groups
+  const float sq = __fmul_rn(x, x);
+  const float a = __fadd_rn(sq, __shfl_xor_sync(FULL_MASK, sq, 1));
+  const float g = __fadd_rn(a, __shfl_xor_sync(FULL_MASK, a, 2));
+  if ((j & 3) == 0) grp[j >> 2] = g;
+  __syncthreads();
+  if (j < 32) {
+    float pl = grp[lane];
+#pragma unroll
+    for (int h = 16; h >= 1; h >>= 1) pl = __fadd_rn(pl, __shfl_xor_sync(FULL_MASK, pl, h));
+    if (lane == 0) nsh = __fsqrt_rn(pl);
+  }
+  __syncthreads();
+  const float n = nsh;
+  u[j] = (n == 0.0f) ? 0.0f : __fdiv_rn(x, n);
+  __syncthreads();
+  const float4 *r4 = reinterpret_cast<const float4 *>(p.pi + (size_t)j * D);  // row j of R
+  float y = 0.f;
+#pragma unroll 8
+  for (int k4 = 0; k4 < D / 4; ++k4) {
+    const float4 r = r4[k4];
+    y = fmaf(r.x, u[4 * k4], y);
+    y = fmaf(r.y, u[4 * k4 + 1], y);
+    y = fmaf(r.z, u[4 * k4 + 2], y);
+    y = fmaf(r.w, u[4 * k4 + 3], y);
+  }
+  ib[j] = (uint8_t)bucket<NB>(y, sb);
+  __syncthreads();
+  if (j < 32) {
+    const uint32_t w4 = *reinterpret_cast<const uint32_t *>(ib + 4 * lane);
+    const uint32_t idx[4] = {w4 & 0xFF, (w4 >> 8) & 0xFF, (w4 >> 16) & 0xFF, w4 >> 24};
+    pack_store_turbo<FMT>(idx, n, buf, p.dst + slot * (FMT == TQ_FMT_TURBO4 ? 68 : 56), lane);
+  }
+}
+
 // ------------------------------------------------------------------ V group quant
 template <int SRC>
 __global__ void __launch_bounds__(WARPS * 32) k_write_vgroup(const WriteParams p) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ __align__(16) uint8_t rowbuf[WARPS][ROWBUF];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t *buf = rowbuf[warp];
@@ -346,8 +419,7 @@ cudaError_t launch_rows(K kernel, const WriteParams &p, int64_t n_rows, int num_
                                          (int)smem);
     if (e != cudaSuccess) return e;
   }
-  kernel<<<grid, WARPS * 32, smem, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kernel, dim3(grid), dim3(WARPS * 32), smem, st, p);
 }
 
 }  // namespace
@@ -383,6 +455,15 @@ cudaError_t launch_write(const tq_ctx *ctx, const WriteLaunch &w, cudaStream_t s
   }
   // Dense rotation on the tensor cores for 16-byte aligned bf16 rows (turbo4 / turbo3).
   if (write_tc_eligible(ctx, w)) return launch_write_tc(ctx, w, st);
+  // A few rows (a decode step's new tokens): one CTA per row, R read from L2.
+  if (w.n_rows <= SMALL_ROWS && fmt != TQ_FMT_PROD3) {
+    const dim3 grid((unsigned)w.n_rows), block(D);
+    if (fmt == TQ_FMT_TURBO4)
+      return bf16 ? launch_pdl(k_write_dense_row<TQ_FMT_TURBO4, TQ_DTYPE_BF16>, grid, block, 0, st, p)
+                  : launch_pdl(k_write_dense_row<TQ_FMT_TURBO4, TQ_DTYPE_F32>, grid, block, 0, st, p);
+    return bf16 ? launch_pdl(k_write_dense_row<TQ_FMT_TURBO3, TQ_DTYPE_BF16>, grid, block, 0, st, p)
+                : launch_pdl(k_write_dense_row<TQ_FMT_TURBO3, TQ_DTYPE_F32>, grid, block, 0, st, p);
+  }
   // Dense rotation on the CUDA cores (prod3 always takes this path; its WHT variant
   // multiplies by the materialised WHT matrix, which the context stores as well).
   const size_t mats = (fmt == TQ_FMT_PROD3 ? 3 : 1) * (size_t)D * D * sizeof(float);

@@ -145,6 +145,7 @@ __global__ void __launch_bounds__(TC_THREADS, 2) k_write_dense_tc(const __grid_c
   TcMisc &ms = *reinterpret_cast<TcMisc *>(smem + OFF_MISC);
   const int tid = threadIdx.x, warp = tid >> 5;
   const int64_t n_tiles = (p.n_rows + TC_ROWS - 1) / TC_ROWS;
+  pdl_trigger();
 
   if (warp == 0) tmem_alloc(smem_addr(&ms.tmem_addr), TMEM_COLS);
   if (tid == 0) {
@@ -168,6 +169,7 @@ __global__ void __launch_bounds__(TC_THREADS, 2) k_write_dense_tc(const __grid_c
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_wait();  // the rows and the cache may be written by the previous kernel
   const uint32_t tmem = ms.tmem_addr;
   const uint32_t sx = smem_addr(smem + OFF_X);
   const uint32_t spih = smem_addr(smem + OFF_PIH), spil = smem_addr(smem + OFF_PIL);
@@ -341,8 +343,7 @@ cudaError_t launch_write_tc(const tq_ctx *ctx, const WriteLaunch &w, cudaStream_
   auto kern = ctx->fmt == TQ_FMT_TURBO4 ? k_write_dense_tc<TQ_FMT_TURBO4> : k_write_dense_tc<TQ_FMT_TURBO3>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_TC);
   if (e != cudaSuccess) return e;
-  kern<<<grid, TC_THREADS, SMEM_TC, st>>>(map, p);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(TC_THREADS), SMEM_TC, st, map, p);
 }
 
 }  // namespace tq

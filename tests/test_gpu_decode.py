@@ -108,6 +108,22 @@ def test_decode_q_dtypes_and_staged_calls(q_dtype):
     assert np.array_equal(out1, out2)
 
 
+def test_decode_many_heads_staged_kernels():
+    """1152 query heads (36 batches x 32): many CTAs of the q-preparation and combine
+    kernels, each serving eight heads."""
+    tq = lib()
+    B, Hq, Hkv, L = 36, 32, 8, 70
+    codec = Codec("turbo4", rotation="dense", rot_seed=7)
+    kb, vb = oracle_cache(codec, B, Hkv, L, 13), oracle_cache(codec, B, Hkv, L, 14)
+    q_t, q32 = torch_rows(np.random.default_rng(8).standard_normal((B, Hq, 128)).astype(np.float32), "bf16")
+    ctx = tq.Ctx("turbo4", "dense", 7)
+    out, sc = run_decode(tq, ctx, ctx, q_t, upload_cache(tq, "turbo4", kb), upload_cache(tq, "turbo4", vb),
+                         B, Hq, Hkv, L)
+    ref, s_ref = reference(q32, codec, kb, codec, vb, None)
+    check_outputs(out, ref)
+    assert np.max(np.abs(sc - s_ref)) <= ATOL
+
+
 def test_decode_scale_argument_and_peaked_attention():
     """A large explicit scale makes the softmax peaked; results still match."""
     tq = lib()

@@ -161,3 +161,19 @@ def test_full_size_prod_vgroup():
         vb = vhost[u * L * 48:(u + 1) * L * 48].reshape(1, 1, L, 48)
         ref, _ = reference(q32[b:b + 1, h:h + 1], kcodec, kb, vcodec, vb, None)
         check_outputs(out[b:b + 1, h:h + 1], ref)
+
+
+def test_decode_pv_many_heads_staged_prep():
+    """1056 query heads (44 batches x 24) through the q preparation with the QJL sketch."""
+    tq = lib()
+    B, Hq, Hkv, L = 44, 24, 4, 40
+    kcodec, vcodec = codecs()
+    kb = encoded(kcodec, B, Hkv, L, 30)
+    vb = encoded(vcodec, B, Hkv, L, 31)
+    q_t, q32 = torch_rows(np.random.default_rng(32).standard_normal((B, Hq, 128)).astype(np.float32), "bf16")
+    kctx, vctx = contexts(tq)
+    out, sc = run(tq, kctx, vctx, q_t, upload_cache(tq, "prod3", kb), upload_cache(tq, "vgroup2", vb),
+                  B, Hq, Hkv, L)
+    ref, s_ref = reference(q32, kcodec, kb, vcodec, vb, None)
+    check_outputs(out, ref)
+    assert np.max(np.abs(sc - s_ref)) <= ATOL
