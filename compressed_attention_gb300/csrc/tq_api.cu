@@ -207,6 +207,7 @@ tq_status tq_ctx_create(const tq_params *params, tq_ctx **out) {
     c->cb.K = 1 << bits;
     store_codebook(c64, c->cb.K, c->cb.c, c->cb.b);
     c->f16 = make_f16_table(c->cb.c, c->cb.K);
+    c->bt = make_bucket_table(c->cb.b, c->cb.K - 1);
     std::vector<float> r;
     s = build_rotation(p.rotation, p.rot_seed, r, c->wht_neg);
     if (s == TQ_OK) s = to_device(&c->d_pi, r.data(), r.size());
@@ -236,6 +237,7 @@ tq_status tq_ctx_create(const tq_params *params, tq_ctx **out) {
       if (s == TQ_OK) s = to_device(&c->d_St, St.data(), St.size());
     }
   }
+  if (s == TQ_OK && rotated) s = to_device(&c->d_bt, &c->bt, 1);
   if (s == TQ_OK) {
     e = cudaMalloc((void **)&c->d_status, sizeof(int32_t));
     if (e != cudaSuccess) s = fail(TQ_ERR_ALLOC, "cudaMalloc failed");
@@ -256,6 +258,7 @@ tq_status tq_ctx_destroy(tq_ctx *ctx) {
   cudaFree(ctx->d_S);
   cudaFree(ctx->d_St);
   cudaFree(ctx->d_pib);
+  cudaFree(ctx->d_bt);
   cudaFree(ctx->d_status);
   delete ctx;
   return TQ_OK;

@@ -211,4 +211,35 @@ F16Table make_f16_table(const float *c32, int K) {
   return t;
 }
 
+BucketTable make_bucket_table(const float *b, int nb) {
+  BucketTable t;
+  if (nb < 1) return t;
+  double gap = 1e300;
+  for (int k = 0; k + 1 < nb; ++k) gap = std::fmin(gap, (double)b[k + 1] - (double)b[k]);
+  if (nb == 1) gap = 1.0;
+  if (!(gap > 0.0) || !std::isfinite(gap)) return t;
+  const double w = gap, lo = (double)b[0] - w, delta = 0.05 * w;
+  const int n = (int)std::ceil(((double)b[nb - 1] - lo) / w) + 2;
+  if (n > 64) return t;
+  for (int c = 0; c < n; ++c) {
+    const double a = lo + c * w - delta, z = lo + (c + 1) * w + delta;
+    int cnt = 0, listed = 0;
+    float e[2] = {INFINITY, INFINITY};
+    for (int k = 0; k < nb; ++k) {
+      if ((double)b[k] < a) {
+        ++cnt;
+      } else if ((double)b[k] <= z) {
+        if (listed == 2) return BucketTable{};
+        e[listed++] = b[k];
+      }
+    }
+    t.cnt[c] = (uint8_t)cnt;
+    t.e[c] = make_float2(e[0], e[1]);
+  }
+  t.scale = (float)(1.0 / w);
+  t.offset = (float)(-lo / w);
+  t.n = n;
+  return t;
+}
+
 }  // namespace tq

@@ -34,6 +34,19 @@ struct F16Table {
   float max_rel_err = 0.0f;
 };
 
+// Nearest-centroid decision through a uniform grid over the decision boundaries.
+// Cell t (width w, the smallest boundary gap) holds cnt[t] = #{k : b_k < left edge - delta}
+// and the at most two boundaries within [left edge - delta, right edge + delta] (+inf
+// where fewer), so idx(y) = #{k : y > b_k} = cnt[t] + [y > e[t].x] + [y > e[t].y] for every
+// y whose computed cell t = clamp(floor(y * scale + offset), 0, n - 1) -- the fp32 cell
+// computation is off by far less than delta.  n == 0: the table is unusable.
+struct alignas(16) BucketTable {
+  float scale = 0.f, offset = 0.f;
+  int n = 0, pad = 0;
+  uint8_t cnt[64] = {};
+  float2 e[64] = {};
+};
+
 }  // namespace tq
 
 struct tq_ctx {
@@ -50,6 +63,8 @@ struct tq_ctx {
   float *d_S = nullptr;                 // QJL matrix S, fp32 [128][128] row-major
   float *d_St = nullptr;                // S^T, fp32 row-major
   uint16_t *d_pib = nullptr;            // dense R as bf16 hi then lo, [2][128][128] (tensor-core write)
+  tq::BucketTable bt{};                 // nearest-centroid grid of the codebook (host copy)
+  tq::BucketTable *d_bt = nullptr;      // the same on the device
   int32_t *d_status = nullptr;          // device status word
 };
 
@@ -82,6 +97,7 @@ void splitmix64_fill(uint64_t seed, uint64_t *out, size_t n);
 void gaussian_fill(uint64_t seed, double *out, size_t n);
 bool dense_rotation_f64(uint64_t seed, int d, double *pi);
 F16Table make_f16_table(const float *c32, int K);
+BucketTable make_bucket_table(const float *b, int nb);
 void set_error(const char *fmt, ...);
 
 // ---- kernel launchers ----

@@ -37,7 +37,19 @@ struct WriteParams {
   const float *pit; // its transpose
   const float *S;   // prod3: fp32 [128][128]
   const float *St;  // its transpose
+  const BucketTable *bt;  // nearest-centroid grid (n == 0: binary search over b)
 };
+
+// Stage the codebook grid in shared memory (16-byte pieces, all threads).
+__device__ __forceinline__ void stage_grid(BucketTable *dst, const BucketTable *src) {
+  constexpr int N16 = sizeof(BucketTable) / 16;
+  for (int i = threadIdx.x; i < N16; i += blockDim.x)
+    reinterpret_cast<uint4 *>(dst)[i] = reinterpret_cast<const uint4 *>(src)[i];
+}
+
+// Nearest-centroid index of y: the grid table when usable, else binary search.
+template <int NB>
+__device__ __forceinline__ uint32_t nearest(float y, const BucketTable &g, const float *sb);
 
 template <int SRC>
 __device__ __forceinline__ void load4(const void *src, int64_t row, int64_t stride, int lane,
@@ -102,6 +114,11 @@ __device__ __forceinline__ uint32_t bucket(float y, const float *sb) {
   return pos;
 }
 
+template <int NB>
+__device__ __forceinline__ uint32_t nearest(float y, const BucketTable &g, const float *sb) {
+  return g.n ? bucket_grid(y, g.scale, g.offset, g.n, g.cnt, g.e) : bucket<NB>(y, sb);
+}
+
 // Pack one turbo4 / turbo3 row from per-lane indices (elements 4l..4l+3) and store
 // it at dst + slot * row_bytes through the warp's staging buffer.
 template <int FMT>
@@ -153,9 +170,11 @@ __global__ void __launch_bounds__(WARPS * 32) k_write_wht(const WriteParams p) {
   constexpr int NB = (FMT == TQ_FMT_TURBO4) ? 15 : 7;
   constexpr int RB = (FMT == TQ_FMT_TURBO4) ? 68 : 56;
   __shared__ float sb[16];
+  __shared__ BucketTable grid;
   __shared__ __align__(16) uint8_t rowbuf[WARPS][ROWBUF];
   pdl_trigger();
   if (threadIdx.x < NB) sb[threadIdx.x] = p.b[threadIdx.x];
+  stage_grid(&grid, p.bt);
   __syncthreads();
   pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -169,7 +188,7 @@ __global__ void __launch_bounds__(WARPS * 32) k_write_wht(const WriteParams p) {
     wht_rotate(v, p.wht_neg, lane);
     uint32_t idx[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) idx[e] = bucket<NB>(v[e], sb);
+    for (int e = 0; e < 4; ++e) idx[e] = nearest<NB>(v[e], grid, sb);
     pack_store_turbo<FMT>(idx, n, rowbuf[warp], p.dst + slot * RB, lane);
   }
 }
@@ -201,7 +220,9 @@ __global__ void __launch_bounds__(WARPS * 32) k_write_dense(const WriteParams p)
   uint8_t *ib = reinterpret_cast<uint8_t *>(vec + WARPS * 3 * D);    // [WARPS][128] indices
   uint8_t *rowbuf = ib + WARPS * D;                                  // [WARPS][ROWBUF]
   float *sb = reinterpret_cast<float *>(rowbuf + WARPS * ROWBUF);    // [16]
+  __shared__ BucketTable grid;
   pdl_trigger();
+  stage_grid(&grid, p.bt);
   stage128(RT, p.pit);
   if (FMT == TQ_FMT_PROD3) {
     stage128(Rm, p.pi);
@@ -235,7 +256,7 @@ __global__ void __launch_bounds__(WARPS * 32) k_write_dense(const WriteParams p)
       for (int m = 0; m < 4; ++m) y[m] = fmaf(rt[32 * m], uk, y[m]);
     }
 #pragma unroll
-    for (int m = 0; m < 4; ++m) myib[lane + 32 * m] = (uint8_t)bucket<NB>(y[m], sb);
+    for (int m = 0; m < 4; ++m) myib[lane + 32 * m] = (uint8_t)nearest<NB>(y[m], grid, sb);
     __syncwarp();
     uint32_t idx[4];
     const uint32_t w4 = *reinterpret_cast<const uint32_t *>(myib + 4 * lane);
@@ -304,6 +325,7 @@ __global__ void __launch_bounds__(D) k_write_dense_row(const WriteParams p) {
   __shared__ float u[D];
   __shared__ float grp[32];
   __shared__ float sb[16];
+  __shared__ BucketTable grid;
   __shared__ float nsh;
   __shared__ __align__(16) uint8_t ib[D];
   __shared__ __align__(16) uint8_t buf[ROWBUF];
@@ -313,6 +335,7 @@ __global__ void __launch_bounds__(D) k_write_dense_row(const WriteParams p) {
 #pragma unroll
     for (int k = 0; k < NB; ++k) sb[k] = p.b[k];  // constant indices keep p in parameter space
   }
+  stage_grid(&grid, p.bt);
   pdl_trigger();
   pdl_wait();
   const int64_t slot = p.row_ids ? p.row_ids[row] : row;
@@ -351,7 +374,7 @@ __global__ void __launch_bounds__(D) k_write_dense_row(const WriteParams p) {
     y = fmaf(r.z, u[4 * k4 + 2], y);
     y = fmaf(r.w, u[4 * k4 + 3], y);
   }
-  ib[j] = (uint8_t)bucket<NB>(y, sb);
+  ib[j] = (uint8_t)nearest<NB>(y, grid, sb);
   __syncthreads();
   if (j < 32) {
     const uint32_t w4 = *reinterpret_cast<const uint32_t *>(ib + 4 * lane);
@@ -440,6 +463,7 @@ cudaError_t launch_write(const tq_ctx *ctx, const WriteLaunch &w, cudaStream_t s
   p.pit = ctx->d_pit;
   p.S = ctx->d_S;
   p.St = ctx->d_St;
+  p.bt = ctx->d_bt;
   const bool bf16 = (w.src_dtype == TQ_DTYPE_BF16);
   const int fmt = ctx->fmt;
   const int sms = ctx->num_sms;
