@@ -61,7 +61,7 @@ DECODE = {
     "single_head": dict(k_fmt="turbo4", v_fmt="turbo4", rotation="wht", k_seed=0, v_seed=100, qjl_seed=0,
                         kernel="k_partial_t4", source="tq_decode.cu"),
 }
-WRITE_KERNEL = {"dense": ("k_write_dense", "tq_write.cu"), "wht": ("k_write_wht", "tq_write.cu")}
+WRITE_KERNEL = {"dense": ("k_write_dense_tc", "tq_write_tc.cu"), "wht": ("k_write_wht", "tq_write.cu")}
 
 
 def measured_peak():
