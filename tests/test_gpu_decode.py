@@ -238,3 +238,47 @@ def test_full_size_gqa_lognormal_dense():
 
 def test_full_size_long_context_wht():
     _full_size("long_context", "wht", 5, [(0, 0), (0, 17), (0, 31)])
+
+
+def test_decode_one_unit_many_splits():
+    """One (batch, KV head) unit of 200,000 keys spread over every SM: about a hundred
+    splits per head to merge, 8 q-heads per KV head (two column groups), a ragged last
+    tile; all heads against the oracle on the GPU-written packed bytes."""
+    import torch
+    tq = lib()
+    B, Hq, Hkv, L = 1, 8, 1, 200_000
+    assert tq.tq_decode_num_splits(tq.Ctx("turbo4", "dense", 9), tq.Ctx("turbo4", "dense", 109), B, Hq, Hkv, L) > 50
+    kctx, vctx = tq.Ctx("turbo4", "dense", 9), tq.Ctx("turbo4", "dense", 109)
+    rng = np.random.default_rng(41)
+    caches = []
+    for ctx in (kctx, vctx):
+        x = rng.standard_normal((L, 128), dtype=np.float32)
+        t = torch.from_numpy(synth.bf16_bits(x).view(np.int16)).view(torch.bfloat16).cuda()
+        cache = tq.alloc_cache("turbo4", L)
+        tq.tq_quantize_set_rows(ctx, t, cache)
+        caches.append(cache)
+    q_t, q32 = torch_rows(rng.standard_normal((B, Hq, 128)).astype(np.float32), "bf16")
+    out, _ = run_decode(tq, kctx, vctx, q_t, caches[0], caches[1], B, Hq, Hkv, L, scores=False)
+    assert tq.tq_ctx_device_status(kctx) == 0
+    kcod, vcod = Codec("turbo4", rotation="dense", rot_seed=9), Codec("turbo4", rotation="dense", rot_seed=109)
+    kb = to_host_bytes_rows(caches[0], L).reshape(1, 1, L, 68)
+    vb = to_host_bytes_rows(caches[1], L).reshape(1, 1, L, 68)
+    ref, _ = reference(q32, kcod, kb, vcod, vb, None)
+    check_outputs(out, ref)
+
+
+def to_host_bytes_rows(cache, n):
+    return cache.cpu().numpy()[: n * 68].reshape(n, 68)
+
+
+def test_decode_shape_limits():
+    """L = 0 and B = 0 are invalid; a shape whose tile count overflows 32 bits is refused."""
+    tq = lib()
+    ctx = tq.Ctx("turbo4", "wht", 0)
+    for args in ((1, 4, 1, 0), (0, 4, 1, 64)):
+        with pytest.raises(tq.TQError) as e:
+            tq.tq_decode_workspace_size(ctx, ctx, *args)
+        assert e.value.status == tq.TQ_ERR_INVALID_ARG
+    with pytest.raises(tq.TQError) as e:
+        tq.tq_decode_workspace_size(ctx, ctx, 1 << 20, 8, 8, 1 << 20)
+    assert e.value.status == tq.TQ_ERR_UNSUPPORTED
