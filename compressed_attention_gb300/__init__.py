@@ -70,6 +70,7 @@ _SIGNATURES = {
     "tq_decode_combine": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _sz, _vp]),
     "tq_decode_attention_static": (_i32, [_vp, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _f32,
                                           _vp, _vp]),
+    "tq_test_decode_wait_timeout": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _sz, _vp]),
 }
 
 

@@ -398,4 +398,21 @@ tq_status tq_decode_attention(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const vo
   return tq_decode_combine(k_ctx, v_ctx, B, Hq, Hkv, L, out, workspace, workspace_bytes, stream);
 }
 
+tq_status tq_test_decode_wait_timeout(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *k_cache,
+                                      const void *v_cache, int B, int Hq, int Hkv, int L, void *workspace,
+                                      size_t workspace_bytes, tq_stream_t stream) {
+  DecodeShape s;
+  tq_status st = check_decode_common(k_ctx, v_ctx, B, Hq, Hkv, L, &s);
+  if (st != TQ_OK) return st;
+  if (s.pv) return fail(TQ_ERR_UNSUPPORTED, "the timeout test runs the turbo4 decode kernel");
+  if (!k_cache || !v_cache) return fail(TQ_ERR_INVALID_ARG, "null cache");
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return fail(TQ_ERR_ALIGNMENT, "caches must be 16-byte aligned");
+  Workspace w;
+  if ((st = check_workspace(s, workspace, workspace_bytes, &w)) != TQ_OK) return st;
+  cudaError_t e = launch_partial(k_ctx, v_ctx, (const uint8_t *)k_cache, (const uint8_t *)v_cache, nullptr, s,
+                                 nullptr, w, (cudaStream_t)stream, true);
+  if (e != cudaSuccess) return cuda_fail(e, "partial launch");
+  return TQ_OK;
+}
+
 }  // extern "C"

@@ -207,6 +207,7 @@ struct PartialParams {
   const float *qsc;
   float *part;
   float *scores;
+  int withhold_first_tile;                  // failure test: the producer never copies tile 0
   uint32_t kc16[8], vc16[8];                // signed fp16 centroids (K, V), two per word
   uint32_t klo[2], khi[2], vlo[2], vhi[2];  // byte-permute tables (K and V codebooks)
   int32_t *status;
@@ -347,6 +348,10 @@ __global__ void __maxnreg__(128)
           if (kf >= Lb) break;  // consumers skip the same tiles
           const int nk = min(TILE, Lb - kf);
           const int s = ctr % NSTAGE;
+          if (p.withhold_first_tile && ctr == 0) {  // failure test: consumers wait in vain
+            ++ctr;
+            continue;
+          }
           if (ctr >= NSTAGE &&
               !mbar_wait_bounded(&sm.empty[s], ((ctr / NSTAGE) - 1) & 1, WAIT_LIMIT_NS)) {
             atomicExch(&sm.abort_flag, 1);
@@ -786,9 +791,11 @@ constexpr int V_PRMT_WORDS = 0;
 
 cudaError_t launch_partial(const tq_ctx *k, const tq_ctx *v, const uint8_t *kc,
                            const uint8_t *vc, const int32_t *seq_lens, const DecodeShape &s,
-                           float *scores_dbg, const Workspace &ws, cudaStream_t st) {
+                           float *scores_dbg, const Workspace &ws, cudaStream_t st,
+                           bool withhold_first_tile) {
   if (s.pv) return launch_partial_pv(k, v, kc, vc, seq_lens, s, scores_dbg, ws, st);
   PartialParams p{};
+  p.withhold_first_tile = withhold_first_tile ? 1 : 0;
   p.kc = kc, p.vc = vc, p.seq_lens = seq_lens;
   p.B = s.B, p.Hq = s.Hq, p.Hkv = s.Hkv, p.L = s.L, p.gq = s.gq, p.n_hg = s.n_hg;
   p.tiles_per_unit = s.tiles_per_unit, p.tiles_per_cta = s.tiles_per_cta;

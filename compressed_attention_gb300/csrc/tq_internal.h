@@ -149,7 +149,8 @@ cudaError_t launch_prepare_q(const tq_ctx *k, const void *q, int q_dtype, const 
                              float scale, const Workspace &ws, cudaStream_t st);
 cudaError_t launch_partial(const tq_ctx *k, const tq_ctx *v, const uint8_t *kc,
                            const uint8_t *vc, const int32_t *seq_lens, const DecodeShape &s,
-                           float *scores_dbg, const Workspace &ws, cudaStream_t st);
+                           float *scores_dbg, const Workspace &ws, cudaStream_t st,
+                           bool withhold_first_tile = false);
 cudaError_t launch_partial_pv(const tq_ctx *k, const tq_ctx *v, const uint8_t *kc,
                               const uint8_t *vc, const int32_t *seq_lens, const DecodeShape &s,
                               float *scores_dbg, const Workspace &ws, cudaStream_t st);

@@ -254,6 +254,18 @@ tq_status tq_decode_attention_static(const tq_ctx *k_ctx, const tq_ctx *v_ctx, c
                                      const int32_t *seq_lens, int B, int Hq, int Hkv, int L,
                                      float scale, float *out, tq_stream_t stream);
 
+/* ------------------------------------------------------------- testing hook */
+
+/* Failure detection test (no counterpart on the pages): runs the split-K decode
+ * kernel of tq_decode_partial (TURBO4 pair) with its producer withholding the first
+ * tile, so every consumer's bounded wait runs out (about 2 s).  The kernel then
+ * records status 3 in k_ctx's status word and returns without output; the context
+ * and the device stay usable.  Arguments as tq_decode_partial (no seq_lens, no
+ * scores); nothing is written to the caches. */
+tq_status tq_test_decode_wait_timeout(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *k_cache,
+                                      const void *v_cache, int B, int Hq, int Hkv, int L, void *workspace,
+                                      size_t workspace_bytes, tq_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
