@@ -65,11 +65,10 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 // Index of the nearest centroid, #{k : y > b_k}, from the grid table (see BucketTable);
 // cnt, e: the table's arrays staged in shared memory.
 __device__ __forceinline__ uint32_t bucket_grid(float y, float scale, float offset, int n,
-                                                const uint8_t *cnt, const float2 *e) {
+                                                const uint8_t *cnt, const float *e) {
   int t = __float2int_rd(fmaf(y, scale, offset));  // NaN -> 0, +-inf -> saturated
   t = min(max(t, 0), n - 1);
-  const float2 ee = e[t];
-  return (uint32_t)cnt[t] + (y > ee.x ? 1u : 0u) + (y > ee.y ? 1u : 0u);
+  return (uint32_t)cnt[t] + (y > e[t] ? 1u : 0u);
 }
 
 // ---- programmatic dependent launch ----

@@ -218,23 +218,24 @@ BucketTable make_bucket_table(const float *b, int nb) {
   for (int k = 0; k + 1 < nb; ++k) gap = std::fmin(gap, (double)b[k + 1] - (double)b[k]);
   if (nb == 1) gap = 1.0;
   if (!(gap > 0.0) || !std::isfinite(gap)) return t;
-  const double w = gap, lo = (double)b[0] - w, delta = 0.05 * w;
+  const double w = 0.4 * gap, lo = (double)b[0] - w, delta = 0.05 * w;
   const int n = (int)std::ceil(((double)b[nb - 1] - lo) / w) + 2;
-  if (n > 64) return t;
+  if (n > GRID_CELLS) return t;
   for (int c = 0; c < n; ++c) {
     const double a = lo + c * w - delta, z = lo + (c + 1) * w + delta;
     int cnt = 0, listed = 0;
-    float e[2] = {INFINITY, INFINITY};
+    float e = INFINITY;
     for (int k = 0; k < nb; ++k) {
       if ((double)b[k] < a) {
         ++cnt;
       } else if ((double)b[k] <= z) {
-        if (listed == 2) return BucketTable{};
-        e[listed++] = b[k];
+        if (listed == 1) return BucketTable{};
+        e = b[k];
+        ++listed;
       }
     }
     t.cnt[c] = (uint8_t)cnt;
-    t.e[c] = make_float2(e[0], e[1]);
+    t.e[c] = e;
   }
   t.scale = (float)(1.0 / w);
   t.offset = (float)(-lo / w);

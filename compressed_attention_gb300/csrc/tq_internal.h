@@ -35,16 +35,18 @@ struct F16Table {
 };
 
 // Nearest-centroid decision through a uniform grid over the decision boundaries.
-// Cell t (width w, the smallest boundary gap) holds cnt[t] = #{k : b_k < left edge - delta}
-// and the at most two boundaries within [left edge - delta, right edge + delta] (+inf
-// where fewer), so idx(y) = #{k : y > b_k} = cnt[t] + [y > e[t].x] + [y > e[t].y] for every
-// y whose computed cell t = clamp(floor(y * scale + offset), 0, n - 1) -- the fp32 cell
-// computation is off by far less than delta.  n == 0: the table is unusable.
+// Cells are 2/5 of the smallest boundary gap wide, so a cell widened by delta (5% of a
+// cell) on each side holds at most one boundary: cell t stores cnt[t] = #{k : b_k <
+// left edge - delta} and that boundary (+inf when none), and idx(y) = #{k : y > b_k} =
+// cnt[t] + [y > e[t]] for every y whose computed cell t = clamp(floor(y * scale +
+// offset), 0, n - 1) -- the fp32 cell computation errs by far less than delta.
+// n == 0: the table is unusable (binary search instead).
+constexpr int GRID_CELLS = 160;
 struct alignas(16) BucketTable {
   float scale = 0.f, offset = 0.f;
   int n = 0, pad = 0;
-  uint8_t cnt[64] = {};
-  float2 e[64] = {};
+  uint8_t cnt[GRID_CELLS] = {};
+  float e[GRID_CELLS] = {};
 };
 
 }  // namespace tq
