@@ -12,6 +12,7 @@ keys/s alongside; the dominant kernel (split-K decode) is also timed alone for t
 roofline.
 
 --workload picks another workload of the same path:
+  gqa_t3k       the gqa_lognormal inputs with turbo3 keys and turbo4 values
   long_context  B=1, Hq=32, Hkv=8, L=131,072, turbo4 K and V, randomized WHT
   prod_vgroup   B=4, Hq=24, Hkv=4, L=30,000, prod3 keys (2-bit + QJL), vgroup2 values
   single_head   B=1, Hq=Hkv=1, L=512, fp32 q, turbo4 K and V, randomized WHT
@@ -60,6 +61,8 @@ DECODE = {
                         kernel="k_partial_pv", source="tq_decode_pv.cu"),
     "single_head": dict(k_fmt="turbo4", v_fmt="turbo4", rotation="wht", k_seed=0, v_seed=100, qjl_seed=0,
                         kernel="k_partial_t4", source="tq_decode.cu"),
+    "gqa_t3k": dict(k_fmt="turbo3", v_fmt="turbo4", rotation="dense", k_seed=6, v_seed=106, qjl_seed=0,
+                    kernel="k_partial_t4", source="tq_decode.cu"),
 }
 WRITE_KERNEL = {"dense": ("k_write_dense_tc", "tq_write_tc.cu"), "wht": ("k_write_wht", "tq_write.cu")}
 

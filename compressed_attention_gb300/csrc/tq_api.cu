@@ -76,7 +76,7 @@ tq_status to_device(T **dst, const T *src, size_t n) {
 }
 
 bool decode_pair_supported(const tq_ctx *k, const tq_ctx *v) {
-  return (k->fmt == TQ_FMT_TURBO4 && v->fmt == TQ_FMT_TURBO4) ||
+  return ((k->fmt == TQ_FMT_TURBO4 || k->fmt == TQ_FMT_TURBO3) && v->fmt == TQ_FMT_TURBO4) ||
          (k->fmt == TQ_FMT_PROD3 && v->fmt == TQ_FMT_VGROUP2);
 }
 

@@ -47,6 +47,7 @@ static_assert(TILE == T4_TILE, "tile size shared with the host");
 constexpr int NTHREADS = (CWARPS + 1) * 32;  // + one producer warp; one CTA per SM
 constexpr int NSTAGE = 4;             // pipeline depth (about 128 KB in flight per SM)
 constexpr int T4_ROW = 68;
+constexpr int T3_ROW = 56;            // four 14-byte blocks of the 2+1 layout
 constexpr int STAGE_BUF = 16352;      // >= 240 * 68 + 2 * 15, multiple of 32
 
 // 8 packed 4-bit indices -> 8 fp16 centroid values as four fp16x2 words.
@@ -219,7 +220,8 @@ struct PartialParams {
 // device reserves the usual 1 KB at the window start, so a lookup's address
 // (b << 8) | (4 * slot) is one byte permute of the packed word and the table base
 // rides in the load's immediate.  Lane l reads slot l (keys) or 32 + l (values): a
-// warp's 32 lookups hit 32 distinct banks.  Eight stage buffers (K and V of NSTAGE
+// warp's 32 lookups hit 32 distinct banks.  With turbo3 keys the key slots of row b
+// hold the spread sign bits of sign byte b instead.  Eight stage buffers (K and V of NSTAGE
 // stages) and the merge scratch are packed around the table.
 struct SmemHead {
   float osm[CWARPS][4][D];              // per-warp accumulators of 4 heads, for the merge
@@ -273,6 +275,43 @@ __device__ __forceinline__ uint32_t ld_u32(const uint8_t *p) {
   return *reinterpret_cast<const uint32_t *>(p);
 }
 
+// Table word of a turbo3 sign byte s (element k's high index bit at bit k): the high
+// bit of element 2a at bit 4a + 2, that of element 2a + 1 at bit 16 + 4a + 2 -- bit 2
+// of nibble a of the two selector words t3_block builds.
+__host__ __device__ constexpr uint32_t t3_sign_word(uint32_t s) {
+  uint32_t w = 0;
+  for (int a = 0; a < 4; ++a)
+    w |= (((s >> (2 * a)) & 1u) << (4 * a + 2)) | (((s >> (2 * a + 1)) & 1u) << (16 + 4 * a + 2));
+  return w;
+}
+
+// Lane t's share of one 32-element turbo3 key block (the "2+1" layout: fp16 norm,
+// qs[8] holding the low two index bits of element j at bits 2(j%4) of qs[j/4],
+// signs[4] holding its high bit at bit j%8 of signs[j/8]): elements 8t..8t+7, i.e.
+// the 16-bit word qs[2t..2t+1] (element 8t+k at bits 2k) and the byte signs[t] (at
+// bit k).  The sign byte's bits are spread by one lookup in the key half of the
+// table; each 3-bit index then selects a byte of the byte planes lo / hi of the eight
+// signed fp16 entries, so any eight-entry codebook decodes.  r gets the fp16x2 pairs
+// (e0,e2), (e4,e6), (e1,e3), (e5,e7); returns the block's norm.
+template <bool FIXED>
+__device__ __forceinline__ float t3_block(const uint8_t *blk, int t, uint32_t lut_addr,
+                                          uint32_t laneword, const uint32_t (&lo)[2],
+                                          const uint32_t (&hi)[2], uint32_t (&r)[4]) {
+  const uint32_t q = *reinterpret_cast<const uint16_t *>(blk + 2 + 2 * t);
+  const uint32_t sw = lut_byte<FIXED, 0>(lut_addr, laneword, blk[10 + t]);
+  // nibble a of the low half: index of e_2a; of the high half: index of e_2a+1
+  const uint32_t x = ((q | (q << 14)) & 0x33333333u) | sw;
+  const uint32_t xo = x >> 16;
+  const uint32_t le = prmt(lo[0], lo[1], x), he = prmt(hi[0], hi[1], x);
+  const uint32_t lodd = prmt(lo[0], lo[1], xo), hodd = prmt(hi[0], hi[1], xo);
+  r[0] = prmt(le, he, 0x5140u);
+  r[1] = prmt(le, he, 0x7362u);
+  r[2] = prmt(lodd, hodd, 0x5140u);
+  r[3] = prmt(lodd, hodd, 0x7362u);
+  return __half2float(*reinterpret_cast<const __half *>(blk));
+}
+
+
 // Physical key (within a 16-key block) of score row r.  Rows g and g+8 belong to
 // lane group g.  With this order the packed-word loads of a warp hit every bank at
 // most twice, and the PV operand of lane (g, t) -- keys a_t, a_t+2, a_t+4, a_t+6
@@ -292,9 +331,16 @@ __device__ __forceinline__ void consumers_sync() { named_sync1<CWARPS * 32>(); }
 // 16g..16g+15 of the PV product.  KP of the 4 key words and VP of the 2 value words
 // per lane are decoded by byte permutes instead of the table, to balance the ALU and
 // shared-memory pipes.
-template <int NG, bool SCORES, int KP, int VP, bool FIXED>
+//
+// K3: turbo3 keys (56-byte rows of four 32-element blocks, each with its own norm),
+// turbo4 values.  The score's k dimension is then ordered block by block: MMA slices
+// 2b and 2b+1 cover block b, lane t holding its elements 8t..8t+7 (the q operand is
+// permuted to match once per item), and each block's product is scaled by that
+// block's norm as it is added to the score.
+template <int NG, bool SCORES, int KP, int VP, bool FIXED, bool K3>
 __global__ void __maxnreg__(128)
     k_partial_t4(const PartialParams p) {
+  constexpr int KROW = K3 ? T3_ROW : T4_ROW;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   SmemHead &sm = *reinterpret_cast<SmemHead *>(smem_raw);
   uint32_t *lut = reinterpret_cast<uint32_t *>(smem_raw + LUT_OFF);
@@ -320,7 +366,8 @@ __global__ void __maxnreg__(128)
     const uint32_t *c16 = (chunk & 4) ? p.vc16 : p.kc16;
     const uint32_t lo = (c16[(byte & 15) >> 1] >> (16 * (byte & 1))) & 0xFFFFu;
     const uint32_t hi = (c16[(byte >> 4) >> 1] >> (16 * ((byte >> 4) & 1))) & 0xFFFFu;
-    const uint32_t e = lo | (hi << 16);
+    // turbo3 keys: the key slots hold the spread sign bits instead
+    const uint32_t e = (K3 && chunk < 4) ? t3_sign_word(byte) : lo | (hi << 16);
     uint4 *dst = reinterpret_cast<uint4 *>(lut + byte * 64 + chunk * 8);
     dst[0] = make_uint4(e, e, e, e);
     dst[1] = make_uint4(e, e, e, e);
@@ -359,13 +406,13 @@ __global__ void __maxnreg__(128)
             ok = false;
             break;
           }
-          const size_t start = (unit_row0 + kf) * T4_ROW;
-          const size_t a0 = start & ~(size_t)15;
-          const size_t a1 = (start + (size_t)nk * T4_ROW + 15) & ~(size_t)15;
-          const uint32_t bytes = (uint32_t)(a1 - a0);
-          mbar_arrive_expect_tx(&sm.full[s], 2 * bytes);
-          bulk_g2s(stage_buf(smem_raw, s), p.kc + a0, bytes, &sm.full[s]);
-          bulk_g2s(stage_buf(smem_raw, 4 + s), p.vc + a0, bytes, &sm.full[s]);
+          const size_t ks = (unit_row0 + kf) * KROW, vs = (unit_row0 + kf) * T4_ROW;
+          const size_t k0 = ks & ~(size_t)15, v0 = vs & ~(size_t)15;
+          const uint32_t kbytes = (uint32_t)(((ks + (size_t)nk * KROW + 15) & ~(size_t)15) - k0);
+          const uint32_t vbytes = (uint32_t)(((vs + (size_t)nk * T4_ROW + 15) & ~(size_t)15) - v0);
+          mbar_arrive_expect_tx(&sm.full[s], kbytes + vbytes);
+          bulk_g2s(stage_buf(smem_raw, s), p.kc + k0, kbytes, &sm.full[s]);
+          bulk_g2s(stage_buf(smem_raw, 4 + s), p.vc + v0, vbytes, &sm.full[s]);
           ++ctr;
         }
       }
@@ -409,7 +456,19 @@ __global__ void __maxnreg__(128)
 #pragma unroll
     for (int c = 0; c < NG; ++c) {
       const int slot = c * 4 + hs;
-      if (slot < G) {
+      if (slot < G && K3) {
+        // slice 2b + h, lane t: dims 32b + 8t + 4h + {0, 2} and {1, 3}
+        const uint32_t *qw = p.qhl + (size_t)(b * p.Hq + head0 + slot) * 256 + (g & 1) * 64 + 4 * t;
+#pragma unroll
+        for (int bl = 0; bl < 4; ++bl) {
+          const uint32_t w0 = qw[16 * bl], w1 = qw[16 * bl + 1];
+          const uint32_t w2 = qw[16 * bl + 2], w3 = qw[16 * bl + 3];
+          qb[c][2 * bl][0] = prmt(w0, w1, 0x5410u);
+          qb[c][2 * bl][1] = prmt(w0, w1, 0x7632u);
+          qb[c][2 * bl + 1][0] = prmt(w2, w3, 0x5410u);
+          qb[c][2 * bl + 1][1] = prmt(w2, w3, 0x7632u);
+        }
+      } else if (slot < G) {
         const uint32_t *qw = p.qhl + (size_t)(b * p.Hq + head0 + slot) * 256 + (g & 1) * 64 + 16 * t;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
@@ -446,9 +505,9 @@ __global__ void __maxnreg__(128)
         break;
       }
       const int nk = min(TILE, Lb - kf);
-      const size_t start = (unit_row0 + kf) * T4_ROW;
-      const uint8_t *Ks = stage_buf(smem_raw, s) + (start & 15) + kb * T4_ROW;
-      const uint8_t *Vs = stage_buf(smem_raw, 4 + s) + (start & 15) + kb * T4_ROW;
+      const size_t ks = (unit_row0 + kf) * KROW, vs = (unit_row0 + kf) * T4_ROW;
+      const uint8_t *Ks = stage_buf(smem_raw, s) + (ks & 15) + kb * KROW;
+      const uint8_t *Vs = stage_buf(smem_raw, 4 + s) + (vs & 15) + kb * T4_ROW;
       const int nkb = nk - kb;  // valid keys of this warp's block (may be <= 0 or > 16)
       if (nkb > 0) {
         // ---- scores S^T[16 rows x 8 cols] = K_hat Q^T, two accumulator chains
@@ -457,10 +516,30 @@ __global__ void __maxnreg__(128)
         for (int c = 0; c < NG; ++c)
 #pragma unroll
           for (int e = 0; e < 4; ++e) sa[c][e] = sb[c][e] = 0.f;
-        const uint8_t *kr0 = Ks + rk0 * T4_ROW + 4 + 16 * t;
-        const uint8_t *kr1 = Ks + rk1 * T4_ROW + 4 + 16 * t;
+        if (K3) {
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
+          for (int bl = 0; bl < 4; ++bl) {
+            uint32_t d0[4], d1[4];
+            const float n0 = t3_block<FIXED>(Ks + rk0 * KROW + 14 * bl, t, lut_base, kword, klo, khi, d0);
+            const float n1 = t3_block<FIXED>(Ks + rk1 * KROW + 14 * bl, t, lut_base, kword, klo, khi, d1);
+            const uint32_t a0[4] = {d0[0], d1[0], d0[2], d1[2]};
+            const uint32_t a1[4] = {d0[1], d1[1], d0[3], d1[3]};
+#pragma unroll
+            for (int c = 0; c < NG; ++c) {
+              float acc[4] = {0.f, 0.f, 0.f, 0.f};
+              mma_f16(acc, a0, qb[c][2 * bl][0], qb[c][2 * bl][1]);
+              mma_f16(acc, a1, qb[c][2 * bl + 1][0], qb[c][2 * bl + 1][1]);
+              sa[c][0] = fmaf(n0, acc[0], sa[c][0]);
+              sa[c][1] = fmaf(n0, acc[1], sa[c][1]);
+              sa[c][2] = fmaf(n1, acc[2], sa[c][2]);
+              sa[c][3] = fmaf(n1, acc[3], sa[c][3]);
+            }
+          }
+        }
+        const uint8_t *kr0 = Ks + rk0 * KROW + 4 + 16 * t;
+        const uint8_t *kr1 = Ks + rk1 * KROW + 4 + 16 * t;
+#pragma unroll
+        for (int w = 0; w < (K3 ? 0 : 4); ++w) {
           uint32_t d0[4], d1[4];
           const uint32_t x0 = ld_u32(kr0 + 4 * w), x1 = ld_u32(kr1 + 4 * w);
           if (w < KP) {
@@ -479,8 +558,9 @@ __global__ void __maxnreg__(128)
           }
         }
         // ---- online softmax over the two keys of this lane, head t of each group
-        const float nk0 = *reinterpret_cast<const float *>(Ks + rk0 * T4_ROW);
-        const float nk1 = *reinterpret_cast<const float *>(Ks + rk1 * T4_ROW);
+        // turbo3 keys carry their block norms in sa already
+        const float nk0 = K3 ? 1.f : *reinterpret_cast<const float *>(Ks + rk0 * KROW);
+        const float nk1 = K3 ? 1.f : *reinterpret_cast<const float *>(Ks + rk1 * KROW);
         const float nv0 = *reinterpret_cast<const float *>(Vs + rk0 * T4_ROW);
         const float nv1 = *reinterpret_cast<const float *>(Vs + rk1 * T4_ROW);
         const bool ok0 = rk0 < nkb, ok1 = rk1 < nkb;
@@ -489,8 +569,10 @@ __global__ void __maxnreg__(128)
         uint32_t pb[NG][2];
 #pragma unroll
         for (int c = 0; c < NG; ++c) {
-          const float s0 = ok0 ? ((sa[c][0] + sa[c][1]) + (sb[c][0] + sb[c][1])) * (nk0 * qs[c]) : -INFINITY;
-          const float s1 = ok1 ? ((sa[c][2] + sa[c][3]) + (sb[c][2] + sb[c][3])) * (nk1 * qs[c]) : -INFINITY;
+          const float d0 = K3 ? sa[c][0] + sa[c][1] : (sa[c][0] + sa[c][1]) + (sb[c][0] + sb[c][1]);
+          const float d1 = K3 ? sa[c][2] + sa[c][3] : (sa[c][2] + sa[c][3]) + (sb[c][2] + sb[c][3]);
+          const float s0 = ok0 ? d0 * (nk0 * qs[c]) : -INFINITY;
+          const float s1 = ok1 ? d1 * (nk1 * qs[c]) : -INFINITY;
           if (SCORES && c * 4 + t < G) {
             float *srow = p.scores + (size_t)(b * p.Hq + head0 + c * 4 + t) * p.L + kf + kb;
             if (ok0) srow[rk0] = s0 * LN2;
@@ -772,10 +854,10 @@ cudaError_t launch_prepare_q(const tq_ctx *k, const void *q, int q_dtype, const 
   return launch_pdl(kern, dim3(grid), dim3(QWARPS * 32), smem, st, p);
 }
 
-template <int NG, bool SC, int KP, int VP, bool FIXED>
+template <int NG, bool SC, int KP, int VP, bool FIXED, bool K3>
 cudaError_t launch_t4(const PartialParams &p, dim3 grid, cudaStream_t st) {
   const size_t smem = SMEM_BYTES;
-  auto kern = k_partial_t4<NG, SC, KP, VP, FIXED>;
+  auto kern = k_partial_t4<NG, SC, KP, VP, FIXED, K3>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -789,6 +871,24 @@ cudaError_t launch_t4(const PartialParams &p, dim3 grid, cudaStream_t st) {
 constexpr int K_PRMT_WORDS = 0;
 constexpr int V_PRMT_WORDS = 0;
 
+template <bool K3>
+cudaError_t launch_t4_variant(const PartialParams &p, int heads_per_cta, bool fixed, bool scores,
+                              dim3 grid, cudaStream_t st) {
+  constexpr int KP = K3 ? 0 : K_PRMT_WORDS;
+  if (heads_per_cta == 8) {
+    if (fixed)
+      return scores ? launch_t4<2, true, KP, V_PRMT_WORDS, true, K3>(p, grid, st)
+                    : launch_t4<2, false, KP, V_PRMT_WORDS, true, K3>(p, grid, st);
+    return scores ? launch_t4<2, true, KP, V_PRMT_WORDS, false, K3>(p, grid, st)
+                  : launch_t4<2, false, KP, V_PRMT_WORDS, false, K3>(p, grid, st);
+  }
+  if (fixed)
+    return scores ? launch_t4<1, true, KP, V_PRMT_WORDS, true, K3>(p, grid, st)
+                  : launch_t4<1, false, KP, V_PRMT_WORDS, true, K3>(p, grid, st);
+  return scores ? launch_t4<1, true, KP, V_PRMT_WORDS, false, K3>(p, grid, st)
+                : launch_t4<1, false, KP, V_PRMT_WORDS, false, K3>(p, grid, st);
+}
+
 cudaError_t launch_partial(const tq_ctx *k, const tq_ctx *v, const uint8_t *kc,
                            const uint8_t *vc, const int32_t *seq_lens, const DecodeShape &s,
                            float *scores_dbg, const Workspace &ws, cudaStream_t st,
@@ -801,26 +901,26 @@ cudaError_t launch_partial(const tq_ctx *k, const tq_ctx *v, const uint8_t *kc,
   p.tiles_per_unit = s.tiles_per_unit, p.tiles_per_cta = s.tiles_per_cta;
   p.total_tiles = s.total_tiles, p.n_part = s.n_part;
   p.qhl = ws.qhl, p.qsc = ws.qsc, p.part = ws.partials, p.scores = scores_dbg;
+  const bool k3 = k->fmt == TQ_FMT_TURBO3;
   for (int i = 0; i < 2; ++i) {
     p.klo[i] = k->f16.lo[i], p.khi[i] = k->f16.hi[i];
     p.vlo[i] = v->f16.lo[i], p.vhi[i] = v->f16.hi[i];
   }
+  if (k3) {
+    // byte planes of the eight signed fp16 key entries, index order
+    p.klo[0] = p.klo[1] = p.khi[0] = p.khi[1] = 0u;
+    for (int e = 0; e < 8; ++e) {
+      const uint32_t bits = (k->f16.c16[e / 2] >> (16 * (e % 2))) & 0xFFFFu;
+      p.klo[e / 4] |= (bits & 0xFFu) << (8 * (e % 4));
+      p.khi[e / 4] |= (bits >> 8) << (8 * (e % 4));
+    }
+  }
   for (int i = 0; i < 8; ++i) p.kc16[i] = k->f16.c16[i], p.vc16[i] = v->f16.c16[i];
   p.status = k->d_status;
-  dim3 grid(s.grid);
   const bool fixed = k->reserved_smem == (int)RESERVED_SMEM;
-  if (s.heads_per_cta == 8) {
-    if (fixed)
-      return scores_dbg ? launch_t4<2, true, K_PRMT_WORDS, V_PRMT_WORDS, true>(p, grid, st)
-                        : launch_t4<2, false, K_PRMT_WORDS, V_PRMT_WORDS, true>(p, grid, st);
-    return scores_dbg ? launch_t4<2, true, K_PRMT_WORDS, V_PRMT_WORDS, false>(p, grid, st)
-                      : launch_t4<2, false, K_PRMT_WORDS, V_PRMT_WORDS, false>(p, grid, st);
-  }
-  if (fixed)
-    return scores_dbg ? launch_t4<1, true, K_PRMT_WORDS, V_PRMT_WORDS, true>(p, grid, st)
-                      : launch_t4<1, false, K_PRMT_WORDS, V_PRMT_WORDS, true>(p, grid, st);
-  return scores_dbg ? launch_t4<1, true, K_PRMT_WORDS, V_PRMT_WORDS, false>(p, grid, st)
-                    : launch_t4<1, false, K_PRMT_WORDS, V_PRMT_WORDS, false>(p, grid, st);
+  const bool sc = scores_dbg != nullptr;
+  return k3 ? launch_t4_variant<true>(p, s.heads_per_cta, fixed, sc, dim3(s.grid), st)
+            : launch_t4_variant<false>(p, s.heads_per_cta, fixed, sc, dim3(s.grid), st);
 }
 
 cudaError_t launch_combine(const tq_ctx *k, const tq_ctx *v, const DecodeShape &s, float *out,

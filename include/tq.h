@@ -186,7 +186,9 @@ tq_status tq_dequantize(const tq_ctx *ctx, const void *cache, int64_t n_rows, in
  * from its indices, online softmax runs split-K across SMs, values are
  * dequantized in registers, and the output is un-rotated once per head.
  *   k_ctx / v_ctx  contexts of the key and value caches.  Supported pairs:
- *                  (TURBO4, TURBO4) and (PROD3, VGROUP2).
+ *                  (TURBO4, TURBO4), (TURBO3, TURBO4) -- the asymmetric 3-bit-key /
+ *                  4-bit-value cache of [turbo4 post-mortem] section 9, each 32-element
+ *                  key block scaled by its own stored norm -- and (PROD3, VGROUP2).
  *   q              device [B][Hq][128] of q_dtype (F32, BF16 or F16), 16-byte aligned.
  *   k_cache/v_cache device [B][Hkv][L] packed rows.
  *   seq_lens       device int32[B] lengths in [1, L], or NULL for all L.

@@ -17,6 +17,8 @@ Workloads (shapes and distributions of the pages' decode and write workloads):
   seed 3.
 * ``write_chunk``: 16384 tokens x 8 KV heads x 128, bf16 N(0,1) K and V; seed 4.
 * ``long_context``: B=1, Hq=32, Hkv=8, L=131072; bf16 q, K, V N(0,1); seed 5.
+* ``gqa_t3k``: the ``gqa_lognormal`` recipe and seed unchanged (the same draws),
+  for the asymmetric cache with 3-bit keys and 4-bit values.
 
 bf16 values are produced by rounding fp32 draws to nearest-even bf16; they are
 returned both as uint16 bit patterns and as the exactly equal fp32 values.
@@ -32,6 +34,8 @@ WORKLOADS = {
     "prod_vgroup": dict(B=4, Hq=24, Hkv=4, L=30000, q_dtype="bf16", kv_dtype="bf16", dist="normal", seed=3),
     "write_chunk": dict(N=16384, Hkv=8, kv_dtype="bf16", dist="normal", seed=4),
     "long_context": dict(B=1, Hq=32, Hkv=8, L=131072, q_dtype="bf16", kv_dtype="bf16", dist="normal", seed=5),
+    # the gqa_lognormal recipe again, for the asymmetric 3-bit-key / 4-bit-value cache
+    "gqa_t3k": dict(B=8, Hq=32, Hkv=8, L=32768, q_dtype="bf16", kv_dtype="bf16", dist="lognormal_outlier", seed=2),
 }
 
 D = 128

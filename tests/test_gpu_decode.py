@@ -92,6 +92,54 @@ def test_decode_turbo4_parity(rot, case):
     assert tq.tq_ctx_device_status(kctx) == 0
 
 
+@pytest.mark.parametrize("rot", ["wht", "dense"])
+@pytest.mark.parametrize("case", CASES)
+def test_decode_turbo3_keys_turbo4_values_parity(rot, case):
+    """The asymmetric cache: 3-bit (2+1 layout) keys, 4-bit values."""
+    tq = lib()
+    B, Hq, Hkv, L, lens = case
+    kcodec = Codec("turbo3", rotation=rot, rot_seed=13)
+    vcodec = Codec("turbo4", rotation=rot, rot_seed=14)
+    kb = oracle_cache(kcodec, B, Hkv, L, 11, scale=2.0, dist="lognormal")
+    vb = oracle_cache(vcodec, B, Hkv, L, 12)
+    q_t, q32 = torch_rows(np.random.default_rng(13).standard_normal((B, Hq, 128)).astype(np.float32), "bf16")
+    kctx, vctx = tq.Ctx("turbo3", rot, 13), tq.Ctx("turbo4", rot, 14)
+    out, sc = run_decode(tq, kctx, vctx, q_t, upload_cache(tq, "turbo3", kb), upload_cache(tq, "turbo4", vb),
+                         B, Hq, Hkv, L, lens)
+    ref, s_ref = reference(q32, kcodec, kb, vcodec, vb, lens)
+    check_outputs(out, ref)
+    m = ~np.isnan(s_ref)
+    assert np.array_equal(m, ~np.isnan(sc)), "scores written for the wrong keys"
+    assert np.max(np.abs(sc[m] - s_ref[m])) <= ATOL
+    assert tq.tq_ctx_device_status(kctx) == 0
+
+
+def test_decode_turbo3_keys_own_block_norms():
+    """Every 32-element key block is scaled by its own stored norm: blocks whose norms
+    differ (set here to other fp16 values, including zero) decode as the oracle's
+    per-block dequantization says.  Staged calls, f32 queries, 8 q-heads per KV head."""
+    tq = lib()
+    B, Hq, Hkv, L = 2, 16, 2, 531
+    kcodec = Codec("turbo3", rotation="wht", rot_seed=21)
+    vcodec = Codec("turbo4", rotation="wht", rot_seed=22)
+    kb = oracle_cache(kcodec, B, Hkv, L, 21).copy()
+    vb = oracle_cache(vcodec, B, Hkv, L, 22)
+    rng = np.random.default_rng(23)
+    for c in range(4):
+        n = kb[..., 14 * c:14 * c + 2].copy().view("<f2").astype(np.float32)
+        f = rng.uniform(0.25, 4.0, size=n.shape).astype(np.float32)
+        f[rng.random(n.shape) < 0.02] = 0.0
+        kb[..., 14 * c:14 * c + 2] = (n * f).astype("<f2").view(np.uint8)
+    q_t, q32 = torch_rows(rng.standard_normal((B, Hq, 128)).astype(np.float32) * 1.5, "f32")
+    kctx, vctx = tq.Ctx("turbo3", "wht", 21), tq.Ctx("turbo4", "wht", 22)
+    out, sc = run_decode(tq, kctx, vctx, q_t, upload_cache(tq, "turbo3", kb), upload_cache(tq, "turbo4", vb),
+                         B, Hq, Hkv, L, staged=True)
+    ref, s_ref = reference(q32, kcodec, kb, vcodec, vb, None)
+    check_outputs(out, ref)
+    assert np.max(np.abs(sc - s_ref)) <= ATOL
+    assert tq.tq_ctx_device_status(kctx) == 0
+
+
 @pytest.mark.parametrize("q_dtype", ["f32", "bf16", "f16"])
 def test_decode_q_dtypes_and_staged_calls(q_dtype):
     tq = lib()
@@ -195,20 +243,21 @@ def test_decode_rejects_bad_arguments():
         tq.tq_decode_workspace_size(ctx, ctx, 1, 5, 2, 64)  # Hq not a multiple of Hkv
     assert e.value.status == tq.TQ_ERR_INVALID_ARG
     t3 = tq.Ctx("turbo3", "wht", 0)
-    with pytest.raises(tq.TQError) as e:
-        tq.tq_decode_workspace_size(t3, t3, 1, 4, 1, 64)
-    assert e.value.status == tq.TQ_ERR_UNSUPPORTED
+    for kc_, vc_ in ((t3, t3), (ctx, t3)):  # turbo3 values have no decode kernel
+        with pytest.raises(tq.TQError) as e:
+            tq.tq_decode_workspace_size(kc_, vc_, 1, 4, 1, 64)
+        assert e.value.status == tq.TQ_ERR_UNSUPPORTED
 
 
-def _full_size(name, rot, rot_seed, sample_heads):
+def _full_size(name, rot, rot_seed, sample_heads, k_fmt="turbo4"):
     """Write the whole cache with the GPU write path, decode in the benchmark's launch
     configuration, and compare sampled (b, h) outputs with the oracle on that head's inputs."""
     import torch
     tq = lib()
     cfg = synth.WORKLOADS[name]
     B, Hq, Hkv, L = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["L"]
-    kctx, vctx = tq.Ctx("turbo4", rot, rot_seed), tq.Ctx("turbo4", rot, rot_seed + 100)
-    kc, vc = tq.alloc_cache("turbo4", B * Hkv * L), tq.alloc_cache("turbo4", B * Hkv * L)
+    kctx, vctx = tq.Ctx(k_fmt, rot, rot_seed), tq.Ctx("turbo4", rot, rot_seed + 100)
+    kc, vc = tq.alloc_cache(k_fmt, B * Hkv * L), tq.alloc_cache("turbo4", B * Hkv * L)
     for tensor, ctx, cache in (("K", kctx, kc), ("V", vctx, vc)):
         for b in range(B):
             for h in range(Hkv):
@@ -220,7 +269,7 @@ def _full_size(name, rot, rot_seed, sample_heads):
     q_t = torch.from_numpy(qbits.view(np.int16)).view(torch.bfloat16).cuda()
     out, _ = run_decode(tq, kctx, vctx, q_t, kc, vc, B, Hq, Hkv, L, scores=False)
     assert tq.tq_ctx_device_status(kctx) == 0
-    kcod = Codec("turbo4", rotation=rot, rot_seed=rot_seed)
+    kcod = Codec(k_fmt, rotation=rot, rot_seed=rot_seed)
     vcod = Codec("turbo4", rotation=rot, rot_seed=rot_seed + 100)
     for (b, h) in sample_heads:
         kv = oracle.gqa_kv_head(h, Hq, Hkv)
@@ -238,6 +287,10 @@ def test_full_size_gqa_lognormal_dense():
 
 def test_full_size_long_context_wht():
     _full_size("long_context", "wht", 5, [(0, 0), (0, 17), (0, 31)])
+
+
+def test_full_size_gqa_turbo3_keys():
+    _full_size("gqa_t3k", "dense", 6, [(0, 0), (4, 21), (7, 31)], k_fmt="turbo3")
 
 
 def test_decode_one_unit_many_splits():
