@@ -68,6 +68,19 @@ __device__ __forceinline__ void load4(const void *src, int64_t row, int64_t stri
   }
 }
 
+// x / n rounded to nearest, given r = RN(1/n): q = RN(x r) is within one ulp of x / n,
+// the residual x - q n is exact under a fused multiply-add, and one correction
+// q + (x - q n) r rounded to nearest is RN(x / n) (Markstein's theorem for binary
+// floating point with a correctly rounded reciprocal).  The theorem needs the
+// residual and the quotient away from the subnormal range and 1/n normal; other
+// operands (zeros included) take the IEEE division.
+__device__ __forceinline__ float div_rn(float x, float n, float r) {
+  const float q = __fmul_rn(x, r);
+  if (fabsf(x) >= 0x1p-100f && fabsf(q) >= 0x1p-124f && n <= 0x1p125f)
+    return __fmaf_rn(__fmaf_rn(-q, n, x), r, q);
+  return __fdiv_rn(x, n);
+}
+
 // Canonical fp32 norm and u = x / n (u = 0 when n == 0).
 __device__ __forceinline__ float norm_normalize(float (&x)[4]) {
   float p = __fadd_rn(__fadd_rn(__fmul_rn(x[0], x[0]), __fmul_rn(x[1], x[1])),
@@ -75,8 +88,9 @@ __device__ __forceinline__ float norm_normalize(float (&x)[4]) {
 #pragma unroll
   for (int h = 16; h >= 1; h >>= 1) p = __fadd_rn(p, __shfl_xor_sync(FULL_MASK, p, h));
   const float n = __fsqrt_rn(p);
+  const float r = __frcp_rn(n);
 #pragma unroll
-  for (int e = 0; e < 4; ++e) x[e] = (n == 0.0f) ? 0.0f : __fdiv_rn(x[e], n);
+  for (int e = 0; e < 4; ++e) x[e] = (n == 0.0f) ? 0.0f : div_rn(x[e], n, r);
   return n;
 }
 
@@ -90,13 +104,15 @@ __device__ __forceinline__ void wht_rotate(float (&v)[4], const uint32_t (&neg)[
   float a2 = __fadd_rn(v[2], v[3]), a3 = __fsub_rn(v[2], v[3]);
   v[0] = __fadd_rn(a0, a2), v[2] = __fsub_rn(a0, a2);
   v[1] = __fadd_rn(a1, a3), v[3] = __fsub_rn(a1, a3);
+  // across lanes: the lower partner keeps v + o, the upper one o - v, both as one
+  // fused o + (+-1) v (the product by +-1 is exact, so the rounding is the same)
 #pragma unroll
   for (int m = 1; m <= 16; m <<= 1) {
-    const bool high = (lane & m) != 0;
+    const float sgn = (lane & m) ? -1.0f : 1.0f;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const float o = __shfl_xor_sync(FULL_MASK, v[e], m);
-      v[e] = high ? __fsub_rn(o, v[e]) : __fadd_rn(v[e], o);
+      v[e] = __fmaf_rn(sgn, v[e], o);
     }
   }
   const float inv_sqrt_d = __int_as_float(0x3DB504F3);  // fp32 nearest 1/sqrt(128)
@@ -434,14 +450,20 @@ __global__ void __launch_bounds__(WARPS * 32) k_write_vgroup(const WriteParams p
 template <typename K>
 cudaError_t launch_rows(K kernel, const WriteParams &p, int64_t n_rows, int num_sms, size_t smem,
                         int blocks_per_sm, cudaStream_t st) {
-  int64_t want = (n_rows + WARPS - 1) / WARPS;
-  int64_t cap = (int64_t)num_sms * blocks_per_sm;
-  const int grid = (int)(want < cap ? want : cap);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
   }
+  // One wave of resident CTAs (the kernels loop over rows): never more CTAs per SM than
+  // fit at once, so no second, partial wave.
+  int resident = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, kernel, WARPS * 32, smem);
+  if (e != cudaSuccess) return e;
+  if (resident >= 1 && resident < blocks_per_sm) blocks_per_sm = resident;
+  int64_t want = (n_rows + WARPS - 1) / WARPS;
+  int64_t cap = (int64_t)num_sms * blocks_per_sm;
+  const int grid = (int)(want < cap ? want : cap);
   return launch_pdl(kernel, dim3(grid), dim3(WARPS * 32), smem, st, p);
 }
 
