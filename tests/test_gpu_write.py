@@ -77,6 +77,55 @@ def test_write_dense_band(fmt, n):
     assert ok, f"{ndiff} indices differ outside the boundary band"
 
 
+def extreme_rows():
+    """Rows at the edges of the fp32 range: squares that underflow, elements whose
+    quotient by the norm is tiny or subnormal, a norm that overflows."""
+    g = np.random.default_rng(79).standard_normal((7, 128)).astype(np.float32)
+    x = np.empty_like(g)
+    x[0] = g[0] * 1e-19                         # squares partly subnormal, normal norm
+    x[1] = g[1] * 1e-31                         # elements below 2^-100 ...
+    x[1, 0] = 1e-18                             # ... beside one that sets the norm
+    x[2] = g[2] * 1e-20                         # quotients subnormal ...
+    x[2, 9] = 1e19                              # ... under a huge element
+    x[3] = g[3] * 1e-25                         # every square underflows: norm 0
+    x[4] = g[4] * 1e-41                         # subnormal elements
+    x[5] = g[5] * 3e18                          # the sum of squares overflows: norm inf
+    x[6] = g[6] * 1e-12
+    x[6, ::7] = 0.0                             # exact zeros among normal elements
+    return x
+
+
+@pytest.mark.parametrize("fmt", ["turbo4", "turbo3"])
+@pytest.mark.parametrize("rot,n", [("wht", 1000), ("dense", 100), ("dense", 1000), ("dense", 2500)])
+def test_write_extreme_magnitudes(fmt, rot, n):
+    """Extreme rows spread through a block of ordinary rows (n rows in all, so each dense
+    kernel -- one CTA per row, staged matrices, tensor cores -- meets them): WHT rows
+    bit-exact, dense rows norm-exact with indices in the boundary band."""
+    tq = lib()
+    x = (np.random.default_rng(80 + n).standard_normal((n, 128)) * 2.0).astype(np.float32)
+    ext = extreme_rows()
+    at = np.linspace(0, n - 1, len(ext)).astype(int)
+    x[at] = ext
+    x_t, x32 = torch_rows(x, "bf16")
+    codec = Codec(fmt, rotation=rot, rot_seed=4)
+    ref, aux = codec.encode(x32)
+    ctx = tq.Ctx(fmt, rot, 4)
+    got = to_host_bytes(write_gpu(tq, ctx, x_t, n), n, ctx.row_bytes)
+    assert tq.tq_ctx_device_status(ctx) == 0
+    if rot == "wht":
+        bad = rows_equal_nan_aware(got, ref, fmt)
+        assert bad.size == 0, f"{bad.size} rows differ, first {bad[:5]}"
+        return
+    if fmt == "turbo4":
+        idx = unpack_turbo4(got)[1]
+        assert np.array_equal(got[:, :4], ref[:, :4])
+    else:
+        norms, idx = unpack_turbo3(got)
+        assert np.array_equal(norms, unpack_turbo3(ref)[0])
+    ok, ndiff = band_ok(idx, aux["idx"], aux["y"], codec.b32)
+    assert ok, f"{ndiff} indices differ outside the boundary band (rows {at})"
+
+
 @pytest.mark.parametrize("n", [100, 3000])
 def test_write_prod3_band(n):
     tq = lib()
