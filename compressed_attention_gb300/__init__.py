@@ -71,6 +71,9 @@ _SIGNATURES = {
     "tq_decode_attention_static": (_i32, [_vp, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _f32,
                                           _vp, _vp]),
     "tq_test_decode_wait_timeout": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _sz, _vp]),
+    "tq_prefill_workspace_size": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(_sz)]),
+    "tq_prefill_attention": (_i32, [_vp, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
+                                    _f32, _vp, _vp, _sz, _vp]),
 }
 
 
@@ -238,6 +241,24 @@ def tq_decode_attention(k_ctx, v_ctx, q, k_cache, v_cache, out, workspace, B, Hq
                                    _ptr(seq_lens), B, Hq, Hkv, L, scale, _ptr(out), _ptr(scores),
                                    _ptr(workspace), workspace.numel() * workspace.element_size(),
                                    _stream(stream)), "tq_decode_attention")
+
+
+def tq_prefill_workspace_size(k_ctx, v_ctx, B, T, Hq, Hkv, L):
+    n = _sz(0)
+    _check(lib.tq_prefill_workspace_size(k_ctx.handle, v_ctx.handle, B, T, Hq, Hkv, L, ctypes.byref(n)),
+           "tq_prefill_workspace_size")
+    return n.value
+
+
+def tq_prefill_attention(k_ctx, v_ctx, q, k_cache, v_cache, q_start, out, workspace, B, T, Hq, Hkv, L,
+                         scale=0.0, stream=None):
+    """Causal attention of T chunk queries per sequence (q [B, T, Hq, 128], query i of
+    sequence b at position q_start[b] + i) over the packed caches."""
+    qp, qd = _q_args(q)
+    _check(lib.tq_prefill_attention(k_ctx.handle, v_ctx.handle, qp, qd, _ptr(k_cache), _ptr(v_cache),
+                                    _ptr(q_start), B, T, Hq, Hkv, L, scale, _ptr(out), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), _stream(stream)),
+           "tq_prefill_attention")
 
 
 TQ_STATIC_WORKSPACE_BYTES = 4 << 20  # capacity of the static scratch of tq_decode_attention_static

@@ -398,6 +398,60 @@ tq_status tq_decode_attention(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const vo
   return tq_decode_combine(k_ctx, v_ctx, B, Hq, Hkv, L, out, workspace, workspace_bytes, stream);
 }
 
+// ---------------------------------------------------------------- prefill
+namespace {
+tq_status check_prefill(const tq_ctx *k, const tq_ctx *v, int B, int T, int Hq, int Hkv, int L,
+                        PrefillShape *s) {
+  if (!k || !v) return fail(TQ_ERR_INVALID_ARG, "null context");
+  if (B < 1 || T < 1 || Hq < 1 || Hkv < 1 || L < 1) return fail(TQ_ERR_INVALID_ARG, "B, T, Hq, Hkv and L must be >= 1");
+  if (T > L) return fail(TQ_ERR_INVALID_ARG, "the chunk (T queries) must fit in the cache (L rows)");
+  if (Hq % Hkv != 0) return fail(TQ_ERR_INVALID_ARG, "Hq must be a multiple of Hkv");
+  if (k->fmt != TQ_FMT_TURBO4 || v->fmt != TQ_FMT_TURBO4)
+    return fail(TQ_ERR_UNSUPPORTED, "the prefill kernel takes turbo4 keys and values");
+  if (!prefill_shape(k, B, T, Hq, Hkv, L, s))
+    return fail(TQ_ERR_UNSUPPORTED, "prefill needs Hq / Hkv dividing 128 and a shape within 32-bit tile counts");
+  return TQ_OK;
+}
+}  // namespace
+
+tq_status tq_prefill_workspace_size(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, int T, int Hq,
+                                    int Hkv, int L, size_t *bytes) {
+  if (!bytes) return fail(TQ_ERR_INVALID_ARG, "null output");
+  PrefillShape s;
+  tq_status st = check_prefill(k_ctx, v_ctx, B, T, Hq, Hkv, L, &s);
+  if (st != TQ_OK) return st;
+  *bytes = carve_workspace(s.q, nullptr).bytes;
+  return TQ_OK;
+}
+
+tq_status tq_prefill_attention(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *q, int q_dtype,
+                               const void *k_cache, const void *v_cache, const int32_t *q_start,
+                               int B, int T, int Hq, int Hkv, int L, float scale, float *out,
+                               void *workspace, size_t workspace_bytes, tq_stream_t stream) {
+  PrefillShape s;
+  tq_status st = check_prefill(k_ctx, v_ctx, B, T, Hq, Hkv, L, &s);
+  if (st != TQ_OK) return st;
+  if (!q || !k_cache || !v_cache || !q_start || !out) return fail(TQ_ERR_INVALID_ARG, "null pointer");
+  if (q_dtype != TQ_DTYPE_F32 && q_dtype != TQ_DTYPE_BF16 && q_dtype != TQ_DTYPE_F16)
+    return fail(TQ_ERR_INVALID_ARG, "bad q dtype");
+  if (!aligned(q, 16)) return fail(TQ_ERR_ALIGNMENT, "q must be 16-byte aligned");
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return fail(TQ_ERR_ALIGNMENT, "caches must be 16-byte aligned");
+  if (!aligned(q_start, 4)) return fail(TQ_ERR_ALIGNMENT, "q_start must be 4-byte aligned");
+  if (!aligned(out, 4)) return fail(TQ_ERR_ALIGNMENT, "output must be 4-byte aligned");
+  if (!std::isfinite(scale)) return fail(TQ_ERR_INVALID_ARG, "scale must be finite");
+  if (scale == 0.f) scale = 1.0f / std::sqrt((float)D);
+  Workspace w;
+  if ((st = check_workspace(s.q, workspace, workspace_bytes, &w)) != TQ_OK) return st;
+  const cudaStream_t cs = (cudaStream_t)stream;
+  cudaError_t e = launch_prepare_q(k_ctx, q, q_dtype, s.q, scale, w, cs);
+  if (e != cudaSuccess) return cuda_fail(e, "prepare_q launch");
+  e = launch_prefill(k_ctx, v_ctx, (const uint8_t *)k_cache, (const uint8_t *)v_cache, q_start, s, w, cs);
+  if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  e = launch_combine_prefill(v_ctx, s, out, w, cs);
+  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  return TQ_OK;
+}
+
 tq_status tq_test_decode_wait_timeout(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *k_cache,
                                       const void *v_cache, int B, int Hq, int Hkv, int L, void *workspace,
                                       size_t workspace_bytes, tq_stream_t stream) {

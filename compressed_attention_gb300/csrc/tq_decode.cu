@@ -50,30 +50,6 @@ constexpr int T4_ROW = 68;
 constexpr int T3_ROW = 56;            // four 14-byte blocks of the 2+1 layout
 constexpr int STAGE_BUF = 16352;      // >= 240 * 68 + 2 * 15, multiple of 32
 
-// 8 packed 4-bit indices -> 8 fp16 centroid values as four fp16x2 words.
-// Magnitude index m = idx for idx < 8 (negative centroids), 15 - idx otherwise;
-// sign is negative when bit 3 of the index is clear.  SEL0 / SEL1 choose how the
-// looked-up bytes pair up: (0,1),(2,3) for dims of one key, (0,2),(1,3) for the
-// same dim of two keys after a byte interleave.
-template <uint32_t SEL0, uint32_t SEL1>
-__device__ __forceinline__ void decode8(uint32_t x, const uint32_t (&lo)[2],
-                                        const uint32_t (&hi)[2], uint32_t (&r)[4]) {
-  const uint32_t t = x & 0x88888888u;
-  const uint32_t m = (x ^ (t - (t >> 3))) & 0x77777777u;
-  const uint32_t x4 = x << 4;
-  const uint32_t pos_a = prmt(x, x4, 0x9D8Cu);  // 0xFF per byte where nibble 0..3 >= 8
-  const uint32_t pos_b = prmt(x, x4, 0xBFAEu);  // nibbles 4..7
-  const uint32_t mh = m >> 16;
-  const uint32_t lo_a = prmt(lo[0], lo[1], m);
-  const uint32_t lo_b = prmt(lo[0], lo[1], mh);
-  const uint32_t hi_a = prmt(hi[0], hi[1], m) | (~pos_a & 0x80808080u);
-  const uint32_t hi_b = prmt(hi[0], hi[1], mh) | (~pos_b & 0x80808080u);
-  r[0] = prmt(lo_a, hi_a, SEL0);
-  r[1] = prmt(lo_a, hi_a, SEL1);
-  r[2] = prmt(lo_b, hi_b, SEL0);
-  r[3] = prmt(lo_b, hi_b, SEL1);
-}
-
 struct QprepParams {
   const void *q;
   int q_dtype;
@@ -702,9 +678,10 @@ __global__ void __maxnreg__(128)
 
 struct CombineParams {
   const float *part;
-  int n_heads;      // B * Hq
+  int n_heads;      // B * Hq (decode) or B * T * Hq (prefill rows)
   int n_split;      // partial slots per head
   int Hq, gq, heads_per_cta, n_hg, tiles_per_unit, tiles_per_cta;
+  int pf_T, pf_Hkv, pf_qpt, pf_n_qt;  // prefill geometry (pf_T = 0: decode)
   const float *r;   // R (row-major) of the value rotation, or null
   float inv_vscale; // 1 / (2^P_SHIFT * alpha_V)
   float *out;
@@ -726,8 +703,14 @@ __global__ void __launch_bounds__(QWARPS * 32) k_combine(const CombineParams p) 
   if (live) {
     const float *part = p.part + (size_t)bh * p.n_split * PARTIAL_FLOATS;
     // slots written for this head: CTAs whose tile range meets its unit
-    const int b = bh / p.Hq, h = bh % p.Hq;
-    const int unit = (b * (p.Hq / p.gq) + h / p.gq) * p.n_hg + (h % p.gq) / p.heads_per_cta;
+    int unit;
+    if (p.pf_T) {  // row (b, i, h) of a prefill: unit (b, KV head, query tile)
+      const int h = bh % p.Hq, i = (bh / p.Hq) % p.pf_T, b = bh / (p.Hq * p.pf_T);
+      unit = (b * p.pf_Hkv + h / p.gq) * p.pf_n_qt + i / p.pf_qpt;
+    } else {
+      const int b = bh / p.Hq, h = bh % p.Hq;
+      unit = (b * (p.Hq / p.gq) + h / p.gq) * p.n_hg + (h % p.gq) / p.heads_per_cta;
+    }
     const int first = unit * p.tiles_per_unit;
     const int n_split = ((first + p.tiles_per_unit - 1) / p.tiles_per_cta) - first / p.tiles_per_cta + 1;
     float ms = -INFINITY;
@@ -935,6 +918,24 @@ cudaError_t launch_combine(const tq_ctx *k, const tq_ctx *v, const DecodeShape &
   const bool vgroup = v->fmt == TQ_FMT_VGROUP2;  // values are not rotated
   p.r = vgroup ? nullptr : v->d_pi;
   p.inv_vscale = 1.0f / (exp2f(P_SHIFT) * (vgroup ? 1.0f : v->f16.alpha));
+  p.out = out;
+  const size_t smem = (size_t)D * D * 4 + QWARPS * D * 4;
+  cudaError_t e = cudaFuncSetAttribute(k_combine, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(k_combine, dim3((p.n_heads + QWARPS - 1) / QWARPS), dim3(QWARPS * 32), smem, st, p);
+}
+
+cudaError_t launch_combine_prefill(const tq_ctx *v, const PrefillShape &s, float *out,
+                                   const Workspace &ws, cudaStream_t st) {
+  CombineParams p{};
+  p.part = ws.partials;
+  p.n_heads = s.B * s.T * s.Hq;
+  p.n_split = s.n_part;
+  p.Hq = s.Hq, p.gq = s.gq;
+  p.tiles_per_unit = s.tiles_per_unit, p.tiles_per_cta = s.tiles_per_cta;
+  p.pf_T = s.T, p.pf_Hkv = s.Hkv, p.pf_qpt = s.qpt, p.pf_n_qt = s.n_qt;
+  p.r = v->d_pi;
+  p.inv_vscale = 1.0f / (exp2f(P_SHIFT) * v->f16.alpha);
   p.out = out;
   const size_t smem = (size_t)D * D * 4 + QWARPS * D * 4;
   cudaError_t e = cudaFuncSetAttribute(k_combine, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

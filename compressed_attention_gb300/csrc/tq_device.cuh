@@ -16,6 +16,31 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return d;
 }
 
+// 8 packed 4-bit indices of a symmetric 16-entry codebook -> 8 fp16 centroid values as
+// four fp16x2 words; lo / hi are the byte planes of the eight magnitudes (F16Table).
+// Magnitude index m = idx for idx < 8 (negative centroids), 15 - idx otherwise;
+// sign is negative when bit 3 of the index is clear.  SEL0 / SEL1 choose how the
+// looked-up bytes pair up: (0,1),(2,3) for dims of one key, (0,2),(1,3) for the
+// same dim of two keys after a byte interleave.
+template <uint32_t SEL0, uint32_t SEL1>
+__device__ __forceinline__ void decode8(uint32_t x, const uint32_t (&lo)[2],
+                                        const uint32_t (&hi)[2], uint32_t (&r)[4]) {
+  const uint32_t t = x & 0x88888888u;
+  const uint32_t m = (x ^ (t - (t >> 3))) & 0x77777777u;
+  const uint32_t x4 = x << 4;
+  const uint32_t pos_a = prmt(x, x4, 0x9D8Cu);  // 0xFF per byte where nibble 0..3 >= 8
+  const uint32_t pos_b = prmt(x, x4, 0xBFAEu);  // nibbles 4..7
+  const uint32_t mh = m >> 16;
+  const uint32_t lo_a = prmt(lo[0], lo[1], m);
+  const uint32_t lo_b = prmt(lo[0], lo[1], mh);
+  const uint32_t hi_a = prmt(hi[0], hi[1], m) | (~pos_a & 0x80808080u);
+  const uint32_t hi_b = prmt(hi[0], hi[1], mh) | (~pos_b & 0x80808080u);
+  r[0] = prmt(lo_a, hi_a, SEL0);
+  r[1] = prmt(lo_a, hi_a, SEL1);
+  r[2] = prmt(lo_b, hi_b, SEL0);
+  r[3] = prmt(lo_b, hi_b, SEL1);
+}
+
 // D += A * B for one m16n8k16 tile, fp16 operands, fp32 accumulate.
 __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                         uint32_t b1) {

@@ -159,4 +159,24 @@ cudaError_t launch_partial_pv(const tq_ctx *k, const tq_ctx *v, const uint8_t *k
 cudaError_t launch_combine(const tq_ctx *k, const tq_ctx *v, const DecodeShape &s, float *out,
                            const Workspace &ws, cudaStream_t st);
 
+// Chunked prefill over the compressed cache: T queries per sequence at positions
+// q_start[b] .. q_start[b] + T - 1, units (batch, KV head, tile of qpt queries x gq heads).
+constexpr int PF_TILE = 128;  // keys per tile of the prefill
+struct PrefillShape {
+  int B, T, Hq, Hkv, L;
+  int gq;              // q-heads per KV head (a divisor of 128)
+  int qpt;             // queries per unit: 128 / gq rows
+  int n_qt;            // query tiles per (batch, KV head)
+  int tiles_per_unit;  // key tiles of one unit (all of L; tiles past a unit's last
+                       // visible key cost no work)
+  int total_tiles, tiles_per_cta, grid, n_part;
+  DecodeShape q;       // the B*T queries as a decode batch: q preparation and workspace
+};
+bool prefill_shape(const tq_ctx *k, int B, int T, int Hq, int Hkv, int L, PrefillShape *s);
+cudaError_t launch_prefill(const tq_ctx *k, const tq_ctx *v, const uint8_t *kc, const uint8_t *vc,
+                           const int32_t *q_start, const PrefillShape &s, const Workspace &ws,
+                           cudaStream_t st);
+cudaError_t launch_combine_prefill(const tq_ctx *v, const PrefillShape &s, float *out,
+                                   const Workspace &ws, cudaStream_t st);
+
 }  // namespace tq

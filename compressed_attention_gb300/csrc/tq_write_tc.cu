@@ -22,6 +22,7 @@
 
 #include "tq_device.cuh"
 #include "tq_internal.h"
+#include "tq_tc.cuh"
 
 namespace tq {
 
@@ -30,8 +31,9 @@ namespace {
 constexpr int TC_THREADS = 256;        // eight warps: warp w serves rows 32 (w % 4) .. + 31,
                                        // columns 64 (w / 4) .. + 63 of the tile
 constexpr int TC_ROWS = 128;           // rows per tile (the MMA's M)
-constexpr uint32_t HALF_BYTES = TC_ROWS * 128;  // one 64-column half of a bf16 tile
-constexpr uint32_t TILE_BYTES = 2 * HALF_BYTES; // 32 KB
+constexpr uint32_t HALF_BYTES = SW_HALF_BYTES;   // one 64-column half of a bf16 tile
+constexpr uint32_t TILE_BYTES = SW_TILE_BYTES;   // 32 KB
+static_assert(TC_ROWS == (int)SW_ROWS, "row tiles are the swizzled operand tiles");
 constexpr uint32_t TMEM_COLS = 128;
 constexpr uint64_t TC_WAIT_NS = 2000000000ull;
 
@@ -63,66 +65,6 @@ struct TcParams {
   int64_t dst_rows;
   int32_t *status;
 };
-
-// Offset of element (row, k) of a 128 x 128 bf16 tile in the 128-byte swizzled K-major
-// layout: two halves of 64 columns, rows of 128 bytes, 16-byte chunk c of row r stored
-// at chunk position c ^ (r % 8).
-__host__ __device__ constexpr uint32_t sw128_offset(uint32_t row, uint32_t k) {
-  return (k >> 6) * HALF_BYTES + row * 128 + ((((k & 63) >> 3) ^ (row & 7)) << 4) + (k & 7) * 2;
-}
-
-// tcgen05 shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
-// 1024 bytes apart (the leading offset is unused for this layout).
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
-  d |= (uint64_t)1 << 16;                    // leading byte offset (unused), 16 B
-  d |= (uint64_t)((1024u >> 4) & 0x3FFFu) << 32;  // stride byte offset: 1024 B
-  d |= (uint64_t)1 << 46;                    // descriptor version
-  d |= (uint64_t)2 << 61;                    // 128-byte swizzle
-  return d;
-}
-
-// Instruction descriptor: kind::f16 with bf16 A and B, fp32 D, both K-major, M = 128,
-// N = 128.
-constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
-
-__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols));
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols));
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(IDESC), "r"(accumulate));
-}
-__device__ __forceinline__ void umma_commit(uint64_t *bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
-               : "memory");
-}
-
-// 32 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint64_t *bar, int c0, int c1) {
   asm volatile(
@@ -170,7 +112,7 @@ __global__ void __launch_bounds__(TC_THREADS, 2) k_write_dense_tc(const __grid_c
       *reinterpret_cast<uint4 *>(smem + (m ? OFF_PIL : OFF_PIH) + sw128_offset(row, chunk * 8)) = v[k];
     }
   }
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> tensor-core reads
+  fence_async_smem();  // generic writes -> tensor-core reads
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -197,8 +139,8 @@ __global__ void __launch_bounds__(TC_THREADS, 2) k_write_dense_tc(const __grid_c
         const uint32_t sb = part ? spil : spih;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t koff = (ks >> 2) * HALF_BYTES + (ks & 3) * 32;
-          umma_bf16(tmem, sw128_desc(sx + koff), sw128_desc(sb + koff), (part | ks) ? 1u : 0u);
+          const uint32_t koff = sw128_kstep(ks);
+          umma<IDESC_BF16>(tmem, sw128_desc(sx + koff), sw128_desc(sb + koff), (part | ks) ? 1u : 0u);
         }
       }
       umma_commit(&ms.mma_done);

@@ -222,6 +222,35 @@ tq_status tq_decode_combine(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, int
                             int L, float *out, void *workspace, size_t workspace_bytes,
                             tq_stream_t stream);
 
+/* Chunked prefill attention over the compressed cache ([turbo4 post-mortem] §9,
+ * the prefill table: a prompt is processed in chunks that attend to the turbo4
+ * cache, which already holds the chunk's own rows -- write them with
+ * tq_quantize_set_rows first).  For batch b, chunk query i (0 <= i < T) and q-head
+ * h, with KV head kv = floor(h * Hkv / Hq) and position p = q_start[b] + i,
+ *   out[b,i,h] = sum_{t <= p} softmax_t(scale * <q[b,i,h], K_hat[b,kv,t]>) V_hat[b,kv,t]
+ * (causal: keys after the query's own position are not attended).  q is rotated
+ * once, scores and the PV product run as tensor-core products over fp16 operands
+ * decoded from the packed tiles, online softmax per row, split over the SMs, and
+ * the output is un-rotated once per row.
+ *   k_ctx / v_ctx  TURBO4 contexts (others: TQ_ERR_UNSUPPORTED).
+ *   q              device [B][T][Hq][128] of q_dtype (F32, BF16 or F16), 16-byte aligned.
+ *   k_cache/v_cache device [B][Hkv][L] packed rows, 16-byte aligned.
+ *   q_start        device int32[B]: position of query 0 of each sequence; must lie
+ *                  in [0, L - T] (outside: clamped and flagged, device status 2).
+ *   scale          softmax scale; 0 selects 1/sqrt(128).
+ *   out            device fp32 [B][T][Hq][128].
+ *   workspace      device scratch of tq_prefill_workspace_size() bytes, 256-byte
+ *                  aligned, no initialisation needed.
+ * Hq / Hkv must divide 128 (the rows of a tile are 128 / (Hq/Hkv) queries of all the
+ * KV head's q-heads); 1 <= T <= L.  The work is split evenly over all of L's key
+ * tiles, so pass the smallest L that covers the attended keys. */
+tq_status tq_prefill_workspace_size(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, int T, int Hq,
+                                    int Hkv, int L, size_t *bytes);
+tq_status tq_prefill_attention(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *q, int q_dtype,
+                               const void *k_cache, const void *v_cache, const int32_t *q_start,
+                               int B, int T, int Hq, int Hkv, int L, float scale, float *out,
+                               void *workspace, size_t workspace_bytes, tq_stream_t stream);
+
 /* Number of key splits the decode uses for this shape on the current device. */
 tq_status tq_decode_num_splits(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, int Hq,
                                int Hkv, int L, int *n_split);

@@ -84,6 +84,7 @@ from .formats import (  # noqa: F401
 from .attention import (  # noqa: F401
     gqa_kv_head,
     attention_reference,
+    prefill_reference,
     attention_compressed_domain,
     online_softmax_merge,
 )

@@ -60,6 +60,25 @@ def attention_reference(q, k_hat, v_hat, seq_lens=None, scale=None):
     return out, scores
 
 
+def prefill_reference(q, k_hat, v_hat, q_start, scale=None):
+    """Causal chunk attention, the prefill of [turbo4 post-mortem] section 9 (a prompt
+    processed in chunks against the cache that already holds the chunk's own rows).
+
+    q: [B, T, Hq, d]; k_hat, v_hat: [B, Hkv, L, d]; query i of sequence b sits at
+    position q_start[b] + i.  Reading: the usual causal mask, keys at positions up to
+    and including the query's own (the pages name the prefill but not its mask).  Each
+    query is the plain definition of ``attention_reference`` over keys
+    0 .. q_start[b] + i.  Returns out [B, T, Hq, d].
+    """
+    q = np.asarray(q, dtype=np.float64)
+    B, T, Hq, d = q.shape
+    out = np.zeros((B, T, Hq, d))
+    for i in range(T):
+        lens = [int(q_start[b]) + i + 1 for b in range(B)]
+        out[:, i], _ = attention_reference(q[:, i], k_hat, v_hat, lens, scale)
+    return out
+
+
 def online_softmax_merge(partials):
     """Merge (m, l, acc) partials of one head by log-sum-exp rescaling.
 

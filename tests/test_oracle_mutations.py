@@ -95,3 +95,30 @@ def test_wrong_gqa_mapping_is_caught():
     wrong = [h % 8 for h in range(32)]
     right = [oracle.gqa_kv_head(h, 32, 8) for h in range(32)]
     assert wrong != right and right[:4] == [0, 0, 0, 0]
+
+
+def test_prefill_mask_off_by_one_is_caught(monkeypatch):
+    """A causal mask that stops one key early (or lets one key too many through) breaks
+    the prefix-mean pin."""
+    import test_oracle_prefill as pins
+
+    def early(q, k_hat, v_hat, q_start, scale=None):
+        q = np.asarray(q, dtype=np.float64)
+        out = np.zeros(q.shape)
+        for i in range(q.shape[1]):
+            lens = [max(int(q_start[b]) + i, 1) for b in range(q.shape[0])]
+            out[:, i], _ = att.attention_reference(q[:, i], k_hat, v_hat, lens, scale)
+        return out
+
+    def late(q, k_hat, v_hat, q_start, scale=None):
+        q = np.asarray(q, dtype=np.float64)
+        out = np.zeros(q.shape)
+        for i in range(q.shape[1]):
+            lens = [int(q_start[b]) + i + 2 for b in range(q.shape[0])]
+            out[:, i], _ = att.attention_reference(q[:, i], k_hat, v_hat, lens, scale)
+        return out
+
+    for broken in (early, late):
+        monkeypatch.setattr(oracle, "prefill_reference", broken)
+        with pytest.raises(AssertionError):
+            pins.test_identical_keys_give_prefix_means()
