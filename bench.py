@@ -13,6 +13,8 @@ roofline.
 
 --workload picks another workload of the same path:
   gqa_t3k       the gqa_lognormal inputs with turbo3 keys and turbo4 values
+  prefill_chunk causal attention of the last 512-token chunk of a 32K-token prompt
+                (B=1, Hq=32, Hkv=8) over the turbo4 cache, tensor cores; TFLOP/s
   long_context  B=1, Hq=32, Hkv=8, L=131,072, turbo4 K and V, randomized WHT
   prod_vgroup   B=4, Hq=24, Hkv=4, L=30,000, prod3 keys (2-bit + QJL), vgroup2 values
   single_head   B=1, Hq=Hkv=1, L=512, fp32 q, turbo4 K and V, randomized WHT
@@ -45,6 +47,8 @@ import synth  # noqa: E402
 
 DECODE_METRIC = "fused compressed-KV decode attention: effective HBM GB/s (% of peak), keys/s"
 WRITE_METRIC = "quantize / SET_ROWS write path: effective HBM GB/s (% of peak), rows/s"
+PREFILL_METRIC = "chunked prefill attention over the compressed cache: effective TFLOP/s (% of tensor peak), tokens/s"
+FALLBACK_TENSOR_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS = 6800.0
 ROW_BYTES = {"turbo4": 68, "turbo3": 56, "prod3": 56, "vgroup2": 48}
@@ -65,6 +69,8 @@ DECODE = {
                     kernel="k_partial_t4", source="tq_decode.cu"),
 }
 WRITE_KERNEL = {"dense": ("k_write_dense_tc", "tq_write_tc.cu"), "wht": ("k_write_wht", "tq_write.cu")}
+PREFILL = {"prefill_chunk": dict(fmt="turbo4", rotation="dense", k_seed=7, v_seed=107,
+                                 kernel="k_prefill_t4", source="tq_prefill.cu")}
 
 
 def measured_peak():
@@ -73,6 +79,16 @@ def measured_peak():
         with open(path) as f:
             return float(json.load(f)["hbm_gbs"]), "measured"
     return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_tensor_peak():
+    """Dense 16-bit tensor-core peak (TFLOP/s) for a kernel timed alone: the burst cuBLAS
+    bf16 figure (fp16 products run at the same nominal rate)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    return FALLBACK_TENSOR_TFLOPS, "fallback"
 
 
 def profiled_traffic(profile_name, source):
@@ -247,10 +263,65 @@ def cpu_sample(oracle_leg, unit_bytes, what, min_seconds=10.0, max_units=64):
             "sample": f"{units} {what}, {elapsed:.1f} s"}
 
 
+def prefill_flops(cfg):
+    """Algorithmic FLOPs of the chunk's attention: 2 d per (row, visible key) for the
+    scores and 2 d for the PV product, rows = (b, query, q-head), query i seeing
+    L - T + i + 1 keys."""
+    T, L = cfg["T"], cfg["L"]
+    pairs = cfg["B"] * cfg["Hq"] * (T * (L - T) + T * (T + 1) // 2)
+    return 4 * 128 * pairs
+
+
+class OraclePrefill:
+    """The oracle's causal attention for a few chunk queries of one (batch, KV head) unit
+    (its g q-heads) over the whole dequantized unit; the unit is encoded once, outside
+    any timing."""
+
+    def __init__(self, n_queries=64):
+        import oracle
+        from oracle.formats import Codec
+        self.ref = oracle.prefill_reference
+        self.cfg, self.spec = synth.WORKLOADS["prefill_chunk"], PREFILL["prefill_chunk"]
+        cfg = self.cfg
+        kc = Codec("turbo4", rotation=self.spec["rotation"], rot_seed=self.spec["k_seed"])
+        vc = Codec("turbo4", rotation=self.spec["rotation"], rot_seed=self.spec["v_seed"])
+        self.kh = kc.dequantize(kc.encode(synth.kv_unit(cfg, "K", 0, 0)[0])[0])[None, None]
+        self.vh = vc.dequantize(vc.encode(synth.kv_unit(cfg, "V", 0, 0)[0])[0])[None, None]
+        g = cfg["Hq"] // cfg["Hkv"]
+        q32 = synth.prefill_queries(cfg)[0]
+        self.n = n_queries
+        self.q = q32[:1, cfg["T"] - n_queries:, :g]          # the chunk's last queries, KV head 0
+        self.start = cfg["L"] - n_queries
+        self.flops = 4 * 128 * g * sum(self.start + i + 1 for i in range(n_queries))
+
+    def unit(self, i):
+        self.ref(self.q, self.kh, self.vh, [self.start])
+        return self.flops
+
+
 def run_reference(args, rank, world):
     """The reference arm: the oracle as it stands on the host cores, one bounded sample of
     the workload per step, on rank 0 only."""
     if rank != 0:
+        return
+    if args.workload == "prefill_chunk":
+        leg = OraclePrefill()
+        for i in range(args.warmup):
+            leg.unit(i)
+        t0 = time.perf_counter()
+        flops = sum(leg.unit(i) for i in range(args.steps))
+        dt = time.perf_counter() - t0
+        tf = flops / dt / 1e12
+        sample = (f"per step: the last {leg.n} chunk queries x {leg.q.shape[2]} q-heads of one KV head "
+                  f"over {leg.cfg['L']} keys, fp64 dequantize-then-softmax")
+        line = {"impl": "reference", "metric": PREFILL_METRIC, "value": tf, "unit": "TFLOP/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": prefill_config(), "flops_per_step": leg.flops,
+                "cpu_baseline": {"value": tf, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                                 "sample": sample},
+                "e2e": {"value": tf, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
         return
     if args.workload == "write_chunk":
         leg = OracleWrite(args.write_format, args.write_rotation)
@@ -286,6 +357,17 @@ def decode_config(name):
             "B": cfg["B"], "Hq": cfg["Hq"], "Hkv": cfg["Hkv"], "L": cfg["L"], "d": 128,
             "k_format": spec["k_fmt"], "v_format": spec["v_fmt"], "rotation": spec["rotation"],
             "q_dtype": cfg["q_dtype"],
+            "l2": "flushed before every step: 256 MB write then a read of it (no dirty lines left)",
+            "launch": "CUDA graphs"}
+
+
+def prefill_config():
+    cfg, spec = synth.WORKLOADS["prefill_chunk"], PREFILL["prefill_chunk"]
+    return {"workload": (f"prefill_chunk: B={cfg['B']} Hq={cfg['Hq']} Hkv={cfg['Hkv']} d=128 L={cfg['L']} "
+                         f"T={cfg['T']} (the last chunk of a {cfg['L']}-token prompt)"),
+            "B": cfg["B"], "Hq": cfg["Hq"], "Hkv": cfg["Hkv"], "L": cfg["L"], "T": cfg["T"], "d": 128,
+            "k_format": spec["fmt"], "v_format": spec["fmt"], "rotation": spec["rotation"],
+            "q_dtype": cfg["q_dtype"], "mask": "causal",
             "l2": "flushed before every step: 256 MB write then a read of it (no dirty lines left)",
             "launch": "CUDA graphs"}
 
@@ -497,6 +579,136 @@ def run_decode(args, rank, world, dist):
     print(json.dumps(line), flush=True)
 
 
+def run_prefill(args, rank, world, dist):
+    import torch
+
+    import compressed_attention_gb300 as tq
+
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    cfg, spec = synth.WORKLOADS["prefill_chunk"], PREFILL["prefill_chunk"]
+    B, Hq, Hkv, L, T = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["L"], cfg["T"]
+    kctx = tq.Ctx(spec["fmt"], spec["rotation"], spec["k_seed"])
+    vctx = tq.Ctx(spec["fmt"], spec["rotation"], spec["v_seed"])
+    kc = tq.alloc_cache(spec["fmt"], B * Hkv * L, device)
+    vc = tq.alloc_cache(spec["fmt"], B * Hkv * L, device)
+    chunk = {}
+    for tensor, ctx, cache in (("K", kctx, kc), ("V", vctx, vc)):
+        rows = []
+        for b in range(B):
+            for h in range(Hkv):
+                x32, bits = synth.kv_unit(cfg, tensor, b, h)
+                src = to_device_rows(torch, x32, bits, device)
+                u = b * Hkv + h
+                tq.tq_quantize_set_rows(ctx, src, cache,
+                                        row_ids=torch.arange(u * L, (u + 1) * L, dtype=torch.int64, device=device))
+                rows.append(src[L - T:])
+        chunk[tensor] = torch.cat(rows).contiguous()  # the chunk's own rows, rewritten every step
+    slots = torch.cat([torch.arange(u * L + L - T, (u + 1) * L, dtype=torch.int64, device=device)
+                       for u in range(B * Hkv)])
+    q32, qbits = synth.prefill_queries(cfg)
+    q = to_device_rows(torch, q32.reshape(-1, 128), qbits.reshape(-1, 128) if qbits is not None else None,
+                       device).reshape(B, T, Hq, 128)
+    q_start = torch.full((B,), L - T, dtype=torch.int32, device=device)
+    ws = tq.alloc_workspace(tq.tq_prefill_workspace_size(kctx, vctx, B, T, Hq, Hkv, L), device)
+    out = torch.empty((B, T, Hq, 128), dtype=torch.float32, device=device)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    flush_l2 = flusher(torch, device)
+
+    def write_and_prepare():
+        tq.tq_quantize_set_rows(kctx, chunk["K"], kc, row_ids=slots)
+        tq.tq_quantize_set_rows(vctx, chunk["V"], vc, row_ids=slots)
+        tq.tq_prefill_prepare_q(kctx, vctx, q, ws, B, T, Hq, Hkv, L)
+
+    def partial():
+        tq.tq_prefill_partial(kctx, vctx, kc, vc, q_start, ws, B, T, Hq, Hkv, L)
+
+    def combine():
+        tq.tq_prefill_combine(kctx, vctx, out, ws, B, T, Hq, Hkv, L)
+
+    if dist:
+        dist.barrier()
+    with ClockSampler(local) as clocks:
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        step_ms = timed_graph_steps(torch, stream, (write_and_prepare, partial, combine), args.steps,
+                                    args.warmup, flush_l2)
+        part_ms = timed_graph_steps(torch, stream, (partial,), args.steps, args.warmup, flush_l2)
+        if dist:
+            dist.barrier()
+    clk = clocks.summary()
+    total_ms = max_over_ranks(sum(step_ms), dist, device)
+    part_avg = max_over_ranks(statistics.mean(part_ms), dist, device)
+
+    # end to end through the public API: q and the chunk's K/V rows in from pinned host
+    # memory, SET_ROWS, tq_prefill_attention, the output back
+    host = {"q": q, "K": chunk["K"], "V": chunk["V"]}
+    pinned = {k: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu()) for k, t in host.items()}
+    hout = torch.empty(out.shape, dtype=torch.float32, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+    d2h = hout.numel() * 4
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush_l2()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for k, t in pinned.items():
+            host[k].copy_(t, non_blocking=True)
+        tq.tq_quantize_set_rows(kctx, chunk["K"], kc, row_ids=slots)
+        tq.tq_quantize_set_rows(vctx, chunk["V"], vc, row_ids=slots)
+        tq.tq_prefill_attention(kctx, vctx, q, kc, vc, q_start, out, ws, B, T, Hq, Hkv, L)
+        hout.copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append((time.perf_counter() - t0) * 1e3)
+    if tq.tq_ctx_device_status(kctx) or tq.tq_ctx_device_status(vctx):
+        raise RuntimeError("device status set after the benchmark")
+
+    flops = prefill_flops(cfg)
+    ms_per_step = total_ms / args.steps
+    value = job_rate(flops, world, ms_per_step) / 1e12
+    peak, peak_kind = measured_tensor_peak()
+    achieved = flops / (part_avg * 1e-3) / 1e12
+    e2e_step_ms = max_over_ranks(statistics.mean(e2e_ms), dist, device)
+    if rank != 0:
+        return
+    cpu = None
+    if world == 1:
+        leg = OraclePrefill()
+        t0, n, work = time.perf_counter(), 0, 0
+        while n < 64 and (time.perf_counter() - t0 < 10.0 or n == 0):
+            work += leg.unit(n)
+            n += 1
+        el = time.perf_counter() - t0
+        cpu = {"value": work / el / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": (f"{n} x the last {leg.n} chunk queries x {leg.q.shape[2]} q-heads of one KV head "
+                          f"over {L} keys, fp64 dequantize-then-softmax, {el:.1f} s")}
+    line = common_line(PREFILL_METRIC, args, world, ms_per_step, value, prefill_config(), "f16")
+    line["unit"] = "TFLOP/s"
+    line["config"]["launch"] = ("each step one CUDA graph (SET_ROWS of the chunk's K and V rows, q preparation, "
+                                "the tensor-core prefill, the combine), steps queued back to back; the prefill "
+                                "kernel timed alone the same way for the roofline")
+    line.update({
+        "tokens_per_s": job_rate(B * T, world, ms_per_step),
+        "flops_per_step": flops,
+        "operands": ("fp16 hi+lo q and p against fp16 centroid tiles decoded from the packed cache; "
+                     "fp32 accumulate in tensor memory; tensor work executed = 2x the algorithmic FLOPs"),
+        "roofline": {"bound": "tensor", "kernel": spec["kernel"], "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "TFLOP/s", "frac": achieved / peak,
+                     "traffic": profiled_traffic("prefill_partial_prefill_chunk", spec["source"]),
+                     "algorithmic_flops_per_launch": flops, "avg_launch_ms": part_avg},
+        "cpu_baseline": cpu,
+        "e2e": {"value": job_rate(flops, world, e2e_step_ms) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step_ms},
+        "gpu_launches": 5 * args.steps,
+        "clocks": clk,
+    })
+    print(json.dumps(line), flush=True)
+
+
 def run_write(args, rank, world, dist):
     import torch
 
@@ -595,7 +807,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["tq", "reference"], default="tq")
-    ap.add_argument("--workload", choices=sorted(DECODE) + ["write_chunk"], default="gqa_lognormal")
+    ap.add_argument("--workload", choices=sorted(DECODE) + ["prefill_chunk", "write_chunk"], default="gqa_lognormal")
     ap.add_argument("--write-format", choices=["turbo4", "turbo3"], default="turbo4")
     ap.add_argument("--write-rotation", choices=["dense", "wht"], default="dense")
     args = ap.parse_args()
@@ -615,6 +827,8 @@ def main():
     try:
         if args.workload == "write_chunk":
             run_write(args, rank, world, dist)
+        elif args.workload == "prefill_chunk":
+            run_prefill(args, rank, world, dist)
         else:
             run_decode(args, rank, world, dist)
     finally:

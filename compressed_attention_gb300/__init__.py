@@ -74,6 +74,9 @@ _SIGNATURES = {
     "tq_prefill_workspace_size": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(_sz)]),
     "tq_prefill_attention": (_i32, [_vp, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
                                     _f32, _vp, _vp, _sz, _vp]),
+    "tq_prefill_prepare_q": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _sz, _vp]),
+    "tq_prefill_partial": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _sz, _vp]),
+    "tq_prefill_combine": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _sz, _vp]),
 }
 
 
@@ -259,6 +262,27 @@ def tq_prefill_attention(k_ctx, v_ctx, q, k_cache, v_cache, q_start, out, worksp
                                     _ptr(q_start), B, T, Hq, Hkv, L, scale, _ptr(out), _ptr(workspace),
                                     workspace.numel() * workspace.element_size(), _stream(stream)),
            "tq_prefill_attention")
+
+
+def _wsb(workspace):
+    return workspace.numel() * workspace.element_size()
+
+
+def tq_prefill_prepare_q(k_ctx, v_ctx, q, workspace, B, T, Hq, Hkv, L, scale=0.0, stream=None):
+    qp, qd = _q_args(q)
+    _check(lib.tq_prefill_prepare_q(k_ctx.handle, v_ctx.handle, qp, qd, B, T, Hq, Hkv, L, scale,
+                                    _ptr(workspace), _wsb(workspace), _stream(stream)), "tq_prefill_prepare_q")
+
+
+def tq_prefill_partial(k_ctx, v_ctx, k_cache, v_cache, q_start, workspace, B, T, Hq, Hkv, L, stream=None):
+    _check(lib.tq_prefill_partial(k_ctx.handle, v_ctx.handle, _ptr(k_cache), _ptr(v_cache), _ptr(q_start),
+                                  B, T, Hq, Hkv, L, _ptr(workspace), _wsb(workspace), _stream(stream)),
+           "tq_prefill_partial")
+
+
+def tq_prefill_combine(k_ctx, v_ctx, out, workspace, B, T, Hq, Hkv, L, stream=None):
+    _check(lib.tq_prefill_combine(k_ctx.handle, v_ctx.handle, B, T, Hq, Hkv, L, _ptr(out), _ptr(workspace),
+                                  _wsb(workspace), _stream(stream)), "tq_prefill_combine")
 
 
 TQ_STATIC_WORKSPACE_BYTES = 4 << 20  # capacity of the static scratch of tq_decode_attention_static

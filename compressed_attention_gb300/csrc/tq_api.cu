@@ -424,32 +424,70 @@ tq_status tq_prefill_workspace_size(const tq_ctx *k_ctx, const tq_ctx *v_ctx, in
   return TQ_OK;
 }
 
-tq_status tq_prefill_attention(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *q, int q_dtype,
-                               const void *k_cache, const void *v_cache, const int32_t *q_start,
-                               int B, int T, int Hq, int Hkv, int L, float scale, float *out,
-                               void *workspace, size_t workspace_bytes, tq_stream_t stream) {
+tq_status tq_prefill_prepare_q(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *q, int q_dtype,
+                               int B, int T, int Hq, int Hkv, int L, float scale, void *workspace,
+                               size_t workspace_bytes, tq_stream_t stream) {
   PrefillShape s;
   tq_status st = check_prefill(k_ctx, v_ctx, B, T, Hq, Hkv, L, &s);
   if (st != TQ_OK) return st;
-  if (!q || !k_cache || !v_cache || !q_start || !out) return fail(TQ_ERR_INVALID_ARG, "null pointer");
+  if (!q) return fail(TQ_ERR_INVALID_ARG, "null q");
   if (q_dtype != TQ_DTYPE_F32 && q_dtype != TQ_DTYPE_BF16 && q_dtype != TQ_DTYPE_F16)
     return fail(TQ_ERR_INVALID_ARG, "bad q dtype");
   if (!aligned(q, 16)) return fail(TQ_ERR_ALIGNMENT, "q must be 16-byte aligned");
-  if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return fail(TQ_ERR_ALIGNMENT, "caches must be 16-byte aligned");
-  if (!aligned(q_start, 4)) return fail(TQ_ERR_ALIGNMENT, "q_start must be 4-byte aligned");
-  if (!aligned(out, 4)) return fail(TQ_ERR_ALIGNMENT, "output must be 4-byte aligned");
   if (!std::isfinite(scale)) return fail(TQ_ERR_INVALID_ARG, "scale must be finite");
   if (scale == 0.f) scale = 1.0f / std::sqrt((float)D);
   Workspace w;
   if ((st = check_workspace(s.q, workspace, workspace_bytes, &w)) != TQ_OK) return st;
-  const cudaStream_t cs = (cudaStream_t)stream;
-  cudaError_t e = launch_prepare_q(k_ctx, q, q_dtype, s.q, scale, w, cs);
+  cudaError_t e = launch_prepare_q(k_ctx, q, q_dtype, s.q, scale, w, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "prepare_q launch");
-  e = launch_prefill(k_ctx, v_ctx, (const uint8_t *)k_cache, (const uint8_t *)v_cache, q_start, s, w, cs);
+  return TQ_OK;
+}
+
+tq_status tq_prefill_partial(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *k_cache,
+                             const void *v_cache, const int32_t *q_start, int B, int T, int Hq,
+                             int Hkv, int L, void *workspace, size_t workspace_bytes,
+                             tq_stream_t stream) {
+  PrefillShape s;
+  tq_status st = check_prefill(k_ctx, v_ctx, B, T, Hq, Hkv, L, &s);
+  if (st != TQ_OK) return st;
+  if (!k_cache || !v_cache || !q_start) return fail(TQ_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return fail(TQ_ERR_ALIGNMENT, "caches must be 16-byte aligned");
+  if (!aligned(q_start, 4)) return fail(TQ_ERR_ALIGNMENT, "q_start must be 4-byte aligned");
+  Workspace w;
+  if ((st = check_workspace(s.q, workspace, workspace_bytes, &w)) != TQ_OK) return st;
+  cudaError_t e = launch_prefill(k_ctx, v_ctx, (const uint8_t *)k_cache, (const uint8_t *)v_cache, q_start, s,
+                                 w, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
-  e = launch_combine_prefill(v_ctx, s, out, w, cs);
+  return TQ_OK;
+}
+
+tq_status tq_prefill_combine(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, int T, int Hq, int Hkv,
+                             int L, float *out, void *workspace, size_t workspace_bytes,
+                             tq_stream_t stream) {
+  PrefillShape s;
+  tq_status st = check_prefill(k_ctx, v_ctx, B, T, Hq, Hkv, L, &s);
+  if (st != TQ_OK) return st;
+  if (!out) return fail(TQ_ERR_INVALID_ARG, "null output");
+  if (!aligned(out, 4)) return fail(TQ_ERR_ALIGNMENT, "output must be 4-byte aligned");
+  Workspace w;
+  if ((st = check_workspace(s.q, workspace, workspace_bytes, &w)) != TQ_OK) return st;
+  cudaError_t e = launch_combine_prefill(v_ctx, s, out, w, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");
   return TQ_OK;
+}
+
+tq_status tq_prefill_attention(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *q, int q_dtype,
+                               const void *k_cache, const void *v_cache, const int32_t *q_start,
+                               int B, int T, int Hq, int Hkv, int L, float scale, float *out,
+                               void *workspace, size_t workspace_bytes, tq_stream_t stream) {
+  if (!k_cache || !v_cache || !q_start || !out) return fail(TQ_ERR_INVALID_ARG, "null pointer");
+  tq_status st = tq_prefill_prepare_q(k_ctx, v_ctx, q, q_dtype, B, T, Hq, Hkv, L, scale, workspace,
+                                      workspace_bytes, stream);
+  if (st != TQ_OK) return st;
+  st = tq_prefill_partial(k_ctx, v_ctx, k_cache, v_cache, q_start, B, T, Hq, Hkv, L, workspace,
+                          workspace_bytes, stream);
+  if (st != TQ_OK) return st;
+  return tq_prefill_combine(k_ctx, v_ctx, B, T, Hq, Hkv, L, out, workspace, workspace_bytes, stream);
 }
 
 tq_status tq_test_decode_wait_timeout(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *k_cache,

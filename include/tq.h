@@ -251,6 +251,20 @@ tq_status tq_prefill_attention(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const v
                                int B, int T, int Hq, int Hkv, int L, float scale, float *out,
                                void *workspace, size_t workspace_bytes, tq_stream_t stream);
 
+/* The three stages of tq_prefill_attention (same arguments and workspace, in this
+ * order on one stream): q rotation and split; the tensor-core scan of the packed
+ * caches -> per-split (max, sum, O) per row; merge, 1/sum and un-rotation. */
+tq_status tq_prefill_prepare_q(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *q, int q_dtype,
+                               int B, int T, int Hq, int Hkv, int L, float scale, void *workspace,
+                               size_t workspace_bytes, tq_stream_t stream);
+tq_status tq_prefill_partial(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *k_cache,
+                             const void *v_cache, const int32_t *q_start, int B, int T, int Hq,
+                             int Hkv, int L, void *workspace, size_t workspace_bytes,
+                             tq_stream_t stream);
+tq_status tq_prefill_combine(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, int T, int Hq, int Hkv,
+                             int L, float *out, void *workspace, size_t workspace_bytes,
+                             tq_stream_t stream);
+
 /* Number of key splits the decode uses for this shape on the current device. */
 tq_status tq_decode_num_splits(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, int Hq,
                                int Hkv, int L, int *n_split);

@@ -19,6 +19,10 @@ Workloads (shapes and distributions of the pages' decode and write workloads):
 * ``long_context``: B=1, Hq=32, Hkv=8, L=131072; bf16 q, K, V N(0,1); seed 5.
 * ``gqa_t3k``: the ``gqa_lognormal`` recipe and seed unchanged (the same draws),
   for the asymmetric cache with 3-bit keys and 4-bit values.
+* ``prefill_chunk``: B=1, Hq=32, Hkv=8, L=32768, T=512 chunk queries at positions
+  L-T .. L-1 (the last chunk of a 32K-token prompt); K and V as ``gqa_lognormal``
+  (lognormal channel scales with one outlier channel per KV head), bf16; q bf16
+  N(0,1) [B, T, Hq, 128]; seed 7.
 
 bf16 values are produced by rounding fp32 draws to nearest-even bf16; they are
 returned both as uint16 bit patterns and as the exactly equal fp32 values.
@@ -36,6 +40,9 @@ WORKLOADS = {
     "long_context": dict(B=1, Hq=32, Hkv=8, L=131072, q_dtype="bf16", kv_dtype="bf16", dist="normal", seed=5),
     # the gqa_lognormal recipe again, for the asymmetric 3-bit-key / 4-bit-value cache
     "gqa_t3k": dict(B=8, Hq=32, Hkv=8, L=32768, q_dtype="bf16", kv_dtype="bf16", dist="lognormal_outlier", seed=2),
+    # the last 512-token chunk of a 32K-token prompt: T chunk queries at positions L-T .. L-1
+    "prefill_chunk": dict(B=1, Hq=32, Hkv=8, L=32768, T=512, q_dtype="bf16", kv_dtype="bf16",
+                          dist="lognormal_outlier", seed=7),
 }
 
 D = 128
@@ -106,6 +113,13 @@ def queries(cfg, B=None, Hq=None):
     Hq = cfg["Hq"] if Hq is None else Hq
     rng = np.random.default_rng([cfg["seed"], _tag("q")])
     return _maybe_bf16(rng.standard_normal((B, Hq, D), dtype=np.float32), cfg["q_dtype"])
+
+
+def prefill_queries(cfg):
+    """Chunk queries q [B, T, Hq, 128]: (fp32 values, bf16 bits or None)."""
+    rng = np.random.default_rng([cfg["seed"], _tag("q"), _tag("prefill")])
+    x = rng.standard_normal((cfg["B"], cfg["T"], cfg["Hq"], D), dtype=np.float32)
+    return _maybe_bf16(x, cfg["q_dtype"])
 
 
 def single_head_inputs():
