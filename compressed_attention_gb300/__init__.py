@@ -23,7 +23,7 @@ TQ_OK, TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_ALIGNMENT, TQ_ERR_CUDA, TQ
 # tq_format
 TQ_FMT_TURBO4, TQ_FMT_TURBO3, TQ_FMT_PROD3, TQ_FMT_VGROUP2 = range(4)
 # tq_codebook_kind
-TQ_CB_DEFAULT, TQ_CB_QUANTILE, TQ_CB_LLOYD = range(3)
+TQ_CB_DEFAULT, TQ_CB_QUANTILE, TQ_CB_LLOYD, TQ_CB_SPHERE = range(4)
 # tq_rotation_kind
 TQ_ROT_WHT, TQ_ROT_DENSE = range(2)
 # tq_dtype
@@ -31,7 +31,8 @@ TQ_DTYPE_F32, TQ_DTYPE_BF16, TQ_DTYPE_F16 = range(3)
 
 FORMATS = {"turbo4": TQ_FMT_TURBO4, "turbo3": TQ_FMT_TURBO3, "prod3": TQ_FMT_PROD3, "vgroup2": TQ_FMT_VGROUP2}
 ROTATIONS = {"wht": TQ_ROT_WHT, "dense": TQ_ROT_DENSE}
-CODEBOOKS = {None: TQ_CB_DEFAULT, "default": TQ_CB_DEFAULT, "quantile": TQ_CB_QUANTILE, "lloyd": TQ_CB_LLOYD}
+CODEBOOKS = {None: TQ_CB_DEFAULT, "default": TQ_CB_DEFAULT, "quantile": TQ_CB_QUANTILE, "lloyd": TQ_CB_LLOYD,
+             "sphere": TQ_CB_SPHERE}
 
 
 class TQError(RuntimeError):
@@ -42,7 +43,8 @@ class TQError(RuntimeError):
 
 class tq_params(ctypes.Structure):
     _fields_ = [("d", ctypes.c_int32), ("format", ctypes.c_int32), ("codebook", ctypes.c_int32),
-                ("rotation", ctypes.c_int32), ("rot_seed", ctypes.c_uint64), ("qjl_seed", ctypes.c_uint64)]
+                ("rotation", ctypes.c_int32), ("rot_seed", ctypes.c_uint64), ("qjl_seed", ctypes.c_uint64),
+                ("qjl_shrink", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 _vp, _i32, _i64, _u64, _f32, _sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64,
@@ -165,12 +167,13 @@ def tq_cache_bytes(fmt, n_rows):
 class Ctx:
     """Owns one tq_ctx (codebook, rotation, QJL matrix on the current device)."""
 
-    def __init__(self, fmt, rotation="wht", rot_seed=0, qjl_seed=0, codebook=None, d=D):
+    def __init__(self, fmt, rotation="wht", rot_seed=0, qjl_seed=0, codebook=None, d=D, qjl_shrink=False):
         self.fmt = fmt
         self.rotation = rotation
         self.rot_seed = rot_seed
         self.qjl_seed = qjl_seed
-        p = tq_params(d, FORMATS[fmt], CODEBOOKS[codebook], ROTATIONS[rotation], rot_seed, qjl_seed)
+        p = tq_params(d, FORMATS[fmt], CODEBOOKS[codebook], ROTATIONS[rotation], rot_seed, qjl_seed,
+                      int(bool(qjl_shrink)), 0)
         h = _vp()
         _check(lib.tq_ctx_create(ctypes.byref(p), ctypes.byref(h)), "tq_ctx_create")
         self.handle = h.value

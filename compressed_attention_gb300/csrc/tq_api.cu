@@ -137,7 +137,8 @@ size_t tq_cache_bytes(int format, int64_t n_rows) {
 tq_status tq_make_codebook(int bits, int d, int kind, float *centroids, float *boundaries) {
   if (d != D) return fail(TQ_ERR_UNSUPPORTED, "only d = 128 is supported");
   if (bits < 1 || bits > 4) return fail(TQ_ERR_UNSUPPORTED, "bits must be 1..4");
-  if (kind != TQ_CB_QUANTILE && kind != TQ_CB_LLOYD) return fail(TQ_ERR_INVALID_ARG, "bad codebook kind");
+  if (kind != TQ_CB_QUANTILE && kind != TQ_CB_LLOYD && kind != TQ_CB_SPHERE)
+    return fail(TQ_ERR_INVALID_ARG, "bad codebook kind");
   if (!centroids) return fail(TQ_ERR_INVALID_ARG, "null centroids");
   double c[16];
   if (!make_codebook_f64(bits, d, kind, c)) return fail(TQ_ERR_INVALID_ARG, "codebook construction failed");
@@ -179,15 +180,19 @@ tq_status tq_ctx_create(const tq_params *params, tq_ctx **out) {
   const bool rotated = p.format != TQ_FMT_VGROUP2;
   if (rotated && p.rotation != TQ_ROT_WHT && p.rotation != TQ_ROT_DENSE)
     return fail(TQ_ERR_INVALID_ARG, "bad rotation kind");
-  if (rotated && p.codebook != TQ_CB_DEFAULT && p.codebook != TQ_CB_QUANTILE && p.codebook != TQ_CB_LLOYD)
+  if (rotated && p.codebook != TQ_CB_DEFAULT && p.codebook != TQ_CB_QUANTILE && p.codebook != TQ_CB_LLOYD &&
+      p.codebook != TQ_CB_SPHERE)
     return fail(TQ_ERR_INVALID_ARG, "bad codebook kind");
   if (p.format == TQ_FMT_PROD3 && p.qjl_seed == p.rot_seed)
     return fail(TQ_ERR_INVALID_ARG, "the QJL seed must differ from the rotation seed");
+  if ((p.qjl_shrink != 0 && p.qjl_shrink != 1) || p.reserved != 0)
+    return fail(TQ_ERR_INVALID_ARG, "qjl_shrink must be 0 or 1 and reserved 0");
 
   tq_ctx *c = new (std::nothrow) tq_ctx();
   if (!c) return fail(TQ_ERR_ALLOC, "host allocation failed");
   c->p = p;
   c->fmt = p.format;
+  c->qjl_factor = (p.format == TQ_FMT_PROD3 && p.qjl_shrink) ? (float)(2.0 / 3.14159265358979323846) : 1.0f;
   cudaError_t e = cudaGetDevice(&c->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
   if (e == cudaSuccess)

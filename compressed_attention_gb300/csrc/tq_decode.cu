@@ -826,7 +826,7 @@ cudaError_t launch_prepare_q(const tq_ctx *k, const void *q, int q_dtype, const 
   p.rt = k->d_pit;
   p.st = s.pv ? k->d_St : nullptr;
   p.mul = LOG2E * scale / k->f16.alpha;
-  p.mul_sk = (float)(LOG2E * (double)scale * 1.2533141373155003 / D);  // sqrt(pi/2) / d
+  p.mul_sk = (float)(LOG2E * (double)scale * (double)k->qjl_factor * 1.2533141373155003 / D);  // sqrt(pi/2) / d
   p.qhl = ws.qhl;
   p.qsc = ws.qsc;
   const int grid = (p.n_q + QWARPS - 1) / QWARPS;

@@ -23,6 +23,7 @@ struct DequantParams {
   float c[16];
   const float *r;  // R row-major
   const float *S;  // S row-major
+  float qjl_factor;  // 1, or 2/pi for the shrunk QJL estimator
   float *dst;
 };
 
@@ -95,7 +96,7 @@ __global__ void __launch_bounds__(WARPS * 32) k_dequant(const DequantParams p) {
         if (prod) {
           const float n = *reinterpret_cast<const float *>(rp);
           const float gamma = *reinterpret_cast<const float *>(rp + 4);
-          const float kq = 1.2533141373155003f / (float)D * gamma;  // sqrt(pi/2)/d * gamma
+          const float kq = p.qjl_factor * (1.2533141373155003f / (float)D) * gamma;  // sqrt(pi/2)/d * gamma
 #pragma unroll
           for (int m = 0; m < 4; ++m) out[m] = n * (acc[m] + kq * q[m]);
         } else {
@@ -122,6 +123,7 @@ cudaError_t launch_dequantize(const tq_ctx *ctx, const uint8_t *cache, int64_t n
   for (int k = 0; k < ctx->cb.K; ++k) p.c[k] = ctx->cb.c[k];
   p.r = ctx->d_pi;
   p.S = ctx->d_S;
+  p.qjl_factor = ctx->qjl_factor;
   p.dst = dst;
   int64_t want = (n_rows + WARPS - 1) / WARPS;
   int64_t cap = (int64_t)ctx->num_sms * 8;

@@ -57,6 +57,63 @@ double std_quantile(double p) {
 
 double cond_mean(double a, double b) { return (std_pdf(a) - std_pdf(b)) / std_mass(a, b); }
 
+// Regularized incomplete beta I_x(a, b) for x <= (a + 1) / (a + b + 2), by the continued
+// fraction of DLMF 8.17.22 evaluated with the modified Lentz method.
+double betainc_cf(double a, double b, double x) {
+  if (x <= 0.0) return 0.0;
+  const double log_front = a * std::log(x) + b * std::log1p(-x) - std::log(a) -
+                           (std::lgamma(a) + std::lgamma(b) - std::lgamma(a + b));
+  const double tiny = 1e-300;
+  double f = 1.0, c = 1.0, dd = 0.0;
+  for (int i = 0; i <= 2000; ++i) {
+    double num;  // the i-th numerator d_i of 1 / (1 + d_1 / (1 + d_2 / ...))
+    if (i == 0) {
+      num = 1.0;
+    } else {
+      const int m = i / 2;
+      num = (i % 2 == 0) ? m * (b - m) * x / ((a + 2.0 * m - 1.0) * (a + 2.0 * m))
+                         : -(a + m) * (a + b + m) * x / ((a + 2.0 * m) * (a + 2.0 * m + 1.0));
+    }
+    dd = 1.0 + num * dd;
+    if (std::fabs(dd) < tiny) dd = tiny;
+    dd = 1.0 / dd;
+    c = 1.0 + num / c;
+    if (std::fabs(c) < tiny) c = tiny;
+    const double delta = c * dd;
+    f *= delta;
+    if (std::fabs(delta - 1.0) < 1e-16) break;
+  }
+  return std::exp(log_front) * (f - 1.0);
+}
+
+// I_t(al, al) for the symmetric case, with the fraction on the side where it converges.
+double betainc_sym(double al, double t) {
+  if (t <= 0.0) return 0.0;
+  if (t >= 1.0) return 1.0;
+  return t <= 0.5 ? betainc_cf(al, al, t) : 1.0 - betainc_cf(al, al, 1.0 - t);
+}
+
+// Law of one coordinate X of a uniform point on the unit sphere in R^d: density
+// proportional to (1 - x^2)^m on [-1, 1], m = (d - 3)/2, i.e. (1 + X)/2 ~ Beta(al, al),
+// al = m + 1.  P(a < X < b), taken on the side that avoids cancellation.
+double sphere_mass(double al, double a, double b) {
+  const double ta = a <= -1.0 ? 0.0 : (a >= 1.0 ? 1.0 : 0.5 * (1.0 + a));
+  const double tb = b <= -1.0 ? 0.0 : (b >= 1.0 ? 1.0 : 0.5 * (1.0 + b));
+  if (tb <= 0.5) return betainc_sym(al, tb) - betainc_sym(al, ta);
+  if (ta >= 0.5) return betainc_sym(al, 1.0 - ta) - betainc_sym(al, 1.0 - tb);
+  return 1.0 - betainc_sym(al, ta) - betainc_sym(al, 1.0 - tb);
+}
+
+// E[X | a < X < b]: the first moment integrates in closed form,
+// int x (1 - x^2)^m dx = -(1 - x^2)^al / (2 al), over Z = 2 4^m B(al, al).
+double sphere_cond_mean(double al, double a, double b) {
+  const double m = al - 1.0;
+  const double log_z = std::log(2.0) + m * std::log(4.0) + 2.0 * std::lgamma(al) - std::lgamma(2.0 * al);
+  const double ga = (a > -1.0 && a < 1.0) ? std::pow(1.0 - a * a, al) : 0.0;
+  const double gb = (b > -1.0 && b < 1.0) ? std::pow(1.0 - b * b, al) : 0.0;
+  return (ga - gb) / (2.0 * al) * std::exp(-log_z) / sphere_mass(al, a, b);
+}
+
 }  // namespace
 
 void set_error(const char *fmt, ...) {
@@ -74,6 +131,25 @@ bool make_codebook_f64(int bits, int d, int kind, double *c) {
   std::vector<double> t(K + 1), cs(K);
   for (int k = 0; k <= K; ++k) t[k] = std_quantile((double)k / K);
   for (int k = 0; k < K; ++k) cs[k] = cond_mean(t[k], t[k + 1]);  // QUANTILE, standard units
+  if (kind == TQ_CB_SPHERE) {
+    // Lloyd-Max under the sphere marginal, from the Gaussian QUANTILE start (in x units)
+    const double al = 0.5 * (d - 1);
+    std::vector<double> cx(K), cn(K);
+    for (int k = 0; k < K; ++k) cx[k] = cs[k] * sigma;
+    for (int it = 0; it < 1000000; ++it) {
+      double moved = 0.0;
+      for (int k = 0; k < K; ++k) {
+        const double a = k == 0 ? -1.0 : 0.5 * (cx[k - 1] + cx[k]);
+        const double b = k == K - 1 ? 1.0 : 0.5 * (cx[k] + cx[k + 1]);
+        cn[k] = sphere_cond_mean(al, a, b);
+        moved = std::fmax(moved, std::fabs(cn[k] - cx[k]));
+      }
+      cx = cn;
+      if (moved < 1e-13) break;
+    }
+    for (int k = 0; k < K; ++k) c[k] = cx[k];
+    return true;
+  }
   if (kind == TQ_CB_LLOYD) {
     std::vector<double> cn(K);
     for (int it = 0; it < 1000000; ++it) {

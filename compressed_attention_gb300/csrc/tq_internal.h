@@ -68,6 +68,7 @@ struct tq_ctx {
   tq::BucketTable bt{};                 // nearest-centroid grid of the codebook (host copy)
   tq::BucketTable *d_bt = nullptr;      // the same on the device
   int32_t *d_status = nullptr;          // device status word
+  float qjl_factor = 1.0f;              // PROD3 reads: 1 (unbiased) or 2/pi (shrunk QJL term)
 };
 
 namespace tq {

@@ -86,7 +86,10 @@ typedef enum tq_format {
 typedef enum tq_codebook_kind {
   TQ_CB_DEFAULT = 0,
   TQ_CB_QUANTILE = 1,
-  TQ_CB_LLOYD = 2
+  TQ_CB_LLOYD = 2,
+  TQ_CB_SPHERE = 3    /* Lloyd-Max under the exact law of a rotated unit-vector coordinate:
+                         (1 + x)/2 ~ Beta((d-1)/2, (d-1)/2) ([Triton deep dive] "write path
+                         and codebook": Lloyd-Max centroids for the rotated Beta law) */
 } tq_codebook_kind;
 
 /* Rotation y = R u applied before quantization.
@@ -115,6 +118,10 @@ typedef struct tq_params {
   uint64_t rot_seed;  /* seed of the rotation */
   uint64_t qjl_seed;  /* seed of the QJL matrix S (PROD3 only; must differ from rot_seed,
                          [turbo4 post-mortem] section 10) */
+  int32_t qjl_shrink; /* PROD3 reads: 0 = the unbiased estimator (sqrt(pi/2)/d) gamma S^T sigma,
+                         1 = that term times 2/pi ([turbo4 post-mortem] section 3's shrinkage).
+                         The stored bytes do not depend on it. */
+  int32_t reserved;   /* must be 0 */
 } tq_params;
 
 /* ---------------------------------------------------------------- host only */

@@ -49,6 +49,8 @@ from .codebook import (  # noqa: F401
     make_codebook,
     quantile_codebook,
     lloyd_codebook,
+    sphere_codebook,
+    sphere_mass,
     stored_codebook,
     codebook_mse,
 )

@@ -137,7 +137,7 @@ def attention_compressed_domain(q, k_codec, k_blocks, v_codec, v_blocks, seq_len
                 s = kf["n"] * (kf["y_hat"] @ q_rot)
                 if k_codec.fmt == "prod3":
                     q_sk = k_codec.S32.astype(np.float64) @ q[b, h]  # trick 2: once per query
-                    s = s + kf["n"] * kf["gamma"] * (QJL_SCALE_NUM / d) * (kf["sigma"] @ q_sk)
+                    s = s + kf["n"] * kf["gamma"] * k_codec.qjl_factor * (QJL_SCALE_NUM / d) * (kf["sigma"] @ q_sk)
                 s = s * scale
                 bounds = np.linspace(0, Lb, n_chunks + 1).astype(int)
                 parts = [_chunk_partial(s[a:e], vals[a:e]) for a, e in zip(bounds[:-1], bounds[1:]) if e > a]

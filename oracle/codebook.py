@@ -13,7 +13,14 @@ Two constructions are provided:
   equal-probability partition, which is the reading under which "Lloyd
   iteration on N(0, 1/d)" reproduces that table.
 * LLOYD: iterate Lloyd-Max (boundaries = midpoints, centroids = conditional
-  means) from the QUANTILE start until it stops moving.  At d=128, 16 levels
+  means) from the QUANTILE start until it stops moving.
+* SPHERE: the same Lloyd-Max iteration under the exact law of one coordinate of a
+  uniformly random unit vector ("Lloyd-Max centroids for the rotated Beta
+  distribution", [Triton deep dive] "write path and codebook"): density
+  proportional to (1 - x^2)^((d-3)/2) on [-1, 1], i.e. (1 + x)/2 ~ Beta((d-1)/2,
+  (d-1)/2).  Reading: the pages' "Beta(63.5, 63.5) for the absolute value" at
+  d = 128 is this marginal written for (1 + x)/2 (the absolute value of a coordinate
+  does not follow a symmetric Beta law).  At d=128, 16 levels
   its outer centroid is 2.733 sigma = 0.2416, the value quoted for the other
   implementation in section 9 of [turbo4 post-mortem]; for 1 and 2 bits the
   section-5 text says the reference uses the closed forms, which Lloyd reaches.
@@ -107,12 +114,68 @@ def lloyd_codebook(bits, d, tol=1e-13, max_iter=1_000_000):
     return c * sigma
 
 
+def _sphere_alpha(d):
+    """Shape of the sphere marginal: (1 + X)/2 ~ Beta(alpha, alpha), alpha = (d - 1)/2."""
+    return 0.5 * (d - 1)
+
+
+def sphere_mass(a, b, d):
+    """P(a < X < b) for one coordinate X of a uniform point on the unit sphere in R^d
+    (density proportional to (1 - x^2)^((d - 3)/2) on [-1, 1]), through the regularized
+    incomplete beta function of (1 + x)/2."""
+    from scipy.special import betainc
+    al = _sphere_alpha(d)
+    ta = 0.0 if a <= -1.0 else (1.0 if a >= 1.0 else 0.5 * (1.0 + a))
+    tb = 0.0 if b <= -1.0 else (1.0 if b >= 1.0 else 0.5 * (1.0 + b))
+    if tb <= 0.5:  # both in the lower half: no cancellation against 1
+        return float(betainc(al, al, tb) - betainc(al, al, ta))
+    if ta >= 0.5:
+        return float(betainc(al, al, 1.0 - ta) - betainc(al, al, 1.0 - tb))
+    return float(1.0 - betainc(al, al, ta) - betainc(al, al, 1.0 - tb))
+
+
+def sphere_cond_mean(a, b, d):
+    """E[X | a < X < b] for the sphere marginal.  The first moment has a closed form,
+    int x (1 - x^2)^m dx = -(1 - x^2)^(m+1) / (2 (m+1)), normalised by
+    Z = int_{-1}^{1} (1 - x^2)^m dx = 2 4^m B(m+1, m+1), m = (d - 3)/2."""
+    al = _sphere_alpha(d)  # = m + 1
+    m = al - 1.0
+    log_z = math.log(2.0) + m * math.log(4.0) + 2.0 * math.lgamma(al) - math.lgamma(2.0 * al)
+    ga = (1.0 - a * a) ** al if -1.0 < a < 1.0 else 0.0
+    gb = (1.0 - b * b) ** al if -1.0 < b < 1.0 else 0.0
+    first = (ga - gb) / (2.0 * al) * math.exp(-log_z)
+    return first / sphere_mass(a, b, d)
+
+
+def sphere_codebook(bits, d, tol=1e-13, max_iter=1_000_000):
+    """Converged Lloyd-Max quantizer for the exact law of a rotated unit-vector coordinate
+    ([Triton deep dive] "write path and codebook": Lloyd-Max centroids for the rotated
+    Beta distribution; (1 + x)/2 ~ Beta((d-1)/2, (d-1)/2) is the sphere marginal), fp64.
+
+    Starts from the Gaussian QUANTILE centroids; boundaries = midpoints of adjacent
+    centroids, centroids = conditional means of the cells under the sphere marginal,
+    until no centroid moves by more than ``tol``.
+    """
+    K = 1 << bits
+    c = quantile_codebook(bits, d)
+    for _ in range(max_iter):
+        t = [-1.0] + [0.5 * (c[k] + c[k + 1]) for k in range(K - 1)] + [1.0]
+        c_new = np.array([sphere_cond_mean(t[k], t[k + 1], d) for k in range(K)])
+        moved = np.max(np.abs(c_new - c))
+        c = c_new
+        if moved < tol:
+            break
+    return c
+
+
 def make_codebook(bits, d, kind):
-    """fp64 centroids of the requested kind ("quantile" or "lloyd")."""
+    """fp64 centroids of the requested kind ("quantile", "lloyd" or "sphere")."""
     if kind == "quantile":
         return quantile_codebook(bits, d)
     if kind == "lloyd":
         return lloyd_codebook(bits, d)
+    if kind == "sphere":
+        return sphere_codebook(bits, d)
     raise ValueError(f"unknown codebook kind {kind!r}")
 
 

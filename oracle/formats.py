@@ -51,6 +51,7 @@ ROW_BYTES = {"turbo4": 68, "turbo3": 56, "prod3": 56, "vgroup2": 48}
 CODE_BITS = {"turbo4": 4, "turbo3": 3, "prod3": 2}
 DEFAULT_CODEBOOK = {"turbo4": "quantile", "turbo3": "lloyd", "prod3": "lloyd"}
 QJL_SCALE_NUM = math.sqrt(math.pi / 2.0)  # the estimator's constant is sqrt(pi/2) / d
+QJL_SHRINK = 2.0 / math.pi  # optional factor on the QJL term ([turbo4 post-mortem] section 3)
 
 
 def canonical_norm_fp32(x):
@@ -225,8 +226,10 @@ def qjl_sign_bits(S, r):
     return (z >= 0.0).astype(np.uint8), z
 
 
-def qjl_residual_estimate(S, sign_bits, gamma):
-    """QJL reconstruction of the residual: (sqrt(pi/2)/d) * gamma * S^T sigma, sigma = +-1.
+def qjl_residual_estimate(S, sign_bits, gamma, shrink=1.0):
+    """QJL reconstruction of the residual: shrink * (sqrt(pi/2)/d) * gamma * S^T sigma,
+    sigma = +-1; shrink = 1 is the unbiased estimator, 2/pi the shrunk one of
+    [turbo4 post-mortem] section 3 ("the MMSE-optimal shrinkage is 2/pi").
 
     [turbo4 post-mortem] section 2 bug 2 (a matrix-vector product with S^T, scaled by
     sqrt(pi/2)/sqrt(d) * ||x|| for S with N(0, 1/d) entries, i.e. sqrt(pi/2)/d for
@@ -236,7 +239,7 @@ def qjl_residual_estimate(S, sign_bits, gamma):
     d = S.shape[-1]
     sigma = np.where(np.asarray(sign_bits) == 1, 1.0, -1.0)
     st_sigma = np.einsum("...ij,...i->...j", S, sigma)
-    return (QJL_SCALE_NUM / d) * np.asarray(gamma, dtype=np.float64)[..., None] * st_sigma
+    return shrink * (QJL_SCALE_NUM / d) * np.asarray(gamma, dtype=np.float64)[..., None] * st_sigma
 
 
 def _pack_2bit(codes):
@@ -334,7 +337,7 @@ class Codec:
     ([turbo4 post-mortem] section 10).
     """
 
-    def __init__(self, fmt, d=128, rotation="wht", rot_seed=0, qjl_seed=None, codebook=None):
+    def __init__(self, fmt, d=128, rotation="wht", rot_seed=0, qjl_seed=None, codebook=None, qjl_shrink=False):
         if d != 128:
             raise ValueError("only d = 128 is defined")
         self.fmt = fmt
@@ -350,6 +353,7 @@ class Codec:
                 raise ValueError("prod3 needs a QJL seed independent of the rotation seed")
             self.S32 = _qjl32(qjl_seed, d)
             self.qjl_seed = qjl_seed
+            self.qjl_factor = QJL_SHRINK if qjl_shrink else 1.0
 
     # -- write path -----------------------------------------------------------------
     def encode(self, x):
@@ -409,6 +413,6 @@ class Codec:
         if self.fmt == "prod3":
             mse = self.rot.inverse(f["y_hat"])
             sign_bits = (f["sigma"] > 0).astype(np.uint8)
-            qjl = qjl_residual_estimate(self.S32, sign_bits, f["gamma"])
+            qjl = qjl_residual_estimate(self.S32, sign_bits, f["gamma"], self.qjl_factor)
             return f["n"][:, None] * (mse + qjl)
         return f["v_hat"]

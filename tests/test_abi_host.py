@@ -40,7 +40,8 @@ def test_library_exports_every_declared_symbol(tq):
     assert missing == []
 
 
-@pytest.mark.parametrize("bits,kind", [(1, "quantile"), (2, "lloyd"), (3, "lloyd"), (4, "quantile"), (4, "lloyd")])
+@pytest.mark.parametrize("bits,kind", [(1, "quantile"), (2, "lloyd"), (3, "lloyd"), (4, "quantile"), (4, "lloyd"),
+                                       (1, "sphere"), (2, "sphere"), (3, "sphere"), (4, "sphere")])
 def test_host_codebook_matches_oracle(tq, bits, kind):
     c, b = tq.tq_make_codebook(bits, 128, kind)
     c32, b32 = oracle.stored_codebook(oracle.make_codebook(bits, 128, kind))
@@ -83,10 +84,14 @@ def test_host_validation_errors(tq):
     assert lib.tq_quantize_set_rows(None, None, 0, 1, 128, None, None, 1, None) == tq.TQ_ERR_INVALID_ARG
     assert lib.tq_decode_attention(None, None, None, 0, None, None, None, 1, 1, 1, 1, 0.0, None, None,
                                    None, 0, None) == tq.TQ_ERR_INVALID_ARG
-    p = tq.tq_params(64, 0, 0, 0, 0, 0)
+    p = tq.tq_params(64, 0, 0, 0, 0, 0, 0, 0)
     h = ctypes.c_void_p()
     assert lib.tq_ctx_create(ctypes.byref(p), ctypes.byref(h)) == tq.TQ_ERR_UNSUPPORTED
-    p = tq.tq_params(128, tq.TQ_FMT_PROD3, 0, tq.TQ_ROT_DENSE, 7, 7)
+    p = tq.tq_params(128, tq.TQ_FMT_PROD3, 0, tq.TQ_ROT_DENSE, 7, 7, 0, 0)
     assert lib.tq_ctx_create(ctypes.byref(p), ctypes.byref(h)) == tq.TQ_ERR_INVALID_ARG
     assert b"QJL seed" in lib.tq_last_error()
+    p = tq.tq_params(128, tq.TQ_FMT_PROD3, 0, tq.TQ_ROT_DENSE, 7, 8, 2, 0)  # qjl_shrink not 0/1
+    assert lib.tq_ctx_create(ctypes.byref(p), ctypes.byref(h)) == tq.TQ_ERR_INVALID_ARG
+    p = tq.tq_params(128, tq.TQ_FMT_TURBO4, tq.TQ_CB_SPHERE + 1, tq.TQ_ROT_WHT, 7, 8, 0, 0)
+    assert lib.tq_ctx_create(ctypes.byref(p), ctypes.byref(h)) == tq.TQ_ERR_INVALID_ARG
     assert lib.tq_status_string(tq.TQ_ERR_WORKSPACE) == b"workspace too small"

@@ -335,3 +335,22 @@ def test_decode_shape_limits():
     with pytest.raises(tq.TQError) as e:
         tq.tq_decode_workspace_size(ctx, ctx, 1 << 20, 8, 8, 1 << 20)
     assert e.value.status == tq.TQ_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("kfmt", ["turbo4", "turbo3"])
+def test_decode_sphere_codebook(kfmt):
+    """Sphere-marginal codebooks for keys and values: the kernels take any symmetric table."""
+    tq = lib()
+    B, Hq, Hkv, L = 2, 8, 2, 450
+    kcodec = Codec(kfmt, rotation="wht", rot_seed=51, codebook="sphere")
+    vcodec = Codec("turbo4", rotation="wht", rot_seed=52, codebook="sphere")
+    kb = oracle_cache(kcodec, B, Hkv, L, 51, scale=2.0, dist="lognormal")
+    vb = oracle_cache(vcodec, B, Hkv, L, 52)
+    q_t, q32 = torch_rows(np.random.default_rng(53).standard_normal((B, Hq, 128)).astype(np.float32), "bf16")
+    kctx = tq.Ctx(kfmt, "wht", 51, codebook="sphere")
+    vctx = tq.Ctx("turbo4", "wht", 52, codebook="sphere")
+    out, sc = run_decode(tq, kctx, vctx, q_t, upload_cache(tq, kfmt, kb), upload_cache(tq, "turbo4", vb),
+                         B, Hq, Hkv, L)
+    ref, s_ref = reference(q32, kcodec, kb, vcodec, vb, None)
+    check_outputs(out, ref)
+    assert np.max(np.abs(sc - s_ref)) <= ATOL

@@ -177,3 +177,27 @@ def test_decode_pv_many_heads_staged_prep():
     ref, s_ref = reference(q32, kcodec, kb, vcodec, vb, None)
     check_outputs(out, ref)
     assert np.max(np.abs(sc - s_ref)) <= ATOL
+
+
+def test_decode_pv_shrunk_qjl_and_sphere_codebook():
+    """The 2/pi-shrunk QJL term and the sphere-marginal 2-bit codebook: the same kernel
+    with a different sketch scale and centroid table, against the oracle's estimator."""
+    tq = lib()
+    B, Hq, Hkv, L = 2, 12, 2, 333
+    kcodec = Codec("prod3", rotation="dense", rot_seed=ROT_SEED, qjl_seed=QJL_SEED, codebook="sphere",
+                   qjl_shrink=True)
+    vcodec = Codec("vgroup2")
+    kb = encoded(kcodec, B, Hkv, L, 41, scale=2.0, lognormal=True)
+    vb = encoded(vcodec, B, Hkv, L, 42, scale=3.0)
+    q_t, q32 = torch_rows(np.random.default_rng(43).standard_normal((B, Hq, 128)).astype(np.float32), "bf16")
+    kctx = tq.Ctx("prod3", "dense", ROT_SEED, QJL_SEED, codebook="sphere", qjl_shrink=True)
+    vctx = tq.Ctx("vgroup2")
+    out, sc = run(tq, kctx, vctx, q_t, upload_cache(tq, "prod3", kb), upload_cache(tq, "vgroup2", vb),
+                  B, Hq, Hkv, L)
+    ref, s_ref = reference(q32, kcodec, kb, vcodec, vb, None)
+    check_outputs(out, ref)
+    assert np.max(np.abs(sc - s_ref)) <= ATOL
+    # the shrunk estimator really differs from the unbiased one on these bytes
+    plain = Codec("prod3", rotation="dense", rot_seed=ROT_SEED, qjl_seed=QJL_SEED, codebook="sphere")
+    ref_plain, _ = reference(q32, plain, kb, vcodec, vb, None)
+    assert np.max(np.abs(ref_plain - ref)) > 10 * ATOL

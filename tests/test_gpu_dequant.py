@@ -63,3 +63,21 @@ def test_dequantize_matches_oracle(fmt, rot, unrotate):
     bound = 1e-6 if one_product else 1e-5
     assert err.max() <= bound, f"max error {err.max():.3e} of the row scale > {bound}"
     assert np.all(got[0] == 0.0)  # a zero row reconstructs to zero
+
+
+@pytest.mark.parametrize("fmt,rot,kind", [("turbo4", "wht", "sphere"), ("turbo3", "dense", "sphere"),
+                                          ("prod3", "dense", "sphere")])
+def test_dequantize_other_codebooks_and_shrunk_qjl(fmt, rot, kind):
+    """The sphere-marginal codebook for each rotated format, and the 2/pi-shrunk QJL term."""
+    tq = lib()
+    x = rows(500, 37)
+    if fmt == "prod3":
+        codec = Codec(fmt, rotation=rot, rot_seed=3, qjl_seed=1003, codebook=kind, qjl_shrink=True)
+        ctx = tq.Ctx(fmt, rot, 3, 1003, codebook=kind, qjl_shrink=True)
+    else:
+        codec, ctx = Codec(fmt, rotation=rot, rot_seed=8, codebook=kind), tq.Ctx(fmt, rot, 8, codebook=kind)
+    blocks, _ = codec.encode(x)
+    got = gpu_dequantize(tq, ctx, blocks, True)
+    ref = codec.dequantize(blocks, unrotate=True)
+    scale = np.maximum(np.abs(ref).max(axis=1, keepdims=True), 1e-30)
+    assert (np.abs(got - ref) / scale).max() <= 1e-5

@@ -268,3 +268,15 @@ def test_write_dense_tensor_core_scatter_and_stride(fmt):
     assert ok, f"{ndiff} indices differ outside the boundary band"
     untouched = sorted(set(range(cap)) - set(int(s) for s in slots if s < cap))
     assert np.all(rows[untouched] == 0xA5)
+
+
+@pytest.mark.parametrize("fmt", ["turbo4", "turbo3"])
+def test_write_wht_sphere_codebook_bit_exact(fmt):
+    """The sphere-marginal codebook (its own boundaries and grid table) under the WHT path."""
+    tq = lib()
+    x_t, x32 = torch_rows(make_rows(1500, 23, scale=2.0), "bf16")
+    ref, _ = Codec(fmt, rotation="wht", rot_seed=23, codebook="sphere").encode(x32)
+    ctx = tq.Ctx(fmt, "wht", 23, codebook="sphere")
+    got = to_host_bytes(write_gpu(tq, ctx, x_t, len(x32)), len(x32), ctx.row_bytes)
+    bad = rows_equal_nan_aware(got, ref, fmt)
+    assert bad.size == 0, f"{bad.size} rows differ, first {bad[:5]}"

@@ -91,7 +91,7 @@ def test_quantile_cells_have_equal_mass_by_quadrature(bits):
         assert abs(mom * K - c[k]) < 1e-10
 
 
-@pytest.mark.parametrize("kind", ["quantile", "lloyd"])
+@pytest.mark.parametrize("kind", ["quantile", "lloyd", "sphere"])
 @pytest.mark.parametrize("bits", [1, 2, 3, 4])
 def test_symmetric_and_increasing(kind, bits):
     c = oracle.make_codebook(bits, D, kind)
@@ -134,3 +134,65 @@ def test_stored_boundaries_are_midpoints_and_encode_is_nearest(kind):
     # a coordinate exactly on a boundary goes to the lower index
     assert np.array_equal(nearest_index(b32.astype(np.float64), b32), np.arange(15))
     assert np.array_equal(nearest_index(b32, b32), np.arange(15))
+
+
+# ---- sphere-marginal (rotated unit-vector coordinate) codebook
+
+def _sphere_pdf(d):
+    m = 0.5 * (d - 3)
+    z = integrate.quad(lambda x: (1 - x * x) ** m, -1, 1, epsabs=0, epsrel=1e-13)[0]
+    return lambda x: (1 - x * x) ** m / z
+
+
+def test_sphere_one_bit_closed_form():
+    """1 bit: the centroid of x > 0 is E|X| = Gamma(d/2) / (sqrt(pi) Gamma((d+1)/2))."""
+    for d in (8, 128, 1024):
+        c = oracle.sphere_codebook(1, d)
+        exact = math.exp(math.lgamma(d / 2) - math.lgamma((d + 1) / 2)) / math.sqrt(math.pi)
+        assert abs(c[1] - exact) < 1e-12 and abs(c[0] + exact) < 1e-12
+
+
+def test_sphere_law_mass_and_variance():
+    """The marginal has unit mass and variance exactly 1/d (E X^2 = 1/d on the sphere)."""
+    assert abs(oracle.sphere_mass(-1.0, 1.0, D) - 1.0) < 1e-14
+    f = _sphere_pdf(D)
+    var = integrate.quad(lambda x: x * x * f(x), -1, 1, epsabs=0, epsrel=1e-12)[0]
+    assert abs(var - 1.0 / D) < 1e-13
+    for a, b in ((-0.3, -0.1), (-0.05, 0.02), (0.1, 0.45)):
+        q = integrate.quad(f, a, b, epsabs=0, epsrel=1e-13)[0]
+        assert abs(oracle.sphere_mass(a, b, D) - q) < 1e-13
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_sphere_lloyd_is_fixed_point_by_quadrature(bits):
+    """Each centroid is the conditional mean of its midpoint cell, by direct quadrature of
+    the density (independent of the incomplete-beta route the codebook takes)."""
+    c = oracle.sphere_codebook(bits, D)
+    f = _sphere_pdf(D)
+    t = [-1.0] + list((c[:-1] + c[1:]) / 2) + [1.0]
+    for k in range(len(c)):
+        mass = integrate.quad(f, t[k], t[k + 1], epsabs=0, epsrel=1e-13)[0]
+        mom = integrate.quad(lambda x: x * f(x), t[k], t[k + 1], epsabs=0, epsrel=1e-13)[0]
+        assert abs(mom / mass - c[k]) < 1e-10
+
+
+def test_sphere_codebook_tends_to_gaussian_lloyd():
+    """The sphere marginal tends to N(0, 1/d): scaled by sqrt(d) the two codebooks meet as
+    d grows (and differ at d = 128 by the 4th decimal)."""
+    for bits in (2, 4):
+        gap = [np.max(np.abs(oracle.sphere_codebook(bits, d) - oracle.lloyd_codebook(bits, d))) * math.sqrt(d)
+               for d in (128, 16384)]
+        assert gap[1] < gap[0] / 50 and gap[1] < 1e-3
+
+
+def test_sphere_codebook_beats_gaussian_lloyd_on_the_sphere_law():
+    """Lloyd-Max optimality: under the sphere marginal, the sphere codebook's distortion is
+    below the Gaussian codebook's (quadrature of both)."""
+    f = _sphere_pdf(D)
+
+    def mse(c):
+        t = [-1.0] + list((c[:-1] + c[1:]) / 2) + [1.0]
+        return sum(integrate.quad(lambda x: (x - c[k]) ** 2 * f(x), t[k], t[k + 1], epsabs=0, epsrel=1e-12)[0]
+                   for k in range(len(c)))
+    for bits in (3, 4):
+        assert mse(oracle.sphere_codebook(bits, D)) < mse(oracle.lloyd_codebook(bits, D))

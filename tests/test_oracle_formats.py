@@ -235,3 +235,31 @@ def test_synth_bf16_rounding():
     b = synth.bf16_bits(x)
     assert list(b) == [0x3F80, 0x3F80, 0x3F81, 0xFF62, 0x7F80]
     assert np.array_equal(synth.bf16_to_f32(b)[:2], [1.0, 1.0])
+
+
+def test_qjl_estimator_energy_and_shrinkage_mse():
+    """For a d x d N(0,1) sketch, r_hat = sqrt(pi/2)/d |r| S^T sign(S r) has
+    E |r_hat|^2 = (pi/2 + (d-1)/d) |r|^2 (diagonal terms d^2, off-diagonal d(d-1) 2/pi),
+    so scaling it by s gives MSE(s) = s^2 kappa - 2 s + 1 (units of |r|^2).  Monte Carlo over
+    independent sketches pins both, including the 2/pi shrinkage the estimator offers."""
+    from oracle.formats import QJL_SHRINK, qjl_residual_estimate
+    d, n = 128, 3000
+    rng = np.random.default_rng(17)
+    r = rng.standard_normal(d)
+    r /= np.linalg.norm(r)
+    e2, err = [], {1.0: [], QJL_SHRINK: []}
+    for _ in range(n):
+        S = rng.standard_normal((d, d))
+        bits = (S @ r >= 0).astype(np.uint8)
+        rh = qjl_residual_estimate(S, bits, 1.0)
+        e2.append(rh @ rh)
+        for s in err:
+            dv = s * rh - r
+            err[s].append(dv @ dv)
+    kappa = np.pi / 2 + (d - 1) / d
+    e2 = np.asarray(e2)
+    assert abs(e2.mean() - kappa) < 4 * e2.std() / np.sqrt(n)
+    for s, v in err.items():
+        v = np.asarray(v)
+        assert abs(v.mean() - (s * s * kappa - 2 * s + 1)) < 4 * v.std() / np.sqrt(n)
+    assert np.mean(err[QJL_SHRINK]) < np.mean(err[1.0])
