@@ -73,6 +73,13 @@ _SIGNATURES = {
     "tq_decode_attention_static": (_i32, [_vp, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _f32,
                                           _vp, _vp]),
     "tq_test_decode_wait_timeout": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _sz, _vp]),
+    "tq_store_create": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, ctypes.POINTER(_vp)]),
+    "tq_store_destroy": (_i32, [_vp]),
+    "tq_store_append": (_i32, [_vp, _vp, _vp, _i32, _vp]),
+    "tq_store_state": (_i32, [_vp, ctypes.POINTER(_i64), ctypes.POINTER(_i64), ctypes.POINTER(_vp),
+                              ctypes.POINTER(_vp)]),
+    "tq_store_workspace_size": (_i32, [_vp, _i32, ctypes.POINTER(_sz)]),
+    "tq_store_decode": (_i32, [_vp, _vp, _i32, _i32, _f32, _vp, _vp, _sz, _vp]),
     "tq_prefill_workspace_size": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(_sz)]),
     "tq_prefill_attention": (_i32, [_vp, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
                                     _f32, _vp, _vp, _sz, _vp]),
@@ -286,6 +293,66 @@ def tq_prefill_partial(k_ctx, v_ctx, k_cache, v_cache, q_start, workspace, B, T,
 def tq_prefill_combine(k_ctx, v_ctx, out, workspace, B, T, Hq, Hkv, L, stream=None):
     _check(lib.tq_prefill_combine(k_ctx.handle, v_ctx.handle, B, T, Hq, Hkv, L, _ptr(out), _ptr(workspace),
                                   _wsb(workspace), _stream(stream)), "tq_prefill_combine")
+
+
+class _DeviceBytes:
+    """A device byte range seen through the CUDA array interface (no copy, no ownership)."""
+
+    def __init__(self, ptr, nbytes):
+        self.__cuda_array_interface__ = {"shape": (nbytes,), "typestr": "|u1", "data": (ptr, False),
+                                         "version": 3}
+
+
+class Store:
+    """A ring-buffer capture + block-append store (tq_store_*): recent tokens exact in a
+    device ring, older ones compressed in the store's caches; decode attends over both."""
+
+    def __init__(self, k_ctx, v_ctx, B, Hkv, L, ring_tokens):
+        self.k_ctx, self.v_ctx, self.B, self.Hkv, self.L = k_ctx, v_ctx, B, Hkv, L
+        h = _vp()
+        _check(lib.tq_store_create(k_ctx.handle, v_ctx.handle, B, Hkv, L, ring_tokens, ctypes.byref(h)),
+               "tq_store_create")
+        self.handle = h.value
+
+    def close(self):
+        if self.handle:
+            lib.tq_store_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def append(self, k_new, v_new, stream=None):
+        """k_new, v_new: bf16 [B, Hkv, n, 128] device tensors."""
+        n = k_new.shape[2]
+        _check(lib.tq_store_append(self.handle, _ptr(k_new), _ptr(v_new), n, _stream(stream)), "tq_store_append")
+
+    def state(self):
+        n, f, kc, vc = _i64(0), _i64(0), _vp(), _vp()
+        _check(lib.tq_store_state(self.handle, ctypes.byref(n), ctypes.byref(f), ctypes.byref(kc), ctypes.byref(vc)),
+               "tq_store_state")
+        return n.value, f.value, kc.value, vc.value
+
+    def cache_bytes(self, which):
+        """The compressed cache (which = "k" or "v") as a uint8 device tensor (a view)."""
+        import torch
+        _, _, kc, vc = self.state()
+        ctx = self.k_ctx if which == "k" else self.v_ctx
+        nbytes = tq_cache_bytes(ctx.fmt, self.B * self.Hkv * self.L)
+        return torch.as_tensor(_DeviceBytes(kc if which == "k" else vc, nbytes), device="cuda")
+
+    def workspace_size(self, Hq):
+        n = _sz(0)
+        _check(lib.tq_store_workspace_size(self.handle, Hq, ctypes.byref(n)), "tq_store_workspace_size")
+        return n.value
+
+    def decode(self, q, out, workspace, Hq, scale=0.0, stream=None):
+        qp, qd = _q_args(q)
+        _check(lib.tq_store_decode(self.handle, qp, qd, Hq, scale, _ptr(out), _ptr(workspace), _wsb(workspace),
+                                   _stream(stream)), "tq_store_decode")
 
 
 TQ_STATIC_WORKSPACE_BYTES = 4 << 20  # capacity of the static scratch of tq_decode_attention_static

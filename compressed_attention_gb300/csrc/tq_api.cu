@@ -75,10 +75,6 @@ tq_status to_device(T **dst, const T *src, size_t n) {
   return TQ_OK;
 }
 
-bool decode_pair_supported(const tq_ctx *k, const tq_ctx *v) {
-  return ((k->fmt == TQ_FMT_TURBO4 || k->fmt == TQ_FMT_TURBO3) && v->fmt == TQ_FMT_TURBO4) ||
-         (k->fmt == TQ_FMT_PROD3 && v->fmt == TQ_FMT_VGROUP2);
-}
 
 tq_status check_decode_common(const tq_ctx *k, const tq_ctx *v, int B, int Hq, int Hkv, int L,
                               DecodeShape *shape) {
@@ -100,6 +96,13 @@ tq_status check_workspace(const DecodeShape &s, void *ws, size_t bytes, Workspac
 }
 
 }  // namespace
+
+namespace tq {
+bool decode_pair_supported(const tq_ctx *k, const tq_ctx *v) {
+  return ((k->fmt == TQ_FMT_TURBO4 || k->fmt == TQ_FMT_TURBO3) && v->fmt == TQ_FMT_TURBO4) ||
+         (k->fmt == TQ_FMT_PROD3 && v->fmt == TQ_FMT_VGROUP2);
+}
+}  // namespace tq
 
 extern "C" {
 

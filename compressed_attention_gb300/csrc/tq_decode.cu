@@ -682,6 +682,8 @@ struct CombineParams {
   int n_split;      // partial slots per head
   int Hq, gq, heads_per_cta, n_hg, tiles_per_unit, tiles_per_cta;
   int pf_T, pf_Hkv, pf_qpt, pf_n_qt;  // prefill geometry (pf_T = 0: decode)
+  int no_main;      // 1: no split-K partials (every key is in the exact tail)
+  int tail_slot;    // slot of an exact-tail partial per head, or -1
   const float *r;   // R (row-major) of the value rotation, or null
   float inv_vscale; // 1 / (2^P_SHIFT * alpha_V)
   float *out;
@@ -712,10 +714,12 @@ __global__ void __launch_bounds__(QWARPS * 32) k_combine(const CombineParams p) 
       unit = (b * (p.Hq / p.gq) + h / p.gq) * p.n_hg + (h % p.gq) / p.heads_per_cta;
     }
     const int first = unit * p.tiles_per_unit;
-    const int n_split = ((first + p.tiles_per_unit - 1) / p.tiles_per_cta) - first / p.tiles_per_cta + 1;
+    const int n_main = p.no_main ? 0 : ((first + p.tiles_per_unit - 1) / p.tiles_per_cta) - first / p.tiles_per_cta + 1;
+    const int n_split = n_main + (p.tail_slot >= 0 ? 1 : 0);
+    auto slot = [&](int s) { return s < n_main ? s : p.tail_slot; };  // the tail partial last
     float ms = -INFINITY;
     for (int s = lane; s < n_split; s += 32) {
-      const float *ps = part + (size_t)s * PARTIAL_FLOATS;
+      const float *ps = part + (size_t)slot(s) * PARTIAL_FLOATS;
       if (ps[1] > 0.f) ms = fmaxf(ms, ps[0]);
     }
 #pragma unroll
@@ -725,7 +729,7 @@ __global__ void __launch_bounds__(QWARPS * 32) k_combine(const CombineParams p) 
       const int s = s0 + lane;
       float w = 0.f;
       if (s < n_split) {
-        const float *ps = part + (size_t)s * PARTIAL_FLOATS;
+        const float *ps = part + (size_t)slot(s) * PARTIAL_FLOATS;
         if (ps[1] > 0.f) {
           w = exp2f(ps[0] - ms);
           lsum += w * ps[1];
@@ -737,7 +741,7 @@ __global__ void __launch_bounds__(QWARPS * 32) k_combine(const CombineParams p) 
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int si = min(s0 + i0 + i, n_split - 1);
-          const float *ps = part + (size_t)si * PARTIAL_FLOATS + 6;
+          const float *ps = part + (size_t)slot(si) * PARTIAL_FLOATS + 6;
 #pragma unroll
           for (int m = 0; m < 4; ++m) v[i][m] = ps[lane + 32 * m];
         }
@@ -915,6 +919,8 @@ cudaError_t launch_combine(const tq_ctx *k, const tq_ctx *v, const DecodeShape &
   p.n_split = s.n_part;
   p.Hq = s.Hq, p.gq = s.gq, p.heads_per_cta = s.heads_per_cta, p.n_hg = s.n_hg;
   p.tiles_per_unit = s.tiles_per_unit, p.tiles_per_cta = s.tiles_per_cta;
+  p.no_main = s.no_main ? 1 : 0;
+  p.tail_slot = s.tail_slot;
   const bool vgroup = v->fmt == TQ_FMT_VGROUP2;  // values are not rotated
   p.r = vgroup ? nullptr : v->d_pi;
   p.inv_vscale = 1.0f / (exp2f(P_SHIFT) * (vgroup ? 1.0f : v->f16.alpha));
@@ -934,6 +940,7 @@ cudaError_t launch_combine_prefill(const tq_ctx *v, const PrefillShape &s, float
   p.Hq = s.Hq, p.gq = s.gq;
   p.tiles_per_unit = s.tiles_per_unit, p.tiles_per_cta = s.tiles_per_cta;
   p.pf_T = s.T, p.pf_Hkv = s.Hkv, p.pf_qpt = s.qpt, p.pf_n_qt = s.n_qt;
+  p.tail_slot = -1;
   p.r = v->d_pi;
   p.inv_vscale = 1.0f / (exp2f(P_SHIFT) * v->f16.alpha);
   p.out = out;

@@ -135,6 +135,8 @@ struct DecodeShape {
   int tiles_per_cta;   // contiguous range per persistent CTA
   int grid;            // persistent CTAs (at most one per SM)
   int n_part;          // partial slots per head
+  int tail_slot = -1;  // slot of an exact-tail partial (the store's ring), or -1
+  bool no_main = false;  // no split-K partials: every key is in the exact tail
 };
 struct Workspace {
   uint32_t *qhl;     // [B*Hq][2 operands][128 fp16]: hi then lo, per operand (q_rot, sketch)
@@ -146,6 +148,7 @@ constexpr int PARTIAL_FLOATS = 2 + 4 + D;  // max, sum, 4 group zero-terms, acc[
 
 bool decode_shape(const tq_ctx *k, const tq_ctx *v, int B, int Hq, int Hkv, int L,
                   DecodeShape *s);
+bool decode_pair_supported(const tq_ctx *k, const tq_ctx *v);  // a decode kernel exists
 Workspace carve_workspace(const DecodeShape &s, void *base);
 
 cudaError_t launch_prepare_q(const tq_ctx *k, const void *q, int q_dtype, const DecodeShape &s,

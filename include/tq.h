@@ -272,6 +272,52 @@ tq_status tq_prefill_combine(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, in
                              int L, float *out, void *workspace, size_t workspace_bytes,
                              tq_stream_t stream);
 
+/* ---------------------------------------------------------- capture + store */
+
+/* Ring-buffer capture and block-append store ([Triton deep dive] "write path and
+ * codebook": a ring buffer holds the most recent exact tokens; when it is full the
+ * oldest batch is compressed into the cache, so the decode hot path quantizes
+ * nothing per token; the store appends by blocks).  One store holds B sequences of
+ * Hkv KV heads, all of the same length:
+ *   tokens [0, flushed)   compressed rows in the store's caches [B][Hkv][L];
+ *   tokens [flushed, len) exact bf16 rows in a ring of ring_tokens slots.
+ * When an append finds the ring full, the oldest ring_tokens/2 tokens of every
+ * (sequence, KV head) are quantized by one SET_ROWS launch per cache and flushed
+ * advances by ring_tokens/2; tq_store_decode attends over both parts (split-K
+ * decode over the compressed prefix, one exact partial over the ring, one merge).
+ * All calls of one store must use one stream; the host-side counters advance with
+ * each call, the device work runs in stream order.  The store owns its device
+ * memory (caches, ring, flush indices), freed by tq_store_destroy. */
+typedef struct tq_store tq_store;
+
+/*   k_ctx / v_ctx  a supported decode pair (see tq_decode_attention), on the
+ *                  current device; the store keeps the pointers (contexts outlive it).
+ *   L              compressed capacity per sequence (tokens).
+ *   ring_tokens    even, 2..4096: exact tokens kept; blocks of ring_tokens/2 are flushed. */
+tq_status tq_store_create(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, int Hkv, int L,
+                          int ring_tokens, tq_store **out);
+tq_status tq_store_destroy(tq_store *store);
+
+/* Append n tokens to every sequence: k_new / v_new device bf16 [B][Hkv][n][128],
+ * 16-byte aligned.  TQ_ERR_INVALID_ARG (and nothing appended) when the flushes the
+ * append needs would pass L. */
+tq_status tq_store_append(tq_store *store, const void *k_new, const void *v_new, int n,
+                          tq_stream_t stream);
+
+/* Host-side state: tokens per sequence, compressed tokens, and the device caches
+ * (packed rows [B][Hkv][L]; rows at or past `flushed` are not yet meaningful).
+ * Any output pointer may be NULL. */
+tq_status tq_store_state(const tq_store *store, int64_t *len, int64_t *flushed,
+                         const void **k_cache, const void **v_cache);
+
+/* Decode over the whole store: q device [B][Hq][128] of q_dtype (F32, BF16, F16),
+ * 16-byte aligned; out device fp32 [B][Hq][128]; scale 0 selects 1/sqrt(128);
+ * workspace of tq_store_workspace_size() bytes, 256-byte aligned.  Hq must be a
+ * multiple of Hkv.  The store must hold at least one token. */
+tq_status tq_store_workspace_size(const tq_store *store, int Hq, size_t *bytes);
+tq_status tq_store_decode(const tq_store *store, const void *q, int q_dtype, int Hq, float scale,
+                          float *out, void *workspace, size_t workspace_bytes, tq_stream_t stream);
+
 /* Number of key splits the decode uses for this shape on the current device. */
 tq_status tq_decode_num_splits(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, int Hq,
                                int Hkv, int L, int *n_split);
