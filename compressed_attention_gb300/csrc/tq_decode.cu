@@ -407,9 +407,17 @@ __global__ void __maxnreg__(128)
   const uint32_t kword = 4u * lane, vword = 128u + 4u * lane;
   const uint32_t klo[2] = {p.klo[0], p.klo[1]}, khi[2] = {p.khi[0], p.khi[1]};
   const uint32_t vlo[2] = {p.vlo[0], p.vlo[1]}, vhi[2] = {p.vhi[0], p.vhi[1]};
-  const int kb = warp * 16;
   const int rk0 = key_of_row(g), rk1 = key_of_row(g + 8);
   const int at = (t & 1) | ((t & 2) << 2);  // a_t = 0, 1, 8, 9
+  // Tile row of the warp's key k.  Rows 16 apart start 16 banks apart (68-byte rows), so a
+  // warp whose keys are rows r0 .. r0+7 and r0+16 .. r0+23 reads its packed words and norms
+  // without bank conflicts in every load shape above; warps 0..13 pair up on 32-row blocks
+  // that way, and the last warp (and turbo3 keys, whose 56-byte rows differ) keeps 16
+  // consecutive rows.  Keys a_t + 2m stay 2m rows after key a_t in both layouts.
+  const bool paired = !K3 && warp < 2 * (CWARPS / 2);
+  const int r0 = paired ? 32 * (warp >> 1) + 8 * (warp & 1) : 16 * warp;
+  auto row_of = [&](int k) { return paired ? r0 + (k & 7) + 16 * (k >> 3) : r0 + k; };
+  const int pk0 = row_of(rk0), pk1 = row_of(rk1), pat = row_of(at);
   const int hs = g >> 1;
   const int src0 = 4 * t + hs, src1 = 4 * (4 + t) + hs;
   const float lo_sel = (g & 1) ? 1.f : 0.f;
@@ -482,10 +490,9 @@ __global__ void __maxnreg__(128)
       }
       const int nk = min(TILE, Lb - kf);
       const size_t ks = (unit_row0 + kf) * KROW, vs = (unit_row0 + kf) * T4_ROW;
-      const uint8_t *Ks = stage_buf(smem_raw, s) + (ks & 15) + kb * KROW;
-      const uint8_t *Vs = stage_buf(smem_raw, 4 + s) + (vs & 15) + kb * T4_ROW;
-      const int nkb = nk - kb;  // valid keys of this warp's block (may be <= 0 or > 16)
-      if (nkb > 0) {
+      const uint8_t *Ks = stage_buf(smem_raw, s) + (ks & 15);
+      const uint8_t *Vs = stage_buf(smem_raw, 4 + s) + (vs & 15);
+      if (r0 < nk) {  // the warp's first row is its lowest: some key is valid
         // ---- scores S^T[16 rows x 8 cols] = K_hat Q^T, two accumulator chains
         float sa[NG][4], sb[NG][4];
 #pragma unroll
@@ -496,8 +503,8 @@ __global__ void __maxnreg__(128)
 #pragma unroll
           for (int bl = 0; bl < 4; ++bl) {
             uint32_t d0[4], d1[4];
-            const float n0 = t3_block<FIXED>(Ks + rk0 * KROW + 14 * bl, t, lut_base, kword, klo, khi, d0);
-            const float n1 = t3_block<FIXED>(Ks + rk1 * KROW + 14 * bl, t, lut_base, kword, klo, khi, d1);
+            const float n0 = t3_block<FIXED>(Ks + pk0 * KROW + 14 * bl, t, lut_base, kword, klo, khi, d0);
+            const float n1 = t3_block<FIXED>(Ks + pk1 * KROW + 14 * bl, t, lut_base, kword, klo, khi, d1);
             const uint32_t a0[4] = {d0[0], d1[0], d0[2], d1[2]};
             const uint32_t a1[4] = {d0[1], d1[1], d0[3], d1[3]};
 #pragma unroll
@@ -512,8 +519,8 @@ __global__ void __maxnreg__(128)
             }
           }
         }
-        const uint8_t *kr0 = Ks + rk0 * KROW + 4 + 16 * t;
-        const uint8_t *kr1 = Ks + rk1 * KROW + 4 + 16 * t;
+        const uint8_t *kr0 = Ks + pk0 * KROW + 4 + 16 * t;
+        const uint8_t *kr1 = Ks + pk1 * KROW + 4 + 16 * t;
 #pragma unroll
         for (int w = 0; w < (K3 ? 0 : 4); ++w) {
           uint32_t d0[4], d1[4];
@@ -535,11 +542,11 @@ __global__ void __maxnreg__(128)
         }
         // ---- online softmax over the two keys of this lane, head t of each group
         // turbo3 keys carry their block norms in sa already
-        const float nk0 = K3 ? 1.f : *reinterpret_cast<const float *>(Ks + rk0 * KROW);
-        const float nk1 = K3 ? 1.f : *reinterpret_cast<const float *>(Ks + rk1 * KROW);
-        const float nv0 = *reinterpret_cast<const float *>(Vs + rk0 * T4_ROW);
-        const float nv1 = *reinterpret_cast<const float *>(Vs + rk1 * T4_ROW);
-        const bool ok0 = rk0 < nkb, ok1 = rk1 < nkb;
+        const float nk0 = K3 ? 1.f : *reinterpret_cast<const float *>(Ks + pk0 * KROW);
+        const float nk1 = K3 ? 1.f : *reinterpret_cast<const float *>(Ks + pk1 * KROW);
+        const float nv0 = *reinterpret_cast<const float *>(Vs + pk0 * T4_ROW);
+        const float nv1 = *reinterpret_cast<const float *>(Vs + pk1 * T4_ROW);
+        const bool ok0 = pk0 < nk, ok1 = pk1 < nk;
         const float nu0 = ok0 ? fmaxf(log2_approx(nv0), -64.f) : 0.f;
         const float nu1 = ok1 ? fmaxf(log2_approx(nv1), -64.f) : 0.f;
         uint32_t pb[NG][2];
@@ -550,9 +557,9 @@ __global__ void __maxnreg__(128)
           const float s0 = ok0 ? d0 * (nk0 * qs[c]) : -INFINITY;
           const float s1 = ok1 ? d1 * (nk1 * qs[c]) : -INFINITY;
           if (SCORES && c * 4 + t < G) {
-            float *srow = p.scores + (size_t)(b * p.Hq + head0 + c * 4 + t) * p.L + kf + kb;
-            if (ok0) srow[rk0] = s0 * LN2;
-            if (ok1) srow[rk1] = s1 * LN2;
+            float *srow = p.scores + (size_t)(b * p.Hq + head0 + c * 4 + t) * p.L + kf;
+            if (ok0) srow[pk0] = s0 * LN2;
+            if (ok1) srow[pk1] = s1 * LN2;
           }
           const float u0 = s0 + nu0, u1 = s1 + nu1;
           float bm = fmaxf(u0, u1);
@@ -584,7 +591,7 @@ __global__ void __maxnreg__(128)
           pb[c][1] = *reinterpret_cast<const uint32_t *>(&rcd);
         }
         // ---- O^T[dims x cols] += V_hat^T[dims x keys] P^T
-        const uint8_t *va_p = Vs + at * T4_ROW + 4 + 8 * g;  // key a_t; a_t+2, +4, +6 follow
+        const uint8_t *va_p = Vs + pat * T4_ROW + 4 + 8 * g;  // key a_t; a_t+2, +4, +6 follow
 #pragma unroll
         for (int w = 0; w < 2; ++w) {
           const uint32_t xa = ld_u32(va_p + 4 * w), xb = ld_u32(va_p + 2 * T4_ROW + 4 * w);
