@@ -5,12 +5,13 @@
 // Triton kernels deep dive", "write path and codebook" (2-bit group
 // quantization, value = code * scale + zero).
 //
-// Lane l of a warp holds elements 4l..4l+3 of its row.  The norm is the
-// canonical fp32 tree: squares and adds rounded one by one (no contraction),
-// four-element partial sums per lane, then a butterfly over lanes 16,8,4,2,1.
-// The WHT rotation is the same butterfly over elements (stages 1, 2 inside a
-// lane, 4..64 across lanes), so its result is bit-identical to a plain
-// sequential fp32 implementation of the same stage order.
+// The norm is the canonical fp32 tree: squares and adds rounded one by one (no
+// contraction), sums of four consecutive squares, then pairwise combination over
+// strides 16, 8, 4, 2, 1 of those 32 partial sums.  The WHT rotation is the
+// butterfly of stages 1, 2, ..., 64 in that order, so its result is bit-identical
+// to a plain sequential fp32 implementation of the same stage order.  The WHT
+// kernel gives each of four threads a quarter of a row; the others give lane l of
+// a warp elements 4l..4l+3 of its row and run the same trees across lanes.
 #include "tq_device.cuh"
 #include "tq_internal.h"
 
@@ -94,32 +95,6 @@ __device__ __forceinline__ float norm_normalize(float (&x)[4]) {
   return n;
 }
 
-// Randomized Hadamard in the canonical fp32 order; lane holds elements 4l..4l+3.
-__device__ __forceinline__ void wht_rotate(float (&v)[4], const uint32_t (&neg)[4], int lane) {
-  const uint32_t nb = (neg[lane >> 3] >> ((lane & 7) * 4)) & 0xFu;
-#pragma unroll
-  for (int e = 0; e < 4; ++e)
-    if (nb & (1u << e)) v[e] = -v[e];
-  float a0 = __fadd_rn(v[0], v[1]), a1 = __fsub_rn(v[0], v[1]);
-  float a2 = __fadd_rn(v[2], v[3]), a3 = __fsub_rn(v[2], v[3]);
-  v[0] = __fadd_rn(a0, a2), v[2] = __fsub_rn(a0, a2);
-  v[1] = __fadd_rn(a1, a3), v[3] = __fsub_rn(a1, a3);
-  // across lanes: the lower partner keeps v + o, the upper one o - v, both as one
-  // fused o + (+-1) v (the product by +-1 is exact, so the rounding is the same)
-#pragma unroll
-  for (int m = 1; m <= 16; m <<= 1) {
-    const float sgn = (lane & m) ? -1.0f : 1.0f;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float o = __shfl_xor_sync(FULL_MASK, v[e], m);
-      v[e] = __fmaf_rn(sgn, v[e], o);
-    }
-  }
-  const float inv_sqrt_d = __int_as_float(0x3DB504F3);  // fp32 nearest 1/sqrt(128)
-#pragma unroll
-  for (int e = 0; e < 4; ++e) v[e] = __fmul_rn(v[e], inv_sqrt_d);
-}
-
 // Number of boundaries strictly below y (binary search over NB sorted boundaries).
 template <int NB>
 __device__ __forceinline__ uint32_t bucket(float y, const float *sb) {
@@ -181,31 +156,239 @@ __device__ __forceinline__ bool slot_of(const WriteParams &p, int64_t row, int l
 }
 
 // ------------------------------------------------------------------ WHT turbo4/turbo3
+// Four threads per row (a warp takes eight rows): thread q holds elements 32q .. 32q+31 in
+// registers, so the norm tree's strides 4, 2, 1 and the butterfly stages 1 .. 16 run inside
+// the thread and only two tree strides and two butterfly stages cross threads (shuffles
+// within the row's four lanes).  The operation order is the canonical one -- four-element
+// partial sums of squares combined over strides 16, 8, 4, 2, 1; butterfly stages of
+// distance 1, 2, ..., 64 with the lower element taking a + b and the upper a - b -- so every
+// value is bit-identical to a sequential fp32 implementation of the same order.  For
+// turbo3 each thread owns exactly one 14-byte block.
+constexpr int WT_THREADS = 256;
+constexpr int WT_E = 32;  // elements per thread
+
+// A thread's quarter row as loaded (bf16 bits or fp32), kept while the previous row is
+// encoded.
+template <int SRC>
+struct Quarter {
+  using T = uint2;  // four bf16 (8-byte aligned rows)
+  T w[WT_E / 4];
+};
+template <>
+struct Quarter<TQ_DTYPE_F32> {
+  using T = float4;  // 16-byte aligned rows
+  T w[WT_E / 4];
+};
+
+template <int SRC>
+__device__ __forceinline__ void load_quarter(const WriteParams &p, int64_t row, int q, Quarter<SRC> &raw) {
+  using T = typename Quarter<SRC>::T;
+  const T *s = reinterpret_cast<const T *>(static_cast<const uint8_t *>(p.src) +
+                                           (row * p.stride + WT_E * q) * (SRC == TQ_DTYPE_F32 ? 4 : 2));
+#pragma unroll
+  for (int i = 0; i < WT_E / 4; ++i) raw.w[i] = s[i];
+}
+
+__device__ __forceinline__ void unpack_quarter(const Quarter<TQ_DTYPE_F32> &raw, float (&x)[WT_E]) {
+#pragma unroll
+  for (int i = 0; i < WT_E / 4; ++i)
+    x[4 * i] = raw.w[i].x, x[4 * i + 1] = raw.w[i].y, x[4 * i + 2] = raw.w[i].z, x[4 * i + 3] = raw.w[i].w;
+}
+__device__ __forceinline__ void unpack_quarter(const Quarter<TQ_DTYPE_BF16> &raw, float (&x)[WT_E]) {
+#pragma unroll
+  for (int i = 0; i < WT_E / 4; ++i) {
+    x[4 * i] = bf16_bits_to_f32(raw.w[i].x & 0xFFFFu), x[4 * i + 1] = bf16_bits_to_f32(raw.w[i].x >> 16);
+    x[4 * i + 2] = bf16_bits_to_f32(raw.w[i].y & 0xFFFFu), x[4 * i + 3] = bf16_bits_to_f32(raw.w[i].y >> 16);
+  }
+}
+
+// Canonical fp32 norm of the row (the four threads end with the same value), then u = x / n
+// in place (u = 0 when n == 0).
+__device__ __forceinline__ float quarter_norm_normalize(float (&x)[WT_E]) {
+  float s[8];  // partial sums of this thread's eight four-element groups (8q .. 8q+7)
+#pragma unroll
+  for (int g = 0; g < 8; ++g)
+    s[g] = __fadd_rn(__fadd_rn(__fmul_rn(x[4 * g], x[4 * g]), __fmul_rn(x[4 * g + 1], x[4 * g + 1])),
+                     __fadd_rn(__fmul_rn(x[4 * g + 2], x[4 * g + 2]), __fmul_rn(x[4 * g + 3], x[4 * g + 3])));
+  // stride 16: groups g and g + 16 sit in threads q and q ^ 2; stride 8: q and q ^ 1
+#pragma unroll
+  for (int g = 0; g < 8; ++g) s[g] = __fadd_rn(s[g], __shfl_xor_sync(FULL_MASK, s[g], 2));
+#pragma unroll
+  for (int g = 0; g < 8; ++g) s[g] = __fadd_rn(s[g], __shfl_xor_sync(FULL_MASK, s[g], 1));
+#pragma unroll
+  for (int h = 4; h >= 1; h >>= 1)
+#pragma unroll
+    for (int g = 0; g < h; ++g) s[g] = __fadd_rn(s[g], s[g + h]);
+  const float n = __fsqrt_rn(s[0]);
+  const float r = __frcp_rn(n);
+  // Markstein's correction is exact when every nonzero |x| >= 2^-100 and n <= 2^24 (then
+  // |q| >= 2^-124 and 1/n is normal); zeros come out as zeros.  Otherwise the guarded
+  // per-element division.
+  uint32_t mb = 0xFFFFFFFFu;  // min over elements of |x| bits - 1 (zero -> 0xFFFFFFFF)
+#pragma unroll
+  for (int j = 0; j < WT_E; ++j) mb = min(mb, (__float_as_uint(x[j]) & 0x7FFFFFFFu) - 1u);
+  const bool fast = n <= 0x1p24f && mb >= 0x0D800000u - 1u;  // 0x0D800000: 2^-100
+  if (n == 0.0f) {
+#pragma unroll
+    for (int j = 0; j < WT_E; ++j) x[j] = 0.0f;
+  } else if (fast) {
+#pragma unroll
+    for (int j = 0; j < WT_E; ++j) {
+      const float qq = __fmul_rn(x[j], r);
+      x[j] = __fmaf_rn(__fmaf_rn(-qq, n, x[j]), r, qq);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < WT_E; ++j) x[j] = div_rn(x[j], n, r);
+  }
+  return n;
+}
+
+// Randomized Hadamard of the row: sign flips (bit j of neg for element j), the butterfly,
+// times RN(1/sqrt(128)); thread q holds elements 32q .. 32q+31 (sign word q).
+__device__ __forceinline__ void wht_quarter(float (&v)[WT_E], uint32_t neg, int q) {
+#pragma unroll
+  for (int i = 0; i < WT_E; ++i)
+    v[i] = __uint_as_float(__float_as_uint(v[i]) ^ ((neg << (31 - i)) & 0x80000000u));
+#pragma unroll
+  for (int h = 1; h < WT_E; h <<= 1)
+#pragma unroll
+    for (int i = 0; i < WT_E; ++i)
+      if (!(i & h)) {
+        const float a = v[i], b = v[i + h];
+        v[i] = __fadd_rn(a, b);
+        v[i + h] = __fsub_rn(a, b);
+      }
+  // distances 32 and 64: partner thread q ^ 1, then q ^ 2; the lower one keeps v + o, the
+  // upper one o - v, both as one fused o + (+-1) v (the product by +-1 is exact)
+#pragma unroll
+  for (int m = 1; m <= 2; m <<= 1) {
+    const float sgn = (q & m) ? -1.0f : 1.0f;
+#pragma unroll
+    for (int i = 0; i < WT_E; ++i) {
+      const float o = __shfl_xor_sync(FULL_MASK, v[i], m);
+      v[i] = __fmaf_rn(sgn, v[i], o);
+    }
+  }
+  const float inv_sqrt_d = __int_as_float(0x3DB504F3);  // fp32 nearest 1/sqrt(128)
+#pragma unroll
+  for (int i = 0; i < WT_E; ++i) v[i] = __fmul_rn(v[i], inv_sqrt_d);
+}
+
+// #{k : y > b_k}: the grid (cell t: boundary ce[t].x, count ce[t].y as integer bits) or,
+// without GRID, binary search over the NB boundaries.
+template <bool GRID, int NB>
+__device__ __forceinline__ uint32_t cell_index(float y, const float2 *ce, float gs, float go, int gn,
+                                               const float *sb) {
+  if (GRID) {
+    int t = __float2int_rd(fmaf(y, gs, go));  // NaN -> 0, +-inf -> saturated
+    t = min(max(t, 0), gn - 1);
+    const float2 c = ce[t];
+    return __float_as_uint(c.y) + (y > c.x ? 1u : 0u);
+  }
+  return bucket<NB>(y, sb);
+}
+
+// Nearest-centroid indices of this thread's 32 rotated elements, packed into its part of
+// the row record at row (4-byte aligned): turbo4 = fp32 norm + 64 nibble bytes (thread q:
+// bytes 4 + 16q .. 4 + 16q + 15, thread 0 also the norm); turbo3 = four 14-byte blocks
+// {fp16 norm, qs[8] (low two index bits of element j at bits 2 (j % 4) of qs[j / 4]),
+// signs[4] (high bit at bit j % 8 of signs[j / 8])}, block q from thread q.
+template <int FMT, bool GRID>
+__device__ __forceinline__ void pack_quarter(const float (&y)[WT_E], float n, const float2 *ce, float gs,
+                                             float go, int gn, const float *sb, uint8_t *row, int q) {
+  constexpr int NB = (FMT == TQ_FMT_TURBO4) ? 15 : 7;
+  if (FMT == TQ_FMT_TURBO4) {
+    uint32_t *dst = reinterpret_cast<uint32_t *>(row) + 1 + 4 * q;
+    if (q == 0) reinterpret_cast<uint32_t *>(row)[0] = __float_as_uint(n);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      uint32_t word = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) word |= cell_index<GRID, NB>(y[8 * w + i], ce, gs, go, gn, sb) << (4 * i);
+      dst[w] = word;
+    }
+  } else {
+    uint32_t idx[WT_E];
+#pragma unroll
+    for (int e = 0; e < WT_E; ++e) idx[e] = cell_index<GRID, NB>(y[e], ce, gs, go, gn, sb);
+    const __half hn = __float2half_rn(n);
+    uint32_t b[14];
+    b[0] = *reinterpret_cast<const uint16_t *>(&hn);  // two bytes, little-endian
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      b[2 + k] = (idx[4 * k] & 3u) | ((idx[4 * k + 1] & 3u) << 2) | ((idx[4 * k + 2] & 3u) << 4) |
+                 ((idx[4 * k + 3] & 3u) << 6);
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      uint32_t sb8 = 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) sb8 |= (idx[8 * s + k] >> 2) << k;
+      b[10 + s] = sb8;
+    }
+    // the block starts at byte 14q: 2-byte aligned, so seven 16-bit stores
+    uint16_t *dst = reinterpret_cast<uint16_t *>(row + 14 * q);
+    dst[0] = (uint16_t)b[0];
+#pragma unroll
+    for (int k = 1; k < 7; ++k) dst[k] = (uint16_t)(b[2 * k] | (b[2 * k + 1] << 8));
+  }
+}
+
 template <int FMT, int SRC>
-__global__ void __launch_bounds__(WARPS * 32) k_write_wht(const WriteParams p) {
+__global__ void __launch_bounds__(WT_THREADS) k_write_wht(const WriteParams p) {
   constexpr int NB = (FMT == TQ_FMT_TURBO4) ? 15 : 7;
   constexpr int RB = (FMT == TQ_FMT_TURBO4) ? 68 : 56;
   __shared__ float sb[16];
-  __shared__ BucketTable grid;
-  __shared__ __align__(16) uint8_t rowbuf[WARPS][ROWBUF];
+  __shared__ float2 ce[GRID_CELLS];
   pdl_trigger();
   if (threadIdx.x < NB) sb[threadIdx.x] = p.b[threadIdx.x];
-  stage_grid(&grid, p.bt);
+  for (int t = threadIdx.x; t < GRID_CELLS; t += blockDim.x)
+    ce[t] = make_float2(p.bt->e[t], __uint_as_float((uint32_t)p.bt->cnt[t]));
+  const float gs = p.bt->scale, go = p.bt->offset;
+  const int gn = p.bt->n;
+  const int q = threadIdx.x & 3;
+  const uint32_t neg = p.wht_neg[q];
   __syncthreads();
   pdl_wait();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int64_t row = (int64_t)blockIdx.x * WARPS + warp; row < p.n_rows;
-       row += (int64_t)gridDim.x * WARPS) {
-    int64_t slot;
-    if (!slot_of(p, row, lane, &slot)) continue;
-    float v[4];
-    load4<SRC>(p.src, row, p.stride, lane, v);
-    const float n = norm_normalize(v);
-    wht_rotate(v, p.wht_neg, lane);
-    uint32_t idx[4];
+  // the four threads of a row stay together (whole warps iterate while any row is left);
+  // the next iteration's source quarter and slot are loaded before this one is encoded
+  const int64_t n_iter = (p.n_rows + 7) / 8;
+  const int64_t step = (int64_t)gridDim.x * (WT_THREADS / 32);
+  const int sub = (threadIdx.x & 31) >> 2;
+  int64_t it = (int64_t)blockIdx.x * (WT_THREADS / 32) + (threadIdx.x >> 5);
+  Quarter<SRC> raw;
+  int64_t slot_next = -1;
+  auto fetch = [&](int64_t i) {
+    const int64_t row = i * 8 + sub;
+    if (i < n_iter && row < p.n_rows) {
+      load_quarter<SRC>(p, row, q, raw);
+      slot_next = p.row_ids ? p.row_ids[row] : row;
+    }
+  };
+  fetch(it);
+  for (; it < n_iter; it += step) {
+    const int64_t row = it * 8 + sub;
+    const bool live = row < p.n_rows;
+    const int64_t slot = slot_next;
+    const bool ok = live && slot >= 0 && slot < p.dst_rows;
+    if (live && !ok && q == 0) atomicExch(p.status, (int32_t)DEVERR_ROW_OOB);
+    float v[WT_E];
+    if (ok) {
+      unpack_quarter(raw, v);
+    } else {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) idx[e] = nearest<NB>(v[e], grid, sb);
-    pack_store_turbo<FMT>(idx, n, rowbuf[warp], p.dst + slot * RB, lane);
+      for (int i = 0; i < WT_E; ++i) v[i] = 0.0f;
+    }
+    fetch(it + step);
+    const float n = quarter_norm_normalize(v);  // shuffles: every lane of the warp takes part
+    wht_quarter(v, neg, q);
+    if (ok) {
+      uint8_t *dst = p.dst + slot * RB;
+      if (gn)
+        pack_quarter<FMT, true>(v, n, ce, gs, go, gn, sb, dst, q);
+      else
+        pack_quarter<FMT, false>(v, n, ce, gs, go, gn, sb, dst, q);
+    }
   }
 }
 
@@ -467,6 +650,19 @@ cudaError_t launch_rows(K kernel, const WriteParams &p, int64_t n_rows, int num_
   return launch_pdl(kernel, dim3(grid), dim3(WARPS * 32), smem, st, p);
 }
 
+// The WHT kernel (four threads per row): as many resident CTAs as the rows need.
+template <typename K>
+cudaError_t launch_thread_rows(K kernel, const WriteParams &p, int64_t n_rows, int num_sms, cudaStream_t st) {
+  int resident = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, kernel, WT_THREADS, 0);
+  if (e != cudaSuccess) return e;
+  if (resident < 1) resident = 1;
+  const int64_t want = (n_rows + WT_THREADS / 4 - 1) / (WT_THREADS / 4);  // four threads per row
+  const int64_t cap = (int64_t)num_sms * resident;
+  const int grid = (int)(want < cap ? want : cap);
+  return launch_pdl(kernel, dim3(grid), dim3(WT_THREADS), 0, st, p);
+}
+
 }  // namespace
 
 cudaError_t launch_write(const tq_ctx *ctx, const WriteLaunch &w, cudaStream_t st) {
@@ -494,10 +690,10 @@ cudaError_t launch_write(const tq_ctx *ctx, const WriteLaunch &w, cudaStream_t s
                 : launch_rows(k_write_vgroup<TQ_DTYPE_F32>, p, w.n_rows, sms, 0, 8, st);
   if (ctx->p.rotation == TQ_ROT_WHT && fmt != TQ_FMT_PROD3) {
     if (fmt == TQ_FMT_TURBO4)
-      return bf16 ? launch_rows(k_write_wht<TQ_FMT_TURBO4, TQ_DTYPE_BF16>, p, w.n_rows, sms, 0, 8, st)
-                  : launch_rows(k_write_wht<TQ_FMT_TURBO4, TQ_DTYPE_F32>, p, w.n_rows, sms, 0, 8, st);
-    return bf16 ? launch_rows(k_write_wht<TQ_FMT_TURBO3, TQ_DTYPE_BF16>, p, w.n_rows, sms, 0, 8, st)
-                : launch_rows(k_write_wht<TQ_FMT_TURBO3, TQ_DTYPE_F32>, p, w.n_rows, sms, 0, 8, st);
+      return bf16 ? launch_thread_rows(k_write_wht<TQ_FMT_TURBO4, TQ_DTYPE_BF16>, p, w.n_rows, sms, st)
+                  : launch_thread_rows(k_write_wht<TQ_FMT_TURBO4, TQ_DTYPE_F32>, p, w.n_rows, sms, st);
+    return bf16 ? launch_thread_rows(k_write_wht<TQ_FMT_TURBO3, TQ_DTYPE_BF16>, p, w.n_rows, sms, st)
+                : launch_thread_rows(k_write_wht<TQ_FMT_TURBO3, TQ_DTYPE_F32>, p, w.n_rows, sms, st);
   }
   // Dense rotation on the tensor cores for 16-byte aligned bf16 rows (turbo4 / turbo3).
   if (write_tc_eligible(ctx, w)) return launch_write_tc(ctx, w, st);
