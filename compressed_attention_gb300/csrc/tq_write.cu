@@ -10,8 +10,8 @@
 // strides 16, 8, 4, 2, 1 of those 32 partial sums.  The WHT rotation is the
 // butterfly of stages 1, 2, ..., 64 in that order, so its result is bit-identical
 // to a plain sequential fp32 implementation of the same stage order.  The WHT
-// kernel gives each of four threads a quarter of a row; the others give lane l of
-// a warp elements 4l..4l+3 of its row and run the same trees across lanes.
+// kernel gives each of four threads four 8-element chunks of a row; the others give
+// lane l of a warp elements 4l..4l+3 of its row and run the same trees across lanes.
 #include "tq_device.cuh"
 #include "tq_internal.h"
 
@@ -156,70 +156,86 @@ __device__ __forceinline__ bool slot_of(const WriteParams &p, int64_t row, int l
 }
 
 // ------------------------------------------------------------------ WHT turbo4/turbo3
-// Four threads per row (a warp takes eight rows): thread q holds elements 32q .. 32q+31 in
-// registers, so the norm tree's strides 4, 2, 1 and the butterfly stages 1 .. 16 run inside
-// the thread and only two tree strides and two butterfly stages cross threads (shuffles
-// within the row's four lanes).  The operation order is the canonical one -- four-element
-// partial sums of squares combined over strides 16, 8, 4, 2, 1; butterfly stages of
-// distance 1, 2, ..., 64 with the lower element taking a + b and the upper a - b -- so every
-// value is bit-identical to a sequential fp32 implementation of the same order.  For
-// turbo3 each thread owns exactly one 14-byte block.
+// Four threads per row (a warp takes eight rows).  Thread q holds the four 8-element
+// chunks 32i + 8q .. 32i + 8q + 7 (i = 0..3) in registers, so one load instruction reads
+// 64 contiguous bytes of each row, the butterfly stages 1, 2, 4, 32, 64 and the norm
+// tree's strides 16, 8, 1 run inside the thread, and only butterfly stages 8, 16 and tree
+// strides 4, 2 cross threads (shuffles within the row's four lanes).  The operation order
+// is the canonical one -- four-element partial sums of squares combined over strides
+// 16, 8, 4, 2, 1; butterfly stages of distance 1, 2, ..., 64 with the lower element taking
+// a + b and the upper a - b -- so every value is bit-identical to a sequential fp32
+// implementation of the same order.  Register element 8i + e is row element 32i + 8q + e.
 constexpr int WT_THREADS = 256;
-constexpr int WT_E = 32;  // elements per thread
+constexpr int WT_E = 32;     // elements per thread
+constexpr int WT_REP = 16;   // copies of the grid table (one per half-warp lane)
 
-// A thread's quarter row as loaded (bf16 bits or fp32), kept while the previous row is
+// A thread's four chunks as loaded (bf16 bits or fp32), kept while the previous row is
 // encoded.
 template <int SRC>
 struct Quarter {
-  using T = uint2;  // four bf16 (8-byte aligned rows)
-  T w[WT_E / 4];
+  uint2 w[8];  // chunk i: w[2i], w[2i + 1] (eight bf16)
 };
 template <>
 struct Quarter<TQ_DTYPE_F32> {
-  using T = float4;  // 16-byte aligned rows
-  T w[WT_E / 4];
+  float4 w[8];  // chunk i: w[2i], w[2i + 1]
 };
 
+// v16: bf16 rows are 16-byte aligned (one 16-byte load per chunk); fp32 rows always are.
 template <int SRC>
-__device__ __forceinline__ void load_quarter(const WriteParams &p, int64_t row, int q, Quarter<SRC> &raw) {
-  using T = typename Quarter<SRC>::T;
-  const T *s = reinterpret_cast<const T *>(static_cast<const uint8_t *>(p.src) +
-                                           (row * p.stride + WT_E * q) * (SRC == TQ_DTYPE_F32 ? 4 : 2));
+__device__ __forceinline__ void load_quarter(const WriteParams &p, int64_t row, int q, bool v16,
+                                             Quarter<SRC> &raw) {
+  if constexpr (SRC == TQ_DTYPE_F32) {
+    const float4 *s = reinterpret_cast<const float4 *>(static_cast<const float *>(p.src) + row * p.stride + 8 * q);
 #pragma unroll
-  for (int i = 0; i < WT_E / 4; ++i) raw.w[i] = s[i];
+    for (int i = 0; i < 4; ++i) raw.w[2 * i] = s[8 * i], raw.w[2 * i + 1] = s[8 * i + 1];
+  } else if (v16) {
+    const uint4 *s = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.src) + row * p.stride + 8 * q);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 c = s[4 * i];
+      raw.w[2 * i] = make_uint2(c.x, c.y), raw.w[2 * i + 1] = make_uint2(c.z, c.w);
+    }
+  } else {
+    const uint2 *s = reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(p.src) + row * p.stride + 8 * q);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) raw.w[2 * i] = s[8 * i], raw.w[2 * i + 1] = s[8 * i + 1];
+  }
 }
 
 __device__ __forceinline__ void unpack_quarter(const Quarter<TQ_DTYPE_F32> &raw, float (&x)[WT_E]) {
 #pragma unroll
-  for (int i = 0; i < WT_E / 4; ++i)
-    x[4 * i] = raw.w[i].x, x[4 * i + 1] = raw.w[i].y, x[4 * i + 2] = raw.w[i].z, x[4 * i + 3] = raw.w[i].w;
+  for (int k = 0; k < 8; ++k)
+    x[4 * k] = raw.w[k].x, x[4 * k + 1] = raw.w[k].y, x[4 * k + 2] = raw.w[k].z, x[4 * k + 3] = raw.w[k].w;
 }
 __device__ __forceinline__ void unpack_quarter(const Quarter<TQ_DTYPE_BF16> &raw, float (&x)[WT_E]) {
 #pragma unroll
-  for (int i = 0; i < WT_E / 4; ++i) {
-    x[4 * i] = bf16_bits_to_f32(raw.w[i].x & 0xFFFFu), x[4 * i + 1] = bf16_bits_to_f32(raw.w[i].x >> 16);
-    x[4 * i + 2] = bf16_bits_to_f32(raw.w[i].y & 0xFFFFu), x[4 * i + 3] = bf16_bits_to_f32(raw.w[i].y >> 16);
+  for (int k = 0; k < 8; ++k) {
+    x[4 * k] = bf16_bits_to_f32(raw.w[k].x & 0xFFFFu), x[4 * k + 1] = bf16_bits_to_f32(raw.w[k].x >> 16);
+    x[4 * k + 2] = bf16_bits_to_f32(raw.w[k].y & 0xFFFFu), x[4 * k + 3] = bf16_bits_to_f32(raw.w[k].y >> 16);
   }
 }
 
 // Canonical fp32 norm of the row (the four threads end with the same value), then u = x / n
-// in place (u = 0 when n == 0).
+// in place (u = 0 when n == 0).  Group g = 8i + 2q + h of the row is register group 2i + h.
 __device__ __forceinline__ float quarter_norm_normalize(float (&x)[WT_E]) {
-  float s[8];  // partial sums of this thread's eight four-element groups (8q .. 8q+7)
+  float p[8];  // four-element partial sums of register groups 2i + h
 #pragma unroll
-  for (int g = 0; g < 8; ++g)
-    s[g] = __fadd_rn(__fadd_rn(__fmul_rn(x[4 * g], x[4 * g]), __fmul_rn(x[4 * g + 1], x[4 * g + 1])),
-                     __fadd_rn(__fmul_rn(x[4 * g + 2], x[4 * g + 2]), __fmul_rn(x[4 * g + 3], x[4 * g + 3])));
-  // stride 16: groups g and g + 16 sit in threads q and q ^ 2; stride 8: q and q ^ 1
+  for (int k = 0; k < 8; ++k)
+    p[k] = __fadd_rn(__fadd_rn(__fmul_rn(x[4 * k], x[4 * k]), __fmul_rn(x[4 * k + 1], x[4 * k + 1])),
+                     __fadd_rn(__fmul_rn(x[4 * k + 2], x[4 * k + 2]), __fmul_rn(x[4 * k + 3], x[4 * k + 3])));
+  float s[2];
 #pragma unroll
-  for (int g = 0; g < 8; ++g) s[g] = __fadd_rn(s[g], __shfl_xor_sync(FULL_MASK, s[g], 2));
+  for (int h = 0; h < 2; ++h) {
+    // stride 16 (chunk i + 2) and stride 8 (chunk i + 1), in this thread
+    const float s16a = __fadd_rn(p[h], p[4 + h]), s16b = __fadd_rn(p[2 + h], p[6 + h]);
+    s[h] = __fadd_rn(s16a, s16b);
+  }
+  // stride 4: threads q and q ^ 2; stride 2: q and q ^ 1; stride 1: h = 0 and 1 here
 #pragma unroll
-  for (int g = 0; g < 8; ++g) s[g] = __fadd_rn(s[g], __shfl_xor_sync(FULL_MASK, s[g], 1));
+  for (int h = 0; h < 2; ++h) s[h] = __fadd_rn(s[h], __shfl_xor_sync(FULL_MASK, s[h], 2));
 #pragma unroll
-  for (int h = 4; h >= 1; h >>= 1)
-#pragma unroll
-    for (int g = 0; g < h; ++g) s[g] = __fadd_rn(s[g], s[g + h]);
-  const float n = __fsqrt_rn(s[0]);
+  for (int h = 0; h < 2; ++h) s[h] = __fadd_rn(s[h], __shfl_xor_sync(FULL_MASK, s[h], 1));
+  const float n = __fsqrt_rn(__fadd_rn(s[0], s[1]));
   const float r = __frcp_rn(n);
   // Markstein's correction is exact when every nonzero |x| >= 2^-100 and n <= 2^24 (then
   // |q| >= 2^-124 and 1/n is normal); zeros come out as zeros.  Otherwise the guarded
@@ -244,93 +260,99 @@ __device__ __forceinline__ float quarter_norm_normalize(float (&x)[WT_E]) {
   return n;
 }
 
-// Randomized Hadamard of the row: sign flips (bit j of neg for element j), the butterfly,
-// times RN(1/sqrt(128)); thread q holds elements 32q .. 32q+31 (sign word q).
-__device__ __forceinline__ void wht_quarter(float (&v)[WT_E], uint32_t neg, int q) {
+// Randomized Hadamard of the row: sign flips (bit j % 32 of word j / 32 for row element j;
+// nq[i] = sign word i shifted down by 8q), the butterfly, times RN(1/sqrt(128)).
+__device__ __forceinline__ void wht_quarter(float (&v)[WT_E], const uint32_t (&nq)[4], int q) {
 #pragma unroll
-  for (int i = 0; i < WT_E; ++i)
-    v[i] = __uint_as_float(__float_as_uint(v[i]) ^ ((neg << (31 - i)) & 0x80000000u));
+  for (int i = 0; i < 4; ++i)
 #pragma unroll
-  for (int h = 1; h < WT_E; h <<= 1)
+    for (int e = 0; e < 8; ++e)
+      v[8 * i + e] = __uint_as_float(__float_as_uint(v[8 * i + e]) ^ ((nq[i] << (31 - e)) & 0x80000000u));
+  auto stage = [&](int h, int hr) {  // row distance h = register distance hr, in this thread
 #pragma unroll
-    for (int i = 0; i < WT_E; ++i)
-      if (!(i & h)) {
-        const float a = v[i], b = v[i + h];
-        v[i] = __fadd_rn(a, b);
-        v[i + h] = __fsub_rn(a, b);
+    for (int k = 0; k < WT_E; ++k)
+      if (!(k & hr)) {
+        const float a = v[k], b = v[k + hr];
+        v[k] = __fadd_rn(a, b);
+        v[k + hr] = __fsub_rn(a, b);
       }
-  // distances 32 and 64: partner thread q ^ 1, then q ^ 2; the lower one keeps v + o, the
+    (void)h;
+  };
+  stage(1, 1);
+  stage(2, 2);
+  stage(4, 4);
+  // distances 8 and 16: partner thread q ^ 1, then q ^ 2; the lower one keeps v + o, the
   // upper one o - v, both as one fused o + (+-1) v (the product by +-1 is exact)
 #pragma unroll
   for (int m = 1; m <= 2; m <<= 1) {
     const float sgn = (q & m) ? -1.0f : 1.0f;
 #pragma unroll
-    for (int i = 0; i < WT_E; ++i) {
-      const float o = __shfl_xor_sync(FULL_MASK, v[i], m);
-      v[i] = __fmaf_rn(sgn, v[i], o);
+    for (int k = 0; k < WT_E; ++k) {
+      const float o = __shfl_xor_sync(FULL_MASK, v[k], m);
+      v[k] = __fmaf_rn(sgn, v[k], o);
     }
   }
+  stage(32, 8);
+  stage(64, 16);
   const float inv_sqrt_d = __int_as_float(0x3DB504F3);  // fp32 nearest 1/sqrt(128)
 #pragma unroll
-  for (int i = 0; i < WT_E; ++i) v[i] = __fmul_rn(v[i], inv_sqrt_d);
+  for (int k = 0; k < WT_E; ++k) v[k] = __fmul_rn(v[k], inv_sqrt_d);
 }
 
-// #{k : y > b_k}: the grid (cell t: boundary ce[t].x, count ce[t].y as integer bits) or,
+// #{k : y > b_k}: the grid (copy l16 of cell t: boundary .x, count .y as integer bits) or,
 // without GRID, binary search over the NB boundaries.
 template <bool GRID, int NB>
-__device__ __forceinline__ uint32_t cell_index(float y, const float2 *ce, float gs, float go, int gn,
+__device__ __forceinline__ uint32_t cell_index(float y, const float2 *ce, int l16, float gs, float go, int gn,
                                                const float *sb) {
   if (GRID) {
     int t = __float2int_rd(fmaf(y, gs, go));  // NaN -> 0, +-inf -> saturated
     t = min(max(t, 0), gn - 1);
-    const float2 c = ce[t];
+    const float2 c = ce[t * WT_REP + l16];
     return __float_as_uint(c.y) + (y > c.x ? 1u : 0u);
   }
   return bucket<NB>(y, sb);
 }
 
-// Nearest-centroid indices of this thread's 32 rotated elements, packed into its part of
-// the row record at row (4-byte aligned): turbo4 = fp32 norm + 64 nibble bytes (thread q:
-// bytes 4 + 16q .. 4 + 16q + 15, thread 0 also the norm); turbo3 = four 14-byte blocks
-// {fp16 norm, qs[8] (low two index bits of element j at bits 2 (j % 4) of qs[j / 4]),
-// signs[4] (high bit at bit j % 8 of signs[j / 8])}, block q from thread q.
+// Nearest-centroid indices of this thread's elements, packed into its part of the row
+// record at row (4-byte aligned).  turbo4 (fp32 norm + 64 nibble bytes): chunk i fills
+// word 1 + 4i + q; thread 0 writes the norm.  turbo3 (four 14-byte blocks {fp16 norm,
+// qs[8] with the low two index bits of block element j at bits 2 (j % 4) of qs[j / 4],
+// signs[4] with the high bit at bit j % 8 of signs[j / 8]}): chunk i is elements
+// 8q .. 8q+7 of block i, i.e. qs[2q], qs[2q + 1] and signs[q].
 template <int FMT, bool GRID>
-__device__ __forceinline__ void pack_quarter(const float (&y)[WT_E], float n, const float2 *ce, float gs,
-                                             float go, int gn, const float *sb, uint8_t *row, int q) {
+__device__ __forceinline__ void pack_quarter(const float (&y)[WT_E], float n, const float2 *ce, int l16,
+                                             float gs, float go, int gn, const float *sb, uint8_t *row,
+                                             int q) {
   constexpr int NB = (FMT == TQ_FMT_TURBO4) ? 15 : 7;
   if (FMT == TQ_FMT_TURBO4) {
-    uint32_t *dst = reinterpret_cast<uint32_t *>(row) + 1 + 4 * q;
-    if (q == 0) reinterpret_cast<uint32_t *>(row)[0] = __float_as_uint(n);
+    uint32_t *w = reinterpret_cast<uint32_t *>(row);
+    if (q == 0) w[0] = __float_as_uint(n);
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
+    for (int i = 0; i < 4; ++i) {
       uint32_t word = 0;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) word |= cell_index<GRID, NB>(y[8 * w + i], ce, gs, go, gn, sb) << (4 * i);
-      dst[w] = word;
+      for (int e = 0; e < 8; ++e) word |= cell_index<GRID, NB>(y[8 * i + e], ce, l16, gs, go, gn, sb) << (4 * e);
+      w[1 + 4 * i + q] = word;
     }
   } else {
-    uint32_t idx[WT_E];
-#pragma unroll
-    for (int e = 0; e < WT_E; ++e) idx[e] = cell_index<GRID, NB>(y[e], ce, gs, go, gn, sb);
     const __half hn = __float2half_rn(n);
-    uint32_t b[14];
-    b[0] = *reinterpret_cast<const uint16_t *>(&hn);  // two bytes, little-endian
+    const uint16_t nb = *reinterpret_cast<const uint16_t *>(&hn);
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
-      b[2 + k] = (idx[4 * k] & 3u) | ((idx[4 * k + 1] & 3u) << 2) | ((idx[4 * k + 2] & 3u) << 4) |
-                 ((idx[4 * k + 3] & 3u) << 6);
+    for (int i = 0; i < 4; ++i) {
+      uint32_t idx[8];
 #pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      uint32_t sb8 = 0;
+      for (int e = 0; e < 8; ++e) idx[e] = cell_index<GRID, NB>(y[8 * i + e], ce, l16, gs, go, gn, sb);
+      uint32_t lo = 0, sg = 0;  // qs[2q] | qs[2q + 1] << 8, signs[q]
 #pragma unroll
-      for (int k = 0; k < 8; ++k) sb8 |= (idx[8 * s + k] >> 2) << k;
-      b[10 + s] = sb8;
+      for (int e = 0; e < 8; ++e) {
+        lo |= (idx[e] & 3u) << (2 * e);
+        sg |= (idx[e] >> 2) << e;
+      }
+      uint8_t *blk = row + 14 * i;  // 2-byte aligned
+      if (q == 0) *reinterpret_cast<uint16_t *>(blk) = nb;
+      *reinterpret_cast<uint16_t *>(blk + 2 + 2 * q) = (uint16_t)lo;
+      blk[10 + q] = (uint8_t)sg;
     }
-    // the block starts at byte 14q: 2-byte aligned, so seven 16-bit stores
-    uint16_t *dst = reinterpret_cast<uint16_t *>(row + 14 * q);
-    dst[0] = (uint16_t)b[0];
-#pragma unroll
-    for (int k = 1; k < 7; ++k) dst[k] = (uint16_t)(b[2 * k] | (b[2 * k + 1] << 8));
   }
 }
 
@@ -339,19 +361,24 @@ __global__ void __launch_bounds__(WT_THREADS) k_write_wht(const WriteParams p) {
   constexpr int NB = (FMT == TQ_FMT_TURBO4) ? 15 : 7;
   constexpr int RB = (FMT == TQ_FMT_TURBO4) ? 68 : 56;
   __shared__ float sb[16];
-  __shared__ float2 ce[GRID_CELLS];
+  __shared__ float2 ce[GRID_CELLS * WT_REP];  // cell t, copy c at t * 16 + c
   pdl_trigger();
   if (threadIdx.x < NB) sb[threadIdx.x] = p.b[threadIdx.x];
-  for (int t = threadIdx.x; t < GRID_CELLS; t += blockDim.x)
-    ce[t] = make_float2(p.bt->e[t], __uint_as_float((uint32_t)p.bt->cnt[t]));
+  for (int k = threadIdx.x; k < GRID_CELLS * WT_REP; k += blockDim.x) {
+    const int t = k / WT_REP;
+    ce[k] = make_float2(p.bt->e[t], __uint_as_float((uint32_t)p.bt->cnt[t]));
+  }
   const float gs = p.bt->scale, go = p.bt->offset;
   const int gn = p.bt->n;
-  const int q = threadIdx.x & 3;
-  const uint32_t neg = p.wht_neg[q];
+  const int q = threadIdx.x & 3, l16 = threadIdx.x & 15;
+  uint32_t nq[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) nq[i] = p.wht_neg[i] >> (8 * q);
+  const bool v16 = ((uintptr_t)p.src & 15) == 0 && ((p.stride * 2) & 15) == 0;
   __syncthreads();
   pdl_wait();
   // the four threads of a row stay together (whole warps iterate while any row is left);
-  // the next iteration's source quarter and slot are loaded before this one is encoded
+  // the next iteration's source chunks and slot are loaded before this one is encoded
   const int64_t n_iter = (p.n_rows + 7) / 8;
   const int64_t step = (int64_t)gridDim.x * (WT_THREADS / 32);
   const int sub = (threadIdx.x & 31) >> 2;
@@ -361,7 +388,7 @@ __global__ void __launch_bounds__(WT_THREADS) k_write_wht(const WriteParams p) {
   auto fetch = [&](int64_t i) {
     const int64_t row = i * 8 + sub;
     if (i < n_iter && row < p.n_rows) {
-      load_quarter<SRC>(p, row, q, raw);
+      load_quarter<SRC>(p, row, q, v16, raw);
       slot_next = p.row_ids ? p.row_ids[row] : row;
     }
   };
@@ -381,13 +408,13 @@ __global__ void __launch_bounds__(WT_THREADS) k_write_wht(const WriteParams p) {
     }
     fetch(it + step);
     const float n = quarter_norm_normalize(v);  // shuffles: every lane of the warp takes part
-    wht_quarter(v, neg, q);
+    wht_quarter(v, nq, q);
     if (ok) {
       uint8_t *dst = p.dst + slot * RB;
       if (gn)
-        pack_quarter<FMT, true>(v, n, ce, gs, go, gn, sb, dst, q);
+        pack_quarter<FMT, true>(v, n, ce, l16, gs, go, gn, sb, dst, q);
       else
-        pack_quarter<FMT, false>(v, n, ce, gs, go, gn, sb, dst, q);
+        pack_quarter<FMT, false>(v, n, ce, l16, gs, go, gn, sb, dst, q);
     }
   }
 }
