@@ -59,11 +59,14 @@ def canonical_norm_fp32(x):
     x32 = np.asarray(x, dtype=np.float32)
     if x32.shape[-1] != 128:
         raise ValueError("the canonical norm tree is defined for d = 128")
-    sq = x32 * x32
-    p = (sq[:, 0::4] + sq[:, 1::4]) + (sq[:, 2::4] + sq[:, 3::4])  # [N, 32], one per lane
-    lanes = np.arange(32)
-    for h in (16, 8, 4, 2, 1):
-        p = p + p[:, lanes ^ h]
+    # rows whose squares or sums exceed the fp32 range give n = inf, as fp32 arithmetic
+    # defines (the extreme-magnitude test rows do this on purpose)
+    with np.errstate(over="ignore"):
+        sq = x32 * x32
+        p = (sq[:, 0::4] + sq[:, 1::4]) + (sq[:, 2::4] + sq[:, 3::4])  # [N, 32], one per lane
+        lanes = np.arange(32)
+        for h in (16, 8, 4, 2, 1):
+            p = p + p[:, lanes ^ h]
     return np.sqrt(p[:, 0]).astype(np.float32)
 
 
@@ -165,7 +168,8 @@ def pack_turbo3(n32, idx):
     """[turbo4 post-mortem] section 4 "2+1" layout, four 14-byte blocks per 128-vector."""
     N = len(n32)
     out = np.zeros((N, 56), dtype=np.uint8)
-    n16 = np.asarray(n32, dtype=np.float32).astype("<f2").reshape(N, 1).view(np.uint8)
+    with np.errstate(over="ignore"):  # norms above the fp16 range store fp16 inf
+        n16 = np.asarray(n32, dtype=np.float32).astype("<f2").reshape(N, 1).view(np.uint8)
     idx = np.asarray(idx, dtype=np.uint8)
     for c in range(4):
         base = 14 * c
