@@ -543,8 +543,10 @@ __global__ void __launch_bounds__(WARPS * 32) k_write_dense(const WriteParams p)
 
 // ---------------------------------------- dense rotation, small batches (one CTA per row)
 // For the few rows of a decode step: thread j computes output coordinate j from row j
-// of R read straight from L2 (no 64 KB staging), so the launch costs about one memory
-// latency.  Norm, normalisation and packing follow the same canonical order as above.
+// of R read straight from L2 (no 64 KB staging) into registers before the wait on the
+// previous kernel (R belongs to the immutable context), so after that wait the launch
+// costs about one memory latency.  Norm, normalisation and packing follow the same
+// canonical order as above.
 template <int FMT, int SRC>
 __global__ void __launch_bounds__(D) k_write_dense_row(const WriteParams p) {
   constexpr int NB = (FMT == TQ_FMT_TURBO4) ? 15 : 7;
@@ -562,6 +564,10 @@ __global__ void __launch_bounds__(D) k_write_dense_row(const WriteParams p) {
     for (int k = 0; k < NB; ++k) sb[k] = p.b[k];  // constant indices keep p in parameter space
   }
   stage_grid(&grid, p.bt);
+  const float4 *r4 = reinterpret_cast<const float4 *>(p.pi + (size_t)j * D);  // row j of R
+  float4 rr[D / 4];
+#pragma unroll
+  for (int k4 = 0; k4 < D / 4; ++k4) rr[k4] = r4[k4];
   pdl_trigger();
   pdl_wait();
   const int64_t slot = p.row_ids ? p.row_ids[row] : row;
@@ -590,11 +596,10 @@ __global__ void __launch_bounds__(D) k_write_dense_row(const WriteParams p) {
   const float n = nsh;
   u[j] = (n == 0.0f) ? 0.0f : __fdiv_rn(x, n);
   __syncthreads();
-  const float4 *r4 = reinterpret_cast<const float4 *>(p.pi + (size_t)j * D);  // row j of R
   float y = 0.f;
-#pragma unroll 8
+#pragma unroll
   for (int k4 = 0; k4 < D / 4; ++k4) {
-    const float4 r = r4[k4];
+    const float4 r = rr[k4];
     y = fmaf(r.x, u[4 * k4], y);
     y = fmaf(r.y, u[4 * k4 + 1], y);
     y = fmaf(r.z, u[4 * k4 + 2], y);
