@@ -468,6 +468,36 @@ def timed_graph_steps(torch, stream, fns, steps, warmup, flush_l2):
     return [e0.elapsed_time(e1) for e0, e1 in ev]
 
 
+E2E_MODE = ("each step one replay of a CUDA graph of the public API calls with the copies; "
+            "direct_ms_per_step: the same calls issued one by one")
+
+
+def timed_e2e(torch, body, steps, warmup, flush_l2):
+    """End-to-end step times (ms, host clock) of `body`: the host-to-device copies of the
+    step's inputs from pinned memory, the public API calls and the device-to-host read of
+    the result.  Returns (graph, direct): each step one replay of a CUDA graph captured
+    from `body` (how a serving loop issues a step), and `body` called directly (host
+    enqueue of every copy and call inside the timed region).  Each step starts with the
+    L2 flushed and the device idle and ends with a host synchronisation."""
+    def run(step):
+        out = []
+        for i in range(warmup + steps):
+            flush_l2()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            step()
+            torch.cuda.synchronize()
+            if i >= warmup:
+                out.append((time.perf_counter() - t0) * 1e3)
+        return out
+
+    direct = run(body)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        body()
+    return run(g.replay), direct
+
+
 def common_line(metric, args, world, ms_per_step, value, config, dtype):
     return {"metric": metric, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -524,20 +554,15 @@ def run_decode(args, rank, world, dist):
     hout = torch.empty(w["out"].shape, dtype=torch.float32, pin_memory=True)
     h2d = sum(t.numel() * t.element_size() for t in pinned.values())
     d2h = hout.numel() * 4
-    e2e_ms = []
-    for i in range(args.warmup + args.steps):
-        flush_l2()
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
+    def e2e_body():
         for k, t in pinned.items():
             w[k].copy_(t, non_blocking=True)
         tq.tq_quantize_set_rows(w["kctx"], w["new_k"], w["kc"], row_ids=w["slots"])
         tq.tq_quantize_set_rows(w["vctx"], w["new_v"], w["vc"], row_ids=w["slots"])
         tq.tq_decode_attention(w["kctx"], w["vctx"], w["q"], w["kc"], w["vc"], w["out"], w["ws"], B, Hq, Hkv, L)
         hout.copy_(w["out"], non_blocking=True)
-        torch.cuda.synchronize()
-        if i >= args.warmup:
-            e2e_ms.append((time.perf_counter() - t0) * 1e3)
+
+    e2e_ms, e2e_direct_ms = timed_e2e(torch, e2e_body, args.steps, args.warmup, flush_l2)
     status = tq.tq_ctx_device_status(w["kctx"]) or tq.tq_ctx_device_status(w["vctx"])
     if status:
         raise RuntimeError(f"device status {status} after the benchmark")
@@ -549,6 +574,7 @@ def run_decode(args, rank, world, dist):
     peak, peak_kind = measured_peak()
     achieved = kv_bytes / (part_avg * 1e-3) / 1e9
     e2e_step_ms = max_over_ranks(statistics.mean(e2e_ms), dist, device)
+    e2e_direct_step_ms = max_over_ranks(statistics.mean(e2e_direct_ms), dist, device)
     if rank != 0:
         return
     cpu = None
@@ -572,7 +598,8 @@ def run_decode(args, rank, world, dist):
                      "algorithmic_bytes_per_launch": kv_bytes, "avg_launch_ms": part_avg},
         "cpu_baseline": cpu,
         "e2e": {"value": job_rate(alg_bytes, world, e2e_step_ms) / 1e9, "unit": "GB/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step_ms},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step_ms,
+                "mode": E2E_MODE, "direct_ms_per_step": e2e_direct_step_ms},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     })
@@ -650,20 +677,15 @@ def run_prefill(args, rank, world, dist):
     hout = torch.empty(out.shape, dtype=torch.float32, pin_memory=True)
     h2d = sum(t.numel() * t.element_size() for t in pinned.values())
     d2h = hout.numel() * 4
-    e2e_ms = []
-    for i in range(args.warmup + args.steps):
-        flush_l2()
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
+    def e2e_body():
         for k, t in pinned.items():
             host[k].copy_(t, non_blocking=True)
         tq.tq_quantize_set_rows(kctx, chunk["K"], kc, row_ids=slots)
         tq.tq_quantize_set_rows(vctx, chunk["V"], vc, row_ids=slots)
         tq.tq_prefill_attention(kctx, vctx, q, kc, vc, q_start, out, ws, B, T, Hq, Hkv, L)
         hout.copy_(out, non_blocking=True)
-        torch.cuda.synchronize()
-        if i >= args.warmup:
-            e2e_ms.append((time.perf_counter() - t0) * 1e3)
+
+    e2e_ms, e2e_direct_ms = timed_e2e(torch, e2e_body, args.steps, args.warmup, flush_l2)
     if tq.tq_ctx_device_status(kctx) or tq.tq_ctx_device_status(vctx):
         raise RuntimeError("device status set after the benchmark")
 
@@ -673,6 +695,7 @@ def run_prefill(args, rank, world, dist):
     peak, peak_kind = measured_tensor_peak()
     achieved = flops / (part_avg * 1e-3) / 1e12
     e2e_step_ms = max_over_ranks(statistics.mean(e2e_ms), dist, device)
+    e2e_direct_step_ms = max_over_ranks(statistics.mean(e2e_direct_ms), dist, device)
     if rank != 0:
         return
     cpu = None
@@ -702,7 +725,8 @@ def run_prefill(args, rank, world, dist):
                      "algorithmic_flops_per_launch": flops, "avg_launch_ms": part_avg},
         "cpu_baseline": cpu,
         "e2e": {"value": job_rate(flops, world, e2e_step_ms) / 1e12, "unit": "TFLOP/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step_ms},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step_ms,
+                "mode": E2E_MODE, "direct_ms_per_step": e2e_direct_step_ms},
         "gpu_launches": 5 * args.steps,
         "clocks": clk,
     })
@@ -750,20 +774,15 @@ def run_write(args, rank, world, dist):
     hc = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in caches.items()}
     h2d = sum(t.numel() * t.element_size() for t in hx.values())
     d2h = sum(t.numel() * t.element_size() for t in hc.values())
-    e2e_ms = []
-    for i in range(args.warmup + args.steps):
-        flush_l2()
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
+    def e2e_body():
         for k in ("K", "V"):
             x[k].copy_(hx[k], non_blocking=True)
         tq.tq_quantize_set_rows(kctx, x["K"], caches["K"])
         tq.tq_quantize_set_rows(vctx, x["V"], caches["V"])
         for k in ("K", "V"):
             hc[k].copy_(caches[k], non_blocking=True)
-        torch.cuda.synchronize()
-        if i >= args.warmup:
-            e2e_ms.append((time.perf_counter() - t0) * 1e3)
+
+    e2e_ms, e2e_direct_ms = timed_e2e(torch, e2e_body, args.steps, args.warmup, flush_l2)
     if tq.tq_ctx_device_status(kctx) or tq.tq_ctx_device_status(vctx):
         raise RuntimeError("device status set after the benchmark")
 
@@ -774,6 +793,7 @@ def run_write(args, rank, world, dist):
     value = job_rate(alg_bytes, world, ms_per_step) / 1e9
     peak, peak_kind = measured_peak()
     e2e_step_ms = max_over_ranks(statistics.mean(e2e_ms), dist, device)
+    e2e_direct_step_ms = max_over_ranks(statistics.mean(e2e_direct_ms), dist, device)
     if rank != 0:
         return
     cpu = None
@@ -794,7 +814,8 @@ def run_write(args, rank, world, dist):
                      "algorithmic_bytes_per_launch": launch_bytes, "avg_launch_ms": launch_avg},
         "cpu_baseline": cpu,
         "e2e": {"value": job_rate(alg_bytes, world, e2e_step_ms) / 1e9, "unit": "GB/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step_ms},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step_ms,
+                "mode": E2E_MODE, "direct_ms_per_step": e2e_direct_step_ms},
         "gpu_launches": 2 * args.steps,
         "clocks": clk,
     })
