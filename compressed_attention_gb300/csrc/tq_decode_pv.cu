@@ -261,9 +261,13 @@ __global__ void __maxnreg__(168) k_partial_pv(const PvParams p) {
       const int nkb = nk - kb;
       if (nkb > 0) {
         // ---- scores of two 8-key blocks: MSE and QJL products
-        float cm[2][4], cq[2][4];
+        // even and odd k-steps accumulate separately (two chains of four dependent MMAs
+        // each instead of one of eight), summed once after the loop
+        float cm[2][2][4], cq[2][2][4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) cm[0][e] = cm[1][e] = cq[0][e] = cq[1][e] = 0.f;
+        for (int e = 0; e < 4; ++e)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) cm[h][0][e] = cm[h][1][e] = cq[h][0][e] = cq[h][1][e] = 0.f;
         const uint2 m0 = lds64(Ks + kr0 * K_ROW + 8 + 8 * t), m1 = lds64(Ks + kr1 * K_ROW + 8 + 8 * t);
         const uint32_t sw0 = lds32(Ks + kr0 * K_ROW + 40 + 4 * t), sw1 = lds32(Ks + kr1 * K_ROW + 40 + 4 * t);
         const uint32_t ev0 = sw0 & 0x0F0F0F0Fu, od0 = (sw0 >> 4) & 0x0F0F0F0Fu;
@@ -281,10 +285,10 @@ __global__ void __maxnreg__(168) k_partial_pv(const PvParams p) {
           lut2<FIXED, LUT_WINDOW>(mse_base, om1, b10, b11);
           lut2<FIXED, SIGN_WINDOW>(sign_base, on0, s00, s01);
           lut2<FIXED, SIGN_WINDOW>(sign_base, on1, s10, s11);
-          mma_f16(cm[0], qa[st], b00, b01);
-          mma_f16(cm[1], qa[st], b10, b11);
-          mma_f16(cq[0], qq[st], s00, s01);
-          mma_f16(cq[1], qq[st], s10, s11);
+          mma_f16(cm[st & 1][0], qa[st], b00, b01);
+          mma_f16(cm[st & 1][1], qa[st], b10, b11);
+          mma_f16(cq[st & 1][0], qq[st], s00, s01);
+          mma_f16(cq[st & 1][1], qq[st], s10, s11);
         }
         // ---- online softmax for head g over keys ks[0..3]
         float sc[4], u[4], tn[4];
@@ -303,8 +307,8 @@ __global__ void __maxnreg__(168) k_partial_pv(const PvParams p) {
           const int nu = (int)((mb >> 10) & 0x1Fu) - 14;
           tn[i] = __uint_as_float((uint32_t)(127 - nu) << 23);
           const int nb = i >> 1, e = i & 1;
-          const float mse = cm[nb][e] + cm[nb][2 + e];
-          const float qjl = cq[nb][e] + cq[nb][2 + e];
+          const float mse = (cm[0][nb][e] + cm[0][nb][2 + e]) + (cm[1][nb][e] + cm[1][nb][2 + e]);
+          const float qjl = (cq[0][nb][e] + cq[0][nb][2 + e]) + (cq[1][nb][e] + cq[1][nb][2 + e]);
           sc[i] = ok[i] ? ng.x * fmaf(ng.y * qsq, qjl, qsm * mse) : -INFINITY;
           u[i] = sc[i] + (float)nu;
           if (SCORES && ok[i] && g < G)
