@@ -9,7 +9,8 @@ that argument for every (format, codebook) the library offers, and the end effec
 attention outputs (cosine against exact fp64 attention over the uncompressed K and V,
 the quality side-metric of the method's write-ups).
 
-Run ``python -m oracle.quality`` for the table.  Inputs are seeded synthetic draws
+Run ``python -m oracle.quality`` for the tables (the second compares head dimensions
+64, 128 and 256 with a codebook built for each).  Inputs are seeded synthetic draws
 (``synth``); no dataset is used.
 """
 
@@ -81,6 +82,34 @@ def output_cosine(kcodec, vcodec, L=2048, Hq=4, seed=0, lognormal=True):
     return float(cos.mean()), float(cos.min())
 
 
+def head_dim_logit_error(d, bits=4, kind="lloyd", n_keys=4096, n_queries=64, seed=0):
+    """Logit error of a d-dimensional head quantized as one block: a seeded dense rotation
+    of the whole head (QR of a Gaussian matrix), nearest-centroid coding of every rotated
+    coordinate with the codebook built for dimension d (the "per-head-dim codebook" of
+    [turbo4 post-mortem] section 9), the norm kept exactly.  Keys are unit vectors,
+    queries N(0, 1) rows, logits q.k / sqrt(d).  Returns (mse_per_element * d,
+    var_logit_error, predicted = E|q|^2 mse / d).
+
+    This is a study of the quality argument at other head dimensions; the packed formats
+    and the GPU path are defined for d = 128."""
+    from .codebook import make_codebook, stored_codebook
+
+    rng = np.random.default_rng([seed, 13, d])
+    rot, rr = np.linalg.qr(rng.standard_normal((d, d)))
+    rot = rot * np.sign(np.diag(rr))  # unique orthogonal factor (diag(R) > 0)
+    c32, b32 = stored_codebook(make_codebook(bits, d, kind))
+    k = rng.standard_normal((n_keys, d))
+    k /= np.linalg.norm(k, axis=1, keepdims=True)
+    q = rng.standard_normal((n_queries, d))
+    y = k @ rot.T
+    idx = np.sum(y[:, :, None] > b32.astype(np.float64)[None, None, :], axis=2)
+    k_hat = c32.astype(np.float64)[idx] @ rot
+    e = k_hat - k
+    mse = float(np.mean(e * e))
+    dl = (q @ e.T) / math.sqrt(d)
+    return mse * d, float(np.var(dl)), float(np.mean(np.sum(q * q, axis=1)) * mse / d)
+
+
 def report(seed=0):
     """Rows of (label, MSE x d, Var(delta logit), predicted, cosine mean, cosine min); values
     use the same format for K and V except prod3 keys, which pair with vgroup2 values."""
@@ -103,6 +132,13 @@ def main():
     for label, msed, var, pred, cmean, cmin in report():
         vals = "vgroup2" if label.startswith("prod3") else label.split()[0] + " " + label.split()[1]
         print(f"| {label} ({vals}) | {msed:.5f} | {var:.3e} | {pred:.3e} | {cmean:.6f} | {cmin:.6f} |")
+    print()
+    print("| head dim | bits | MSE x d | Var(delta logit) | |q|^2 MSE / d |")
+    print("|---|---|---|---|---|")
+    for d in (64, 128, 256):
+        for bits in (4, 3):
+            msed, var, pred = head_dim_logit_error(d, bits)
+            print(f"| {d} | {bits} | {msed:.5f} | {var:.3e} | {pred:.3e} |")
 
 
 if __name__ == "__main__":

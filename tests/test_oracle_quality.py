@@ -56,3 +56,16 @@ def test_output_cosine_orders_formats():
             cos[label] = quality.output_cosine(kc, vc, L=1024, seed=9)[0]
     assert cos["turbo4 lloyd"] > cos["turbo3 lloyd"] > cos["prod3 lloyd"]
     assert cos["turbo4 lloyd"] > 0.97
+
+
+@pytest.mark.parametrize("bits,levels", [(4, 16), (3, 8)])
+def test_head_dim_256_halves_the_logit_noise(bits, levels):
+    """[turbo4 post-mortem] section 9: with a codebook built for each head dimension, the
+    per-element error times d is the same Gaussian distortion (Max's table), so the logit
+    error variance |q|^2 MSE / d halves from d = 128 to d = 256."""
+    r = {d: quality.head_dim_logit_error(d, bits, n_keys=2048, n_queries=48, seed=5) for d in (128, 256)}
+    for d, (msed, var, pred) in r.items():
+        assert abs(msed - max_distortion(levels)) / max_distortion(levels) < 0.03, d
+        assert abs(var - pred) / pred < 0.06, d
+    ratio = r[128][1] / r[256][1]
+    assert 1.8 < ratio < 2.2
