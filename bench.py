@@ -519,18 +519,17 @@ def run_decode(args, rank, world, dist):
     stream = torch.cuda.current_stream()
     flush_l2 = flusher(torch, device)
 
-    def write_and_prepare():
+    def write():
         tq.tq_quantize_set_rows(w["kctx"], w["new_k"], w["kc"], row_ids=w["slots"])
         tq.tq_quantize_set_rows(w["vctx"], w["new_v"], w["vc"], row_ids=w["slots"])
-        tq.tq_decode_prepare_q(w["kctx"], w["vctx"], w["q"], w["ws"], B, Hq, Hkv, L)
+
+    def attention():  # q preparation, split-K decode (with the merge fused where it applies)
+        tq.tq_decode_attention(w["kctx"], w["vctx"], w["q"], w["kc"], w["vc"], w["out"], w["ws"], B, Hq, Hkv, L)
 
     def partial():
         tq.tq_decode_partial(w["kctx"], w["vctx"], w["kc"], w["vc"], w["ws"], B, Hq, Hkv, L)
 
-    def combine():
-        tq.tq_decode_combine(w["kctx"], w["vctx"], w["out"], w["ws"], B, Hq, Hkv, L)
-
-    launches_per_step = 5
+    launches_per_step = 2 + tq.tq_decode_num_launches(w["kctx"], w["vctx"], B, Hq, Hkv, L)
     if dist:
         dist.barrier()
     with ClockSampler(local) as clocks:
@@ -538,8 +537,7 @@ def run_decode(args, rank, world, dist):
         if dist:
             dist.barrier()
         # the step, then the decode kernel alone (the roofline), same workload and flushes
-        step_ms = timed_graph_steps(torch, stream, (write_and_prepare, partial, combine), args.steps,
-                                    args.warmup, flush_l2)
+        step_ms = timed_graph_steps(torch, stream, (write, attention), args.steps, args.warmup, flush_l2)
         part_ms = timed_graph_steps(torch, stream, (partial,), args.steps, args.warmup, flush_l2)
         if dist:
             dist.barrier()
@@ -661,8 +659,7 @@ def run_prefill(args, rank, world, dist):
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
-        step_ms = timed_graph_steps(torch, stream, (write_and_prepare, partial, combine), args.steps,
-                                    args.warmup, flush_l2)
+        step_ms = timed_graph_steps(torch, stream, (write, attention), args.steps, args.warmup, flush_l2)
         part_ms = timed_graph_steps(torch, stream, (partial,), args.steps, args.warmup, flush_l2)
         if dist:
             dist.barrier()

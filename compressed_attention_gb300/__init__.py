@@ -65,6 +65,7 @@ _SIGNATURES = {
     "tq_dequantize": (_i32, [_vp, _vp, _i64, _i32, _vp, _vp]),
     "tq_decode_workspace_size": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, ctypes.POINTER(_sz)]),
     "tq_decode_num_splits": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, ctypes.POINTER(_i32)]),
+    "tq_decode_num_launches": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, ctypes.POINTER(_i32)]),
     "tq_decode_attention": (_i32, [_vp, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _f32,
                                    _vp, _vp, _vp, _sz, _vp]),
     "tq_decode_prepare_q": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _sz, _vp]),
@@ -233,6 +234,13 @@ def tq_decode_workspace_size(k_ctx, v_ctx, B, Hq, Hkv, L):
     n = _sz(0)
     _check(lib.tq_decode_workspace_size(k_ctx.handle, v_ctx.handle, B, Hq, Hkv, L, ctypes.byref(n)),
            "tq_decode_workspace_size")
+    return n.value
+
+
+def tq_decode_num_launches(k_ctx, v_ctx, B, Hq, Hkv, L):
+    n = _i32(0)
+    _check(lib.tq_decode_num_launches(k_ctx.handle, v_ctx.handle, B, Hq, Hkv, L, ctypes.byref(n)),
+           "tq_decode_num_launches")
     return n.value
 
 

@@ -392,18 +392,46 @@ tq_status tq_decode_combine(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, int
   return TQ_OK;
 }
 
+tq_status tq_decode_num_launches(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, int Hq, int Hkv,
+                                 int L, int *n) {
+  if (!n) return fail(TQ_ERR_INVALID_ARG, "null output");
+  DecodeShape s;
+  tq_status st = check_decode_common(k_ctx, v_ctx, B, Hq, Hkv, L, &s);
+  if (st != TQ_OK) return st;
+  *n = partial_fuses_combine(s) ? 2 : 3;
+  return TQ_OK;
+}
+
 tq_status tq_decode_attention(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *q,
                               int q_dtype, const void *k_cache, const void *v_cache,
                               const int32_t *seq_lens, int B, int Hq, int Hkv, int L, float scale,
                               float *out, float *scores_dbg, void *workspace,
                               size_t workspace_bytes, tq_stream_t stream) {
-  tq_status st = tq_decode_prepare_q(k_ctx, v_ctx, q, q_dtype, B, Hq, Hkv, L, scale, workspace,
-                                     workspace_bytes, stream);
+  // the three stages' checks up front, so nothing is launched for a call that fails
+  DecodeShape s;
+  tq_status st = check_decode_common(k_ctx, v_ctx, B, Hq, Hkv, L, &s);
   if (st != TQ_OK) return st;
-  st = tq_decode_partial(k_ctx, v_ctx, k_cache, v_cache, seq_lens, B, Hq, Hkv, L, scores_dbg,
-                         workspace, workspace_bytes, stream);
+  if (!k_cache || !v_cache) return fail(TQ_ERR_INVALID_ARG, "null cache");
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return fail(TQ_ERR_ALIGNMENT, "caches must be 16-byte aligned");
+  if (seq_lens && !aligned(seq_lens, 4)) return fail(TQ_ERR_ALIGNMENT, "seq_lens must be 4-byte aligned");
+  if (scores_dbg && !aligned(scores_dbg, 4)) return fail(TQ_ERR_ALIGNMENT, "scores must be 4-byte aligned");
+  if (!out) return fail(TQ_ERR_INVALID_ARG, "null output");
+  if (!aligned(out, 4)) return fail(TQ_ERR_ALIGNMENT, "output must be 4-byte aligned");
+  st = tq_decode_prepare_q(k_ctx, v_ctx, q, q_dtype, B, Hq, Hkv, L, scale, workspace,
+                           workspace_bytes, stream);
   if (st != TQ_OK) return st;
-  return tq_decode_combine(k_ctx, v_ctx, B, Hq, Hkv, L, out, workspace, workspace_bytes, stream);
+  Workspace w;
+  if ((st = check_workspace(s, workspace, workspace_bytes, &w)) != TQ_OK) return st;
+  // the split-K kernel merges the splits itself when it can (the CTA completing a unit
+  // writes its outputs); otherwise the combine kernel does
+  bool fused = false;
+  cudaError_t e = launch_partial(k_ctx, v_ctx, (const uint8_t *)k_cache, (const uint8_t *)v_cache, seq_lens,
+                                 s, scores_dbg, w, (cudaStream_t)stream, false, out, &fused);
+  if (e != cudaSuccess) return cuda_fail(e, "partial launch");
+  if (fused) return TQ_OK;
+  e = launch_combine(k_ctx, v_ctx, s, out, w, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  return TQ_OK;
 }
 
 // ---------------------------------------------------------------- prefill

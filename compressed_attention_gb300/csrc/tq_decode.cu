@@ -60,6 +60,8 @@ struct QprepParams {
   float mul_sk;       // log2(e) * scale * sqrt(pi/2) / d (sketch)
   uint32_t *qhl;
   float *qsc;
+  int32_t *unit_done;  // zeroed here for the fused combine of the next split-K launch
+  int n_units;
 };
 
 constexpr int QWARPS = 8;  // queries per CTA, one warp each
@@ -145,6 +147,9 @@ __global__ void __launch_bounds__(QWARPS * 32) k_prepare_q(const QprepParams p) 
     }
   }
   *reinterpret_cast<float4 *>(&qv[warp * D + 4 * lane]) = make_float4(x[0], x[1], x[2], x[3]);
+  // after the wait: the previous split-K launch may still have been counting
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < p.n_units; i += gridDim.x * blockDim.x)
+    p.unit_done[i] = 0;
   __syncthreads();
   __half *hw = hs + warp * 2 * D;
   uint32_t *dst = p.qhl + (size_t)qi * 256;
@@ -188,7 +193,14 @@ struct PartialParams {
   uint32_t kc16[8], vc16[8];                // signed fp16 centroids (K, V), two per word
   uint32_t klo[2], khi[2], vlo[2], vhi[2];  // byte-permute tables (K and V codebooks)
   int32_t *status;
+  // fused combine: out != null makes the CTA that completes a unit's partials merge them,
+  // un-rotate (R row-major of the value rotation, or null) and write the unit's outputs
+  float *out;
+  const float *r;
+  float inv_vscale;   // 1 / (2^P_SHIFT * alpha_V)
+  int32_t *unit_done;  // [units] CTAs that have written their partial of the unit
 };
+constexpr int FIN_MAX = 8;  // units one CTA may complete (the host fuses only below this)
 
 // Shared memory of one CTA, as offsets from the start of dynamic shared memory.
 // The 64 KB table lut[b][s] (slots s < 32: key table, s >= 32: value table; entry =
@@ -206,6 +218,8 @@ struct SmemHead {
   float mw[CWARPS][8];
   float lw[CWARPS][8];
   int abort_flag;
+  int n_fin;                            // units this CTA completed (fused combine)
+  int fin[FIN_MAX];
 };
 constexpr uint32_t STAGE_A_OFF = (sizeof(SmemHead) + 15) & ~15u;
 constexpr uint32_t LUT_OFF = LUT_WINDOW - RESERVED_SMEM;
@@ -333,6 +347,7 @@ __global__ void __maxnreg__(128)
       mbar_init(&sm.empty[s], CWARPS);
     }
     sm.abort_flag = 0;
+    sm.n_fin = 0;
     fence_mbar_init();
   }
   // Fill the table: each (byte, half) entry is computed once and stored to its 32
@@ -680,6 +695,105 @@ __global__ void __maxnreg__(128)
       }
       consumers_sync();
     }
+    if (p.out) {
+      // fused combine: this CTA's partial of the unit is written (every consumer thread's
+      // stores fenced before the barrier); the CTA whose count completes the unit keeps it
+      // for the merge at its end
+      __threadfence();
+      consumers_sync();
+      if (threadIdx.x == 0) {
+        const int first = it.unit * p.tiles_per_unit;
+        const int n_split = (first + p.tiles_per_unit - 1) / p.tiles_per_cta - first / p.tiles_per_cta + 1;
+        if (atomicAdd(&p.unit_done[it.unit], 1) == n_split - 1 && sm.n_fin < FIN_MAX) sm.fin[sm.n_fin++] = it.unit;
+      }
+    }
+  }
+
+  // ---------------- fused combine of the units this CTA completed: merge every CTA's
+  // partial (m* = max m_s, l* = sum l_s 2^(m_s - m*), o = sum acc_s 2^(m_s - m*) / l*), then
+  // out = R^T o with R staged in the stage buffers, which are idle now (every copy was
+  // consumed).  Only after a clean finish: a CTA that gave up leaves its units unwritten
+  // and the status flag set.
+  if (!p.out) return;
+  consumers_sync();
+  const int n_fin = sm.n_fin;
+  // (the flag, read after the barrier, is the same for every consumer warp)
+  if (n_fin == 0 || *reinterpret_cast<volatile int *>(&sm.abort_flag)) return;
+  __threadfence();  // the other CTAs' partials, published before their counts
+  float *rs = reinterpret_cast<float *>(smem_raw + STAGE_B_OFF);  // R, row-major [128][128]
+  static_assert(6 * STAGE_BUF >= D * D * 4, "R fits in the idle stage buffers");
+  if (p.r) {  // asynchronous copy, overlapping the first merge's loads
+    for (int i = threadIdx.x; i < D * D / 4; i += CWARPS * 32)
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(rs + 4 * i)), "l"(p.r + 4 * i)
+                   : "memory");
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+  for (int f = 0; f < n_fin; ++f) {
+    const int u = sm.fin[f];
+    const int hg = u % p.n_hg, bk = u / p.n_hg;
+    const int b = bk / p.Hkv, kvh = bk % p.Hkv;
+    const int G = min(4 * NG, p.gq - hg * 4 * NG);
+    const int head0 = kvh * p.gq + hg * 4 * NG;
+    const int first = u * p.tiles_per_unit;
+    const int n_split = (first + p.tiles_per_unit - 1) / p.tiles_per_cta - first / p.tiles_per_cta + 1;
+    if (warp < G) {  // warp w merges head head0 + w; lane l holds dims l + 32 m
+      const float *part = p.part + (size_t)(b * p.Hq + head0 + warp) * p.n_part * PARTIAL_FLOATS;
+      float ms = -INFINITY, lsum = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int s0 = 0; s0 < n_split; s0 += 8) {
+        // eight splits' (max, sum) and accumulator slices loaded at once
+        float mh[8], lh[8], v[8][4];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float *ps = part + (size_t)min(s0 + i, n_split - 1) * PARTIAL_FLOATS;
+          mh[i] = __ldcg(ps), lh[i] = __ldcg(ps + 1);
+#pragma unroll
+          for (int m = 0; m < 4; ++m) v[i][m] = __ldcg(ps + 6 + lane + 32 * m);
+        }
+        // running merge: raise the max of this chunk's live splits, rescale what is held
+        float mc = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (s0 + i < n_split && lh[i] > 0.f) mc = fmaxf(mc, mh[i]);
+        if (mc > ms) {
+          const float a = (ms == -INFINITY) ? 0.f : exp2f(ms - mc);
+          lsum *= a;
+#pragma unroll
+          for (int m = 0; m < 4; ++m) acc[m] *= a;
+          ms = mc;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (s0 + i < n_split && lh[i] > 0.f) {
+            const float w = exp2f(mh[i] - ms);
+            lsum += w * lh[i];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) acc[m] = fmaf(w, v[i][m], acc[m]);
+          }
+        }
+      }
+      const float fo = p.inv_vscale / lsum;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) sm.osm[warp][0][lane + 32 * m] = acc[m] * fo;
+    }
+    if (f == 0 && p.r) asm volatile("cp.async.wait_all;" ::: "memory");
+    consumers_sync();  // merged heads (and, the first time, R) in shared memory
+    for (int idx = threadIdx.x; idx < G * D; idx += CWARPS * 32) {
+      const int hh = idx / D, j = idx % D;
+      const float *o = sm.osm[hh][0];
+      float res = o[j];
+      if (p.r) {  // four independent chains over k, summed at the end
+        float c4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+        for (int k = 0; k < D; k += 4) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) c4[e] = fmaf(rs[(k + e) * D + j], o[k + e], c4[e]);
+        }
+        res = (c4[0] + c4[1]) + (c4[2] + c4[3]);
+      }
+      p.out[(size_t)(b * p.Hq + head0 + hh) * D + j] = res;
+    }
+    if (threadIdx.x == 0) p.unit_done[u] = 0;
+    consumers_sync();
   }
 }
 
@@ -819,12 +933,16 @@ Workspace carve_workspace(const DecodeShape &s, void *base) {
   const size_t b_qhl = up(nq * 256 * sizeof(uint32_t));
   const size_t b_qsc = up(nq * 2 * sizeof(float));
   const size_t b_part = up(nq * s.n_part * PARTIAL_FLOATS * sizeof(float));
+  const int n_units = s.B * s.Hkv * (s.n_hg > 0 ? s.n_hg : 1);
+  const size_t b_cnt = up((size_t)n_units * sizeof(int32_t));
   Workspace w{};
   uint8_t *p = static_cast<uint8_t *>(base);
   w.qhl = reinterpret_cast<uint32_t *>(p);
   w.qsc = reinterpret_cast<float *>(p ? p + b_qhl : nullptr);
   w.partials = reinterpret_cast<float *>(p ? p + b_qhl + b_qsc : nullptr);
-  w.bytes = b_qhl + b_qsc + b_part;
+  w.unit_done = reinterpret_cast<int32_t *>(p ? p + b_qhl + b_qsc + b_part : nullptr);
+  w.n_units = n_units;
+  w.bytes = b_qhl + b_qsc + b_part + b_cnt;
   return w;
 }
 
@@ -840,6 +958,8 @@ cudaError_t launch_prepare_q(const tq_ctx *k, const void *q, int q_dtype, const 
   p.mul_sk = (float)(LOG2E * (double)scale * (double)k->qjl_factor * 1.2533141373155003 / D);  // sqrt(pi/2) / d
   p.qhl = ws.qhl;
   p.qsc = ws.qsc;
+  p.unit_done = ws.unit_done;
+  p.n_units = ws.n_units;
   const int grid = (p.n_q + QWARPS - 1) / QWARPS;
   const size_t smem = (size_t)D * D * 4 + QWARPS * D * 4 + QWARPS * 2 * D * 2;
   auto kern = s.pv ? k_prepare_q<true> : k_prepare_q<false>;
@@ -883,12 +1003,26 @@ cudaError_t launch_t4_variant(const PartialParams &p, int heads_per_cta, bool fi
                 : launch_t4<1, false, KP, V_PRMT_WORDS, false, K3>(p, grid, st);
 }
 
+// The fused combine serves the plain turbo4 / turbo3-key decode (no exact tail) when a CTA
+// completes at most FIN_MAX units: it touches at most tiles_per_cta / tiles_per_unit + 2.
+bool partial_fuses_combine(const DecodeShape &s) {
+  return !s.pv && s.tail_slot < 0 && !s.no_main && s.tiles_per_cta / s.tiles_per_unit + 2 <= FIN_MAX;
+}
+
 cudaError_t launch_partial(const tq_ctx *k, const tq_ctx *v, const uint8_t *kc,
                            const uint8_t *vc, const int32_t *seq_lens, const DecodeShape &s,
                            float *scores_dbg, const Workspace &ws, cudaStream_t st,
-                           bool withhold_first_tile) {
+                           bool withhold_first_tile, float *out, bool *fused) {
+  if (fused) *fused = false;
   if (s.pv) return launch_partial_pv(k, v, kc, vc, seq_lens, s, scores_dbg, ws, st);
   PartialParams p{};
+  const bool fuse = out && ws.unit_done && partial_fuses_combine(s);
+  if (fuse) {
+    p.out = out;
+    p.r = v->d_pi;
+    p.inv_vscale = 1.0f / (exp2f(P_SHIFT) * v->f16.alpha);
+    p.unit_done = ws.unit_done;
+  }
   p.withhold_first_tile = withhold_first_tile ? 1 : 0;
   p.kc = kc, p.vc = vc, p.seq_lens = seq_lens;
   p.B = s.B, p.Hq = s.Hq, p.Hkv = s.Hkv, p.L = s.L, p.gq = s.gq, p.n_hg = s.n_hg;
@@ -913,8 +1047,10 @@ cudaError_t launch_partial(const tq_ctx *k, const tq_ctx *v, const uint8_t *kc,
   p.status = k->d_status;
   const bool fixed = k->reserved_smem == (int)RESERVED_SMEM;
   const bool sc = scores_dbg != nullptr;
-  return k3 ? launch_t4_variant<true>(p, s.heads_per_cta, fixed, sc, dim3(s.grid), st)
-            : launch_t4_variant<false>(p, s.heads_per_cta, fixed, sc, dim3(s.grid), st);
+  const cudaError_t e = k3 ? launch_t4_variant<true>(p, s.heads_per_cta, fixed, sc, dim3(s.grid), st)
+                           : launch_t4_variant<false>(p, s.heads_per_cta, fixed, sc, dim3(s.grid), st);
+  if (e == cudaSuccess && fused) *fused = fuse;
+  return e;
 }
 
 cudaError_t launch_combine(const tq_ctx *k, const tq_ctx *v, const DecodeShape &s, float *out,

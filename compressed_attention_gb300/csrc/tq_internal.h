@@ -142,6 +142,9 @@ struct Workspace {
   uint32_t *qhl;     // [B*Hq][2 operands][128 fp16]: hi then lo, per operand (q_rot, sketch)
   float *qsc;        // [B*Hq][2] power-of-two scales of the two operands
   float *partials;   // [B*Hq][n_split][PARTIAL_FLOATS]
+  int32_t *unit_done;  // [units] CTAs that wrote their partial of a unit (fused combine);
+                       // zeroed by the q preparation
+  int n_units;
   size_t bytes;
 };
 constexpr int PARTIAL_FLOATS = 2 + 4 + D;  // max, sum, 4 group zero-terms, acc[128]
@@ -153,10 +156,14 @@ Workspace carve_workspace(const DecodeShape &s, void *base);
 
 cudaError_t launch_prepare_q(const tq_ctx *k, const void *q, int q_dtype, const DecodeShape &s,
                              float scale, const Workspace &ws, cudaStream_t st);
+bool partial_fuses_combine(const DecodeShape &s);  // tq_decode_attention skips the combine
+// out != null asks for the combine fused into the split-K kernel (the CTA that completes a
+// unit merges it and writes the outputs); *fused tells whether it was (else launch_combine).
 cudaError_t launch_partial(const tq_ctx *k, const tq_ctx *v, const uint8_t *kc,
                            const uint8_t *vc, const int32_t *seq_lens, const DecodeShape &s,
                            float *scores_dbg, const Workspace &ws, cudaStream_t st,
-                           bool withhold_first_tile = false);
+                           bool withhold_first_tile = false, float *out = nullptr,
+                           bool *fused = nullptr);
 cudaError_t launch_partial_pv(const tq_ctx *k, const tq_ctx *v, const uint8_t *kc,
                               const uint8_t *vc, const int32_t *seq_lens, const DecodeShape &s,
                               float *scores_dbg, const Workspace &ws, cudaStream_t st);

@@ -204,9 +204,17 @@ tq_status tq_dequantize(const tq_ctx *ctx, const void *cache, int64_t n_rows, in
  *   scores_dbg     NULL, or device fp32 [B][Hq][L]: the scaled scores (tests).
  *   workspace      device scratch of at least tq_decode_workspace_size() bytes,
  *                  256-byte aligned; its contents need no initialisation.
- * Hq must be a multiple of Hkv.  L >= 1, B >= 1. */
+ * Hq must be a multiple of Hkv.  L >= 1, B >= 1.
+ * Launches: the q preparation, the split-K kernel and, unless the split-K kernel
+ * merges the splits itself (the CTA that completes a (batch, KV head, head group)
+ * unit merges its partials, un-rotates and writes the unit's outputs; TURBO4 /
+ * TURBO3 keys when each CTA completes few units), the combine kernel;
+ * tq_decode_num_launches tells which for a shape. */
 tq_status tq_decode_workspace_size(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, int Hq,
                                    int Hkv, int L, size_t *bytes);
+/* Number of kernels tq_decode_attention launches for this shape (2 or 3). */
+tq_status tq_decode_num_launches(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, int Hq,
+                                 int Hkv, int L, int *n);
 tq_status tq_decode_attention(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *q,
                               int q_dtype, const void *k_cache, const void *v_cache,
                               const int32_t *seq_lens, int B, int Hq, int Hkv, int L,

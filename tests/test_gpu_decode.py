@@ -153,7 +153,9 @@ def test_decode_q_dtypes_and_staged_calls(q_dtype):
     out2, _ = run_decode(tq, ctx, ctx, q_t, kc, vc, B, Hq, Hkv, L, scores=False, staged=True)
     ref, _ = reference(q32, codec, kb, codec, vb, None)
     check_outputs(out1, ref)
-    assert np.array_equal(out1, out2)
+    # the one-call API merges the splits inside the split-K kernel: same arithmetic as the
+    # combine kernel in another fp32 summation order
+    np.testing.assert_allclose(out1, out2, rtol=2e-6, atol=1e-7)
 
 
 def test_decode_many_heads_staged_kernels():
@@ -354,3 +356,36 @@ def test_decode_sphere_codebook(kfmt):
     ref, s_ref = reference(q32, kcodec, kb, vcodec, vb, None)
     check_outputs(out, ref)
     assert np.max(np.abs(sc - s_ref)) <= ATOL
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,L,fused", [(2, 8, 2, 300, True), (1, 8, 1, 60_000, True),
+                                              (256, 8, 8, 240, False)])
+def test_decode_merge_in_split_kernel_matches_combine(B, Hq, Hkv, L, fused):
+    """tq_decode_attention lets the CTA that completes a unit merge its splits and write the
+    outputs (two launches) unless CTAs would complete too many units (three launches, the
+    combine kernel); either way the outputs equal the stage-by-stage path's (prepare_q,
+    partial, combine) up to fp32 summation order, and the oracle's."""
+    tq = lib()
+    kcodec = Codec("turbo4", rotation="dense", rot_seed=13)
+    vcodec = Codec("turbo4", rotation="dense", rot_seed=14)
+    lens = list(np.random.default_rng(7).integers(1, L + 1, B)) if B > 1 else None
+    kb = oracle_cache(kcodec, B, Hkv, L, 5, scale=2.0, dist="lognormal")
+    vb = oracle_cache(vcodec, B, Hkv, L, 6)
+    q_t, q32 = torch_rows(np.random.default_rng(8).standard_normal((B, Hq, 128)).astype(np.float32), "bf16")
+    kctx, vctx = tq.Ctx("turbo4", "dense", 13), tq.Ctx("turbo4", "dense", 14)
+    assert tq.tq_decode_num_launches(kctx, vctx, B, Hq, Hkv, L) == (2 if fused else 3)
+    kc, vc = upload_cache(tq, "turbo4", kb), upload_cache(tq, "turbo4", vb)
+    for _ in range(2):  # twice: the unit counters are reset between calls
+        out, _ = run_decode(tq, kctx, vctx, q_t, kc, vc, B, Hq, Hkv, L, lens, scores=False)
+    staged, _ = run_decode(tq, kctx, vctx, q_t, kc, vc, B, Hq, Hkv, L, lens, scores=False, staged=True)
+    np.testing.assert_allclose(out, staged, rtol=1e-5, atol=1e-6)
+    ref, _ = reference(q32, kcodec, kb, vcodec, vb, lens)
+    check_outputs(out, ref)
+    assert tq.tq_ctx_device_status(kctx) == 0
+
+
+def test_decode_num_launches_prod3():
+    """prod3 keys with vgroup2 values keep the combine kernel."""
+    tq = lib()
+    kctx, vctx = tq.Ctx("prod3", "dense", 1, 1001), tq.Ctx("vgroup2")
+    assert tq.tq_decode_num_launches(kctx, vctx, 2, 12, 2, 1000) == 3
