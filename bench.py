@@ -519,17 +519,15 @@ def run_decode(args, rank, world, dist):
     stream = torch.cuda.current_stream()
     flush_l2 = flusher(torch, device)
 
-    def write():
-        tq.tq_quantize_set_rows(w["kctx"], w["new_k"], w["kc"], row_ids=w["slots"])
-        tq.tq_quantize_set_rows(w["vctx"], w["new_v"], w["vc"], row_ids=w["slots"])
-
-    def attention():  # q preparation, split-K decode (with the merge fused where it applies)
-        tq.tq_decode_attention(w["kctx"], w["vctx"], w["q"], w["kc"], w["vc"], w["out"], w["ws"], B, Hq, Hkv, L)
+    def step():  # SET_ROWS of K and V, q preparation, split-K decode (merge fused where it applies)
+        tq.tq_decode_step(w["kctx"], w["vctx"], w["new_k"], w["new_v"], w["q"], w["kc"], w["vc"], w["out"],
+                          w["ws"], B, Hq, Hkv, L, row_ids=w["slots"])
 
     def partial():
         tq.tq_decode_partial(w["kctx"], w["vctx"], w["kc"], w["vc"], w["ws"], B, Hq, Hkv, L)
 
-    launches_per_step = 2 + tq.tq_decode_num_launches(w["kctx"], w["vctx"], B, Hq, Hkv, L)
+    launches_per_step = tq.tq_decode_step_num_launches(w["kctx"], w["vctx"], w["new_k"].dtype,
+                                                       w["new_k"].shape[0], B, Hq, Hkv, L)
     if dist:
         dist.barrier()
     with ClockSampler(local) as clocks:
@@ -537,7 +535,7 @@ def run_decode(args, rank, world, dist):
         if dist:
             dist.barrier()
         # the step, then the decode kernel alone (the roofline), same workload and flushes
-        step_ms = timed_graph_steps(torch, stream, (write, attention), args.steps, args.warmup, flush_l2)
+        step_ms = timed_graph_steps(torch, stream, (step,), args.steps, args.warmup, flush_l2)
         part_ms = timed_graph_steps(torch, stream, (partial,), args.steps, args.warmup, flush_l2)
         if dist:
             dist.barrier()
@@ -546,18 +544,26 @@ def run_decode(args, rank, world, dist):
     part_avg = max_over_ranks(statistics.mean(part_ms), dist, device)
 
     # end to end through the public API with host buffers: q and the new K/V rows copied in,
-    # the output read back, every step.
-    pinned = {k: torch.empty(w[k].shape, dtype=w[k].dtype, pin_memory=True).copy_(w[k].cpu())
-              for k in ("q", "new_k", "new_v")}
+    # the output read back, every step.  The step's inputs sit back to back in one pinned
+    # host buffer (each part a multiple of 16 bytes), so they cross in one copy.
+    names = ("q", "new_k", "new_v")
+    sizes = [w[k].numel() * w[k].element_size() for k in names]
+    assert all(n % 16 == 0 for n in sizes)
+    h2d = sum(sizes)
+    hstage = torch.empty(h2d, dtype=torch.uint8, pin_memory=True)
+    dstage = torch.empty(h2d, dtype=torch.uint8, device=device)
+    dev, off = {}, 0
+    for k, n in zip(names, sizes):
+        hstage[off:off + n].view(w[k].dtype).view(w[k].shape).copy_(w[k].cpu())
+        dev[k] = dstage[off:off + n].view(w[k].dtype).view(w[k].shape)
+        off += n
     hout = torch.empty(w["out"].shape, dtype=torch.float32, pin_memory=True)
-    h2d = sum(t.numel() * t.element_size() for t in pinned.values())
     d2h = hout.numel() * 4
+
     def e2e_body():
-        for k, t in pinned.items():
-            w[k].copy_(t, non_blocking=True)
-        tq.tq_quantize_set_rows(w["kctx"], w["new_k"], w["kc"], row_ids=w["slots"])
-        tq.tq_quantize_set_rows(w["vctx"], w["new_v"], w["vc"], row_ids=w["slots"])
-        tq.tq_decode_attention(w["kctx"], w["vctx"], w["q"], w["kc"], w["vc"], w["out"], w["ws"], B, Hq, Hkv, L)
+        dstage.copy_(hstage, non_blocking=True)
+        tq.tq_decode_step(w["kctx"], w["vctx"], dev["new_k"], dev["new_v"], dev["q"], w["kc"], w["vc"], w["out"],
+                          w["ws"], B, Hq, Hkv, L, row_ids=w["slots"])
         hout.copy_(w["out"], non_blocking=True)
 
     e2e_ms, e2e_direct_ms = timed_e2e(torch, e2e_body, args.steps, args.warmup, flush_l2)
@@ -659,7 +665,7 @@ def run_prefill(args, rank, world, dist):
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
-        step_ms = timed_graph_steps(torch, stream, (write, attention), args.steps, args.warmup, flush_l2)
+        step_ms = timed_graph_steps(torch, stream, (step,), args.steps, args.warmup, flush_l2)
         part_ms = timed_graph_steps(torch, stream, (partial,), args.steps, args.warmup, flush_l2)
         if dist:
             dist.barrier()

@@ -66,6 +66,9 @@ _SIGNATURES = {
     "tq_decode_workspace_size": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, ctypes.POINTER(_sz)]),
     "tq_decode_num_splits": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, ctypes.POINTER(_i32)]),
     "tq_decode_num_launches": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, ctypes.POINTER(_i32)]),
+    "tq_decode_step_num_launches": (_i32, [_vp, _vp, _i32, _i64, _i32, _i32, _i32, _i32, ctypes.POINTER(_i32)]),
+    "tq_decode_step": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i64, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _i32,
+                              _i32, _i32, _f32, _vp, _vp, _sz, _vp]),
     "tq_decode_attention": (_i32, [_vp, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _f32,
                                    _vp, _vp, _vp, _sz, _vp]),
     "tq_decode_prepare_q": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _sz, _vp]),
@@ -234,6 +237,30 @@ def tq_decode_workspace_size(k_ctx, v_ctx, B, Hq, Hkv, L):
     n = _sz(0)
     _check(lib.tq_decode_workspace_size(k_ctx.handle, v_ctx.handle, B, Hq, Hkv, L, ctypes.byref(n)),
            "tq_decode_workspace_size")
+    return n.value
+
+
+def tq_decode_step(k_ctx, v_ctx, new_k, new_v, q, k_cache, v_cache, out, workspace, B, Hq, Hkv, L,
+                   row_ids=None, seq_lens=None, scale=0.0, stream=None):
+    """SET_ROWS of the step's new K / V rows ([n, 128] tensors, rows at slots row_ids of the
+    [B][Hkv][L] caches), then decode attention over the updated caches."""
+    if new_v.dtype != new_k.dtype or new_v.shape != new_k.shape or new_v.stride() != new_k.stride():
+        raise ValueError("new_k and new_v must have one dtype, shape and row stride")
+    n = new_k.shape[0] if new_k.dim() == 2 else new_k.numel() // D
+    qp, qd = _q_args(q)
+    _check(lib.tq_decode_step(k_ctx.handle, v_ctx.handle, _ptr(new_k), _ptr(new_v), _dtype_code(new_k), n,
+                              new_k.stride(-2) if new_k.dim() >= 2 else D, _ptr(row_ids), qp, qd, _ptr(k_cache),
+                              _ptr(v_cache), _ptr(seq_lens), B, Hq, Hkv, L, scale, _ptr(out), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _stream(stream)), "tq_decode_step")
+
+
+def tq_decode_step_num_launches(k_ctx, v_ctx, src_dtype, n_rows, B, Hq, Hkv, L):
+    """Kernels one tq_decode_step call launches (``src_dtype`` a torch dtype)."""
+    import torch
+    n = _i32(0)
+    code = TQ_DTYPE_BF16 if src_dtype == torch.bfloat16 else TQ_DTYPE_F32
+    _check(lib.tq_decode_step_num_launches(k_ctx.handle, v_ctx.handle, code, n_rows, B, Hq, Hkv, L,
+                                           ctypes.byref(n)), "tq_decode_step_num_launches")
     return n.value
 
 

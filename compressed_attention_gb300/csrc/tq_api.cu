@@ -282,12 +282,10 @@ tq_status tq_ctx_device_status(const tq_ctx *ctx, int32_t *status, int clear) {
   return TQ_OK;
 }
 
-tq_status tq_quantize_set_rows(const tq_ctx *ctx, const void *src, int src_dtype, int64_t n_rows,
-                               int64_t src_row_stride, const int64_t *row_ids, void *dst_cache,
-                               int64_t dst_rows, tq_stream_t stream) {
-  if (!ctx) return fail(TQ_ERR_INVALID_ARG, "null context");
-  if (n_rows < 0) return fail(TQ_ERR_INVALID_ARG, "n_rows < 0");
-  if (n_rows == 0) return TQ_OK;
+namespace {
+// The argument checks of tq_quantize_set_rows for a call with n_rows >= 1.
+tq_status check_write_args(const void *src, int src_dtype, int64_t src_row_stride, const int64_t *row_ids,
+                           const void *dst_cache, int64_t n_rows, int64_t dst_rows) {
   if (!src || !dst_cache) return fail(TQ_ERR_INVALID_ARG, "null source or cache");
   if (src_dtype != TQ_DTYPE_F32 && src_dtype != TQ_DTYPE_BF16)
     return fail(TQ_ERR_UNSUPPORTED, "source dtype must be F32 or BF16");
@@ -300,6 +298,18 @@ tq_status tq_quantize_set_rows(const tq_ctx *ctx, const void *src, int src_dtype
     return fail(TQ_ERR_ALIGNMENT, "source rows must be 16-byte (F32) or 8-byte (BF16) aligned");
   if (!aligned(dst_cache, 16)) return fail(TQ_ERR_ALIGNMENT, "cache must be 16-byte aligned");
   if (row_ids && !aligned(row_ids, 8)) return fail(TQ_ERR_ALIGNMENT, "row_ids must be 8-byte aligned");
+  return TQ_OK;
+}
+}  // namespace
+
+tq_status tq_quantize_set_rows(const tq_ctx *ctx, const void *src, int src_dtype, int64_t n_rows,
+                               int64_t src_row_stride, const int64_t *row_ids, void *dst_cache,
+                               int64_t dst_rows, tq_stream_t stream) {
+  if (!ctx) return fail(TQ_ERR_INVALID_ARG, "null context");
+  if (n_rows < 0) return fail(TQ_ERR_INVALID_ARG, "n_rows < 0");
+  if (n_rows == 0) return TQ_OK;
+  tq_status st = check_write_args(src, src_dtype, src_row_stride, row_ids, dst_cache, n_rows, dst_rows);
+  if (st != TQ_OK) return st;
   WriteLaunch w{src, src_dtype, n_rows, src_row_stride, row_ids, (uint8_t *)dst_cache, dst_rows};
   cudaError_t e = launch_write(ctx, w, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "write kernel launch");
@@ -431,6 +441,78 @@ tq_status tq_decode_attention(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const vo
   if (fused) return TQ_OK;
   e = launch_combine(k_ctx, v_ctx, s, out, w, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  return TQ_OK;
+}
+
+
+tq_status tq_decode_step(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *new_k, const void *new_v,
+                         int src_dtype, int64_t n_rows, int64_t src_row_stride, const int64_t *row_ids,
+                         const void *q, int q_dtype, void *k_cache, void *v_cache,
+                         const int32_t *seq_lens, int B, int Hq, int Hkv, int L, float scale, float *out,
+                         void *workspace, size_t workspace_bytes, tq_stream_t stream) {
+  // every check of the three calls first, so that nothing is launched for a call that fails
+  DecodeShape s;
+  tq_status st = check_decode_common(k_ctx, v_ctx, B, Hq, Hkv, L, &s);
+  if (st != TQ_OK) return st;
+  if (n_rows < 0) return fail(TQ_ERR_INVALID_ARG, "n_rows < 0");
+  const int64_t dst_rows = (int64_t)B * Hkv * L;
+  if (n_rows > 0) {
+    if ((st = check_write_args(new_k, src_dtype, src_row_stride, row_ids, k_cache, n_rows, dst_rows)) != TQ_OK ||
+        (st = check_write_args(new_v, src_dtype, src_row_stride, row_ids, v_cache, n_rows, dst_rows)) != TQ_OK)
+      return st;
+  }
+  if (!k_cache || !v_cache) return fail(TQ_ERR_INVALID_ARG, "null cache");
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return fail(TQ_ERR_ALIGNMENT, "caches must be 16-byte aligned");
+  if (!q) return fail(TQ_ERR_INVALID_ARG, "null q");
+  if (q_dtype != TQ_DTYPE_F32 && q_dtype != TQ_DTYPE_BF16 && q_dtype != TQ_DTYPE_F16)
+    return fail(TQ_ERR_INVALID_ARG, "bad q dtype");
+  if (!aligned(q, 16)) return fail(TQ_ERR_ALIGNMENT, "q must be 16-byte aligned");
+  if (!std::isfinite(scale)) return fail(TQ_ERR_INVALID_ARG, "scale must be finite");
+  if (seq_lens && !aligned(seq_lens, 4)) return fail(TQ_ERR_ALIGNMENT, "seq_lens must be 4-byte aligned");
+  if (!out) return fail(TQ_ERR_INVALID_ARG, "null output");
+  if (!aligned(out, 4)) return fail(TQ_ERR_ALIGNMENT, "output must be 4-byte aligned");
+  Workspace w;
+  if ((st = check_workspace(s, workspace, workspace_bytes, &w)) != TQ_OK) return st;
+  if (scale == 0.f) scale = 1.0f / std::sqrt((float)D);
+
+  const WriteLaunch wk{new_k, src_dtype, n_rows, src_row_stride, row_ids, (uint8_t *)k_cache, dst_rows};
+  const WriteLaunch wv{new_v, src_dtype, n_rows, src_row_stride, row_ids, (uint8_t *)v_cache, dst_rows};
+  const cudaStream_t cs = (cudaStream_t)stream;
+  cudaError_t e;
+  if (n_rows > 0 && step_front_eligible(k_ctx, v_ctx, wk, wv)) {
+    // the two writes and the q preparation are independent: one launch does all three
+    e = launch_step_front(k_ctx, v_ctx, wk, wv, make_qprep_params(k_ctx, q, q_dtype, s, scale, w), cs);
+    if (e != cudaSuccess) return cuda_fail(e, "decode step front launch");
+  } else {
+    if (n_rows > 0) {
+      if ((e = launch_write(k_ctx, wk, cs)) != cudaSuccess) return cuda_fail(e, "write kernel launch");
+      if ((e = launch_write(v_ctx, wv, cs)) != cudaSuccess) return cuda_fail(e, "write kernel launch");
+    }
+    if ((e = launch_prepare_q(k_ctx, q, q_dtype, s, scale, w, cs)) != cudaSuccess)
+      return cuda_fail(e, "prepare_q launch");
+  }
+  bool fused = false;
+  e = launch_partial(k_ctx, v_ctx, (const uint8_t *)k_cache, (const uint8_t *)v_cache, seq_lens, s, nullptr, w,
+                     cs, false, out, &fused);
+  if (e != cudaSuccess) return cuda_fail(e, "partial launch");
+  if (fused) return TQ_OK;
+  e = launch_combine(k_ctx, v_ctx, s, out, w, cs);
+  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  return TQ_OK;
+}
+
+tq_status tq_decode_step_num_launches(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int src_dtype, int64_t n_rows,
+                                      int B, int Hq, int Hkv, int L, int *n) {
+  if (!n) return fail(TQ_ERR_INVALID_ARG, "null output");
+  DecodeShape s;
+  tq_status st = check_decode_common(k_ctx, v_ctx, B, Hq, Hkv, L, &s);
+  if (st != TQ_OK) return st;
+  if (n_rows < 0) return fail(TQ_ERR_INVALID_ARG, "n_rows < 0");
+  const int64_t dst_rows = (int64_t)B * Hkv * L;
+  const WriteLaunch wk{nullptr, src_dtype, n_rows, D, nullptr, nullptr, dst_rows};
+  const int attn = partial_fuses_combine(s) ? 2 : 3;
+  if (n_rows > 0 && step_front_eligible(k_ctx, v_ctx, wk, wk)) *n = attn;
+  else *n = attn + (n_rows > 0 ? 2 : 0);
   return TQ_OK;
 }
 

@@ -34,6 +34,7 @@
 #include <cstring>
 
 #include "tq_decode_common.cuh"
+#include "tq_qprep.cuh"
 #include "tq_device.cuh"
 #include "tq_internal.h"
 
@@ -50,133 +51,15 @@ constexpr int T4_ROW = 68;
 constexpr int T3_ROW = 56;            // four 14-byte blocks of the 2+1 layout
 constexpr int STAGE_BUF = 16352;      // >= 240 * 68 + 2 * 15, multiple of 32
 
-struct QprepParams {
-  const void *q;
-  int q_dtype;
-  int n_q;            // B * Hq
-  const float *rt;    // R^T, fp32 [128][128] (row k = column k of R)
-  const float *st;    // S^T for the QJL sketch (prod3 keys), or null
-  float mul;          // log2(e) * scale / alpha_K
-  float mul_sk;       // log2(e) * scale * sqrt(pi/2) / d (sketch)
-  uint32_t *qhl;
-  float *qsc;
-  int32_t *unit_done;  // zeroed here for the fused combine of the next split-K launch
-  int n_units;
-};
-
-constexpr int QWARPS = 8;  // queries per CTA, one warp each
-
-// Stage a 128 x 128 fp32 matrix in shared memory with 16-byte loads, all in flight.
-__device__ __forceinline__ void stage_matrix(float *dst, const float *src) {
-  const float4 *s4 = reinterpret_cast<const float4 *>(src);
-  float4 *d4 = reinterpret_cast<float4 *>(dst);
-  constexpr int N4 = D * D / 4;
-  constexpr int PER = N4 / (QWARPS * 32);
-  float4 v[PER];
-#pragma unroll
-  for (int i = 0; i < PER; ++i) v[i] = s4[threadIdx.x + i * QWARPS * 32];
-#pragma unroll
-  for (int i = 0; i < PER; ++i) d4[threadIdx.x + i * QWARPS * 32] = v[i];
-}
-
-// y = M x for the staged M^T (lane l computes y[l + 32 m]), times mul, scaled by a power
-// of two 2^-e so that the largest element lies in [2^13, 2^14), split into fp16 hi and
-// lo written to hw[0..127] and hw[128..255].  Returns e.
-__device__ __forceinline__ int transform_split(const float *mt, const float *x, float mul,
-                                               __half *hw, int lane) {
-  float y[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-  for (int k = 0; k < D; ++k) {
-    const float xk = x[k];
-    const float *row = mt + k * D + lane;
-#pragma unroll
-    for (int m = 0; m < 4; ++m) y[m] = fmaf(row[32 * m], xk, y[m]);
-  }
-  float amax = 0.f;
-#pragma unroll
-  for (int m = 0; m < 4; ++m) {
-    y[m] *= mul;
-    amax = fmaxf(amax, fabsf(y[m]));
-  }
-#pragma unroll
-  for (int h = 16; h >= 1; h >>= 1) amax = fmaxf(amax, __shfl_xor_sync(FULL_MASK, amax, h));
-  int e = 0;
-  if (amax > 0.f && isfinite(amax)) e = ilogbf(amax) - 13;
-#pragma unroll
-  for (int m = 0; m < 4; ++m) {
-    const float v = ldexpf(y[m], -e);
-    const __half h = __float2half_rn(v);
-    hw[lane + 32 * m] = h;
-    hw[D + lane + 32 * m] = __float2half_rn(v - __half2float(h));
-  }
-  return e;
-}
-
 // For 8 queries per CTA: q_rot = R q and, with SKETCH, the QJL sketch S q, each
-// pre-scaled and split into the fp16 hi + lo tensor-core operands:
-// qhl[q][0..127] = q_rot (hi, lo), qhl[q][128..255] = sketch (hi, lo).
+// pre-scaled and split into the fp16 hi + lo tensor-core operands (tq_qprep.cuh).
 template <bool SKETCH>
 __global__ void __launch_bounds__(QWARPS * 32) k_prepare_q(const QprepParams p) {
   extern __shared__ __align__(16) float qsm[];
-  float *mt = qsm;                       // [128][128]
-  float *qv = qsm + D * D;               // [QWARPS][128]
-  __half *hs = reinterpret_cast<__half *>(qv + QWARPS * D);  // [QWARPS][2][128]
   pdl_trigger();
-  stage_matrix(mt, p.rt);
+  stage_matrix(qsm, p.rt);
   pdl_wait();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qi = blockIdx.x * QWARPS + warp;
-  const bool live = qi < p.n_q;
-  float x[4] = {0.f, 0.f, 0.f, 0.f};
-  if (live) {
-    if (p.q_dtype == TQ_DTYPE_F32) {
-      const float4 v = reinterpret_cast<const float4 *>(p.q)[(size_t)qi * 32 + lane];
-      x[0] = v.x, x[1] = v.y, x[2] = v.z, x[3] = v.w;
-    } else {
-      const uint2 v = reinterpret_cast<const uint2 *>(p.q)[(size_t)qi * 32 + lane];
-      const uint32_t w[4] = {v.x & 0xFFFFu, v.x >> 16, v.y & 0xFFFFu, v.y >> 16};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if (p.q_dtype == TQ_DTYPE_BF16) {
-          x[e] = bf16_bits_to_f32(w[e]);
-        } else {
-          const unsigned short us = (unsigned short)w[e];
-          x[e] = __half2float(*reinterpret_cast<const __half *>(&us));
-        }
-      }
-    }
-  }
-  *reinterpret_cast<float4 *>(&qv[warp * D + 4 * lane]) = make_float4(x[0], x[1], x[2], x[3]);
-  // after the wait: the previous split-K launch may still have been counting
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < p.n_units; i += gridDim.x * blockDim.x)
-    p.unit_done[i] = 0;
-  __syncthreads();
-  __half *hw = hs + warp * 2 * D;
-  uint32_t *dst = p.qhl + (size_t)qi * 256;
-  const uint32_t *src = reinterpret_cast<const uint32_t *>(hw);
-  if (live) {
-    const int e = transform_split(mt, qv + warp * D, p.mul, hw, lane);
-    __syncwarp();
-#pragma unroll
-    for (int i = 0; i < 4; ++i) dst[lane + 32 * i] = src[lane + 32 * i];
-    if (lane == 0) {
-      p.qsc[2 * qi] = ldexpf(1.0f, e);
-      if (!SKETCH) p.qsc[2 * qi + 1] = 0.f;
-    }
-  }
-  if (SKETCH) {
-    __syncthreads();  // every warp is done with R^T
-    stage_matrix(mt, p.st);
-    __syncthreads();
-    if (live) {
-      __syncwarp();
-      const int e = transform_split(mt, qv + warp * D, p.mul_sk, hw, lane);
-      __syncwarp();
-#pragma unroll
-      for (int i = 0; i < 4; ++i) dst[128 + lane + 32 * i] = src[lane + 32 * i];
-      if (lane == 0) p.qsc[2 * qi + 1] = ldexpf(1.0f, e);
-    }
-  }
+  prepare_q_body<SKETCH>(p, blockIdx.x, gridDim.x, qsm);
 }
 
 struct PartialParams {
@@ -946,8 +829,8 @@ Workspace carve_workspace(const DecodeShape &s, void *base) {
   return w;
 }
 
-cudaError_t launch_prepare_q(const tq_ctx *k, const void *q, int q_dtype, const DecodeShape &s,
-                             float scale, const Workspace &ws, cudaStream_t st) {
+QprepParams make_qprep_params(const tq_ctx *k, const void *q, int q_dtype, const DecodeShape &s,
+                              float scale, const Workspace &ws) {
   QprepParams p{};
   p.q = q;
   p.q_dtype = q_dtype;
@@ -960,12 +843,17 @@ cudaError_t launch_prepare_q(const tq_ctx *k, const void *q, int q_dtype, const 
   p.qsc = ws.qsc;
   p.unit_done = ws.unit_done;
   p.n_units = ws.n_units;
+  return p;
+}
+
+cudaError_t launch_prepare_q(const tq_ctx *k, const void *q, int q_dtype, const DecodeShape &s,
+                             float scale, const Workspace &ws, cudaStream_t st) {
+  const QprepParams p = make_qprep_params(k, q, q_dtype, s, scale, ws);
   const int grid = (p.n_q + QWARPS - 1) / QWARPS;
-  const size_t smem = (size_t)D * D * 4 + QWARPS * D * 4 + QWARPS * 2 * D * 2;
   auto kern = s.pv ? k_prepare_q<true> : k_prepare_q<false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)QPREP_SMEM);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(grid), dim3(QWARPS * 32), smem, st, p);
+  return launch_pdl(kern, dim3(grid), dim3(QWARPS * 32), QPREP_SMEM, st, p);
 }
 
 template <int NG, bool SC, int KP, int VP, bool FIXED, bool K3>

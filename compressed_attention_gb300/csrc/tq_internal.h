@@ -114,6 +114,12 @@ struct WriteLaunch {
   int64_t dst_rows;
 };
 cudaError_t launch_write(const tq_ctx *ctx, const WriteLaunch &w, cudaStream_t st);
+// The decode step's front in one launch (tq_decode_step): both small-batch dense writes and
+// the q preparation; eligible for dense-rotation turbo4 / turbo3 caches and at most 256 rows.
+struct QprepParams;
+bool step_front_eligible(const tq_ctx *k, const tq_ctx *v, const WriteLaunch &wk, const WriteLaunch &wv);
+cudaError_t launch_step_front(const tq_ctx *k, const tq_ctx *v, const WriteLaunch &wk, const WriteLaunch &wv,
+                              const QprepParams &q, cudaStream_t st);
 bool write_tc_eligible(const tq_ctx *ctx, const WriteLaunch &w);
 cudaError_t launch_write_tc(const tq_ctx *ctx, const WriteLaunch &w, cudaStream_t st);
 
@@ -149,11 +155,28 @@ struct Workspace {
 };
 constexpr int PARTIAL_FLOATS = 2 + 4 + D;  // max, sum, 4 group zero-terms, acc[128]
 
+// Arguments of the q preparation (tq_qprep.cuh).
+struct QprepParams {
+  const void *q;
+  int q_dtype;
+  int n_q;            // B * Hq
+  const float *rt;    // R^T, fp32 [128][128] (row k = column k of R)
+  const float *st;    // S^T for the QJL sketch (prod3 keys), or null
+  float mul;          // log2(e) * scale / alpha_K
+  float mul_sk;       // log2(e) * scale * sqrt(pi/2) / d (sketch)
+  uint32_t *qhl;
+  float *qsc;
+  int32_t *unit_done;  // zeroed there for the fused combine of the next split-K launch
+  int n_units;
+};
+
 bool decode_shape(const tq_ctx *k, const tq_ctx *v, int B, int Hq, int Hkv, int L,
                   DecodeShape *s);
 bool decode_pair_supported(const tq_ctx *k, const tq_ctx *v);  // a decode kernel exists
 Workspace carve_workspace(const DecodeShape &s, void *base);
 
+QprepParams make_qprep_params(const tq_ctx *k, const void *q, int q_dtype, const DecodeShape &s,
+                              float scale, const Workspace &ws);
 cudaError_t launch_prepare_q(const tq_ctx *k, const void *q, int q_dtype, const DecodeShape &s,
                              float scale, const Workspace &ws, cudaStream_t st);
 bool partial_fuses_combine(const DecodeShape &s);  // tq_decode_attention skips the combine

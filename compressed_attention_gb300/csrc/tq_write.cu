@@ -14,6 +14,7 @@
 // lane l of a warp elements 4l..4l+3 of its row and run the same trees across lanes.
 #include "tq_device.cuh"
 #include "tq_internal.h"
+#include "tq_qprep.cuh"
 
 namespace tq {
 
@@ -542,75 +543,138 @@ __global__ void __launch_bounds__(WARPS * 32) k_write_dense(const WriteParams p)
 }
 
 // ---------------------------------------- dense rotation, small batches (one CTA per row)
-// For the few rows of a decode step: thread j computes output coordinate j from row j
-// of R read straight from L2 (no 64 KB staging) into registers before the wait on the
+// For the few rows of a decode step: thread j < 128 computes output coordinate j from row
+// j of R read straight from L2 (no 64 KB staging) into registers before the wait on the
 // previous kernel (R belongs to the immutable context), so after that wait the launch
 // costs about one memory latency.  Norm, normalisation and packing follow the same
-// canonical order as above.
-template <int FMT, int SRC>
-__global__ void __launch_bounds__(D) k_write_dense_row(const WriteParams p) {
-  constexpr int NB = (FMT == TQ_FMT_TURBO4) ? 15 : 7;
-  __shared__ float u[D];
-  __shared__ float grp[32];
-  __shared__ float sb[16];
-  __shared__ BucketTable grid;
-  __shared__ float nsh;
-  __shared__ __align__(16) uint8_t ib[D];
-  __shared__ __align__(16) uint8_t buf[ROWBUF];
-  const int64_t row = blockIdx.x;
-  const int j = threadIdx.x, lane = j & 31;
+// canonical order as above.  Threads j >= 128 of a larger CTA only join the barriers.
+struct RowScratch {
+  float u[D];
+  float grp[32];
+  float sb[16];
+  float nsh;
+  BucketTable grid;
+  alignas(16) uint8_t ib[D];
+  alignas(16) uint8_t buf[ROWBUF];
+};
+
+// Before the wait: the boundaries, the grid table, this thread's row of R.
+template <int NB>
+__device__ __forceinline__ void dense_row_prologue(const WriteParams &p, RowScratch &sc, int j,
+                                                   float4 (&rr)[D / 4]) {
   if (j == 0) {
 #pragma unroll
-    for (int k = 0; k < NB; ++k) sb[k] = p.b[k];  // constant indices keep p in parameter space
+    for (int k = 0; k < NB; ++k) sc.sb[k] = p.b[k];
   }
-  stage_grid(&grid, p.bt);
-  const float4 *r4 = reinterpret_cast<const float4 *>(p.pi + (size_t)j * D);  // row j of R
-  float4 rr[D / 4];
+  stage_grid(&sc.grid, p.bt);
+  if (j < D) {
+    const float4 *r4 = reinterpret_cast<const float4 *>(p.pi + (size_t)j * D);  // row j of R
 #pragma unroll
-  for (int k4 = 0; k4 < D / 4; ++k4) rr[k4] = r4[k4];
-  pdl_trigger();
-  pdl_wait();
+    for (int k4 = 0; k4 < D / 4; ++k4) rr[k4] = r4[k4];
+  }
+}
+
+// After the wait: encode source row `row` into its slot (the whole CTA takes the same row).
+template <int FMT, int SRC>
+__device__ __forceinline__ void dense_row_body(const WriteParams &p, int64_t row, RowScratch &sc, int j,
+                                               const float4 (&rr)[D / 4]) {
+  constexpr int NB = (FMT == TQ_FMT_TURBO4) ? 15 : 7;
+  const int lane = j & 31;
+  const bool act = j < D;
   const int64_t slot = p.row_ids ? p.row_ids[row] : row;
-  if (slot < 0 || slot >= p.dst_rows) {
+  if (slot < 0 || slot >= p.dst_rows) {  // the same for every thread of the CTA
     if (j == 0) atomicExch(p.status, (int32_t)DEVERR_ROW_OOB);
     return;
   }
-  float x;
-  if (SRC == TQ_DTYPE_F32)
-    x = static_cast<const float *>(p.src)[row * p.stride + j];
-  else
-    x = bf16_bits_to_f32(static_cast<const uint16_t *>(p.src)[row * p.stride + j]);
-  // canonical norm: groups of four (pairs summed first), then the butterfly over groups
-  const float sq = __fmul_rn(x, x);
-  const float a = __fadd_rn(sq, __shfl_xor_sync(FULL_MASK, sq, 1));
-  const float g = __fadd_rn(a, __shfl_xor_sync(FULL_MASK, a, 2));
-  if ((j & 3) == 0) grp[j >> 2] = g;
+  float x = 0.f;
+  if (act) {
+    if (SRC == TQ_DTYPE_F32)
+      x = static_cast<const float *>(p.src)[row * p.stride + j];
+    else
+      x = bf16_bits_to_f32(static_cast<const uint16_t *>(p.src)[row * p.stride + j]);
+    // canonical norm: groups of four (pairs summed first), then the butterfly over groups
+    const float sq = __fmul_rn(x, x);
+    const float a = __fadd_rn(sq, __shfl_xor_sync(FULL_MASK, sq, 1));
+    const float g = __fadd_rn(a, __shfl_xor_sync(FULL_MASK, a, 2));
+    if ((j & 3) == 0) sc.grp[j >> 2] = g;
+  }
   __syncthreads();
   if (j < 32) {
-    float pl = grp[lane];
+    float pl = sc.grp[lane];
 #pragma unroll
     for (int h = 16; h >= 1; h >>= 1) pl = __fadd_rn(pl, __shfl_xor_sync(FULL_MASK, pl, h));
-    if (lane == 0) nsh = __fsqrt_rn(pl);
+    if (lane == 0) sc.nsh = __fsqrt_rn(pl);
   }
   __syncthreads();
-  const float n = nsh;
-  u[j] = (n == 0.0f) ? 0.0f : __fdiv_rn(x, n);
+  const float n = sc.nsh;
+  if (act) sc.u[j] = (n == 0.0f) ? 0.0f : __fdiv_rn(x, n);
   __syncthreads();
-  float y = 0.f;
+  if (act) {
+    float y = 0.f;
 #pragma unroll
-  for (int k4 = 0; k4 < D / 4; ++k4) {
-    const float4 r = rr[k4];
-    y = fmaf(r.x, u[4 * k4], y);
-    y = fmaf(r.y, u[4 * k4 + 1], y);
-    y = fmaf(r.z, u[4 * k4 + 2], y);
-    y = fmaf(r.w, u[4 * k4 + 3], y);
+    for (int k4 = 0; k4 < D / 4; ++k4) {
+      const float4 r = rr[k4];
+      y = fmaf(r.x, sc.u[4 * k4], y);
+      y = fmaf(r.y, sc.u[4 * k4 + 1], y);
+      y = fmaf(r.z, sc.u[4 * k4 + 2], y);
+      y = fmaf(r.w, sc.u[4 * k4 + 3], y);
+    }
+    sc.ib[j] = (uint8_t)nearest<NB>(y, sc.grid, sc.sb);
   }
-  ib[j] = (uint8_t)nearest<NB>(y, grid, sb);
   __syncthreads();
   if (j < 32) {
-    const uint32_t w4 = *reinterpret_cast<const uint32_t *>(ib + 4 * lane);
+    const uint32_t w4 = *reinterpret_cast<const uint32_t *>(sc.ib + 4 * lane);
     const uint32_t idx[4] = {w4 & 0xFF, (w4 >> 8) & 0xFF, (w4 >> 16) & 0xFF, w4 >> 24};
-    pack_store_turbo<FMT>(idx, n, buf, p.dst + slot * (FMT == TQ_FMT_TURBO4 ? 68 : 56), lane);
+    pack_store_turbo<FMT>(idx, n, sc.buf, p.dst + slot * (FMT == TQ_FMT_TURBO4 ? 68 : 56), lane);
+  }
+}
+
+template <int FMT, int SRC>
+__global__ void __launch_bounds__(D) k_write_dense_row(const WriteParams p) {
+  __shared__ RowScratch sc;
+  float4 rr[D / 4];
+  dense_row_prologue<(FMT == TQ_FMT_TURBO4) ? 15 : 7>(p, sc, threadIdx.x, rr);
+  pdl_trigger();
+  pdl_wait();
+  dense_row_body<FMT, SRC>(p, blockIdx.x, sc, threadIdx.x, rr);
+}
+
+// ------------------------------------------------ decode step front (tq_decode_step)
+// One launch for what a decode step does before its split-K kernel: CTAs 0 .. n - 1
+// encode the step's n new K rows, CTAs n .. 2n - 1 its n new V rows (the small-batch dense
+// write above), the remaining CTAs prepare q (tq_qprep.cuh).  The three jobs are
+// independent, so they share one wait on the previous kernel instead of three.
+struct StepFrontParams {
+  WriteParams wk, wv;
+  QprepParams q;
+  int n_rows;
+  int q_ctas;
+};
+
+template <int KF, int VF, int SRC>
+__global__ void __launch_bounds__(QWARPS * 32) k_step_front(const StepFrontParams sp) {
+  extern __shared__ __align__(16) float fsm[];
+  const int c = blockIdx.x;
+  if (c < 2 * sp.n_rows) {
+    RowScratch &sc = *reinterpret_cast<RowScratch *>(fsm);
+    const bool v = c >= sp.n_rows;
+    const int j = threadIdx.x;
+    float4 rr[D / 4];
+    if (v)
+      dense_row_prologue<(VF == TQ_FMT_TURBO4) ? 15 : 7>(sp.wv, sc, j, rr);
+    else
+      dense_row_prologue<(KF == TQ_FMT_TURBO4) ? 15 : 7>(sp.wk, sc, j, rr);
+    pdl_trigger();
+    pdl_wait();
+    if (v)
+      dense_row_body<VF, SRC>(sp.wv, c - sp.n_rows, sc, j, rr);
+    else
+      dense_row_body<KF, SRC>(sp.wk, c, sc, j, rr);
+  } else {
+    pdl_trigger();
+    stage_matrix(fsm, sp.q.rt);
+    pdl_wait();
+    prepare_q_body<false>(sp.q, c - 2 * sp.n_rows, sp.q_ctas, fsm);
   }
 }
 
@@ -695,9 +759,7 @@ cudaError_t launch_thread_rows(K kernel, const WriteParams &p, int64_t n_rows, i
   return launch_pdl(kernel, dim3(grid), dim3(WT_THREADS), 0, st, p);
 }
 
-}  // namespace
-
-cudaError_t launch_write(const tq_ctx *ctx, const WriteLaunch &w, cudaStream_t st) {
+WriteParams write_params(const tq_ctx *ctx, const WriteLaunch &w) {
   WriteParams p{};
   p.src = w.src;
   p.n_rows = w.n_rows;
@@ -714,6 +776,13 @@ cudaError_t launch_write(const tq_ctx *ctx, const WriteLaunch &w, cudaStream_t s
   p.S = ctx->d_S;
   p.St = ctx->d_St;
   p.bt = ctx->d_bt;
+  return p;
+}
+
+}  // namespace
+
+cudaError_t launch_write(const tq_ctx *ctx, const WriteLaunch &w, cudaStream_t st) {
+  const WriteParams p = write_params(ctx, w);
   const bool bf16 = (w.src_dtype == TQ_DTYPE_BF16);
   const int fmt = ctx->fmt;
   const int sms = ctx->num_sms;
@@ -755,6 +824,44 @@ cudaError_t launch_write(const tq_ctx *ctx, const WriteLaunch &w, cudaStream_t s
       return bf16 ? launch_rows(k_write_dense<TQ_FMT_PROD3, TQ_DTYPE_BF16>, p, w.n_rows, sms, smem, per_sm, st)
                   : launch_rows(k_write_dense<TQ_FMT_PROD3, TQ_DTYPE_F32>, p, w.n_rows, sms, smem, per_sm, st);
   }
+}
+
+
+bool step_front_eligible(const tq_ctx *k, const tq_ctx *v, const WriteLaunch &wk, const WriteLaunch &wv) {
+  auto ok = [](const tq_ctx *c, const WriteLaunch &w) {
+    return c->p.rotation == TQ_ROT_DENSE && (c->fmt == TQ_FMT_TURBO4 || c->fmt == TQ_FMT_TURBO3) &&
+           w.n_rows >= 1 && w.n_rows <= SMALL_ROWS && !write_tc_eligible(c, w);
+  };
+  return ok(k, wk) && ok(v, wv) && wk.n_rows == wv.n_rows && wk.src_dtype == wv.src_dtype;
+}
+
+cudaError_t launch_step_front(const tq_ctx *k, const tq_ctx *v, const WriteLaunch &wk, const WriteLaunch &wv,
+                              const QprepParams &q, cudaStream_t st) {
+  StepFrontParams sp{};
+  sp.wk = write_params(k, wk);
+  sp.wv = write_params(v, wv);
+  sp.q = q;
+  sp.n_rows = (int)wk.n_rows;
+  sp.q_ctas = (q.n_q + QWARPS - 1) / QWARPS;
+  const bool bf16 = wk.src_dtype == TQ_DTYPE_BF16;
+  const bool k4 = k->fmt == TQ_FMT_TURBO4, v4 = v->fmt == TQ_FMT_TURBO4;
+  static_assert(sizeof(RowScratch) <= QPREP_SMEM, "one dynamic shared area for both roles");
+  auto pick = [&]() {
+    if (bf16) {
+      if (k4) return v4 ? k_step_front<TQ_FMT_TURBO4, TQ_FMT_TURBO4, TQ_DTYPE_BF16>
+                        : k_step_front<TQ_FMT_TURBO4, TQ_FMT_TURBO3, TQ_DTYPE_BF16>;
+      return v4 ? k_step_front<TQ_FMT_TURBO3, TQ_FMT_TURBO4, TQ_DTYPE_BF16>
+                : k_step_front<TQ_FMT_TURBO3, TQ_FMT_TURBO3, TQ_DTYPE_BF16>;
+    }
+    if (k4) return v4 ? k_step_front<TQ_FMT_TURBO4, TQ_FMT_TURBO4, TQ_DTYPE_F32>
+                      : k_step_front<TQ_FMT_TURBO4, TQ_FMT_TURBO3, TQ_DTYPE_F32>;
+    return v4 ? k_step_front<TQ_FMT_TURBO3, TQ_FMT_TURBO4, TQ_DTYPE_F32>
+              : k_step_front<TQ_FMT_TURBO3, TQ_FMT_TURBO3, TQ_DTYPE_F32>;
+  };
+  auto kern = pick();
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)QPREP_SMEM);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(kern, dim3(2 * sp.n_rows + sp.q_ctas), dim3(QWARPS * 32), QPREP_SMEM, st, sp);
 }
 
 }  // namespace tq

@@ -212,6 +212,24 @@ tq_status tq_dequantize(const tq_ctx *ctx, const void *cache, int64_t n_rows, in
  * tq_decode_num_launches tells which for a shape. */
 tq_status tq_decode_workspace_size(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, int Hq,
                                    int Hkv, int L, size_t *bytes);
+/* One decode step: append the step's new K and V rows (SET_ROWS of new_k into k_cache
+ * and new_v into v_cache, n_rows rows each at slots row_ids of the [B][Hkv][L] caches,
+ * as tq_quantize_set_rows), then tq_decode_attention over the updated caches.  The
+ * same results as those three calls; for dense-rotation TURBO4 / TURBO3 caches and at
+ * most 256 rows, the two writes and the q preparation share one launch (they are
+ * independent), so the step has one wait on the previous kernel where the three calls
+ * have three.  Arguments as in tq_quantize_set_rows (dst_rows = B * Hkv * L) and
+ * tq_decode_attention (no scores). */
+tq_status tq_decode_step(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *new_k,
+                         const void *new_v, int src_dtype, int64_t n_rows, int64_t src_row_stride,
+                         const int64_t *row_ids, const void *q, int q_dtype, void *k_cache,
+                         void *v_cache, const int32_t *seq_lens, int B, int Hq, int Hkv, int L,
+                         float scale, float *out, void *workspace, size_t workspace_bytes,
+                         tq_stream_t stream);
+/* Number of kernels tq_decode_step launches for these arguments: 2 or 3 on the one-launch
+ * front (see above), else 2 more for the two writes (none when n_rows == 0). */
+tq_status tq_decode_step_num_launches(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int src_dtype,
+                                      int64_t n_rows, int B, int Hq, int Hkv, int L, int *n);
 /* Number of kernels tq_decode_attention launches for this shape (2 or 3). */
 tq_status tq_decode_num_launches(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, int Hq,
                                  int Hkv, int L, int *n);
