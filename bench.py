@@ -665,7 +665,8 @@ def run_prefill(args, rank, world, dist):
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
-        step_ms = timed_graph_steps(torch, stream, (step,), args.steps, args.warmup, flush_l2)
+        step_ms = timed_graph_steps(torch, stream, (write_and_prepare, partial, combine), args.steps,
+                                    args.warmup, flush_l2)
         part_ms = timed_graph_steps(torch, stream, (partial,), args.steps, args.warmup, flush_l2)
         if dist:
             dist.barrier()

@@ -67,7 +67,7 @@ struct PartialParams {
   const uint8_t *vc;
   const int32_t *seq_lens;
   int B, Hq, Hkv, L, gq, n_hg;
-  int tiles_per_unit, tiles_per_cta, total_tiles, n_part;
+  int tiles_per_unit, tiles_per_cta, vx, total_tiles, n_part;
   const uint32_t *qhl;
   const float *qsc;
   float *part;
@@ -101,8 +101,8 @@ struct SmemHead {
   float mw[CWARPS][8];
   float lw[CWARPS][8];
   int abort_flag;
-  int n_fin;                            // units this CTA completed (fused combine)
-  int fin[FIN_MAX];
+  int n_units;                          // fused combine: the units whose partials this CTA
+  int units[FIN_MAX];                   // wrote; after the counts, the ones it completed
 };
 constexpr uint32_t STAGE_A_OFF = (sizeof(SmemHead) + 15) & ~15u;
 constexpr uint32_t LUT_OFF = LUT_WINDOW - RESERVED_SMEM;
@@ -230,7 +230,7 @@ __global__ void __maxnreg__(128)
       mbar_init(&sm.empty[s], CWARPS);
     }
     sm.abort_flag = 0;
-    sm.n_fin = 0;
+    sm.n_units = 0;
     fence_mbar_init();
   }
   // Fill the table: each (byte, half) entry is computed once and stored to its 32
@@ -258,7 +258,7 @@ __global__ void __maxnreg__(128)
   if (warp == CWARPS) {
     // ---------------- producer: one elected lane streams every tile of every item
     if (lane == 0) {
-      int ctr = 0, tt = cta * p.tiles_per_cta;
+      int ctr = 0, tt = cta_first_tile(p, cta);
       Item it;
       bool ok = true;
       while (ok && next_item(p, cta, tt, it)) {
@@ -290,6 +290,9 @@ __global__ void __maxnreg__(128)
           ++ctr;
         }
       }
+      // R for the merge at the CTA's end, pulled into L2 now: the stream has evicted it,
+      // and the last few tiles take longer than its fetch
+      if (ok && p.out && p.r) bulk_prefetch_l2(p.r, D * D * sizeof(float));
       // Let every issued copy land before the CTA can exit (only matters after a
       // bounded wait gave up; otherwise the consumers have consumed them all).
       if (!ok || sm.abort_flag) {
@@ -320,7 +323,7 @@ __global__ void __maxnreg__(128)
   const int src0 = 4 * t + hs, src1 = 4 * (4 + t) + hs;
   const float lo_sel = (g & 1) ? 1.f : 0.f;
 
-  int ctr = 0, tt = cta * p.tiles_per_cta;
+  int ctr = 0, tt = cta_first_tile(p, cta);
   Item it;
   bool aborted = false;
   while (!aborted && next_item(p, cta, tt, it)) {
@@ -578,17 +581,12 @@ __global__ void __maxnreg__(128)
       }
       consumers_sync();
     }
-    if (p.out) {
-      // fused combine: this CTA's partial of the unit is written (every consumer thread's
-      // stores fenced before the barrier); the CTA whose count completes the unit keeps it
-      // for the merge at its end
-      __threadfence();
-      consumers_sync();
-      if (threadIdx.x == 0) {
-        const int first = it.unit * p.tiles_per_unit;
-        const int n_split = (first + p.tiles_per_unit - 1) / p.tiles_per_cta - first / p.tiles_per_cta + 1;
-        if (atomicAdd(&p.unit_done[it.unit], 1) == n_split - 1 && sm.n_fin < FIN_MAX) sm.fin[sm.n_fin++] = it.unit;
-      }
+    // fused combine: the unit's count is raised once at the CTA's end, for all its items
+    if (p.out && threadIdx.x == 0) {
+      if (sm.n_units < FIN_MAX)
+        sm.units[sm.n_units++] = it.unit;
+      else  // (the host launches the fused form only where a CTA meets at most FIN_MAX units)
+        atomicExch(p.status, (int32_t)DEVERR_LAYOUT);
     }
   }
 
@@ -598,93 +596,145 @@ __global__ void __maxnreg__(128)
   // consumed).  Only after a clean finish: a CTA that gave up leaves its units unwritten
   // and the status flag set.
   if (!p.out) return;
+  // Every consumer thread's partial stores fenced, then one count per item; the CTA whose
+  // count completes a unit merges it.  The atomics are issued together (one round trip).
+  __threadfence();
   consumers_sync();
-  const int n_fin = sm.n_fin;
   // (the flag, read after the barrier, is the same for every consumer warp)
-  if (n_fin == 0 || *reinterpret_cast<volatile int *>(&sm.abort_flag)) return;
-  __threadfence();  // the other CTAs' partials, published before their counts
+  const bool gave_up = *reinterpret_cast<volatile int *>(&sm.abort_flag);
+  if (threadIdx.x == 0 && !gave_up) {
+    const int ni = sm.n_units;
+    int old[FIN_MAX];
+#pragma unroll
+    for (int i = 0; i < FIN_MAX; ++i) old[i] = i < ni ? atomicAdd(&p.unit_done[sm.units[i]], 1) : -1;
+    int nf = 0;  // completed units, compacted in place
+#pragma unroll
+    for (int i = 0; i < FIN_MAX; ++i)
+      if (i < ni && old[i] == unit_n_split(p, sm.units[i]) - 1) sm.units[nf++] = sm.units[i];
+    sm.n_units = nf;
+    __threadfence();  // the other CTAs' partials, published before their counts
+  }
+  consumers_sync();
+  const int n_fin = gave_up ? 0 : sm.n_units;
+  if (n_fin == 0) return;
+  // The completed units' heads in quads of four (NG quads per unit), up to three quads per
+  // round: warp w merges head w % 4 of the round's quad w / 4, and thread (quad, j)
+  // un-rotates dim j of that quad's heads.  R is copied first into the idle stage
+  // buffers (every tile was consumed: the last item ended with a barrier of all consumer
+  // warps), overlapping the first round's loads.
+  constexpr int QUADS = 3;
+  static_assert(4 * QUADS <= CWARPS && QUADS * D <= CWARPS * 32, "a round's heads and dims");
   float *rs = reinterpret_cast<float *>(smem_raw + STAGE_B_OFF);  // R, row-major [128][128]
   static_assert(6 * STAGE_BUF >= D * D * 4, "R fits in the idle stage buffers");
-  if (p.r) {  // asynchronous copy, overlapping the first merge's loads
+  if (p.r) {
     for (int i = threadIdx.x; i < D * D / 4; i += CWARPS * 32)
       asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(rs + 4 * i)), "l"(p.r + 4 * i)
                    : "memory");
     asm volatile("cp.async.commit_group;" ::: "memory");
   }
-  for (int f = 0; f < n_fin; ++f) {
-    const int u = sm.fin[f];
-    const int hg = u % p.n_hg, bk = u / p.n_hg;
-    const int b = bk / p.Hkv, kvh = bk % p.Hkv;
-    const int G = min(4 * NG, p.gq - hg * 4 * NG);
-    const int head0 = kvh * p.gq + hg * 4 * NG;
-    const int first = u * p.tiles_per_unit;
-    const int n_split = (first + p.tiles_per_unit - 1) / p.tiles_per_cta - first / p.tiles_per_cta + 1;
-    if (warp < G) {  // warp w merges head head0 + w; lane l holds dims l + 32 m
-      const float *part = p.part + (size_t)(b * p.Hq + head0 + warp) * p.n_part * PARTIAL_FLOATS;
-      float ms = -INFINITY, lsum = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int s0 = 0; s0 < n_split; s0 += 8) {
-        // eight splits' (max, sum) and accumulator slices loaded at once
-        float mh[8], lh[8], v[8][4];
+  const int n_quads = n_fin * NG;
+  for (int q0 = 0; q0 < n_quads; q0 += QUADS) {
+    {
+      const int qq = q0 + warp / 4;
+      const int u = qq < n_quads ? sm.units[qq / NG] : 0;
+      const int hg = u % p.n_hg, bk = u / p.n_hg;
+      const int b = bk / p.Hkv, kvh = bk % p.Hkv;
+      const int G = min(4 * NG, p.gq - hg * 4 * NG);
+      const int hu = 4 * (qq % NG) + warp % 4;  // head within the unit
+      if (warp < 4 * QUADS && qq < n_quads && hu < G) {
+        const int head = kvh * p.gq + hg * 4 * NG + hu;
+        const int n_split = unit_n_split(p, u);
+        const float *part = p.part + (size_t)(b * p.Hq + head) * p.n_part * PARTIAL_FLOATS;
+        float ms = -INFINITY, lsum = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};  // lane l: dims l + 32 m
+        for (int s0 = 0; s0 < n_split; s0 += 8) {
+          // eight splits' (max, sum) and accumulator slices loaded at once
+          float mh[8], lh[8], v[8][4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float *ps = part + (size_t)min(s0 + i, n_split - 1) * PARTIAL_FLOATS;
-          mh[i] = __ldcg(ps), lh[i] = __ldcg(ps + 1);
+          for (int i = 0; i < 8; ++i) {
+            const float *ps = part + (size_t)min(s0 + i, n_split - 1) * PARTIAL_FLOATS;
+            mh[i] = __ldcg(ps), lh[i] = __ldcg(ps + 1);
 #pragma unroll
-          for (int m = 0; m < 4; ++m) v[i][m] = __ldcg(ps + 6 + lane + 32 * m);
-        }
-        // running merge: raise the max of this chunk's live splits, rescale what is held
-        float mc = -INFINITY;
+            for (int m = 0; m < 4; ++m) v[i][m] = __ldcg(ps + 6 + lane + 32 * m);
+          }
+          // running merge: raise the max of this chunk's live splits, rescale what is held
+          float mc = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          if (s0 + i < n_split && lh[i] > 0.f) mc = fmaxf(mc, mh[i]);
-        if (mc > ms) {
-          const float a = (ms == -INFINITY) ? 0.f : exp2f(ms - mc);
-          lsum *= a;
+          for (int i = 0; i < 8; ++i)
+            if (s0 + i < n_split && lh[i] > 0.f) mc = fmaxf(mc, mh[i]);
+          if (mc > ms) {
+            const float a = (ms == -INFINITY) ? 0.f : exp2f(ms - mc);
+            lsum *= a;
 #pragma unroll
-          for (int m = 0; m < 4; ++m) acc[m] *= a;
-          ms = mc;
-        }
+            for (int m = 0; m < 4; ++m) acc[m] *= a;
+            ms = mc;
+          }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          if (s0 + i < n_split && lh[i] > 0.f) {
-            const float w = exp2f(mh[i] - ms);
-            lsum += w * lh[i];
+          for (int i = 0; i < 8; ++i) {
+            if (s0 + i < n_split && lh[i] > 0.f) {
+              const float w = exp2f(mh[i] - ms);
+              lsum += w * lh[i];
 #pragma unroll
-            for (int m = 0; m < 4; ++m) acc[m] = fmaf(w, v[i][m], acc[m]);
+              for (int m = 0; m < 4; ++m) acc[m] = fmaf(w, v[i][m], acc[m]);
+            }
           }
         }
-      }
-      const float fo = p.inv_vscale / lsum;
+        const float fo = p.inv_vscale / lsum;
 #pragma unroll
-      for (int m = 0; m < 4; ++m) sm.osm[warp][0][lane + 32 * m] = acc[m] * fo;
+        for (int m = 0; m < 4; ++m) sm.osm[warp][0][lane + 32 * m] = acc[m] * fo;
+      }
     }
-    if (f == 0 && p.r) asm volatile("cp.async.wait_all;" ::: "memory");
+    if (q0 == 0 && p.r) asm volatile("cp.async.wait_all;" ::: "memory");
     consumers_sync();  // merged heads (and, the first time, R) in shared memory
-    for (int idx = threadIdx.x; idx < G * D; idx += CWARPS * 32) {
-      const int hh = idx / D, j = idx % D;
-      const float *o = sm.osm[hh][0];
-      float res = o[j];
-      if (p.r) {  // four independent chains over k, summed at the end
-        float c4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-        for (int k = 0; k < D; k += 4) {
+    // out = R^T o: thread (quad, j) reads column j of R once for the four heads of its
+    // quad (o read as broadcast float4), four independent chains over k per head,
+    // summed at the end
+    const int qs = threadIdx.x / D, qq = q0 + qs;
+    if (qs < QUADS && qq < n_quads) {
+      const int u = sm.units[qq / NG];
+      const int hg = u % p.n_hg, bk = u / p.n_hg;
+      const int b = bk / p.Hkv, kvh = bk % p.Hkv;
+      const int G = min(4 * NG, p.gq - hg * 4 * NG);
+      const int hu0 = 4 * (qq % NG);  // first head of the quad within the unit
+      const int j = threadIdx.x % D, hb = 4 * qs;
+      float res[4];
+      if (p.r) {
+        float c4[4][4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) c4[e] = fmaf(rs[(k + e) * D + j], o[k + e], c4[e]);
+        for (int h = 0; h < 4; ++h) c4[h][0] = c4[h][1] = c4[h][2] = c4[h][3] = 0.f;
+#pragma unroll 4
+        for (int k = 0; k < D; k += 4) {
+          const float r0 = rs[k * D + j], r1 = rs[(k + 1) * D + j];
+          const float r2 = rs[(k + 2) * D + j], r3 = rs[(k + 3) * D + j];
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {  // heads past G hold stale values and are not stored
+            const float4 o4 = *reinterpret_cast<const float4 *>(&sm.osm[hb + h][0][k]);
+            c4[h][0] = fmaf(r0, o4.x, c4[h][0]);
+            c4[h][1] = fmaf(r1, o4.y, c4[h][1]);
+            c4[h][2] = fmaf(r2, o4.z, c4[h][2]);
+            c4[h][3] = fmaf(r3, o4.w, c4[h][3]);
+          }
         }
-        res = (c4[0] + c4[1]) + (c4[2] + c4[3]);
+#pragma unroll
+        for (int h = 0; h < 4; ++h) res[h] = (c4[h][0] + c4[h][1]) + (c4[h][2] + c4[h][3]);
+      } else {
+#pragma unroll
+        for (int h = 0; h < 4; ++h) res[h] = sm.osm[hb + h][0][j];
       }
-      p.out[(size_t)(b * p.Hq + head0 + hh) * D + j] = res;
+      const int head0 = kvh * p.gq + hg * 4 * NG + hu0;
+#pragma unroll
+      for (int h = 0; h < 4; ++h)
+        if (hu0 + h < G) p.out[(size_t)(b * p.Hq + head0 + h) * D + j] = res[h];
     }
-    if (threadIdx.x == 0) p.unit_done[u] = 0;
-    consumers_sync();
+    consumers_sync();  // the round's merged heads are free again
   }
+  if (threadIdx.x < n_fin) p.unit_done[sm.units[threadIdx.x]] = 0;
 }
 
 struct CombineParams {
   const float *part;
   int n_heads;      // B * Hq (decode) or B * T * Hq (prefill rows)
   int n_split;      // partial slots per head
-  int Hq, gq, heads_per_cta, n_hg, tiles_per_unit, tiles_per_cta;
+  int Hq, gq, heads_per_cta, n_hg, tiles_per_unit, tiles_per_cta, vx;
   int pf_T, pf_Hkv, pf_qpt, pf_n_qt;  // prefill geometry (pf_T = 0: decode)
   int no_main;      // 1: no split-K partials (every key is in the exact tail)
   int tail_slot;    // slot of an exact-tail partial per head, or -1
@@ -717,8 +767,7 @@ __global__ void __launch_bounds__(QWARPS * 32) k_combine(const CombineParams p) 
       const int b = bh / p.Hq, h = bh % p.Hq;
       unit = (b * (p.Hq / p.gq) + h / p.gq) * p.n_hg + (h % p.gq) / p.heads_per_cta;
     }
-    const int first = unit * p.tiles_per_unit;
-    const int n_main = p.no_main ? 0 : ((first + p.tiles_per_unit - 1) / p.tiles_per_cta) - first / p.tiles_per_cta + 1;
+    const int n_main = p.no_main ? 0 : unit_n_split(p, unit);
     const int n_split = n_main + (p.tail_slot >= 0 ? 1 : 0);
     auto slot = [&](int s) { return s < n_main ? s : p.tail_slot; };  // the tail partial last
     float ms = -INFINITY;
@@ -799,12 +848,15 @@ bool decode_shape(const tq_ctx *k, const tq_ctx *v, int B, int Hq, int Hkv, int 
   const int64_t units = (int64_t)B * Hkv * s->n_hg;
   s->tiles_per_unit = (L + s->tile - 1) / s->tile;
   const int64_t total = units * s->tiles_per_unit;
-  if (total > INT32_MAX) return false;
+  s->vx = s->pv ? PV_ITEM_TILES : k->fmt == TQ_FMT_TURBO3 ? T3_ITEM_TILES : T4_ITEM_TILES;
+  const int64_t vtotal = units * (s->vx + s->tiles_per_unit);
+  if (vtotal > INT32_MAX) return false;
   s->total_tiles = (int)total;
-  // One persistent CTA per SM; contiguous equal tile ranges (the last may be shorter).
-  const int64_t tpc = (total + k->num_sms - 1) / k->num_sms;
+  // One persistent CTA per SM; contiguous equal ranges of the virtual tile sequence
+  // (each unit with its item cost ahead of its tiles; the last range may be shorter).
+  const int64_t tpc = (vtotal + k->num_sms - 1) / k->num_sms;
   s->tiles_per_cta = (int)(tpc < 1 ? 1 : tpc);
-  s->grid = (int)((total + s->tiles_per_cta - 1) / s->tiles_per_cta);
+  s->grid = (int)((vtotal + s->tiles_per_cta - 1) / s->tiles_per_cta);
   // Partial slots per head: CTAs whose range meets one unit.
   s->n_part = (s->tiles_per_unit + s->tiles_per_cta - 1) / s->tiles_per_cta + 1;
   return true;
@@ -892,9 +944,9 @@ cudaError_t launch_t4_variant(const PartialParams &p, int heads_per_cta, bool fi
 }
 
 // The fused combine serves the plain turbo4 / turbo3-key decode (no exact tail) when a CTA
-// completes at most FIN_MAX units: it touches at most tiles_per_cta / tiles_per_unit + 2.
+// completes at most FIN_MAX units: it touches at most tiles_per_cta / (vx + tiles_per_unit) + 2.
 bool partial_fuses_combine(const DecodeShape &s) {
-  return !s.pv && s.tail_slot < 0 && !s.no_main && s.tiles_per_cta / s.tiles_per_unit + 2 <= FIN_MAX;
+  return !s.pv && s.tail_slot < 0 && !s.no_main && s.tiles_per_cta / (s.vx + s.tiles_per_unit) + 2 <= FIN_MAX;
 }
 
 cudaError_t launch_partial(const tq_ctx *k, const tq_ctx *v, const uint8_t *kc,
@@ -914,7 +966,7 @@ cudaError_t launch_partial(const tq_ctx *k, const tq_ctx *v, const uint8_t *kc,
   p.withhold_first_tile = withhold_first_tile ? 1 : 0;
   p.kc = kc, p.vc = vc, p.seq_lens = seq_lens;
   p.B = s.B, p.Hq = s.Hq, p.Hkv = s.Hkv, p.L = s.L, p.gq = s.gq, p.n_hg = s.n_hg;
-  p.tiles_per_unit = s.tiles_per_unit, p.tiles_per_cta = s.tiles_per_cta;
+  p.tiles_per_unit = s.tiles_per_unit, p.tiles_per_cta = s.tiles_per_cta; p.vx = s.vx;
   p.total_tiles = s.total_tiles, p.n_part = s.n_part;
   p.qhl = ws.qhl, p.qsc = ws.qsc, p.part = ws.partials, p.scores = scores_dbg;
   const bool k3 = k->fmt == TQ_FMT_TURBO3;
@@ -949,7 +1001,7 @@ cudaError_t launch_combine(const tq_ctx *k, const tq_ctx *v, const DecodeShape &
   p.n_heads = s.B * s.Hq;
   p.n_split = s.n_part;
   p.Hq = s.Hq, p.gq = s.gq, p.heads_per_cta = s.heads_per_cta, p.n_hg = s.n_hg;
-  p.tiles_per_unit = s.tiles_per_unit, p.tiles_per_cta = s.tiles_per_cta;
+  p.tiles_per_unit = s.tiles_per_unit, p.tiles_per_cta = s.tiles_per_cta; p.vx = s.vx;
   p.no_main = s.no_main ? 1 : 0;
   p.tail_slot = s.tail_slot;
   const bool vgroup = v->fmt == TQ_FMT_VGROUP2;  // values are not rotated
@@ -970,6 +1022,7 @@ cudaError_t launch_combine_prefill(const tq_ctx *v, const PrefillShape &s, float
   p.n_split = s.n_part;
   p.Hq = s.Hq, p.gq = s.gq;
   p.tiles_per_unit = s.tiles_per_unit, p.tiles_per_cta = s.tiles_per_cta;
+  p.vx = 0;  // the prefill splits its tiles equally
   p.pf_T = s.T, p.pf_Hkv = s.Hkv, p.pf_qpt = s.qpt, p.pf_n_qt = s.n_qt;
   p.tail_slot = -1;
   p.r = v->d_pi;

@@ -22,18 +22,47 @@ constexpr uint32_t RESERVED_SMEM = 1024;  // window bytes before dynamic smem (u
 // Work item = the tiles of one unit (batch, KV head, head group) inside this CTA's
 // contiguous range of the global tile sequence; units are laid end to end, so a CTA
 // touches at most a few units and each (unit, CTA) pair gives one partial.
+//
+// Cost-balanced ranges: each unit counts vx virtual tiles ahead of its tiles_per_unit
+// real ones (the fixed cost of one more item: the warps' merge, the partial's write,
+// the next unit's q), and every CTA takes tiles_per_cta tiles of that virtual sequence,
+// so a CTA whose range crosses into another unit gets fewer real tiles.  vx = 0 is an
+// equal split of the real tiles.
 struct Item {
   int unit, t0, t1, slot;  // tiles [t0, t1) of the unit; partial slot of this CTA
 };
 
+// First real tile at or after virtual position v.
+template <typename P>
+__device__ __forceinline__ int real_tile(const P &p, int64_t v) {
+  const int64_t vu = (int64_t)p.vx + p.tiles_per_unit;
+  const int64_t u = v / vu;
+  const int64_t o = v - u * vu - p.vx;
+  return (int)(u * p.tiles_per_unit + (o > 0 ? o : 0));
+}
+template <typename P>
+__device__ __forceinline__ int cta_first_tile(const P &p, int cta) {
+  return min(real_tile(p, (int64_t)cta * p.tiles_per_cta), p.total_tiles);
+}
+// CTAs whose range meets unit u: unit_first_cta(u) .. + unit_n_split(u) - 1.
+template <typename P>
+__device__ __forceinline__ int unit_first_cta(const P &p, int u) {
+  return (int)(((int64_t)u * (p.vx + p.tiles_per_unit) + p.vx) / p.tiles_per_cta);
+}
+template <typename P>
+__device__ __forceinline__ int unit_n_split(const P &p, int u) {
+  const int64_t v0 = (int64_t)u * (p.vx + p.tiles_per_unit) + p.vx;
+  return (int)((v0 + p.tiles_per_unit - 1) / p.tiles_per_cta - v0 / p.tiles_per_cta + 1);
+}
+
 template <typename P>
 __device__ __forceinline__ bool next_item(const P &p, int cta, int &t, Item &it) {
-  const int end = min((cta + 1) * p.tiles_per_cta, p.total_tiles);
+  const int end = cta_first_tile(p, cta + 1);
   if (t >= end) return false;
   it.unit = t / p.tiles_per_unit;
   it.t0 = t - it.unit * p.tiles_per_unit;
   it.t1 = min(end - it.unit * p.tiles_per_unit, p.tiles_per_unit);
-  it.slot = cta - (it.unit * p.tiles_per_unit) / p.tiles_per_cta;
+  it.slot = cta - unit_first_cta(p, it.unit);
   t += it.t1 - it.t0;
   return true;
 }

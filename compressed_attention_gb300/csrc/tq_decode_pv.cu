@@ -50,7 +50,7 @@ struct PvParams {
   const uint8_t *vc;
   const int32_t *seq_lens;
   int B, Hq, Hkv, L, gq, n_hg;
-  int tiles_per_unit, tiles_per_cta, total_tiles, n_part;
+  int tiles_per_unit, tiles_per_cta, vx, total_tiles, n_part;
   const uint32_t *qhl;
   const float *qsc;
   float *part;
@@ -146,7 +146,7 @@ __global__ void __maxnreg__(168) k_partial_pv(const PvParams p) {
   if (warp == CW) {
     // ---------------- producer
     if (lane == 0) {
-      int ctr = 0, tt = cta * p.tiles_per_cta;
+      int ctr = 0, tt = cta_first_tile(p, cta);
       Item it;
       bool ok = true;
       while (ok && next_item(p, cta, tt, it)) {
@@ -194,7 +194,7 @@ __global__ void __maxnreg__(168) k_partial_pv(const PvParams p) {
   const uint32_t code_sel = (uint32_t)(g & 3) | ((4u + (g & 3)) << 8);
   const int code_word = 4 * (g >> 2);  // byte offset of word (g >> 2) inside a group
 
-  int ctr = 0, tt = cta * p.tiles_per_cta;
+  int ctr = 0, tt = cta_first_tile(p, cta);
   Item it;
   bool aborted = false;
   while (!aborted && next_item(p, cta, tt, it)) {
@@ -445,7 +445,7 @@ cudaError_t launch_partial_pv(const tq_ctx *k, const tq_ctx *v, const uint8_t *k
   PvParams p{};
   p.kc = kc, p.vc = vc, p.seq_lens = seq_lens;
   p.B = s.B, p.Hq = s.Hq, p.Hkv = s.Hkv, p.L = s.L, p.gq = s.gq, p.n_hg = s.n_hg;
-  p.tiles_per_unit = s.tiles_per_unit, p.tiles_per_cta = s.tiles_per_cta;
+  p.tiles_per_unit = s.tiles_per_unit, p.tiles_per_cta = s.tiles_per_cta, p.vx = s.vx;
   p.total_tiles = s.total_tiles, p.n_part = s.n_part;
   p.qhl = ws.qhl, p.qsc = ws.qsc, p.part = ws.partials, p.scores = scores_dbg;
   p.kc16[0] = k->f16.c16[0], p.kc16[1] = k->f16.c16[1];

@@ -157,6 +157,11 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
 
 // 1-D bulk copy global -> shared, completing `bytes` of transaction on `bar`.
 // dst and src 16-byte aligned, bytes a multiple of 16.
+// Prefetch `bytes` (a multiple of 16, 16-byte aligned source) into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
                                          uint64_t *bar) {
   asm volatile(

@@ -128,6 +128,11 @@ cudaError_t launch_dequantize(const tq_ctx *ctx, const uint8_t *cache, int64_t n
 
 constexpr int T4_TILE = 240;  // keys per tile of the turbo4 decode
 constexpr int PV_TILE = 176;  // keys per tile of the prod3-key / vgroup2-value decode
+// Fixed cost of one more work item in a CTA's range (the consumer warps' merge, the
+// partial's write, the next unit's q), in tiles of the kernel's own streaming time.
+constexpr int T4_ITEM_TILES = 4;
+constexpr int T3_ITEM_TILES = 3;  // turbo3 keys: longer tiles
+constexpr int PV_ITEM_TILES = 2;
 
 struct DecodeShape {
   int B, Hq, Hkv, L;
@@ -138,7 +143,9 @@ struct DecodeShape {
   int n_hg;     // head groups per KV head
   int tiles_per_unit;  // key tiles of one (batch, KV head, head group) unit
   int total_tiles;     // over all units, laid end to end
-  int tiles_per_cta;   // contiguous range per persistent CTA
+  int tiles_per_cta;   // contiguous range per persistent CTA, in virtual tiles: each
+                       // unit counts vx tiles of item cost ahead of its own
+  int vx;
   int grid;            // persistent CTAs (at most one per SM)
   int n_part;          // partial slots per head
   int tail_slot = -1;  // slot of an exact-tail partial (the store's ring), or -1

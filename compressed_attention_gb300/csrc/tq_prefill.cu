@@ -90,7 +90,7 @@ struct PrefillParams {
   const uint8_t *vc;
   const int32_t *q_start;   // [B] position of each sequence's first chunk query
   int B, T, Hq, Hkv, L, gq, qpt, n_qt;
-  int tiles_per_unit, tiles_per_cta, total_tiles, n_part;
+  int tiles_per_unit, tiles_per_cta, vx, total_tiles, n_part;  // vx = 0: equal tile ranges
   const uint32_t *qhl;      // prepared q: [B*T*Hq][256 words], hi then lo fp16
   const float *qsc;         // [B*T*Hq][2] power-of-two scales
   float *part;              // [B*T*Hq][n_part][PARTIAL_FLOATS]
@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) k_prefill_t4(const PrefillParam
     return done;
   };
 
-  int t = blockIdx.x * p.tiles_per_cta;
+  int t = cta_first_tile(p, (int)blockIdx.x);
   Item it;
   while (next_item(p, (int)blockIdx.x, t, it)) {
     __syncthreads();  // the previous item is finished by every warp
@@ -618,7 +618,7 @@ cudaError_t launch_prefill(const tq_ctx *k, const tq_ctx *v, const uint8_t *kc, 
   PrefillParams p{};
   p.kc = kc, p.vc = vc, p.q_start = q_start;
   p.B = s.B, p.T = s.T, p.Hq = s.Hq, p.Hkv = s.Hkv, p.L = s.L, p.gq = s.gq, p.qpt = s.qpt, p.n_qt = s.n_qt;
-  p.tiles_per_unit = s.tiles_per_unit, p.tiles_per_cta = s.tiles_per_cta;
+  p.tiles_per_unit = s.tiles_per_unit, p.tiles_per_cta = s.tiles_per_cta, p.vx = 0;
   p.total_tiles = s.total_tiles, p.n_part = s.n_part;
   p.qhl = ws.qhl, p.qsc = ws.qsc, p.part = ws.partials;
   for (int i = 0; i < 2; ++i) {
