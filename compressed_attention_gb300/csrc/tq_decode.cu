@@ -904,8 +904,6 @@ cudaError_t launch_prepare_q(const tq_ctx *k, const void *q, int q_dtype, const 
   const int grid = (p.n_q + QWARPS - 1) / QWARPS;
   auto kern = s.pv ? k_prepare_q<true> : k_prepare_q<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)QPREP_SMEM);
-  if (e == cudaSuccess)  // the decode's carveout (no reconfiguration between the two)
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(grid), dim3(QWARPS * 32), QPREP_SMEM, st, p);
 }

@@ -860,10 +860,6 @@ cudaError_t launch_step_front(const tq_ctx *k, const tq_ctx *v, const WriteLaunc
   };
   auto kern = pick();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)QPREP_SMEM);
-  // the split-K decode that follows wants the whole shared-memory carveout: ask for the
-  // same split so that the SMs need not be reconfigured between the two
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(2 * sp.n_rows + sp.q_ctas), dim3(QWARPS * 32), QPREP_SMEM, st, sp);
 }
