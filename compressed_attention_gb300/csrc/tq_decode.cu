@@ -634,24 +634,28 @@ __global__ void __maxnreg__(128)
   }
   const int n_quads = n_fin * NG;
   for (int q0 = 0; q0 < n_quads; q0 += QUADS) {
-    {
-      const int qq = q0 + warp / 4;
-      const int u = qq < n_quads ? sm.units[qq / NG] : 0;
+    // nh heads this round; W warps per head split its partials between them (warp w takes
+    // head slot w % nh and every W-th chunk of eight splits from chunk w / nh)
+    const int nh = 4 * min(QUADS, n_quads - q0), W = (4 * QUADS) / nh;
+    const int hs = warp % nh, part = warp / nh;
+    if (part < W) {
+      const int qq = q0 + hs / 4;
+      const int u = sm.units[qq / NG];
       const int hg = u % p.n_hg, bk = u / p.n_hg;
       const int b = bk / p.Hkv, kvh = bk % p.Hkv;
       const int G = min(4 * NG, p.gq - hg * 4 * NG);
-      const int hu = 4 * (qq % NG) + warp % 4;  // head within the unit
-      if (warp < 4 * QUADS && qq < n_quads && hu < G) {
+      const int hu = 4 * (qq % NG) + hs % 4;  // head within the unit
+      float ms = -INFINITY, lsum = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};  // lane l: dims l + 32 m
+      if (hu < G) {
         const int head = kvh * p.gq + hg * 4 * NG + hu;
         const int n_split = unit_n_split(p, u);
-        const float *part = p.part + (size_t)(b * p.Hq + head) * p.n_part * PARTIAL_FLOATS;
-        float ms = -INFINITY, lsum = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};  // lane l: dims l + 32 m
-        for (int s0 = 0; s0 < n_split; s0 += 8) {
+        const float *part_base = p.part + (size_t)(b * p.Hq + head) * p.n_part * PARTIAL_FLOATS;
+        for (int s0 = 8 * part; s0 < n_split; s0 += 8 * W) {
           // eight splits' (max, sum) and accumulator slices loaded at once
           float mh[8], lh[8], v[8][4];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const float *ps = part + (size_t)min(s0 + i, n_split - 1) * PARTIAL_FLOATS;
+            const float *ps = part_base + (size_t)min(s0 + i, n_split - 1) * PARTIAL_FLOATS;
             mh[i] = __ldcg(ps), lh[i] = __ldcg(ps + 1);
 #pragma unroll
             for (int m = 0; m < 4; ++m) v[i][m] = __ldcg(ps + 6 + lane + 32 * m);
@@ -678,10 +682,30 @@ __global__ void __maxnreg__(128)
             }
           }
         }
-        const float fo = p.inv_vscale / lsum;
-#pragma unroll
-        for (int m = 0; m < 4; ++m) sm.osm[warp][0][lane + 32 * m] = acc[m] * fo;
       }
+      // this warp's share of the head: (max, sum) and its unnormalised accumulator
+      if (lane == 0) sm.mw[warp][0] = ms, sm.lw[warp][0] = lsum;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) sm.osm[warp][1][lane + 32 * m] = acc[m];
+    }
+    consumers_sync();
+    if (warp < nh) {  // the W shares of head slot `warp`, merged (heads past G unused)
+      float mx = -INFINITY;
+      for (int pp = 0; pp < W; ++pp) mx = fmaxf(mx, sm.mw[warp + pp * nh][0]);
+      float lt = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int pp = 0; pp < W; ++pp) {
+        const int w2 = warp + pp * nh;
+        const float m2 = sm.mw[w2][0];
+        if (m2 != -INFINITY) {
+          const float f = exp2f(m2 - mx);
+          lt += f * sm.lw[w2][0];
+#pragma unroll
+          for (int m = 0; m < 4; ++m) o[m] = fmaf(f, sm.osm[w2][1][lane + 32 * m], o[m]);
+        }
+      }
+      const float fo = lt > 0.f ? p.inv_vscale / lt : 0.f;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) sm.osm[warp][0][lane + 32 * m] = o[m] * fo;
     }
     if (q0 == 0 && p.r) asm volatile("cp.async.wait_all;" ::: "memory");
     consumers_sync();  // merged heads (and, the first time, R) in shared memory
