@@ -84,6 +84,12 @@ def test_host_validation_errors(tq):
     assert lib.tq_quantize_set_rows(None, None, 0, 1, 128, None, None, 1, None) == tq.TQ_ERR_INVALID_ARG
     assert lib.tq_decode_attention(None, None, None, 0, None, None, None, 1, 1, 1, 1, 0.0, None, None,
                                    None, 0, None) == tq.TQ_ERR_INVALID_ARG
+    assert lib.tq_decode_step(None, None, None, None, 0, 1, 128, None, None, 0, None, None, None, 1, 1, 1, 1,
+                              0.0, None, None, 0, None) == tq.TQ_ERR_INVALID_ARG
+    n = ctypes.c_int32(-1)
+    assert lib.tq_decode_step_num_launches(None, None, 0, 1, 1, 1, 1, 1, ctypes.byref(n)) == tq.TQ_ERR_INVALID_ARG
+    assert lib.tq_decode_step_num_launches(None, None, 0, 1, 1, 1, 1, 1, None) == tq.TQ_ERR_INVALID_ARG
+    assert n.value == -1  # untouched on failure
     p = tq.tq_params(64, 0, 0, 0, 0, 0, 0, 0)
     h = ctypes.c_void_p()
     assert lib.tq_ctx_create(ctypes.byref(p), ctypes.byref(h)) == tq.TQ_ERR_UNSUPPORTED
