@@ -618,10 +618,10 @@ __global__ void __maxnreg__(128)
   const int n_fin = gave_up ? 0 : sm.n_units;
   if (n_fin == 0) return;
   // The completed units' heads in quads of four (NG quads per unit), up to three quads per
-  // round: warp w merges head w % 4 of the round's quad w / 4, and thread (quad, j)
-  // un-rotates dim j of that quad's heads.  R is copied first into the idle stage
-  // buffers (every tile was consumed: the last item ended with a barrier of all consumer
-  // warps), overlapping the first round's loads.
+  // round: the round's nh heads are merged by twelve warps (W = 12 / nh per head, see
+  // below), and thread (quad, j) un-rotates dim j of that quad's heads.  R is copied
+  // first into the idle stage buffers (every tile was consumed: the last item ended with
+  // a barrier of all consumer warps), overlapping the first round's loads.
   constexpr int QUADS = 3;
   static_assert(4 * QUADS <= CWARPS && QUADS * D <= CWARPS * 32, "a round's heads and dims");
   float *rs = reinterpret_cast<float *>(smem_raw + STAGE_B_OFF);  // R, row-major [128][128]
