@@ -34,6 +34,25 @@ def test_header_declares_the_boundary():
         assert required in names
 
 
+def declared_arity():
+    """Parameter count of every function the header declares."""
+    text = open(os.path.join(ROOT, "include", "tq.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    out = {}
+    for m in re.finditer(r"\b(tq_[a-z0-9_]+)\s*\(([^;{]*?)\)\s*;", text):
+        params = m.group(2).strip()
+        out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_matches_the_header(tq):
+    """The Python binding declares every header function, with as many arguments."""
+    decl, sig = declared_arity(), tq._SIGNATURES
+    assert sorted(decl) == sorted(sig)
+    assert {n: len(sig[n][1]) for n in decl} == decl
+
+
 def test_library_exports_every_declared_symbol(tq):
     lib = ctypes.CDLL(tq.LIB_PATH)
     missing = [n for n in declared_functions() if not hasattr(lib, n)]
