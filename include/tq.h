@@ -212,14 +212,20 @@ tq_status tq_dequantize(const tq_ctx *ctx, const void *cache, int64_t n_rows, in
  * tq_decode_num_launches tells which for a shape. */
 tq_status tq_decode_workspace_size(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, int Hq,
                                    int Hkv, int L, size_t *bytes);
-/* One decode step: append the step's new K and V rows (SET_ROWS of new_k into k_cache
- * and new_v into v_cache, n_rows rows each at slots row_ids of the [B][Hkv][L] caches,
- * as tq_quantize_set_rows), then tq_decode_attention over the updated caches.  The
- * same results as those three calls; for dense-rotation TURBO4 / TURBO3 caches and at
- * most 256 rows, the two writes and the q preparation share one launch (they are
- * independent), so the step has one wait on the previous kernel where the three calls
- * have three.  Arguments as in tq_quantize_set_rows (dst_rows = B * Hkv * L) and
- * tq_decode_attention (no scores). */
+/* One decode step ([turbo4 post-mortem] §1-§2 for the row writes, [Triton deep dive]
+ * tricks 1-3 for the decode): append the step's new K and V rows (SET_ROWS of new_k
+ * into k_cache and new_v into v_cache, n_rows rows each at slots row_ids of the
+ * [B][Hkv][L] caches, as tq_quantize_set_rows), then tq_decode_attention over the
+ * updated caches.  The same results as those three calls; for dense-rotation TURBO4 /
+ * TURBO3 caches and at most 256 rows, the two writes and the q preparation share one
+ * launch (they are independent), so the step has one wait on the previous kernel where
+ * the three calls have three.  Arguments as in tq_quantize_set_rows (dst_rows =
+ * B * Hkv * L; new_k and new_v share src_dtype and src_row_stride) and
+ * tq_decode_attention (no scores); every buffer is the caller's device memory, used in
+ * stream order.  Errors: all the checks of the three calls are made before anything is
+ * launched (TQ_ERR_INVALID_ARG, TQ_ERR_ALIGNMENT, TQ_ERR_UNSUPPORTED, TQ_ERR_WORKSPACE);
+ * a slot outside the caches is skipped and flagged in the context's device status, as
+ * in tq_quantize_set_rows. */
 tq_status tq_decode_step(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *new_k,
                          const void *new_v, int src_dtype, int64_t n_rows, int64_t src_row_stride,
                          const int64_t *row_ids, const void *q, int q_dtype, void *k_cache,
