@@ -120,3 +120,16 @@ def test_host_validation_errors(tq):
     p = tq.tq_params(128, tq.TQ_FMT_TURBO4, tq.TQ_CB_SPHERE + 1, tq.TQ_ROT_WHT, 7, 8, 0, 0)
     assert lib.tq_ctx_create(ctypes.byref(p), ctypes.byref(h)) == tq.TQ_ERR_INVALID_ARG
     assert lib.tq_status_string(tq.TQ_ERR_WORKSPACE) == b"workspace too small"
+
+
+def test_decode_step_binding_rejects_mismatched_rows(tq):
+    """The binding hands one source dtype and row stride to the C call, so new K and V
+    rows that differ in either are refused before anything reaches the library."""
+    import torch
+
+    class Ctx:
+        handle = None
+    k = torch.zeros((4, 128), dtype=torch.bfloat16)
+    for v in (torch.zeros((4, 128), dtype=torch.float32), torch.zeros((8, 128), dtype=torch.bfloat16)[::2]):
+        with pytest.raises(ValueError):
+            tq.tq_decode_step(Ctx, Ctx, k, v, None, None, None, None, None, 1, 4, 1, 8)

@@ -1,0 +1,44 @@
+"""Host-side parts of the benchmark that need no GPU: the reference arm (the oracle on
+the host cores) and the workload configs the JSON line reports."""
+
+import json
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_reference_arm_json_line():
+    """`bench.py --impl reference` (the oracle on the host cores) prints one JSON line with
+    the contract's keys; its end-to-end number moves no bytes between host and device."""
+    import subprocess
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "0"], capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["steps"] == 1 and d["warmup"] >= 3
+    assert d["value"] > 0 and d["unit"] == "GB/s" and d["higher_is_better"] is True
+    assert d["config"]["workload"].startswith("gqa_lognormal")
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["value"] == d["value"] and d["cpu_baseline"]["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_bench_configs_name_their_workloads():
+    """Every decode workload's config names it with its sizes and formats (the JSON line's
+    `config`), and the default workload is the GQA decode at 32K keys."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth
+    for name in bench.DECODE:
+        c = bench.decode_config(name)
+        w = synth.WORKLOADS[name]
+        assert c["workload"].startswith(f"{name}: B={w['B']} Hq={w['Hq']} Hkv={w['Hkv']} d=128 L={w['L']}")
+        assert c["k_format"] in ("turbo4", "turbo3", "prod3") and c["v_format"] in ("turbo4", "vgroup2")
+        assert "flushed" in c["l2"]
+    d = bench.decode_config("gqa_lognormal")
+    assert (d["B"], d["Hq"], d["Hkv"], d["L"], d["rotation"]) == (8, 32, 8, 32768, "dense")
+    p = bench.prefill_config()
+    assert p["mask"] == "causal" and p["T"] == synth.WORKLOADS["prefill_chunk"]["T"]
