@@ -122,3 +122,40 @@ def test_prefill_mask_off_by_one_is_caught(monkeypatch):
         monkeypatch.setattr(oracle, "prefill_reference", broken)
         with pytest.raises(AssertionError):
             pins.test_identical_keys_give_prefix_means()
+
+
+def test_vgroup_scale_zero_swapped_is_caught(monkeypatch):
+    """A value dequantizer that reads the group's zero as its scale (and the scale as its
+    zero) breaks the half-step reconstruction bound of the group quantizer."""
+    from oracle.formats import Codec
+    x = np.random.default_rng(9).standard_normal((300, D)).astype(np.float32) * 2.0
+    codes, s16, z16 = oracle.encode_vgroup(x)
+    blk = oracle.pack_vgroup(codes, s16, z16)
+    s = np.repeat(s16.astype(np.float64), 32, axis=1)
+
+    def within_bound(xh):
+        return bool(np.all(np.abs(xh - x) <= 0.5 * s + 2e-3 * np.abs(x).max()))
+
+    assert within_bound(Codec("vgroup2").dequantize(blk))
+    good = fm.unpack_vgroup
+
+    def swapped(blocks):
+        c, sc, ze = good(blocks)
+        return c, ze, sc
+
+    monkeypatch.setattr(fm, "unpack_vgroup", swapped)
+    assert not within_bound(Codec("vgroup2").dequantize(blk))
+
+
+def test_turbo3_sign_bit_order_is_caught():
+    """Sign bits stored most-significant first in their byte (instead of bit j % 8 for
+    element j) contradict the layout the pages print, which the by-hand pin checks."""
+    idx = (np.arange(D) % 8).astype(np.uint8)[None, :]
+    good = oracle.pack_turbo3(np.array([1.0], np.float32), idx)
+    bad = good.copy()
+    for c in range(4):
+        sl = slice(14 * c + 10, 14 * c + 14)
+        bad[:, sl] = np.packbits(np.unpackbits(bad[:, sl], axis=1, bitorder="little"), axis=1, bitorder="big")
+    for blk, ok in ((good, True), (bad, False)):
+        assert (list(blk[0, 10:14]) == [0xF0] * 4) == ok
+        assert np.array_equal(oracle.unpack_turbo3(blk)[1], idx) == ok
