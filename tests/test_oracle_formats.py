@@ -263,3 +263,51 @@ def test_qjl_estimator_energy_and_shrinkage_mse():
         v = np.asarray(v)
         assert abs(v.mean() - (s * s * kappa - 2 * s + 1)) < 4 * v.std() / np.sqrt(n)
     assert np.mean(err[QJL_SHRINK]) < np.mean(err[1.0])
+
+
+def norm_tree_row():
+    """The row of tests/golden/norm_tree_row.txt."""
+    x = np.zeros((1, D), np.float32)
+    x[0, 0] = 8192.0
+    for lane in (2, 4, 8, 16):
+        x[0, 4 * lane] = 2.0
+    for lane in range(1, 32, 2):
+        x[0, 4 * lane:4 * lane + 3] = 1.0
+    return x
+
+
+def test_canonical_norm_tree_order_by_hand():
+    """The fp32 norm follows the canonical addition order exactly: a row whose sum depends
+    on the order gives the bits derived by hand from that order (golden file)."""
+    from conftest import golden_lines
+    fields = dict(ln.split()[:2] for ln in golden_lines("norm_tree_row.txt"))
+    n = oracle.canonical_norm_fp32(norm_tree_row())
+    assert int(n.view(np.uint32)[0]) == int(fields["n_bits"], 16)
+
+
+def test_wht_signs_take_the_top_bit():
+    """Sign j is -1 exactly when the top bit of splitmix64 output j is set: the golden
+    outputs of seed 0 start 0xe220..., 0x6e78..., 0x06c4..., so the signs are -1, +1, +1."""
+    from conftest import golden_lines
+    outs = [int(v, 16) for v in golden_lines("splitmix64_seed0.txt")]
+    assert [o >> 63 for o in outs] == [1, 0, 0]
+    assert list(oracle.wht_signs(0, 3)) == [-1.0, 1.0, 1.0]
+
+
+def test_prod3_layout_by_hand():
+    """fp32 norm at bytes 0-3, fp32 residual norm at 4-7, 2-bit index of element j at bits
+    2*(j%4) of byte 8 + j/4, QJL sign i at bit i%8 of byte 40 + i/8 (1 = +1)."""
+    j = np.arange(D)
+    idx = np.stack([j % 4, (j // 4) % 4]).astype(np.uint8)
+    signs = np.stack([(j % 8 == 0), (j < 8) | (j % 8 == 7)]).astype(np.uint8)
+    blk = oracle.pack_prod(np.array([2.0, 2.0], np.float32), np.array([0.5, 0.5], np.float32), idx, signs)
+    for r in range(2):
+        assert list(blk[r, 0:4]) == [0, 0, 0, 0x40]  # 2.0f = 0x40000000
+        assert list(blk[r, 4:8]) == [0, 0, 0, 0x3F]  # 0.5f = 0x3F000000
+    assert list(blk[0, 8:40]) == [0xE4] * 32  # elements 0..3 = 0, 1, 2, 3 -> 0b11100100
+    assert list(blk[1, 8:40]) == [0x00, 0x55, 0xAA, 0xFF] * 8  # four equal codes per byte
+    assert list(blk[0, 40:56]) == [0x01] * 16  # bit 0 of every byte
+    assert list(blk[1, 40:56]) == [0xFF] + [0x80] * 15  # signs 0..7, then bit 7 of each byte
+    n, g, back, sb = oracle.unpack_prod(blk)
+    assert np.all(n == 2.0) and np.all(g == 0.5)
+    assert np.array_equal(back, idx) and np.array_equal(sb, signs)

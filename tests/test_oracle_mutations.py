@@ -159,3 +159,77 @@ def test_turbo3_sign_bit_order_is_caught():
     for blk, ok in ((good, True), (bad, False)):
         assert (list(blk[0, 10:14]) == [0xF0] * 4) == ok
         assert np.array_equal(oracle.unpack_turbo3(blk)[1], idx) == ok
+
+
+def test_prod3_sign_bits_reversed_is_caught(monkeypatch):
+    """QJL sign i stored at bit 7 - i%8 (in both the packer and the unpacker, so a round
+    trip still passes) contradicts the by-hand byte layout."""
+    import test_oracle_formats as pins
+    good_pack, good_unpack = fm.pack_prod, fm.unpack_prod
+
+    def rev(b):
+        return np.packbits(np.unpackbits(b, axis=1, bitorder="little"), axis=1, bitorder="big")
+
+    def pack(n32, gamma32, idx, sign_bits):
+        out = good_pack(n32, gamma32, idx, sign_bits)
+        out[:, 40:56] = rev(out[:, 40:56])
+        return out
+
+    def unpack(blocks):
+        b = np.array(blocks, dtype=np.uint8, copy=True)
+        b[:, 40:56] = rev(b[:, 40:56])
+        return good_unpack(b)
+
+    for name, f in (("pack_prod", pack), ("unpack_prod", unpack)):
+        monkeypatch.setattr(oracle, name, f)
+        monkeypatch.setattr(fm, name, f)
+    with pytest.raises(AssertionError):
+        pins.test_prod3_layout_by_hand()
+
+
+def test_prod3_norm_and_residual_norm_swapped_is_caught(monkeypatch):
+    import test_oracle_formats as pins
+    good_pack = fm.pack_prod
+    monkeypatch.setattr(oracle, "pack_prod", lambda n, g, i, s: good_pack(g, n, i, s))
+    with pytest.raises(AssertionError):
+        pins.test_prod3_layout_by_hand()
+
+
+def test_wht_sign_from_low_bit_is_caught(monkeypatch):
+    """Taking bit 0 of each splitmix64 output instead of the top bit passes the +-1 and
+    balance checks but not the signs the golden outputs fix."""
+    import test_oracle_formats as pins
+
+    def low_bit(seed, d):
+        return np.where((rot.splitmix64(seed, d) & np.uint64(1)) == 1, -1.0, 1.0)
+
+    monkeypatch.setattr(oracle, "wht_signs", low_bit)
+    with pytest.raises(AssertionError):
+        pins.test_wht_signs_take_the_top_bit()
+
+
+@pytest.mark.parametrize("order", ["elements_left_to_right", "adjacent_lanes_first", "fp64_then_round"])
+def test_norm_in_another_order_is_caught(monkeypatch, order):
+    """Any summation order other than the canonical tree changes the norm of the golden
+    row; each plausible alternative is planted and caught."""
+    import test_oracle_formats as pins
+
+    def other(x):
+        x32 = np.asarray(x, dtype=np.float32)
+        sq = x32 * x32
+        if order == "elements_left_to_right":
+            s = np.zeros(len(x32), np.float32)
+            for j in range(x32.shape[1]):
+                s = (s + sq[:, j]).astype(np.float32)
+        elif order == "adjacent_lanes_first":
+            p = (sq[:, 0::4] + sq[:, 1::4]) + (sq[:, 2::4] + sq[:, 3::4])
+            while p.shape[1] > 1:
+                p = (p[:, 0::2] + p[:, 1::2]).astype(np.float32)
+            s = p[:, 0]
+        else:
+            s = (x32.astype(np.float64) ** 2).sum(axis=1).astype(np.float32)
+        return np.sqrt(s).astype(np.float32)
+
+    monkeypatch.setattr(oracle, "canonical_norm_fp32", other)
+    with pytest.raises(AssertionError):
+        pins.test_canonical_norm_tree_order_by_hand()
