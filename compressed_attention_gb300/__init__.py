@@ -76,7 +76,9 @@ _SIGNATURES = {
     "tq_decode_combine": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _sz, _vp]),
     "tq_decode_attention_static": (_i32, [_vp, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _f32,
                                           _vp, _vp]),
+    "tq_static_workspace_bytes": (_sz, []),
     "tq_test_decode_wait_timeout": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _sz, _vp]),
+    "tq_test_ctx_set_device": (_i32, [_vp, _i32]),
     "tq_store_create": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, ctypes.POINTER(_vp)]),
     "tq_store_destroy": (_i32, [_vp]),
     "tq_store_append": (_i32, [_vp, _vp, _vp, _i32, _vp]),
@@ -390,7 +392,7 @@ class Store:
                                    _stream(stream)), "tq_store_decode")
 
 
-TQ_STATIC_WORKSPACE_BYTES = 4 << 20  # capacity of the static scratch of tq_decode_attention_static
+TQ_STATIC_WORKSPACE_BYTES = lib.tq_static_workspace_bytes()  # capacity of tq_decode_attention_static's scratch
 
 
 def tq_decode_attention_static(k_ctx, v_ctx, q, k_cache, v_cache, out, B, Hq, Hkv, L, seq_lens=None,

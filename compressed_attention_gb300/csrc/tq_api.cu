@@ -79,6 +79,9 @@ tq_status to_device(T **dst, const T *src, size_t n) {
 tq_status check_decode_common(const tq_ctx *k, const tq_ctx *v, int B, int Hq, int Hkv, int L,
                               DecodeShape *shape) {
   if (!k || !v) return fail(TQ_ERR_INVALID_ARG, "null context");
+  if (k->device != v->device) return fail(TQ_ERR_INVALID_ARG, "the key and value contexts belong to different devices");
+  tq_status st = check_current_device(k->device, "decode");
+  if (st != TQ_OK) return st;
   if (B < 1 || Hq < 1 || Hkv < 1 || L < 1) return fail(TQ_ERR_INVALID_ARG, "B, Hq, Hkv and L must be >= 1");
   if (Hq % Hkv != 0) return fail(TQ_ERR_INVALID_ARG, "Hq must be a multiple of Hkv");
   if (!decode_pair_supported(k, v))
@@ -98,6 +101,20 @@ tq_status check_workspace(const DecodeShape &s, void *ws, size_t bytes, Workspac
 }  // namespace
 
 namespace tq {
+tq_status check_current_device(int device, const char *who) {
+  int cur = -1;
+  const cudaError_t e = cudaGetDevice(&cur);
+  if (e != cudaSuccess) {
+    set_error("%s: cannot read the current device: %s", who, cudaGetErrorString(e));
+    return TQ_ERR_CUDA;
+  }
+  if (cur != device) {
+    set_error("%s: the context belongs to device %d but device %d is current", who, device, cur);
+    return TQ_ERR_INVALID_ARG;
+  }
+  return TQ_OK;
+}
+
 bool decode_pair_supported(const tq_ctx *k, const tq_ctx *v) {
   return ((k->fmt == TQ_FMT_TURBO4 || k->fmt == TQ_FMT_TURBO3) && v->fmt == TQ_FMT_TURBO4) ||
          (k->fmt == TQ_FMT_PROD3 && v->fmt == TQ_FMT_VGROUP2);
@@ -274,6 +291,8 @@ tq_status tq_ctx_destroy(tq_ctx *ctx) {
 
 tq_status tq_ctx_device_status(const tq_ctx *ctx, int32_t *status, int clear) {
   if (!ctx || !status) return fail(TQ_ERR_INVALID_ARG, "null argument");
+  tq_status st = check_current_device(ctx->device, "tq_ctx_device_status");
+  if (st != TQ_OK) return st;
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
   e = cudaMemcpy(status, ctx->d_status, sizeof(int32_t), cudaMemcpyDeviceToHost);
@@ -308,8 +327,10 @@ tq_status tq_quantize_set_rows(const tq_ctx *ctx, const void *src, int src_dtype
   if (!ctx) return fail(TQ_ERR_INVALID_ARG, "null context");
   if (n_rows < 0) return fail(TQ_ERR_INVALID_ARG, "n_rows < 0");
   if (n_rows == 0) return TQ_OK;
-  tq_status st = check_write_args(src, src_dtype, src_row_stride, row_ids, dst_cache, n_rows, dst_rows);
+  tq_status st = check_current_device(ctx->device, "tq_quantize_set_rows");
   if (st != TQ_OK) return st;
+  if ((st = check_write_args(src, src_dtype, src_row_stride, row_ids, dst_cache, n_rows, dst_rows)) != TQ_OK)
+    return st;
   WriteLaunch w{src, src_dtype, n_rows, src_row_stride, row_ids, (uint8_t *)dst_cache, dst_rows};
   cudaError_t e = launch_write(ctx, w, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "write kernel launch");
@@ -321,6 +342,8 @@ tq_status tq_dequantize(const tq_ctx *ctx, const void *cache, int64_t n_rows, in
   if (!ctx) return fail(TQ_ERR_INVALID_ARG, "null context");
   if (n_rows < 0) return fail(TQ_ERR_INVALID_ARG, "n_rows < 0");
   if (n_rows == 0) return TQ_OK;
+  tq_status st = check_current_device(ctx->device, "tq_dequantize");
+  if (st != TQ_OK) return st;
   if (!cache || !dst) return fail(TQ_ERR_INVALID_ARG, "null cache or output");
   if (!aligned(cache, 16)) return fail(TQ_ERR_ALIGNMENT, "cache must be 16-byte aligned");
   if (!aligned(dst, 4)) return fail(TQ_ERR_ALIGNMENT, "output must be 4-byte aligned");
@@ -521,6 +544,9 @@ namespace {
 tq_status check_prefill(const tq_ctx *k, const tq_ctx *v, int B, int T, int Hq, int Hkv, int L,
                         PrefillShape *s) {
   if (!k || !v) return fail(TQ_ERR_INVALID_ARG, "null context");
+  if (k->device != v->device) return fail(TQ_ERR_INVALID_ARG, "the key and value contexts belong to different devices");
+  tq_status st = check_current_device(k->device, "prefill");
+  if (st != TQ_OK) return st;
   if (B < 1 || T < 1 || Hq < 1 || Hkv < 1 || L < 1) return fail(TQ_ERR_INVALID_ARG, "B, T, Hq, Hkv and L must be >= 1");
   if (T > L) return fail(TQ_ERR_INVALID_ARG, "the chunk (T queries) must fit in the cache (L rows)");
   if (Hq % Hkv != 0) return fail(TQ_ERR_INVALID_ARG, "Hq must be a multiple of Hkv");
@@ -606,6 +632,12 @@ tq_status tq_prefill_attention(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const v
                           workspace_bytes, stream);
   if (st != TQ_OK) return st;
   return tq_prefill_combine(k_ctx, v_ctx, B, T, Hq, Hkv, L, out, workspace, workspace_bytes, stream);
+}
+
+tq_status tq_test_ctx_set_device(tq_ctx *ctx, int device) {
+  if (!ctx) return fail(TQ_ERR_INVALID_ARG, "null context");
+  ctx->device = device;
+  return TQ_OK;
 }
 
 tq_status tq_test_decode_wait_timeout(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *k_cache,

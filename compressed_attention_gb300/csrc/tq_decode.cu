@@ -3,7 +3,8 @@
 // its 4-bit indices, online softmax runs over key tiles split across the SMs,
 // values are dequantized in registers, and the output is un-rotated once.
 //
-// Three launches:
+// Kernels (tq_decode_attention launches two, k_prepare_q and k_partial_t4 with the merge
+// fused; the stage-by-stage calls, the store and larger unit counts use k_combine too):
 //   k_prepare_q  q_rot = R q (one warp per query), pre-scaled by
 //                log2(e) * scale / alpha and by a power of two, split into fp16
 //                hi + lo parts (the tensor-core operand).
@@ -16,6 +17,8 @@
 //                centroid pairs (a conflict-free shared-memory table, or byte
 //                permutes for a tunable share of the words), and run the score and
 //                PV products as m16n8k16 MMAs with fp32 accumulators.
+//                The CTA that completes a unit's partials merges them and writes its
+//                outputs (the fused combine).
 //   k_combine    log-sum-exp merge of the splits, 1/sum, un-rotation R^T o.
 //
 // MMA operand layout (one warp, 16 keys, 4 q-heads per column group):

@@ -102,6 +102,11 @@ bool dense_rotation_f64(uint64_t seed, int d, double *pi);
 F16Table make_f16_table(const float *c32, int K);
 BucketTable make_bucket_table(const float *b, int nb);
 void set_error(const char *fmt, ...);
+// TQ_OK when `device` is the calling thread's current device; else TQ_ERR_INVALID_ARG
+// (or TQ_ERR_CUDA when the current device cannot be read), with the reason recorded.
+// Every call that launches work checks its contexts' device this way: their tables and
+// status word live in that device's memory, and the kernels run on the current one.
+tq_status check_current_device(int device, const char *who);
 
 // ---- kernel launchers ----
 struct WriteLaunch {

@@ -27,8 +27,9 @@ constexpr int MAX_DEVICES = 64;
 std::mutex g_scratch_mu;
 void *g_scratch_ptr[MAX_DEVICES] = {};
 
-// Device address of g_decode_scratch on `device`, resolved once per device with that
-// device current (the first lookup may load the module on it).
+// Device address of g_decode_scratch on `device`, resolved once per device.  The caller
+// has checked that `device` is current, so the lookup (which may load the module on it)
+// needs no switch of the current device.
 tq_status scratch_on(int device, void **ptr) {
   if (device < 0 || device >= MAX_DEVICES) {
     set_error("tq_decode_attention_static: device %d beyond the %d devices it supports", device,
@@ -37,12 +38,8 @@ tq_status scratch_on(int device, void **ptr) {
   }
   std::lock_guard<std::mutex> lock(g_scratch_mu);
   if (!g_scratch_ptr[device]) {
-    int cur = 0;
-    cudaError_t e = cudaGetDevice(&cur);
-    if (e == cudaSuccess && cur != device) e = cudaSetDevice(device);
     void *p = nullptr;
-    if (e == cudaSuccess) e = cudaGetSymbolAddress(&p, g_decode_scratch);
-    if (cur != device) cudaSetDevice(cur);
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_decode_scratch);
     if (e != cudaSuccess) {
       set_error("tq_decode_attention_static: static scratch lookup on device %d: %s", device,
                 cudaGetErrorString(e));
@@ -66,6 +63,7 @@ tq_status tq_decode_attention_static(const tq_ctx *k_ctx, const tq_ctx *v_ctx, c
     set_error("tq_decode_attention_static: null context");
     return TQ_ERR_INVALID_ARG;
   }
+  // (the size query also checks that both contexts belong to the current device)
   size_t need = 0;
   tq_status st = tq_decode_workspace_size(k_ctx, v_ctx, B, Hq, Hkv, L, &need);
   if (st != TQ_OK) return st;
@@ -80,5 +78,7 @@ tq_status tq_decode_attention_static(const tq_ctx *k_ctx, const tq_ctx *v_ctx, c
   return tq_decode_attention(k_ctx, v_ctx, q, q_dtype, k_cache, v_cache, seq_lens, B, Hq, Hkv, L,
                              scale, out, nullptr, ws, (size_t)TQ_STATIC_WORKSPACE_BYTES, stream);
 }
+
+size_t tq_static_workspace_bytes(void) { return (size_t)TQ_STATIC_WORKSPACE_BYTES; }
 
 }  // extern "C"

@@ -225,9 +225,7 @@ tq_status tq_store_create(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, int H
   if (!decode_pair_supported(k_ctx, v_ctx) || !decode_shape(k_ctx, v_ctx, B, Hkv, Hkv, L, &probe))
     return fail(TQ_ERR_UNSUPPORTED, "no decode kernel for this (key, value) format pair or shape");
   if (k_ctx->device != v_ctx->device) return fail(TQ_ERR_INVALID_ARG, "contexts on different devices");
-  int cur = 0;
-  cudaGetDevice(&cur);
-  if (cur != k_ctx->device) return fail(TQ_ERR_INVALID_ARG, "the current device is not the contexts' device");
+  if (tq_status cs = check_current_device(k_ctx->device, "tq_store_create")) return cs;
   tq_store *st = new (std::nothrow) tq_store();
   if (!st) return fail(TQ_ERR_CUDA, "host allocation failed");
   st->k = k_ctx, st->v = v_ctx, st->B = B, st->Hkv = Hkv, st->L = L, st->R = ring_tokens, st->F = ring_tokens / 2;
@@ -268,6 +266,7 @@ tq_status tq_store_append(tq_store *st, const void *k_new, const void *v_new, in
   if (!st) return fail(TQ_ERR_INVALID_ARG, "null store");
   if (n < 0) return fail(TQ_ERR_INVALID_ARG, "n < 0");
   if (n == 0) return TQ_OK;
+  if (tq_status cs = check_current_device(st->device, "tq_store_append")) return cs;
   if (!k_new || !v_new) return fail(TQ_ERR_INVALID_ARG, "null source");
   if (((uintptr_t)k_new | (uintptr_t)v_new) % 16) return fail(TQ_ERR_ALIGNMENT, "sources must be 16-byte aligned");
   // every flush this append needs must fit: tokens beyond the last flush stay in the ring
@@ -318,6 +317,7 @@ tq_status tq_store_workspace_size(const tq_store *st, int Hq, size_t *bytes) {
 tq_status tq_store_decode(const tq_store *st, const void *q, int q_dtype, int Hq, float scale, float *out,
                           void *workspace, size_t workspace_bytes, tq_stream_t stream) {
   if (!st) return fail(TQ_ERR_INVALID_ARG, "null store");
+  if (tq_status cs = check_current_device(st->device, "tq_store_decode")) return cs;
   if (!q || !out || !workspace) return fail(TQ_ERR_INVALID_ARG, "null pointer");
   if (st->len == 0) return fail(TQ_ERR_INVALID_ARG, "the store is empty");
   if (q_dtype != TQ_DTYPE_F32 && q_dtype != TQ_DTYPE_BF16 && q_dtype != TQ_DTYPE_F16)

@@ -26,6 +26,12 @@
  *     the device can see (a row id out of range, a sequence length outside
  *     [1, L], a bounded wait that ran out) are recorded in the context's
  *     device status word, read with tq_ctx_device_status().
+ *   - A context belongs to the device that was current when it was created
+ *     (its tables and status word live in that device's memory).  Every call
+ *     that launches work, and every size query of the decode and prefill,
+ *     checks that this device is the calling thread's current device and that
+ *     the key and value contexts of the call belong to the same device;
+ *     otherwise it returns TQ_ERR_INVALID_ARG and launches nothing.
  *   - The caller owns every device buffer (sources, caches, q, outputs,
  *     workspace).  The library owns only tq_ctx, which is immutable after
  *     creation and may be shared across streams.
@@ -369,10 +375,10 @@ tq_status tq_decode_num_splits(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, 
  * Errors: TQ_ERR_WORKSPACE when the shape needs more scratch than
  *   TQ_STATIC_WORKSPACE_BYTES (tq_decode_workspace_size() tells; such shapes
  *   use tq_decode_attention); the other errors of tq_decode_attention.
- * Set-up: the first call on each device (that of k_ctx) looks up the static
- *   area's address once with that device current, which may load the module
- *   there; make that first call before any other work that must not be
- *   interrupted by module loading.
+ * Set-up: the contexts' device must be current (as for every call).  The first
+ *   call on each device looks up the static area's address there once, which
+ *   may load the module on that device; make that first call before any other
+ *   work that must not be interrupted by module loading.
  * Nothing in the area needs to start at zero: every word the decode reads is
  *   written earlier in the same call.
  * Concurrency: all calls on one device share the single area.  Two calls whose
@@ -383,6 +389,8 @@ tq_status tq_decode_attention_static(const tq_ctx *k_ctx, const tq_ctx *v_ctx, c
                                      int q_dtype, const void *k_cache, const void *v_cache,
                                      const int32_t *seq_lens, int B, int Hq, int Hkv, int L,
                                      float scale, float *out, tq_stream_t stream);
+/* TQ_STATIC_WORKSPACE_BYTES as compiled into the library (bindings read it here). */
+size_t tq_static_workspace_bytes(void);
 
 /* ------------------------------------------------------------- testing hook */
 
@@ -395,6 +403,12 @@ tq_status tq_decode_attention_static(const tq_ctx *k_ctx, const tq_ctx *v_ctx, c
 tq_status tq_test_decode_wait_timeout(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *k_cache,
                                       const void *v_cache, int B, int Hq, int Hkv, int L, void *workspace,
                                       size_t workspace_bytes, tq_stream_t stream);
+
+/* Device-check test (no counterpart on the pages): overwrites the device a context
+ * is recorded to belong to, so a test on a one-GPU machine can make the
+ * current-device check of every launching call fail (TQ_ERR_INVALID_ARG, nothing
+ * launched) and then restore the true device.  Not for use outside tests. */
+tq_status tq_test_ctx_set_device(tq_ctx *ctx, int device);
 
 #ifdef __cplusplus
 }

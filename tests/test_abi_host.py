@@ -133,3 +133,12 @@ def test_decode_step_binding_rejects_mismatched_rows(tq):
     for v in (torch.zeros((4, 128), dtype=torch.float32), torch.zeros((8, 128), dtype=torch.bfloat16)[::2]):
         with pytest.raises(ValueError):
             tq.tq_decode_step(Ctx, Ctx, k, v, None, None, None, None, None, 1, 4, 1, 8)
+
+
+def test_static_area_size_matches_the_header(tq):
+    """The binding reads the static scratch capacity from the library; it must equal the
+    header's TQ_STATIC_WORKSPACE_BYTES."""
+    text = open(os.path.join(ROOT, "include", "tq.h")).read()
+    m = re.search(r"#define\s+TQ_STATIC_WORKSPACE_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", text)
+    assert m is not None
+    assert tq.TQ_STATIC_WORKSPACE_BYTES == int(m.group(1)) << int(m.group(2))

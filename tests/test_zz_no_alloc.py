@@ -14,16 +14,27 @@ from gpu_util import check_outputs, lib
 pytestmark = pytest.mark.gpu
 
 
-def make_case(tq, B, Hq, Hkv, L, seed):
+# (key format, rotation, seed, QJL seed), then the same for the values
+PAIRS = {
+    "turbo4": (("turbo4", "dense", 21, 0), ("turbo4", "wht", 22, 0)),
+    "turbo3_keys": (("turbo3", "dense", 23, 0), ("turbo4", "dense", 24, 0)),
+    "prod3_vgroup2": (("prod3", "dense", 25, 1025), ("vgroup2", "wht", 0, 0)),
+}
+
+
+def make_ctx_pair(tq, pair="turbo4"):
+    return tuple(tq.Ctx(fmt, rot, seed, qjl) for fmt, rot, seed, qjl in PAIRS[pair])
+
+
+def make_case(tq, B, Hq, Hkv, L, seed, pair="turbo4"):
     import torch
-    kctx = tq.Ctx("turbo4", "dense", 21)
-    vctx = tq.Ctx("turbo4", "wht", 22)
+    kctx, vctx = make_ctx_pair(tq, pair)
     rng = np.random.default_rng(seed)
     caches = []
-    for ctx in (kctx, vctx):
+    for ctx, (fmt, _, _, _) in zip((kctx, vctx), PAIRS[pair]):
         x = torch.from_numpy(synth.bf16_bits(rng.standard_normal((B * Hkv * L, 128), dtype=np.float32))
                              .view(np.int16)).view(torch.bfloat16).cuda()
-        cache = tq.alloc_cache("turbo4", B * Hkv * L)
+        cache = tq.alloc_cache(fmt, B * Hkv * L)
         tq.tq_quantize_set_rows(ctx, x, cache)
         caches.append(cache)
     q = torch.from_numpy(rng.standard_normal((B, Hq, 128), dtype=np.float32)).cuda()
@@ -44,24 +55,24 @@ def run_both(tq, case, B, Hq, Hkv, L):
     return out.cpu().numpy(), ref.cpu().numpy()
 
 
-def test_static_scratch_matches_workspace_entry_twice_in_a_row():
+@pytest.mark.parametrize("pair", list(PAIRS))
+def test_static_scratch_matches_workspace_entry_twice_in_a_row(pair):
+    """Each (key, value) format pair has its own workspace layout (the prod3 + vgroup2
+    decode adds the QJL sketch of q); every pair is run through the static area."""
     tq = lib()
     shapes = [(4, 32, 8, 5000, 1), (2, 12, 1, 700, 2)]  # larger first, then a smaller one
     for B, Hq, Hkv, L, seed in shapes:
-        needed = tq.tq_decode_workspace_size(*make_ctx_pair(tq), B, Hq, Hkv, L)
+        needed = tq.tq_decode_workspace_size(*make_ctx_pair(tq, pair), B, Hq, Hkv, L)
         assert needed <= tq.TQ_STATIC_WORKSPACE_BYTES
-        case = make_case(tq, B, Hq, Hkv, L, seed)
+        case = make_case(tq, B, Hq, Hkv, L, seed, pair)
         out, ref = run_both(tq, case, B, Hq, Hkv, L)
         check_outputs(out, ref)
 
 
-def make_ctx_pair(tq):
-    return tq.Ctx("turbo4", "dense", 21), tq.Ctx("turbo4", "wht", 22)
-
-
-def test_static_scratch_rejects_oversized_shape():
+@pytest.mark.parametrize("pair", list(PAIRS))
+def test_static_scratch_rejects_oversized_shape(pair):
     tq = lib()
-    kctx, vctx = make_ctx_pair(tq)
+    kctx, vctx = make_ctx_pair(tq, pair)
     B, Hq, Hkv, L = 64, 64, 8, 32768
     assert tq.tq_decode_workspace_size(kctx, vctx, B, Hq, Hkv, L) > tq.TQ_STATIC_WORKSPACE_BYTES
     st = tq.lib.tq_decode_attention_static(kctx.handle, vctx.handle, None, tq.TQ_DTYPE_F32, None, None, None,
