@@ -23,15 +23,23 @@ roofline.
 Inputs are synthetic and seeded (see synth.py).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tq|reference]
-                       [--workload NAME]
+                       [--workload NAME] [--B B] [--L L]
+--B / --L override the batch and context of a decode workload (the context sweep:
+long_context at L = 4K, 16K, 64K, 128K and B = 1, 16).
 Under torchrun every rank runs the same per-GPU workload (weak scaling) and rank 0
-prints one JSON line.
+prints one JSON line; --gpus N > 1 outside torchrun starts N ranks under torchrun.
 """
+
+import os
+
+# The oracle legs (numpy) run on one host core: their BLAS calls are kept single-threaded
+# so that the reported core count is the one used.
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+os.environ.setdefault("MKL_NUM_THREADS", "1")
 
 import argparse
 import hashlib
 import json
-import os
 import statistics
 import subprocess
 import sys
@@ -216,10 +224,10 @@ class OracleDecode:
     """The oracle (fp64 dequantize-then-softmax attention) over whole (batch, KV head)
     units of a decode workload; inputs are encoded once, outside any timing."""
 
-    def __init__(self, name, n_units=2):
+    def __init__(self, name, cfg, n_units=2):
         import oracle
         self.attend = oracle.attention_reference
-        self.cfg, self.spec = synth.WORKLOADS[name], DECODE[name]
+        self.cfg, self.spec = cfg, DECODE[name]
         self.kc, self.vc = decode_codecs(self.spec)
         self.q32, _ = decode_queries(name, self.cfg)
         self.g = self.cfg["Hq"] // self.cfg["Hkv"]
@@ -234,6 +242,48 @@ class OracleDecode:
         self.attend(self.q32[b:b + 1, h * self.g:(h + 1) * self.g], self.kc.dequantize(kb)[None, None],
                     self.vc.dequantize(vb)[None, None])
         return self.cfg["L"]
+
+
+def cpu_fp32_loop(leg, min_seconds=3.0):
+    """The plain fp32 compressed-domain decode loop (oracle/cpu_decode_fp32.c: rotate q once,
+    score from indices, online softmax, one un-rotation) over the oracle's encoded units,
+    on one host core and on every host core (OpenMP over units).  turbo4 keys and values
+    only; None for other formats or without a C compiler."""
+    if leg.spec["k_fmt"] != "turbo4" or leg.spec["v_fmt"] != "turbo4":
+        return None
+    from oracle import build_cpu_baseline
+    f = build_cpu_baseline.load()
+    if f is None:
+        return None
+    L, g, cores = leg.cfg["L"], leg.g, os.cpu_count() or 1
+    rk = np.ascontiguousarray(leg.kc.rot.R, np.float32)
+    rv = np.ascontiguousarray(leg.vc.rot.R, np.float32)
+    ck = np.ascontiguousarray(leg.kc.c32, np.float32)
+    cv = np.ascontiguousarray(leg.vc.c32, np.float32)
+    scale = np.float32(1.0 / np.sqrt(128.0))
+    out = {}
+    for threads in sorted({1, cores}):
+        n_units = threads * 2  # the encoded units in turn, two per thread
+        kb = np.ascontiguousarray(np.concatenate([leg.blocks[u % len(leg.blocks)][2] for u in range(n_units)]))
+        vb = np.ascontiguousarray(np.concatenate([leg.blocks[u % len(leg.blocks)][3] for u in range(n_units)]))
+        q = np.ascontiguousarray(np.concatenate([
+            leg.q32[b:b + 1, h * g:(h + 1) * g] for b, h, _, _ in
+            (leg.blocks[u % len(leg.blocks)] for u in range(n_units))], axis=1).reshape(1, n_units * g, 128),
+            np.float32)
+        o = np.zeros((1, n_units * g, 128), np.float32)
+        t0, reps, used = time.perf_counter(), 0, 0
+        while reps == 0 or time.perf_counter() - t0 < min_seconds:
+            used = f(q.ctypes.data, kb.ctypes.data, vb.ctypes.data, 1, n_units * g, n_units, L, rk.ctypes.data,
+                     rv.ctypes.data, ck.ctypes.data, cv.ctypes.data, scale, o.ctypes.data, threads)
+            reps += 1
+        dt = time.perf_counter() - t0
+        keys = reps * n_units * L
+        out["cores_1" if threads == 1 else "cores_all"] = {
+            "value": keys * decode_unit_bytes(leg.spec) / dt / 1e9, "unit": "GB/s", "keys_per_s": keys / dt,
+            "threads": used, "sample": f"{reps} x {n_units} units of {L} keys x {g} q-heads, {dt:.1f} s"}
+    out["kind"] = "plain fp32 compressed-domain decode loop (C, OpenMP over units), not the oracle"
+    out["host_cores"] = cores
+    return out
 
 
 class OracleWrite:
@@ -258,9 +308,10 @@ def cpu_sample(oracle_leg, unit_bytes, what, min_seconds=10.0, max_units=64):
         items += oracle_leg.unit(units)
         elapsed += time.perf_counter() - t0
         units += 1
-    return {"value": items * unit_bytes / elapsed / 1e9, "unit": "GB/s", "cores": os.cpu_count(),
+    return {"value": items * unit_bytes / elapsed / 1e9, "unit": "GB/s", "cores": 1,
             "kind": "oracle", "rate": items / elapsed,
-            "sample": f"{units} {what}, {elapsed:.1f} s"}
+            "sample": f"{units} {what}, {elapsed:.1f} s, one host core (BLAS single-threaded)",
+            "host_cores": os.cpu_count()}
 
 
 def prefill_flops(cfg):
@@ -318,8 +369,9 @@ def run_reference(args, rank, world):
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic", "config": prefill_config(), "flops_per_step": leg.flops,
-                "cpu_baseline": {"value": tf, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
-                                 "sample": sample},
+                "cpu_baseline": {"value": tf, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                                 "sample": sample + ", one host core (BLAS single-threaded)",
+                                 "host_cores": os.cpu_count()},
                 "e2e": {"value": tf, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
         return
@@ -329,12 +381,13 @@ def run_reference(args, rank, world):
         metric, what = WRITE_METRIC, f"blocks of {len(leg.x32)} bf16 rows encoded by the oracle"
         config = write_config(args)
     else:
-        leg = OracleDecode(args.workload)
+        cfg = decode_workload(args)
+        leg = OracleDecode(args.workload, cfg)
         unit_bytes = decode_unit_bytes(leg.spec)
         metric = DECODE_METRIC
         what = (f"(batch, KV head) units of {leg.cfg['L']} keys x {leg.g} q-heads, "
                 "fp64 dequantize-then-softmax")
-        config = decode_config(args.workload)
+        config = decode_config(args.workload, cfg)
     for i in range(args.warmup):
         leg.unit(i)
     t0 = time.perf_counter()
@@ -345,20 +398,32 @@ def run_reference(args, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": config, "items_per_s": items / dt,
-            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
-                             "sample": f"one of {what} per step"},
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"one of {what} per step, one host core (BLAS single-threaded)",
+                             "host_cores": os.cpu_count()},
             "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
-def decode_config(name):
-    cfg, spec = synth.WORKLOADS[name], DECODE[name]
+def decode_workload(args):
+    """The decode workload's shape, with --B / --L applied."""
+    cfg = dict(synth.WORKLOADS[args.workload])
+    if getattr(args, "B", None):
+        cfg["B"] = args.B
+    if getattr(args, "L", None):
+        cfg["L"] = args.L
+    return cfg
+
+
+L2_NOTE = "flushed before every step: 256 MB write then a read of it (no dirty lines left)"
+
+
+def decode_config(name, cfg):
+    spec = DECODE[name]
     return {"workload": f"{name}: B={cfg['B']} Hq={cfg['Hq']} Hkv={cfg['Hkv']} d=128 L={cfg['L']}",
             "B": cfg["B"], "Hq": cfg["Hq"], "Hkv": cfg["Hkv"], "L": cfg["L"], "d": 128,
             "k_format": spec["k_fmt"], "v_format": spec["v_fmt"], "rotation": spec["rotation"],
-            "q_dtype": cfg["q_dtype"],
-            "l2": "flushed before every step: 256 MB write then a read of it (no dirty lines left)",
-            "launch": "CUDA graphs"}
+            "q_dtype": cfg["q_dtype"], "l2": L2_NOTE}
 
 
 def prefill_config():
@@ -367,18 +432,14 @@ def prefill_config():
                          f"T={cfg['T']} (the last chunk of a {cfg['L']}-token prompt)"),
             "B": cfg["B"], "Hq": cfg["Hq"], "Hkv": cfg["Hkv"], "L": cfg["L"], "T": cfg["T"], "d": 128,
             "k_format": spec["fmt"], "v_format": spec["fmt"], "rotation": spec["rotation"],
-            "q_dtype": cfg["q_dtype"], "mask": "causal",
-            "l2": "flushed before every step: 256 MB write then a read of it (no dirty lines left)",
-            "launch": "CUDA graphs"}
+            "q_dtype": cfg["q_dtype"], "mask": "causal", "l2": L2_NOTE}
 
 
 def write_config(args):
     cfg = synth.WORKLOADS["write_chunk"]
     return {"workload": f"write_chunk: {cfg['N']} tokens x {cfg['Hkv']} KV heads x 128, bf16 K and V",
             "rows_per_tensor": cfg["N"] * cfg["Hkv"], "format": args.write_format,
-            "rotation": args.write_rotation,
-            "l2": "flushed before every step: 256 MB write then a read of it (no dirty lines left)",
-            "launch": "CUDA graphs"}
+            "rotation": args.write_rotation, "l2": L2_NOTE}
 
 
 # ----------------------------------------------------------------------------- GPU side
@@ -395,20 +456,31 @@ def to_device_rows(torch, x32, bits, device):
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
 
 
-def build_decode(name, tq, torch, device):
-    cfg, spec = synth.WORKLOADS[name], DECODE[name]
+def generated_units(name, cfg, tensor, workers=None):
+    """(b, h, fp32 rows, bf16 bits) of every (batch, KV head) unit in order, drawn by a few
+    host threads at a time (numpy's generators release the GIL while they fill arrays)."""
+    from concurrent.futures import ThreadPoolExecutor
+    units = [(b, h) for b in range(cfg["B"]) for h in range(cfg["Hkv"])]
+    workers = workers or max(1, min(16, os.cpu_count() or 1))
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        for i in range(0, len(units), workers):
+            chunk = units[i:i + workers]
+            for (b, h), (x32, bits) in zip(chunk, ex.map(lambda u: unit_rows(name, cfg, tensor, *u), chunk)):
+                yield b, h, x32, bits
+
+
+def build_decode(name, cfg, tq, torch, device):
+    spec = DECODE[name]
     B, Hq, Hkv, L = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["L"]
     kctx = make_ctx(tq, spec["k_fmt"], spec, spec["k_seed"])
     vctx = make_ctx(tq, spec["v_fmt"], spec, spec["v_seed"])
     kc = tq.alloc_cache(spec["k_fmt"], B * Hkv * L, device)
     vc = tq.alloc_cache(spec["v_fmt"], B * Hkv * L, device)
     for tensor, ctx, cache in (("K", kctx, kc), ("V", vctx, vc)):
-        for b in range(B):
-            for h in range(Hkv):
-                x32, bits = unit_rows(name, cfg, tensor, b, h)
-                src = to_device_rows(torch, x32, bits, device)
-                rows = torch.arange((b * Hkv + h) * L, (b * Hkv + h + 1) * L, dtype=torch.int64, device=device)
-                tq.tq_quantize_set_rows(ctx, src, cache, row_ids=rows)
+        for b, h, x32, bits in generated_units(name, cfg, tensor):
+            src = to_device_rows(torch, x32, bits, device)
+            rows = torch.arange((b * Hkv + h) * L, (b * Hkv + h + 1) * L, dtype=torch.int64, device=device)
+            tq.tq_quantize_set_rows(ctx, src, cache, row_ids=rows)
     q32, qbits = decode_queries(name, cfg)
     q = to_device_rows(torch, q32, qbits, device).reshape(B, Hq, 128)
     # the step's new token: one K and one V row per (b, KV head), written to slot L-1
@@ -468,8 +540,9 @@ def timed_graph_steps(torch, stream, fns, steps, warmup, flush_l2):
     return [e0.elapsed_time(e1) for e0, e1 in ev]
 
 
-E2E_MODE = ("each step one replay of a CUDA graph of the public API calls with the copies; "
-            "direct_ms_per_step: the same calls issued one by one")
+E2E_MODE = ("value: the public API calls and the copies issued one by one from Python every step "
+            "(host validation and enqueue inside the timed region); graph_*: the same calls and copies "
+            "captured once in a CUDA graph and replayed every step")
 
 
 def timed_e2e(torch, body, steps, warmup, flush_l2):
@@ -513,9 +586,9 @@ def run_decode(args, rank, world, dist):
     local = int(os.environ.get("LOCAL_RANK", 0))
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
-    cfg, spec = synth.WORKLOADS[name], DECODE[name]
+    cfg, spec = decode_workload(args), DECODE[name]
     B, Hq, Hkv, L = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["L"]
-    w = build_decode(name, tq, torch, device)
+    w = build_decode(name, cfg, tq, torch, device)
     stream = torch.cuda.current_stream()
     flush_l2 = flusher(torch, device)
 
@@ -523,8 +596,11 @@ def run_decode(args, rank, world, dist):
         tq.tq_decode_step(w["kctx"], w["vctx"], w["new_k"], w["new_v"], w["q"], w["kc"], w["vc"], w["out"],
                           w["ws"], B, Hq, Hkv, L, row_ids=w["slots"])
 
-    def partial():
+    def partial():  # the split-K kernel alone, writing partials (the stage call)
         tq.tq_decode_partial(w["kctx"], w["vctx"], w["kc"], w["vc"], w["ws"], B, Hq, Hkv, L)
+
+    def partial_merge():  # the split-K kernel as the step launches it, merge fused
+        tq.tq_decode_partial_merge(w["kctx"], w["vctx"], w["kc"], w["vc"], w["out"], w["ws"], B, Hq, Hkv, L)
 
     launches_per_step = tq.tq_decode_step_num_launches(w["kctx"], w["vctx"], w["new_k"].dtype,
                                                        w["new_k"].shape[0], B, Hq, Hkv, L)
@@ -534,14 +610,19 @@ def run_decode(args, rank, world, dist):
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
-        # the step, then the decode kernel alone (the roofline), same workload and flushes
+        # the step, then the decode kernel alone (the roofline), same workload and flushes:
+        # as the step launches it (merge fused, over the q the step prepared), and the
+        # stage kernel that writes partials only
         step_ms = timed_graph_steps(torch, stream, (step,), args.steps, args.warmup, flush_l2)
+        merge_ms = timed_graph_steps(torch, stream, (partial_merge,), args.steps, args.warmup, flush_l2)
         part_ms = timed_graph_steps(torch, stream, (partial,), args.steps, args.warmup, flush_l2)
         if dist:
             dist.barrier()
     clk = clocks.summary()
     total_ms = max_over_ranks(sum(step_ms), dist, device)
+    merge_avg = max_over_ranks(statistics.mean(merge_ms), dist, device)
     part_avg = max_over_ranks(statistics.mean(part_ms), dist, device)
+    merge_launches = tq.tq_decode_num_launches(w["kctx"], w["vctx"], B, Hq, Hkv, L) - 1
 
     # end to end through the public API with host buffers: q and the new K/V rows copied in,
     # the output read back, every step.  The step's inputs sit back to back in one pinned
@@ -576,34 +657,45 @@ def run_decode(args, rank, world, dist):
     ms_per_step = total_ms / args.steps
     value = job_rate(alg_bytes, world, ms_per_step) / 1e9
     peak, peak_kind = measured_peak()
-    achieved = kv_bytes / (part_avg * 1e-3) / 1e9
-    e2e_step_ms = max_over_ranks(statistics.mean(e2e_ms), dist, device)
-    e2e_direct_step_ms = max_over_ranks(statistics.mean(e2e_direct_ms), dist, device)
+    achieved = kv_bytes / (merge_avg * 1e-3) / 1e9
+    achieved_stage = kv_bytes / (part_avg * 1e-3) / 1e9
+    e2e_graph_ms = max_over_ranks(statistics.mean(e2e_ms), dist, device)
+    e2e_direct_ms = max_over_ranks(statistics.mean(e2e_direct_ms), dist, device)
     if rank != 0:
         return
-    cpu = None
-    if world == 1:  # the host-core baseline: N=1 only
-        leg = OracleDecode(name)
+    cpu = fp32_loop = None
+    if world == 1:  # the host-core baselines: N=1 only
+        leg = OracleDecode(name, cfg)
         cpu = cpu_sample(leg, decode_unit_bytes(spec),
                          f"whole (batch, KV head) units of {L} keys x {Hq // Hkv} q-heads, "
                          "fp64 dequantize-then-softmax")
-    line = common_line(DECODE_METRIC, args, world, ms_per_step, value, decode_config(name), "f32")
-    line["config"]["launch"] = ("each step one CUDA graph, steps queued back to back; the dominant kernel "
-                                "timed alone the same way for the roofline")
+        fp32_loop = cpu_fp32_loop(leg)
+    line = common_line(DECODE_METRIC, args, world, ms_per_step, value, decode_config(name, cfg), "f32")
+    merged = "merge fused" if merge_launches == 1 else "then the combine kernel"
     line.update({
+        "timing": ("each step one CUDA graph (tq_decode_step: SET_ROWS of the new K/V rows and the q "
+                   "preparation in one launch, then the split-K decode with the merge fused), steps queued "
+                   "back to back; the split-K decode alone timed the same way for the roofline"),
         "keys_per_s": job_rate(B * Hkv * L, world, ms_per_step),
         "q_head_scores_per_s": job_rate(B * Hq * L, world, ms_per_step),
         "hbm_frac_of_measured_step": value / peak,
         "algorithmic_bytes_per_step": alg_bytes,
         "operands": "packed K/V decoded in registers to fp16 operands; fp16 hi+lo q and p; fp32 accumulate",
-        "roofline": {"bound": "hbm", "kernel": spec["kernel"] + " (split-K decode)", "achieved": achieved,
-                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+        "roofline": {"bound": "hbm", "kernel": f"{spec['kernel']} (split-K decode, {merged}, as in the step)",
+                     "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": achieved / peak,
                      "traffic": profiled_traffic("decode_partial_" + name, spec["source"]),
-                     "algorithmic_bytes_per_launch": kv_bytes, "avg_launch_ms": part_avg},
+                     "algorithmic_bytes_per_launch": kv_bytes, "avg_launch_ms": merge_avg,
+                     "launches": merge_launches},
+        "roofline_stage_kernel": {"kernel": f"{spec['kernel']} (stage call: partials only, no merge)",
+                                  "achieved": achieved_stage, "frac": achieved_stage / peak,
+                                  "avg_launch_ms": part_avg},
         "cpu_baseline": cpu,
-        "e2e": {"value": job_rate(alg_bytes, world, e2e_step_ms) / 1e9, "unit": "GB/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step_ms,
-                "mode": E2E_MODE, "direct_ms_per_step": e2e_direct_step_ms},
+        "cpu_fp32_loop": fp32_loop,
+        "e2e": {"value": job_rate(alg_bytes, world, e2e_direct_ms) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_direct_ms,
+                "mode": E2E_MODE, "graph_value": job_rate(alg_bytes, world, e2e_graph_ms) / 1e9,
+                "graph_ms_per_step": e2e_graph_ms},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     })
@@ -710,15 +802,17 @@ def run_prefill(args, rank, world, dist):
             work += leg.unit(n)
             n += 1
         el = time.perf_counter() - t0
-        cpu = {"value": work / el / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+        cpu = {"value": work / el / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
                "sample": (f"{n} x the last {leg.n} chunk queries x {leg.q.shape[2]} q-heads of one KV head "
-                          f"over {L} keys, fp64 dequantize-then-softmax, {el:.1f} s")}
+                          f"over {L} keys, fp64 dequantize-then-softmax, {el:.1f} s, one host core "
+                          "(BLAS single-threaded)"),
+               "host_cores": os.cpu_count()}
     line = common_line(PREFILL_METRIC, args, world, ms_per_step, value, prefill_config(), "f16")
     line["unit"] = "TFLOP/s"
-    line["config"]["launch"] = ("each step one CUDA graph (SET_ROWS of the chunk's K and V rows, q preparation, "
-                                "the tensor-core prefill, the combine), steps queued back to back; the prefill "
-                                "kernel timed alone the same way for the roofline")
     line.update({
+        "timing": ("each step one CUDA graph (SET_ROWS of the chunk's K and V rows, q preparation, "
+                   "the tensor-core prefill, the combine), steps queued back to back; the prefill "
+                   "kernel timed alone the same way for the roofline"),
         "tokens_per_s": job_rate(B * T, world, ms_per_step),
         "flops_per_step": flops,
         "operands": ("fp16 hi+lo q and p against fp16 centroid tiles decoded from the packed cache; "
@@ -728,9 +822,10 @@ def run_prefill(args, rank, world, dist):
                      "traffic": profiled_traffic("prefill_partial_prefill_chunk", spec["source"]),
                      "algorithmic_flops_per_launch": flops, "avg_launch_ms": part_avg},
         "cpu_baseline": cpu,
-        "e2e": {"value": job_rate(flops, world, e2e_step_ms) / 1e12, "unit": "TFLOP/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step_ms,
-                "mode": E2E_MODE, "direct_ms_per_step": e2e_direct_step_ms},
+        "e2e": {"value": job_rate(flops, world, e2e_direct_step_ms) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_direct_step_ms,
+                "mode": E2E_MODE, "graph_value": job_rate(flops, world, e2e_step_ms) / 1e12,
+                "graph_ms_per_step": e2e_step_ms},
         "gpu_launches": 5 * args.steps,
         "clocks": clk,
     })
@@ -806,9 +901,9 @@ def run_write(args, rank, world, dist):
         cpu = cpu_sample(leg, 256 + row_bytes, f"blocks of {len(leg.x32)} bf16 rows encoded by the oracle")
     kernel, source = WRITE_KERNEL[rot]
     line = common_line(WRITE_METRIC, args, world, ms_per_step, value, write_config(args), "f32")
-    line["config"]["launch"] = ("each step one CUDA graph, steps queued back to back; the dominant kernel "
-                                "timed alone the same way for the roofline")
     line.update({
+        "timing": ("each step one CUDA graph (SET_ROWS of the K rows, then of the V rows), steps queued back "
+                   "to back; the first SET_ROWS launch timed alone the same way for the roofline"),
         "rows_per_s": job_rate(2 * n, world, ms_per_step),
         "algorithmic_bytes_per_step": alg_bytes,
         "roofline": {"bound": "hbm", "kernel": kernel, "achieved": launch_bytes / (launch_avg * 1e-3) / 1e9,
@@ -817,13 +912,26 @@ def run_write(args, rank, world, dist):
                      "traffic": profiled_traffic(f"write_{fmt}_{rot}_write_chunk", source),
                      "algorithmic_bytes_per_launch": launch_bytes, "avg_launch_ms": launch_avg},
         "cpu_baseline": cpu,
-        "e2e": {"value": job_rate(alg_bytes, world, e2e_step_ms) / 1e9, "unit": "GB/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step_ms,
-                "mode": E2E_MODE, "direct_ms_per_step": e2e_direct_step_ms},
+        "e2e": {"value": job_rate(alg_bytes, world, e2e_direct_step_ms) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_direct_step_ms,
+                "mode": E2E_MODE, "graph_value": job_rate(alg_bytes, world, e2e_step_ms) / 1e9,
+                "graph_ms_per_step": e2e_step_ms},
         "gpu_launches": 2 * args.steps,
         "clocks": clk,
     })
     print(json.dumps(line), flush=True)
+
+
+def relaunch_under_torchrun(n):
+    """Run this command again as n ranks under torchrun (one node, 127.0.0.1) and return
+    its exit status; rank 0 prints the JSON line."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *sys.argv[1:]]
+    return subprocess.run(cmd).returncode
 
 
 def main():
@@ -833,13 +941,21 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["tq", "reference"], default="tq")
     ap.add_argument("--workload", choices=sorted(DECODE) + ["prefill_chunk", "write_chunk"], default="gqa_lognormal")
+    ap.add_argument("--B", type=int, default=None, help="batch of a decode workload (default: the workload's)")
+    ap.add_argument("--L", type=int, default=None, help="context of a decode workload (default: the workload's)")
     ap.add_argument("--write-format", choices=["turbo4", "turbo3"], default="turbo4")
     ap.add_argument("--write-rotation", choices=["dense", "wht"], default="dense")
     args = ap.parse_args()
-    if args.warmup < 3:
-        args.warmup = 3
+    if args.steps < 1 or args.warmup < 0 or args.gpus < 1:
+        ap.error("--steps must be >= 1, --warmup >= 0 and --gpus >= 1")
+    if (args.B or args.L) and args.workload not in DECODE:
+        ap.error("--B and --L apply to the decode workloads")
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        sys.exit(relaunch_under_torchrun(args.gpus))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
+    if world != args.gpus:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE is {world}")
     if args.impl == "reference":
         run_reference(args, rank, world)
         return

@@ -74,6 +74,7 @@ _SIGNATURES = {
     "tq_decode_prepare_q": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _sz, _vp]),
     "tq_decode_partial": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _sz, _vp]),
     "tq_decode_combine": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _sz, _vp]),
+    "tq_decode_partial_merge": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _sz, _vp]),
     "tq_decode_attention_static": (_i32, [_vp, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _f32,
                                           _vp, _vp]),
     "tq_static_workspace_bytes": (_sz, []),
@@ -403,6 +404,14 @@ def tq_decode_attention_static(k_ctx, v_ctx, q, k_cache, v_cache, out, B, Hq, Hk
     _check(lib.tq_decode_attention_static(k_ctx.handle, v_ctx.handle, qp, qd, _ptr(k_cache), _ptr(v_cache),
                                           _ptr(seq_lens), B, Hq, Hkv, L, scale, _ptr(out), _stream(stream)),
            "tq_decode_attention_static")
+
+
+def tq_decode_partial_merge(k_ctx, v_ctx, k_cache, v_cache, out, workspace, B, Hq, Hkv, L, seq_lens=None,
+                            stream=None):
+    _check(lib.tq_decode_partial_merge(k_ctx.handle, v_ctx.handle, _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
+                                       B, Hq, Hkv, L, _ptr(out), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _stream(stream)),
+           "tq_decode_partial_merge")
 
 
 def tq_decode_prepare_q(k_ctx, v_ctx, q, workspace, B, Hq, Hkv, L, scale=0.0, stream=None):

@@ -425,6 +425,30 @@ tq_status tq_decode_combine(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, int
   return TQ_OK;
 }
 
+tq_status tq_decode_partial_merge(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *k_cache,
+                                  const void *v_cache, const int32_t *seq_lens, int B, int Hq, int Hkv,
+                                  int L, float *out, void *workspace, size_t workspace_bytes,
+                                  tq_stream_t stream) {
+  DecodeShape s;
+  tq_status st = check_decode_common(k_ctx, v_ctx, B, Hq, Hkv, L, &s);
+  if (st != TQ_OK) return st;
+  if (!k_cache || !v_cache) return fail(TQ_ERR_INVALID_ARG, "null cache");
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return fail(TQ_ERR_ALIGNMENT, "caches must be 16-byte aligned");
+  if (seq_lens && !aligned(seq_lens, 4)) return fail(TQ_ERR_ALIGNMENT, "seq_lens must be 4-byte aligned");
+  if (!out) return fail(TQ_ERR_INVALID_ARG, "null output");
+  if (!aligned(out, 4)) return fail(TQ_ERR_ALIGNMENT, "output must be 4-byte aligned");
+  Workspace w;
+  if ((st = check_workspace(s, workspace, workspace_bytes, &w)) != TQ_OK) return st;
+  bool fused = false;
+  cudaError_t e = launch_partial(k_ctx, v_ctx, (const uint8_t *)k_cache, (const uint8_t *)v_cache, seq_lens,
+                                 s, nullptr, w, (cudaStream_t)stream, false, out, &fused);
+  if (e != cudaSuccess) return cuda_fail(e, "partial launch");
+  if (fused) return TQ_OK;
+  e = launch_combine(k_ctx, v_ctx, s, out, w, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  return TQ_OK;
+}
+
 tq_status tq_decode_num_launches(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, int Hq, int Hkv,
                                  int L, int *n) {
   if (!n) return fail(TQ_ERR_INVALID_ARG, "null output");

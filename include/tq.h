@@ -267,6 +267,19 @@ tq_status tq_decode_combine(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, int
                             int L, float *out, void *workspace, size_t workspace_bytes,
                             tq_stream_t stream);
 
+/* Stages two and three of tq_decode_attention in one call, as tq_decode_attention
+ * runs them: the split-K decode with the merge and the un-rotation done inside the
+ * split-K kernel where the shape allows it (one launch), else the split-K kernel and
+ * the combine kernel (tq_decode_num_launches() - 1 launches either way).  The
+ * workspace must hold tq_decode_prepare_q's output for the same shape; the per-unit
+ * counters of the fused merge are zeroed there and every completed call leaves them
+ * zero again, so the call may be repeated over the same prepared q.  Arguments and
+ * errors as tq_decode_attention (no q, scale or scores). */
+tq_status tq_decode_partial_merge(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *k_cache,
+                                  const void *v_cache, const int32_t *seq_lens, int B, int Hq, int Hkv,
+                                  int L, float *out, void *workspace, size_t workspace_bytes,
+                                  tq_stream_t stream);
+
 /* Chunked prefill attention over the compressed cache ([turbo4 post-mortem] §9,
  * the prefill table: a prompt is processed in chunks that attend to the turbo4
  * cache, which already holds the chunk's own rows -- write them with

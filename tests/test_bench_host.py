@@ -18,10 +18,10 @@ def test_reference_arm_json_line():
     lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
     assert len(lines) == 1
     d = json.loads(lines[0])
-    assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["steps"] == 1 and d["warmup"] >= 3
+    assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["steps"] == 1 and d["warmup"] == 0
     assert d["value"] > 0 and d["unit"] == "GB/s" and d["higher_is_better"] is True
     assert d["config"]["workload"].startswith("gqa_lognormal")
-    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
     assert d["cpu_baseline"]["value"] == d["value"] and d["cpu_baseline"]["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
 
@@ -33,12 +33,49 @@ def test_bench_configs_name_their_workloads():
     import bench
     import synth
     for name in bench.DECODE:
-        c = bench.decode_config(name)
         w = synth.WORKLOADS[name]
+        c = bench.decode_config(name, w)
         assert c["workload"].startswith(f"{name}: B={w['B']} Hq={w['Hq']} Hkv={w['Hkv']} d=128 L={w['L']}")
         assert c["k_format"] in ("turbo4", "turbo3", "prod3") and c["v_format"] in ("turbo4", "vgroup2")
         assert "flushed" in c["l2"]
-    d = bench.decode_config("gqa_lognormal")
+    d = bench.decode_config("gqa_lognormal", synth.WORKLOADS["gqa_lognormal"])
     assert (d["B"], d["Hq"], d["Hkv"], d["L"], d["rotation"]) == (8, 32, 8, 32768, "dense")
     p = bench.prefill_config()
     assert p["mask"] == "causal" and p["T"] == synth.WORKLOADS["prefill_chunk"]["T"]
+
+
+def _bench(*args, timeout=600):
+    import subprocess
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], capture_output=True, text=True,
+                       timeout=timeout, cwd=ROOT, env={k: v for k, v in os.environ.items() if k != "WORLD_SIZE"})
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout[-3000:]
+    return json.loads(lines[0])
+
+
+def test_gpus_flag_starts_that_many_ranks():
+    """`--gpus 2` outside torchrun starts two ranks under torchrun (127.0.0.1); rank 0 alone
+    prints the line, which reports n_gpus 2 (the reference arm: no GPU needed)."""
+    d = _bench("--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "0", "--workload", "single_head")
+    assert d["n_gpus"] == 2 and d["impl"] == "reference" and d["warmup"] == 0
+
+
+def test_context_sweep_flags_set_the_workload():
+    """--B / --L override a decode workload's batch and context, and the config says so."""
+    d = _bench("--impl", "reference", "--steps", "1", "--warmup", "0", "--workload", "long_context",
+               "--B", "2", "--L", "4096")
+    assert (d["config"]["B"], d["config"]["L"]) == (2, 4096)
+    assert d["config"]["workload"] == "long_context: B=2 Hq=32 Hkv=8 d=128 L=4096"
+
+
+def test_gpu_arm_and_reference_arm_share_one_config_builder():
+    """Both arms report decode_config(name, workload): the same dict for the same flags."""
+    sys.path.insert(0, ROOT)
+    import argparse
+
+    import bench
+    a = argparse.Namespace(workload="long_context", B=16, L=65536)
+    assert bench.decode_config("long_context", bench.decode_workload(a)) == \
+        bench.decode_config("long_context", bench.decode_workload(a))
+    assert "launch" not in bench.decode_config("long_context", bench.decode_workload(a))

@@ -251,22 +251,31 @@ def test_decode_rejects_bad_arguments():
         assert e.value.status == tq.TQ_ERR_UNSUPPORTED
 
 
-def _full_size(name, rot, rot_seed, sample_heads, k_fmt="turbo4"):
+def _units(cfg, tensor, workers=16):
+    """(b, h, bf16 bits) of every unit, drawn by a few host threads at a time."""
+    from concurrent.futures import ThreadPoolExecutor
+    units = [(b, h) for b in range(cfg["B"]) for h in range(cfg["Hkv"])]
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        for i in range(0, len(units), workers):
+            chunk = units[i:i + workers]
+            for (b, h), (_, bits) in zip(chunk, ex.map(lambda u: synth.kv_unit(cfg, tensor, *u), chunk)):
+                yield b, h, bits
+
+
+def _full_size(name, rot, rot_seed, sample_heads, k_fmt="turbo4", **override):
     """Write the whole cache with the GPU write path, decode in the benchmark's launch
     configuration, and compare sampled (b, h) outputs with the oracle on that head's inputs."""
     import torch
     tq = lib()
-    cfg = synth.WORKLOADS[name]
+    cfg = dict(synth.WORKLOADS[name], **override)
     B, Hq, Hkv, L = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["L"]
     kctx, vctx = tq.Ctx(k_fmt, rot, rot_seed), tq.Ctx("turbo4", rot, rot_seed + 100)
     kc, vc = tq.alloc_cache(k_fmt, B * Hkv * L), tq.alloc_cache("turbo4", B * Hkv * L)
     for tensor, ctx, cache in (("K", kctx, kc), ("V", vctx, vc)):
-        for b in range(B):
-            for h in range(Hkv):
-                x32, bits = synth.kv_unit(cfg, tensor, b, h)
-                src = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
-                rows = torch.arange((b * Hkv + h) * L, (b * Hkv + h + 1) * L, dtype=torch.int64, device="cuda")
-                tq.tq_quantize_set_rows(ctx, src, cache, row_ids=rows)
+        for b, h, bits in _units(cfg, tensor):
+            src = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+            rows = torch.arange((b * Hkv + h) * L, (b * Hkv + h + 1) * L, dtype=torch.int64, device="cuda")
+            tq.tq_quantize_set_rows(ctx, src, cache, row_ids=rows)
     q32, qbits = synth.queries(cfg)
     q_t = torch.from_numpy(qbits.view(np.int16)).view(torch.bfloat16).cuda()
     out, _ = run_decode(tq, kctx, vctx, q_t, kc, vc, B, Hq, Hkv, L, scores=False)
@@ -289,6 +298,12 @@ def test_full_size_gqa_lognormal_dense():
 
 def test_full_size_long_context_wht():
     _full_size("long_context", "wht", 5, [(0, 0), (0, 17), (0, 31)])
+
+
+def test_full_size_long_context_batch16_wht():
+    """The largest point of the context sweep: B = 16 sequences of 131,072 keys (2.28 GB of
+    packed K and V), sampled heads of the first, a middle and the last sequence."""
+    _full_size("long_context", "wht", 5, [(0, 0), (7, 9), (15, 31)], B=16)
 
 
 def test_full_size_gqa_turbo3_keys():
@@ -379,6 +394,17 @@ def test_decode_merge_in_split_kernel_matches_combine(B, Hq, Hkv, L, fused):
         out, _ = run_decode(tq, kctx, vctx, q_t, kc, vc, B, Hq, Hkv, L, lens, scores=False)
     staged, _ = run_decode(tq, kctx, vctx, q_t, kc, vc, B, Hq, Hkv, L, lens, scores=False, staged=True)
     np.testing.assert_allclose(out, staged, rtol=1e-5, atol=1e-6)
+    # tq_decode_partial_merge repeated over one q preparation gives the same outputs
+    import torch
+    ws = tq.alloc_workspace(tq.tq_decode_workspace_size(kctx, vctx, B, Hq, Hkv, L))
+    sl = None if lens is None else torch.tensor(np.asarray(lens, np.int32), device="cuda")
+    tq.tq_decode_prepare_q(kctx, vctx, q_t, ws, B, Hq, Hkv, L)
+    for _ in range(3):
+        merged = torch.full((B, Hq, 128), float("nan"), dtype=torch.float32, device="cuda")
+        tq.tq_decode_partial_merge(kctx, vctx, kc, vc, merged, ws, B, Hq, Hkv, L, seq_lens=sl)
+        # (the CTA completing a unit can differ between runs, and with it the merge's
+        # fp32 summation order)
+        np.testing.assert_allclose(merged.cpu().numpy(), out, rtol=1e-5, atol=1e-6)
     ref, _ = reference(q32, kcodec, kb, vcodec, vb, lens)
     check_outputs(out, ref)
     assert tq.tq_ctx_device_status(kctx) == 0
