@@ -13,6 +13,7 @@ roofline.
 
 --workload picks another workload of the same path:
   gqa_t3k       the gqa_lognormal inputs with turbo3 keys and turbo4 values
+  gqa_t3        the gqa_lognormal inputs with turbo3 keys and turbo3 values
   prefill_chunk causal attention of the last 512-token chunk of a 32K-token prompt
                 (B=1, Hq=32, Hkv=8) over the turbo4 cache, tensor cores; TFLOP/s
   long_context  B=1, Hq=32, Hkv=8, L=131,072, turbo4 K and V, randomized WHT
@@ -75,6 +76,8 @@ DECODE = {
                         kernel="k_partial_t4", source="tq_decode.cu"),
     "gqa_t3k": dict(k_fmt="turbo3", v_fmt="turbo4", rotation="dense", k_seed=6, v_seed=106, qjl_seed=0,
                     kernel="k_partial_t4", source="tq_decode.cu"),
+    "gqa_t3": dict(k_fmt="turbo3", v_fmt="turbo3", rotation="dense", k_seed=8, v_seed=108, qjl_seed=0,
+                   kernel="k_partial_t4", source="tq_decode.cu"),
 }
 WRITE_KERNEL = {"dense": ("k_write_dense_tc", "tq_write_tc.cu"), "wht": ("k_write_wht", "tq_write.cu")}
 PREFILL = {"prefill_chunk": dict(fmt="turbo4", rotation="dense", k_seed=7, v_seed=107,
@@ -416,14 +419,22 @@ def decode_workload(args):
 
 
 L2_NOTE = "flushed before every step: 256 MB write then a read of it (no dirty lines left)"
+L2_B2B_NOTE = "packed K/V larger than twice the L2: steps back to back, no flush"
+L2_NOMINAL = 129 << 20  # GB300
 
 
-def decode_config(name, cfg):
+def decode_back_to_back(name, cfg, l2=L2_NOMINAL):
+    """Whether the decode workload's packed K/V exceed twice the L2 (then the steps run back
+    to back without a flush: no step can be served from the L2)."""
+    return cfg["B"] * cfg["Hkv"] * cfg["L"] * decode_unit_bytes(DECODE[name]) > 2 * l2
+
+
+def decode_config(name, cfg, l2=L2_NOMINAL):
     spec = DECODE[name]
     return {"workload": f"{name}: B={cfg['B']} Hq={cfg['Hq']} Hkv={cfg['Hkv']} d=128 L={cfg['L']}",
             "B": cfg["B"], "Hq": cfg["Hq"], "Hkv": cfg["Hkv"], "L": cfg["L"], "d": 128,
             "k_format": spec["k_fmt"], "v_format": spec["v_fmt"], "rotation": spec["rotation"],
-            "q_dtype": cfg["q_dtype"], "l2": L2_NOTE}
+            "q_dtype": cfg["q_dtype"], "l2": L2_B2B_NOTE if decode_back_to_back(name, cfg, l2) else L2_NOTE}
 
 
 def prefill_config():
@@ -540,6 +551,37 @@ def timed_graph_steps(torch, stream, fns, steps, warmup, flush_l2):
     return [e0.elapsed_time(e1) for e0, e1 in ev]
 
 
+def timed_graph_loop(torch, stream, fns, steps, warmup):
+    """Time `steps` steps issued back to back: one CUDA graph holding `steps` repetitions of
+    the callables `fns`, replayed once between two events; returns the mean step time (ms).
+
+    For inputs larger than twice the L2 (no flush between steps): every step reads the
+    whole input again after the other steps' reads evicted it, so no step is served from
+    the L2, and the library's kernels keep their programmatic launch overlap from one step
+    to the next, as in a decode loop."""
+    for _ in range(warmup):
+        for fn in fns:
+            fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(steps):
+            for fn in fns:
+                fn()
+    g.replay()  # the graph's own first replay, untimed
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def l2_bytes(torch, device):
+    return int(getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 0) or (129 << 20))
+
+
 E2E_MODE = ("value: the public API calls and the copies issued one by one from Python every step "
             "(host validation and enqueue inside the timed region); graph_*: the same calls and copies "
             "captured once in a CUDA graph and replayed every step")
@@ -604,24 +646,35 @@ def run_decode(args, rank, world, dist):
 
     launches_per_step = tq.tq_decode_step_num_launches(w["kctx"], w["vctx"], w["new_k"].dtype,
                                                        w["new_k"].shape[0], B, Hq, Hkv, L)
+    l2 = max(l2_bytes(torch, device), L2_NOMINAL)
+    b2b = decode_back_to_back(name, cfg, l2)
     if dist:
         dist.barrier()
     with ClockSampler(local) as clocks:
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
-        # the step, then the decode kernel alone (the roofline), same workload and flushes:
-        # as the step launches it (merge fused, over the q the step prepared), and the
-        # stage kernel that writes partials only
+        # the step, then the decode kernel alone (the roofline), same workload: as the step
+        # launches it (merge fused, over the q the step prepared), and the stage kernel that
+        # writes partials only.  Each both back to back (when the packed K/V exceed twice
+        # the L2) and with the L2 flushed before every launch.
+        loop = {}
+        if b2b:
+            for key, fn in (("step", step), ("merge", partial_merge), ("stage", partial)):
+                loop[key] = timed_graph_loop(torch, stream, (fn,), args.steps, args.warmup)
         step_ms = timed_graph_steps(torch, stream, (step,), args.steps, args.warmup, flush_l2)
         merge_ms = timed_graph_steps(torch, stream, (partial_merge,), args.steps, args.warmup, flush_l2)
         part_ms = timed_graph_steps(torch, stream, (partial,), args.steps, args.warmup, flush_l2)
         if dist:
             dist.barrier()
     clk = clocks.summary()
-    total_ms = max_over_ranks(sum(step_ms), dist, device)
-    merge_avg = max_over_ranks(statistics.mean(merge_ms), dist, device)
-    part_avg = max_over_ranks(statistics.mean(part_ms), dist, device)
+    flushed = {"step": statistics.mean(step_ms), "merge": statistics.mean(merge_ms),
+               "stage": statistics.mean(part_ms)}
+    timed = loop if b2b else flushed
+    total_ms = max_over_ranks(timed["step"] * args.steps, dist, device)
+    merge_avg = max_over_ranks(timed["merge"], dist, device)
+    part_avg = max_over_ranks(timed["stage"], dist, device)
+    flushed = {k: max_over_ranks(v, dist, device) for k, v in flushed.items()}
     merge_launches = tq.tq_decode_num_launches(w["kctx"], w["vctx"], B, Hq, Hkv, L) - 1
 
     # end to end through the public API with host buffers: q and the new K/V rows copied in,
@@ -670,12 +723,17 @@ def run_decode(args, rank, world, dist):
                          f"whole (batch, KV head) units of {L} keys x {Hq // Hkv} q-heads, "
                          "fp64 dequantize-then-softmax")
         fp32_loop = cpu_fp32_loop(leg)
-    line = common_line(DECODE_METRIC, args, world, ms_per_step, value, decode_config(name, cfg), "f32")
+    line = common_line(DECODE_METRIC, args, world, ms_per_step, value, decode_config(name, cfg, l2), "f32")
     merged = "merge fused" if merge_launches == 1 else "then the combine kernel"
     line.update({
-        "timing": ("each step one CUDA graph (tq_decode_step: SET_ROWS of the new K/V rows and the q "
-                   "preparation in one launch, then the split-K decode with the merge fused), steps queued "
-                   "back to back; the split-K decode alone timed the same way for the roofline"),
+        "timing": (("the steps back to back: one CUDA graph of K tq_decode_step calls (each SET_ROWS of the "
+                    "new K/V rows and the q preparation in one launch, then the split-K decode with the merge "
+                    "fused), replayed once between two events; the split-K decode alone timed the same way "
+                    "for the roofline" if b2b else
+                    "each step one CUDA graph replay (tq_decode_step) between two events, the L2 flushed "
+                    "before every step; the split-K decode alone timed the same way for the roofline")),
+        "l2_flushed_ms": {"step": flushed["step"], "kernel": flushed["merge"], "stage_kernel": flushed["stage"],
+                          "note": "the same launches one at a time, the L2 flushed before each"},
         "keys_per_s": job_rate(B * Hkv * L, world, ms_per_step),
         "q_head_scores_per_s": job_rate(B * Hq * L, world, ms_per_step),
         "hbm_frac_of_measured_step": value / peak,

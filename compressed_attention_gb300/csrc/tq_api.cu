@@ -116,7 +116,8 @@ tq_status check_current_device(int device, const char *who) {
 }
 
 bool decode_pair_supported(const tq_ctx *k, const tq_ctx *v) {
-  return ((k->fmt == TQ_FMT_TURBO4 || k->fmt == TQ_FMT_TURBO3) && v->fmt == TQ_FMT_TURBO4) ||
+  return ((k->fmt == TQ_FMT_TURBO4 || k->fmt == TQ_FMT_TURBO3) &&
+          (v->fmt == TQ_FMT_TURBO4 || v->fmt == TQ_FMT_TURBO3)) ||
          (k->fmt == TQ_FMT_PROD3 && v->fmt == TQ_FMT_VGROUP2);
 }
 }  // namespace tq

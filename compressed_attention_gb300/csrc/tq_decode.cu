@@ -70,7 +70,7 @@ struct PartialParams {
   const uint8_t *vc;
   const int32_t *seq_lens;
   int B, Hq, Hkv, L, gq, n_hg;
-  int tiles_per_unit, tiles_per_cta, vx, total_tiles, n_part;
+  int tiles_per_unit, sched_g, sched_v, vx, total_tiles, n_part;
   const uint32_t *qhl;
   const float *qsc;
   float *part;
@@ -107,10 +107,22 @@ struct SmemHead {
   int n_units;                          // fused combine: the units whose partials this CTA
   int units[FIN_MAX];                   // wrote; after the counts, the ones it completed
 };
+// The next work item's rotated q (fp16 hi and lo operand halves of up to 8 heads, 512 B
+// each) and its per-head scales, copied in by the producer ahead of the consumers.
+struct QStage {
+  uint64_t full;    // producer: scales stored, then the q copies' bytes
+  uint64_t empty;   // consumer warps: q taken into registers
+  float qs[8];
+  uint32_t pad[4];
+  uint32_t q[8][128];
+};
 constexpr uint32_t STAGE_A_OFF = (sizeof(SmemHead) + 15) & ~15u;
 constexpr uint32_t LUT_OFF = LUT_WINDOW - RESERVED_SMEM;
 constexpr uint32_t STAGE_B_OFF = LUT_OFF + 256 * 64 * 4;
-constexpr uint32_t SMEM_BYTES = STAGE_B_OFF + 6 * STAGE_BUF;
+constexpr uint32_t QSTAGE_OFF = STAGE_B_OFF + 6 * STAGE_BUF;
+constexpr uint32_t SMEM_BYTES = QSTAGE_OFF + sizeof(QStage);
+static_assert(QSTAGE_OFF % 16 == 0 && offsetof(QStage, q) % 16 == 0, "bulk-copy destinations");
+static_assert(SMEM_BYTES + RESERVED_SMEM <= 228 * 1024, "shared memory of one SM");
 static_assert(STAGE_A_OFF + 2 * STAGE_BUF <= LUT_OFF, "two stage buffers below the table");
 static_assert(NSTAGE == 4, "stage buffer placement assumes four stages");
 
@@ -188,6 +200,41 @@ __device__ __forceinline__ float t3_block(const uint8_t *blk, int t, uint32_t lu
 }
 
 
+__device__ __forceinline__ float half_at(const uint8_t *p) {
+  return __half2float(*reinterpret_cast<const __half *>(p));
+}
+
+// Largest of the four block norms of a 56-byte turbo3 row.
+__device__ __forceinline__ float t3_max_norm(const uint8_t *row) {
+  return fmaxf(fmaxf(half_at(row), half_at(row + 14)), fmaxf(half_at(row + 28), half_at(row + 42)));
+}
+
+// Four 3-bit turbo3 indices, one per byte: byte j = (2-bit field j of the qs byte) | (bit j
+// of the sign nibble selected by `shift`) << 2.  The 2-bit fields spread to their bytes by
+// two multiplies over disjoint bit ranges (fields 0, 2 by 1 + 2^12; fields 1, 3 by 2^6 +
+// 2^18), the four sign bits by one (1 + 2^7 + 2^14 + 2^21).
+__device__ __forceinline__ uint32_t t3_index_word(uint32_t qbyte, uint32_t sbyte, uint32_t shift) {
+  const uint32_t q = ((qbyte & 0x33u) * 0x1001u & 0x00030003u) | ((qbyte & 0xCCu) * 0x40040u & 0x03000300u);
+  const uint32_t sg = ((sbyte >> shift) & 15u) * 0x204081u & 0x01010101u;
+  return q | (sg << 2);
+}
+
+// The PV B operand of one column group from the probabilities of this lane's two score
+// rows: column g takes head g/2, its fp16 hi (g even) or lo (g odd) part, for the keys
+// a_t, a_t+2 (k 2t, 2t+1) and a_t+4, a_t+6 (k 2t+8, 2t+9), gathered from the lanes that
+// own those keys' scores.
+__device__ __forceinline__ void p_operand(float pp0, float pp1, int src0, int src1, float lo_sel,
+                                          uint32_t (&pb)[2]) {
+  const float va = __shfl_sync(FULL_MASK, pp0, src0), vb = __shfl_sync(FULL_MASK, pp0, src1);
+  const float vc = __shfl_sync(FULL_MASK, pp1, src0), vd = __shfl_sync(FULL_MASK, pp1, src1);
+  const __half2 hab = __floats2half2_rn(va, vb), hcd = __floats2half2_rn(vc, vd);
+  const float2 fab = __half22float2(hab), fcd = __half22float2(hcd);
+  const __half2 rab = __floats2half2_rn(fmaf(-lo_sel, fab.x, va), fmaf(-lo_sel, fab.y, vb));
+  const __half2 rcd = __floats2half2_rn(fmaf(-lo_sel, fcd.x, vc), fmaf(-lo_sel, fcd.y, vd));
+  pb[0] = *reinterpret_cast<const uint32_t *>(&rab);
+  pb[1] = *reinterpret_cast<const uint32_t *>(&rcd);
+}
+
 // Physical key (within a 16-key block) of score row r.  Rows g and g+8 belong to
 // lane group g.  With this order the packed-word loads of a warp hit every bank at
 // most twice, and the PV operand of lane (g, t) -- keys a_t, a_t+2, a_t+4, a_t+6
@@ -213,10 +260,11 @@ __device__ __forceinline__ void consumers_sync() { named_sync1<CWARPS * 32>(); }
 // 2b and 2b+1 cover block b, lane t holding its elements 8t..8t+7 (the q operand is
 // permuted to match once per item), and each block's product is scaled by that
 // block's norm as it is added to the score.
-template <int NG, bool SCORES, int KP, int VP, bool FIXED, bool K3>
+template <int NG, bool SCORES, int KP, int VP, bool FIXED, bool K3, bool V3>
 __global__ void __maxnreg__(128)
     k_partial_t4(const PartialParams p) {
   constexpr int KROW = K3 ? T3_ROW : T4_ROW;
+  constexpr int VROW = V3 ? T3_ROW : T4_ROW;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   SmemHead &sm = *reinterpret_cast<SmemHead *>(smem_raw);
   uint32_t *lut = reinterpret_cast<uint32_t *>(smem_raw + LUT_OFF);
@@ -227,44 +275,47 @@ __global__ void __maxnreg__(128)
     return;
   }
 
-  if (threadIdx.x == 0) {
+  QStage &qst = *reinterpret_cast<QStage *>(smem_raw + QSTAGE_OFF);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == CWARPS * 32) {  // the producer's lane sets up the barriers
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], CWARPS);
     }
+    mbar_init(&qst.full, 1);
+    mbar_init(&qst.empty, CWARPS);
     sm.abort_flag = 0;
     sm.n_units = 0;
     fence_mbar_init();
   }
-  // Fill the table: each (byte, half) entry is computed once and stored to its 32
-  // slots with 16-byte stores.
-  for (int piece = threadIdx.x; piece < 256 * 8; piece += NTHREADS) {
-    const int byte = piece >> 3, chunk = piece & 7;  // chunks 0-3: key slots, 4-7: value slots
-    const uint32_t *c16 = (chunk & 4) ? p.vc16 : p.kc16;
-    const uint32_t lo = (c16[(byte & 15) >> 1] >> (16 * (byte & 1))) & 0xFFFFu;
-    const uint32_t hi = (c16[(byte >> 4) >> 1] >> (16 * ((byte >> 4) & 1))) & 0xFFFFu;
-    // turbo3 keys: the key slots hold the spread sign bits instead
-    const uint32_t e = (K3 && chunk < 4) ? t3_sign_word(byte) : lo | (hi << 16);
-    uint4 *dst = reinterpret_cast<uint4 *>(lut + byte * 64 + chunk * 8);
-    dst[0] = make_uint4(e, e, e, e);
-    dst[1] = make_uint4(e, e, e, e);
-  }
-  pdl_wait();  // the caches, q and the workspace may be written by the previous kernel
-  if (threadIdx.x == 0 && p.seq_lens) {
-    for (int b = 0; b < p.B; ++b)
-      if (p.seq_lens[b] < 1 || p.seq_lens[b] > p.L) atomicExch(p.status, (int32_t)DEVERR_SEQLEN);
-  }
-  __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, t = lane & 3;
-
   if (warp == CWARPS) {
-    // ---------------- producer: one elected lane streams every tile of every item
+    // ---------------- producer: streams every tile (and every item's q) of the range.  It
+    // takes no part in the table fill: once the previous kernel is complete it starts the
+    // first copies at once.
+    named_arrive0<NTHREADS>();  // the barriers are set up
+    pdl_wait();
     if (lane == 0) {
-      int ctr = 0, tt = cta_first_tile(p, cta);
+      int ctr = 0, tt = cta_first_tile(p, cta), n_item = 0;
       Item it;
       bool ok = true;
       while (ok && next_item(p, cta, tt, it)) {
+        // this item's q: after the consumers have taken the previous item's
+        if (n_item > 0 && !mbar_wait_bounded(&qst.empty, (n_item - 1) & 1, WAIT_LIMIT_NS)) {
+          atomicExch(&sm.abort_flag, 1);
+          atomicExch(p.status, (int32_t)DEVERR_TIMEOUT);
+          ok = false;
+          break;
+        }
+        {
+          const int hg = it.unit % p.n_hg, bk = it.unit / p.n_hg;
+          const int b = bk / p.Hkv, kvh = bk % p.Hkv;
+          const int G = min(4 * NG, p.gq - hg * 4 * NG);
+          const size_t row0 = (size_t)b * p.Hq + kvh * p.gq + hg * 4 * NG;
+          for (int h = 0; h < G; ++h) qst.qs[h] = p.qsc[2 * (row0 + h)];
+          mbar_arrive_expect_tx(&qst.full, (uint32_t)G * 512u);
+          for (int h = 0; h < G; ++h) bulk_g2s(qst.q[h], p.qhl + (row0 + h) * 256, 512u, &qst.full);
+          ++n_item;
+        }
         const int Lb = unit_len(p, it.unit);
         const size_t unit_row0 = (size_t)(it.unit / p.n_hg) * p.L;
         for (int j = it.t0; j < it.t1; ++j) {
@@ -283,10 +334,10 @@ __global__ void __maxnreg__(128)
             ok = false;
             break;
           }
-          const size_t ks = (unit_row0 + kf) * KROW, vs = (unit_row0 + kf) * T4_ROW;
+          const size_t ks = (unit_row0 + kf) * KROW, vs = (unit_row0 + kf) * VROW;
           const size_t k0 = ks & ~(size_t)15, v0 = vs & ~(size_t)15;
           const uint32_t kbytes = (uint32_t)(((ks + (size_t)nk * KROW + 15) & ~(size_t)15) - k0);
-          const uint32_t vbytes = (uint32_t)(((vs + (size_t)nk * T4_ROW + 15) & ~(size_t)15) - v0);
+          const uint32_t vbytes = (uint32_t)(((vs + (size_t)nk * VROW + 15) & ~(size_t)15) - v0);
           mbar_arrive_expect_tx(&sm.full[s], kbytes + vbytes);
           bulk_g2s(stage_buf(smem_raw, s), p.kc + k0, kbytes, &sm.full[s]);
           bulk_g2s(stage_buf(smem_raw, 4 + s), p.vc + v0, vbytes, &sm.full[s]);
@@ -301,10 +352,36 @@ __global__ void __maxnreg__(128)
       if (!ok || sm.abort_flag) {
         for (int c = (ctr > NSTAGE ? ctr - NSTAGE : 0); c < ctr; ++c)
           (void)mbar_wait_bounded(&sm.full[c % NSTAGE], (c / NSTAGE) & 1, WAIT_LIMIT_NS);
+        if (n_item > 0) (void)mbar_wait_bounded(&qst.full, (n_item - 1) & 1, WAIT_LIMIT_NS);
       }
     }
     return;
   }
+  // Fill the table (consumer warps): each (byte, half) entry is computed once and stored
+  // to its 32 slots with 16-byte stores.
+  for (int piece = threadIdx.x; piece < 256 * 8; piece += CWARPS * 32) {
+    const int byte = piece >> 3, chunk = piece & 7;  // chunks 0-3: key slots, 4-7: value slots
+    const uint32_t *c16 = (chunk & 4) ? p.vc16 : p.kc16;
+    const uint32_t lo = (c16[(byte & 15) >> 1] >> (16 * (byte & 1))) & 0xFFFFu;
+    const uint32_t hi = (c16[(byte >> 4) >> 1] >> (16 * ((byte >> 4) & 1))) & 0xFFFFu;
+    // turbo3 values: byte = 3-bit index of key a | 3-bit index of key b << 3 (rows 0-63)
+    const uint32_t lo3 = (c16[(byte & 7) >> 1] >> (16 * (byte & 1))) & 0xFFFFu;
+    const uint32_t hi3 = (c16[((byte >> 3) & 7) >> 1] >> (16 * ((byte >> 3) & 1))) & 0xFFFFu;
+    // turbo3 keys: the key slots hold the spread sign bits instead
+    const uint32_t e = (K3 && chunk < 4)   ? t3_sign_word(byte)
+                       : (V3 && chunk >= 4) ? (byte < 64 ? lo3 | (hi3 << 16) : 0u)
+                                            : lo | (hi << 16);
+    uint4 *dst = reinterpret_cast<uint4 *>(lut + byte * 64 + chunk * 8);
+    dst[0] = make_uint4(e, e, e, e);
+    dst[1] = make_uint4(e, e, e, e);
+  }
+  pdl_wait();  // the caches, q and the workspace may be written by the previous kernel
+  if (threadIdx.x == 0 && p.seq_lens) {
+    for (int b = 0; b < p.B; ++b)
+      if (p.seq_lens[b] < 1 || p.seq_lens[b] > p.L) atomicExch(p.status, (int32_t)DEVERR_SEQLEN);
+  }
+  named_sync0<NTHREADS>();  // the table is filled and the barriers are set up
+  const int g = lane >> 2, t = lane & 3;
 
   // ---------------- consumers
   const uint32_t lut_base = smem_addr(lut);
@@ -318,7 +395,7 @@ __global__ void __maxnreg__(128)
   // without bank conflicts in every load shape above; warps 0..13 pair up on 32-row blocks
   // that way, and the last warp (and turbo3 keys, whose 56-byte rows differ) keeps 16
   // consecutive rows.  Keys a_t + 2m stay 2m rows after key a_t in both layouts.
-  const bool paired = !K3 && warp < 2 * (CWARPS / 2);
+  const bool paired = !K3 && !V3 && warp < 2 * (CWARPS / 2);
   const int r0 = paired ? 32 * (warp >> 1) + 8 * (warp & 1) : 16 * warp;
   auto row_of = [&](int k) { return paired ? r0 + (k & 7) + 16 * (k >> 3) : r0 + k; };
   const int pk0 = row_of(rk0), pk1 = row_of(rk1), pat = row_of(at);
@@ -326,7 +403,7 @@ __global__ void __maxnreg__(128)
   const int src0 = 4 * t + hs, src1 = 4 * (4 + t) + hs;
   const float lo_sel = (g & 1) ? 1.f : 0.f;
 
-  int ctr = 0, tt = cta_first_tile(p, cta);
+  int ctr = 0, tt = cta_first_tile(p, cta), n_item = 0;
   Item it;
   bool aborted = false;
   while (!aborted && next_item(p, cta, tt, it)) {
@@ -338,7 +415,16 @@ __global__ void __maxnreg__(128)
     const int head0 = kvh * p.gq + hg * 4 * NG;
     const size_t unit_row0 = (size_t)bk * p.L;
 
-    // q as the B operand: column g = (head slot g/2, part g%2 = hi/lo), rows = dims.
+    // q as the B operand: column g = (head slot g/2, part g%2 = hi/lo), rows = dims, from
+    // the q stage the producer filled for this item
+    if (!mbar_wait_bounded(&qst.full, n_item & 1, WAIT_LIMIT_NS)) {
+      if (lane == 0) {
+        atomicExch(p.status, (int32_t)DEVERR_TIMEOUT);
+        atomicExch(&sm.abort_flag, 1);
+      }
+      aborted = true;
+      break;
+    }
     uint32_t qb[NG][8][2];
     float qs[NG];
 #pragma unroll
@@ -346,7 +432,7 @@ __global__ void __maxnreg__(128)
       const int slot = c * 4 + hs;
       if (slot < G && K3) {
         // slice 2b + h, lane t: dims 32b + 8t + 4h + {0, 2} and {1, 3}
-        const uint32_t *qw = p.qhl + (size_t)(b * p.Hq + head0 + slot) * 256 + (g & 1) * 64 + 4 * t;
+        const uint32_t *qw = qst.q[slot] + (g & 1) * 64 + 4 * t;
 #pragma unroll
         for (int bl = 0; bl < 4; ++bl) {
           const uint32_t w0 = qw[16 * bl], w1 = qw[16 * bl + 1];
@@ -357,7 +443,7 @@ __global__ void __maxnreg__(128)
           qb[c][2 * bl + 1][1] = prmt(w2, w3, 0x7632u);
         }
       } else if (slot < G) {
-        const uint32_t *qw = p.qhl + (size_t)(b * p.Hq + head0 + slot) * 256 + (g & 1) * 64 + 16 * t;
+        const uint32_t *qw = qst.q[slot] + (g & 1) * 64 + 16 * t;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           qb[c][kk][0] = qw[2 * kk];
@@ -368,8 +454,11 @@ __global__ void __maxnreg__(128)
         for (int kk = 0; kk < 8; ++kk) qb[c][kk][0] = qb[c][kk][1] = 0u;
       }
       const int my = c * 4 + t;  // the head whose scores this lane holds
-      qs[c] = (my < G) ? p.qsc[2 * (b * p.Hq + head0 + my)] : 0.f;
+      qs[c] = (my < G) ? qst.qs[my] : 0.f;
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&qst.empty);  // this warp's q is in registers
+    ++n_item;
     float O[NG][8][4];
     float M[NG], lsum[NG];
 #pragma unroll
@@ -393,7 +482,7 @@ __global__ void __maxnreg__(128)
         break;
       }
       const int nk = min(TILE, Lb - kf);
-      const size_t ks = (unit_row0 + kf) * KROW, vs = (unit_row0 + kf) * T4_ROW;
+      const size_t ks = (unit_row0 + kf) * KROW, vs = (unit_row0 + kf) * VROW;
       const uint8_t *Ks = stage_buf(smem_raw, s) + (ks & 15);
       const uint8_t *Vs = stage_buf(smem_raw, 4 + s) + (vs & 15);
       if (r0 < nk) {  // the warp's first row is its lowest: some key is valid
@@ -448,12 +537,15 @@ __global__ void __maxnreg__(128)
         // turbo3 keys carry their block norms in sa already
         const float nk0 = K3 ? 1.f : *reinterpret_cast<const float *>(Ks + pk0 * KROW);
         const float nk1 = K3 ? 1.f : *reinterpret_cast<const float *>(Ks + pk1 * KROW);
-        const float nv0 = *reinterpret_cast<const float *>(Vs + pk0 * T4_ROW);
-        const float nv1 = *reinterpret_cast<const float *>(Vs + pk1 * T4_ROW);
+        // turbo3 values: the largest of the key's four block norms goes into the exponent,
+        // each block's ratio to it into that block's probability operand
+        const float nv0 = V3 ? t3_max_norm(Vs + pk0 * VROW) : *reinterpret_cast<const float *>(Vs + pk0 * VROW);
+        const float nv1 = V3 ? t3_max_norm(Vs + pk1 * VROW) : *reinterpret_cast<const float *>(Vs + pk1 * VROW);
         const bool ok0 = pk0 < nk, ok1 = pk1 < nk;
         const float nu0 = ok0 ? fmaxf(log2_approx(nv0), -64.f) : 0.f;
         const float nu1 = ok1 ? fmaxf(log2_approx(nv1), -64.f) : 0.f;
         uint32_t pb[NG][2];
+        float pq0[NG], pq1[NG];  // turbo3 values: the probabilities, scaled per block below
 #pragma unroll
         for (int c = 0; c < NG; ++c) {
           const float d0 = K3 ? sa[c][0] + sa[c][1] : (sa[c][0] + sa[c][1]) + (sb[c][0] + sb[c][1]);
@@ -483,21 +575,53 @@ __global__ void __maxnreg__(128)
           lsum[c] += exp2_approx(s0 - Mu) + exp2_approx(s1 - Mu);
           const float pp0 = exp2_approx(u0 - Mu + P_SHIFT);
           const float pp1 = exp2_approx(u1 - Mu + P_SHIFT);
-          // P^T as the B operand: column g takes head g/2, hi (g even) or lo (g odd) part,
-          // for the keys a_t, a_t+2 (k 2t, 2t+1) and a_t+4, a_t+6 (k 2t+8, 2t+9).
-          const float va = __shfl_sync(FULL_MASK, pp0, src0), vb = __shfl_sync(FULL_MASK, pp0, src1);
-          const float vc = __shfl_sync(FULL_MASK, pp1, src0), vd = __shfl_sync(FULL_MASK, pp1, src1);
-          const __half2 hab = __floats2half2_rn(va, vb), hcd = __floats2half2_rn(vc, vd);
-          const float2 fab = __half22float2(hab), fcd = __half22float2(hcd);
-          const __half2 rab = __floats2half2_rn(fmaf(-lo_sel, fab.x, va), fmaf(-lo_sel, fab.y, vb));
-          const __half2 rcd = __floats2half2_rn(fmaf(-lo_sel, fcd.x, vc), fmaf(-lo_sel, fcd.y, vd));
-          pb[c][0] = *reinterpret_cast<const uint32_t *>(&rab);
-          pb[c][1] = *reinterpret_cast<const uint32_t *>(&rcd);
+          if (V3) {
+            pq0[c] = pp0, pq1[c] = pp1;
+          } else {
+            p_operand(pp0, pp1, src0, src1, lo_sel, pb[c]);
+          }
+        }
+        if (V3) {
+          // ---- turbo3 values.  Each 16-row m-tile lies inside one 32-element block b: m-tile
+          // 2b + h, rows g and g+8 = elements 4g + 2h and 4g + 2h + 1 of block b, so block b's
+          // norm (over the key's largest, which sits in the exponent) scales that m-tile's
+          // probability operand exactly; lane group g decodes elements 4g .. 4g+3 of every
+          // block, two keys per table lookup (a 6-bit index: 3 bits of each key).
+          // (rows past the tile's valid keys hold stale bytes: their ratios are forced to 0)
+          const float inv0 = (ok0 && nv0 > 0.f) ? 1.f / nv0 : 0.f, inv1 = (ok1 && nv1 > 0.f) ? 1.f / nv1 : 0.f;
+          const uint8_t *vq = Vs + pat * VROW + 2 + g;            // key a_t, block 0: qs byte g
+          const uint8_t *vsg = Vs + pat * VROW + 10 + (g >> 1);  // and its sign byte
+          const uint32_t ssh = 4u * (g & 1);
+#pragma unroll
+          for (int bl = 0; bl < 4; ++bl) {
+            const float r0 = inv0 > 0.f ? half_at(Vs + pk0 * VROW + 14 * bl) * inv0 : 0.f;
+            const float r1 = inv1 > 0.f ? half_at(Vs + pk1 * VROW + 14 * bl) * inv1 : 0.f;
+            uint32_t pbb[NG][2];
+#pragma unroll
+            for (int c = 0; c < NG; ++c) p_operand(pq0[c] * r0, pq1[c] * r1, src0, src1, lo_sel, pbb[c]);
+            uint32_t wk[4];  // keys a_t + 2i: byte j = 3-bit index of element 4g + j
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              wk[i] = t3_index_word(vq[2 * i * VROW + 14 * bl], vsg[2 * i * VROW + 14 * bl], ssh);
+            const uint32_t w01 = wk[0] | (wk[1] << 3), w23 = wk[2] | (wk[3] << 3);
+            {
+              const uint32_t a[4] = {lut_byte<FIXED, 0>(lut_base, vword, w01), lut_byte<FIXED, 1>(lut_base, vword, w01),
+                                     lut_byte<FIXED, 0>(lut_base, vword, w23), lut_byte<FIXED, 1>(lut_base, vword, w23)};
+#pragma unroll
+              for (int c = 0; c < NG; ++c) mma_f16(O[c][2 * bl], a, pbb[c][0], pbb[c][1]);
+            }
+            {
+              const uint32_t a[4] = {lut_byte<FIXED, 2>(lut_base, vword, w01), lut_byte<FIXED, 3>(lut_base, vword, w01),
+                                     lut_byte<FIXED, 2>(lut_base, vword, w23), lut_byte<FIXED, 3>(lut_base, vword, w23)};
+#pragma unroll
+              for (int c = 0; c < NG; ++c) mma_f16(O[c][2 * bl + 1], a, pbb[c][0], pbb[c][1]);
+            }
+          }
         }
         // ---- O^T[dims x cols] += V_hat^T[dims x keys] P^T
-        const uint8_t *va_p = Vs + pat * T4_ROW + 4 + 8 * g;  // key a_t; a_t+2, +4, +6 follow
+        const uint8_t *va_p = Vs + pat * VROW + 4 + 8 * g;  // key a_t; a_t+2, +4, +6 follow
 #pragma unroll
-        for (int w = 0; w < 2; ++w) {
+        for (int w = 0; w < (V3 ? 0 : 2); ++w) {
           const uint32_t xa = ld_u32(va_p + 4 * w), xb = ld_u32(va_p + 2 * T4_ROW + 4 * w);
           const uint32_t xc = ld_u32(va_p + 4 * T4_ROW + 4 * w), xd = ld_u32(va_p + 6 * T4_ROW + 4 * w);
           // byte i of zlo = (low nibble of key a, low nibble of key b) of byte 8g + 4w + i
@@ -554,11 +678,14 @@ __global__ void __maxnreg__(128)
       float ms = -INFINITY;
       for (int w = 0; w < CWARPS; ++w) ms = fmaxf(ms, sm.mw[w][hh]);
       const float fac = (M[c] == -INFINITY) ? 0.f : exp2_approx(M[c] - ms);
-      float *orow = &sm.osm[warp][t][16 * g];
+      // rows g and g+8 of m-tile mt: dims 16g + 2mt and +1 (turbo4 values), or for turbo3
+      // values (m-tile 2b + h inside block b) dims 32b + 4g + 2h and +1
+      float *orow = &sm.osm[warp][t][0];
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
-        orow[2 * mt] = (O[c][mt][0] + O[c][mt][1]) * fac;
-        orow[2 * mt + 1] = (O[c][mt][2] + O[c][mt][3]) * fac;
+        const int dm = V3 ? 32 * (mt >> 1) + 4 * g + 2 * (mt & 1) : 16 * g + 2 * mt;
+        orow[dm] = (O[c][mt][0] + O[c][mt][1]) * fac;
+        orow[dm + 1] = (O[c][mt][2] + O[c][mt][3]) * fac;
       }
       consumers_sync();
       const int Gc = min(4, G - c * 4);
@@ -599,6 +726,19 @@ __global__ void __maxnreg__(128)
   // consumed).  Only after a clean finish: a CTA that gave up leaves its units unwritten
   // and the status flag set.
   if (!p.out) return;
+  // R is copied into the idle stage buffers at once, by every CTA that finished cleanly
+  // (every tile was consumed: the last item ended with a barrier of all consumer warps;
+  // no warp can give up after that), so that it lands while the counts make their
+  // round trip; most CTAs complete a unit.
+  float *rs = reinterpret_cast<float *>(smem_raw + STAGE_B_OFF);  // R, row-major [128][128]
+  static_assert(6 * STAGE_BUF >= D * D * 4, "R fits in the idle stage buffers");
+  const bool r_copy = p.r && !*reinterpret_cast<volatile int *>(&sm.abort_flag);
+  if (r_copy) {
+    for (int i = threadIdx.x; i < D * D / 4; i += CWARPS * 32)
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(rs + 4 * i)), "l"(p.r + 4 * i)
+                   : "memory");
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
   // Every consumer thread's partial stores fenced, then one count per item; the CTA whose
   // count completes a unit merges it.  The atomics are issued together (one round trip).
   __threadfence();
@@ -619,22 +759,16 @@ __global__ void __maxnreg__(128)
   }
   consumers_sync();
   const int n_fin = gave_up ? 0 : sm.n_units;
-  if (n_fin == 0) return;
+  if (n_fin == 0) {
+    if (r_copy) asm volatile("cp.async.wait_all;" ::: "memory");
+    return;
+  }
   // The completed units' heads in quads of four (NG quads per unit), up to three quads per
   // round: the round's nh heads are merged by twelve warps (W = 12 / nh per head, see
-  // below), and thread (quad, j) un-rotates dim j of that quad's heads.  R is copied
-  // first into the idle stage buffers (every tile was consumed: the last item ended with
-  // a barrier of all consumer warps), overlapping the first round's loads.
+  // below), and thread (quad, j) un-rotates dim j of that quad's heads, with R from the
+  // stage buffers (its copy was issued before the counts).
   constexpr int QUADS = 3;
   static_assert(4 * QUADS <= CWARPS && QUADS * D <= CWARPS * 32, "a round's heads and dims");
-  float *rs = reinterpret_cast<float *>(smem_raw + STAGE_B_OFF);  // R, row-major [128][128]
-  static_assert(6 * STAGE_BUF >= D * D * 4, "R fits in the idle stage buffers");
-  if (p.r) {
-    for (int i = threadIdx.x; i < D * D / 4; i += CWARPS * 32)
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(rs + 4 * i)), "l"(p.r + 4 * i)
-                   : "memory");
-    asm volatile("cp.async.commit_group;" ::: "memory");
-  }
   const int n_quads = n_fin * NG;
   for (int q0 = 0; q0 < n_quads; q0 += QUADS) {
     // nh heads this round; W warps per head split its partials between them (warp w takes
@@ -710,7 +844,7 @@ __global__ void __maxnreg__(128)
 #pragma unroll
       for (int m = 0; m < 4; ++m) sm.osm[warp][0][lane + 32 * m] = o[m] * fo;
     }
-    if (q0 == 0 && p.r) asm volatile("cp.async.wait_all;" ::: "memory");
+    if (q0 == 0 && r_copy) asm volatile("cp.async.wait_all;" ::: "memory");
     consumers_sync();  // merged heads (and, the first time, R) in shared memory
     // out = R^T o: thread (quad, j) reads column j of R once for the four heads of its
     // quad (o read as broadcast float4), four independent chains over k per head,
@@ -761,7 +895,7 @@ struct CombineParams {
   const float *part;
   int n_heads;      // B * Hq (decode) or B * T * Hq (prefill rows)
   int n_split;      // partial slots per head
-  int Hq, gq, heads_per_cta, n_hg, tiles_per_unit, tiles_per_cta, vx;
+  int Hq, gq, heads_per_cta, n_hg, tiles_per_unit, sched_g, sched_v, vx;
   int pf_T, pf_Hkv, pf_qpt, pf_n_qt;  // prefill geometry (pf_T = 0: decode)
   int no_main;      // 1: no split-K partials (every key is in the exact tail)
   int tail_slot;    // slot of an exact-tail partial per head, or -1
@@ -865,7 +999,6 @@ __global__ void __launch_bounds__(QWARPS * 32) k_combine(const CombineParams p) 
 
 bool decode_shape(const tq_ctx *k, const tq_ctx *v, int B, int Hq, int Hkv, int L,
                   DecodeShape *s) {
-  (void)v;
   s->B = B, s->Hq = Hq, s->Hkv = Hkv, s->L = L;
   s->gq = Hq / Hkv;
   s->pv = k->fmt == TQ_FMT_PROD3;
@@ -875,17 +1008,19 @@ bool decode_shape(const tq_ctx *k, const tq_ctx *v, int B, int Hq, int Hkv, int 
   const int64_t units = (int64_t)B * Hkv * s->n_hg;
   s->tiles_per_unit = (L + s->tile - 1) / s->tile;
   const int64_t total = units * s->tiles_per_unit;
-  s->vx = s->pv ? PV_ITEM_TILES : k->fmt == TQ_FMT_TURBO3 ? T3_ITEM_TILES : T4_ITEM_TILES;
+  s->vx = s->pv ? PV_ITEM_TILES
+                : (k->fmt == TQ_FMT_TURBO3 || v->fmt == TQ_FMT_TURBO3) ? T3_ITEM_TILES : T4_ITEM_TILES;
   const int64_t vtotal = units * (s->vx + s->tiles_per_unit);
   if (vtotal > INT32_MAX) return false;
   s->total_tiles = (int)total;
-  // One persistent CTA per SM; contiguous equal ranges of the virtual tile sequence
-  // (each unit with its item cost ahead of its tiles; the last range may be shorter).
-  const int64_t tpc = (vtotal + k->num_sms - 1) / k->num_sms;
-  s->tiles_per_cta = (int)(tpc < 1 ? 1 : tpc);
-  s->grid = (int)((vtotal + s->tiles_per_cta - 1) / s->tiles_per_cta);
+  // One persistent CTA per SM; the virtual tile sequence (each unit with its item cost
+  // ahead of its tiles) split in proportion, so the ranges differ by at most one tile.
+  s->vtotal = (int)vtotal;
+  s->grid = (int)(vtotal < k->num_sms ? vtotal : k->num_sms);
+  const int shortest = (int)(vtotal / s->grid);
+  s->tiles_per_cta = (int)((vtotal + s->grid - 1) / s->grid);
   // Partial slots per head: CTAs whose range meets one unit.
-  s->n_part = (s->tiles_per_unit + s->tiles_per_cta - 1) / s->tiles_per_cta + 1;
+  s->n_part = (s->tiles_per_unit + shortest - 1) / shortest + 1;
   return true;
 }
 
@@ -935,10 +1070,10 @@ cudaError_t launch_prepare_q(const tq_ctx *k, const void *q, int q_dtype, const 
   return launch_pdl(kern, dim3(grid), dim3(QWARPS * 32), QPREP_SMEM, st, p);
 }
 
-template <int NG, bool SC, int KP, int VP, bool FIXED, bool K3>
+template <int NG, bool SC, int KP, int VP, bool FIXED, bool K3, bool V3>
 cudaError_t launch_t4(const PartialParams &p, dim3 grid, cudaStream_t st) {
   const size_t smem = SMEM_BYTES;
-  auto kern = k_partial_t4<NG, SC, KP, VP, FIXED, K3>;
+  auto kern = k_partial_t4<NG, SC, KP, VP, FIXED, K3, V3>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -952,22 +1087,23 @@ cudaError_t launch_t4(const PartialParams &p, dim3 grid, cudaStream_t st) {
 constexpr int K_PRMT_WORDS = 0;
 constexpr int V_PRMT_WORDS = 0;
 
-template <bool K3>
+template <bool K3, bool V3>
 cudaError_t launch_t4_variant(const PartialParams &p, int heads_per_cta, bool fixed, bool scores,
                               dim3 grid, cudaStream_t st) {
   constexpr int KP = K3 ? 0 : K_PRMT_WORDS;
+  constexpr int VP = V3 ? 0 : V_PRMT_WORDS;
   if (heads_per_cta == 8) {
     if (fixed)
-      return scores ? launch_t4<2, true, KP, V_PRMT_WORDS, true, K3>(p, grid, st)
-                    : launch_t4<2, false, KP, V_PRMT_WORDS, true, K3>(p, grid, st);
-    return scores ? launch_t4<2, true, KP, V_PRMT_WORDS, false, K3>(p, grid, st)
-                  : launch_t4<2, false, KP, V_PRMT_WORDS, false, K3>(p, grid, st);
+      return scores ? launch_t4<2, true, KP, VP, true, K3, V3>(p, grid, st)
+                    : launch_t4<2, false, KP, VP, true, K3, V3>(p, grid, st);
+    return scores ? launch_t4<2, true, KP, VP, false, K3, V3>(p, grid, st)
+                  : launch_t4<2, false, KP, VP, false, K3, V3>(p, grid, st);
   }
   if (fixed)
-    return scores ? launch_t4<1, true, KP, V_PRMT_WORDS, true, K3>(p, grid, st)
-                  : launch_t4<1, false, KP, V_PRMT_WORDS, true, K3>(p, grid, st);
-  return scores ? launch_t4<1, true, KP, V_PRMT_WORDS, false, K3>(p, grid, st)
-                : launch_t4<1, false, KP, V_PRMT_WORDS, false, K3>(p, grid, st);
+    return scores ? launch_t4<1, true, KP, VP, true, K3, V3>(p, grid, st)
+                  : launch_t4<1, false, KP, VP, true, K3, V3>(p, grid, st);
+  return scores ? launch_t4<1, true, KP, VP, false, K3, V3>(p, grid, st)
+                : launch_t4<1, false, KP, VP, false, K3, V3>(p, grid, st);
 }
 
 // The fused combine serves the plain turbo4 / turbo3-key decode (no exact tail) when a CTA
@@ -993,7 +1129,7 @@ cudaError_t launch_partial(const tq_ctx *k, const tq_ctx *v, const uint8_t *kc,
   p.withhold_first_tile = withhold_first_tile ? 1 : 0;
   p.kc = kc, p.vc = vc, p.seq_lens = seq_lens;
   p.B = s.B, p.Hq = s.Hq, p.Hkv = s.Hkv, p.L = s.L, p.gq = s.gq, p.n_hg = s.n_hg;
-  p.tiles_per_unit = s.tiles_per_unit, p.tiles_per_cta = s.tiles_per_cta; p.vx = s.vx;
+  p.tiles_per_unit = s.tiles_per_unit, p.sched_g = s.grid, p.sched_v = s.vtotal; p.vx = s.vx;
   p.total_tiles = s.total_tiles, p.n_part = s.n_part;
   p.qhl = ws.qhl, p.qsc = ws.qsc, p.part = ws.partials, p.scores = scores_dbg;
   const bool k3 = k->fmt == TQ_FMT_TURBO3;
@@ -1014,8 +1150,13 @@ cudaError_t launch_partial(const tq_ctx *k, const tq_ctx *v, const uint8_t *kc,
   p.status = k->d_status;
   const bool fixed = k->reserved_smem == (int)RESERVED_SMEM;
   const bool sc = scores_dbg != nullptr;
-  const cudaError_t e = k3 ? launch_t4_variant<true>(p, s.heads_per_cta, fixed, sc, dim3(s.grid), st)
-                           : launch_t4_variant<false>(p, s.heads_per_cta, fixed, sc, dim3(s.grid), st);
+  const bool v3 = v->fmt == TQ_FMT_TURBO3;
+  const dim3 grid(s.grid);
+  const cudaError_t e =
+      k3 ? (v3 ? launch_t4_variant<true, true>(p, s.heads_per_cta, fixed, sc, grid, st)
+               : launch_t4_variant<true, false>(p, s.heads_per_cta, fixed, sc, grid, st))
+         : (v3 ? launch_t4_variant<false, true>(p, s.heads_per_cta, fixed, sc, grid, st)
+               : launch_t4_variant<false, false>(p, s.heads_per_cta, fixed, sc, grid, st));
   if (e == cudaSuccess && fused) *fused = fuse;
   return e;
 }
@@ -1028,7 +1169,7 @@ cudaError_t launch_combine(const tq_ctx *k, const tq_ctx *v, const DecodeShape &
   p.n_heads = s.B * s.Hq;
   p.n_split = s.n_part;
   p.Hq = s.Hq, p.gq = s.gq, p.heads_per_cta = s.heads_per_cta, p.n_hg = s.n_hg;
-  p.tiles_per_unit = s.tiles_per_unit, p.tiles_per_cta = s.tiles_per_cta; p.vx = s.vx;
+  p.tiles_per_unit = s.tiles_per_unit, p.sched_g = s.grid, p.sched_v = s.vtotal; p.vx = s.vx;
   p.no_main = s.no_main ? 1 : 0;
   p.tail_slot = s.tail_slot;
   const bool vgroup = v->fmt == TQ_FMT_VGROUP2;  // values are not rotated
@@ -1048,7 +1189,7 @@ cudaError_t launch_combine_prefill(const tq_ctx *v, const PrefillShape &s, float
   p.n_heads = s.B * s.T * s.Hq;
   p.n_split = s.n_part;
   p.Hq = s.Hq, p.gq = s.gq;
-  p.tiles_per_unit = s.tiles_per_unit, p.tiles_per_cta = s.tiles_per_cta;
+  p.tiles_per_unit = s.tiles_per_unit, p.sched_g = s.grid, p.sched_v = s.total_tiles;
   p.vx = 0;  // the prefill splits its tiles equally
   p.pf_T = s.T, p.pf_Hkv = s.Hkv, p.pf_qpt = s.qpt, p.pf_n_qt = s.n_qt;
   p.tail_slot = -1;

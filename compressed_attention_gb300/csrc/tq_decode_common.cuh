@@ -25,9 +25,10 @@ constexpr uint32_t RESERVED_SMEM = 1024;  // window bytes before dynamic smem (u
 //
 // Cost-balanced ranges: each unit counts vx virtual tiles ahead of its tiles_per_unit
 // real ones (the fixed cost of one more item: the warps' merge, the partial's write,
-// the next unit's q), and every CTA takes tiles_per_cta tiles of that virtual sequence,
-// so a CTA whose range crosses into another unit gets fewer real tiles.  vx = 0 is an
-// equal split of the real tiles.
+// the next unit's q), and the sched_v virtual tiles are split over the sched_g CTAs in
+// proportion: CTA c takes [c * sched_v / sched_g, (c + 1) * sched_v / sched_g), rounded
+// down, so the ranges differ by at most one tile and a CTA whose range crosses into
+// another unit gets fewer real tiles.  vx = 0 is an equal split of the real tiles.
 struct Item {
   int unit, t0, t1, slot;  // tiles [t0, t1) of the unit; partial slot of this CTA
 };
@@ -42,17 +43,22 @@ __device__ __forceinline__ int real_tile(const P &p, int64_t v) {
 }
 template <typename P>
 __device__ __forceinline__ int cta_first_tile(const P &p, int cta) {
-  return min(real_tile(p, (int64_t)cta * p.tiles_per_cta), p.total_tiles);
+  return min(real_tile(p, (int64_t)cta * p.sched_v / p.sched_g), p.total_tiles);
+}
+// The CTA whose range holds virtual tile v: the largest c with c * sched_v / sched_g <= v.
+template <typename P>
+__device__ __forceinline__ int cta_of_vtile(const P &p, int64_t v) {
+  return (int)(((v + 1) * p.sched_g - 1) / p.sched_v);
 }
 // CTAs whose range meets unit u: unit_first_cta(u) .. + unit_n_split(u) - 1.
 template <typename P>
 __device__ __forceinline__ int unit_first_cta(const P &p, int u) {
-  return (int)(((int64_t)u * (p.vx + p.tiles_per_unit) + p.vx) / p.tiles_per_cta);
+  return cta_of_vtile(p, (int64_t)u * (p.vx + p.tiles_per_unit) + p.vx);
 }
 template <typename P>
 __device__ __forceinline__ int unit_n_split(const P &p, int u) {
   const int64_t v0 = (int64_t)u * (p.vx + p.tiles_per_unit) + p.vx;
-  return (int)((v0 + p.tiles_per_unit - 1) / p.tiles_per_cta - v0 / p.tiles_per_cta + 1);
+  return cta_of_vtile(p, v0 + p.tiles_per_unit - 1) - cta_of_vtile(p, v0) + 1;
 }
 
 template <typename P>
@@ -80,6 +86,18 @@ __device__ __forceinline__ int unit_len(const P &p, int unit) {
 template <int N>
 __device__ __forceinline__ void named_sync1() {
   asm volatile("bar.sync 1, %0;" ::"n"(N) : "memory");
+}
+
+// CTA-wide barrier 0 of N threads, split: the producer warp arrives without waiting, the
+// consumer warps wait for every thread (the producer's shared-memory writes before its
+// arrive are visible to them afterwards).
+template <int N>
+__device__ __forceinline__ void named_arrive0() {
+  asm volatile("bar.arrive 0, %0;" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void named_sync0() {
+  asm volatile("bar.sync 0, %0;" ::"n"(N) : "memory");
 }
 
 }  // namespace tq

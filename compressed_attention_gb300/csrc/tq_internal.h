@@ -148,8 +148,9 @@ struct DecodeShape {
   int n_hg;     // head groups per KV head
   int tiles_per_unit;  // key tiles of one (batch, KV head, head group) unit
   int total_tiles;     // over all units, laid end to end
-  int tiles_per_cta;   // contiguous range per persistent CTA, in virtual tiles: each
-                       // unit counts vx tiles of item cost ahead of its own
+  int vtotal;          // virtual tiles: each unit counts vx tiles of item cost ahead of its own
+  int tiles_per_cta;   // longest CTA range, in virtual tiles (CTA c takes virtual tiles
+                       // [c * vtotal / grid, (c + 1) * vtotal / grid), rounded down)
   int vx;
   int grid;            // persistent CTAs (at most one per SM)
   int n_part;          // partial slots per head
@@ -215,7 +216,7 @@ struct PrefillShape {
   int n_qt;            // query tiles per (batch, KV head)
   int tiles_per_unit;  // key tiles of one unit (all of L; tiles past a unit's last
                        // visible key cost no work)
-  int total_tiles, tiles_per_cta, grid, n_part;
+  int total_tiles, tiles_per_cta, grid, n_part;  // tiles_per_cta: the longest CTA range
   DecodeShape q;       // the B*T queries as a decode batch: q preparation and workspace
 };
 bool prefill_shape(const tq_ctx *k, int B, int T, int Hq, int Hkv, int L, PrefillShape *s);

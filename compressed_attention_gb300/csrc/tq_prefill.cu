@@ -90,7 +90,7 @@ struct PrefillParams {
   const uint8_t *vc;
   const int32_t *q_start;   // [B] position of each sequence's first chunk query
   int B, T, Hq, Hkv, L, gq, qpt, n_qt;
-  int tiles_per_unit, tiles_per_cta, vx, total_tiles, n_part;  // vx = 0: equal tile ranges
+  int tiles_per_unit, sched_g, sched_v, vx, total_tiles, n_part;  // vx = 0: equal tile ranges
   const uint32_t *qhl;      // prepared q: [B*T*Hq][256 words], hi then lo fp16
   const float *qsc;         // [B*T*Hq][2] power-of-two scales
   float *part;              // [B*T*Hq][n_part][PARTIAL_FLOATS]
@@ -599,10 +599,11 @@ bool prefill_shape(const tq_ctx *k, int B, int T, int Hq, int Hkv, int L, Prefil
   const int64_t total = units * s->tiles_per_unit;
   if (total > INT32_MAX || (int64_t)B * T * Hq > INT32_MAX / 256) return false;
   s->total_tiles = (int)total;
-  const int64_t tpc = (total + k->num_sms - 1) / k->num_sms;
-  s->tiles_per_cta = (int)(tpc < 1 ? 1 : tpc);
-  s->grid = (int)((total + s->tiles_per_cta - 1) / s->tiles_per_cta);
-  s->n_part = (s->tiles_per_unit + s->tiles_per_cta - 1) / s->tiles_per_cta + 1;
+  // the tiles split over one CTA per SM in proportion (ranges differ by at most one tile)
+  s->grid = (int)(total < k->num_sms ? total : k->num_sms);
+  const int shortest = (int)(total / s->grid);
+  s->tiles_per_cta = (int)((total + s->grid - 1) / s->grid);
+  s->n_part = (s->tiles_per_unit + shortest - 1) / shortest + 1;
   // the q preparation and the workspace see the B*T queries of Hq heads as a batch
   DecodeShape &d = s->q;
   d = DecodeShape{};
@@ -618,7 +619,7 @@ cudaError_t launch_prefill(const tq_ctx *k, const tq_ctx *v, const uint8_t *kc, 
   PrefillParams p{};
   p.kc = kc, p.vc = vc, p.q_start = q_start;
   p.B = s.B, p.T = s.T, p.Hq = s.Hq, p.Hkv = s.Hkv, p.L = s.L, p.gq = s.gq, p.qpt = s.qpt, p.n_qt = s.n_qt;
-  p.tiles_per_unit = s.tiles_per_unit, p.tiles_per_cta = s.tiles_per_cta, p.vx = 0;
+  p.tiles_per_unit = s.tiles_per_unit, p.sched_g = s.grid, p.sched_v = s.total_tiles, p.vx = 0;
   p.total_tiles = s.total_tiles, p.n_part = s.n_part;
   p.qhl = ws.qhl, p.qsc = ws.qsc, p.part = ws.partials;
   for (int i = 0; i < 2; ++i) {

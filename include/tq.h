@@ -199,9 +199,11 @@ tq_status tq_dequantize(const tq_ctx *ctx, const void *cache, int64_t n_rows, in
  * from its indices, online softmax runs split-K across SMs, values are
  * dequantized in registers, and the output is un-rotated once per head.
  *   k_ctx / v_ctx  contexts of the key and value caches.  Supported pairs:
- *                  (TURBO4, TURBO4), (TURBO3, TURBO4) -- the asymmetric 3-bit-key /
- *                  4-bit-value cache of [turbo4 post-mortem] section 9, each 32-element
- *                  key block scaled by its own stored norm -- and (PROD3, VGROUP2).
+ *                  (TURBO4, TURBO4); (TURBO3, TURBO4) -- the asymmetric 3-bit-key /
+ *                  4-bit-value cache of [turbo4 post-mortem] section 9; (TURBO3,
+ *                  TURBO3) -- the 3.5-bit cache of its section 1; (TURBO4, TURBO3);
+ *                  (PROD3, VGROUP2).  Every 32-element TURBO3 block, key or value, is
+ *                  scaled by its own stored norm.
  *   q              device [B][Hq][128] of q_dtype (F32, BF16 or F16), 16-byte aligned.
  *   k_cache/v_cache device [B][Hkv][L] packed rows.
  *   seq_lens       device int32[B] lengths in [1, L], or NULL for all L.
@@ -214,7 +216,7 @@ tq_status tq_dequantize(const tq_ctx *ctx, const void *cache, int64_t n_rows, in
  * Launches: the q preparation, the split-K kernel and, unless the split-K kernel
  * merges the splits itself (the CTA that completes a (batch, KV head, head group)
  * unit merges its partials, un-rotates and writes the unit's outputs; TURBO4 /
- * TURBO3 keys when each CTA completes few units), the combine kernel;
+ * TURBO3 keys and values when each CTA completes few units), the combine kernel;
  * tq_decode_num_launches tells which for a shape. */
 tq_status tq_decode_workspace_size(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, int Hq,
                                    int Hkv, int L, size_t *bytes);

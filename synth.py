@@ -19,6 +19,8 @@ Workloads (shapes and distributions of the pages' decode and write workloads):
 * ``long_context``: B=1, Hq=32, Hkv=8, L=131072; bf16 q, K, V N(0,1); seed 5.
 * ``gqa_t3k``: the ``gqa_lognormal`` recipe and seed unchanged (the same draws),
   for the asymmetric cache with 3-bit keys and 4-bit values.
+* ``gqa_t3``: the same draws again, for the symmetric turbo3 cache (3-bit keys
+  and values).
 * ``prefill_chunk``: B=1, Hq=32, Hkv=8, L=32768, T=512 chunk queries at positions
   L-T .. L-1 (the last chunk of a 32K-token prompt); K and V as ``gqa_lognormal``
   (lognormal channel scales with one outlier channel per KV head), bf16; q bf16
@@ -40,6 +42,8 @@ WORKLOADS = {
     "long_context": dict(B=1, Hq=32, Hkv=8, L=131072, q_dtype="bf16", kv_dtype="bf16", dist="normal", seed=5),
     # the gqa_lognormal recipe again, for the asymmetric 3-bit-key / 4-bit-value cache
     "gqa_t3k": dict(B=8, Hq=32, Hkv=8, L=32768, q_dtype="bf16", kv_dtype="bf16", dist="lognormal_outlier", seed=2),
+    # and for the symmetric 3.5-bit cache (turbo3 keys and values)
+    "gqa_t3": dict(B=8, Hq=32, Hkv=8, L=32768, q_dtype="bf16", kv_dtype="bf16", dist="lognormal_outlier", seed=2),
     # the last 512-token chunk of a 32K-token prompt: T chunk queries at positions L-T .. L-1
     "prefill_chunk": dict(B=1, Hq=32, Hkv=8, L=32768, T=512, q_dtype="bf16", kv_dtype="bf16",
                           dist="lognormal_outlier", seed=7),

@@ -36,8 +36,10 @@ def test_bench_configs_name_their_workloads():
         w = synth.WORKLOADS[name]
         c = bench.decode_config(name, w)
         assert c["workload"].startswith(f"{name}: B={w['B']} Hq={w['Hq']} Hkv={w['Hkv']} d=128 L={w['L']}")
-        assert c["k_format"] in ("turbo4", "turbo3", "prod3") and c["v_format"] in ("turbo4", "vgroup2")
-        assert "flushed" in c["l2"]
+        assert c["k_format"] in ("turbo4", "turbo3", "prod3") and c["v_format"] in ("turbo4", "turbo3", "vgroup2")
+        # inputs larger than twice the L2 run back to back, the others flush before each step
+        big = w["B"] * w["Hkv"] * w["L"] * bench.decode_unit_bytes(bench.DECODE[name]) > 2 * bench.L2_NOMINAL
+        assert ("back to back" in c["l2"]) == big and ("flushed" in c["l2"]) != big
     d = bench.decode_config("gqa_lognormal", synth.WORKLOADS["gqa_lognormal"])
     assert (d["B"], d["Hq"], d["Hkv"], d["L"], d["rotation"]) == (8, 32, 8, 32768, "dense")
     p = bench.prefill_config()

@@ -114,6 +114,58 @@ def test_decode_turbo3_keys_turbo4_values_parity(rot, case):
     assert tq.tq_ctx_device_status(kctx) == 0
 
 
+@pytest.mark.parametrize("kfmt", ["turbo3", "turbo4"])
+@pytest.mark.parametrize("rot", ["wht", "dense"])
+@pytest.mark.parametrize("case", CASES)
+def test_decode_turbo3_values_parity(kfmt, rot, case):
+    """turbo3 values (3.5-bit, the 2+1 layout) with turbo3 keys (the symmetric turbo3 cache)
+    or turbo4 keys."""
+    tq = lib()
+    B, Hq, Hkv, L, lens = case
+    kcodec = Codec(kfmt, rotation=rot, rot_seed=33)
+    vcodec = Codec("turbo3", rotation=rot, rot_seed=34)
+    kb = oracle_cache(kcodec, B, Hkv, L, 31, scale=2.0, dist="lognormal")
+    vb = oracle_cache(vcodec, B, Hkv, L, 32)
+    q_t, q32 = torch_rows(np.random.default_rng(33).standard_normal((B, Hq, 128)).astype(np.float32), "bf16")
+    kctx, vctx = tq.Ctx(kfmt, rot, 33), tq.Ctx("turbo3", rot, 34)
+    out, sc = run_decode(tq, kctx, vctx, q_t, upload_cache(tq, kfmt, kb), upload_cache(tq, "turbo3", vb),
+                         B, Hq, Hkv, L, lens)
+    ref, s_ref = reference(q32, kcodec, kb, vcodec, vb, lens)
+    check_outputs(out, ref)
+    m = ~np.isnan(s_ref)
+    assert np.array_equal(m, ~np.isnan(sc)), "scores written for the wrong keys"
+    assert np.max(np.abs(sc[m] - s_ref[m])) <= ATOL
+    assert tq.tq_ctx_device_status(kctx) == 0
+
+
+def test_decode_turbo3_values_own_block_norms():
+    """Every 32-element value block is scaled by its own stored norm: blocks whose norms
+    differ by up to 4x (and some set to zero) decode as the oracle's per-block
+    dequantization says, with peaked attention (queries 2x) so few keys dominate; staged
+    calls and 8 q-heads per KV head too."""
+    tq = lib()
+    B, Hq, Hkv, L = 2, 16, 2, 531
+    kcodec = Codec("turbo3", rotation="wht", rot_seed=41)
+    vcodec = Codec("turbo3", rotation="wht", rot_seed=42)
+    kb = oracle_cache(kcodec, B, Hkv, L, 41)
+    vb = oracle_cache(vcodec, B, Hkv, L, 42).copy()
+    rng = np.random.default_rng(43)
+    for c in range(4):
+        n = vb[..., 14 * c:14 * c + 2].copy().view("<f2").astype(np.float32)
+        f = rng.uniform(0.5, 2.0, size=n.shape).astype(np.float32)
+        f[rng.random(n.shape) < 0.02] = 0.0
+        vb[..., 14 * c:14 * c + 2] = (n * f).astype("<f2").view(np.uint8)
+    q_t, q32 = torch_rows(rng.standard_normal((B, Hq, 128)).astype(np.float32) * 2.0, "f32")
+    kctx, vctx = tq.Ctx("turbo3", "wht", 41), tq.Ctx("turbo3", "wht", 42)
+    kc, vc = upload_cache(tq, "turbo3", kb), upload_cache(tq, "turbo3", vb)
+    ref, s_ref = reference(q32, kcodec, kb, vcodec, vb, None)
+    for staged in (False, True):
+        out, sc = run_decode(tq, kctx, vctx, q_t, kc, vc, B, Hq, Hkv, L, staged=staged)
+        check_outputs(out, ref)
+        assert np.max(np.abs(sc - s_ref)) <= ATOL
+    assert tq.tq_ctx_device_status(kctx) == 0
+
+
 def test_decode_turbo3_keys_own_block_norms():
     """Every 32-element key block is scaled by its own stored norm: blocks whose norms
     differ (set here to other fp16 values, including zero) decode as the oracle's
@@ -244,8 +296,8 @@ def test_decode_rejects_bad_arguments():
     with pytest.raises(tq.TQError) as e:
         tq.tq_decode_workspace_size(ctx, ctx, 1, 5, 2, 64)  # Hq not a multiple of Hkv
     assert e.value.status == tq.TQ_ERR_INVALID_ARG
-    t3 = tq.Ctx("turbo3", "wht", 0)
-    for kc_, vc_ in ((t3, t3), (ctx, t3)):  # turbo3 values have no decode kernel
+    t3, vg = tq.Ctx("turbo3", "wht", 0), tq.Ctx("vgroup2")
+    for kc_, vc_ in ((t3, vg), (ctx, vg), (vg, ctx)):  # pairs without a decode kernel
         with pytest.raises(tq.TQError) as e:
             tq.tq_decode_workspace_size(kc_, vc_, 1, 4, 1, 64)
         assert e.value.status == tq.TQ_ERR_UNSUPPORTED
@@ -262,15 +314,15 @@ def _units(cfg, tensor, workers=16):
                 yield b, h, bits
 
 
-def _full_size(name, rot, rot_seed, sample_heads, k_fmt="turbo4", **override):
+def _full_size(name, rot, rot_seed, sample_heads, k_fmt="turbo4", v_fmt="turbo4", **override):
     """Write the whole cache with the GPU write path, decode in the benchmark's launch
     configuration, and compare sampled (b, h) outputs with the oracle on that head's inputs."""
     import torch
     tq = lib()
     cfg = dict(synth.WORKLOADS[name], **override)
     B, Hq, Hkv, L = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["L"]
-    kctx, vctx = tq.Ctx(k_fmt, rot, rot_seed), tq.Ctx("turbo4", rot, rot_seed + 100)
-    kc, vc = tq.alloc_cache(k_fmt, B * Hkv * L), tq.alloc_cache("turbo4", B * Hkv * L)
+    kctx, vctx = tq.Ctx(k_fmt, rot, rot_seed), tq.Ctx(v_fmt, rot, rot_seed + 100)
+    kc, vc = tq.alloc_cache(k_fmt, B * Hkv * L), tq.alloc_cache(v_fmt, B * Hkv * L)
     for tensor, ctx, cache in (("K", kctx, kc), ("V", vctx, vc)):
         for b, h, bits in _units(cfg, tensor):
             src = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
@@ -281,7 +333,7 @@ def _full_size(name, rot, rot_seed, sample_heads, k_fmt="turbo4", **override):
     out, _ = run_decode(tq, kctx, vctx, q_t, kc, vc, B, Hq, Hkv, L, scores=False)
     assert tq.tq_ctx_device_status(kctx) == 0
     kcod = Codec(k_fmt, rotation=rot, rot_seed=rot_seed)
-    vcod = Codec("turbo4", rotation=rot, rot_seed=rot_seed + 100)
+    vcod = Codec(v_fmt, rotation=rot, rot_seed=rot_seed + 100)
     for (b, h) in sample_heads:
         kv = oracle.gqa_kv_head(h, Hq, Hkv)
         xk, _ = synth.kv_unit(cfg, "K", b, kv)
@@ -304,6 +356,10 @@ def test_full_size_long_context_batch16_wht():
     """The largest point of the context sweep: B = 16 sequences of 131,072 keys (2.28 GB of
     packed K and V), sampled heads of the first, a middle and the last sequence."""
     _full_size("long_context", "wht", 5, [(0, 0), (7, 9), (15, 31)], B=16)
+
+
+def test_full_size_gqa_turbo3_keys_and_values():
+    _full_size("gqa_t3", "dense", 8, [(0, 0), (5, 18), (7, 31)], k_fmt="turbo3", v_fmt="turbo3")
 
 
 def test_full_size_gqa_turbo3_keys():

@@ -55,6 +55,8 @@ STEP_CASES = [
     ("turbo4", "turbo4", "dense", "bf16", 4, 32, 8, 1000, True),
     ("turbo4", "turbo4", "dense", "f32", 3, 12, 2, 300, True),
     ("turbo3", "turbo4", "dense", "bf16", 2, 16, 4, 700, True),
+    ("turbo3", "turbo3", "dense", "bf16", 2, 16, 4, 700, True),
+    ("turbo4", "turbo3", "wht", "f32", 2, 8, 2, 300, False),
     ("turbo4", "turbo4", "dense", "bf16", 32, 64, 8, 64, True),    # 256 rows, the most the front takes
     ("turbo4", "turbo4", "dense", "bf16", 33, 64, 8, 64, False),   # 264 rows
     ("turbo4", "turbo4", "wht", "bf16", 2, 8, 2, 500, False),
@@ -103,7 +105,7 @@ def test_decode_step_matches_separate_calls(case):
     kb0 = to_host_bytes(k0, n_cache, kctx.row_bytes)
     assert np.any(kb[slots.cpu().numpy()] != kb0[slots.cpu().numpy()])
 
-    if kf in ("turbo4", "turbo3") and vf == "turbo4":
+    if kf in ("turbo4", "turbo3") and vf in ("turbo4", "turbo3"):
         vb = to_host_bytes(vc_b, n_cache, vctx.row_bytes)
         kh = _codec(kf, rot, 21).dequantize(kb).reshape(B, Hkv, L, 128)
         vh = _codec(vf, rot, 22).dequantize(vb).reshape(B, Hkv, L, 128)

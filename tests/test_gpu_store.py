@@ -41,7 +41,7 @@ def check_store(tq, st, kcod, vcod, kx, vx, n, R, q32, q_t, Hq, fmt_k="turbo4"):
     L = st.L
     rb = {"turbo4": 68, "turbo3": 56, "prod3": 56}[fmt_k]
     kbytes = st.cache_bytes("k").cpu().numpy()[: B * Hkv * L * rb].reshape(B, Hkv, L, rb)
-    vrb = 48 if vcod.fmt == "vgroup2" else 68
+    vrb = {"vgroup2": 48, "turbo3": 56}.get(vcod.fmt, 68)
     vbytes = st.cache_bytes("v").cpu().numpy()[: B * Hkv * L * vrb].reshape(B, Hkv, L, vrb)
     if flushed:
         ref_k, _ = kcod.encode(kx[:, :, :flushed].reshape(-1, 128))
@@ -98,6 +98,27 @@ def test_store_chunked_appends_cross_several_flushes():
         st.append(kd[:, :, t:t + c].contiguous(), vd[:, :, t:t + c].contiguous())
         t += c
         check_store(tq, st, kcod, vcod, kx, vx, t, R, q32, q_t, Hq, fmt_k="turbo3")
+
+
+def test_store_symmetric_turbo3():
+    """turbo3 keys and turbo3 values (the 3.5-bit cache of the post-mortem's section 1)."""
+    tq = lib()
+    B, Hkv, Hq, L, R = 2, 2, 8, 300, 32
+    kcod, vcod = Codec("turbo3", rotation="wht", rot_seed=91), Codec("turbo3", rotation="wht", rot_seed=92)
+    kctx, vctx = tq.Ctx("turbo3", "wht", 91), tq.Ctx("turbo3", "wht", 92)
+    chunks = [20, 50, 3, 40]
+    N = sum(chunks)
+    kx, kb = tokens(B, Hkv, N, 91, scale=2.0)
+    vx, vb = tokens(B, Hkv, N, 92)
+    q_t, q32 = torch_rows(np.random.default_rng(93).standard_normal((B, Hq, 128)).astype(np.float32), "bf16")
+    st = tq.Store(kctx, vctx, B, Hkv, L, R)
+    kd, vd = to_dev(kb), to_dev(vb)
+    t = 0
+    for c in chunks:
+        st.append(kd[:, :, t:t + c].contiguous(), vd[:, :, t:t + c].contiguous())
+        t += c
+        check_store(tq, st, kcod, vcod, kx, vx, t, R, q32, q_t, Hq, fmt_k="turbo3")
+    assert tq.tq_ctx_device_status(kctx) == 0 and tq.tq_ctx_device_status(vctx) == 0
 
 
 def test_store_prod3_keys_group_values():
