@@ -69,7 +69,9 @@ from .formats import (  # noqa: F401
     canonical_norm_fp32,
     encode_turbo,
     pack_turbo4,
+    pack_turbo4_rows,
     unpack_turbo4,
+    unpack_turbo4_rows,
     pack_turbo3,
     unpack_turbo3,
     encode_prod,

@@ -110,7 +110,8 @@ def attention_compressed_domain(q, k_codec, k_blocks, v_codec, v_blocks, seq_len
     """Compressed-domain decode (fp64): rotate q once, score from indices, online softmax.
 
     q: [B, Hq, d]; k_blocks / v_blocks: packed rows [B, Hkv, L, row_bytes].
-    Supported pairs: keys turbo4 or prod3, values turbo4 or vgroup2.
+    Supported pairs: keys turbo4, turbo3 or prod3, values turbo4, turbo3 or vgroup2
+    (turbo3 blocks and the blocks of d = 256 turbo4 rows carry per-block norms).
     Returns (out [B, Hq, d], scores [B, Hq, L]).
     """
     q = np.asarray(q, dtype=np.float64)
@@ -126,7 +127,9 @@ def attention_compressed_domain(q, k_codec, k_blocks, v_codec, v_blocks, seq_len
         for kv in range(Hkv):
             kf = k_codec.fields(k_blocks[b, kv, :Lb])
             vf = v_codec.fields(v_blocks[b, kv, :Lb])
-            if v_codec.fmt == "turbo4":
+            if "n_elem" in vf:  # per-block norms
+                vals = vf["y_hat"] * vf["n_elem"]  # rotated basis
+            elif v_codec.fmt == "turbo4":
                 vals = vf["y_hat"] * vf["n"][:, None]  # rotated basis
             else:
                 vals = vf["v_hat"]
@@ -134,7 +137,10 @@ def attention_compressed_domain(q, k_codec, k_blocks, v_codec, v_blocks, seq_len
                 if gqa_kv_head(h, Hq, Hkv) != kv:
                     continue
                 q_rot = k_codec.rot.forward(q[b, h][None, :])[0]  # trick 1: once per query
-                s = kf["n"] * (kf["y_hat"] @ q_rot)
+                if "n_elem" in kf:  # per-block norms
+                    s = (kf["y_hat"] * kf["n_elem"]) @ q_rot
+                else:
+                    s = kf["n"] * (kf["y_hat"] @ q_rot)
                 if k_codec.fmt == "prod3":
                     q_sk = k_codec.S32.astype(np.float64) @ q[b, h]  # trick 2: once per query
                     s = s + kf["n"] * kf["gamma"] * k_codec.qjl_factor * (QJL_SCALE_NUM / d) * (kf["sigma"] @ q_sk)
@@ -143,7 +149,7 @@ def attention_compressed_domain(q, k_codec, k_blocks, v_codec, v_blocks, seq_len
                 parts = [_chunk_partial(s[a:e], vals[a:e]) for a, e in zip(bounds[:-1], bounds[1:]) if e > a]
                 _, l_star, acc = online_softmax_merge(parts)
                 o = acc / l_star
-                if v_codec.fmt == "turbo4":
+                if v_codec.fmt in ("turbo4", "turbo3"):
                     o = v_codec.rot.inverse(o[None, :])[0]  # un-rotate once
                 out[b, h] = o
                 scores[b, h, :Lb] = s

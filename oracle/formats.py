@@ -55,15 +55,21 @@ QJL_SHRINK = 2.0 / math.pi  # optional factor on the QJL term ([turbo4 post-mort
 
 
 def canonical_norm_fp32(x):
-    """The canonical fp32 norm of each row of x ([N, 128]); see the module docstring."""
+    """The canonical fp32 norm of each row of x ([N, d], d = 128 or 256); see the module
+    docstring.  Lane l of 32 holds elements (d/32) l .. (d/32) l + d/32 - 1, whose squares
+    it sums as a balanced pairwise tree (adjacent pairs first); d = 128 gives
+    p_l = (x_4l^2 + x_4l+1^2) + (x_4l+2^2 + x_4l+3^2)."""
     x32 = np.asarray(x, dtype=np.float32)
-    if x32.shape[-1] != 128:
-        raise ValueError("the canonical norm tree is defined for d = 128")
+    d = x32.shape[-1]
+    if d not in (128, 256):
+        raise ValueError("the canonical norm tree is defined for d = 128 and 256")
     # rows whose squares or sums exceed the fp32 range give n = inf, as fp32 arithmetic
     # defines (the extreme-magnitude test rows do this on purpose)
     with np.errstate(over="ignore"):
-        sq = x32 * x32
-        p = (sq[:, 0::4] + sq[:, 1::4]) + (sq[:, 2::4] + sq[:, 3::4])  # [N, 32], one per lane
+        p = (x32 * x32).reshape(-1, 32, d // 32)
+        while p.shape[-1] > 1:
+            p = p[..., 0::2] + p[..., 1::2]
+        p = p[..., 0]  # [N, 32], one per lane
         lanes = np.arange(32)
         for h in (16, 8, 4, 2, 1):
             p = p + p[:, lanes ^ h]
@@ -162,6 +168,21 @@ def unpack_turbo4(blocks):
     j = np.arange(128)
     idx = (blocks[:, 4 + j // 2] >> ((j % 2) * 4)) & 0xF
     return n.astype(np.float32), idx.astype(np.uint8)
+
+
+def pack_turbo4_rows(n32, idx):
+    """A d-element turbo4 row as d/128 consecutive 68-byte blocks: block c holds elements
+    128c .. 128c+127 and the row's norm (repeated in every block, as turbo3 repeats it)."""
+    idx = np.asarray(idx, dtype=np.uint8)
+    return np.concatenate([pack_turbo4(n32, idx[:, 128 * c:128 * c + 128]) for c in range(idx.shape[1] // 128)],
+                          axis=1)
+
+
+def unpack_turbo4_rows(rows, d):
+    """Per-block norms [N, d/128] and indices [N, d] of d-element turbo4 rows."""
+    rows = np.asarray(rows, dtype=np.uint8)
+    parts = [unpack_turbo4(rows[:, 68 * c:68 * c + 68]) for c in range(d // 128)]
+    return np.stack([n for n, _ in parts], axis=1), np.concatenate([i for _, i in parts], axis=1)
 
 
 def pack_turbo3(n32, idx):
@@ -342,11 +363,11 @@ class Codec:
     """
 
     def __init__(self, fmt, d=128, rotation="wht", rot_seed=0, qjl_seed=None, codebook=None, qjl_shrink=False):
-        if d != 128:
-            raise ValueError("only d = 128 is defined")
+        if d != 128 and not (d == 256 and fmt == "turbo4"):
+            raise ValueError("d = 128 for every format; d = 256 for turbo4")
         self.fmt = fmt
         self.d = d
-        self.row_bytes = ROW_BYTES[fmt]
+        self.row_bytes = ROW_BYTES[fmt] * d // 128
         self.rot = None
         if fmt in CODE_BITS:
             self.rot = _rotation(rotation, rot_seed, d)
@@ -365,7 +386,7 @@ class Codec:
         x = np.asarray(x, dtype=np.float32)
         if self.fmt == "turbo4":
             n, idx, y = encode_turbo(x, self.rot, self.b32)
-            return pack_turbo4(n, idx), {"n": n, "idx": idx, "y": y}
+            return pack_turbo4_rows(n, idx), {"n": n, "idx": idx, "y": y}
         if self.fmt == "turbo3":
             n, idx, y = encode_turbo(x, self.rot, self.b32)
             return pack_turbo3(n, idx), {"n": n, "idx": idx, "y": y}
@@ -382,9 +403,12 @@ class Codec:
         """Decoded fields in fp64: per-row scalars and per-element rotated-basis values."""
         blocks = np.asarray(blocks, dtype=np.uint8).reshape(-1, self.row_bytes)
         c = self.c32.astype(np.float64) if self.fmt in CODE_BITS else None
-        if self.fmt == "turbo4":
+        if self.fmt == "turbo4" and self.d == 128:
             n, idx = unpack_turbo4(blocks)
             return {"n": n.astype(np.float64), "y_hat": c[idx]}
+        if self.fmt == "turbo4":  # d/128 blocks, each scaled by its own stored norm
+            norms, idx = unpack_turbo4_rows(blocks, self.d)
+            return {"n_elem": np.repeat(norms.astype(np.float64), 128, axis=1), "y_hat": c[idx]}
         if self.fmt == "turbo3":
             norms, idx = unpack_turbo3(blocks)
             n_elem = np.repeat(norms.astype(np.float64), 32, axis=1)
@@ -408,8 +432,11 @@ class Codec:
         return the rotated-basis values n * c[idx] (prod3 ignores it).
         """
         f = self.fields(blocks)
-        if self.fmt == "turbo4":
+        if self.fmt == "turbo4" and self.d == 128:
             y = f["y_hat"] * f["n"][:, None]
+            return self.rot.inverse(y) if unrotate else y
+        if self.fmt == "turbo4":
+            y = f["y_hat"] * f["n_elem"]
             return self.rot.inverse(y) if unrotate else y
         if self.fmt == "turbo3":
             y = f["y_hat"] * f["n_elem"]
