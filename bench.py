@@ -14,6 +14,7 @@ roofline.
 --workload picks another workload of the same path:
   gqa_t3k       the gqa_lognormal inputs with turbo3 keys and turbo4 values
   gqa_t3        the gqa_lognormal inputs with turbo3 keys and turbo3 values
+  gqa_d256      head dimension 256: B=4, Hq=32, Hkv=8, L=32,768, turbo4 K and V, dense
   prefill_chunk causal attention of the last 512-token chunk of a 32K-token prompt
                 (B=1, Hq=32, Hkv=8) over the turbo4 cache, tensor cores; TFLOP/s
   long_context  B=1, Hq=32, Hkv=8, L=131,072, turbo4 K and V, randomized WHT
@@ -78,6 +79,8 @@ DECODE = {
                     kernel="k_partial_t4", source="tq_decode.cu"),
     "gqa_t3": dict(k_fmt="turbo3", v_fmt="turbo3", rotation="dense", k_seed=8, v_seed=108, qjl_seed=0,
                    kernel="k_partial_t4", source="tq_decode.cu"),
+    "gqa_d256": dict(k_fmt="turbo4", v_fmt="turbo4", rotation="dense", k_seed=9, v_seed=109, qjl_seed=0,
+                     kernel="k_partial_d256", source="tq_d256.cu", d=256),
 }
 WRITE_KERNEL = {"dense": ("k_write_dense_tc", "tq_write_tc.cu"), "wht": ("k_write_wht", "tq_write.cu")}
 PREFILL = {"prefill_chunk": dict(fmt="turbo4", rotation="dense", k_seed=7, v_seed=107,
@@ -200,7 +203,7 @@ def decode_codecs(spec):
     def make(fmt, seed):
         if fmt == "vgroup2":
             return Codec("vgroup2")
-        return Codec(fmt, rotation=spec["rotation"], rot_seed=seed, qjl_seed=spec["qjl_seed"])
+        return Codec(fmt, d=spec.get("d", 128), rotation=spec["rotation"], rot_seed=seed, qjl_seed=spec["qjl_seed"])
     return make(spec["k_fmt"], spec["k_seed"]), make(spec["v_fmt"], spec["v_seed"])
 
 
@@ -220,7 +223,7 @@ def decode_queries(name, cfg):
 
 
 def decode_unit_bytes(spec):
-    return ROW_BYTES[spec["k_fmt"]] + ROW_BYTES[spec["v_fmt"]]
+    return (ROW_BYTES[spec["k_fmt"]] + ROW_BYTES[spec["v_fmt"]]) * spec.get("d", 128) // 128
 
 
 class OracleDecode:
@@ -252,7 +255,7 @@ def cpu_fp32_loop(leg, min_seconds=3.0):
     score from indices, online softmax, one un-rotation) over the oracle's encoded units,
     on one host core and on every host core (OpenMP over units).  turbo4 keys and values
     only; None for other formats or without a C compiler."""
-    if leg.spec["k_fmt"] != "turbo4" or leg.spec["v_fmt"] != "turbo4":
+    if leg.spec["k_fmt"] != "turbo4" or leg.spec["v_fmt"] != "turbo4" or leg.spec.get("d", 128) != 128:
         return None
     from oracle import build_cpu_baseline
     f = build_cpu_baseline.load()
@@ -431,8 +434,9 @@ def decode_back_to_back(name, cfg, l2=L2_NOMINAL):
 
 def decode_config(name, cfg, l2=L2_NOMINAL):
     spec = DECODE[name]
-    return {"workload": f"{name}: B={cfg['B']} Hq={cfg['Hq']} Hkv={cfg['Hkv']} d=128 L={cfg['L']}",
-            "B": cfg["B"], "Hq": cfg["Hq"], "Hkv": cfg["Hkv"], "L": cfg["L"], "d": 128,
+    d = spec.get("d", 128)
+    return {"workload": f"{name}: B={cfg['B']} Hq={cfg['Hq']} Hkv={cfg['Hkv']} d={d} L={cfg['L']}",
+            "B": cfg["B"], "Hq": cfg["Hq"], "Hkv": cfg["Hkv"], "L": cfg["L"], "d": d,
             "k_format": spec["k_fmt"], "v_format": spec["v_fmt"], "rotation": spec["rotation"],
             "q_dtype": cfg["q_dtype"], "l2": L2_B2B_NOTE if decode_back_to_back(name, cfg, l2) else L2_NOTE}
 
@@ -458,7 +462,7 @@ def write_config(args):
 def make_ctx(tq, fmt, spec, seed):
     if fmt == "vgroup2":
         return tq.Ctx("vgroup2")
-    return tq.Ctx(fmt, spec["rotation"], seed, spec["qjl_seed"])
+    return tq.Ctx(fmt, spec["rotation"], seed, spec["qjl_seed"], d=spec.get("d", 128))
 
 
 def to_device_rows(torch, x32, bits, device):
@@ -485,24 +489,25 @@ def build_decode(name, cfg, tq, torch, device):
     B, Hq, Hkv, L = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["L"]
     kctx = make_ctx(tq, spec["k_fmt"], spec, spec["k_seed"])
     vctx = make_ctx(tq, spec["v_fmt"], spec, spec["v_seed"])
-    kc = tq.alloc_cache(spec["k_fmt"], B * Hkv * L, device)
-    vc = tq.alloc_cache(spec["v_fmt"], B * Hkv * L, device)
+    d = spec.get("d", 128)
+    kc = tq.alloc_cache(spec["k_fmt"], B * Hkv * L, device, d=d)
+    vc = tq.alloc_cache(spec["v_fmt"], B * Hkv * L, device, d=d)
     for tensor, ctx, cache in (("K", kctx, kc), ("V", vctx, vc)):
         for b, h, x32, bits in generated_units(name, cfg, tensor):
             src = to_device_rows(torch, x32, bits, device)
             rows = torch.arange((b * Hkv + h) * L, (b * Hkv + h + 1) * L, dtype=torch.int64, device=device)
             tq.tq_quantize_set_rows(ctx, src, cache, row_ids=rows)
     q32, qbits = decode_queries(name, cfg)
-    q = to_device_rows(torch, q32, qbits, device).reshape(B, Hq, 128)
+    q = to_device_rows(torch, q32, qbits, device).reshape(B, Hq, d)
     # the step's new token: one K and one V row per (b, KV head), written to slot L-1
     rng = np.random.default_rng([cfg["seed"], 99])
     new = []
     for _ in range(2):
-        x = rng.standard_normal((B * Hkv, 128), dtype=np.float32)
+        x = rng.standard_normal((B * Hkv, d), dtype=np.float32)
         new.append(to_device_rows(torch, x, synth.bf16_bits(x) if cfg["kv_dtype"] == "bf16" else None, device))
     slots = torch.tensor([(u + 1) * L - 1 for u in range(B * Hkv)], dtype=torch.int64, device=device)
     ws = tq.alloc_workspace(tq.tq_decode_workspace_size(kctx, vctx, B, Hq, Hkv, L), device)
-    out = torch.empty((B, Hq, 128), dtype=torch.float32, device=device)
+    out = torch.empty((B, Hq, d), dtype=torch.float32, device=device)
     torch.cuda.synchronize()
     return dict(kctx=kctx, vctx=vctx, kc=kc, vc=vc, q=q, new_k=new[0], new_v=new[1], slots=slots, ws=ws, out=out)
 
@@ -706,7 +711,7 @@ def run_decode(args, rank, world, dist):
         raise RuntimeError(f"device status {status} after the benchmark")
 
     kv_bytes = B * Hkv * L * decode_unit_bytes(spec)
-    alg_bytes = kv_bytes + w["q"].numel() * w["q"].element_size() + B * Hq * 128 * 4
+    alg_bytes = kv_bytes + w["q"].numel() * w["q"].element_size() + w["out"].numel() * 4
     ms_per_step = total_ms / args.steps
     value = job_rate(alg_bytes, world, ms_per_step) / 1e9
     peak, peak_kind = measured_peak()

@@ -191,7 +191,9 @@ class Ctx:
         h = _vp()
         _check(lib.tq_ctx_create(ctypes.byref(p), ctypes.byref(h)), "tq_ctx_create")
         self.handle = h.value
-        self.row_bytes = tq_row_bytes(fmt)
+        self.d = d
+        # a row of head dimension 256 is two 128-element turbo4 blocks
+        self.row_bytes = tq_row_bytes(fmt) * d // D
 
     def close(self):
         if getattr(self, "handle", None):
@@ -222,7 +224,7 @@ def tq_ctx_device_status(ctx, clear=True):
 # --------------------------------------------------------------------------- write / read
 
 def tq_quantize_set_rows(ctx, src, dst_cache, row_ids=None, n_rows=None, stream=None):
-    """Quantize rows of ``src`` ([n, 128] fp32/bf16 CUDA tensor) into ``dst_cache`` (uint8 CUDA
+    """Quantize rows of ``src`` ([n, d] fp32/bf16 CUDA tensor) into ``dst_cache`` (uint8 CUDA
     tensor of packed rows) at slots ``row_ids`` (int64 CUDA tensor) or 0..n-1."""
     n = src.shape[0] if n_rows is None else n_rows
     stride = src.stride(0) if src.dim() == 2 else D
@@ -441,7 +443,8 @@ def alloc_workspace(nbytes, device="cuda"):
     return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
 
 
-def alloc_cache(fmt, n_rows, device="cuda"):
-    """A uint8 CUDA tensor sized by tq_cache_bytes (readable to the next 16-byte boundary)."""
+def alloc_cache(fmt, n_rows, device="cuda", d=D):
+    """A uint8 CUDA tensor sized by tq_cache_bytes (readable to the next 16-byte boundary);
+    rows of head dimension 256 take two 128-element blocks each."""
     import torch
-    return torch.zeros(tq_cache_bytes(fmt, n_rows), dtype=torch.uint8, device=device)
+    return torch.zeros(tq_cache_bytes(fmt, n_rows * d // D), dtype=torch.uint8, device=device)

@@ -22,7 +22,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "lib", "libtq.so")
 
-SOURCES = ["tq_host.cu", "tq_api.cu", "tq_write.cu", "tq_decode.cu", "tq_dequant.cu", "tq_static_ws.cu", "tq_decode_pv.cu", "tq_write_tc.cu", "tq_prefill.cu", "tq_store.cu"]
+SOURCES = ["tq_host.cu", "tq_api.cu", "tq_write.cu", "tq_decode.cu", "tq_dequant.cu", "tq_static_ws.cu", "tq_decode_pv.cu", "tq_write_tc.cu", "tq_prefill.cu", "tq_store.cu", "tq_d256.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE, "-I", CSRC]

@@ -39,29 +39,30 @@ int code_bits(int fmt) {
   }
 }
 
-tq_status build_rotation(int kind, uint64_t seed, std::vector<float> &r, uint32_t *neg) {
-  r.assign((size_t)D * D, 0.f);
+// The d x d rotation R (row-major fp32) and, for the WHT, its sign bits (d / 32 words).
+tq_status build_rotation(int kind, int d, uint64_t seed, std::vector<float> &r, uint32_t *neg) {
+  r.assign((size_t)d * d, 0.f);
   if (kind == TQ_ROT_DENSE) {
-    std::vector<double> pi((size_t)D * D);
-    if (!dense_rotation_f64(seed, D, pi.data())) return fail(TQ_ERR_INVALID_ARG, "rank-deficient Gaussian");
+    std::vector<double> pi((size_t)d * d);
+    if (!dense_rotation_f64(seed, d, pi.data())) return fail(TQ_ERR_INVALID_ARG, "rank-deficient Gaussian");
     for (size_t i = 0; i < pi.size(); ++i) r[i] = (float)pi[i];
     return TQ_OK;
   }
-  uint64_t out[D];
-  splitmix64_fill(seed, out, D);
-  for (int i = 0; i < 4; ++i) neg[i] = 0;
-  double s[D];
-  for (int j = 0; j < D; ++j) {
+  std::vector<uint64_t> out(d);
+  splitmix64_fill(seed, out.data(), d);
+  for (int i = 0; i < d / 32; ++i) neg[i] = 0;
+  std::vector<double> s(d);
+  for (int j = 0; j < d; ++j) {
     const bool minus = (out[j] >> 63) != 0;
     s[j] = minus ? -1.0 : 1.0;
     if (minus) neg[j / 32] |= 1u << (j % 32);
   }
   // R = (1/sqrt(d)) H D with H the Sylvester Hadamard matrix, H[i][j] = (-1)^popcount(i & j).
-  const double inv = 1.0 / std::sqrt((double)D);
-  for (int i = 0; i < D; ++i)
-    for (int j = 0; j < D; ++j) {
+  const double inv = 1.0 / std::sqrt((double)d);
+  for (int i = 0; i < d; ++i)
+    for (int j = 0; j < d; ++j) {
       const double h = (__builtin_popcount(i & j) & 1) ? -1.0 : 1.0;
-      r[(size_t)i * D + j] = (float)(h * s[j] * inv);
+      r[(size_t)i * d + j] = (float)(h * s[j] * inv);
     }
   return TQ_OK;
 }
@@ -87,6 +88,60 @@ tq_status check_decode_common(const tq_ctx *k, const tq_ctx *v, int B, int Hq, i
   if (!decode_pair_supported(k, v))
     return fail(TQ_ERR_UNSUPPORTED, "no decode kernel for this (key, value) format pair");
   if (!decode_shape(k, v, B, Hq, Hkv, L, shape)) return fail(TQ_ERR_UNSUPPORTED, "shape too large");
+  return TQ_OK;
+}
+
+// Head dimension 256: turbo4 keys and values only, through the kernels of tq_d256.cu.
+bool is_d256(const tq_ctx *k, const tq_ctx *v) { return (k && k->d == D256) || (v && v->d == D256); }
+
+tq_status check_d256(const tq_ctx *k, const tq_ctx *v, int B, int Hq, int Hkv, int L, D256Shape *s) {
+  if (!k || !v) return fail(TQ_ERR_INVALID_ARG, "null context");
+  if (k->device != v->device) return fail(TQ_ERR_INVALID_ARG, "the key and value contexts belong to different devices");
+  tq_status st = check_current_device(k->device, "decode");
+  if (st != TQ_OK) return st;
+  if (k->d != D256 || v->d != D256 || k->fmt != TQ_FMT_TURBO4 || v->fmt != TQ_FMT_TURBO4)
+    return fail(TQ_ERR_UNSUPPORTED, "at head dimension 256 both contexts must be TURBO4 with d = 256");
+  if (B < 1 || Hq < 1 || Hkv < 1 || L < 1) return fail(TQ_ERR_INVALID_ARG, "B, Hq, Hkv and L must be >= 1");
+  if (Hq % Hkv != 0) return fail(TQ_ERR_INVALID_ARG, "Hq must be a multiple of Hkv");
+  if (!d256_shape(k, B, Hq, Hkv, L, s)) return fail(TQ_ERR_UNSUPPORTED, "shape too large");
+  return TQ_OK;
+}
+
+tq_status check_workspace256(const D256Shape &s, void *ws, size_t bytes, Workspace *w) {
+  if (!ws) return fail(TQ_ERR_INVALID_ARG, "null workspace");
+  if (!aligned(ws, 256)) return fail(TQ_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  if (bytes < d256_workspace(s, ws, w)) return fail(TQ_ERR_WORKSPACE, "workspace smaller than tq_decode_workspace_size()");
+  return TQ_OK;
+}
+
+tq_status check_q(const void *q, int q_dtype, float scale) {
+  if (!q) return fail(TQ_ERR_INVALID_ARG, "null q");
+  if (q_dtype != TQ_DTYPE_F32 && q_dtype != TQ_DTYPE_BF16 && q_dtype != TQ_DTYPE_F16)
+    return fail(TQ_ERR_INVALID_ARG, "bad q dtype");
+  if (!aligned(q, 16)) return fail(TQ_ERR_ALIGNMENT, "q must be 16-byte aligned");
+  if (!std::isfinite(scale)) return fail(TQ_ERR_INVALID_ARG, "scale must be finite");
+  return TQ_OK;
+}
+
+tq_status check_caches(const void *k_cache, const void *v_cache, const int32_t *seq_lens) {
+  if (!k_cache || !v_cache) return fail(TQ_ERR_INVALID_ARG, "null cache");
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return fail(TQ_ERR_ALIGNMENT, "caches must be 16-byte aligned");
+  if (seq_lens && !aligned(seq_lens, 4)) return fail(TQ_ERR_ALIGNMENT, "seq_lens must be 4-byte aligned");
+  return TQ_OK;
+}
+
+// The d = 256 decode stages: q preparation, split-K partials, combine (mask: 1, 2, 4).
+tq_status run_d256(const tq_ctx *k, const tq_ctx *v, const void *q, int q_dtype, const void *kc, const void *vc,
+                   const int32_t *seq_lens, const D256Shape &s, float scale, float *out, const Workspace &w,
+                   cudaStream_t st, int stages) {
+  cudaError_t e = cudaSuccess;
+  if ((stages & 1) && (e = launch_prepare_q256(k, q, q_dtype, s, scale == 0.f ? 1.0f / 16.0f : scale, w, st)) !=
+                          cudaSuccess)
+    return cuda_fail(e, "prepare_q launch");
+  if ((stages & 2) && (e = launch_partial_d256(k, v, (const uint8_t *)kc, (const uint8_t *)vc, seq_lens, s, w, st)) !=
+                          cudaSuccess)
+    return cuda_fail(e, "partial launch");
+  if ((stages & 4) && (e = launch_combine_d256(v, s, out, w, st)) != cudaSuccess) return cuda_fail(e, "combine launch");
   return TQ_OK;
 }
 
@@ -116,6 +171,7 @@ tq_status check_current_device(int device, const char *who) {
 }
 
 bool decode_pair_supported(const tq_ctx *k, const tq_ctx *v) {
+  if (k->d != D || v->d != D) return false;  // d = 256 has its own path (turbo4 only)
   return ((k->fmt == TQ_FMT_TURBO4 || k->fmt == TQ_FMT_TURBO3) &&
           (v->fmt == TQ_FMT_TURBO4 || v->fmt == TQ_FMT_TURBO3)) ||
          (k->fmt == TQ_FMT_PROD3 && v->fmt == TQ_FMT_VGROUP2);
@@ -156,7 +212,7 @@ size_t tq_cache_bytes(int format, int64_t n_rows) {
 }
 
 tq_status tq_make_codebook(int bits, int d, int kind, float *centroids, float *boundaries) {
-  if (d != D) return fail(TQ_ERR_UNSUPPORTED, "only d = 128 is supported");
+  if (d != D && d != D256) return fail(TQ_ERR_UNSUPPORTED, "d must be 128 or 256");
   if (bits < 1 || bits > 4) return fail(TQ_ERR_UNSUPPORTED, "bits must be 1..4");
   if (kind != TQ_CB_QUANTILE && kind != TQ_CB_LLOYD && kind != TQ_CB_SPHERE)
     return fail(TQ_ERR_INVALID_ARG, "bad codebook kind");
@@ -168,17 +224,17 @@ tq_status tq_make_codebook(int bits, int d, int kind, float *centroids, float *b
 }
 
 tq_status tq_make_rotation(int kind, int d, uint64_t seed, float *out) {
-  if (d != D) return fail(TQ_ERR_UNSUPPORTED, "only d = 128 is supported");
+  if (d != D && d != D256) return fail(TQ_ERR_UNSUPPORTED, "d must be 128 or 256");
   if (!out) return fail(TQ_ERR_INVALID_ARG, "null output");
   if (kind != TQ_ROT_WHT && kind != TQ_ROT_DENSE) return fail(TQ_ERR_INVALID_ARG, "bad rotation kind");
   std::vector<float> r;
-  uint32_t neg[4];
-  tq_status s = build_rotation(kind, seed, r, neg);
+  uint32_t neg[8];
+  tq_status s = build_rotation(kind, d, seed, r, neg);
   if (s != TQ_OK) return s;
   if (kind == TQ_ROT_DENSE) {
     std::memcpy(out, r.data(), r.size() * sizeof(float));
   } else {
-    for (int j = 0; j < D; ++j) out[j] = ((neg[j / 32] >> (j % 32)) & 1u) ? -1.f : 1.f;
+    for (int j = 0; j < d; ++j) out[j] = ((neg[j / 32] >> (j % 32)) & 1u) ? -1.f : 1.f;
   }
   return TQ_OK;
 }
@@ -196,8 +252,9 @@ tq_status tq_ctx_create(const tq_params *params, tq_ctx **out) {
   if (!params || !out) return fail(TQ_ERR_INVALID_ARG, "null argument");
   *out = nullptr;
   const tq_params &p = *params;
-  if (p.d != D) return fail(TQ_ERR_UNSUPPORTED, "only d = 128 is supported");
   if (p.format < TQ_FMT_TURBO4 || p.format > TQ_FMT_VGROUP2) return fail(TQ_ERR_INVALID_ARG, "bad format");
+  if (p.d != D && !(p.d == D256 && p.format == TQ_FMT_TURBO4))
+    return fail(TQ_ERR_UNSUPPORTED, "d = 128 for every format, d = 256 for TURBO4");
   const bool rotated = p.format != TQ_FMT_VGROUP2;
   if (rotated && p.rotation != TQ_ROT_WHT && p.rotation != TQ_ROT_DENSE)
     return fail(TQ_ERR_INVALID_ARG, "bad rotation kind");
@@ -213,6 +270,8 @@ tq_status tq_ctx_create(const tq_params *params, tq_ctx **out) {
   if (!c) return fail(TQ_ERR_ALLOC, "host allocation failed");
   c->p = p;
   c->fmt = p.format;
+  c->d = p.d;
+  const int d = p.d;
   c->qjl_factor = (p.format == TQ_FMT_PROD3 && p.qjl_shrink) ? (float)(2.0 / 3.14159265358979323846) : 1.0f;
   cudaError_t e = cudaGetDevice(&c->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
@@ -228,22 +287,22 @@ tq_status tq_ctx_create(const tq_params *params, tq_ctx **out) {
     int kind = p.codebook;
     if (kind == TQ_CB_DEFAULT) kind = (p.format == TQ_FMT_TURBO4) ? TQ_CB_QUANTILE : TQ_CB_LLOYD;
     double c64[16];
-    make_codebook_f64(bits, D, kind, c64);
+    make_codebook_f64(bits, d, kind, c64);
     c->cb.bits = bits;
     c->cb.K = 1 << bits;
     store_codebook(c64, c->cb.K, c->cb.c, c->cb.b);
     c->f16 = make_f16_table(c->cb.c, c->cb.K);
     c->bt = make_bucket_table(c->cb.b, c->cb.K - 1);
     std::vector<float> r;
-    s = build_rotation(p.rotation, p.rot_seed, r, c->wht_neg);
+    s = build_rotation(p.rotation, d, p.rot_seed, r, c->wht_neg);
     if (s == TQ_OK) s = to_device(&c->d_pi, r.data(), r.size());
     if (s == TQ_OK) {
-      std::vector<float> rt((size_t)D * D);
-      for (int i = 0; i < D; ++i)
-        for (int j = 0; j < D; ++j) rt[(size_t)j * D + i] = r[(size_t)i * D + j];
+      std::vector<float> rt((size_t)d * d);
+      for (int i = 0; i < d; ++i)
+        for (int j = 0; j < d; ++j) rt[(size_t)j * d + i] = r[(size_t)i * d + j];
       s = to_device(&c->d_pit, rt.data(), rt.size());
     }
-    if (s == TQ_OK && p.rotation == TQ_ROT_DENSE) {
+    if (s == TQ_OK && p.rotation == TQ_ROT_DENSE && d == D) {
       // bf16 hi + lo parts of R for the tensor-core write: hi = RN(r), lo = RN(r - hi)
       std::vector<uint16_t> rb(2 * (size_t)D * D);
       for (size_t i = 0; i < (size_t)D * D; ++i) {
@@ -305,11 +364,11 @@ tq_status tq_ctx_device_status(const tq_ctx *ctx, int32_t *status, int clear) {
 namespace {
 // The argument checks of tq_quantize_set_rows for a call with n_rows >= 1.
 tq_status check_write_args(const void *src, int src_dtype, int64_t src_row_stride, const int64_t *row_ids,
-                           const void *dst_cache, int64_t n_rows, int64_t dst_rows) {
+                           const void *dst_cache, int64_t n_rows, int64_t dst_rows, int d = D) {
   if (!src || !dst_cache) return fail(TQ_ERR_INVALID_ARG, "null source or cache");
   if (src_dtype != TQ_DTYPE_F32 && src_dtype != TQ_DTYPE_BF16)
     return fail(TQ_ERR_UNSUPPORTED, "source dtype must be F32 or BF16");
-  if (src_row_stride < D) return fail(TQ_ERR_INVALID_ARG, "source row stride < 128");
+  if (src_row_stride < d) return fail(TQ_ERR_INVALID_ARG, "source row stride below the head dimension");
   if (dst_rows < 1) return fail(TQ_ERR_INVALID_ARG, "dst_rows < 1");
   if (!row_ids && dst_rows < n_rows) return fail(TQ_ERR_INVALID_ARG, "identity slots need dst_rows >= n_rows");
   const size_t esz = src_dtype == TQ_DTYPE_F32 ? 4 : 2;
@@ -330,10 +389,12 @@ tq_status tq_quantize_set_rows(const tq_ctx *ctx, const void *src, int src_dtype
   if (n_rows == 0) return TQ_OK;
   tq_status st = check_current_device(ctx->device, "tq_quantize_set_rows");
   if (st != TQ_OK) return st;
-  if ((st = check_write_args(src, src_dtype, src_row_stride, row_ids, dst_cache, n_rows, dst_rows)) != TQ_OK)
+  if ((st = check_write_args(src, src_dtype, src_row_stride, row_ids, dst_cache, n_rows, dst_rows, ctx->d)) !=
+      TQ_OK)
     return st;
   WriteLaunch w{src, src_dtype, n_rows, src_row_stride, row_ids, (uint8_t *)dst_cache, dst_rows};
-  cudaError_t e = launch_write(ctx, w, (cudaStream_t)stream);
+  cudaError_t e = ctx->d == D256 ? launch_write_d256(ctx, w, (cudaStream_t)stream)
+                                 : launch_write(ctx, w, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "write kernel launch");
   return TQ_OK;
 }
@@ -348,13 +409,23 @@ tq_status tq_dequantize(const tq_ctx *ctx, const void *cache, int64_t n_rows, in
   if (!cache || !dst) return fail(TQ_ERR_INVALID_ARG, "null cache or output");
   if (!aligned(cache, 16)) return fail(TQ_ERR_ALIGNMENT, "cache must be 16-byte aligned");
   if (!aligned(dst, 4)) return fail(TQ_ERR_ALIGNMENT, "output must be 4-byte aligned");
-  cudaError_t e = launch_dequantize(ctx, (const uint8_t *)cache, n_rows, unrotate, dst, (cudaStream_t)stream);
+  cudaError_t e = ctx->d == D256 ? launch_dequant_d256(ctx, (const uint8_t *)cache, n_rows, unrotate, dst,
+                                                      (cudaStream_t)stream)
+                                 : launch_dequantize(ctx, (const uint8_t *)cache, n_rows, unrotate, dst,
+                                                     (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "dequantize launch");
   return TQ_OK;
 }
 
 tq_status tq_decode_num_splits(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, int Hq, int Hkv,
                                int L, int *n_split) {
+  if (is_d256(k_ctx, v_ctx)) {
+    if (!n_split) return fail(TQ_ERR_INVALID_ARG, "null output");
+    D256Shape s;
+    tq_status st = check_d256(k_ctx, v_ctx, B, Hq, Hkv, L, &s);
+    if (st == TQ_OK) *n_split = s.n_split;
+    return st;
+  }
   if (!n_split) return fail(TQ_ERR_INVALID_ARG, "null output");
   DecodeShape s;
   tq_status st = check_decode_common(k_ctx, v_ctx, B, Hq, Hkv, L, &s);
@@ -365,6 +436,13 @@ tq_status tq_decode_num_splits(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, 
 
 tq_status tq_decode_workspace_size(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, int Hq,
                                    int Hkv, int L, size_t *bytes) {
+  if (is_d256(k_ctx, v_ctx)) {
+    if (!bytes) return fail(TQ_ERR_INVALID_ARG, "null output");
+    D256Shape s;
+    tq_status st = check_d256(k_ctx, v_ctx, B, Hq, Hkv, L, &s);
+    if (st == TQ_OK) *bytes = d256_workspace(s, nullptr, nullptr);
+    return st;
+  }
   if (!bytes) return fail(TQ_ERR_INVALID_ARG, "null output");
   DecodeShape s;
   tq_status st = check_decode_common(k_ctx, v_ctx, B, Hq, Hkv, L, &s);
@@ -376,6 +454,15 @@ tq_status tq_decode_workspace_size(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int
 tq_status tq_decode_prepare_q(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *q,
                               int q_dtype, int B, int Hq, int Hkv, int L, float scale,
                               void *workspace, size_t workspace_bytes, tq_stream_t stream) {
+  if (is_d256(k_ctx, v_ctx)) {
+    D256Shape s;
+    Workspace w;
+    tq_status st = check_d256(k_ctx, v_ctx, B, Hq, Hkv, L, &s);
+    if (st == TQ_OK) st = check_q(q, q_dtype, scale);
+    if (st == TQ_OK) st = check_workspace256(s, workspace, workspace_bytes, &w);
+    if (st != TQ_OK) return st;
+    return run_d256(k_ctx, v_ctx, q, q_dtype, nullptr, nullptr, nullptr, s, scale, nullptr, w, (cudaStream_t)stream, 1);
+  }
   DecodeShape s;
   tq_status st = check_decode_common(k_ctx, v_ctx, B, Hq, Hkv, L, &s);
   if (st != TQ_OK) return st;
@@ -396,6 +483,16 @@ tq_status tq_decode_partial(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void
                             const void *v_cache, const int32_t *seq_lens, int B, int Hq, int Hkv,
                             int L, float *scores_dbg, void *workspace, size_t workspace_bytes,
                             tq_stream_t stream) {
+  if (is_d256(k_ctx, v_ctx)) {
+    D256Shape s;
+    Workspace w;
+    tq_status st = check_d256(k_ctx, v_ctx, B, Hq, Hkv, L, &s);
+    if (st == TQ_OK) st = check_caches(k_cache, v_cache, seq_lens);
+    if (st == TQ_OK && scores_dbg) st = fail(TQ_ERR_UNSUPPORTED, "no score output at head dimension 256");
+    if (st == TQ_OK) st = check_workspace256(s, workspace, workspace_bytes, &w);
+    if (st != TQ_OK) return st;
+    return run_d256(k_ctx, v_ctx, nullptr, 0, k_cache, v_cache, seq_lens, s, 0.f, nullptr, w, (cudaStream_t)stream, 2);
+  }
   DecodeShape s;
   tq_status st = check_decode_common(k_ctx, v_ctx, B, Hq, Hkv, L, &s);
   if (st != TQ_OK) return st;
@@ -414,6 +511,16 @@ tq_status tq_decode_partial(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void
 tq_status tq_decode_combine(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, int Hq, int Hkv,
                             int L, float *out, void *workspace, size_t workspace_bytes,
                             tq_stream_t stream) {
+  if (is_d256(k_ctx, v_ctx)) {
+    D256Shape s;
+    Workspace w;
+    tq_status st = check_d256(k_ctx, v_ctx, B, Hq, Hkv, L, &s);
+    if (st == TQ_OK && !out) st = fail(TQ_ERR_INVALID_ARG, "null output");
+    if (st == TQ_OK && !aligned(out, 16)) st = fail(TQ_ERR_ALIGNMENT, "output must be 16-byte aligned at d = 256");
+    if (st == TQ_OK) st = check_workspace256(s, workspace, workspace_bytes, &w);
+    if (st != TQ_OK) return st;
+    return run_d256(k_ctx, v_ctx, nullptr, 0, nullptr, nullptr, nullptr, s, 0.f, out, w, (cudaStream_t)stream, 4);
+  }
   DecodeShape s;
   tq_status st = check_decode_common(k_ctx, v_ctx, B, Hq, Hkv, L, &s);
   if (st != TQ_OK) return st;
@@ -430,6 +537,17 @@ tq_status tq_decode_partial_merge(const tq_ctx *k_ctx, const tq_ctx *v_ctx, cons
                                   const void *v_cache, const int32_t *seq_lens, int B, int Hq, int Hkv,
                                   int L, float *out, void *workspace, size_t workspace_bytes,
                                   tq_stream_t stream) {
+  if (is_d256(k_ctx, v_ctx)) {
+    D256Shape s;
+    Workspace w;
+    tq_status st = check_d256(k_ctx, v_ctx, B, Hq, Hkv, L, &s);
+    if (st == TQ_OK) st = check_caches(k_cache, v_cache, seq_lens);
+    if (st == TQ_OK && !out) st = fail(TQ_ERR_INVALID_ARG, "null output");
+    if (st == TQ_OK && !aligned(out, 16)) st = fail(TQ_ERR_ALIGNMENT, "output must be 16-byte aligned at d = 256");
+    if (st == TQ_OK) st = check_workspace256(s, workspace, workspace_bytes, &w);
+    if (st != TQ_OK) return st;
+    return run_d256(k_ctx, v_ctx, nullptr, 0, k_cache, v_cache, seq_lens, s, 0.f, out, w, (cudaStream_t)stream, 6);
+  }
   DecodeShape s;
   tq_status st = check_decode_common(k_ctx, v_ctx, B, Hq, Hkv, L, &s);
   if (st != TQ_OK) return st;
@@ -452,6 +570,13 @@ tq_status tq_decode_partial_merge(const tq_ctx *k_ctx, const tq_ctx *v_ctx, cons
 
 tq_status tq_decode_num_launches(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int B, int Hq, int Hkv,
                                  int L, int *n) {
+  if (is_d256(k_ctx, v_ctx)) {
+    if (!n) return fail(TQ_ERR_INVALID_ARG, "null output");
+    D256Shape s;
+    tq_status st = check_d256(k_ctx, v_ctx, B, Hq, Hkv, L, &s);
+    if (st == TQ_OK) *n = 3;
+    return st;
+  }
   if (!n) return fail(TQ_ERR_INVALID_ARG, "null output");
   DecodeShape s;
   tq_status st = check_decode_common(k_ctx, v_ctx, B, Hq, Hkv, L, &s);
@@ -465,6 +590,19 @@ tq_status tq_decode_attention(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const vo
                               const int32_t *seq_lens, int B, int Hq, int Hkv, int L, float scale,
                               float *out, float *scores_dbg, void *workspace,
                               size_t workspace_bytes, tq_stream_t stream) {
+  if (is_d256(k_ctx, v_ctx)) {
+    D256Shape s;
+    Workspace w;
+    tq_status st = check_d256(k_ctx, v_ctx, B, Hq, Hkv, L, &s);
+    if (st == TQ_OK) st = check_caches(k_cache, v_cache, seq_lens);
+    if (st == TQ_OK && scores_dbg) st = fail(TQ_ERR_UNSUPPORTED, "no score output at head dimension 256");
+    if (st == TQ_OK && !out) st = fail(TQ_ERR_INVALID_ARG, "null output");
+    if (st == TQ_OK && !aligned(out, 16)) st = fail(TQ_ERR_ALIGNMENT, "output must be 16-byte aligned at d = 256");
+    if (st == TQ_OK) st = check_q(q, q_dtype, scale);
+    if (st == TQ_OK) st = check_workspace256(s, workspace, workspace_bytes, &w);
+    if (st != TQ_OK) return st;
+    return run_d256(k_ctx, v_ctx, q, q_dtype, k_cache, v_cache, seq_lens, s, scale, out, w, (cudaStream_t)stream, 7);
+  }
   // the three stages' checks up front, so nothing is launched for a call that fails
   DecodeShape s;
   tq_status st = check_decode_common(k_ctx, v_ctx, B, Hq, Hkv, L, &s);
@@ -498,6 +636,32 @@ tq_status tq_decode_step(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *n
                          const void *q, int q_dtype, void *k_cache, void *v_cache,
                          const int32_t *seq_lens, int B, int Hq, int Hkv, int L, float scale, float *out,
                          void *workspace, size_t workspace_bytes, tq_stream_t stream) {
+  if (is_d256(k_ctx, v_ctx)) {
+    D256Shape s;
+    Workspace w;
+    tq_status st = check_d256(k_ctx, v_ctx, B, Hq, Hkv, L, &s);
+    if (st != TQ_OK) return st;
+    if (n_rows < 0) return fail(TQ_ERR_INVALID_ARG, "n_rows < 0");
+    const int64_t dst_rows = (int64_t)B * Hkv * L;
+    if (n_rows > 0 &&
+        ((st = check_write_args(new_k, src_dtype, src_row_stride, row_ids, k_cache, n_rows, dst_rows, D256)) != TQ_OK ||
+         (st = check_write_args(new_v, src_dtype, src_row_stride, row_ids, v_cache, n_rows, dst_rows, D256)) != TQ_OK))
+      return st;
+    if ((st = check_caches(k_cache, v_cache, seq_lens)) != TQ_OK || (st = check_q(q, q_dtype, scale)) != TQ_OK)
+      return st;
+    if (!out) return fail(TQ_ERR_INVALID_ARG, "null output");
+    if (!aligned(out, 16)) return fail(TQ_ERR_ALIGNMENT, "output must be 16-byte aligned at d = 256");
+    if ((st = check_workspace256(s, workspace, workspace_bytes, &w)) != TQ_OK) return st;
+    const cudaStream_t cs = (cudaStream_t)stream;
+    if (n_rows > 0) {
+      const WriteLaunch wk{new_k, src_dtype, n_rows, src_row_stride, row_ids, (uint8_t *)k_cache, dst_rows};
+      const WriteLaunch wv{new_v, src_dtype, n_rows, src_row_stride, row_ids, (uint8_t *)v_cache, dst_rows};
+      cudaError_t e;
+      if ((e = launch_write_d256(k_ctx, wk, cs)) != cudaSuccess || (e = launch_write_d256(v_ctx, wv, cs)) != cudaSuccess)
+        return cuda_fail(e, "write kernel launch");
+    }
+    return run_d256(k_ctx, v_ctx, q, q_dtype, k_cache, v_cache, seq_lens, s, scale, out, w, cs, 7);
+  }
   // every check of the three calls first, so that nothing is launched for a call that fails
   DecodeShape s;
   tq_status st = check_decode_common(k_ctx, v_ctx, B, Hq, Hkv, L, &s);
@@ -551,6 +715,15 @@ tq_status tq_decode_step(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *n
 
 tq_status tq_decode_step_num_launches(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int src_dtype, int64_t n_rows,
                                       int B, int Hq, int Hkv, int L, int *n) {
+  if (is_d256(k_ctx, v_ctx)) {
+    if (!n) return fail(TQ_ERR_INVALID_ARG, "null output");
+    D256Shape s;
+    tq_status st = check_d256(k_ctx, v_ctx, B, Hq, Hkv, L, &s);
+    if (st != TQ_OK) return st;
+    if (n_rows < 0) return fail(TQ_ERR_INVALID_ARG, "n_rows < 0");
+    *n = 3 + (n_rows > 0 ? 2 : 0);
+    return TQ_OK;
+  }
   if (!n) return fail(TQ_ERR_INVALID_ARG, "null output");
   DecodeShape s;
   tq_status st = check_decode_common(k_ctx, v_ctx, B, Hq, Hkv, L, &s);
@@ -575,8 +748,8 @@ tq_status check_prefill(const tq_ctx *k, const tq_ctx *v, int B, int T, int Hq, 
   if (B < 1 || T < 1 || Hq < 1 || Hkv < 1 || L < 1) return fail(TQ_ERR_INVALID_ARG, "B, T, Hq, Hkv and L must be >= 1");
   if (T > L) return fail(TQ_ERR_INVALID_ARG, "the chunk (T queries) must fit in the cache (L rows)");
   if (Hq % Hkv != 0) return fail(TQ_ERR_INVALID_ARG, "Hq must be a multiple of Hkv");
-  if (k->fmt != TQ_FMT_TURBO4 || v->fmt != TQ_FMT_TURBO4)
-    return fail(TQ_ERR_UNSUPPORTED, "the prefill kernel takes turbo4 keys and values");
+  if (k->fmt != TQ_FMT_TURBO4 || v->fmt != TQ_FMT_TURBO4 || k->d != D || v->d != D)
+    return fail(TQ_ERR_UNSUPPORTED, "the prefill kernel takes turbo4 keys and values of head dimension 128");
   if (!prefill_shape(k, B, T, Hq, Hkv, L, s))
     return fail(TQ_ERR_UNSUPPORTED, "prefill needs Hq / Hkv dividing 128 and a shape within 32-bit tile counts");
   return TQ_OK;

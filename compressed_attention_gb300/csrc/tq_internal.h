@@ -9,6 +9,11 @@
 namespace tq {
 
 constexpr int D = 128;
+// Head dimension 256 (turbo4): a row is two consecutive 68-byte turbo4 blocks.
+constexpr int D256 = 256;
+constexpr int ROW256 = 136;
+constexpr int ACC256 = 8;                 // a d = 256 partial: max, sum, 6 spare, acc[256]
+constexpr int PARTIAL256 = ACC256 + D256;
 
 // Device status codes (see tq_ctx_device_status in tq.h).
 enum DevErr : int32_t { DEVERR_ROW_OOB = 1, DEVERR_SEQLEN = 2, DEVERR_TIMEOUT = 3, DEVERR_LAYOUT = 4 };
@@ -59,7 +64,8 @@ struct tq_ctx {
   int fmt = 0;
   tq::Codebook cb{};
   tq::F16Table f16{};
-  uint32_t wht_neg[4] = {0, 0, 0, 0};  // bit j set: WHT sign j is -1
+  int d = 128;                         // head dimension: 128, or 256 (turbo4)
+  uint32_t wht_neg[8] = {};             // bit j set: WHT sign j is -1
   float *d_pi = nullptr;                // rotation R (dense Pi or the WHT matrix), fp32 row-major
   float *d_pit = nullptr;               // R^T, fp32 row-major
   float *d_S = nullptr;                 // QJL matrix S, fp32 [128][128] row-major
@@ -187,6 +193,24 @@ bool decode_shape(const tq_ctx *k, const tq_ctx *v, int B, int Hq, int Hkv, int 
                   DecodeShape *s);
 bool decode_pair_supported(const tq_ctx *k, const tq_ctx *v);  // a decode kernel exists
 Workspace carve_workspace(const DecodeShape &s, void *base);
+
+// Head dimension 256 (tq_d256.cu): turbo4 keys and values only.
+struct D256Shape {
+  int B, Hq, Hkv, L, gq, n_hg;  // units: (batch, KV head, group of up to 4 q-heads)
+  int n_split, chunk;          // splits per unit, keys per split (a multiple of 16)
+  int units;
+};
+bool d256_shape(const tq_ctx *k, int B, int Hq, int Hkv, int L, D256Shape *s);
+size_t d256_workspace(const D256Shape &s, void *base, Workspace *w);  // returns the bytes
+cudaError_t launch_write_d256(const tq_ctx *ctx, const WriteLaunch &w, cudaStream_t st);
+cudaError_t launch_dequant_d256(const tq_ctx *ctx, const uint8_t *cache, int64_t n_rows, int unrotate,
+                                float *dst, cudaStream_t st);
+cudaError_t launch_prepare_q256(const tq_ctx *k, const void *q, int q_dtype, const D256Shape &s, float scale,
+                                const Workspace &w, cudaStream_t st);
+cudaError_t launch_partial_d256(const tq_ctx *k, const tq_ctx *v, const uint8_t *kc, const uint8_t *vc,
+                                const int32_t *seq_lens, const D256Shape &s, const Workspace &w, cudaStream_t st);
+cudaError_t launch_combine_d256(const tq_ctx *v, const D256Shape &s, float *out, const Workspace &w,
+                                cudaStream_t st);
 
 QprepParams make_qprep_params(const tq_ctx *k, const void *q, int q_dtype, const DecodeShape &s,
                               float scale, const Workspace &ws);

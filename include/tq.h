@@ -16,7 +16,16 @@
  *                         group value quantization).
  *
  * Conventions common to every call
- *   - Head dimension d = 128 only; any other d returns TQ_ERR_UNSUPPORTED.
+ *   - Head dimension d = 128 for every format, and d = 256 for TURBO4 ([turbo4
+ *     post-mortem] section 9, per-head-dimension codebooks): a 256-element row is
+ *     rotated as a whole, quantized with the codebook of N(0, 1/256), and stored as
+ *     two consecutive 68-byte TURBO4 blocks (elements 128c .. 128c+127 in block c,
+ *     the row's norm in both), each read with its own stored norm; a cache of n such
+ *     rows is tq_cache_bytes(TQ_FMT_TURBO4, 2n) bytes.  At d = 256 the write,
+ *     dequantize and decode calls (one-call, staged and step) are available, for
+ *     TURBO4 keys and values; prefill, the store, score output (scores_dbg) and the
+ *     other formats return TQ_ERR_UNSUPPORTED.  Any other d returns
+ *     TQ_ERR_UNSUPPORTED.
  *   - All functions return a tq_status; no exception crosses the ABI.
  *     tq_last_error() gives a one-line description of the last failure on the
  *     calling thread.
@@ -58,7 +67,7 @@ typedef struct tq_ctx tq_ctx;
 typedef enum tq_status {
   TQ_OK = 0,
   TQ_ERR_INVALID_ARG = 1,  /* null pointer, bad size, bad enum, L == 0, ... */
-  TQ_ERR_UNSUPPORTED = 2,  /* d != 128, format pair without a decode kernel, ... */
+  TQ_ERR_UNSUPPORTED = 2,  /* d not 128 / 256, format pair without a decode kernel, ... */
   TQ_ERR_ALIGNMENT = 3,    /* a pointer or stride breaks the stated alignment */
   TQ_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
   TQ_ERR_ALLOC = 5,        /* device or host allocation failed */

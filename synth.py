@@ -21,6 +21,9 @@ Workloads (shapes and distributions of the pages' decode and write workloads):
   for the asymmetric cache with 3-bit keys and 4-bit values.
 * ``gqa_t3``: the same draws again, for the symmetric turbo3 cache (3-bit keys
   and values).
+* ``gqa_d256``: head dimension 256 (turbo4): B=4, Hq=32, Hkv=8, L=32768, the
+  ``gqa_lognormal`` law over 256 channels (round(1% of 256) = 3 outlier channels
+  per KV head); seed 9.
 * ``prefill_chunk``: B=1, Hq=32, Hkv=8, L=32768, T=512 chunk queries at positions
   L-T .. L-1 (the last chunk of a 32K-token prompt); K and V as ``gqa_lognormal``
   (lognormal channel scales with one outlier channel per KV head), bf16; q bf16
@@ -47,6 +50,9 @@ WORKLOADS = {
     # the last 512-token chunk of a 32K-token prompt: T chunk queries at positions L-T .. L-1
     "prefill_chunk": dict(B=1, Hq=32, Hkv=8, L=32768, T=512, q_dtype="bf16", kv_dtype="bf16",
                           dist="lognormal_outlier", seed=7),
+    # head dimension 256: the gqa_lognormal law over 256 channels, half the batch
+    "gqa_d256": dict(B=4, Hq=32, Hkv=8, L=32768, d=256, q_dtype="bf16", kv_dtype="bf16",
+                     dist="lognormal_outlier", seed=9),
 }
 
 D = 128
@@ -80,10 +86,11 @@ def _maybe_bf16(x32, dtype):
 def channel_scales(cfg, tensor):
     """Per-(KV-head, channel) multipliers [Hkv, 128] for the lognormal-with-outliers law."""
     rng = np.random.default_rng([cfg["seed"], _tag(tensor), _tag("scales")])
-    s = np.exp(rng.normal(0.0, 0.5, size=(cfg["Hkv"], D)))
-    n_out = int(round(0.01 * D))
+    d = cfg.get("d", D)
+    s = np.exp(rng.normal(0.0, 0.5, size=(cfg["Hkv"], d)))
+    n_out = int(round(0.01 * d))
     for h in range(cfg["Hkv"]):
-        s[h, rng.permutation(D)[:n_out]] *= 8.0
+        s[h, rng.permutation(d)[:n_out]] *= 8.0
     return s
 
 
@@ -91,7 +98,7 @@ def kv_unit(cfg, tensor, b, h, L=None):
     """K or V rows of one (batch, KV-head) unit: (fp32 values [L, 128], bf16 bits or None)."""
     L = cfg["L"] if L is None else L
     rng = np.random.default_rng([cfg["seed"], _tag(tensor), b, h])
-    z = rng.standard_normal((L, D), dtype=np.float32)
+    z = rng.standard_normal((L, cfg.get("d", D)), dtype=np.float32)
     if cfg["dist"] == "lognormal_outlier":
         z = (z * channel_scales(cfg, tensor)[h][None, :].astype(np.float32)).astype(np.float32)
     return _maybe_bf16(z, cfg["kv_dtype"])
@@ -116,7 +123,7 @@ def queries(cfg, B=None, Hq=None):
     B = cfg["B"] if B is None else B
     Hq = cfg["Hq"] if Hq is None else Hq
     rng = np.random.default_rng([cfg["seed"], _tag("q")])
-    return _maybe_bf16(rng.standard_normal((B, Hq, D), dtype=np.float32), cfg["q_dtype"])
+    return _maybe_bf16(rng.standard_normal((B, Hq, cfg.get("d", D)), dtype=np.float32), cfg["q_dtype"])
 
 
 def prefill_queries(cfg):

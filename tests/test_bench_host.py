@@ -35,7 +35,8 @@ def test_bench_configs_name_their_workloads():
     for name in bench.DECODE:
         w = synth.WORKLOADS[name]
         c = bench.decode_config(name, w)
-        assert c["workload"].startswith(f"{name}: B={w['B']} Hq={w['Hq']} Hkv={w['Hkv']} d=128 L={w['L']}")
+        assert c["workload"].startswith(f"{name}: B={w['B']} Hq={w['Hq']} Hkv={w['Hkv']} d={w.get('d', 128)} "
+                                        f"L={w['L']}")
         assert c["k_format"] in ("turbo4", "turbo3", "prod3") and c["v_format"] in ("turbo4", "turbo3", "vgroup2")
         # inputs larger than twice the L2 run back to back, the others flush before each step
         big = w["B"] * w["Hkv"] * w["L"] * bench.decode_unit_bytes(bench.DECODE[name]) > 2 * bench.L2_NOMINAL
