@@ -275,10 +275,25 @@ struct Part256 {
 // a warp's 32 lookups hit 32 banks), each warp's 16 K and 16 V rows, the merge scratch.
 struct Smem256 {
   uint32_t lut[256][64];
-  uint8_t kv[PW][2][PSTAGE];
-  float osm[PW][4][D256];
+  union {
+    uint8_t kv[PW][2][2][PSTAGE];  // warp, buffer (double-buffered), K / V
+    float osm[PW][4][D256];        // the merge scratch, after the last block
+  };
   float mw[PW][4], lw[PW][4];
 };
+
+// Start copying a warp's block of nk rows (keys kb ..) of K and V into shared memory
+// (8-byte pieces of the valid rows; rows start 8-byte aligned), as one cp.async group.
+__device__ __forceinline__ void stage_block(uint8_t *ks, uint8_t *vs, const uint8_t *kc, const uint8_t *vc,
+                                            size_t row0, int nk, int lane) {
+  const int n8 = nk * (ROW256 / 8);
+  const uint8_t *kg = kc + row0 * ROW256, *vg = vc + row0 * ROW256;
+  for (int i = lane; i < n8; i += 32) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(ks + 8 * i)), "l"(kg + 8 * i) : "memory");
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(vs + 8 * i)), "l"(vg + 8 * i) : "memory");
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
 
 __device__ __forceinline__ uint32_t lut_at(const uint32_t *lut, uint32_t laneword, uint32_t w, int i) {
   return lut[((w >> (8 * i)) & 0xFFu) * 64 + laneword];
@@ -349,20 +364,24 @@ __global__ void __launch_bounds__(PW * 32, 1) k_partial_d256(const Part256 p) {
 #pragma unroll
   for (int mt = 0; mt < 16; ++mt) O[mt][0] = O[mt][1] = O[mt][2] = O[mt][3] = 0.f;
   float M = -INFINITY, lsum = 0.f;
-  uint8_t *Ks = sm.kv[warp][0], *Vs = sm.kv[warp][1];
-
-  for (int kb = k0 + 16 * warp; kb < k1; kb += 16 * PW) {
+  // the warp's blocks of 16 keys: kb = k0 + 16 (warp + PW i); each block's K and V rows are
+  // copied into one of two buffers while the previous block is computed
+  int buf = 0;
+  if (k0 + 16 * warp < k1)
+    stage_block(sm.kv[warp][0][0], sm.kv[warp][0][1], p.kc, p.vc, unit_row0 + k0 + 16 * warp,
+                min(16, k1 - k0 - 16 * warp), lane);
+  for (int kb = k0 + 16 * warp; kb < k1; kb += 16 * PW, buf ^= 1) {
     const int nk = min(16, k1 - kb);
-    // the warp's 16 K and V rows into shared memory (8-byte pieces of the valid rows)
-    const uint2 *ksrc = reinterpret_cast<const uint2 *>(p.kc + (unit_row0 + kb) * ROW256);
-    const uint2 *vsrc = reinterpret_cast<const uint2 *>(p.vc + (unit_row0 + kb) * ROW256);
-    const int n8 = nk * (ROW256 / 8);
-    __syncwarp();
-    for (int i = lane; i < n8; i += 32) {
-      reinterpret_cast<uint2 *>(Ks)[i] = ksrc[i];
-      reinterpret_cast<uint2 *>(Vs)[i] = vsrc[i];
+    const int kn = kb + 16 * PW;
+    if (kn < k1) {
+      stage_block(sm.kv[warp][buf ^ 1][0], sm.kv[warp][buf ^ 1][1], p.kc, p.vc, unit_row0 + kn, min(16, k1 - kn),
+                  lane);
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+    } else {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
     }
     __syncwarp();
+    const uint8_t *Ks = sm.kv[warp][buf][0], *Vs = sm.kv[warp][buf][1];
     const bool ok0 = pk0 < nk, ok1 = pk1 < nk;
     // ---- scores, block half by block half, each scaled by its own key norm
     float s0 = 0.f, s1 = 0.f;
@@ -451,13 +470,14 @@ __global__ void __launch_bounds__(PW * 32, 1) k_partial_d256(const Part256 p) {
         }
       }
     }
+    __syncwarp();  // every lane is done with this buffer before it is refilled
   }
   lsum += __shfl_xor_sync(FULL_MASK, lsum, 4);
   lsum += __shfl_xor_sync(FULL_MASK, lsum, 8);
   lsum += __shfl_xor_sync(FULL_MASK, lsum, 16);
   // ---- merge the four warps' states and write this split's partial of the unit's heads
   if (g == 0) sm.mw[warp][t] = M, sm.lw[warp][t] = lsum;
-  __syncthreads();
+  __syncthreads();  // (also: every warp is done with the staging buffers the scratch reuses)
   float ms = -INFINITY;
 #pragma unroll
   for (int w = 0; w < PW; ++w) ms = fmaxf(ms, sm.mw[w][t]);
@@ -627,7 +647,7 @@ cudaError_t launch_partial_d256(const tq_ctx *k, const tq_ctx *v, const uint8_t 
   for (int i = 0; i < 8; ++i) p.kc16[i] = k->f16.c16[i], p.vc16[i] = v->f16.c16[i];
   p.status = k->d_status;
   const size_t smem = sizeof(Smem256);
-  cudaError_t e = cudaFuncSetAttribute(k_partial_d256, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = kernel_smem_attr((const void *)k_partial_d256, (int)smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(k_partial_d256, dim3(s.units * s.n_split), dim3(PW * 32), smem, st, p);
 }

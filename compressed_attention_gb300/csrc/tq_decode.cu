@@ -1065,7 +1065,7 @@ cudaError_t launch_prepare_q(const tq_ctx *k, const void *q, int q_dtype, const 
   const QprepParams p = make_qprep_params(k, q, q_dtype, s, scale, ws);
   const int grid = (p.n_q + QWARPS - 1) / QWARPS;
   auto kern = s.pv ? k_prepare_q<true> : k_prepare_q<false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)QPREP_SMEM);
+  cudaError_t e = kernel_smem_attr((const void *)kern, (int)QPREP_SMEM);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(grid), dim3(QWARPS * 32), QPREP_SMEM, st, p);
 }
@@ -1074,10 +1074,7 @@ template <int NG, bool SC, int KP, int VP, bool FIXED, bool K3, bool V3>
 cudaError_t launch_t4(const PartialParams &p, dim3 grid, cudaStream_t st) {
   const size_t smem = SMEM_BYTES;
   auto kern = k_partial_t4<NG, SC, KP, VP, FIXED, K3, V3>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             (int)cudaSharedmemCarveoutMaxShared);
+  cudaError_t e = kernel_smem_attr((const void *)kern, (int)smem, true);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, grid, dim3(NTHREADS), smem, st, p);
 }
@@ -1177,7 +1174,7 @@ cudaError_t launch_combine(const tq_ctx *k, const tq_ctx *v, const DecodeShape &
   p.inv_vscale = 1.0f / (exp2f(P_SHIFT) * (vgroup ? 1.0f : v->f16.alpha));
   p.out = out;
   const size_t smem = (size_t)D * D * 4 + QWARPS * D * 4;
-  cudaError_t e = cudaFuncSetAttribute(k_combine, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = kernel_smem_attr((const void *)k_combine, (int)smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(k_combine, dim3((p.n_heads + QWARPS - 1) / QWARPS), dim3(QWARPS * 32), smem, st, p);
 }
@@ -1197,7 +1194,7 @@ cudaError_t launch_combine_prefill(const tq_ctx *v, const PrefillShape &s, float
   p.inv_vscale = 1.0f / (exp2f(P_SHIFT) * v->f16.alpha);
   p.out = out;
   const size_t smem = (size_t)D * D * 4 + QWARPS * D * 4;
-  cudaError_t e = cudaFuncSetAttribute(k_combine, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = kernel_smem_attr((const void *)k_combine, (int)smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(k_combine, dim3((p.n_heads + QWARPS - 1) / QWARPS), dim3(QWARPS * 32), smem, st, p);
 }

@@ -428,10 +428,7 @@ __global__ void __maxnreg__(168) k_partial_pv(const PvParams p) {
 template <bool SC, bool FIXED>
 cudaError_t launch_pv(const PvParams &p, dim3 grid, cudaStream_t st) {
   auto kern = k_partial_pv<SC, FIXED>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_PV);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             (int)cudaSharedmemCarveoutMaxShared);
+  cudaError_t e = kernel_smem_attr((const void *)kern, (int)SMEM_PV, true);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, grid, dim3(NTH), SMEM_PV, st, p);
 }

@@ -10,6 +10,9 @@
 #include <cuda_fp16.h>
 
 #include <cmath>
+#include <map>
+#include <mutex>
+#include <tuple>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -115,6 +118,40 @@ double sphere_cond_mean(double al, double a, double b) {
 }
 
 }  // namespace
+
+cudaError_t kernel_smem_attr(const void *func, int bytes, bool max_shared) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static std::mutex mu;
+  static std::map<std::tuple<const void *, int, int, bool>, bool> done;
+  const auto key = std::make_tuple(func, dev, bytes, max_shared);
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count(key)) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && max_shared)
+    e = cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+  if (e == cudaSuccess) done[key] = true;
+  return e;
+}
+
+cudaError_t kernel_occupancy(const void *func, int threads, size_t smem, int *blocks) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static std::mutex mu;
+  static std::map<std::tuple<const void *, int, int, size_t>, int> known;
+  const auto key = std::make_tuple(func, dev, threads, smem);
+  std::lock_guard<std::mutex> lock(mu);
+  const auto it = known.find(key);
+  if (it != known.end()) {
+    *blocks = it->second;
+    return cudaSuccess;
+  }
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, func, threads, smem);
+  if (e == cudaSuccess) known[key] = *blocks;
+  return e;
+}
 
 void set_error(const char *fmt, ...) {
   va_list ap;

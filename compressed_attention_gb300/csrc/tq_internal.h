@@ -113,6 +113,13 @@ void set_error(const char *fmt, ...);
 // Every call that launches work checks its contexts' device this way: their tables and
 // status word live in that device's memory, and the kernels run on the current one.
 tq_status check_current_device(int device, const char *who);
+// Raises a kernel's dynamic shared-memory limit to `bytes` (and, with max_shared, asks for
+// the largest shared-memory carveout) once per (kernel, device, setting): the attribute
+// stays with the function on that device, so later launches skip the driver calls.
+cudaError_t kernel_smem_attr(const void *func, int bytes, bool max_shared = false);
+// Resident CTAs per SM of a kernel at `threads` threads and `smem` bytes of dynamic shared
+// memory, asked of the runtime once per (kernel, device, launch shape).
+cudaError_t kernel_occupancy(const void *func, int threads, size_t smem, int *blocks);
 
 // ---- kernel launchers ----
 struct WriteLaunch {

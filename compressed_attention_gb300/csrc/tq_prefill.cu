@@ -627,7 +627,7 @@ cudaError_t launch_prefill(const tq_ctx *k, const tq_ctx *v, const uint8_t *kc, 
     p.vlo[i] = v->f16.lo[i], p.vhi[i] = v->f16.hi[i];
   }
   p.status = k->d_status;
-  cudaError_t e = cudaFuncSetAttribute(k_prefill_t4, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_PF);
+  cudaError_t e = kernel_smem_attr((const void *)k_prefill_t4, (int)SMEM_PF);
   if (e != cudaSuccess) return e;
   return launch_pdl(k_prefill_t4, dim3(s.grid), dim3(PF_THREADS), SMEM_PF, st, p);
 }

@@ -730,14 +730,13 @@ template <typename K>
 cudaError_t launch_rows(K kernel, const WriteParams &p, int64_t n_rows, int num_sms, size_t smem,
                         int blocks_per_sm, cudaStream_t st) {
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    cudaError_t e = kernel_smem_attr((const void *)kernel, (int)smem);
     if (e != cudaSuccess) return e;
   }
   // One wave of resident CTAs (the kernels loop over rows): never more CTAs per SM than
   // fit at once, so no second, partial wave.
   int resident = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, kernel, WARPS * 32, smem);
+  cudaError_t e = kernel_occupancy((const void *)kernel, WARPS * 32, smem, &resident);
   if (e != cudaSuccess) return e;
   if (resident >= 1 && resident < blocks_per_sm) blocks_per_sm = resident;
   int64_t want = (n_rows + WARPS - 1) / WARPS;
@@ -750,7 +749,7 @@ cudaError_t launch_rows(K kernel, const WriteParams &p, int64_t n_rows, int num_
 template <typename K>
 cudaError_t launch_thread_rows(K kernel, const WriteParams &p, int64_t n_rows, int num_sms, cudaStream_t st) {
   int resident = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, kernel, WT_THREADS, 0);
+  cudaError_t e = kernel_occupancy((const void *)kernel, WT_THREADS, 0, &resident);
   if (e != cudaSuccess) return e;
   if (resident < 1) resident = 1;
   const int64_t want = (n_rows + WT_THREADS / 4 - 1) / (WT_THREADS / 4);  // four threads per row
@@ -859,7 +858,7 @@ cudaError_t launch_step_front(const tq_ctx *k, const tq_ctx *v, const WriteLaunc
               : k_step_front<TQ_FMT_TURBO3, TQ_FMT_TURBO3, TQ_DTYPE_F32>;
   };
   auto kern = pick();
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)QPREP_SMEM);
+  cudaError_t e = kernel_smem_attr((const void *)kern, (int)QPREP_SMEM);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(2 * sp.n_rows + sp.q_ctas), dim3(QWARPS * 32), QPREP_SMEM, st, sp);
 }

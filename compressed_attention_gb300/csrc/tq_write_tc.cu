@@ -305,7 +305,7 @@ cudaError_t launch_write_tc(const tq_ctx *ctx, const WriteLaunch &w, cudaStream_
   const int64_t n_tiles = (w.n_rows + TC_ROWS - 1) / TC_ROWS;
   const int grid = (int)(n_tiles < 2 * ctx->num_sms ? n_tiles : 2 * ctx->num_sms);
   auto kern = ctx->fmt == TQ_FMT_TURBO4 ? k_write_dense_tc<TQ_FMT_TURBO4> : k_write_dense_tc<TQ_FMT_TURBO3>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_TC);
+  cudaError_t e = kernel_smem_attr((const void *)kern, (int)SMEM_TC);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(grid), dim3(TC_THREADS), SMEM_TC, st, map, p);
 }
