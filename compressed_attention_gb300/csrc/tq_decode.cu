@@ -71,6 +71,8 @@ struct PartialParams {
   const int32_t *seq_lens;
   int B, Hq, Hkv, L, gq, n_hg;
   int tiles_per_unit, sched_g, sched_v, vx, total_tiles, n_part;
+  uint32_t sched_q, sched_r;  // V / G and V % G (set_schedule)
+  float sched_ginv, sched_inv;  // 1 / G and G / V
   const uint32_t *qhl;
   const float *qsc;
   float *part;
@@ -406,6 +408,9 @@ __global__ void __maxnreg__(128)
   int ctr = 0, tt = cta_first_tile(p, cta), n_item = 0;
   Item it;
   bool aborted = false;
+  // fused combine, thread 0: per recorded unit, b * Hq + its first head and (its head count
+  // | its partial count << 4), taken at the item's start, off the merge's path
+  int t0_row[FIN_MAX], t0_pk[FIN_MAX];
   while (!aborted && next_item(p, cta, tt, it)) {
     const int Lb = unit_len(p, it.unit);
     const int hg = it.unit % p.n_hg;
@@ -414,6 +419,7 @@ __global__ void __maxnreg__(128)
     const int G = min(4 * NG, p.gq - hg * 4 * NG);
     const int head0 = kvh * p.gq + hg * 4 * NG;
     const size_t unit_row0 = (size_t)bk * p.L;
+    const int it_nsplit = (p.out && threadIdx.x == 0) ? unit_n_split(p, it.unit) : 0;
 
     // q as the B operand: column g = (head slot g/2, part g%2 = hi/lo), rows = dims, from
     // the q stage the producer filled for this item
@@ -675,8 +681,20 @@ __global__ void __maxnreg__(128)
 #pragma unroll
     for (int c = 0; c < NG; ++c) {
       const int hh = c * 4 + t;
-      float ms = -INFINITY;
-      for (int w = 0; w < CWARPS; ++w) ms = fmaxf(ms, sm.mw[w][hh]);
+      // the head's max and sum over the warps, by shuffles: lane (g, t) takes warps g and
+      // g + 8, the xor steps over g combine them (every lane of a warp ends with its t's)
+      const float m0 = sm.mw[g][hh], l0 = sm.lw[g][hh];
+      const bool has1 = g + 8 < CWARPS;
+      const float m1 = has1 ? sm.mw[g + 8][hh] : -INFINITY, l1 = has1 ? sm.lw[g + 8][hh] : 0.f;
+      float ms = fmaxf(m0, m1);
+      ms = fmaxf(ms, __shfl_xor_sync(FULL_MASK, ms, 4));
+      ms = fmaxf(ms, __shfl_xor_sync(FULL_MASK, ms, 8));
+      ms = fmaxf(ms, __shfl_xor_sync(FULL_MASK, ms, 16));
+      float ls = (m0 == -INFINITY ? 0.f : l0 * exp2_approx(m0 - ms)) +
+                 (m1 == -INFINITY ? 0.f : l1 * exp2_approx(m1 - ms));
+      ls += __shfl_xor_sync(FULL_MASK, ls, 4);
+      ls += __shfl_xor_sync(FULL_MASK, ls, 8);
+      ls += __shfl_xor_sync(FULL_MASK, ls, 16);
       const float fac = (M[c] == -INFINITY) ? 0.f : exp2_approx(M[c] - ms);
       // rows g and g+8 of m-tile mt: dims 16g + 2mt and +1 (turbo4 values), or for turbo3
       // values (m-tile 2b + h inside block b) dims 32b + 4g + 2h and +1
@@ -692,31 +710,27 @@ __global__ void __maxnreg__(128)
       for (int idx = threadIdx.x; idx < Gc * D; idx += CWARPS * 32) {
         const int h4 = idx / D, jd = idx % D;
         const int hh2 = c * 4 + h4;
-        float ms2 = -INFINITY;
-        for (int w = 0; w < CWARPS; ++w) ms2 = fmaxf(ms2, sm.mw[w][hh2]);
+        // (warp-uniform h4: lane h4 = (g 0, t h4) holds that head's max and sum)
+        const float ms2 = __shfl_sync(FULL_MASK, ms, h4), ls2 = __shfl_sync(FULL_MASK, ls, h4);
         float acc = 0.f;
+#pragma unroll
         for (int w = 0; w < CWARPS; ++w) acc += sm.osm[w][h4][jd];
         float *dst = p.part + ((size_t)(b * p.Hq + head0 + hh2) * p.n_part + it.slot) * PARTIAL_FLOATS;
         dst[6 + jd] = (ms2 == -INFINITY) ? 0.f : acc;
-        if (jd < 6) {
-          float v = 0.f;
-          if (jd == 0) {
-            v = ms2;
-          } else if (jd == 1 && ms2 != -INFINITY) {
-            for (int w = 0; w < CWARPS; ++w)
-              if (sm.mw[w][hh2] != -INFINITY) v += sm.lw[w][hh2] * exp2_approx(sm.mw[w][hh2] - ms2);
-          }
-          dst[jd] = v;
-        }
+        if (jd < 6) dst[jd] = jd == 0 ? ms2 : (jd == 1 ? ls2 : 0.f);
       }
       consumers_sync();
     }
     // fused combine: the unit's count is raised once at the CTA's end, for all its items
     if (p.out && threadIdx.x == 0) {
-      if (sm.n_units < FIN_MAX)
-        sm.units[sm.n_units++] = it.unit;
-      else  // (the host launches the fused form only where a CTA meets at most FIN_MAX units)
+      if (sm.n_units < FIN_MAX) {
+        const int n = sm.n_units++;
+        sm.units[n] = it.unit;
+        t0_row[n] = b * p.Hq + head0;
+        t0_pk[n] = G | (it_nsplit << 4);
+      } else {  // (the host launches the fused form only where a CTA meets at most FIN_MAX units)
         atomicExch(p.status, (int32_t)DEVERR_LAYOUT);
+      }
     }
   }
 
@@ -739,6 +753,9 @@ __global__ void __maxnreg__(128)
                    : "memory");
     asm volatile("cp.async.commit_group;" ::: "memory");
   }
+  // The completed units' rows and (head count | partial count << 4), by thread 0 into the
+  // idle stage buffer A (no copy is in flight after a clean finish).
+  int *meta = reinterpret_cast<int *>(smem_raw + STAGE_A_OFF);
   // Every consumer thread's partial stores fenced, then one count per item; the CTA whose
   // count completes a unit merges it.  The atomics are issued together (one round trip).
   __threadfence();
@@ -753,7 +770,10 @@ __global__ void __maxnreg__(128)
     int nf = 0;  // completed units, compacted in place
 #pragma unroll
     for (int i = 0; i < FIN_MAX; ++i)
-      if (i < ni && old[i] == unit_n_split(p, sm.units[i]) - 1) sm.units[nf++] = sm.units[i];
+      if (i < ni && old[i] == (t0_pk[i] >> 4) - 1) {
+        sm.units[nf] = sm.units[i], meta[nf] = t0_row[i], meta[FIN_MAX + nf] = t0_pk[i];
+        ++nf;
+      }
     sm.n_units = nf;
     __threadfence();  // the other CTAs' partials, published before their counts
   }
@@ -773,20 +793,18 @@ __global__ void __maxnreg__(128)
   for (int q0 = 0; q0 < n_quads; q0 += QUADS) {
     // nh heads this round; W warps per head split its partials between them (warp w takes
     // head slot w % nh and every W-th chunk of eight splits from chunk w / nh)
-    const int nh = 4 * min(QUADS, n_quads - q0), W = (4 * QUADS) / nh;
-    const int hs = warp % nh, part = warp / nh;
+    // (nq = 1: four heads, W = 3; nq = 2 or 3: eight or twelve heads, W = 1)
+    const int nq = min(QUADS, n_quads - q0), nh = 4 * nq, W = nq == 1 ? 3 : 1;
+    const int hs = nq == 1 ? (warp & 3) : warp, part = nq == 1 ? (warp >> 2) : (warp < nh ? 0 : 1);
     if (part < W) {
-      const int qq = q0 + hs / 4;
-      const int u = sm.units[qq / NG];
-      const int hg = u % p.n_hg, bk = u / p.n_hg;
-      const int b = bk / p.Hkv, kvh = bk % p.Hkv;
-      const int G = min(4 * NG, p.gq - hg * 4 * NG);
-      const int hu = 4 * (qq % NG) + hs % 4;  // head within the unit
+      const int qq = q0 + (hs >> 2);
+      const int ui = qq / NG;  // the completed unit
+      const int G = meta[FIN_MAX + ui] & 15;
+      const int hu = 4 * (qq % NG) + (hs & 3);  // head within the unit
       float ms = -INFINITY, lsum = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};  // lane l: dims l + 32 m
       if (hu < G) {
-        const int head = kvh * p.gq + hg * 4 * NG + hu;
-        const int n_split = unit_n_split(p, u);
-        const float *part_base = p.part + (size_t)(b * p.Hq + head) * p.n_part * PARTIAL_FLOATS;
+        const int n_split = meta[FIN_MAX + ui] >> 4;
+        const float *part_base = p.part + (size_t)(meta[ui] + hu) * p.n_part * PARTIAL_FLOATS;
         for (int s0 = 8 * part; s0 < n_split; s0 += 8 * W) {
           // eight splits' (max, sum) and accumulator slices loaded at once
           float mh[8], lh[8], v[8][4];
@@ -846,24 +864,26 @@ __global__ void __maxnreg__(128)
     }
     if (q0 == 0 && r_copy) asm volatile("cp.async.wait_all;" ::: "memory");
     consumers_sync();  // merged heads (and, the first time, R) in shared memory
-    // out = R^T o: thread (quad, j) reads column j of R once for the four heads of its
-    // quad (o read as broadcast float4), four independent chains over k per head,
-    // summed at the end
-    const int qs = threadIdx.x / D, qq = q0 + qs;
-    if (qs < QUADS && qq < n_quads) {
-      const int u = sm.units[qq / NG];
-      const int hg = u % p.n_hg, bk = u / p.n_hg;
-      const int b = bk / p.Hkv, kvh = bk % p.Hkv;
-      const int G = min(4 * NG, p.gq - hg * 4 * NG);
-      const int hu0 = 4 * (qq % NG);  // first head of the quad within the unit
-      const int j = threadIdx.x % D, hb = 4 * qs;
-      float res[4];
+    // out = R^T o: thread (group, j) reads column j of R once for the four heads of a quad
+    // (o read as broadcast float4), four independent chains over k per head, summed at the
+    // end.  With three quads in the round each group takes one; with one quad the three
+    // groups split k in three (the partial sums of groups 1 and 2 meet in the shares'
+    // scratch, idle now); with two quads each group takes one.
+    const int ks = (nq == 1 && p.r) ? 3 : 1;  // uniform over the CTA
+    const int grp = threadIdx.x / D, j = threadIdx.x % D;
+    const int qs = ks == 1 ? grp : 0, kpart = ks == 1 ? 0 : grp;
+    const int qq = q0 + qs;
+    const bool act = grp < QUADS && qs < nq;
+    float res[4];
+    if (act) {
+      const int hb = 4 * qs;
       if (p.r) {
+        const int kb = 44 * kpart, ke = ks == 1 ? D : min(D, kb + 44);
         float c4[4][4];
 #pragma unroll
         for (int h = 0; h < 4; ++h) c4[h][0] = c4[h][1] = c4[h][2] = c4[h][3] = 0.f;
 #pragma unroll 4
-        for (int k = 0; k < D; k += 4) {
+        for (int k = kb; k < ke; k += 4) {
           const float r0 = rs[k * D + j], r1 = rs[(k + 1) * D + j];
           const float r2 = rs[(k + 2) * D + j], r3 = rs[(k + 3) * D + j];
 #pragma unroll
@@ -881,10 +901,23 @@ __global__ void __maxnreg__(128)
 #pragma unroll
         for (int h = 0; h < 4; ++h) res[h] = sm.osm[hb + h][0][j];
       }
-      const int head0 = kvh * p.gq + hg * 4 * NG + hu0;
+      if (kpart > 0) {
+#pragma unroll
+        for (int h = 0; h < 4; ++h) sm.osm[4 * kpart + h][1][j] = res[h];
+      }
+    }
+    if (ks > 1) consumers_sync();  // the k parts of groups 1 and 2 in shared memory
+    if (act && kpart == 0) {
+      if (ks > 1) {
+#pragma unroll
+        for (int h = 0; h < 4; ++h) res[h] += sm.osm[4 + h][1][j] + sm.osm[8 + h][1][j];
+      }
+      const int ui = qq / NG, G = meta[FIN_MAX + ui] & 15;
+      const int hu0 = 4 * (qq % NG);  // first head of the quad within the unit
+      float *dst = p.out + (size_t)(meta[ui] + hu0) * D + j;
 #pragma unroll
       for (int h = 0; h < 4; ++h)
-        if (hu0 + h < G) p.out[(size_t)(b * p.Hq + head0 + h) * D + j] = res[h];
+        if (hu0 + h < G) dst[h * D] = res[h];
     }
     consumers_sync();  // the round's merged heads are free again
   }
@@ -896,6 +929,8 @@ struct CombineParams {
   int n_heads;      // B * Hq (decode) or B * T * Hq (prefill rows)
   int n_split;      // partial slots per head
   int Hq, gq, heads_per_cta, n_hg, tiles_per_unit, sched_g, sched_v, vx;
+  uint32_t sched_q, sched_r;  // V / G and V % G (set_schedule)
+  float sched_ginv, sched_inv;  // 1 / G and G / V
   int pf_T, pf_Hkv, pf_qpt, pf_n_qt;  // prefill geometry (pf_T = 0: decode)
   int no_main;      // 1: no split-K partials (every key is in the exact tail)
   int tail_slot;    // slot of an exact-tail partial per head, or -1
@@ -1126,7 +1161,8 @@ cudaError_t launch_partial(const tq_ctx *k, const tq_ctx *v, const uint8_t *kc,
   p.withhold_first_tile = withhold_first_tile ? 1 : 0;
   p.kc = kc, p.vc = vc, p.seq_lens = seq_lens;
   p.B = s.B, p.Hq = s.Hq, p.Hkv = s.Hkv, p.L = s.L, p.gq = s.gq, p.n_hg = s.n_hg;
-  p.tiles_per_unit = s.tiles_per_unit, p.sched_g = s.grid, p.sched_v = s.vtotal; p.vx = s.vx;
+  p.tiles_per_unit = s.tiles_per_unit, p.vx = s.vx;
+  if (!set_schedule(p, s.grid, s.vtotal)) return cudaErrorInvalidValue;
   p.total_tiles = s.total_tiles, p.n_part = s.n_part;
   p.qhl = ws.qhl, p.qsc = ws.qsc, p.part = ws.partials, p.scores = scores_dbg;
   const bool k3 = k->fmt == TQ_FMT_TURBO3;
@@ -1166,7 +1202,8 @@ cudaError_t launch_combine(const tq_ctx *k, const tq_ctx *v, const DecodeShape &
   p.n_heads = s.B * s.Hq;
   p.n_split = s.n_part;
   p.Hq = s.Hq, p.gq = s.gq, p.heads_per_cta = s.heads_per_cta, p.n_hg = s.n_hg;
-  p.tiles_per_unit = s.tiles_per_unit, p.sched_g = s.grid, p.sched_v = s.vtotal; p.vx = s.vx;
+  p.tiles_per_unit = s.tiles_per_unit, p.vx = s.vx;
+  if (!set_schedule(p, s.grid, s.vtotal)) return cudaErrorInvalidValue;
   p.no_main = s.no_main ? 1 : 0;
   p.tail_slot = s.tail_slot;
   const bool vgroup = v->fmt == TQ_FMT_VGROUP2;  // values are not rotated
@@ -1186,7 +1223,8 @@ cudaError_t launch_combine_prefill(const tq_ctx *v, const PrefillShape &s, float
   p.n_heads = s.B * s.T * s.Hq;
   p.n_split = s.n_part;
   p.Hq = s.Hq, p.gq = s.gq;
-  p.tiles_per_unit = s.tiles_per_unit, p.sched_g = s.grid, p.sched_v = s.total_tiles;
+  p.tiles_per_unit = s.tiles_per_unit;
+  if (!set_schedule(p, s.grid, s.total_tiles)) return cudaErrorInvalidValue;
   p.vx = 0;  // the prefill splits its tiles equally
   p.pf_T = s.T, p.pf_Hkv = s.Hkv, p.pf_qpt = s.qpt, p.pf_n_qt = s.n_qt;
   p.tail_slot = -1;

@@ -33,32 +33,70 @@ struct Item {
   int unit, t0, t1, slot;  // tiles [t0, t1) of the unit; partial slot of this CTA
 };
 
-// First real tile at or after virtual position v.
+// The schedule arithmetic runs in 32 bits: the host checks vtotal < 2^31 and
+// grid^2 < 2^31 and stores V / G, V % G and two float reciprocals (set_schedule), so no
+// 64-bit division sits on a CTA's path (each took several hundred cycles at the start of
+// an item and in the fused merge).
+
+// Start of CTA c's virtual range, floor(c * V / G) for 0 <= c <= G: c * (V / G) plus
+// floor(c * (V % G) / G), the second from a float estimate that is within one of it.
 template <typename P>
-__device__ __forceinline__ int real_tile(const P &p, int64_t v) {
-  const int64_t vu = (int64_t)p.vx + p.tiles_per_unit;
-  const int64_t u = v / vu;
-  const int64_t o = v - u * vu - p.vx;
-  return (int)(u * p.tiles_per_unit + (o > 0 ? o : 0));
+__device__ __forceinline__ int sched_start(const P &p, int c) {
+  const uint32_t G = (uint32_t)p.sched_g;
+  const uint32_t x = (uint32_t)c * p.sched_r;  // < G^2 < 2^31
+  uint32_t t = __float2uint_rz((float)x * p.sched_ginv);
+  if (t * G > x)
+    --t;
+  else if ((t + 1) * G <= x)
+    ++t;
+  return (int)((uint32_t)c * p.sched_q + t);
+}
+
+// First real tile at or after virtual position v (0 <= v <= V).
+template <typename P>
+__device__ __forceinline__ int real_tile(const P &p, int v) {
+  const uint32_t vu = (uint32_t)(p.vx + p.tiles_per_unit);
+  const uint32_t u = (uint32_t)v / vu;
+  const int o = v - (int)(u * vu) - p.vx;
+  return (int)u * p.tiles_per_unit + (o > 0 ? o : 0);
 }
 template <typename P>
 __device__ __forceinline__ int cta_first_tile(const P &p, int cta) {
-  return min(real_tile(p, (int64_t)cta * p.sched_v / p.sched_g), p.total_tiles);
+  return min(real_tile(p, sched_start(p, cta)), p.total_tiles);
 }
-// The CTA whose range holds virtual tile v: the largest c with c * sched_v / sched_g <= v.
+// The CTA whose range holds virtual tile v (0 <= v < V): the largest c < G with
+// sched_start(c) <= v.  A float estimate of v * G / V lies within two of it; the
+// monotone steps below end on the exact value.
 template <typename P>
-__device__ __forceinline__ int cta_of_vtile(const P &p, int64_t v) {
-  return (int)(((v + 1) * p.sched_g - 1) / p.sched_v);
+__device__ __forceinline__ int cta_of_vtile(const P &p, int v) {
+  int c = min(max(__float2int_rz((float)v * p.sched_inv), 0), p.sched_g - 1);
+  while (c > 0 && sched_start(p, c) > v) --c;
+  while (c + 1 < p.sched_g && sched_start(p, c + 1) <= v) ++c;
+  return c;
 }
 // CTAs whose range meets unit u: unit_first_cta(u) .. + unit_n_split(u) - 1.
 template <typename P>
 __device__ __forceinline__ int unit_first_cta(const P &p, int u) {
-  return cta_of_vtile(p, (int64_t)u * (p.vx + p.tiles_per_unit) + p.vx);
+  return cta_of_vtile(p, u * (p.vx + p.tiles_per_unit) + p.vx);
 }
 template <typename P>
 __device__ __forceinline__ int unit_n_split(const P &p, int u) {
-  const int64_t v0 = (int64_t)u * (p.vx + p.tiles_per_unit) + p.vx;
+  const int v0 = u * (p.vx + p.tiles_per_unit) + p.vx;
   return cta_of_vtile(p, v0 + p.tiles_per_unit - 1) - cta_of_vtile(p, v0) + 1;
+}
+
+// Host: the schedule's fields of a kernel's parameters (grid G CTAs over V virtual
+// tiles).  False when the 32-bit arithmetic above does not hold for these sizes.
+template <typename P>
+inline bool set_schedule(P &p, int grid, int64_t vtotal) {
+  if (grid < 1 || vtotal < grid || vtotal > INT32_MAX || (int64_t)grid * grid > INT32_MAX) return false;
+  p.sched_g = grid;
+  p.sched_v = (int)vtotal;
+  p.sched_q = (uint32_t)(vtotal / grid);
+  p.sched_r = (uint32_t)(vtotal % grid);
+  p.sched_ginv = 1.0f / (float)grid;
+  p.sched_inv = (float)grid / (float)vtotal;
+  return true;
 }
 
 template <typename P>

@@ -51,6 +51,8 @@ struct PvParams {
   const int32_t *seq_lens;
   int B, Hq, Hkv, L, gq, n_hg;
   int tiles_per_unit, sched_g, sched_v, vx, total_tiles, n_part;
+  uint32_t sched_q, sched_r;  // V / G and V % G (set_schedule)
+  float sched_ginv, sched_inv;  // 1 / G and G / V
   const uint32_t *qhl;
   const float *qsc;
   float *part;
@@ -442,7 +444,8 @@ cudaError_t launch_partial_pv(const tq_ctx *k, const tq_ctx *v, const uint8_t *k
   PvParams p{};
   p.kc = kc, p.vc = vc, p.seq_lens = seq_lens;
   p.B = s.B, p.Hq = s.Hq, p.Hkv = s.Hkv, p.L = s.L, p.gq = s.gq, p.n_hg = s.n_hg;
-  p.tiles_per_unit = s.tiles_per_unit, p.sched_g = s.grid, p.sched_v = s.vtotal, p.vx = s.vx;
+  p.tiles_per_unit = s.tiles_per_unit, p.vx = s.vx;
+  if (!set_schedule(p, s.grid, s.vtotal)) return cudaErrorInvalidValue;
   p.total_tiles = s.total_tiles, p.n_part = s.n_part;
   p.qhl = ws.qhl, p.qsc = ws.qsc, p.part = ws.partials, p.scores = scores_dbg;
   p.kc16[0] = k->f16.c16[0], p.kc16[1] = k->f16.c16[1];

@@ -91,6 +91,8 @@ struct PrefillParams {
   const int32_t *q_start;   // [B] position of each sequence's first chunk query
   int B, T, Hq, Hkv, L, gq, qpt, n_qt;
   int tiles_per_unit, sched_g, sched_v, vx, total_tiles, n_part;  // vx = 0: equal tile ranges
+  uint32_t sched_q, sched_r;  // V / G and V % G (set_schedule)
+  float sched_ginv, sched_inv;  // 1 / G and G / V
   const uint32_t *qhl;      // prepared q: [B*T*Hq][256 words], hi then lo fp16
   const float *qsc;         // [B*T*Hq][2] power-of-two scales
   float *part;              // [B*T*Hq][n_part][PARTIAL_FLOATS]
@@ -619,7 +621,8 @@ cudaError_t launch_prefill(const tq_ctx *k, const tq_ctx *v, const uint8_t *kc, 
   PrefillParams p{};
   p.kc = kc, p.vc = vc, p.q_start = q_start;
   p.B = s.B, p.T = s.T, p.Hq = s.Hq, p.Hkv = s.Hkv, p.L = s.L, p.gq = s.gq, p.qpt = s.qpt, p.n_qt = s.n_qt;
-  p.tiles_per_unit = s.tiles_per_unit, p.sched_g = s.grid, p.sched_v = s.total_tiles, p.vx = 0;
+  p.tiles_per_unit = s.tiles_per_unit, p.vx = 0;
+  if (!set_schedule(p, s.grid, s.total_tiles)) return cudaErrorInvalidValue;
   p.total_tiles = s.total_tiles, p.n_part = s.n_part;
   p.qhl = ws.qhl, p.qsc = ws.qsc, p.part = ws.partials;
   for (int i = 0; i < 2; ++i) {
