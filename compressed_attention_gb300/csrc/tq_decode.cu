@@ -88,6 +88,7 @@ struct PartialParams {
   float inv_vscale;   // 1 / (2^P_SHIFT * alpha_V)
   int32_t *unit_done;  // [units] CTAs that have written their partial of the unit
 };
+constexpr int PREFETCH_TILES = 4;  // tiles per CTA pulled into L2 before the previous kernel ends
 constexpr int FIN_MAX = 8;  // units one CTA may complete (the host fuses only below this)
 
 // Shared memory of one CTA, as offsets from the start of dynamic shared memory.
@@ -295,6 +296,25 @@ __global__ void __maxnreg__(128)
     // takes no part in the table fill: once the previous kernel is complete it starts the
     // first copies at once.
     named_arrive0<NTHREADS>();  // the barriers are set up
+    if (lane == 0) {
+      // The range's first tiles pulled into L2 before the wait on the previous kernel (in a
+      // decode loop, while the previous launch merges): a prefetch moves no data into the
+      // CTA, and the previous kernel's writes land in L2, so the copies after the wait read
+      // current rows.  Units taken at full length (seq_lens may still be written); every
+      // range lies inside the rows the copies below read.
+      int tp = cta_first_tile(p, cta), n_pre = 0;
+      Item ip;
+      while (n_pre < PREFETCH_TILES && next_item(p, cta, tp, ip)) {
+        const size_t row0 = (size_t)(ip.unit / p.n_hg) * p.L;
+        for (int j = ip.t0; j < ip.t1 && n_pre < PREFETCH_TILES && j * TILE < p.L; ++j, ++n_pre) {
+          const int nk = min(TILE, p.L - j * TILE);
+          const size_t ks = (row0 + (size_t)j * TILE) * KROW, vs = (row0 + (size_t)j * TILE) * VROW;
+          const size_t k0 = ks & ~(size_t)15, v0 = vs & ~(size_t)15;
+          bulk_prefetch_l2(p.kc + k0, (uint32_t)(((ks + (size_t)nk * KROW + 15) & ~(size_t)15) - k0));
+          bulk_prefetch_l2(p.vc + v0, (uint32_t)(((vs + (size_t)nk * VROW + 15) & ~(size_t)15) - v0));
+        }
+      }
+    }
     pdl_wait();
     if (lane == 0) {
       int ctr = 0, tt = cta_first_tile(p, cta), n_item = 0;
