@@ -105,10 +105,10 @@ def measured_tensor_peak():
     return FALLBACK_TENSOR_TFLOPS, "fallback"
 
 
-def profiled_traffic(profile_name, source):
-    """Per-launch DRAM bytes of a kernel from its committed ncu summary
-    (profiles/<profile_name>.md), or None when the kernel source changed since the
-    capture or there is no summary."""
+def profiled_fields(profile_name, source):
+    """The "- key: value" fields of a kernel's committed ncu summary
+    (profiles/<profile_name>.md), or None when the kernel source changed since the capture
+    or there is no summary."""
     path = os.path.join(ROOT, "profiles", profile_name + ".md")
     if not os.path.exists(path):
         return None
@@ -120,10 +120,35 @@ def profiled_traffic(profile_name, source):
     digest = hashlib.sha256(open(os.path.join(CSRC, source), "rb").read()).hexdigest()[:16]
     if fields.get("source_sha256_16") != digest:
         return None
+    return fields
+
+
+def profiled_number(profile_name, source, key):
+    fields = profiled_fields(profile_name, source)
     try:
-        return float(fields["traffic_bytes_per_launch"])
+        return float(fields[key]) if fields else None
     except (KeyError, ValueError):
         return None
+
+
+def profiled_traffic(profile_name, source):
+    """Per-launch DRAM bytes of a kernel from its committed ncu summary, or None."""
+    return profiled_number(profile_name, source, "traffic_bytes_per_launch")
+
+
+def issue_roofline(profile_name, source, kernel, avg_ms, clk, n_sms):
+    """Instruction-issue roofline of a kernel bound by issue rather than by DRAM: its warp
+    instructions per launch (ncu's smsp__inst_executed.sum in the committed summary, null
+    when the source changed since) over the live launch time, against one warp instruction
+    per cycle on each of the four schedulers of every SM at the SM clock sampled during the
+    timed region."""
+    inst = profiled_number(profile_name, source, "warp_instructions_per_launch")
+    mhz = clk.get("sm_mhz") or clk.get("sm_max_mhz")
+    peak = 4 * n_sms * mhz * 1e6 / 1e9 if mhz else None  # Ginst/s
+    achieved = inst / (avg_ms * 1e-3) / 1e9 if inst else None
+    return {"bound": "issue", "kernel": kernel, "achieved": achieved, "peak": peak, "unit": "Gwarp-inst/s",
+            "frac": achieved / peak if achieved and peak else None,
+            "warp_instructions_per_launch": inst, "sm_mhz": mhz, "sms": n_sms, "avg_launch_ms": avg_ms}
 
 
 class ClockSampler:
@@ -750,6 +775,8 @@ def run_decode(args, rank, world, dist):
                      "traffic": profiled_traffic("decode_partial_" + name, spec["source"]),
                      "algorithmic_bytes_per_launch": kv_bytes, "avg_launch_ms": merge_avg,
                      "launches": merge_launches},
+        "roofline_issue": issue_roofline("decode_partial_" + name, spec["source"], spec["kernel"], merge_avg, clk,
+                                         torch.cuda.get_device_properties(device).multi_processor_count),
         "roofline_stage_kernel": {"kernel": f"{spec['kernel']} (stage call: partials only, no merge)",
                                   "achieved": achieved_stage, "frac": achieved_stage / peak,
                                   "avg_launch_ms": part_avg},
@@ -974,6 +1001,8 @@ def run_write(args, rank, world, dist):
                      "frac": launch_bytes / (launch_avg * 1e-3) / 1e9 / peak,
                      "traffic": profiled_traffic(f"write_{fmt}_{rot}_write_chunk", source),
                      "algorithmic_bytes_per_launch": launch_bytes, "avg_launch_ms": launch_avg},
+        "roofline_issue": issue_roofline(f"write_{fmt}_{rot}_write_chunk", source, kernel, launch_avg, clk,
+                                         torch.cuda.get_device_properties(device).multi_processor_count),
         "cpu_baseline": cpu,
         "e2e": {"value": job_rate(alg_bytes, world, e2e_direct_step_ms) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_direct_step_ms,

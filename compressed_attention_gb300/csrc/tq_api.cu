@@ -695,6 +695,9 @@ tq_status tq_decode_step(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *n
     // the two writes and the q preparation are independent: one launch does all three
     e = launch_step_front(k_ctx, v_ctx, wk, wv, make_qprep_params(k_ctx, q, q_dtype, s, scale, w), cs);
     if (e != cudaSuccess) return cuda_fail(e, "decode step front launch");
+  } else if (n_rows > 0 && step_front_pv_eligible(k_ctx, v_ctx, wk, wv)) {
+    e = launch_step_front_pv(k_ctx, v_ctx, wk, wv, make_qprep_params(k_ctx, q, q_dtype, s, scale, w), cs);
+    if (e != cudaSuccess) return cuda_fail(e, "decode step front launch");
   } else {
     if (n_rows > 0) {
       if ((e = launch_write(k_ctx, wk, cs)) != cudaSuccess) return cuda_fail(e, "write kernel launch");
@@ -732,7 +735,9 @@ tq_status tq_decode_step_num_launches(const tq_ctx *k_ctx, const tq_ctx *v_ctx, 
   const int64_t dst_rows = (int64_t)B * Hkv * L;
   const WriteLaunch wk{nullptr, src_dtype, n_rows, D, nullptr, nullptr, dst_rows};
   const int attn = partial_fuses_combine(s) ? 2 : 3;
-  if (n_rows > 0 && step_front_eligible(k_ctx, v_ctx, wk, wk)) *n = attn;
+  const WriteLaunch wv{nullptr, src_dtype, n_rows, D, nullptr, nullptr, dst_rows};
+  if (n_rows > 0 && (step_front_eligible(k_ctx, v_ctx, wk, wv) || step_front_pv_eligible(k_ctx, v_ctx, wk, wv)))
+    *n = attn;
   else *n = attn + (n_rows > 0 ? 2 : 0);
   return TQ_OK;
 }

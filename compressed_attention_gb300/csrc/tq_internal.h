@@ -138,6 +138,10 @@ struct QprepParams;
 bool step_front_eligible(const tq_ctx *k, const tq_ctx *v, const WriteLaunch &wk, const WriteLaunch &wv);
 cudaError_t launch_step_front(const tq_ctx *k, const tq_ctx *v, const WriteLaunch &wk, const WriteLaunch &wv,
                               const QprepParams &q, cudaStream_t st);
+// prod3 keys, vgroup2 values: the same one-launch front (K rows by CTA, V rows by warp, q with its sketch)
+bool step_front_pv_eligible(const tq_ctx *k, const tq_ctx *v, const WriteLaunch &wk, const WriteLaunch &wv);
+cudaError_t launch_step_front_pv(const tq_ctx *k, const tq_ctx *v, const WriteLaunch &wk, const WriteLaunch &wv,
+                              const QprepParams &q, cudaStream_t st);
 bool write_tc_eligible(const tq_ctx *ctx, const WriteLaunch &w);
 cudaError_t launch_write_tc(const tq_ctx *ctx, const WriteLaunch &w, cudaStream_t st);
 

@@ -574,17 +574,18 @@ __device__ __forceinline__ void dense_row_prologue(const WriteParams &p, RowScra
   }
 }
 
-// After the wait: encode source row `row` into its slot (the whole CTA takes the same row).
-template <int FMT, int SRC>
-__device__ __forceinline__ void dense_row_body(const WriteParams &p, int64_t row, RowScratch &sc, int j,
-                                               const float4 (&rr)[D / 4]) {
-  constexpr int NB = (FMT == TQ_FMT_TURBO4) ? 15 : 7;
+// After the wait, the first part of a row's encoding (the whole CTA takes the same row):
+// its slot (-1 when out of range: flagged, nothing to write), the canonical norm n and
+// u = x / n in sc.u (thread j < 128 holds element j; every thread takes the barriers).
+template <int SRC>
+__device__ __forceinline__ int64_t dense_row_normalize(const WriteParams &p, int64_t row, RowScratch &sc, int j,
+                                                       float *n_out) {
   const int lane = j & 31;
   const bool act = j < D;
   const int64_t slot = p.row_ids ? p.row_ids[row] : row;
   if (slot < 0 || slot >= p.dst_rows) {  // the same for every thread of the CTA
     if (j == 0) atomicExch(p.status, (int32_t)DEVERR_ROW_OOB);
-    return;
+    return -1;
   }
   float x = 0.f;
   if (act) {
@@ -609,16 +610,36 @@ __device__ __forceinline__ void dense_row_body(const WriteParams &p, int64_t row
   const float n = sc.nsh;
   if (act) sc.u[j] = (n == 0.0f) ? 0.0f : __fdiv_rn(x, n);
   __syncthreads();
-  if (act) {
-    float y = 0.f;
+  *n_out = n;
+  return slot;
+}
+
+// y_j = (R u)_j from row j of R held in registers, in k order.
+__device__ __forceinline__ float row_times_u(const float4 (&rr)[D / 4], const float *u) {
+  float y = 0.f;
 #pragma unroll
-    for (int k4 = 0; k4 < D / 4; ++k4) {
-      const float4 r = rr[k4];
-      y = fmaf(r.x, sc.u[4 * k4], y);
-      y = fmaf(r.y, sc.u[4 * k4 + 1], y);
-      y = fmaf(r.z, sc.u[4 * k4 + 2], y);
-      y = fmaf(r.w, sc.u[4 * k4 + 3], y);
-    }
+  for (int k4 = 0; k4 < D / 4; ++k4) {
+    const float4 r = rr[k4];
+    y = fmaf(r.x, u[4 * k4], y);
+    y = fmaf(r.y, u[4 * k4 + 1], y);
+    y = fmaf(r.z, u[4 * k4 + 2], y);
+    y = fmaf(r.w, u[4 * k4 + 3], y);
+  }
+  return y;
+}
+
+// After the wait: encode source row `row` into its slot (the whole CTA takes the same row).
+template <int FMT, int SRC>
+__device__ __forceinline__ void dense_row_body(const WriteParams &p, int64_t row, RowScratch &sc, int j,
+                                               const float4 (&rr)[D / 4]) {
+  constexpr int NB = (FMT == TQ_FMT_TURBO4) ? 15 : 7;
+  const int lane = j & 31;
+  const bool act = j < D;
+  float n;
+  const int64_t slot = dense_row_normalize<SRC>(p, row, sc, j, &n);
+  if (slot < 0) return;
+  if (act) {
+    const float y = row_times_u(rr, sc.u);
     sc.ib[j] = (uint8_t)nearest<NB>(y, sc.grid, sc.sb);
   }
   __syncthreads();
@@ -637,6 +658,64 @@ __global__ void __launch_bounds__(D) k_write_dense_row(const WriteParams p) {
   pdl_trigger();
   pdl_wait();
   dense_row_body<FMT, SRC>(p, blockIdx.x, sc, threadIdx.x, rr);
+}
+
+// A prod3 row by one CTA (the decode step's few new keys): the same steps as the warp-per-row
+// kernel above with thread j < 128 on coordinate j.  y = R u from row j of R in registers,
+// x_tilde = R^T y_hat and z = S r from R and S^T staged in shared memory (column j read by
+// thread j: no bank conflicts).
+struct Prod3Scratch {
+  RowScratch base;
+  float yh[D];  // centroids of the indices
+  float r[D];   // residual u - R^T y_hat
+};
+
+template <int SRC>
+__device__ __forceinline__ void prod3_row_body(const WriteParams &p, int64_t row, Prod3Scratch &sc, const float *Rs,
+                                               const float *STs, int j, const float4 (&rr)[D / 4]) {
+  const int lane = j & 31, warp = j >> 5;
+  const bool act = j < D;
+  float n;
+  const int64_t slot = dense_row_normalize<SRC>(p, row, sc.base, j, &n);
+  if (slot < 0) return;
+  if (act) {
+    const uint32_t idx = nearest<3>(row_times_u(rr, sc.base.u), sc.base.grid, sc.base.sb);
+    sc.base.ib[j] = (uint8_t)idx;
+    sc.yh[j] = p.c[idx];
+  }
+  __syncthreads();
+  if (act) {
+    float xt = 0.f;  // (R^T y_hat)_j = sum_k R[k][j] y_hat_k
+#pragma unroll 8
+    for (int k = 0; k < D; ++k) xt = fmaf(Rs[k * D + j], sc.yh[k], xt);
+    sc.r[j] = sc.base.u[j] - xt;
+  }
+  __syncthreads();
+  if (act) {
+    float z = 0.f;  // (S r)_j = sum_k S^T[k][j] r_k
+#pragma unroll 8
+    for (int k = 0; k < D; ++k) z = fmaf(STs[k * D + j], sc.r[k], z);
+    const uint32_t sbits = __ballot_sync(FULL_MASK, z >= 0.0f);  // elements 32 warp + lane
+    uint8_t *buf = sc.base.buf;
+    if (lane == 0) reinterpret_cast<uint32_t *>(buf)[10 + warp] = sbits;
+    if (warp == 0) {  // gamma^2 in the warp kernel's order: lane l sums l + 32 m, then the lanes
+      float g2 = 0.f;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) g2 = fmaf(sc.r[lane + 32 * m], sc.r[lane + 32 * m], g2);
+#pragma unroll
+      for (int h = 16; h >= 1; h >>= 1) g2 += __shfl_xor_sync(FULL_MASK, g2, h);
+      if (lane == 0) {
+        reinterpret_cast<float *>(buf)[0] = n;
+        reinterpret_cast<float *>(buf)[1] = sqrtf(g2);
+      }
+    }
+    if (j < 32) {
+      const uint32_t w4 = *reinterpret_cast<const uint32_t *>(sc.base.ib + 4 * j);
+      buf[8 + j] = (uint8_t)((w4 & 3) | (((w4 >> 8) & 3) << 2) | (((w4 >> 16) & 3) << 4) | (((w4 >> 24) & 3) << 6));
+    }
+  }
+  __syncthreads();
+  if (j < 14) reinterpret_cast<uint32_t *>(p.dst + slot * 56)[j] = reinterpret_cast<const uint32_t *>(sc.base.buf)[j];
 }
 
 // ------------------------------------------------ decode step front (tq_decode_step)
@@ -679,50 +758,89 @@ __global__ void __launch_bounds__(QWARPS * 32) k_step_front(const StepFrontParam
 }
 
 // ------------------------------------------------------------------ V group quant
+// One vgroup2 row by one warp: per 32-element group the fp16 min z and step s = (max - min) / 3,
+// indices round((x - z) / s) clamped to 0..3 (48-byte record: 32 index bytes, then {s, z}
+// per group).
+template <int SRC>
+__device__ __forceinline__ void vgroup_row(const WriteParams &p, int64_t row, int lane, uint8_t *buf) {
+  int64_t slot;
+  if (!slot_of(p, row, lane, &slot)) return;
+  float x[4];
+  load4<SRC>(p.src, row, p.stride, lane, x);
+  float mn = fminf(fminf(x[0], x[1]), fminf(x[2], x[3]));
+  float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+#pragma unroll
+  for (int h = 1; h <= 4; h <<= 1) {  // lanes 8g..8g+7 hold group g
+    mn = fminf(mn, __shfl_xor_sync(FULL_MASK, mn, h));
+    mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, h));
+  }
+  mn = __fadd_rn(mn, 0.0f);
+  mx = __fadd_rn(mx, 0.0f);
+  const float s32 = __fdiv_rn(__fsub_rn(mx, mn), 3.0f);
+  const __half sh = __float2half_rn(s32);
+  const __half zh = __float2half_rn(mn);
+  const float s = __half2float(sh), z = __half2float(zh);
+  uint32_t byte = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    float c = 0.0f;
+    if (s > 0.0f) c = fminf(fmaxf(rintf(__fdiv_rn(__fsub_rn(x[e], z), s)), 0.0f), 3.0f);
+    byte |= ((uint32_t)c) << (2 * e);
+  }
+  buf[lane] = (uint8_t)byte;
+  if ((lane & 7) == 0) {
+    const int g = lane >> 3;
+    *reinterpret_cast<__half *>(buf + 32 + 4 * g) = sh;
+    *reinterpret_cast<__half *>(buf + 34 + 4 * g) = zh;
+  }
+  __syncwarp();
+  if (lane < 12)
+    reinterpret_cast<uint32_t *>(p.dst + slot * 48)[lane] =
+        reinterpret_cast<const uint32_t *>(buf)[lane];
+  __syncwarp();
+}
+
 template <int SRC>
 __global__ void __launch_bounds__(WARPS * 32) k_write_vgroup(const WriteParams p) {
   pdl_trigger();
   pdl_wait();
   __shared__ __align__(16) uint8_t rowbuf[WARPS][ROWBUF];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint8_t *buf = rowbuf[warp];
-  for (int64_t row = (int64_t)blockIdx.x * WARPS + warp; row < p.n_rows;
-       row += (int64_t)gridDim.x * WARPS) {
-    int64_t slot;
-    if (!slot_of(p, row, lane, &slot)) continue;
-    float x[4];
-    load4<SRC>(p.src, row, p.stride, lane, x);
-    float mn = fminf(fminf(x[0], x[1]), fminf(x[2], x[3]));
-    float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-#pragma unroll
-    for (int h = 1; h <= 4; h <<= 1) {  // lanes 8g..8g+7 hold group g
-      mn = fminf(mn, __shfl_xor_sync(FULL_MASK, mn, h));
-      mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, h));
-    }
-    mn = __fadd_rn(mn, 0.0f);
-    mx = __fadd_rn(mx, 0.0f);
-    const float s32 = __fdiv_rn(__fsub_rn(mx, mn), 3.0f);
-    const __half sh = __float2half_rn(s32);
-    const __half zh = __float2half_rn(mn);
-    const float s = __half2float(sh), z = __half2float(zh);
-    uint32_t byte = 0;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      float c = 0.0f;
-      if (s > 0.0f) c = fminf(fmaxf(rintf(__fdiv_rn(__fsub_rn(x[e], z), s)), 0.0f), 3.0f);
-      byte |= ((uint32_t)c) << (2 * e);
-    }
-    buf[lane] = (uint8_t)byte;
-    if ((lane & 7) == 0) {
-      const int g = lane >> 3;
-      *reinterpret_cast<__half *>(buf + 32 + 4 * g) = sh;
-      *reinterpret_cast<__half *>(buf + 34 + 4 * g) = zh;
-    }
-    __syncwarp();
-    if (lane < 12)
-      reinterpret_cast<uint32_t *>(p.dst + slot * 48)[lane] =
-          reinterpret_cast<const uint32_t *>(buf)[lane];
-    __syncwarp();
+  for (int64_t row = (int64_t)blockIdx.x * WARPS + warp; row < p.n_rows; row += (int64_t)gridDim.x * WARPS)
+    vgroup_row<SRC>(p, row, lane, rowbuf[warp]);
+}
+
+// Decode step front for prod3 keys and vgroup2 values: CTAs 0 .. n - 1 encode the n new K
+// rows (one CTA per row, R and S^T staged before the wait), the next ceil(n / QWARPS) CTAs
+// the V rows (one warp per row), the remaining CTAs prepare q with its QJL sketch.
+constexpr size_t FRONT_PV_SMEM = 2 * (size_t)D * D * sizeof(float) + sizeof(Prod3Scratch);
+
+template <int SRC>
+__global__ void __launch_bounds__(QWARPS * 32) k_step_front_pv(const StepFrontParams sp) {
+  extern __shared__ __align__(16) float fsm[];
+  const int c = blockIdx.x;
+  const int v_ctas = (sp.n_rows + QWARPS - 1) / QWARPS;
+  if (c < sp.n_rows) {
+    float *Rs = fsm, *STs = fsm + D * D;
+    Prod3Scratch &sc = *reinterpret_cast<Prod3Scratch *>(fsm + 2 * D * D);
+    float4 rr[D / 4];
+    dense_row_prologue<3>(sp.wk, sc.base, threadIdx.x, rr);
+    stage_matrix(Rs, sp.wk.pi);
+    stage_matrix(STs, sp.wk.St);
+    pdl_trigger();
+    pdl_wait();
+    prod3_row_body<SRC>(sp.wk, c, sc, Rs, STs, threadIdx.x, rr);
+  } else if (c < sp.n_rows + v_ctas) {
+    pdl_trigger();
+    pdl_wait();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)(c - sp.n_rows) * QWARPS + warp;
+    if (row < sp.n_rows) vgroup_row<SRC>(sp.wv, row, lane, reinterpret_cast<uint8_t *>(fsm) + warp * ROWBUF);
+  } else {
+    pdl_trigger();
+    stage_matrix(fsm, sp.q.rt);
+    pdl_wait();
+    prepare_q_body<true>(sp.q, c - sp.n_rows - v_ctas, sp.q_ctas, fsm);
   }
 }
 
@@ -832,6 +950,27 @@ bool step_front_eligible(const tq_ctx *k, const tq_ctx *v, const WriteLaunch &wk
            w.n_rows >= 1 && w.n_rows <= SMALL_ROWS && !write_tc_eligible(c, w);
   };
   return ok(k, wk) && ok(v, wv) && wk.n_rows == wv.n_rows && wk.src_dtype == wv.src_dtype;
+}
+
+bool step_front_pv_eligible(const tq_ctx *k, const tq_ctx *v, const WriteLaunch &wk, const WriteLaunch &wv) {
+  return k->fmt == TQ_FMT_PROD3 && v->fmt == TQ_FMT_VGROUP2 && wk.n_rows >= 1 && wk.n_rows <= SMALL_ROWS &&
+         wk.n_rows == wv.n_rows && wk.src_dtype == wv.src_dtype;
+}
+
+cudaError_t launch_step_front_pv(const tq_ctx *k, const tq_ctx *v, const WriteLaunch &wk, const WriteLaunch &wv,
+                                 const QprepParams &q, cudaStream_t st) {
+  StepFrontParams sp{};
+  sp.wk = write_params(k, wk);
+  sp.wv = write_params(v, wv);
+  sp.q = q;
+  sp.n_rows = (int)wk.n_rows;
+  sp.q_ctas = (q.n_q + QWARPS - 1) / QWARPS;
+  static_assert(FRONT_PV_SMEM >= QPREP_SMEM && FRONT_PV_SMEM >= QWARPS * ROWBUF, "one dynamic area for every role");
+  auto kern = wk.src_dtype == TQ_DTYPE_BF16 ? k_step_front_pv<TQ_DTYPE_BF16> : k_step_front_pv<TQ_DTYPE_F32>;
+  cudaError_t e = kernel_smem_attr((const void *)kern, (int)FRONT_PV_SMEM);
+  if (e != cudaSuccess) return e;
+  const int grid = sp.n_rows + (sp.n_rows + QWARPS - 1) / QWARPS + sp.q_ctas;
+  return launch_pdl(kern, dim3(grid), dim3(QWARPS * 32), FRONT_PV_SMEM, st, sp);
 }
 
 cudaError_t launch_step_front(const tq_ctx *k, const tq_ctx *v, const WriteLaunch &wk, const WriteLaunch &wv,

@@ -3,8 +3,9 @@ the compressed caches and attends over the updated caches.
 
 The call must leave exactly the cache bytes and give the outputs that the three
 separate calls give (SET_ROWS of K, SET_ROWS of V, decode attention), whichever
-launch plan it takes: the one-launch front (dense-rotation turbo4 / turbo3, few rows)
-or the separate kernels (WHT rotation, prod3 keys, vgroup2 values).  For the turbo
+launch plan it takes: the one-launch front (at most 256 new rows: dense-rotation turbo4 /
+turbo3, or prod3 keys with vgroup2 values in any rotation) or the separate kernels (WHT
+rotation of the turbo formats, more rows).  For the turbo
 formats the outputs are also checked against the oracle's attention over the caches
 the call wrote, dequantized by the oracle."""
 
@@ -60,7 +61,10 @@ STEP_CASES = [
     ("turbo4", "turbo4", "dense", "bf16", 32, 64, 8, 64, True),    # 256 rows, the most the front takes
     ("turbo4", "turbo4", "dense", "bf16", 33, 64, 8, 64, False),   # 264 rows
     ("turbo4", "turbo4", "wht", "bf16", 2, 8, 2, 500, False),
-    ("prod3", "vgroup2", "dense", "bf16", 2, 12, 2, 400, False),
+    ("prod3", "vgroup2", "dense", "bf16", 2, 12, 2, 400, True),
+    ("prod3", "vgroup2", "wht", "f32", 3, 12, 3, 300, True),
+    ("prod3", "vgroup2", "dense", "bf16", 32, 64, 8, 64, True),    # 256 rows
+    ("prod3", "vgroup2", "dense", "bf16", 33, 64, 8, 64, False),   # 264 rows: the separate kernels
 ]
 
 
