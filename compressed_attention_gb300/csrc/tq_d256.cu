@@ -7,18 +7,22 @@
 // own stored norm.
 //
 // Kernels:
-//   k_write_d256    SET_ROWS: one warp per row, lane l holding elements 8l .. 8l+7 (the
-//                   canonical norm tree: a balanced pairwise sum in the lane, then the
-//                   butterfly over the lanes; IEEE division; the Hadamard butterfly with
-//                   stages 1, 2, 4 in the lane and 8 .. 128 across lanes; x 1/16).
+//   k_write_d256    SET_ROWS, lane l of a warp holding elements 8l .. 8l+7 (the canonical
+//                   norm tree: a balanced pairwise sum in the lane, then the butterfly over
+//                   the lanes; IEEE division).  Randomized Hadamard: one warp per row, the
+//                   butterfly with stages 1, 2, 4 in the lane and 8 .. 128 across lanes,
+//                   x 1/16.  Dense Pi: one CTA per row, the 256 x 256 product split over
+//                   its eight warps (32 rows of R^T each, summed in shared memory).
 //   k_dequant_d256  reconstruction, one warp per row.
-//   k_prepare_q256  q_rot = R q, scaled and split into fp16 hi + lo operands.
+//   k_prepare_q256  q_rot = R q (one CTA per query, the product split as above), scaled
+//                   and split into fp16 hi + lo operands.
 //   k_partial_d256  split-K decode: CTA (unit, split) of four warps, each taking 16 keys at
 //                   a time; scores and PV as m16n8k16 MMAs with table-decoded fp16
 //                   centroids, per-block norms on the scores, the largest value norm in the
 //                   softmax exponent and each block's ratio to it in that block's
 //                   probability operand.
-//   k_combine_d256  merge of the splits and the un-rotation R^T o.
+//   k_combine_d256  merge of the splits (one CTA per head, the splits shared by its warps)
+//                   and the un-rotation R^T o (the product split as above).
 #include <cuda_fp16.h>
 #include <math.h>
 
@@ -83,6 +87,38 @@ __device__ __forceinline__ uint32_t count_below(float y, const float *b) {
   return n;
 }
 
+// y = M^T x for a 256 x 256 fp32 matrix (row k at mt + 256 k) and x in shared memory, by
+// the CTA's eight warps: warp w sums rows 32w .. 32w+31 (their loads issued eight rows at a
+// time), lane l outputs 8l .. 8l+7; the slices meet in red[8][256] and every warp sums them
+// in warp order.  Ends with a barrier after which red and x may be rewritten only after
+// another barrier.
+__device__ __forceinline__ void cta_matvec256(const float *mt, const float *xs, float (*red)[D256], int warp,
+                                              int lane, float (&y)[8]) {
+#pragma unroll
+  for (int e = 0; e < 8; ++e) y[e] = 0.f;
+#pragma unroll 8
+  for (int i = 0; i < 32; ++i) {
+    const int k = 32 * warp + i;
+    const float xk = xs[k];
+    const float4 *r4 = reinterpret_cast<const float4 *>(mt + (size_t)k * D256 + 8 * lane);
+    const float4 a = __ldg(r4), b = __ldg(r4 + 1);
+    y[0] = fmaf(a.x, xk, y[0]), y[1] = fmaf(a.y, xk, y[1]), y[2] = fmaf(a.z, xk, y[2]), y[3] = fmaf(a.w, xk, y[3]);
+    y[4] = fmaf(b.x, xk, y[4]), y[5] = fmaf(b.y, xk, y[5]), y[6] = fmaf(b.z, xk, y[6]), y[7] = fmaf(b.w, xk, y[7]);
+  }
+  float4 *r4 = reinterpret_cast<float4 *>(&red[warp][8 * lane]);
+  r4[0] = make_float4(y[0], y[1], y[2], y[3]);
+  r4[1] = make_float4(y[4], y[5], y[6], y[7]);
+  __syncthreads();
+#pragma unroll
+  for (int e = 0; e < 8; ++e) y[e] = 0.f;
+#pragma unroll
+  for (int w = 0; w < WARPS2; ++w) {
+    const float4 *q4 = reinterpret_cast<const float4 *>(&red[w][8 * lane]);
+    const float4 a = q4[0], b = q4[1];
+    y[0] += a.x, y[1] += a.y, y[2] += a.z, y[3] += a.w, y[4] += b.x, y[5] += b.y, y[6] += b.z, y[7] += b.w;
+  }
+}
+
 template <int SRC, bool DENSE>
 __global__ void __launch_bounds__(WARPS2 * 32) k_write_d256(const Write256 p) {
   __shared__ float sb[16];
@@ -91,6 +127,41 @@ __global__ void __launch_bounds__(WARPS2 * 32) k_write_d256(const Write256 p) {
   __syncthreads();
   pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (DENSE) {
+    // one CTA per row: warp 0 normalises it, the eight warps share the rotation, warp 0
+    // quantizes and packs
+    __shared__ __align__(16) float us[D256];
+    __shared__ __align__(16) float red[WARPS2][D256];
+    __shared__ float nsh;
+    for (int64_t row = blockIdx.x; row < p.n_rows; row += gridDim.x) {
+      const int64_t slot = p.row_ids ? p.row_ids[row] : row;  // the same for the whole CTA
+      if (slot < 0 || slot >= p.dst_rows) {
+        if (threadIdx.x == 0) atomicExch(p.status, (int32_t)DEVERR_ROW_OOB);
+        continue;
+      }
+      if (warp == 0) {
+        float v[8];
+        load8(p.src, SRC, row, p.stride, lane, v);
+        const float n = norm256(v);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) us[8 * lane + e] = (n == 0.0f) ? 0.0f : __fdiv_rn(v[e], n);
+        if (lane == 0) nsh = n;
+      }
+      __syncthreads();
+      float y[8];
+      cta_matvec256(p.rt, us, red, warp, lane, y);
+      if (warp == 0) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) word |= count_below(y[e], sb) << (4 * e);
+        uint8_t *blk = p.dst + slot * ROW256 + 68 * (lane >> 4);
+        reinterpret_cast<uint32_t *>(blk + 4)[lane & 15] = word;
+        if ((lane & 15) == 0) *reinterpret_cast<float *>(blk) = nsh;
+      }
+      __syncthreads();  // us, red and nsh free for the next row
+    }
+    return;
+  }
   for (int64_t row = (int64_t)blockIdx.x * WARPS2 + warp; row < p.n_rows; row += (int64_t)gridDim.x * WARPS2) {
     const int64_t slot = p.row_ids ? p.row_ids[row] : row;
     if (slot < 0 || slot >= p.dst_rows) {
@@ -103,18 +174,7 @@ __global__ void __launch_bounds__(WARPS2 * 32) k_write_d256(const Write256 p) {
 #pragma unroll
     for (int e = 0; e < 8; ++e) v[e] = (n == 0.0f) ? 0.0f : __fdiv_rn(v[e], n);
     float y[8];
-    if (DENSE) {
-      // y_j = sum_k R[j][k] u_k = sum_k R^T[k][j] u_k: lane l takes j = 8l .. 8l+7
-#pragma unroll
-      for (int e = 0; e < 8; ++e) y[e] = 0.f;
-      for (int k = 0; k < D256; ++k) {
-        const float uk = __shfl_sync(FULL_MASK, v[k & 7], k >> 3);
-        const float4 *r4 = reinterpret_cast<const float4 *>(p.rt + (size_t)k * D256 + 8 * lane);
-        const float4 a = r4[0], b = r4[1];
-        y[0] = fmaf(a.x, uk, y[0]), y[1] = fmaf(a.y, uk, y[1]), y[2] = fmaf(a.z, uk, y[2]), y[3] = fmaf(a.w, uk, y[3]);
-        y[4] = fmaf(b.x, uk, y[4]), y[5] = fmaf(b.y, uk, y[5]), y[6] = fmaf(b.z, uk, y[6]), y[7] = fmaf(b.w, uk, y[7]);
-      }
-    } else {
+    {
       // signs (exact), the butterfly stages h = 1, 2, 4 in the lane, 8 .. 128 across lanes
       // (the lower element of a pair keeps a + b, the upper a - b), then x RN(1/16) = 1/16
       const uint32_t sw = p.neg[lane >> 2] >> (8 * (lane & 3));
@@ -177,6 +237,7 @@ __global__ void __launch_bounds__(WARPS2 * 32) k_dequant_d256(const Dequant256 p
       // x_j = sum_k R[k][j] y_k: lane l takes j = 8l .. 8l+7 from row k of R
 #pragma unroll
       for (int e = 0; e < 8; ++e) x[e] = 0.f;
+#pragma unroll 16
       for (int k = 0; k < D256; ++k) {
         const float yk = __shfl_sync(FULL_MASK, y[k & 7], k >> 3);
         const float4 *r4 = reinterpret_cast<const float4 *>(p.r + (size_t)k * D256 + 8 * lane);
@@ -205,35 +266,36 @@ struct Prep256 {
 };
 
 __global__ void __launch_bounds__(WARPS2 * 32) k_prepare_q256(const Prep256 p) {
+  // one CTA per query: warp 0 loads it, the eight warps share q_rot = R q, warp 0 splits
+  __shared__ __align__(16) float xs[D256];
+  __shared__ __align__(16) float red[WARPS2][D256];
   pdl_trigger();
   pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qi = blockIdx.x * WARPS2 + warp;
+  const int qi = blockIdx.x;
   if (qi >= p.n_q) return;
-  float x[8];
-  if (p.q_dtype == TQ_DTYPE_F32) {
-    load8(p.q, TQ_DTYPE_F32, qi, D256, lane, x);
-  } else if (p.q_dtype == TQ_DTYPE_BF16) {
-    load8(p.q, TQ_DTYPE_BF16, qi, D256, lane, x);
-  } else {
-    const uint4 w = reinterpret_cast<const uint4 *>(static_cast<const __half *>(p.q) + (size_t)qi * D256)[lane];
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+  if (warp == 0) {
+    float x[8];
+    if (p.q_dtype == TQ_DTYPE_F32) {
+      load8(p.q, TQ_DTYPE_F32, qi, D256, lane, x);
+    } else if (p.q_dtype == TQ_DTYPE_BF16) {
+      load8(p.q, TQ_DTYPE_BF16, qi, D256, lane, x);
+    } else {
+      const uint4 w = reinterpret_cast<const uint4 *>(static_cast<const __half *>(p.q) + (size_t)qi * D256)[lane];
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&ws[i]));
-      x[2 * i] = f.x, x[2 * i + 1] = f.y;
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&ws[i]));
+        x[2 * i] = f.x, x[2 * i + 1] = f.y;
+      }
     }
-  }
-  float y[8];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) y[e] = 0.f;
-  for (int k = 0; k < D256; ++k) {
-    const float xk = __shfl_sync(FULL_MASK, x[k & 7], k >> 3);
-    const float4 *r4 = reinterpret_cast<const float4 *>(p.rt + (size_t)k * D256 + 8 * lane);
-    const float4 a = r4[0], b = r4[1];
-    y[0] = fmaf(a.x, xk, y[0]), y[1] = fmaf(a.y, xk, y[1]), y[2] = fmaf(a.z, xk, y[2]), y[3] = fmaf(a.w, xk, y[3]);
-    y[4] = fmaf(b.x, xk, y[4]), y[5] = fmaf(b.y, xk, y[5]), y[6] = fmaf(b.z, xk, y[6]), y[7] = fmaf(b.w, xk, y[7]);
+    for (int e = 0; e < 8; ++e) xs[8 * lane + e] = x[e];
   }
+  __syncthreads();
+  float y[8];
+  cta_matvec256(p.rt, xs, red, warp, lane, y);
+  if (warp != 0) return;
   float amax = 0.f;
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
@@ -522,20 +584,25 @@ struct Comb256 {
   float *out;
 };
 
-// One warp per head: m* = max m_s, l* = sum l_s 2^(m_s - m*), o = sum acc_s 2^(m_s - m*) / l*
-// in the rotated basis (lane l: dims 8l .. 8l+7), then out = R^T o.
+// One CTA per head: warp w merges splits w, w + 8, ... (m_w = max m_s, l_w, o_w with
+// weights 2^(m_s - m_w)); the eight states meet in shared memory (m* = max m_w, l* = sum
+// l_w 2^(m_w - m*), o = sum o_w 2^(m_w - m*) / l*, in the rotated basis); the eight warps
+// then share out = R^T o.
 __global__ void __launch_bounds__(WARPS2 * 32) k_combine_d256(const Comb256 p) {
+  __shared__ __align__(16) float os[D256];
+  __shared__ __align__(16) float red[WARPS2][D256];
+  __shared__ float mws[WARPS2], lws[WARPS2];
   pdl_trigger();
   pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.x * WARPS2 + warp;
+  const int bh = blockIdx.x;
   if (bh >= p.n_heads) return;
   const float *part = p.part + (size_t)bh * p.n_split * PARTIAL256;
   float ms = -INFINITY;
-  for (int s = 0; s < p.n_split; ++s)
+  for (int s = warp; s < p.n_split; s += WARPS2)
     if (part[(size_t)s * PARTIAL256 + 1] > 0.f) ms = fmaxf(ms, part[(size_t)s * PARTIAL256]);
   float l = 0.f, o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int s = 0; s < p.n_split; ++s) {
+  for (int s = warp; s < p.n_split; s += WARPS2) {
     const float *ps = part + (size_t)s * PARTIAL256;
     if (!(ps[1] > 0.f)) continue;
     const float w = exp2f(ps[0] - ms);
@@ -545,17 +612,32 @@ __global__ void __launch_bounds__(WARPS2 * 32) k_combine_d256(const Comb256 p) {
     o[0] = fmaf(w, a.x, o[0]), o[1] = fmaf(w, a.y, o[1]), o[2] = fmaf(w, a.z, o[2]), o[3] = fmaf(w, a.w, o[3]);
     o[4] = fmaf(w, c.x, o[4]), o[5] = fmaf(w, c.y, o[5]), o[6] = fmaf(w, c.z, o[6]), o[7] = fmaf(w, c.w, o[7]);
   }
-  const float f = l > 0.f ? p.inv_vscale / l : 0.f;
+  if (lane == 0) mws[warp] = ms, lws[warp] = l;
+  float4 *r4 = reinterpret_cast<float4 *>(&red[warp][8 * lane]);
+  r4[0] = make_float4(o[0], o[1], o[2], o[3]);
+  r4[1] = make_float4(o[4], o[5], o[6], o[7]);
+  __syncthreads();
+  if (warp == 0) {
+    float mx = -INFINITY;
 #pragma unroll
-  for (int e = 0; e < 8; ++e) o[e] *= f;
-  float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int k = 0; k < D256; ++k) {
-    const float ok = __shfl_sync(FULL_MASK, o[k & 7], k >> 3);
-    const float4 *r4 = reinterpret_cast<const float4 *>(p.r + (size_t)k * D256 + 8 * lane);
-    const float4 a = r4[0], c = r4[1];
-    x[0] = fmaf(a.x, ok, x[0]), x[1] = fmaf(a.y, ok, x[1]), x[2] = fmaf(a.z, ok, x[2]), x[3] = fmaf(a.w, ok, x[3]);
-    x[4] = fmaf(c.x, ok, x[4]), x[5] = fmaf(c.y, ok, x[5]), x[6] = fmaf(c.z, ok, x[6]), x[7] = fmaf(c.w, ok, x[7]);
+    for (int w = 0; w < WARPS2; ++w) mx = fmaxf(mx, mws[w]);
+    float lt = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int w = 0; w < WARPS2; ++w) {
+      if (mws[w] == -INFINITY) continue;
+      const float f = exp2f(mws[w] - mx);
+      lt += f * lws[w];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = fmaf(f, red[w][8 * lane + e], acc[e]);
+    }
+    const float f = lt > 0.f ? p.inv_vscale / lt : 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) os[8 * lane + e] = acc[e] * f;
   }
+  __syncthreads();
+  float x[8];
+  cta_matvec256(p.r, os, red, warp, lane, x);
+  if (warp != 0) return;
   float4 *o4 = reinterpret_cast<float4 *>(p.out + (size_t)bh * D256 + 8 * lane);
   o4[0] = make_float4(x[0], x[1], x[2], x[3]);
   o4[1] = make_float4(x[4], x[5], x[6], x[7]);
@@ -576,7 +658,8 @@ cudaError_t launch_write_d256(const tq_ctx *ctx, const WriteLaunch &w, cudaStrea
   for (int i = 0; i < 8; ++i) p.neg[i] = ctx->wht_neg[i];
   for (int k = 0; k < 15; ++k) p.b[k] = ctx->cb.b[k];
   const bool dense = ctx->p.rotation == TQ_ROT_DENSE, bf16 = w.src_dtype == TQ_DTYPE_BF16;
-  const dim3 grid(grid_rows(ctx, w.n_rows, WARPS2)), block(WARPS2 * 32);
+  // dense: one CTA per row (the rotation split over its warps); WHT: one warp per row
+  const dim3 grid(grid_rows(ctx, w.n_rows, dense ? 1 : WARPS2)), block(WARPS2 * 32);
   if (dense)
     return bf16 ? launch_pdl(k_write_d256<TQ_DTYPE_BF16, true>, grid, block, 0, st, p)
                 : launch_pdl(k_write_d256<TQ_DTYPE_F32, true>, grid, block, 0, st, p);
@@ -634,7 +717,7 @@ cudaError_t launch_prepare_q256(const tq_ctx *k, const void *q, int q_dtype, con
   p.q = q, p.q_dtype = q_dtype, p.n_q = s.B * s.Hq, p.rt = k->d_pit;
   p.mul = LOG2E * scale / k->f16.alpha;
   p.qhl = w.qhl, p.qsc = w.qsc;
-  return launch_pdl(k_prepare_q256, dim3((p.n_q + WARPS2 - 1) / WARPS2), dim3(WARPS2 * 32), 0, st, p);
+  return launch_pdl(k_prepare_q256, dim3(p.n_q), dim3(WARPS2 * 32), 0, st, p);
 }
 
 cudaError_t launch_partial_d256(const tq_ctx *k, const tq_ctx *v, const uint8_t *kc, const uint8_t *vc,
@@ -658,7 +741,7 @@ cudaError_t launch_combine_d256(const tq_ctx *v, const D256Shape &s, float *out,
   p.part = w.partials, p.n_heads = s.B * s.Hq, p.n_split = s.n_split, p.r = v->d_pi;
   p.inv_vscale = 1.0f / (exp2f(P_SHIFT) * v->f16.alpha);
   p.out = out;
-  return launch_pdl(k_combine_d256, dim3((p.n_heads + WARPS2 - 1) / WARPS2), dim3(WARPS2 * 32), 0, st, p);
+  return launch_pdl(k_combine_d256, dim3(p.n_heads), dim3(WARPS2 * 32), 0, st, p);
 }
 
 }  // namespace tq
