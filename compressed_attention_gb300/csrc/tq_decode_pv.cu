@@ -31,8 +31,8 @@ namespace tq {
 
 namespace {
 
-constexpr int CW = 11;                 // consumer warps, 16 keys each per tile; with the
-                                       // producer 12 warps = 3 per scheduler at 168 registers
+constexpr int CW = 15;                 // consumer warps, 16 keys each per tile; with the
+                                       // producer 16 warps = 4 per scheduler at 128 registers
 constexpr int NTH = (CW + 1) * 32;     // + one producer warp; one CTA per SM
 static_assert(16 * CW == PV_TILE, "a tile is 16 keys per consumer warp");
 constexpr int NST = 4;                 // pipeline stages
@@ -62,10 +62,12 @@ struct PvParams {
 };
 
 struct PvHead {
-  float osm[CW][8][D];  // per-warp O of 8 heads (zero terms folded in), for the merge
+  float osm[CW][4][D];  // per-warp O of 4 heads (zero terms folded in), for the merge
+  uint4 qf[2][8][32];   // the item's q (0) and sketch (1) A fragments: k-step, lane
   float mw[CW][8];
   float lw[CW][8];
   float zw[CW][8][4];
+  float mh[8], lh[8];   // an item's per-head max and sum over the warps
   uint64_t full[NST];
   uint64_t empty[NST];
   int abort_flag;
@@ -101,7 +103,7 @@ __device__ __forceinline__ void lut2(uint32_t base, uint32_t off, uint32_t &w0, 
 }
 
 template <bool SCORES, bool FIXED>
-__global__ void __maxnreg__(168) k_partial_pv(const PvParams p) {
+__global__ void __maxnreg__(128) k_partial_pv(const PvParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   PvHead &sm = *reinterpret_cast<PvHead *>(smem_raw);
   uint32_t *mse_lut = reinterpret_cast<uint32_t *>(smem_raw + MSE_OFF);
@@ -209,32 +211,27 @@ __global__ void __maxnreg__(168) k_partial_pv(const PvParams p) {
     const size_t unit_row0 = (size_t)bk * p.L;
 
     // q and the sketch S q as A operands: rows g / g+8 = fp16 hi / lo of head g; k-step
-    // s covers dims 32t + 4s .. 32t + 4s + 3 in lane t.
-    uint32_t qa[8][4], qq[8][4];
+    // s covers dims 32t + 4s .. 32t + 4s + 3 in lane t.  The fragments of the item are
+    // written to shared memory once by all consumer warps (the previous item's merge ended
+    // with their barrier) and read at each k-step.
+    for (int i = threadIdx.x; i < 2 * 8 * 32; i += CW * 32) {
+      const int which = i >> 8, st = (i >> 5) & 7, ln = i & 31;
+      const int fg = ln >> 2, ft = ln & 3, v = st >> 1, h = st & 1;
+      uint4 f = make_uint4(0u, 0u, 0u, 0u);
+      if (fg < G) {
+        const uint4 *qw = reinterpret_cast<const uint4 *>(p.qhl + (size_t)(b * p.Hq + head0 + fg) * 256);
+        const uint4 hi = qw[32 * which + 4 * ft + v], lo = qw[32 * which + 16 + 4 * ft + v];
+        const uint32_t hw[4] = {hi.x, hi.y, hi.z, hi.w}, lw[4] = {lo.x, lo.y, lo.z, lo.w};
+        f = make_uint4(hw[2 * h], lw[2 * h], hw[2 * h + 1], lw[2 * h + 1]);
+      }
+      sm.qf[which][st][ln] = f;
+    }
     float qsm = 0.f, qsq = 0.f;
     if (g < G) {
-      const uint4 *qw = reinterpret_cast<const uint4 *>(p.qhl + (size_t)(b * p.Hq + head0 + g) * 256);
-#pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        const uint4 mh = qw[4 * t + v], ml = qw[16 + 4 * t + v];
-        const uint4 sh = qw[32 + 4 * t + v], sl = qw[48 + 4 * t + v];
-        const uint32_t mhw[4] = {mh.x, mh.y, mh.z, mh.w}, mlw[4] = {ml.x, ml.y, ml.z, ml.w};
-        const uint32_t shw[4] = {sh.x, sh.y, sh.z, sh.w}, slw[4] = {sl.x, sl.y, sl.z, sl.w};
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int s = 2 * v + h;
-          qa[s][0] = mhw[2 * h], qa[s][1] = mlw[2 * h], qa[s][2] = mhw[2 * h + 1], qa[s][3] = mlw[2 * h + 1];
-          qq[s][0] = shw[2 * h], qq[s][1] = slw[2 * h], qq[s][2] = shw[2 * h + 1], qq[s][3] = slw[2 * h + 1];
-        }
-      }
       qsm = p.qsc[2 * (b * p.Hq + head0 + g)];
       qsq = p.qsc[2 * (b * p.Hq + head0 + g) + 1];
-    } else {
-#pragma unroll
-      for (int s = 0; s < 8; ++s)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) qa[s][e] = qq[s][e] = 0u;
     }
+    named_sync1<CW * 32>();
     float O[8][4];
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) O[mt][0] = O[mt][1] = O[mt][2] = O[mt][3] = 0.f;
@@ -287,10 +284,12 @@ __global__ void __maxnreg__(168) k_partial_pv(const PvParams p) {
           lut2<FIXED, LUT_WINDOW>(mse_base, om1, b10, b11);
           lut2<FIXED, SIGN_WINDOW>(sign_base, on0, s00, s01);
           lut2<FIXED, SIGN_WINDOW>(sign_base, on1, s10, s11);
-          mma_f16(cm[st & 1][0], qa[st], b00, b01);
-          mma_f16(cm[st & 1][1], qa[st], b10, b11);
-          mma_f16(cq[st & 1][0], qq[st], s00, s01);
-          mma_f16(cq[st & 1][1], qq[st], s10, s11);
+          const uint4 fa = sm.qf[0][st][lane], fq = sm.qf[1][st][lane];
+          const uint32_t qa[4] = {fa.x, fa.y, fa.z, fa.w}, qq[4] = {fq.x, fq.y, fq.z, fq.w};
+          mma_f16(cm[st & 1][0], qa, b00, b01);
+          mma_f16(cm[st & 1][1], qa, b10, b11);
+          mma_f16(cq[st & 1][0], qq, s00, s01);
+          mma_f16(cq[st & 1][1], qq, s10, s11);
         }
         // ---- online softmax for head g over keys ks[0..3]
         float sc[4], u[4], tn[4];
@@ -379,7 +378,9 @@ __global__ void __maxnreg__(168) k_partial_pv(const PvParams p) {
       zt[G4] += __shfl_xor_sync(FULL_MASK, zt[G4], 2);
     }
 
-    // ---- merge the consumer warps' states of this item and write its partial
+    // ---- merge the consumer warps' states of this item and write its partial: the
+    // per-head max and sum over the warps by eight lanes of warp 0, then the accumulators
+    // in two passes of four heads through osm
     if (t == 0) {
       sm.mw[warp][g] = M;
       sm.lw[warp][g] = lsum;
@@ -387,43 +388,49 @@ __global__ void __maxnreg__(168) k_partial_pv(const PvParams p) {
       for (int G4 = 0; G4 < 4; ++G4) sm.zw[warp][g][G4] = zt[G4];
     }
     named_sync1<CW * 32>();
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int hh = 2 * t + e;  // head of accumulator columns c0/c2 (e = 0), c1/c3 (e = 1)
+    if (warp == 0 && lane < 8) {
       float ms = -INFINITY;
-      for (int w = 0; w < CW; ++w) ms = fmaxf(ms, sm.mw[w][hh]);
-      const float mine = sm.mw[warp][hh];
-      const float fac = (mine == -INFINITY) ? 0.f : exp2_approx(mine - ms);
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        const int G4 = mt >> 1;
-        const float z = sm.zw[warp][hh][G4];
-        const int d0 = 32 * G4 + 4 * g + 2 * (mt & 1);
-        sm.osm[warp][hh][d0] = fmaf(O[mt][e], 16777216.f, z) * fac;
-        sm.osm[warp][hh][d0 + 1] = fmaf(O[mt][2 + e], 16777216.f, z) * fac;
-      }
+      for (int w = 0; w < CW; ++w) ms = fmaxf(ms, sm.mw[w][lane]);
+      float v = 0.f;
+      if (ms != -INFINITY)
+        for (int w = 0; w < CW; ++w)
+          if (sm.mw[w][lane] != -INFINITY) v += sm.lw[w][lane] * exp2_approx(sm.mw[w][lane] - ms);
+      sm.mh[lane] = ms, sm.lh[lane] = v;
     }
-    named_sync1<CW * 32>();
-    for (int idx = threadIdx.x; idx < G * D; idx += CW * 32) {
-      const int hh = idx / D, jd = idx % D;
-      float ms = -INFINITY;
-      for (int w = 0; w < CW; ++w) ms = fmaxf(ms, sm.mw[w][hh]);
-      float acc = 0.f;
-      for (int w = 0; w < CW; ++w) acc += sm.osm[w][hh][jd];
-      float *dst = p.part + ((size_t)(b * p.Hq + head0 + hh) * p.n_part + it.slot) * PARTIAL_FLOATS;
-      dst[6 + jd] = (ms == -INFINITY) ? 0.f : acc;
-      if (jd < 6) {
-        float v = 0.f;
-        if (jd == 0) {
-          v = ms;
-        } else if (jd == 1 && ms != -INFINITY) {
-          for (int w = 0; w < CW; ++w)
-            if (sm.mw[w][hh] != -INFINITY) v += sm.lw[w][hh] * exp2_approx(sm.mw[w][hh] - ms);
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) {
+      if ((t >> 1) == pass) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int hh = 2 * t + e;  // head of accumulator columns c0/c2 (e = 0), c1/c3 (e = 1)
+          float ms = -INFINITY;
+          for (int w = 0; w < CW; ++w) ms = fmaxf(ms, sm.mw[w][hh]);
+          const float mine = sm.mw[warp][hh];
+          const float fac = (mine == -INFINITY) ? 0.f : exp2_approx(mine - ms);
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            const int G4 = mt >> 1;
+            const float z = sm.zw[warp][hh][G4];
+            const int d0 = 32 * G4 + 4 * g + 2 * (mt & 1);
+            sm.osm[warp][hh - 4 * pass][d0] = fmaf(O[mt][e], 16777216.f, z) * fac;
+            sm.osm[warp][hh - 4 * pass][d0 + 1] = fmaf(O[mt][2 + e], 16777216.f, z) * fac;
+          }
         }
-        dst[jd] = v;
       }
+      named_sync1<CW * 32>();
+      const int Gp = min(4, G - 4 * pass);
+      for (int idx = threadIdx.x; idx < Gp * D; idx += CW * 32) {
+        const int h4 = idx / D, jd = idx % D, hh = 4 * pass + h4;
+        const float ms = sm.mh[hh];
+        float acc = 0.f;
+#pragma unroll
+        for (int w = 0; w < CW; ++w) acc += sm.osm[w][h4][jd];
+        float *dst = p.part + ((size_t)(b * p.Hq + head0 + hh) * p.n_part + it.slot) * PARTIAL_FLOATS;
+        dst[6 + jd] = (ms == -INFINITY) ? 0.f : acc;
+        if (jd < 6) dst[jd] = jd == 0 ? ms : (jd == 1 ? sm.lh[hh] : 0.f);
+      }
+      named_sync1<CW * 32>();
     }
-    named_sync1<CW * 32>();
   }
 }
 

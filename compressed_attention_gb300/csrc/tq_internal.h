@@ -149,7 +149,7 @@ cudaError_t launch_dequantize(const tq_ctx *ctx, const uint8_t *cache, int64_t n
                               int unrotate, float *dst, cudaStream_t st);
 
 constexpr int T4_TILE = 240;  // keys per tile of the turbo4 decode
-constexpr int PV_TILE = 176;  // keys per tile of the prod3-key / vgroup2-value decode
+constexpr int PV_TILE = 240;  // keys per tile of the prod3-key / vgroup2-value decode
 // Fixed cost of one more work item in a CTA's range (the consumer warps' merge, the
 // partial's write, the next unit's q), in tiles of the kernel's own streaming time.
 constexpr int T4_ITEM_TILES = 4;
