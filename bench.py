@@ -775,7 +775,10 @@ def run_decode(args, rank, world, dist):
                      "traffic": profiled_traffic("decode_partial_" + name, spec["source"]),
                      "algorithmic_bytes_per_launch": kv_bytes, "avg_launch_ms": merge_avg,
                      "launches": merge_launches},
-        "roofline_issue": issue_roofline("decode_partial_" + name, spec["source"], spec["kernel"], merge_avg, clk,
+        # (the profiled launch is the split-K kernel alone: where the step follows it with a
+        # separate combine, its stage-form time)
+        "roofline_issue": issue_roofline("decode_partial_" + name, spec["source"], spec["kernel"],
+                                         merge_avg if merge_launches == 1 else part_avg, clk,
                                          torch.cuda.get_device_properties(device).multi_processor_count),
         "roofline_stage_kernel": {"kernel": f"{spec['kernel']} (stage call: partials only, no merge)",
                                   "achieved": achieved_stage, "frac": achieved_stage / peak,
