@@ -60,7 +60,7 @@ template <bool SKETCH>
 __global__ void __launch_bounds__(QWARPS * 32) k_prepare_q(const QprepParams p) {
   extern __shared__ __align__(16) float qsm[];
   pdl_trigger();
-  stage_matrix(qsm, p.rt);
+  stage_rows_padded(qsm, p.r);
   pdl_wait();
   prepare_q_body<SKETCH>(p, blockIdx.x, gridDim.x, qsm);
 }
@@ -1104,8 +1104,8 @@ QprepParams make_qprep_params(const tq_ctx *k, const void *q, int q_dtype, const
   p.q = q;
   p.q_dtype = q_dtype;
   p.n_q = s.B * s.Hq;
-  p.rt = k->d_pit;
-  p.st = s.pv ? k->d_St : nullptr;
+  p.r = k->d_pi;
+  p.s = s.pv ? k->d_S : nullptr;
   p.mul = LOG2E * scale / k->f16.alpha;
   p.mul_sk = (float)(LOG2E * (double)scale * (double)k->qjl_factor * 1.2533141373155003 / D);  // sqrt(pi/2) / d
   p.qhl = ws.qhl;

@@ -190,8 +190,8 @@ struct QprepParams {
   const void *q;
   int q_dtype;
   int n_q;            // B * Hq
-  const float *rt;    // R^T, fp32 [128][128] (row k = column k of R)
-  const float *st;    // S^T for the QJL sketch (prod3 keys), or null
+  const float *r;     // R, fp32 [128][128] row-major
+  const float *s;     // S for the QJL sketch (prod3 keys), row-major, or null
   float mul;          // log2(e) * scale / alpha_K
   float mul_sk;       // log2(e) * scale * sqrt(pi/2) / d (sketch)
   uint32_t *qhl;

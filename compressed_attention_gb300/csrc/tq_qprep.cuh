@@ -1,7 +1,10 @@
-// q preparation of the decode (shared by its own kernel and the decode-step front kernel):
+// q preparation of the decode (shared by its own kernel and the decode-step front kernels):
 // q_rot = R q and, with SKETCH, the QJL sketch S q, each pre-scaled and split into the fp16
 // hi + lo tensor-core operands: qhl[q][0..127] = q_rot (hi, lo), qhl[q][128..255] =
-// sketch (hi, lo).  A CTA of QWARPS warps takes QWARPS queries, one per warp.
+// sketch (hi, lo).  A CTA of QWARPS warps takes QWARPS queries: for the products warp w
+// computes outputs 16w .. 16w+15 of every query of the CTA from R (row-major, padded rows
+// in shared memory), so each row of R is read from shared memory once per CTA rather than
+// once per query; then warp w scales and splits query w.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -12,9 +15,11 @@
 
 namespace tq {
 
-constexpr int QWARPS = 8;  // queries per CTA, one warp each
-// dynamic shared memory: R^T (or S^T), the warps' q rows, their fp16 hi + lo rows
-constexpr size_t QPREP_SMEM = (size_t)D * D * 4 + QWARPS * D * 4 + QWARPS * 2 * D * 2;
+constexpr int QWARPS = 8;  // queries per CTA
+constexpr int RPAD = D + 4;  // padded row of a staged matrix: rows 16 apart share no bank
+// dynamic shared memory: R (or S) with padded rows, the CTA's q rows, their products, the
+// fp16 hi + lo rows
+constexpr size_t QPREP_SMEM = (size_t)D * RPAD * 4 + 2 * QWARPS * D * 4 + QWARPS * 2 * D * 2;
 
 // Stage a 128 x 128 fp32 matrix in shared memory with 16-byte loads, all in flight.
 static __device__ __forceinline__ void stage_matrix(float *dst, const float *src) {
@@ -29,19 +34,52 @@ static __device__ __forceinline__ void stage_matrix(float *dst, const float *src
   for (int i = 0; i < PER; ++i) d4[threadIdx.x + i * QWARPS * 32] = v[i];
 }
 
-// y = M x for the staged M^T (lane l computes y[l + 32 m]), times mul, scaled by a power
-// of two 2^-e so that the largest element lies in [2^13, 2^14), split into fp16 hi and
-// lo written to hw[0..127] and hw[128..255].  Returns e.
-static __device__ __forceinline__ int transform_split(const float *mt, const float *x, float mul,
-                                               __half *hw, int lane) {
-  float y[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-  for (int k = 0; k < D; ++k) {
-    const float xk = x[k];
-    const float *row = mt + k * D + lane;
+// Stage a 128 x 128 fp32 matrix row-major with rows padded to RPAD floats, loads in flight.
+static __device__ __forceinline__ void stage_rows_padded(float *dst, const float *src) {
+  const float4 *s4 = reinterpret_cast<const float4 *>(src);
+  constexpr int N4 = D * D / 4;
+  constexpr int PER = N4 / (QWARPS * 32);
+  float4 v[PER];
 #pragma unroll
-    for (int m = 0; m < 4; ++m) y[m] = fmaf(row[32 * m], xk, y[m]);
+  for (int i = 0; i < PER; ++i) v[i] = s4[threadIdx.x + i * QWARPS * 32];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int e = 4 * (threadIdx.x + i * QWARPS * 32), row = e / D, col = e % D;
+    *reinterpret_cast<float4 *>(dst + row * RPAD + col) = v[i];
   }
+}
+
+// ys[q][j] = (M x_q)_j for the CTA's QWARPS queries xs[q][0..127] and the staged M (padded
+// rows): warp w takes outputs j = 16w + (lane & 15) of queries 4 (lane >> 4) .. + 3, each a
+// chain of fused multiply-adds over k in order (as one query per warp would give).
+static __device__ __forceinline__ void transform_cta(const float *m, const float *xs, float *ys, int warp,
+                                                     int lane) {
+  const int j = 16 * warp + (lane & 15), q0 = 4 * (lane >> 4);
+  const float *mr = m + j * RPAD;
+  float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+  for (int k = 0; k < D; k += 4) {
+    const float4 r = *reinterpret_cast<const float4 *>(mr + k);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 x = *reinterpret_cast<const float4 *>(xs + (q0 + i) * D + k);
+      y[i] = fmaf(r.x, x.x, y[i]);
+      y[i] = fmaf(r.y, x.y, y[i]);
+      y[i] = fmaf(r.z, x.z, y[i]);
+      y[i] = fmaf(r.w, x.w, y[i]);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) ys[(q0 + i) * D + j] = y[i];
+}
+
+// Query `warp`'s products ys[warp][0..127] times mul, scaled by a power of two 2^-e so that
+// the largest element lies in [2^13, 2^14), split into fp16 hi and lo written to
+// hw[0..127] and hw[128..255].  Returns e.
+static __device__ __forceinline__ int scale_split(const float *yrow, float mul, __half *hw, int lane) {
+  float y[4];
+#pragma unroll
+  for (int m = 0; m < 4; ++m) y[m] = yrow[lane + 32 * m];
   float amax = 0.f;
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
@@ -62,14 +100,15 @@ static __device__ __forceinline__ int transform_split(const float *mt, const flo
   return e;
 }
 
-// After stage_matrix(qsm, p.rt) and the wait on the previous kernel: CTA cta of n_ctas
+// After stage_rows_padded(qsm, p.r) and the wait on the previous kernel: CTA cta of n_ctas
 // (QWARPS * 32 threads) prepares queries cta * QWARPS .. + QWARPS - 1 and zeroes its share
 // of the fused combine's unit counters.
 template <bool SKETCH>
 static __device__ __forceinline__ void prepare_q_body(const QprepParams &p, int cta, int n_ctas, float *qsm) {
-  float *mt = qsm;                       // [128][128]
-  float *qv = qsm + D * D;               // [QWARPS][128]
-  __half *hs = reinterpret_cast<__half *>(qv + QWARPS * D);  // [QWARPS][2][128]
+  float *mt = qsm;                       // [128][RPAD]
+  float *qv = qsm + D * RPAD;            // [QWARPS][128]
+  float *yv = qv + QWARPS * D;           // [QWARPS][128]
+  __half *hs = reinterpret_cast<__half *>(yv + QWARPS * D);  // [QWARPS][2][128]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qi = cta * QWARPS + warp;
   const bool live = qi < p.n_q;
@@ -99,8 +138,10 @@ static __device__ __forceinline__ void prepare_q_body(const QprepParams &p, int 
   __half *hw = hs + warp * 2 * D;
   uint32_t *dst = p.qhl + (size_t)qi * 256;
   const uint32_t *src = reinterpret_cast<const uint32_t *>(hw);
+  transform_cta(mt, qv, yv, warp, lane);
+  __syncthreads();
   if (live) {
-    const int e = transform_split(mt, qv + warp * D, p.mul, hw, lane);
+    const int e = scale_split(yv + warp * D, p.mul, hw, lane);
     __syncwarp();
 #pragma unroll
     for (int i = 0; i < 4; ++i) dst[lane + 32 * i] = src[lane + 32 * i];
@@ -110,12 +151,14 @@ static __device__ __forceinline__ void prepare_q_body(const QprepParams &p, int 
     }
   }
   if (SKETCH) {
-    __syncthreads();  // every warp is done with R^T
-    stage_matrix(mt, p.st);
+    __syncthreads();  // every warp is done with R and with its products
+    stage_rows_padded(mt, p.s);
+    __syncthreads();
+    transform_cta(mt, qv, yv, warp, lane);
     __syncthreads();
     if (live) {
       __syncwarp();
-      const int e = transform_split(mt, qv + warp * D, p.mul_sk, hw, lane);
+      const int e = scale_split(yv + warp * D, p.mul_sk, hw, lane);
       __syncwarp();
 #pragma unroll
       for (int i = 0; i < 4; ++i) dst[128 + lane + 32 * i] = src[lane + 32 * i];

@@ -582,17 +582,20 @@ __device__ __forceinline__ int64_t dense_row_normalize(const WriteParams &p, int
                                                        float *n_out) {
   const int lane = j & 31;
   const bool act = j < D;
-  const int64_t slot = p.row_ids ? p.row_ids[row] : row;
-  if (slot < 0 || slot >= p.dst_rows) {  // the same for every thread of the CTA
-    if (j == 0) atomicExch(p.status, (int32_t)DEVERR_ROW_OOB);
-    return -1;
-  }
+  // the source element is read before the slot is checked, so the two loads overlap
   float x = 0.f;
   if (act) {
     if (SRC == TQ_DTYPE_F32)
       x = static_cast<const float *>(p.src)[row * p.stride + j];
     else
       x = bf16_bits_to_f32(static_cast<const uint16_t *>(p.src)[row * p.stride + j]);
+  }
+  const int64_t slot = p.row_ids ? p.row_ids[row] : row;
+  if (slot < 0 || slot >= p.dst_rows) {  // the same for every thread of the CTA
+    if (j == 0) atomicExch(p.status, (int32_t)DEVERR_ROW_OOB);
+    return -1;
+  }
+  if (act) {
     // canonical norm: groups of four (pairs summed first), then the butterfly over groups
     const float sq = __fmul_rn(x, x);
     const float a = __fadd_rn(sq, __shfl_xor_sync(FULL_MASK, sq, 1));
@@ -719,10 +722,11 @@ __device__ __forceinline__ void prod3_row_body(const WriteParams &p, int64_t row
 }
 
 // ------------------------------------------------ decode step front (tq_decode_step)
-// One launch for what a decode step does before its split-K kernel: CTAs 0 .. n - 1
-// encode the step's n new K rows, CTAs n .. 2n - 1 its n new V rows (the small-batch dense
-// write above), the remaining CTAs prepare q (tq_qprep.cuh).  The three jobs are
-// independent, so they share one wait on the previous kernel instead of three.
+// One launch for what a decode step does before its split-K kernel: the first q_ctas CTAs
+// prepare q (tq_qprep.cuh; first, since theirs is the longest job), the next n encode the
+// step's n new K rows, the last n its n new V rows (the small-batch dense write above).
+// The three jobs are independent, so they share one wait on the previous kernel instead
+// of three.
 struct StepFrontParams {
   WriteParams wk, wv;
   QprepParams q;
@@ -733,8 +737,8 @@ struct StepFrontParams {
 template <int KF, int VF, int SRC>
 __global__ void __launch_bounds__(QWARPS * 32) k_step_front(const StepFrontParams sp) {
   extern __shared__ __align__(16) float fsm[];
-  const int c = blockIdx.x;
-  if (c < 2 * sp.n_rows) {
+  const int c = blockIdx.x - sp.q_ctas;  // row CTAs from 0
+  if (c >= 0) {
     RowScratch &sc = *reinterpret_cast<RowScratch *>(fsm);
     const bool v = c >= sp.n_rows;
     const int j = threadIdx.x;
@@ -751,9 +755,9 @@ __global__ void __launch_bounds__(QWARPS * 32) k_step_front(const StepFrontParam
       dense_row_body<KF, SRC>(sp.wk, c, sc, j, rr);
   } else {
     pdl_trigger();
-    stage_matrix(fsm, sp.q.rt);
+    stage_rows_padded(fsm, sp.q.r);
     pdl_wait();
-    prepare_q_body<false>(sp.q, c - 2 * sp.n_rows, sp.q_ctas, fsm);
+    prepare_q_body<false>(sp.q, blockIdx.x, sp.q_ctas, fsm);
   }
 }
 
@@ -810,17 +814,16 @@ __global__ void __launch_bounds__(WARPS * 32) k_write_vgroup(const WriteParams p
     vgroup_row<SRC>(p, row, lane, rowbuf[warp]);
 }
 
-// Decode step front for prod3 keys and vgroup2 values: CTAs 0 .. n - 1 encode the n new K
-// rows (one CTA per row, R and S^T staged before the wait), the next ceil(n / QWARPS) CTAs
-// the V rows (one warp per row), the remaining CTAs prepare q with its QJL sketch.
+// Decode step front for prod3 keys and vgroup2 values: the first q_ctas CTAs prepare q with
+// its QJL sketch, the next n encode the n new K rows (one CTA per row, R and S^T staged
+// before the wait), the last ceil(n / QWARPS) the V rows (one warp per row).
 constexpr size_t FRONT_PV_SMEM = 2 * (size_t)D * D * sizeof(float) + sizeof(Prod3Scratch);
 
 template <int SRC>
 __global__ void __launch_bounds__(QWARPS * 32) k_step_front_pv(const StepFrontParams sp) {
   extern __shared__ __align__(16) float fsm[];
-  const int c = blockIdx.x;
-  const int v_ctas = (sp.n_rows + QWARPS - 1) / QWARPS;
-  if (c < sp.n_rows) {
+  const int c = blockIdx.x - sp.q_ctas;  // row CTAs from 0: K rows, then V rows by warp
+  if (c >= 0 && c < sp.n_rows) {
     float *Rs = fsm, *STs = fsm + D * D;
     Prod3Scratch &sc = *reinterpret_cast<Prod3Scratch *>(fsm + 2 * D * D);
     float4 rr[D / 4];
@@ -830,7 +833,7 @@ __global__ void __launch_bounds__(QWARPS * 32) k_step_front_pv(const StepFrontPa
     pdl_trigger();
     pdl_wait();
     prod3_row_body<SRC>(sp.wk, c, sc, Rs, STs, threadIdx.x, rr);
-  } else if (c < sp.n_rows + v_ctas) {
+  } else if (c >= 0) {
     pdl_trigger();
     pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -838,9 +841,9 @@ __global__ void __launch_bounds__(QWARPS * 32) k_step_front_pv(const StepFrontPa
     if (row < sp.n_rows) vgroup_row<SRC>(sp.wv, row, lane, reinterpret_cast<uint8_t *>(fsm) + warp * ROWBUF);
   } else {
     pdl_trigger();
-    stage_matrix(fsm, sp.q.rt);
+    stage_rows_padded(fsm, sp.q.r);
     pdl_wait();
-    prepare_q_body<true>(sp.q, c - sp.n_rows - v_ctas, sp.q_ctas, fsm);
+    prepare_q_body<true>(sp.q, blockIdx.x, sp.q_ctas, fsm);
   }
 }
 
