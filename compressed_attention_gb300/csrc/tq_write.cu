@@ -558,20 +558,27 @@ struct RowScratch {
   alignas(16) uint8_t buf[ROWBUF];
 };
 
-// Before the wait: the boundaries, the grid table, this thread's row of R.
+// Stage R (row-major) into shared memory with rows padded to RPAD floats, by every thread of
+// the CTA: thread j then reads row j as float4 pieces without bank conflicts, and column j
+// (one element per row) likewise.
+__device__ __forceinline__ void stage_r_padded(float *dst, const float *src) {
+  const float4 *s4 = reinterpret_cast<const float4 *>(src);
+#pragma unroll 8
+  for (int i = threadIdx.x; i < D * D / 4; i += blockDim.x) {
+    const float4 v = s4[i];
+    *reinterpret_cast<float4 *>(dst + (i / (D / 4)) * RPAD + 4 * (i % (D / 4))) = v;
+  }
+}
+
+// Before the wait: the boundaries, the grid table, R staged (padded rows) at Rs.
 template <int NB>
-__device__ __forceinline__ void dense_row_prologue(const WriteParams &p, RowScratch &sc, int j,
-                                                   float4 (&rr)[D / 4]) {
+__device__ __forceinline__ void dense_row_prologue(const WriteParams &p, RowScratch &sc, int j, float *Rs) {
   if (j == 0) {
 #pragma unroll
     for (int k = 0; k < NB; ++k) sc.sb[k] = p.b[k];
   }
   stage_grid(&sc.grid, p.bt);
-  if (j < D) {
-    const float4 *r4 = reinterpret_cast<const float4 *>(p.pi + (size_t)j * D);  // row j of R
-#pragma unroll
-    for (int k4 = 0; k4 < D / 4; ++k4) rr[k4] = r4[k4];
-  }
+  stage_r_padded(Rs, p.pi);
 }
 
 // After the wait, the first part of a row's encoding (the whole CTA takes the same row):
@@ -617,12 +624,12 @@ __device__ __forceinline__ int64_t dense_row_normalize(const WriteParams &p, int
   return slot;
 }
 
-// y_j = (R u)_j from row j of R held in registers, in k order.
-__device__ __forceinline__ float row_times_u(const float4 (&rr)[D / 4], const float *u) {
+// y_j = (R u)_j from row j of R (rrow: its padded row in shared memory), in k order.
+__device__ __forceinline__ float row_times_u(const float *rrow, const float *u) {
   float y = 0.f;
-#pragma unroll
+#pragma unroll 8
   for (int k4 = 0; k4 < D / 4; ++k4) {
-    const float4 r = rr[k4];
+    const float4 r = *reinterpret_cast<const float4 *>(rrow + 4 * k4);
     y = fmaf(r.x, u[4 * k4], y);
     y = fmaf(r.y, u[4 * k4 + 1], y);
     y = fmaf(r.z, u[4 * k4 + 2], y);
@@ -634,7 +641,7 @@ __device__ __forceinline__ float row_times_u(const float4 (&rr)[D / 4], const fl
 // After the wait: encode source row `row` into its slot (the whole CTA takes the same row).
 template <int FMT, int SRC>
 __device__ __forceinline__ void dense_row_body(const WriteParams &p, int64_t row, RowScratch &sc, int j,
-                                               const float4 (&rr)[D / 4]) {
+                                               const float *Rs) {
   constexpr int NB = (FMT == TQ_FMT_TURBO4) ? 15 : 7;
   const int lane = j & 31;
   const bool act = j < D;
@@ -642,7 +649,7 @@ __device__ __forceinline__ void dense_row_body(const WriteParams &p, int64_t row
   const int64_t slot = dense_row_normalize<SRC>(p, row, sc, j, &n);
   if (slot < 0) return;
   if (act) {
-    const float y = row_times_u(rr, sc.u);
+    const float y = row_times_u(Rs + j * RPAD, sc.u);
     sc.ib[j] = (uint8_t)nearest<NB>(y, sc.grid, sc.sb);
   }
   __syncthreads();
@@ -653,20 +660,22 @@ __device__ __forceinline__ void dense_row_body(const WriteParams &p, int64_t row
   }
 }
 
+constexpr size_t ROW_SMEM = (size_t)D * RPAD * sizeof(float);  // R with padded rows
+
 template <int FMT, int SRC>
 __global__ void __launch_bounds__(D) k_write_dense_row(const WriteParams p) {
+  extern __shared__ __align__(16) float rsm[];
   __shared__ RowScratch sc;
-  float4 rr[D / 4];
-  dense_row_prologue<(FMT == TQ_FMT_TURBO4) ? 15 : 7>(p, sc, threadIdx.x, rr);
+  dense_row_prologue<(FMT == TQ_FMT_TURBO4) ? 15 : 7>(p, sc, threadIdx.x, rsm);
   pdl_trigger();
   pdl_wait();
-  dense_row_body<FMT, SRC>(p, blockIdx.x, sc, threadIdx.x, rr);
+  dense_row_body<FMT, SRC>(p, blockIdx.x, sc, threadIdx.x, rsm);
 }
 
 // A prod3 row by one CTA (the decode step's few new keys): the same steps as the warp-per-row
-// kernel above with thread j < 128 on coordinate j.  y = R u from row j of R in registers,
-// x_tilde = R^T y_hat and z = S r from R and S^T staged in shared memory (column j read by
-// thread j: no bank conflicts).
+// kernel above with thread j < 128 on coordinate j.  y = R u (row j of the staged R),
+// x_tilde = R^T y_hat (column j of R) and z = S r (column j of S^T), R with padded rows and
+// S^T in shared memory: no bank conflicts.
 struct Prod3Scratch {
   RowScratch base;
   float yh[D];  // centroids of the indices
@@ -675,14 +684,14 @@ struct Prod3Scratch {
 
 template <int SRC>
 __device__ __forceinline__ void prod3_row_body(const WriteParams &p, int64_t row, Prod3Scratch &sc, const float *Rs,
-                                               const float *STs, int j, const float4 (&rr)[D / 4]) {
+                                               const float *STs, int j) {
   const int lane = j & 31, warp = j >> 5;
   const bool act = j < D;
   float n;
   const int64_t slot = dense_row_normalize<SRC>(p, row, sc.base, j, &n);
   if (slot < 0) return;
   if (act) {
-    const uint32_t idx = nearest<3>(row_times_u(rr, sc.base.u), sc.base.grid, sc.base.sb);
+    const uint32_t idx = nearest<3>(row_times_u(Rs + j * RPAD, sc.base.u), sc.base.grid, sc.base.sb);
     sc.base.ib[j] = (uint8_t)idx;
     sc.yh[j] = p.c[idx];
   }
@@ -690,7 +699,7 @@ __device__ __forceinline__ void prod3_row_body(const WriteParams &p, int64_t row
   if (act) {
     float xt = 0.f;  // (R^T y_hat)_j = sum_k R[k][j] y_hat_k
 #pragma unroll 8
-    for (int k = 0; k < D; ++k) xt = fmaf(Rs[k * D + j], sc.yh[k], xt);
+    for (int k = 0; k < D; ++k) xt = fmaf(Rs[k * RPAD + j], sc.yh[k], xt);
     sc.r[j] = sc.base.u[j] - xt;
   }
   __syncthreads();
@@ -739,20 +748,20 @@ __global__ void __launch_bounds__(QWARPS * 32) k_step_front(const StepFrontParam
   extern __shared__ __align__(16) float fsm[];
   const int c = blockIdx.x - sp.q_ctas;  // row CTAs from 0
   if (c >= 0) {
-    RowScratch &sc = *reinterpret_cast<RowScratch *>(fsm);
+    float *Rs = fsm;  // R with padded rows
+    RowScratch &sc = *reinterpret_cast<RowScratch *>(fsm + D * RPAD);
     const bool v = c >= sp.n_rows;
     const int j = threadIdx.x;
-    float4 rr[D / 4];
     if (v)
-      dense_row_prologue<(VF == TQ_FMT_TURBO4) ? 15 : 7>(sp.wv, sc, j, rr);
+      dense_row_prologue<(VF == TQ_FMT_TURBO4) ? 15 : 7>(sp.wv, sc, j, Rs);
     else
-      dense_row_prologue<(KF == TQ_FMT_TURBO4) ? 15 : 7>(sp.wk, sc, j, rr);
+      dense_row_prologue<(KF == TQ_FMT_TURBO4) ? 15 : 7>(sp.wk, sc, j, Rs);
     pdl_trigger();
     pdl_wait();
     if (v)
-      dense_row_body<VF, SRC>(sp.wv, c - sp.n_rows, sc, j, rr);
+      dense_row_body<VF, SRC>(sp.wv, c - sp.n_rows, sc, j, Rs);
     else
-      dense_row_body<KF, SRC>(sp.wk, c, sc, j, rr);
+      dense_row_body<KF, SRC>(sp.wk, c, sc, j, Rs);
   } else {
     pdl_trigger();
     stage_rows_padded(fsm, sp.q.r);
@@ -817,22 +826,20 @@ __global__ void __launch_bounds__(WARPS * 32) k_write_vgroup(const WriteParams p
 // Decode step front for prod3 keys and vgroup2 values: the first q_ctas CTAs prepare q with
 // its QJL sketch, the next n encode the n new K rows (one CTA per row, R and S^T staged
 // before the wait), the last ceil(n / QWARPS) the V rows (one warp per row).
-constexpr size_t FRONT_PV_SMEM = 2 * (size_t)D * D * sizeof(float) + sizeof(Prod3Scratch);
+constexpr size_t FRONT_PV_SMEM = ((size_t)D * RPAD + D * D) * sizeof(float) + sizeof(Prod3Scratch);
 
 template <int SRC>
 __global__ void __launch_bounds__(QWARPS * 32) k_step_front_pv(const StepFrontParams sp) {
   extern __shared__ __align__(16) float fsm[];
   const int c = blockIdx.x - sp.q_ctas;  // row CTAs from 0: K rows, then V rows by warp
   if (c >= 0 && c < sp.n_rows) {
-    float *Rs = fsm, *STs = fsm + D * D;
-    Prod3Scratch &sc = *reinterpret_cast<Prod3Scratch *>(fsm + 2 * D * D);
-    float4 rr[D / 4];
-    dense_row_prologue<3>(sp.wk, sc.base, threadIdx.x, rr);
-    stage_matrix(Rs, sp.wk.pi);
+    float *Rs = fsm, *STs = fsm + D * RPAD;  // R with padded rows, S^T
+    Prod3Scratch &sc = *reinterpret_cast<Prod3Scratch *>(fsm + D * RPAD + D * D);
+    dense_row_prologue<3>(sp.wk, sc.base, threadIdx.x, Rs);
     stage_matrix(STs, sp.wk.St);
     pdl_trigger();
     pdl_wait();
-    prod3_row_body<SRC>(sp.wk, c, sc, Rs, STs, threadIdx.x, rr);
+    prod3_row_body<SRC>(sp.wk, c, sc, Rs, STs, threadIdx.x);
   } else if (c >= 0) {
     pdl_trigger();
     pdl_wait();
@@ -921,11 +928,12 @@ cudaError_t launch_write(const tq_ctx *ctx, const WriteLaunch &w, cudaStream_t s
   // A few rows (a decode step's new tokens): one CTA per row, R read from L2.
   if (w.n_rows <= SMALL_ROWS && fmt != TQ_FMT_PROD3) {
     const dim3 grid((unsigned)w.n_rows), block(D);
-    if (fmt == TQ_FMT_TURBO4)
-      return bf16 ? launch_pdl(k_write_dense_row<TQ_FMT_TURBO4, TQ_DTYPE_BF16>, grid, block, 0, st, p)
-                  : launch_pdl(k_write_dense_row<TQ_FMT_TURBO4, TQ_DTYPE_F32>, grid, block, 0, st, p);
-    return bf16 ? launch_pdl(k_write_dense_row<TQ_FMT_TURBO3, TQ_DTYPE_BF16>, grid, block, 0, st, p)
-                : launch_pdl(k_write_dense_row<TQ_FMT_TURBO3, TQ_DTYPE_F32>, grid, block, 0, st, p);
+    auto kern = fmt == TQ_FMT_TURBO4
+                    ? (bf16 ? k_write_dense_row<TQ_FMT_TURBO4, TQ_DTYPE_BF16> : k_write_dense_row<TQ_FMT_TURBO4, TQ_DTYPE_F32>)
+                    : (bf16 ? k_write_dense_row<TQ_FMT_TURBO3, TQ_DTYPE_BF16> : k_write_dense_row<TQ_FMT_TURBO3, TQ_DTYPE_F32>);
+    cudaError_t e = kernel_smem_attr((const void *)kern, (int)ROW_SMEM);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(kern, grid, block, ROW_SMEM, st, p);
   }
   // Dense rotation on the CUDA cores (prod3 always takes this path; its WHT variant
   // multiplies by the materialised WHT matrix, which the context stores as well).
@@ -986,7 +994,7 @@ cudaError_t launch_step_front(const tq_ctx *k, const tq_ctx *v, const WriteLaunc
   sp.q_ctas = (q.n_q + QWARPS - 1) / QWARPS;
   const bool bf16 = wk.src_dtype == TQ_DTYPE_BF16;
   const bool k4 = k->fmt == TQ_FMT_TURBO4, v4 = v->fmt == TQ_FMT_TURBO4;
-  static_assert(sizeof(RowScratch) <= QPREP_SMEM, "one dynamic shared area for both roles");
+  static_assert(ROW_SMEM + sizeof(RowScratch) <= QPREP_SMEM, "one dynamic shared area for both roles");
   auto pick = [&]() {
     if (bf16) {
       if (k4) return v4 ? k_step_front<TQ_FMT_TURBO4, TQ_FMT_TURBO4, TQ_DTYPE_BF16>
