@@ -21,32 +21,24 @@ constexpr int RPAD = D + 4;  // padded row of a staged matrix: rows 16 apart sha
 // fp16 hi + lo rows
 constexpr size_t QPREP_SMEM = (size_t)D * RPAD * 4 + 2 * QWARPS * D * 4 + QWARPS * 2 * D * 2;
 
-// Stage a 128 x 128 fp32 matrix in shared memory with 16-byte loads, all in flight.
-static __device__ __forceinline__ void stage_matrix(float *dst, const float *src) {
-  const float4 *s4 = reinterpret_cast<const float4 *>(src);
-  float4 *d4 = reinterpret_cast<float4 *>(dst);
-  constexpr int N4 = D * D / 4;
-  constexpr int PER = N4 / (QWARPS * 32);
-  float4 v[PER];
-#pragma unroll
-  for (int i = 0; i < PER; ++i) v[i] = s4[threadIdx.x + i * QWARPS * 32];
-#pragma unroll
-  for (int i = 0; i < PER; ++i) d4[threadIdx.x + i * QWARPS * 32] = v[i];
+// One 16-byte asynchronous copy global -> shared (both 16-byte aligned).
+static __device__ __forceinline__ void cp16_async(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
 }
 
-// Stage a 128 x 128 fp32 matrix row-major with rows padded to RPAD floats, loads in flight.
+// Stage a 128 x 128 fp32 matrix (row-major) in shared memory with rows of `pitch` floats
+// (D: packed; RPAD: padded, so that rows 16 apart share no bank), by every thread of the
+// CTA with 16-byte asynchronous copies, all in flight at once; each thread waits for its
+// own copies, so the caller's next barrier makes the matrix visible to the CTA.
+static __device__ __forceinline__ void stage_matrix_pitch(float *dst, const float *src, int pitch) {
+  for (int i = threadIdx.x; i < D * D / 4; i += blockDim.x)
+    cp16_async(dst + (i / (D / 4)) * pitch + 4 * (i % (D / 4)), src + 4 * i);
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+static __device__ __forceinline__ void stage_matrix(float *dst, const float *src) { stage_matrix_pitch(dst, src, D); }
 static __device__ __forceinline__ void stage_rows_padded(float *dst, const float *src) {
-  const float4 *s4 = reinterpret_cast<const float4 *>(src);
-  constexpr int N4 = D * D / 4;
-  constexpr int PER = N4 / (QWARPS * 32);
-  float4 v[PER];
-#pragma unroll
-  for (int i = 0; i < PER; ++i) v[i] = s4[threadIdx.x + i * QWARPS * 32];
-#pragma unroll
-  for (int i = 0; i < PER; ++i) {
-    const int e = 4 * (threadIdx.x + i * QWARPS * 32), row = e / D, col = e % D;
-    *reinterpret_cast<float4 *>(dst + row * RPAD + col) = v[i];
-  }
+  stage_matrix_pitch(dst, src, RPAD);
 }
 
 // ys[q][j] = (M x_q)_j for the CTA's QWARPS queries xs[q][0..127] and the staged M (padded

@@ -558,18 +558,6 @@ struct RowScratch {
   alignas(16) uint8_t buf[ROWBUF];
 };
 
-// Stage R (row-major) into shared memory with rows padded to RPAD floats, by every thread of
-// the CTA: thread j then reads row j as float4 pieces without bank conflicts, and column j
-// (one element per row) likewise.
-__device__ __forceinline__ void stage_r_padded(float *dst, const float *src) {
-  const float4 *s4 = reinterpret_cast<const float4 *>(src);
-#pragma unroll 8
-  for (int i = threadIdx.x; i < D * D / 4; i += blockDim.x) {
-    const float4 v = s4[i];
-    *reinterpret_cast<float4 *>(dst + (i / (D / 4)) * RPAD + 4 * (i % (D / 4))) = v;
-  }
-}
-
 // Before the wait: the boundaries, the grid table, R staged (padded rows) at Rs.
 template <int NB>
 __device__ __forceinline__ void dense_row_prologue(const WriteParams &p, RowScratch &sc, int j, float *Rs) {
@@ -578,7 +566,7 @@ __device__ __forceinline__ void dense_row_prologue(const WriteParams &p, RowScra
     for (int k = 0; k < NB; ++k) sc.sb[k] = p.b[k];
   }
   stage_grid(&sc.grid, p.bt);
-  stage_r_padded(Rs, p.pi);
+  stage_rows_padded(Rs, p.pi);
 }
 
 // After the wait, the first part of a row's encoding (the whole CTA takes the same row):
