@@ -804,14 +804,14 @@ __global__ void __maxnreg__(128)
     return;
   }
   // The completed units' heads in quads of four (NG quads per unit), up to three quads per
-  // round: the round's nh heads are merged by twelve warps (W = 12 / nh per head, see
+  // pass: the pass's nh heads are merged by twelve warps (W = 12 / nh per head, see
   // below), and thread (quad, j) un-rotates dim j of that quad's heads, with R from the
   // stage buffers (its copy was issued before the counts).
   constexpr int QUADS = 3;
-  static_assert(4 * QUADS <= CWARPS && QUADS * D <= CWARPS * 32, "a round's heads and dims");
+  static_assert(4 * QUADS <= CWARPS && QUADS * D <= CWARPS * 32, "a pass's heads and dims");
   const int n_quads = n_fin * NG;
   for (int q0 = 0; q0 < n_quads; q0 += QUADS) {
-    // nh heads this round; W warps per head split its partials between them (warp w takes
+    // nh heads in this pass; W warps per head split its partials between them (warp w takes
     // head slot w % nh and every W-th chunk of eight splits from chunk w / nh)
     // (nq = 1: four heads, W = 3; nq = 2 or 3: eight or twelve heads, W = 1)
     const int nq = min(QUADS, n_quads - q0), nh = 4 * nq, W = nq == 1 ? 3 : 1;
@@ -886,7 +886,7 @@ __global__ void __maxnreg__(128)
     consumers_sync();  // merged heads (and, the first time, R) in shared memory
     // out = R^T o: thread (group, j) reads column j of R once for the four heads of a quad
     // (o read as broadcast float4), four independent chains over k per head, summed at the
-    // end.  With three quads in the round each group takes one; with one quad the three
+    // end.  With three quads in the pass each group takes one; with one quad the three
     // groups split k in three (the partial sums of groups 1 and 2 meet in the shares'
     // scratch, idle now); with two quads each group takes one.
     const int ks = (nq == 1 && p.r) ? 3 : 1;  // uniform over the CTA
@@ -939,7 +939,7 @@ __global__ void __maxnreg__(128)
       for (int h = 0; h < 4; ++h)
         if (hu0 + h < G) dst[h * D] = res[h];
     }
-    consumers_sync();  // the round's merged heads are free again
+    consumers_sync();  // the pass's merged heads are free again
   }
   if (threadIdx.x < n_fin) p.unit_done[sm.units[threadIdx.x]] = 0;
 }

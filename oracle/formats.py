@@ -17,7 +17,7 @@ normalise -> random rotation -> nearest centroid ("抽范数 -> 归一化 -> 随
   path's "2-bit group quantization + bit packing"): 48 bytes = q[32] (2-bit
   codes) + 4 x (fp16 scale, fp16 zero) for groups of 32 elements.
 
-Readings taken where the pages are silent (all listed in the design doc):
+Readings taken where the pages are silent:
 
 * Header first, little-endian, in every block.
 * The canonical fp32 norm: squares rounded separately (no fused multiply-add),
