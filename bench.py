@@ -41,6 +41,7 @@ os.environ.setdefault("MKL_NUM_THREADS", "1")
 
 import argparse
 import hashlib
+import re
 import json
 import statistics
 import subprocess
@@ -105,6 +106,16 @@ def measured_tensor_peak():
     return FALLBACK_TENSOR_TFLOPS, "fallback"
 
 
+def source_digest(source):
+    """First 16 hex digits of the SHA-256 of a kernel source with its comments and blank
+    space removed: what the compiler sees, so a comment edit keeps a profile valid while
+    any code change retires it."""
+    text = open(os.path.join(CSRC, source), encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return hashlib.sha256(" ".join(text.split()).encode()).hexdigest()[:16]
+
+
 def profiled_fields(profile_name, source):
     """The "- key: value" fields of a kernel's committed ncu summary
     (profiles/<profile_name>.md), or None when the kernel source changed since the capture
@@ -117,8 +128,7 @@ def profiled_fields(profile_name, source):
         if ":" in ln and ln.strip().startswith("- "):
             k, v = ln.strip()[2:].split(":", 1)
             fields[k.strip()] = v.strip()
-    digest = hashlib.sha256(open(os.path.join(CSRC, source), "rb").read()).hexdigest()[:16]
-    if fields.get("source_sha256_16") != digest:
+    if fields.get("source_sha256_16") != source_digest(source):
         return None
     return fields
 

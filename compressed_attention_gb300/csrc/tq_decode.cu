@@ -808,7 +808,7 @@ __global__ void __maxnreg__(128)
   // below), and thread (quad, j) un-rotates dim j of that quad's heads, with R from the
   // stage buffers (its copy was issued before the counts).
   constexpr int QUADS = 3;
-  static_assert(4 * QUADS <= CWARPS && QUADS * D <= CWARPS * 32, "a pass's heads and dims");
+  static_assert(4 * QUADS <= CWARPS && QUADS * D <= CWARPS * 32, "a round's heads and dims");
   const int n_quads = n_fin * NG;
   for (int q0 = 0; q0 < n_quads; q0 += QUADS) {
     // nh heads in this pass; W warps per head split its partials between them (warp w takes
