@@ -627,6 +627,12 @@ E2E_MODE = ("value: the public API calls and the copies issued one by one from P
             "captured once in a CUDA graph and replayed every step")
 
 
+E2E_MODE_DECODE = ("value: one public C-ABI call per step with host buffers (tq_decode_step_host: the input "
+                   "copy from pinned host memory, the step and the output copy back), issued from Python every "
+                   "step (host validation and enqueue inside the timed region); graph_*: the same call captured "
+                   "once in a CUDA graph and replayed every step")
+
+
 def timed_e2e(torch, body, steps, warmup, flush_l2):
     """End-to-end step times (ms, host clock) of `body`: the host-to-device copies of the
     step's inputs from pinned memory, the public API calls and the device-to-host read of
@@ -717,28 +723,19 @@ def run_decode(args, rank, world, dist):
     flushed = {k: max_over_ranks(v, dist, device) for k, v in flushed.items()}
     merge_launches = tq.tq_decode_num_launches(w["kctx"], w["vctx"], B, Hq, Hkv, L) - 1
 
-    # end to end through the public API with host buffers: q and the new K/V rows copied in,
-    # the output read back, every step.  The step's inputs sit back to back in one pinned
-    # host buffer (each part a multiple of 16 bytes), so they cross in one copy.
-    names = ("q", "new_k", "new_v")
-    sizes = [w[k].numel() * w[k].element_size() for k in names]
-    assert all(n % 16 == 0 for n in sizes)
-    h2d = sum(sizes)
-    hstage = torch.empty(h2d, dtype=torch.uint8, pin_memory=True)
-    dstage = torch.empty(h2d, dtype=torch.uint8, device=device)
-    dev, off = {}, 0
-    for k, n in zip(names, sizes):
-        hstage[off:off + n].view(w[k].dtype).view(w[k].shape).copy_(w[k].cpu())
-        dev[k] = dstage[off:off + n].view(w[k].dtype).view(w[k].shape)
-        off += n
+    # end to end through the public API with host buffers, every step: the new K rows, the
+    # new V rows and q, back to back in one pinned host buffer, copied in in one piece; the
+    # output read back.
+    hstage, _ = tq.pack_step_inputs(w["new_k"], w["new_v"], w["q"])
+    h2d = hstage.numel()
     hout = torch.empty(w["out"].shape, dtype=torch.float32, pin_memory=True)
     d2h = hout.numel() * 4
+    staging = tq.alloc_workspace(tq.tq_decode_step_host_staging_size(
+        w["kctx"], w["new_k"].dtype, w["new_k"].shape[0], w["q"].dtype, B, Hq), device)
 
-    def e2e_body():
-        dstage.copy_(hstage, non_blocking=True)
-        tq.tq_decode_step(w["kctx"], w["vctx"], dev["new_k"], dev["new_v"], dev["q"], w["kc"], w["vc"], w["out"],
-                          w["ws"], B, Hq, Hkv, L, row_ids=w["slots"])
-        hout.copy_(w["out"], non_blocking=True)
+    def e2e_body():  # one C-ABI call: input copy, the step, output copy
+        tq.tq_decode_step_host(w["kctx"], w["vctx"], hstage, w["new_k"].dtype, w["new_k"].shape[0], w["q"].dtype,
+                               hout, w["slots"], w["kc"], w["vc"], staging, w["ws"], B, Hq, Hkv, L)
 
     e2e_ms, e2e_direct_ms = timed_e2e(torch, e2e_body, args.steps, args.warmup, flush_l2)
     status = tq.tq_ctx_device_status(w["kctx"]) or tq.tq_ctx_device_status(w["vctx"])
@@ -797,7 +794,7 @@ def run_decode(args, rank, world, dist):
         "cpu_fp32_loop": fp32_loop,
         "e2e": {"value": job_rate(alg_bytes, world, e2e_direct_ms) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_direct_ms,
-                "mode": E2E_MODE, "graph_value": job_rate(alg_bytes, world, e2e_graph_ms) / 1e9,
+                "mode": E2E_MODE_DECODE, "graph_value": job_rate(alg_bytes, world, e2e_graph_ms) / 1e9,
                 "graph_ms_per_step": e2e_graph_ms},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,

@@ -69,6 +69,9 @@ _SIGNATURES = {
     "tq_decode_step_num_launches": (_i32, [_vp, _vp, _i32, _i64, _i32, _i32, _i32, _i32, ctypes.POINTER(_i32)]),
     "tq_decode_step": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i64, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _i32,
                               _i32, _i32, _f32, _vp, _vp, _sz, _vp]),
+    "tq_decode_step_host": (_i32, [_vp, _vp, _vp, _i32, _i64, _vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
+                                   _f32, _vp, _vp, _sz, _vp, _sz, _vp]),
+    "tq_decode_step_host_staging_size": (_i32, [_vp, _i32, _i64, _i32, _i32, _i32, ctypes.POINTER(_sz)]),
     "tq_decode_attention": (_i32, [_vp, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _f32,
                                    _vp, _vp, _vp, _sz, _vp]),
     "tq_decode_prepare_q": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _sz, _vp]),
@@ -136,9 +139,13 @@ def _stream(stream):
     return stream.cuda_stream
 
 
-def _dtype_code(t):
+def _torch_dtype_code(dt):
     import torch
-    return {torch.float32: TQ_DTYPE_F32, torch.bfloat16: TQ_DTYPE_BF16, torch.float16: TQ_DTYPE_F16}[t.dtype]
+    return {torch.float32: TQ_DTYPE_F32, torch.bfloat16: TQ_DTYPE_BF16, torch.float16: TQ_DTYPE_F16}[dt]
+
+
+def _dtype_code(t):
+    return _torch_dtype_code(t.dtype)
 
 
 # --------------------------------------------------------------------------- host only
@@ -257,6 +264,46 @@ def tq_decode_step(k_ctx, v_ctx, new_k, new_v, q, k_cache, v_cache, out, workspa
                               new_k.stride(-2) if new_k.dim() >= 2 else D, _ptr(row_ids), qp, qd, _ptr(k_cache),
                               _ptr(v_cache), _ptr(seq_lens), B, Hq, Hkv, L, scale, _ptr(out), _ptr(workspace),
                               workspace.numel() * workspace.element_size(), _stream(stream)), "tq_decode_step")
+
+
+def tq_decode_step_host_staging_size(k_ctx, src_dtype, n_rows, q_dtype, B, Hq):
+    """Device staging bytes tq_decode_step_host needs (torch dtypes of the rows and of q)."""
+    n = _sz(0)
+    _check(lib.tq_decode_step_host_staging_size(k_ctx.handle, _torch_dtype_code(src_dtype), n_rows,
+                                                _torch_dtype_code(q_dtype), B, Hq, ctypes.byref(n)),
+           "tq_decode_step_host_staging_size")
+    return n.value
+
+
+def pack_step_inputs(new_k, new_v, q):
+    """One pinned host buffer holding new_k, new_v and q back to back (tq_decode_step_host's
+    input layout), and the host views of the three parts in it."""
+    import torch
+    parts = [new_k, new_v, q]
+    sizes = [t.numel() * t.element_size() for t in parts]
+    buf = torch.empty(sum(sizes), dtype=torch.uint8, pin_memory=True)
+    views, off = [], 0
+    for t, n in zip(parts, sizes):
+        v = buf[off:off + n].view(t.dtype).view(t.shape)
+        v.copy_(t.detach().cpu())
+        views.append(v)
+        off += n
+    return buf, views
+
+
+def tq_decode_step_host(k_ctx, v_ctx, inputs, src_dtype, n_rows, q_dtype, out, row_ids, k_cache, v_cache, staging,
+                        workspace, B, Hq, Hkv, L, seq_lens=None, scale=0.0, stream=None):
+    """tq_decode_step with host buffers: ``inputs`` a (pinned) host buffer holding the new K
+    rows, the new V rows ([n_rows, d] of src_dtype each) and q ([B, Hq, d] of q_dtype) back
+    to back (pack_step_inputs), ``out`` fp32 [B, Hq, d] in host memory; one C call copies
+    the inputs in, runs the step on the device staging area and copies the output back, on
+    the stream, without waiting."""
+    _check(lib.tq_decode_step_host(k_ctx.handle, v_ctx.handle, _ptr(inputs), _torch_dtype_code(src_dtype), n_rows,
+                                   _ptr(row_ids), _torch_dtype_code(q_dtype), _ptr(k_cache), _ptr(v_cache),
+                                   _ptr(seq_lens), B, Hq, Hkv, L, scale, _ptr(out), _ptr(staging),
+                                   staging.numel() * staging.element_size(), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(stream)),
+           "tq_decode_step_host")
 
 
 def tq_decode_step_num_launches(k_ctx, v_ctx, src_dtype, n_rows, B, Hq, Hkv, L):

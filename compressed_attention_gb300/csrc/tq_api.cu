@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstring>
 #include <new>
+#include <string>
 #include <vector>
 
 #include "tq_internal.h"
@@ -25,6 +26,7 @@ tq_status fail(tq_status s, const char *msg) {
 
 tq_status cuda_fail(cudaError_t e, const char *where) {
   set_error("%s: %s", where, cudaGetErrorString(e));
+  (void)cudaGetLastError();  // a reported failure does not surface again in a later launch check
   return TQ_ERR_CUDA;
 }
 
@@ -713,6 +715,65 @@ tq_status tq_decode_step(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *n
   if (fused) return TQ_OK;
   e = launch_combine(k_ctx, v_ctx, s, out, w, cs);
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  return TQ_OK;
+}
+
+namespace {
+size_t dtype_bytes(int dtype) { return dtype == TQ_DTYPE_F32 ? 4 : 2; }
+bool dtype_known(int dtype) { return dtype == TQ_DTYPE_F32 || dtype == TQ_DTYPE_BF16 || dtype == TQ_DTYPE_F16; }
+// Staging layout of tq_decode_step_host: new K rows, new V rows and q back to back (the
+// host order for the one-copy case), then the output at the next 256-byte boundary.
+struct HostStaging {
+  size_t k_bytes, q_bytes, out_off, out_bytes, total;
+};
+HostStaging host_staging(int d, int src_dtype, int64_t n_rows, int q_dtype, int B, int Hq) {
+  HostStaging h{};
+  h.k_bytes = (size_t)n_rows * d * dtype_bytes(src_dtype);
+  h.q_bytes = (size_t)B * Hq * d * dtype_bytes(q_dtype);
+  h.out_off = (2 * h.k_bytes + h.q_bytes + 255) & ~(size_t)255;
+  h.out_bytes = (size_t)B * Hq * d * sizeof(float);
+  h.total = h.out_off + h.out_bytes;
+  return h;
+}
+}  // namespace
+
+tq_status tq_decode_step_host_staging_size(const tq_ctx *k_ctx, int src_dtype, int64_t n_rows, int q_dtype,
+                                           int B, int Hq, size_t *bytes) {
+  if (!k_ctx || !bytes) return fail(TQ_ERR_INVALID_ARG, "null context or output");
+  if (n_rows < 0 || B < 1 || Hq < 1) return fail(TQ_ERR_INVALID_ARG, "n_rows >= 0, B >= 1 and Hq >= 1 are required");
+  if (!dtype_known(q_dtype) || (src_dtype != TQ_DTYPE_F32 && src_dtype != TQ_DTYPE_BF16))
+    return fail(TQ_ERR_INVALID_ARG, "unknown dtype");
+  *bytes = host_staging(k_ctx->d, src_dtype, n_rows, q_dtype, B, Hq).total;
+  return TQ_OK;
+}
+
+tq_status tq_decode_step_host(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *inputs_host, int src_dtype,
+                              int64_t n_rows, const int64_t *row_ids, int q_dtype, void *k_cache, void *v_cache,
+                              const int32_t *seq_lens, int B, int Hq, int Hkv, int L, float scale, float *out_host,
+                              void *staging, size_t staging_bytes, void *workspace, size_t workspace_bytes,
+                              tq_stream_t stream) {
+  if (!k_ctx || !v_ctx) return fail(TQ_ERR_INVALID_ARG, "null context");
+  tq_status st = check_current_device(k_ctx->device, "decode");
+  if (st != TQ_OK) return st;
+  size_t need = 0;
+  if ((st = tq_decode_step_host_staging_size(k_ctx, src_dtype, n_rows, q_dtype, B, Hq, &need)) != TQ_OK) return st;
+  if (!inputs_host || !out_host) return fail(TQ_ERR_INVALID_ARG, "null host buffer");
+  if (!staging || staging_bytes < need) return fail(TQ_ERR_WORKSPACE, "staging smaller than tq_decode_step_host_staging_size()");
+  if (!aligned(staging, 256)) return fail(TQ_ERR_ALIGNMENT, "staging must be 256-byte aligned");
+  size_t ws_need = 0;  // the shape and workspace checks of the step, before the copy
+  if ((st = tq_decode_workspace_size(k_ctx, v_ctx, B, Hq, Hkv, L, &ws_need)) != TQ_OK) return st;
+  if (!workspace || workspace_bytes < ws_need) return fail(TQ_ERR_WORKSPACE, "workspace smaller than tq_decode_workspace_size()");
+  const HostStaging h = host_staging(k_ctx->d, src_dtype, n_rows, q_dtype, B, Hq);
+  uint8_t *dk = static_cast<uint8_t *>(staging), *dv = dk + h.k_bytes, *dq = dv + h.k_bytes;
+  float *dout = reinterpret_cast<float *>(dk + h.out_off);
+  const cudaStream_t cs = (cudaStream_t)stream;
+  cudaError_t e = cudaMemcpyAsync(dk, inputs_host, 2 * h.k_bytes + h.q_bytes, cudaMemcpyHostToDevice, cs);
+  if (e != cudaSuccess) return cuda_fail(e, "input copy");
+  st = tq_decode_step(k_ctx, v_ctx, dk, dv, src_dtype, n_rows, k_ctx->d, row_ids, dq, q_dtype, k_cache, v_cache,
+                      seq_lens, B, Hq, Hkv, L, scale, dout, workspace, workspace_bytes, stream);
+  if (st != TQ_OK) return st;
+  e = cudaMemcpyAsync(out_host, dout, h.out_bytes, cudaMemcpyDeviceToHost, cs);
+  if (e != cudaSuccess) return cuda_fail(e, "output copy");
   return TQ_OK;
 }
 

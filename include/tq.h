@@ -249,6 +249,29 @@ tq_status tq_decode_step(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *n
                          void *v_cache, const int32_t *seq_lens, int B, int Hq, int Hkv, int L,
                          float scale, float *out, void *workspace, size_t workspace_bytes,
                          tq_stream_t stream);
+/* tq_decode_step with host buffers: the step's new K / V rows and q are copied in one
+ * piece from host memory into the caller's device staging area, tq_decode_step runs on
+ * them, and the output is copied back to host memory -- all enqueued on `stream`; the call
+ * returns without waiting (synchronize the stream before reading out_host).  Host buffers
+ * should be pinned (page-locked) for the copies to be asynchronous.
+ *   inputs_host    one host buffer: the n_rows new K rows [n_rows][d] of src_dtype (F32 or
+ *                  BF16), then the n_rows new V rows, then q [B][Hq][d] of q_dtype, back to
+ *                  back; d = k_ctx's head dimension.
+ *   out_host       host fp32 [B][Hq][d].
+ *   staging        device scratch of at least tq_decode_step_host_staging_size() bytes,
+ *                  256-byte aligned: the inputs and the output on the device.
+ *   the rest       as tq_decode_step (row_ids, caches, seq_lens, workspace: device).
+ * Errors: the checks of the staging, the shape and the workspace come before the copy;
+ * the remaining checks are tq_decode_step's (made before it launches anything; the input
+ * copy has then already been enqueued, into the staging area only). */
+tq_status tq_decode_step_host(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *inputs_host, int src_dtype,
+                              int64_t n_rows, const int64_t *row_ids, int q_dtype, void *k_cache, void *v_cache,
+                              const int32_t *seq_lens, int B, int Hq, int Hkv, int L, float scale,
+                              float *out_host, void *staging, size_t staging_bytes, void *workspace,
+                              size_t workspace_bytes, tq_stream_t stream);
+/* Bytes of device staging tq_decode_step_host needs for these inputs. */
+tq_status tq_decode_step_host_staging_size(const tq_ctx *k_ctx, int src_dtype, int64_t n_rows, int q_dtype,
+                                           int B, int Hq, size_t *bytes);
 /* Number of kernels tq_decode_step launches for these arguments: 2 or 3 on the one-launch
  * front (see above), else 2 more for the two writes (none when n_rows == 0). */
 tq_status tq_decode_step_num_launches(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int src_dtype,

@@ -105,6 +105,11 @@ def test_host_validation_errors(tq):
                                    None, 0, None) == tq.TQ_ERR_INVALID_ARG
     assert lib.tq_decode_step(None, None, None, None, 0, 1, 128, None, None, 0, None, None, None, 1, 1, 1, 1,
                               0.0, None, None, 0, None) == tq.TQ_ERR_INVALID_ARG
+    assert lib.tq_decode_step_host(None, None, None, 0, 1, None, 0, None, None, None, 1, 1, 1, 1,
+                                   0.0, None, None, 0, None, 0, None) == tq.TQ_ERR_INVALID_ARG
+    sz = ctypes.c_size_t(7)
+    assert lib.tq_decode_step_host_staging_size(None, 0, 1, 0, 1, 1, ctypes.byref(sz)) == tq.TQ_ERR_INVALID_ARG
+    assert sz.value == 7
     n = ctypes.c_int32(-1)
     assert lib.tq_decode_step_num_launches(None, None, 0, 1, 1, 1, 1, 1, ctypes.byref(n)) == tq.TQ_ERR_INVALID_ARG
     assert lib.tq_decode_step_num_launches(None, None, 0, 1, 1, 1, 1, 1, None) == tq.TQ_ERR_INVALID_ARG

@@ -197,3 +197,42 @@ def test_decode_step_out_of_range_slot_is_flagged():
     changed = np.nonzero(np.any(kb != kb0, axis=1))[0]
     assert list(changed) == [5]
     assert np.all(np.isfinite(out.cpu().numpy()))
+
+
+@pytest.mark.parametrize("kf,vf,rot", [("turbo4", "turbo4", "dense"), ("turbo4", "turbo4", "wht"),
+                                        ("prod3", "vgroup2", "dense")])
+def test_decode_step_host_buffers_match_device_call(kf, vf, rot):
+    """tq_decode_step_host (the inputs copied in from one pinned host buffer, the output
+    copied back, one C call) leaves the cache bytes and gives the outputs of tq_decode_step
+    on the same inputs in device memory."""
+    import torch
+    tq = lib()
+    B, Hq, Hkv, L = 2, 8, 2, 300
+    n_cache = B * Hkv * L
+    kctx, vctx = _ctx(tq, kf, rot, 41), _ctx(tq, vf, rot, 42)
+    lens = [L, 200]
+    nk, nv, slots, q_t, _ = _step_inputs(B, Hq, Hkv, L, lens, 43, "bf16")
+    k0, v0 = _filled_cache(tq, kctx, kf, n_cache, 44), _filled_cache(tq, vctx, vf, n_cache, 45)
+    sl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    ws = tq.alloc_workspace(tq.tq_decode_workspace_size(kctx, vctx, B, Hq, Hkv, L))
+    kc_a, vc_a = k0.clone(), v0.clone()
+    out_a = torch.empty((B, Hq, 128), dtype=torch.float32, device="cuda")
+    tq.tq_decode_step(kctx, vctx, nk, nv, q_t, kc_a, vc_a, out_a, ws, B, Hq, Hkv, L, row_ids=slots, seq_lens=sl)
+    inputs, _ = tq.pack_step_inputs(nk, nv, q_t)
+    out_h = torch.full((B, Hq, 128), float("nan"), dtype=torch.float32, pin_memory=True)
+    staging = tq.alloc_workspace(tq.tq_decode_step_host_staging_size(kctx, nk.dtype, nk.shape[0], q_t.dtype, B, Hq))
+    kc_b, vc_b = k0.clone(), v0.clone()
+    tq.tq_decode_step_host(kctx, vctx, inputs, nk.dtype, nk.shape[0], q_t.dtype, out_h, slots, kc_b, vc_b, staging,
+                           ws, B, Hq, Hkv, L, seq_lens=sl)
+    torch.cuda.synchronize()
+    assert torch.equal(kc_a, kc_b) and torch.equal(vc_a, vc_b)
+    # (the CTA that completes a unit, and with it the fused merge's summation order, can
+    # differ between runs)
+    np.testing.assert_allclose(out_h.numpy(), out_a.cpu().numpy(), rtol=1e-5, atol=1e-6)
+    assert tq.tq_ctx_device_status(kctx) == 0
+    # a staging area smaller than required is refused before anything is copied or launched
+    short = staging[: staging.numel() - 256]
+    with pytest.raises(tq.TQError) as e:
+        tq.tq_decode_step_host(kctx, vctx, inputs, nk.dtype, nk.shape[0], q_t.dtype, out_h, slots, kc_b, vc_b,
+                               short, ws, B, Hq, Hkv, L, seq_lens=sl)
+    assert e.value.status == tq.TQ_ERR_WORKSPACE
