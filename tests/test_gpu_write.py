@@ -59,7 +59,9 @@ def test_write_wht_bit_exact(fmt, dtype, seed):
 
 
 @pytest.mark.parametrize("fmt", ["turbo4", "turbo3"])
-@pytest.mark.parametrize("n", [100, 1000, 3000])  # one CTA per row / staged matrices / tensor cores
+# one CTA per row / staged matrices / tensor cores; the last with several tiles per CTA
+# (the row-tile ring and both accumulators reused) and a ragged last tile
+@pytest.mark.parametrize("n", [100, 1000, 3000, 116786])
 def test_write_dense_band(fmt, n):
     tq = lib()
     x_t, x32 = torch_rows(make_rows(n, 9, scale=2.0)[8:], "bf16")  # finite rows
