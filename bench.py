@@ -676,6 +676,10 @@ def run_decode(args, rank, world, dist):
     device = torch.device("cuda", local)
     cfg, spec = decode_workload(args), DECODE[name]
     B, Hq, Hkv, L = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["L"]
+    # the committed ncu summary of the workload holds its named shape: its traffic and
+    # instruction counts apply only there (not to a --B / --L point of the sweep)
+    base = synth.WORKLOADS[name]
+    profiled_shape = (B, L) == (base["B"], base["L"])
     w = build_decode(name, cfg, tq, torch, device)
     stream = torch.cuda.current_stream()
     flush_l2 = flusher(torch, device)
@@ -779,14 +783,15 @@ def run_decode(args, rank, world, dist):
         "roofline": {"bound": "hbm", "kernel": f"{spec['kernel']} (split-K decode, {merged}, as in the step)",
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": achieved / peak,
-                     "traffic": profiled_traffic("decode_partial_" + name, spec["source"]),
+                     "traffic": profiled_traffic("decode_partial_" + name, spec["source"]) if profiled_shape else None,
                      "algorithmic_bytes_per_launch": kv_bytes, "avg_launch_ms": merge_avg,
                      "launches": merge_launches},
         # (the profiled launch is the split-K kernel alone: where the step follows it with a
         # separate combine, its stage-form time)
         "roofline_issue": issue_roofline("decode_partial_" + name, spec["source"], spec["kernel"],
                                          merge_avg if merge_launches == 1 else part_avg, clk,
-                                         torch.cuda.get_device_properties(device).multi_processor_count),
+                                         torch.cuda.get_device_properties(device).multi_processor_count)
+                          if profiled_shape else None,
         "roofline_stage_kernel": {"kernel": f"{spec['kernel']} (stage call: partials only, no merge)",
                                   "achieved": achieved_stage, "frac": achieved_stage / peak,
                                   "avg_launch_ms": part_avg},
