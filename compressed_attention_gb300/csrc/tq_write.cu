@@ -357,33 +357,46 @@ __device__ __forceinline__ void pack_quarter(const float (&y)[WT_E], float n, co
   }
 }
 
-template <int FMT, int SRC>
-__global__ void __launch_bounds__(WT_THREADS) k_write_wht(const WriteParams p) {
+// The WHT write's shared tables: the boundaries, the grid table (cell t, copy c at
+// t * WT_REP + c: boundary .x, count .y as integer bits) and its scale, offset and size.
+struct WhtTables {
+  float sb[16];
+  float2 ce[GRID_CELLS * WT_REP];
+  float2 cell0[GRID_CELLS];  // one copy, read from memory
+  float gs, go;
+  int gn;
+};
+
+// Filled by every thread of the CTA (the caller synchronises again before use).
+template <int FMT>
+__device__ __forceinline__ void wht_tables_fill(const WriteParams &p, WhtTables &tb) {
   constexpr int NB = (FMT == TQ_FMT_TURBO4) ? 15 : 7;
+  if (threadIdx.x < NB) tb.sb[threadIdx.x] = p.b[threadIdx.x];
+  // each cell read from memory once (one latency for the whole table), then copied with
+  // consecutive threads on consecutive entries
+  for (int t = threadIdx.x; t < GRID_CELLS; t += blockDim.x)
+    tb.cell0[t] = make_float2(p.bt->e[t], __uint_as_float((uint32_t)p.bt->cnt[t]));
+  if (threadIdx.x == 0) tb.gs = p.bt->scale, tb.go = p.bt->offset, tb.gn = p.bt->n;
+  __syncthreads();
+  for (int k = threadIdx.x; k < GRID_CELLS * WT_REP; k += blockDim.x) tb.ce[k] = tb.cell0[k / WT_REP];
+}
+
+// Rows in groups of eight per warp (four threads per row): this warp takes row groups it,
+// it + step, ...  The four threads of a row stay together (whole warps iterate while any
+// row is left); the next group's source chunks and slot are loaded before this one is
+// encoded.
+template <int FMT, int SRC>
+__device__ __forceinline__ void wht_rows(const WriteParams &p, const WhtTables &tb, int64_t it, int64_t step) {
   constexpr int RB = (FMT == TQ_FMT_TURBO4) ? 68 : 56;
-  __shared__ float sb[16];
-  __shared__ float2 ce[GRID_CELLS * WT_REP];  // cell t, copy c at t * 16 + c
-  pdl_trigger();
-  if (threadIdx.x < NB) sb[threadIdx.x] = p.b[threadIdx.x];
-  for (int k = threadIdx.x; k < GRID_CELLS * WT_REP; k += blockDim.x) {
-    const int t = k / WT_REP;
-    ce[k] = make_float2(p.bt->e[t], __uint_as_float((uint32_t)p.bt->cnt[t]));
-  }
-  const float gs = p.bt->scale, go = p.bt->offset;
-  const int gn = p.bt->n;
+  const float gs = tb.gs, go = tb.go;
+  const int gn = tb.gn;
   const int q = threadIdx.x & 3, l16 = threadIdx.x & 15;
   uint32_t nq[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) nq[i] = p.wht_neg[i] >> (8 * q);
   const bool v16 = ((uintptr_t)p.src & 15) == 0 && ((p.stride * 2) & 15) == 0;
-  __syncthreads();
-  pdl_wait();
-  // the four threads of a row stay together (whole warps iterate while any row is left);
-  // the next iteration's source chunks and slot are loaded before this one is encoded
   const int64_t n_iter = (p.n_rows + 7) / 8;
-  const int64_t step = (int64_t)gridDim.x * (WT_THREADS / 32);
   const int sub = (threadIdx.x & 31) >> 2;
-  int64_t it = (int64_t)blockIdx.x * (WT_THREADS / 32) + (threadIdx.x >> 5);
   Quarter<SRC> raw;
   int64_t slot_next = -1;
   auto fetch = [&](int64_t i) {
@@ -413,11 +426,22 @@ __global__ void __launch_bounds__(WT_THREADS) k_write_wht(const WriteParams p) {
     if (ok) {
       uint8_t *dst = p.dst + slot * RB;
       if (gn)
-        pack_quarter<FMT, true>(v, n, ce, l16, gs, go, gn, sb, dst, q);
+        pack_quarter<FMT, true>(v, n, tb.ce, l16, gs, go, gn, tb.sb, dst, q);
       else
-        pack_quarter<FMT, false>(v, n, ce, l16, gs, go, gn, sb, dst, q);
+        pack_quarter<FMT, false>(v, n, tb.ce, l16, gs, go, gn, tb.sb, dst, q);
     }
   }
+}
+
+template <int FMT, int SRC>
+__global__ void __launch_bounds__(WT_THREADS) k_write_wht(const WriteParams p) {
+  __shared__ WhtTables tb;
+  pdl_trigger();
+  wht_tables_fill<FMT>(p, tb);
+  __syncthreads();
+  pdl_wait();
+  wht_rows<FMT, SRC>(p, tb, (int64_t)blockIdx.x * (WT_THREADS / 32) + (threadIdx.x >> 5),
+                     (int64_t)gridDim.x * (WT_THREADS / 32));
 }
 
 // ------------------------------------------------- dense rotation (CUDA-core matvec)
@@ -758,6 +782,41 @@ __global__ void __launch_bounds__(QWARPS * 32) k_step_front(const StepFrontParam
   }
 }
 
+// The same front for randomized-WHT caches: the q CTAs as above (q_rot = R q with the
+// stored WHT matrix), then ceil(n / 64) CTAs for the K rows and as many for the V rows,
+// each warp encoding eight rows with the WHT write's four-threads-per-row body.
+constexpr int FRONT_WHT_ROWS = WT_THREADS / 4;  // rows per row CTA
+static_assert(QWARPS * 32 == WT_THREADS, "the front's CTAs are the WHT write's");
+
+template <int KF, int VF, int SRC>
+__global__ void __launch_bounds__(QWARPS * 32) k_step_front_wht(const StepFrontParams sp) {
+  extern __shared__ __align__(16) float fsm[];
+  const int c = blockIdx.x - sp.q_ctas;  // row CTAs from 0: K rows, then V rows
+  if (c >= 0) {
+    WhtTables &tb = *reinterpret_cast<WhtTables *>(fsm);
+    const int rc = (sp.n_rows + FRONT_WHT_ROWS - 1) / FRONT_WHT_ROWS;  // row CTAs per tensor
+    const bool v = c >= rc;
+    const int cl = v ? c - rc : c;
+    if (v)
+      wht_tables_fill<VF>(sp.wv, tb);
+    else
+      wht_tables_fill<KF>(sp.wk, tb);
+    __syncthreads();
+    pdl_trigger();
+    pdl_wait();
+    const int64_t it = (int64_t)cl * QWARPS + (threadIdx.x >> 5), step = (int64_t)rc * QWARPS;
+    if (v)
+      wht_rows<VF, SRC>(sp.wv, tb, it, step);
+    else
+      wht_rows<KF, SRC>(sp.wk, tb, it, step);
+  } else {
+    pdl_trigger();
+    stage_rows_padded(fsm, sp.q.r);
+    pdl_wait();
+    prepare_q_body<false>(sp.q, blockIdx.x, sp.q_ctas, fsm);
+  }
+}
+
 // ------------------------------------------------------------------ V group quant
 // One vgroup2 row by one warp: per 32-element group the fp16 min z and step s = (max - min) / 3,
 // indices round((x - z) / s) clamped to 0..3 (48-byte record: 32 index bytes, then {s, z}
@@ -944,11 +1003,14 @@ cudaError_t launch_write(const tq_ctx *ctx, const WriteLaunch &w, cudaStream_t s
 
 
 bool step_front_eligible(const tq_ctx *k, const tq_ctx *v, const WriteLaunch &wk, const WriteLaunch &wv) {
+  // dense: the small-batch dense write; WHT: the WHT write's row body.  Both contexts in
+  // the same rotation family.
   auto ok = [](const tq_ctx *c, const WriteLaunch &w) {
-    return c->p.rotation == TQ_ROT_DENSE && (c->fmt == TQ_FMT_TURBO4 || c->fmt == TQ_FMT_TURBO3) &&
-           w.n_rows >= 1 && w.n_rows <= SMALL_ROWS && !write_tc_eligible(c, w);
+    return (c->fmt == TQ_FMT_TURBO4 || c->fmt == TQ_FMT_TURBO3) && w.n_rows >= 1 && w.n_rows <= SMALL_ROWS &&
+           (c->p.rotation == TQ_ROT_WHT || !write_tc_eligible(c, w));
   };
-  return ok(k, wk) && ok(v, wv) && wk.n_rows == wv.n_rows && wk.src_dtype == wv.src_dtype;
+  return ok(k, wk) && ok(v, wv) && k->p.rotation == v->p.rotation && wk.n_rows == wv.n_rows &&
+         wk.src_dtype == wv.src_dtype;
 }
 
 bool step_front_pv_eligible(const tq_ctx *k, const tq_ctx *v, const WriteLaunch &wk, const WriteLaunch &wv) {
@@ -995,6 +1057,26 @@ cudaError_t launch_step_front(const tq_ctx *k, const tq_ctx *v, const WriteLaunc
     return v4 ? k_step_front<TQ_FMT_TURBO3, TQ_FMT_TURBO4, TQ_DTYPE_F32>
               : k_step_front<TQ_FMT_TURBO3, TQ_FMT_TURBO3, TQ_DTYPE_F32>;
   };
+  if (k->p.rotation == TQ_ROT_WHT) {
+    static_assert(sizeof(WhtTables) <= QPREP_SMEM, "one dynamic shared area for both roles");
+    auto pick_wht = [&]() {
+      if (bf16) {
+        if (k4) return v4 ? k_step_front_wht<TQ_FMT_TURBO4, TQ_FMT_TURBO4, TQ_DTYPE_BF16>
+                          : k_step_front_wht<TQ_FMT_TURBO4, TQ_FMT_TURBO3, TQ_DTYPE_BF16>;
+        return v4 ? k_step_front_wht<TQ_FMT_TURBO3, TQ_FMT_TURBO4, TQ_DTYPE_BF16>
+                  : k_step_front_wht<TQ_FMT_TURBO3, TQ_FMT_TURBO3, TQ_DTYPE_BF16>;
+      }
+      if (k4) return v4 ? k_step_front_wht<TQ_FMT_TURBO4, TQ_FMT_TURBO4, TQ_DTYPE_F32>
+                        : k_step_front_wht<TQ_FMT_TURBO4, TQ_FMT_TURBO3, TQ_DTYPE_F32>;
+      return v4 ? k_step_front_wht<TQ_FMT_TURBO3, TQ_FMT_TURBO4, TQ_DTYPE_F32>
+                : k_step_front_wht<TQ_FMT_TURBO3, TQ_FMT_TURBO3, TQ_DTYPE_F32>;
+    };
+    auto kern = pick_wht();
+    cudaError_t e = kernel_smem_attr((const void *)kern, (int)QPREP_SMEM);
+    if (e != cudaSuccess) return e;
+    const int rc = (sp.n_rows + FRONT_WHT_ROWS - 1) / FRONT_WHT_ROWS;
+    return launch_pdl(kern, dim3(2 * rc + sp.q_ctas), dim3(QWARPS * 32), QPREP_SMEM, st, sp);
+  }
   auto kern = pick();
   cudaError_t e = kernel_smem_attr((const void *)kern, (int)QPREP_SMEM);
   if (e != cudaSuccess) return e;

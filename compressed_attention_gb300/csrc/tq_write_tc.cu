@@ -77,6 +77,7 @@ struct TcMisc {
   // so a warp's lookups of any cells take the minimum two wavefronts): (e[t] * scale +
   // offset, cnt[t] as int bits)
   float2 cell[GRID_CELLS * CELL_COPIES];
+  float2 cell0[GRID_CELLS];     // one copy, read from memory
   float nrm[NACC][TC_ROWS];     // row norm
   float su[NACC][TC_ROWS];      // scale / norm (0 for a zero row)
   int64_t slot[NACC][TC_ROWS];  // destination row, -1: not stored
@@ -153,12 +154,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_write_dense_tc(const __grid_c
     ms.abort_flag = 0;
     fence_mbar_init();
   }
-  if (tid < GRID_CELLS) {  // the grid table: each cell's boundary (mapped like y) and count
-    const float2 c = make_float2(fmaf(p.bt->e[tid], p.bt->scale, p.bt->offset),
-                                 __int_as_float(tid < p.bt->n ? (int)p.bt->cnt[tid] : 0));
-#pragma unroll
-    for (int k = 0; k < CELL_COPIES; ++k) ms.cell[tid * CELL_COPIES + k] = c;
-  }
+  if (tid < GRID_CELLS)  // the grid table: each cell's boundary (mapped like y) and count
+    ms.cell0[tid] = make_float2(fmaf(p.bt->e[tid], p.bt->scale, p.bt->offset),
+                                __int_as_float(tid < p.bt->n ? (int)p.bt->cnt[tid] : 0));
   {  // Pi hi / lo into the swizzled layout, eight 16-byte loads in flight per thread
     constexpr int N16 = 2 * TC_ROWS * 16;
     for (int i0 = tid; i0 < N16; i0 += 8 * TC_THREADS) {
@@ -179,6 +177,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_write_dense_tc(const __grid_c
       }
     }
   }
+  __syncthreads();
+  // the cells' copies, consecutive threads on consecutive entries
+  for (int k = tid; k < GRID_CELLS * CELL_COPIES; k += TC_THREADS) ms.cell[k] = ms.cell0[k / CELL_COPIES];
   fence_async_smem();  // generic writes -> tensor-core reads
   tc_fence_before();
   __syncthreads();

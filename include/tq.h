@@ -233,10 +233,11 @@ tq_status tq_decode_workspace_size(const tq_ctx *k_ctx, const tq_ctx *v_ctx, int
  * tricks 1-3 for the decode): append the step's new K and V rows (SET_ROWS of new_k
  * into k_cache and new_v into v_cache, n_rows rows each at slots row_ids of the
  * [B][Hkv][L] caches, as tq_quantize_set_rows), then tq_decode_attention over the
- * updated caches.  The same results as those three calls; for dense-rotation TURBO4 /
- * TURBO3 caches and at most 256 rows, the two writes and the q preparation share one
- * launch (they are independent), so the step has one wait on the previous kernel where
- * the three calls have three.  Arguments as in tq_quantize_set_rows (dst_rows =
+ * updated caches.  The same results as those three calls; for TURBO4 / TURBO3 caches
+ * (both under the dense or both under the WHT rotation), or PROD3 keys with VGROUP2
+ * values, and at most 256 rows, the two writes and the q preparation share one launch
+ * (they are independent), so the step has one wait on the previous kernel where the
+ * three calls have three.  Arguments as in tq_quantize_set_rows (dst_rows =
  * B * Hkv * L; new_k and new_v share src_dtype and src_row_stride) and
  * tq_decode_attention (no scores); every buffer is the caller's device memory, used in
  * stream order.  Errors: all the checks of the three calls are made before anything is

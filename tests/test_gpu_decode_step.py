@@ -3,9 +3,9 @@ the compressed caches and attends over the updated caches.
 
 The call must leave exactly the cache bytes and give the outputs that the three
 separate calls give (SET_ROWS of K, SET_ROWS of V, decode attention), whichever
-launch plan it takes: the one-launch front (at most 256 new rows: dense-rotation turbo4 /
-turbo3, or prod3 keys with vgroup2 values in any rotation) or the separate kernels (WHT
-rotation of the turbo formats, more rows).  For the turbo
+launch plan it takes: the one-launch front (at most 256 new rows: turbo4 / turbo3 under
+the dense or the WHT rotation, or prod3 keys with vgroup2 values in any rotation) or the
+separate kernels (more rows).  For the turbo
 formats the outputs are also checked against the oracle's attention over the caches
 the call wrote, dequantized by the oracle."""
 
@@ -57,10 +57,13 @@ STEP_CASES = [
     ("turbo4", "turbo4", "dense", "f32", 3, 12, 2, 300, True),
     ("turbo3", "turbo4", "dense", "bf16", 2, 16, 4, 700, True),
     ("turbo3", "turbo3", "dense", "bf16", 2, 16, 4, 700, True),
-    ("turbo4", "turbo3", "wht", "f32", 2, 8, 2, 300, False),
+    ("turbo4", "turbo3", "wht", "f32", 2, 8, 2, 300, True),
     ("turbo4", "turbo4", "dense", "bf16", 32, 64, 8, 64, True),    # 256 rows, the most the front takes
     ("turbo4", "turbo4", "dense", "bf16", 33, 64, 8, 64, False),   # 264 rows
-    ("turbo4", "turbo4", "wht", "bf16", 2, 8, 2, 500, False),
+    ("turbo4", "turbo4", "wht", "bf16", 2, 8, 2, 500, True),
+    ("turbo3", "turbo3", "wht", "bf16", 5, 20, 4, 200, True),      # 20 rows: a ragged row CTA
+    ("turbo4", "turbo4", "wht", "bf16", 32, 64, 8, 64, True),      # 256 rows: four row CTAs per tensor
+    ("turbo4", "turbo4", "wht", "bf16", 33, 64, 8, 64, False),     # 264 rows
     ("prod3", "vgroup2", "dense", "bf16", 2, 12, 2, 400, True),
     ("prod3", "vgroup2", "wht", "f32", 3, 12, 3, 300, True),
     ("prod3", "vgroup2", "dense", "bf16", 32, 64, 8, 64, True),    # 256 rows
