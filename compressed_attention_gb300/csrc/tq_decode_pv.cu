@@ -7,9 +7,9 @@
 // rotated, so the combine applies no un-rotation.
 //
 // Persistent split-K like the turbo4 kernel: one CTA per SM takes a contiguous range
-// of 176-key tiles of the (batch, KV head, 8-head group) units; a producer warp
+// of 240-key tiles of the (batch, KV head, 8-head group) units; a producer warp
 // streams the K (56 B rows) and V (48 B rows) tiles with 1-D bulk copies on a
-// four-stage mbarrier ring; eleven consumer warps take 16 keys each.
+// four-stage mbarrier ring; fifteen consumer warps take 16 keys each.
 //
 // MMA orientation (m16n8k16, fp16 operands, fp32 accumulate), per 8-key block:
 //   scores  C[16 x 8 keys] = Q[16 x 128] K_hat^T : rows 0-7 hold head g's fp16 hi
