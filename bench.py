@@ -627,10 +627,12 @@ E2E_MODE = ("value: the public API calls and the copies issued one by one from P
             "captured once in a CUDA graph and replayed every step")
 
 
-E2E_MODE_DECODE = ("value: one public C-ABI call per step with host buffers (tq_decode_step_host: the input "
-                   "copy from pinned host memory, the step and the output copy back), issued from Python every "
-                   "step (host validation and enqueue inside the timed region); graph_*: the same call captured "
-                   "once in a CUDA graph and replayed every step")
+E2E_MODE_DECODE = ("value: one public C-ABI call per step with host buffers (tq_decode_step_host), issued from "
+                   "Python every step (host validation and enqueue inside the timed region): with page-locked "
+                   "buffers at head dimension 128 the step's kernels read the new K/V rows and q from host "
+                   "memory and write the output to host memory in place over the chip-to-chip link; at "
+                   "d = 256 one copy in to a device staging area and one copy of the output back; "
+                   "graph_*: the same call captured once in a CUDA graph and replayed every step")
 
 
 def timed_e2e(torch, body, steps, warmup, flush_l2):
@@ -728,8 +730,9 @@ def run_decode(args, rank, world, dist):
     merge_launches = tq.tq_decode_num_launches(w["kctx"], w["vctx"], B, Hq, Hkv, L) - 1
 
     # end to end through the public API with host buffers, every step: the new K rows, the
-    # new V rows and q, back to back in one pinned host buffer, copied in in one piece; the
-    # output read back.
+    # new V rows and q, back to back in one pinned host buffer, and a pinned output buffer
+    # (read and written by the step's kernels in place, or copied through the staging
+    # area, as the call decides).
     hstage, _ = tq.pack_step_inputs(w["new_k"], w["new_v"], w["q"])
     h2d = hstage.numel()
     hout = torch.empty(w["out"].shape, dtype=torch.float32, pin_memory=True)

@@ -1,10 +1,13 @@
 // The extern "C" entry points of tq.h: argument validation on the host, context
 // construction, and dispatch to the kernel launchers.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <string>
 #include <vector>
@@ -737,6 +740,47 @@ HostStaging host_staging(int d, int src_dtype, int64_t n_rows, int q_dtype, int 
 }
 }  // namespace
 
+namespace {
+// cuPointerGetAttribute through the runtime's driver entry point (no link to libcuda).
+PFN_cuPointerGetAttribute_v4000 pointer_attr_fn() {
+  static PFN_cuPointerGetAttribute_v4000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuPointerGetAttribute", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuPointerGetAttribute_v4000>(p);
+  });
+  return fn;
+}
+
+// The device address of the host range [p, p + bytes) when kernels on the current device
+// may read and write all of it in place: both ends page-locked host memory of one and the
+// same CUDA allocation (so no unmapped gap lies between them), mapped for this device
+// contiguously.  Null otherwise (pageable memory, two allocations, no mapping).
+void *mapped_host_range(const void *p, size_t bytes) {
+  if (!p || bytes == 0) return nullptr;
+  const char *b = static_cast<const char *>(p), *e = b + (bytes - 1);
+  cudaPointerAttributes a0{}, a1{};
+  if (cudaPointerGetAttributes(&a0, b) != cudaSuccess || cudaPointerGetAttributes(&a1, e) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  if (a0.type != cudaMemoryTypeHost || a1.type != cudaMemoryTypeHost || !a0.devicePointer || !a1.devicePointer)
+    return nullptr;
+  if (static_cast<const char *>(a1.devicePointer) - static_cast<const char *>(a0.devicePointer) !=
+      static_cast<ptrdiff_t>(bytes - 1))
+    return nullptr;
+  const PFN_cuPointerGetAttribute_v4000 fn = pointer_attr_fn();
+  unsigned long long id0 = 0, id1 = 0;
+  if (!fn || fn(&id0, CU_POINTER_ATTRIBUTE_BUFFER_ID, (CUdeviceptr)(uintptr_t)b) != CUDA_SUCCESS ||
+      fn(&id1, CU_POINTER_ATTRIBUTE_BUFFER_ID, (CUdeviceptr)(uintptr_t)e) != CUDA_SUCCESS || id0 == 0 || id0 != id1)
+    return nullptr;
+  return a0.devicePointer;
+}
+}  // namespace
+
 tq_status tq_decode_step_host_staging_size(const tq_ctx *k_ctx, int src_dtype, int64_t n_rows, int q_dtype,
                                            int B, int Hq, size_t *bytes) {
   if (!k_ctx || !bytes) return fail(TQ_ERR_INVALID_ARG, "null context or output");
@@ -764,6 +808,20 @@ tq_status tq_decode_step_host(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const vo
   if ((st = tq_decode_workspace_size(k_ctx, v_ctx, B, Hq, Hkv, L, &ws_need)) != TQ_OK) return st;
   if (!workspace || workspace_bytes < ws_need) return fail(TQ_ERR_WORKSPACE, "workspace smaller than tq_decode_workspace_size()");
   const HostStaging h = host_staging(k_ctx->d, src_dtype, n_rows, q_dtype, B, Hq);
+  // In place when the host buffers are page-locked and mapped (coherent over the
+  // chip-to-chip link): the step's kernels read the inputs from and write the output to
+  // host memory, so neither copy is issued.  Only where every kernel the step may launch
+  // touches those buffers with plain loads and stores: head dimension 128 and at most
+  // SMALL_ROWS new rows (the one-launch fronts or the per-row writes; never the
+  // tensor-map write).
+  if (k_ctx->d == 128 && n_rows <= 256 && aligned(inputs_host, 16) && aligned(out_host, 4)) {
+    const uint8_t *hin = static_cast<const uint8_t *>(mapped_host_range(inputs_host, 2 * h.k_bytes + h.q_bytes));
+    float *hout = hin ? static_cast<float *>(mapped_host_range(out_host, h.out_bytes)) : nullptr;
+    if (hin && hout)
+      return tq_decode_step(k_ctx, v_ctx, hin, hin + h.k_bytes, src_dtype, n_rows, k_ctx->d, row_ids,
+                            hin + 2 * h.k_bytes, q_dtype, k_cache, v_cache, seq_lens, B, Hq, Hkv, L, scale, hout,
+                            workspace, workspace_bytes, stream);
+  }
   uint8_t *dk = static_cast<uint8_t *>(staging), *dv = dk + h.k_bytes, *dq = dv + h.k_bytes;
   float *dout = reinterpret_cast<float *>(dk + h.out_off);
   const cudaStream_t cs = (cudaStream_t)stream;

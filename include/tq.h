@@ -262,6 +262,12 @@ tq_status tq_decode_step(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const void *n
  *   staging        device scratch of at least tq_decode_step_host_staging_size() bytes,
  *                  256-byte aligned: the inputs and the output on the device.
  *   the rest       as tq_decode_step (row_ids, caches, seq_lens, workspace: device).
+ * In place: when inputs_host and out_host are each one page-locked allocation
+ * (cudaHostAlloc / cudaMallocHost) mapped for the current device, inputs_host 16-byte
+ * and out_host 4-byte aligned, the head dimension 128 and n_rows <= 256, no copy is
+ * issued: the step's kernels read the inputs from and write the output to host memory
+ * directly (coherent over the chip-to-chip link on GB300), and the staging area is not
+ * used.  The host checks both ends of each range before taking this path.
  * Errors: the checks of the staging, the shape and the workspace come before the copy;
  * the remaining checks are tq_decode_step's (made before it launches anything; the input
  * copy has then already been enqueued, into the staging area only). */

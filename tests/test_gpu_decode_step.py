@@ -202,12 +202,18 @@ def test_decode_step_out_of_range_slot_is_flagged():
     assert np.all(np.isfinite(out.cpu().numpy()))
 
 
-@pytest.mark.parametrize("kf,vf,rot", [("turbo4", "turbo4", "dense"), ("turbo4", "turbo4", "wht"),
-                                        ("prod3", "vgroup2", "dense")])
-def test_decode_step_host_buffers_match_device_call(kf, vf, rot):
-    """tq_decode_step_host (the inputs copied in from one pinned host buffer, the output
-    copied back, one C call) leaves the cache bytes and gives the outputs of tq_decode_step
-    on the same inputs in device memory."""
+@pytest.mark.parametrize("kf,vf,rot,host", [("turbo4", "turbo4", "dense", "pinned"),
+                                             ("turbo4", "turbo4", "dense", "pageable"),
+                                             ("turbo4", "turbo4", "dense", "pinned_in_pageable_out"),
+                                             ("turbo4", "turbo4", "wht", "pinned"),
+                                             ("turbo4", "turbo4", "wht", "pageable"),
+                                             ("prod3", "vgroup2", "dense", "pinned"),
+                                             ("prod3", "vgroup2", "dense", "pageable")])
+def test_decode_step_host_buffers_match_device_call(kf, vf, rot, host):
+    """tq_decode_step_host (one C call with host buffers) leaves the cache bytes and gives
+    the outputs of tq_decode_step on the same inputs in device memory, whether it runs in
+    place (page-locked input and output: the kernels read and write host memory) or
+    through the staging area (copies in and out)."""
     import torch
     tq = lib()
     B, Hq, Hkv, L = 2, 8, 2, 300
@@ -222,7 +228,10 @@ def test_decode_step_host_buffers_match_device_call(kf, vf, rot):
     out_a = torch.empty((B, Hq, 128), dtype=torch.float32, device="cuda")
     tq.tq_decode_step(kctx, vctx, nk, nv, q_t, kc_a, vc_a, out_a, ws, B, Hq, Hkv, L, row_ids=slots, seq_lens=sl)
     inputs, _ = tq.pack_step_inputs(nk, nv, q_t)
-    out_h = torch.full((B, Hq, 128), float("nan"), dtype=torch.float32, pin_memory=True)
+    if host == "pageable":
+        inputs = torch.empty(inputs.shape, dtype=inputs.dtype).copy_(inputs)
+        assert not inputs.is_pinned()
+    out_h = torch.full((B, Hq, 128), float("nan"), dtype=torch.float32, pin_memory=(host == "pinned"))
     staging = tq.alloc_workspace(tq.tq_decode_step_host_staging_size(kctx, nk.dtype, nk.shape[0], q_t.dtype, B, Hq))
     kc_b, vc_b = k0.clone(), v0.clone()
     tq.tq_decode_step_host(kctx, vctx, inputs, nk.dtype, nk.shape[0], q_t.dtype, out_h, slots, kc_b, vc_b, staging,

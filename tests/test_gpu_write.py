@@ -273,6 +273,39 @@ def test_write_dense_tensor_core_scatter_and_stride(fmt):
 
 
 @pytest.mark.parametrize("fmt", ["turbo4", "turbo3"])
+def test_write_dense_tensor_core_scatter_many_tiles(fmt):
+    """The tensor-core write with several tiles per CTA (the row-tile ring and the
+    accumulators reused), a ragged last tile and every record scattered to a permuted
+    slot: each record lands whole in its slot (norm exact, indices in the band), one
+    out-of-range slot is skipped and flagged, and no other slot is touched."""
+    tq = lib()
+    n, cap = 40_000 + 77, 41_000
+    x = make_rows(n + 8, 31, scale=2.0)[8:]
+    x_t, x32 = torch_rows(x, "bf16")
+    slots = synth.row_permutation(cap, 7)[:n].copy()
+    slots[12_345] = -1
+    ctx = tq.Ctx(fmt, "dense", 8)
+    cache = write_gpu(tq, ctx, x_t, n, row_ids=slots, capacity=cap)
+    assert tq.tq_ctx_device_status(ctx) == 1
+    codec = Codec(fmt, rotation="dense", rot_seed=8)
+    ref, aux = codec.encode(x32)
+    rb = ctx.row_bytes
+    rows = cache.cpu().numpy()[: cap * rb].reshape(cap, rb)
+    live = np.array([i for i in range(n) if i != 12_345])
+    got = rows[slots[live]]
+    if fmt == "turbo4":
+        assert np.array_equal(got[:, :4], ref[live, :4])
+        idx = unpack_turbo4(got)[1]
+    else:
+        assert np.array_equal(unpack_turbo3(got)[0], unpack_turbo3(ref[live])[0])
+        idx = unpack_turbo3(got)[1]
+    ok, ndiff = band_ok(idx, aux["idx"][live], aux["y"][live], codec.b32)
+    assert ok, f"{ndiff} indices differ outside the boundary band"
+    untouched = sorted(set(range(cap)) - set(int(v) for v in slots[live]))
+    assert np.all(rows[untouched] == 0xA5)
+
+
+@pytest.mark.parametrize("fmt", ["turbo4", "turbo3"])
 def test_write_wht_sphere_codebook_bit_exact(fmt):
     """The sphere-marginal codebook (its own boundaries and grid table) under the WHT path."""
     tq = lib()
