@@ -306,8 +306,8 @@ template <bool GRID, int NB>
 __device__ __forceinline__ uint32_t cell_index(float y, const float2 *ce, int l16, float gs, float go, int gn,
                                                const float *sb) {
   if (GRID) {
-    int t = __float2int_rd(fmaf(y, gs, go));  // NaN -> 0, +-inf -> saturated
-    t = min(max(t, 0), gn - 1);
+    // unsigned round-down conversion: negative, -inf and NaN give 0, +inf saturates
+    const uint32_t t = min(__float2uint_rd(fmaf(y, gs, go)), (uint32_t)(gn - 1));
     const float2 c = ce[t * WT_REP + l16];
     return __float_as_uint(c.y) + (y > c.x ? 1u : 0u);
   }
