@@ -248,3 +248,32 @@ def test_decode_step_host_buffers_match_device_call(kf, vf, rot, host):
         tq.tq_decode_step_host(kctx, vctx, inputs, nk.dtype, nk.shape[0], q_t.dtype, out_h, slots, kc_b, vc_b,
                                short, ws, B, Hq, Hkv, L, seq_lens=sl)
     assert e.value.status == tq.TQ_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("pinned", [True, False])
+def test_decode_step_host_no_new_rows(pinned):
+    """tq_decode_step_host with n_rows = 0: the host buffer holds q alone (read in place
+    when page-locked, copied otherwise), the caches are untouched, and the output is
+    tq_decode_attention's."""
+    import torch
+    tq = lib()
+    B, Hq, Hkv, L = 2, 8, 2, 300
+    kctx, vctx = _ctx(tq, "turbo4", "dense", 51), _ctx(tq, "turbo4", "dense", 52)
+    k0, v0 = _filled_cache(tq, kctx, "turbo4", B * Hkv * L, 53), _filled_cache(tq, vctx, "turbo4", B * Hkv * L, 54)
+    nk, nv, slots, q_t, _ = _step_inputs(B, Hq, Hkv, L, [L, 120], 55, "bf16")
+    sl = torch.tensor([L, 120], dtype=torch.int32, device="cuda")
+    ws = tq.alloc_workspace(tq.tq_decode_workspace_size(kctx, vctx, B, Hq, Hkv, L))
+    out_a = torch.empty((B, Hq, 128), dtype=torch.float32, device="cuda")
+    tq.tq_decode_attention(kctx, vctx, q_t, k0, v0, out_a, ws, B, Hq, Hkv, L, seq_lens=sl)
+    inputs, _ = tq.pack_step_inputs(nk[:0], nv[:0], q_t)
+    if not pinned:
+        inputs = torch.empty(inputs.shape, dtype=inputs.dtype).copy_(inputs)
+    out_h = torch.full((B, Hq, 128), float("nan"), dtype=torch.float32, pin_memory=pinned)
+    staging = tq.alloc_workspace(tq.tq_decode_step_host_staging_size(kctx, nk.dtype, 0, q_t.dtype, B, Hq))
+    kc, vc = k0.clone(), v0.clone()
+    tq.tq_decode_step_host(kctx, vctx, inputs, nk.dtype, 0, q_t.dtype, out_h, slots, kc, vc, staging, ws,
+                           B, Hq, Hkv, L, seq_lens=sl)
+    torch.cuda.synchronize()
+    assert torch.equal(kc, k0) and torch.equal(vc, v0)
+    np.testing.assert_allclose(out_h.numpy(), out_a.cpu().numpy(), rtol=1e-5, atol=1e-6)
+    assert tq.tq_ctx_device_status(kctx) == 0
