@@ -121,27 +121,45 @@ def _check(status, func):
 def _ptr(x):
     if x is None:
         return None
+    dp = getattr(x, "data_ptr", None)  # a tensor (the common case first)
+    if dp is not None:
+        return dp()
     if isinstance(x, int):
         return x
-    if hasattr(x, "data_ptr"):
-        return x.data_ptr()
     if hasattr(x, "ctypes"):  # numpy array (host)
         return x.ctypes.data
     raise TypeError(f"cannot take the address of {type(x).__name__}")
 
 
+_TORCH = None  # (torch module, CUDA available, dtype -> library code), looked up once
+
+
+def _torch():
+    global _TORCH
+    if _TORCH is None:
+        import torch
+        _TORCH = (torch, torch.cuda.is_available(),
+                  {torch.float32: TQ_DTYPE_F32, torch.bfloat16: TQ_DTYPE_BF16, torch.float16: TQ_DTYPE_F16})
+    return _TORCH
+
+
 def _stream(stream):
     if stream is None:
-        import torch
-        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+        torch, cuda, _ = _torch()
+        if not cuda:
+            return None
+        # the raw handle of the current stream, without building a Stream object
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        if raw is not None:
+            return raw(torch.cuda.current_device()) or None
+        return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, int):
         return stream
     return stream.cuda_stream
 
 
 def _torch_dtype_code(dt):
-    import torch
-    return {torch.float32: TQ_DTYPE_F32, torch.bfloat16: TQ_DTYPE_BF16, torch.float16: TQ_DTYPE_F16}[dt]
+    return _torch()[2][dt]
 
 
 def _dtype_code(t):
