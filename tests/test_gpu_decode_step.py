@@ -202,25 +202,29 @@ def test_decode_step_out_of_range_slot_is_flagged():
     assert np.all(np.isfinite(out.cpu().numpy()))
 
 
-@pytest.mark.parametrize("kf,vf,rot,host", [("turbo4", "turbo4", "dense", "pinned"),
-                                             ("turbo4", "turbo4", "dense", "pageable"),
-                                             ("turbo4", "turbo4", "dense", "pinned_in_pageable_out"),
-                                             ("turbo4", "turbo4", "wht", "pinned"),
-                                             ("turbo4", "turbo4", "wht", "pageable"),
-                                             ("prod3", "vgroup2", "dense", "pinned"),
-                                             ("prod3", "vgroup2", "dense", "pageable")])
-def test_decode_step_host_buffers_match_device_call(kf, vf, rot, host):
+@pytest.mark.parametrize("kf,vf,rot,src,host", [("turbo4", "turbo4", "dense", "bf16", "pinned"),
+                                                 ("turbo4", "turbo4", "dense", "bf16", "pageable"),
+                                                 ("turbo4", "turbo4", "dense", "bf16", "pinned_in_pageable_out"),
+                                                 ("turbo4", "turbo3", "dense", "f32", "pinned"),
+                                                 ("turbo4", "turbo4", "wht", "bf16", "pinned"),
+                                                 ("turbo4", "turbo4", "wht", "bf16", "pageable"),
+                                                 ("turbo4", "turbo4", "dense/wht", "bf16", "pinned"),
+                                                 ("prod3", "vgroup2", "dense", "bf16", "pinned"),
+                                                 ("prod3", "vgroup2", "dense", "bf16", "pageable")])
+def test_decode_step_host_buffers_match_device_call(kf, vf, rot, src, host):
     """tq_decode_step_host (one C call with host buffers) leaves the cache bytes and gives
     the outputs of tq_decode_step on the same inputs in device memory, whether it runs in
-    place (page-locked input and output: the kernels read and write host memory) or
-    through the staging area (copies in and out)."""
+    place (page-locked input and output: the kernels read and write host memory; with the
+    one-launch front, or with the separate row writes when the key and value rotations
+    differ) or through the staging area (copies in and out)."""
     import torch
     tq = lib()
     B, Hq, Hkv, L = 2, 8, 2, 300
     n_cache = B * Hkv * L
-    kctx, vctx = _ctx(tq, kf, rot, 41), _ctx(tq, vf, rot, 42)
+    krot, vrot = rot.split("/") if "/" in rot else (rot, rot)
+    kctx, vctx = _ctx(tq, kf, krot, 41), _ctx(tq, vf, vrot, 42)
     lens = [L, 200]
-    nk, nv, slots, q_t, _ = _step_inputs(B, Hq, Hkv, L, lens, 43, "bf16")
+    nk, nv, slots, q_t, _ = _step_inputs(B, Hq, Hkv, L, lens, 43, src)
     k0, v0 = _filled_cache(tq, kctx, kf, n_cache, 44), _filled_cache(tq, vctx, vf, n_cache, 45)
     sl = torch.tensor(lens, dtype=torch.int32, device="cuda")
     ws = tq.alloc_workspace(tq.tq_decode_workspace_size(kctx, vctx, B, Hq, Hkv, L))
