@@ -120,11 +120,39 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// ((x0^2 + x1^2) + (x2^2 + x3^2)) of the four bf16 in w0 (x0 low, x1 high) and w1
-__device__ __forceinline__ float sq4(uint32_t w0, uint32_t w1) {
-  const float x0 = __uint_as_float(w0 << 16), x1 = __uint_as_float(w0 & 0xFFFF0000u);
-  const float x2 = __uint_as_float(w1 << 16), x3 = __uint_as_float(w1 & 0xFFFF0000u);
-  return __fadd_rn(__fadd_rn(__fmul_rn(x0, x0), __fmul_rn(x1, x1)), __fadd_rn(__fmul_rn(x2, x2), __fmul_rn(x3, x3)));
+// Packed fp32 pairs (two independent round-to-nearest operations, subnormals kept: each
+// lane rounds exactly as the scalar operation would).
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n .reg .b64 ra, rb, rr;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mul.rn.f32x2 rr, ra, rb;\n mov.b64 {%0, %1}, rr;\n}"
+      : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n .reg .b64 ra, rb, rr;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " add.rn.f32x2 rr, ra, rb;\n mov.b64 {%0, %1}, rr;\n}"
+      : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 r;
+  asm("{\n .reg .b64 ra, rb, rc, rr;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rr, ra, rb, rc;\n mov.b64 {%0, %1}, rr;\n}"
+      : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return r;
+}
+
+// The four-element partial sums of squares ((x0^2 + x1^2) + (x2^2 + x3^2)) of the two
+// groups in a 16-byte chunk (eight bf16: group 0 in words x, y, group 1 in z, w; element
+// 2k in the low half of word k), both at once with packed pairs.
+__device__ __forceinline__ float2 sq8(uint4 v) {
+  const float2 e0 = make_float2(__uint_as_float(v.x << 16), __uint_as_float(v.z << 16));  // x0 of each group
+  const float2 e1 = make_float2(__uint_as_float(v.x & 0xFFFF0000u), __uint_as_float(v.z & 0xFFFF0000u));
+  const float2 e2 = make_float2(__uint_as_float(v.y << 16), __uint_as_float(v.w << 16));
+  const float2 e3 = make_float2(__uint_as_float(v.y & 0xFFFF0000u), __uint_as_float(v.w & 0xFFFF0000u));
+  return add2(add2(mul2(e0, e0), mul2(e1, e1)), add2(mul2(e2, e2), mul2(e3, e3)));
 }
 
 template <int FMT>
@@ -153,6 +181,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_write_dense_tc(const __grid_c
     }
     ms.abort_flag = 0;
     fence_mbar_init();
+    // the first row tiles are requested at once, so they land while Pi is staged (only the
+    // source rows need the previous kernel to have finished)
+    pdl_wait();
+    for (int i = 0; i < NSTAGE && i < n_local; ++i) {
+      const int row0 = (int)((blockIdx.x + (int64_t)i * gridDim.x) * TC_ROWS);
+      const uint32_t sx = smem_addr(smem + OFF_X) + i * TILE_BYTES;
+      mbar_arrive_expect_tx(&ms.x_full[i], TILE_BYTES);
+      tma_load_2d(sx, &xmap, &ms.x_full[i], 0, row0);
+      tma_load_2d(sx + HALF_BYTES, &xmap, &ms.x_full[i], 64, row0);
+    }
   }
   if (tid < GRID_CELLS)  // the grid table: each cell's boundary (mapped like y) and count
     ms.cell0[tid] = make_float2(fmaf(p.bt->e[tid], p.bt->scale, p.bt->offset),
@@ -192,7 +230,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_write_dense_tc(const __grid_c
   if (warp == 0) {
     // ---------------- producer: one thread keeps NSTAGE row tiles in flight
     if (lane == 0) {
-      int i = 0;
+      int i = NSTAGE < n_local ? NSTAGE : n_local;  // (the first ones were issued in the prologue)
       for (; i < n_local; ++i) {
         const int s = i % NSTAGE, use = i / NSTAGE;
         if (use > 0 && !mbar_wait_bounded(&ms.x_empty[s], (use - 1) & 1, TC_WAIT_NS)) *abort_flag = 1;
@@ -251,23 +289,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_write_dense_tc(const __grid_c
       if (ok && use > 0) ok = mbar_wait_bounded(&ms.acc_empty[b], (use - 1) & 1, TC_WAIT_NS);
       if (!__all_sync(FULL_MASK, ok)) *abort_flag = 1;
       if (*abort_flag) break;
-      // sixteen 16-byte chunks of the row: chunk c holds groups 2 c, 2 c + 1
+      // sixteen 16-byte chunks of the row: chunk c holds groups 2 c, 2 c + 1, so pair c
+      // of p1 = (p_2c + p_2c+16, p_2c+1 + p_2c+17) -- the tree's first level -- and the
+      // levels 8, 4, 2 combine adjacent pairs, in the canonical order
       const uint8_t *xs = smem + OFF_X + s * TILE_BYTES;
-      float p1[16];  // p_l + p_{l+16}
+      float2 p1[8];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint4 a = *reinterpret_cast<const uint4 *>(xs + sw128_offset(r, 8 * c));
-        const uint4 v = *reinterpret_cast<const uint4 *>(xs + sw128_offset(r, 8 * (c + 8)));
-        p1[2 * c] = __fadd_rn(sq4(a.x, a.y), sq4(v.x, v.y));
-        p1[2 * c + 1] = __fadd_rn(sq4(a.z, a.w), sq4(v.z, v.w));
-      }
+      for (int c = 0; c < 8; ++c)
+        p1[c] = add2(sq8(*reinterpret_cast<const uint4 *>(xs + sw128_offset(r, 8 * c))),
+                     sq8(*reinterpret_cast<const uint4 *>(xs + sw128_offset(r, 8 * (c + 8)))));
       __syncwarp();
       if (lane == 0) mbar_arrive(&ms.x_empty[s]);  // this warp's reads of the rows are done
 #pragma unroll
-      for (int h = 8; h >= 1; h >>= 1)
+      for (int h = 4; h >= 1; h >>= 1)
 #pragma unroll
-        for (int l = 0; l < h; ++l) p1[l] = __fadd_rn(p1[l], p1[l + h]);
-      const float n = __fsqrt_rn(p1[0]);
+        for (int l = 0; l < h; ++l) p1[l] = add2(p1[l], p1[l + h]);
+      const float n = __fsqrt_rn(__fadd_rn(p1[0].x, p1[0].y));
       const bool in_range = live && slot >= 0 && slot < p.dst_rows;
       if (live && !in_range) atomicExch(p.status, (int32_t)DEVERR_ROW_OOB);
       ms.nrm[b][r] = n;
@@ -300,10 +337,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_write_dense_tc(const __grid_c
       for (int h = 0; h < 2; ++h) {  // columns 32 cq + 16 h .. + 15
         float acc[16];
         tmem_ld16(tmem + ((uint32_t)(32 * qt) << 16) + b * 128 + 32 * cq + 16 * h, acc);
+        float uu[16];  // cell coordinates, two per packed FMA
+#pragma unroll
+        for (int jj = 0; jj < 16; jj += 2) {
+          const float2 u2 = fma2(make_float2(acc[jj], acc[jj + 1]), make_float2(su, su), make_float2(boffset, boffset));
+          uu[jj] = u2.x, uu[jj + 1] = u2.y;
+        }
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) {
           const int j = 16 * h + jj;
-          const float u = fmaf(acc[jj], su, boffset);
+          const float u = uu[jj];
           const uint32_t t = min(__float2uint_rd(u), (uint32_t)(bn - 1));  // NaN, u < 0 -> 0
           const float2 cl = cells[t * CELL_COPIES];
           const uint32_t idx = (uint32_t)__float_as_int(cl.y) + (u > cl.x ? 1u : 0u);
