@@ -812,8 +812,8 @@ tq_status tq_decode_step_host(const tq_ctx *k_ctx, const tq_ctx *v_ctx, const vo
   // chip-to-chip link): the step's kernels read the inputs from and write the output to
   // host memory, so neither copy is issued.  Only where every kernel the step may launch
   // touches those buffers with plain loads and stores: head dimension 128 and at most
-  // SMALL_ROWS new rows (the one-launch fronts or the per-row writes; never the
-  // tensor-map write).
+  // 256 new rows (the one-launch fronts or the small-batch writes; never the tensor-map
+  // write, which takes 2048 rows or more).
   if (k_ctx->d == 128 && n_rows <= 256 && aligned(inputs_host, 16) && aligned(out_host, 4)) {
     const uint8_t *hin = static_cast<const uint8_t *>(mapped_host_range(inputs_host, 2 * h.k_bytes + h.q_bytes));
     float *hout = hin ? static_cast<float *>(mapped_host_range(out_host, h.out_bytes)) : nullptr;
